@@ -1,0 +1,248 @@
+"""Python binding of libf8's C ABI (include/f8.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls.  torch is
+used to allocate device memory for outputs the caller did not pass and to
+find the current CUDA stream; all arithmetic runs in libf8's kernels.  There
+is no fallback: if ``_lib/libf8.so`` is missing the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libf8.so")
+
+F8_OK = 0
+F8_ERR_INVALID = 1
+F8_ERR_ALIGN = 2
+F8_ERR_SHAPE = 3
+F8_ERR_CUDA = 4
+F8_ERR_TIMEOUT = 5
+F8_ERR_NONFINITE = 6
+F8_ERR_UNSUPPORTED = 7
+
+# every symbol include/f8.h declares
+EXPORTS = ("f8_amax", "f8_cast_transpose", "f8_gemm", "f8_linear_workspace_bytes",
+           "f8_linear_fwd", "f8_linear_bwd", "f8_last_device_status", "f8_status_string",
+           "f8_selftest_wait_timeout", "f8_set_wait_limit_ns")
+
+
+class F8Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {f8_status_string(status)}")
+
+
+class _Saved(ctypes.Structure):
+    _fields_ = [("x_t", ctypes.c_void_p), ("w_t", ctypes.c_void_p),
+                ("amax_x", ctypes.c_void_p), ("scale_x", ctypes.c_void_p),
+                ("amax_w", ctypes.c_void_p), ("scale_w", ctypes.c_void_p)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libf8 (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libf8 is not built ({LIB_PATH} missing): run "
+                "`python -m float8_mixed_precision_gb300.build` (needs nvcc)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64
+        st = ctypes.c_int
+        L.f8_amax.argtypes = [vp, i64, vp, vp]
+        L.f8_amax.restype = st
+        L.f8_cast_transpose.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp]
+        L.f8_cast_transpose.restype = st
+        L.f8_gemm.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, vp]
+        L.f8_gemm.restype = st
+        L.f8_linear_workspace_bytes.argtypes = [i64, i64, i64]
+        L.f8_linear_workspace_bytes.restype = ctypes.c_size_t
+        L.f8_linear_fwd.argtypes = [vp, vp, i64, i64, i64, vp, ctypes.POINTER(_Saved), vp,
+                                    ctypes.c_size_t, vp]
+        L.f8_linear_fwd.restype = st
+        L.f8_linear_bwd.argtypes = [vp, ctypes.POINTER(_Saved), i64, i64, i64, vp, vp, vp,
+                                    ctypes.c_size_t, vp]
+        L.f8_linear_bwd.restype = st
+        L.f8_last_device_status.argtypes = [vp]
+        L.f8_last_device_status.restype = st
+        L.f8_status_string.argtypes = [st]
+        L.f8_status_string.restype = ctypes.c_char_p
+        L.f8_selftest_wait_timeout.argtypes = [u64, vp]
+        L.f8_selftest_wait_timeout.restype = st
+        L.f8_set_wait_limit_ns.argtypes = [u64]
+        L.f8_set_wait_limit_ns.restype = None
+        _lib = L
+        return L
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libf8 takes device tensors only")
+    if not t.is_contiguous():
+        raise ValueError("libf8 takes contiguous (row-major) tensors only")
+    return t.data_ptr()
+
+
+def _check(status: int, where: str):
+    if status != F8_OK:
+        raise F8Error(status, where)
+
+
+def f8_status_string(status: int) -> str:
+    return lib().f8_status_string(int(status)).decode()
+
+
+def f8_last_device_status(stream=None) -> int:
+    """Synchronise the stream and read (and clear) the device status word."""
+    return int(lib().f8_last_device_status(_stream(stream)))
+
+
+def f8_set_wait_limit_ns(limit_ns: int) -> None:
+    lib().f8_set_wait_limit_ns(int(limit_ns))
+
+
+def f8_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check(lib().f8_selftest_wait_timeout(int(limit_ns), _stream(stream)), "f8_selftest_wait_timeout")
+
+
+def f8_amax(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """max |x| of a bf16 tensor as a device fp32 scalar tensor."""
+    if x.dtype != torch.bfloat16:
+        raise TypeError("f8_amax takes a bf16 tensor")
+    if out is None:
+        out = torch.empty((), dtype=torch.float32, device=x.device)
+    _check(lib().f8_amax(_ptr(x), x.numel(), _ptr(out), _stream(stream)), "f8_amax")
+    return out
+
+
+def f8_cast_transpose(x: torch.Tensor, amax: torch.Tensor, scale_out: torch.Tensor | None = None,
+                      q: torch.Tensor | None = None, q_t: torch.Tensor | None = None,
+                      want_q: bool = True, want_t: bool = True, stream=None):
+    """(q [rows, cols] uint8, q_t [cols, rows] uint8, scale fp32 scalar) of a 2-D bf16 tensor."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise TypeError("f8_cast_transpose takes a 2-D bf16 tensor")
+    rows, cols = x.shape
+    dev = x.device
+    if scale_out is None:
+        scale_out = torch.empty((), dtype=torch.float32, device=dev)
+    if q is None and want_q:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    if q_t is None and want_t:
+        q_t = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+    _check(lib().f8_cast_transpose(_ptr(x), rows, cols, _ptr(amax), _ptr(scale_out), _ptr(q),
+                                   _ptr(q_t), _stream(stream)), "f8_cast_transpose")
+    return q, q_t, scale_out
+
+
+def f8_gemm(a: torch.Tensor, b: torch.Tensor, scale_a: torch.Tensor, scale_b: torch.Tensor,
+            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """bf16(a b^T / (scale_a scale_b)) for E4M3 codes a [M,K], b [N,K] (uint8)."""
+    M, K = a.shape
+    N, K2 = b.shape
+    if K != K2:
+        raise ValueError("contraction sizes differ")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    _check(lib().f8_gemm(_ptr(a), _ptr(b), M, N, K, _ptr(scale_a), _ptr(scale_b), _ptr(out),
+                         _stream(stream)), "f8_gemm")
+    return out
+
+
+def f8_linear_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().f8_linear_workspace_bytes(M, N, K))
+
+
+@dataclass
+class LinearSaved:
+    """Device buffers the forward pass leaves for the backward pass."""
+    x_t: torch.Tensor      # [K, M] uint8
+    w_t: torch.Tensor      # [K, N] uint8
+    scalars: torch.Tensor  # [4] fp32: amax_x, scale_x, amax_w, scale_w
+
+    @classmethod
+    def empty(cls, M: int, N: int, K: int, device) -> "LinearSaved":
+        return cls(torch.empty((K, M), dtype=torch.uint8, device=device),
+                   torch.empty((K, N), dtype=torch.uint8, device=device),
+                   torch.empty(4, dtype=torch.float32, device=device))
+
+    def c_struct(self) -> _Saved:
+        p = self.scalars.data_ptr()
+        return _Saved(self.x_t.data_ptr(), self.w_t.data_ptr(), p, p + 4, p + 8, p + 12)
+
+    @property
+    def amax_x(self): return self.scalars[0]
+
+    @property
+    def scale_x(self): return self.scalars[1]
+
+    @property
+    def amax_w(self): return self.scalars[2]
+
+    @property
+    def scale_w(self): return self.scalars[3]
+
+
+def workspace(M: int, N: int, K: int, device) -> torch.Tensor:
+    return torch.empty(max(f8_linear_workspace_bytes(M, N, K), 1), dtype=torch.uint8, device=device)
+
+
+def f8_linear_fwd(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | None = None,
+                  saved: LinearSaved | None = None, ws: torch.Tensor | None = None, stream=None):
+    """Y = X W^T through the Float8 path; returns (Y, saved)."""
+    M, K = x.shape
+    N, K2 = w.shape
+    if K != K2:
+        raise ValueError("in-feature sizes differ")
+    dev = x.device
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if saved is None:
+        saved = LinearSaved.empty(M, N, K, dev)
+    if ws is None:
+        ws = workspace(M, N, K, dev)
+    s = saved.c_struct()
+    _check(lib().f8_linear_fwd(_ptr(x), _ptr(w), M, N, K, _ptr(y), ctypes.byref(s), _ptr(ws),
+                               ws.numel(), _stream(stream)), "f8_linear_fwd")
+    return y, saved
+
+
+def f8_linear_bwd(dy: torch.Tensor, saved: LinearSaved, K: int | None = None,
+                  dx: torch.Tensor | None = None, dw: torch.Tensor | None = None,
+                  ws: torch.Tensor | None = None, want_dx: bool = True, want_dw: bool = True,
+                  stream=None):
+    """(dX, dW) of the linear whose forward produced ``saved``."""
+    M, N = dy.shape
+    K = saved.x_t.shape[0]
+    dev = dy.device
+    if dx is None and want_dx:
+        dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    if dw is None and want_dw:
+        dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    if ws is None:
+        ws = workspace(M, N, K, dev)
+    s = saved.c_struct()
+    _check(lib().f8_linear_bwd(_ptr(dy), ctypes.byref(s), M, N, K, _ptr(dx), _ptr(dw), _ptr(ws),
+                               ws.numel(), _stream(stream)), "f8_linear_bwd")
+    return dx, dw

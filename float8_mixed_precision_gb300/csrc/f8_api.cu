@@ -1,0 +1,322 @@
+// C-ABI of libf8: argument checks on the host, per-device state, the
+// device status word, and the forward / backward composition of a Float8
+// linear out of the amax, cast_transpose and GEMM launches.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "f8.h"
+#include "f8_internal.h"
+#include "f8_ptx.cuh"
+
+// One status word per device (each device that loads the module gets its
+// own instance); kernels OR error bits into it.
+__device__ unsigned g_f8_status_word;
+
+namespace f8 {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices];
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+f8_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return F8_OK;
+    if (e == cudaErrorNotSupported)
+        return F8_ERR_UNSUPPORTED;
+    return F8_ERR_CUDA;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct FwdWs {
+    uint8_t *x_q;
+    uint8_t *w_q;
+};
+struct BwdWs {
+    uint8_t *dy_q;
+    uint8_t *dy_t;
+    float *amax_dy;
+    float *scale_dy;
+};
+
+size_t fwd_ws_bytes(int64_t M, int64_t N, int64_t K)
+{
+    return round256(static_cast<size_t>(M) * K) + round256(static_cast<size_t>(N) * K);
+}
+
+size_t bwd_ws_bytes(int64_t M, int64_t N)
+{
+    return 2 * round256(static_cast<size_t>(M) * N) + 256;
+}
+
+} // namespace
+
+const DeviceInfo *device_info()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_dev_ready[dev]) {
+        DeviceInfo info;
+        info.ordinal = dev;
+        if (cudaDeviceGetAttribute(&info.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&info.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&info.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return nullptr;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_f8_status_word) != cudaSuccess)
+            return nullptr;
+        info.status = static_cast<unsigned *>(p);
+        g_dev[dev] = info;
+        g_dev_ready[dev] = true;
+    }
+    return &g_dev[dev];
+}
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+} // namespace f8
+
+using namespace f8;
+
+namespace {
+
+// The kernels are built for sm_103a only; refuse anything else up front.
+f8_status get_device(const DeviceInfo **out)
+{
+    const DeviceInfo *d = device_info();
+    if (d == nullptr)
+        return F8_ERR_CUDA;
+    if (d->cc_major != 10 || d->cc_minor != 3)
+        return F8_ERR_UNSUPPORTED;
+    *out = d;
+    return F8_OK;
+}
+
+f8_status check_cast_args(const void *x, int64_t rows, int64_t cols, const float *amax,
+                          const float *scale_out, const uint8_t *q, const uint8_t *q_t)
+{
+    if (rows < 0 || cols < 0 || amax == nullptr)
+        return F8_ERR_INVALID;
+    if (rows > 0 && cols > 0 && x == nullptr)
+        return F8_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(q, 16) || !aligned(q_t, 16) || !aligned(amax, 4) ||
+        !aligned(scale_out, 4))
+        return F8_ERR_ALIGN;
+    return F8_OK;
+}
+
+f8_status check_gemm_args(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
+                          const float *sa, const float *sb, const void *c)
+{
+    if (M < 0 || N < 0 || K < 0 || sa == nullptr || sb == nullptr)
+        return F8_ERR_INVALID;
+    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2)
+        return F8_ERR_SHAPE;
+    if (M > 0 && N > 0 && (c == nullptr || (K > 0 && (a == nullptr || b == nullptr))))
+        return F8_ERR_INVALID;
+    if (K % 16 != 0)
+        return F8_ERR_SHAPE;
+    if (!aligned(a, 16) || !aligned(b, 16) || !aligned(c, 16) || !aligned(sa, 4) || !aligned(sb, 4))
+        return F8_ERR_ALIGN;
+    return F8_OK;
+}
+
+f8_status check_linear_shape(int64_t M, int64_t N, int64_t K)
+{
+    if (M <= 0 || N <= 0 || K <= 0)
+        return F8_ERR_INVALID;
+    if (M % 16 || N % 16 || K % 16)
+        return F8_ERR_SHAPE;
+    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2)
+        return F8_ERR_SHAPE;
+    return F8_OK;
+}
+
+f8_status check_saved(const f8_linear_saved *s)
+{
+    if (s == nullptr || s->x_t == nullptr || s->w_t == nullptr || s->amax_x == nullptr ||
+        s->scale_x == nullptr || s->amax_w == nullptr || s->scale_w == nullptr)
+        return F8_ERR_INVALID;
+    if (!aligned(s->x_t, 16) || !aligned(s->w_t, 16) || !aligned(s->amax_x, 4) ||
+        !aligned(s->scale_x, 4) || !aligned(s->amax_w, 4) || !aligned(s->scale_w, 4))
+        return F8_ERR_ALIGN;
+    return F8_OK;
+}
+
+#define F8_TRY(expr)                                                                               \
+    do {                                                                                           \
+        f8_status st_ = (expr);                                                                    \
+        if (st_ != F8_OK)                                                                          \
+            return st_;                                                                            \
+    } while (0)
+
+#define F8_TRY_CUDA(expr) F8_TRY(from_cuda(expr))
+
+} // namespace
+
+extern "C" {
+
+const char *f8_status_string(f8_status s)
+{
+    switch (s) {
+    case F8_OK: return "F8_OK";
+    case F8_ERR_INVALID: return "F8_ERR_INVALID: invalid argument";
+    case F8_ERR_ALIGN: return "F8_ERR_ALIGN: misaligned pointer";
+    case F8_ERR_SHAPE: return "F8_ERR_SHAPE: unsupported shape";
+    case F8_ERR_CUDA: return "F8_ERR_CUDA: CUDA runtime error";
+    case F8_ERR_TIMEOUT: return "F8_ERR_TIMEOUT: device wait exceeded its time limit";
+    case F8_ERR_NONFINITE: return "F8_ERR_NONFINITE: non-finite value in an amax input";
+    case F8_ERR_UNSUPPORTED: return "F8_ERR_UNSUPPORTED: needs an sm_103 device and driver";
+    }
+    return "F8_ERR_UNKNOWN";
+}
+
+void f8_set_wait_limit_ns(uint64_t limit_ns)
+{
+    g_wait_limit_ns.store(limit_ns ? limit_ns : kDefaultWaitLimitNs, std::memory_order_relaxed);
+}
+
+f8_status f8_amax(const void *x, int64_t n, float *amax_out, void *stream)
+{
+    if (n < 0 || amax_out == nullptr || (n > 0 && x == nullptr))
+        return F8_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(amax_out, 4))
+        return F8_ERR_ALIGN;
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n == 0)
+        return from_cuda(cudaMemsetAsync(amax_out, 0, sizeof(float), st));
+    return from_cuda(launch_amax(x, n, amax_out, *dev, st));
+}
+
+f8_status f8_cast_transpose(const void *x, int64_t rows, int64_t cols, const float *amax,
+                            float *scale_out, uint8_t *q, uint8_t *q_t, void *stream)
+{
+    F8_TRY(check_cast_args(x, rows, cols, amax, scale_out, q, q_t));
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    return from_cuda(launch_cast_transpose(x, rows, cols, amax, scale_out, q, q_t, *dev,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+f8_status f8_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
+                  const float *scale_a, const float *scale_b, void *c, void *stream)
+{
+    F8_TRY(check_gemm_args(a, b, M, N, K, scale_a, scale_b, c));
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (M == 0 || N == 0)
+        return F8_OK;
+    if (K == 0)
+        return from_cuda(cudaMemsetAsync(c, 0, static_cast<size_t>(M) * N * 2, st));
+    return from_cuda(launch_gemm(a, b, M, N, K, scale_a, scale_b, c, *dev, st));
+}
+
+size_t f8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K)
+{
+    if (M <= 0 || N <= 0 || K <= 0)
+        return 0;
+    size_t f = fwd_ws_bytes(M, N, K), b = bwd_ws_bytes(M, N);
+    return f > b ? f : b;
+}
+
+f8_status f8_linear_fwd(const void *x, const void *w, int64_t M, int64_t N, int64_t K, void *y,
+                        const f8_linear_saved *saved, void *workspace, size_t workspace_bytes,
+                        void *stream)
+{
+    F8_TRY(check_linear_shape(M, N, K));
+    F8_TRY(check_saved(saved));
+    if (x == nullptr || w == nullptr || y == nullptr || workspace == nullptr)
+        return F8_ERR_INVALID;
+    if (workspace_bytes < fwd_ws_bytes(M, N, K))
+        return F8_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(workspace, 256))
+        return F8_ERR_ALIGN;
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    FwdWs fw{ws, ws + round256(static_cast<size_t>(M) * K)};
+
+    F8_TRY_CUDA(launch_amax(x, M * K, saved->amax_x, *dev, st));
+    F8_TRY_CUDA(launch_amax(w, N * K, saved->amax_w, *dev, st));
+    F8_TRY_CUDA(launch_cast_transpose(x, M, K, saved->amax_x, saved->scale_x, fw.x_q, saved->x_t, *dev, st));
+    F8_TRY_CUDA(launch_cast_transpose(w, N, K, saved->amax_w, saved->scale_w, fw.w_q, saved->w_t, *dev, st));
+    return from_cuda(launch_gemm(fw.x_q, fw.w_q, M, N, K, saved->scale_x, saved->scale_w, y, *dev, st));
+}
+
+f8_status f8_linear_bwd(const void *dy, const f8_linear_saved *saved, int64_t M, int64_t N,
+                        int64_t K, void *dx, void *dw, void *workspace, size_t workspace_bytes,
+                        void *stream)
+{
+    F8_TRY(check_linear_shape(M, N, K));
+    F8_TRY(check_saved(saved));
+    if (dy == nullptr || workspace == nullptr)
+        return F8_ERR_INVALID;
+    if (workspace_bytes < bwd_ws_bytes(M, N))
+        return F8_ERR_INVALID;
+    if (!aligned(dy, 16) || !aligned(dx, 16) || !aligned(dw, 16) || !aligned(workspace, 256))
+        return F8_ERR_ALIGN;
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t mn = round256(static_cast<size_t>(M) * N);
+    BwdWs bw{ws, ws + mn, reinterpret_cast<float *>(ws + 2 * mn),
+             reinterpret_cast<float *>(ws + 2 * mn + 128)};
+
+    F8_TRY_CUDA(launch_amax(dy, M * N, bw.amax_dy, *dev, st));
+    F8_TRY_CUDA(launch_cast_transpose(dy, M, N, bw.amax_dy, bw.scale_dy, dx ? bw.dy_q : nullptr,
+                                      dw ? bw.dy_t : nullptr, *dev, st));
+    // dX [M,K] = q(dY) [M,N] . (q(W)^T [K,N])^T
+    if (dx != nullptr)
+        F8_TRY_CUDA(launch_gemm(bw.dy_q, saved->w_t, M, K, N, bw.scale_dy, saved->scale_w, dx, *dev, st));
+    // dW [N,K] = q(dY)^T [N,M] . (q(X)^T [K,M])^T
+    if (dw != nullptr)
+        F8_TRY_CUDA(launch_gemm(bw.dy_t, saved->x_t, N, K, M, bw.scale_dy, saved->scale_x, dw, *dev, st));
+    return F8_OK;
+}
+
+f8_status f8_last_device_status(void *stream)
+{
+    const DeviceInfo *dev = device_info();
+    if (dev == nullptr)
+        return F8_ERR_CUDA;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return F8_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, dev->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return F8_ERR_CUDA;
+    const unsigned zero = 0;
+    if (cudaMemcpy(dev->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+        return F8_ERR_CUDA;
+    if (word & kStatusTimeout)
+        return F8_ERR_TIMEOUT;
+    if (word & kStatusNonfinite)
+        return F8_ERR_NONFINITE;
+    return F8_OK;
+}
+
+f8_status f8_selftest_wait_timeout(uint64_t limit_ns, void *stream)
+{
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    return from_cuda(launch_wait_selftest(limit_ns, *dev, static_cast<cudaStream_t>(stream)));
+}
+
+} // extern "C"

@@ -1,0 +1,241 @@
+// amax reduction and fused scale + cast + transpose (bf16 -> E4M3), the two
+// HBM-bound steps of dynamic tensorwise scaling.
+//
+// amax: every thread streams 16-byte vectors of 8 bf16 values with four
+// independent loads in flight, keeps the maximum of the magnitude bits
+// (bits & 0x7FFF: for non-negative IEEE values the integer order is the
+// numeric order, and inf/NaN sort above every finite value), reduces through
+// redux.sync within the warp and shared memory within the block, and folds
+// the block result into the output with one atomicMax on the fp32 bit
+// pattern (valid because the value is non-negative).
+//
+// cast_transpose: a CTA owns a 128 x 128 tile.  Phase 1 reads it with 16-byte
+// loads (each thread 16 consecutive bf16 of one row), scales in fp32,
+// converts with the hardware's saturating RNE E4M3 conversion, writes the
+// row-major codes with 16-byte stores and parks them in a 16 KB shared tile
+// whose 16-byte chunks are XOR-swizzled by (row / 16) % 8.  Phase 2 gives each
+// thread a 16-row x 4-column block: 16 conflict-free 4-byte shared loads,
+// a byte transpose with PRMT, and four 16-byte stores of the column-major
+// copy (8 consecutive threads write 128 contiguous bytes of one column).
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "f8_internal.h"
+#include "f8_ptx.cuh"
+
+namespace f8 {
+namespace {
+
+constexpr int kAmaxThreads = 256;
+constexpr int kAmaxUnroll = 4;
+
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t acc, uint4 v)
+{
+    acc = __vmaxu2(acc, v.x & 0x7FFF7FFFu);
+    acc = __vmaxu2(acc, v.y & 0x7FFF7FFFu);
+    acc = __vmaxu2(acc, v.z & 0x7FFF7FFFu);
+    acc = __vmaxu2(acc, v.w & 0x7FFF7FFFu);
+    return acc;
+}
+
+__global__ void __launch_bounds__(kAmaxThreads)
+amax_kernel(const uint4 *__restrict__ x, int64_t nvec, const uint16_t *__restrict__ tail, int ntail,
+            unsigned *__restrict__ out_bits, unsigned *__restrict__ status)
+{
+    uint32_t m2 = 0;
+    const int64_t S = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; i + (kAmaxUnroll - 1) * S < nvec; i += kAmaxUnroll * S) {
+        uint4 v[kAmaxUnroll];
+#pragma unroll
+        for (int u = 0; u < kAmaxUnroll; ++u)
+            v[u] = __ldg(x + i + u * S);
+#pragma unroll
+        for (int u = 0; u < kAmaxUnroll; ++u)
+            m2 = max_u16x2(m2, v[u]);
+    }
+    for (; i < nvec; i += S)
+        m2 = max_u16x2(m2, __ldg(x + i));
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    if (blockIdx.x == 0 && threadIdx.x < ntail)
+        m = max(m, static_cast<uint32_t>(tail[threadIdx.x]) & 0x7FFFu);
+
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    __shared__ uint32_t warp_max[kAmaxThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0)
+        warp_max[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        m = lane < kAmaxThreads / 32 ? warp_max[lane] : 0u;
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if (lane == 0) {
+            if (m >= 0x7F80u)
+                atomicOr(status, kStatusNonfinite);
+            atomicMax(out_bits, m << 16);
+        }
+    }
+}
+
+// ----------------------------------------------------------------- cast
+constexpr int kTile = 128;
+constexpr int kCastThreads = 256;
+
+__device__ __forceinline__ float scale_from_amax(const float *amax)
+{
+    return __fdiv_rn(448.0f, fmaxf(__ldg(amax), 1e-12f));
+}
+
+__device__ __forceinline__ uint16_t cvt2(float lo, float hi)
+{
+    return static_cast<uint16_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_e4m3x2(uint32_t w, float s)
+{
+    const float lo = __uint_as_float(w << 16);
+    const float hi = __uint_as_float(w & 0xFFFF0000u);
+    return cvt2(__fmul_rn(lo, s), __fmul_rn(hi, s));
+}
+
+// 8 bf16 (one uint4) -> 8 E4M3 codes (one uint2), element order preserved.
+__device__ __forceinline__ uint2 cvt8(uint4 v, float s)
+{
+    uint2 r;
+    r.x = bf16x2_to_e4m3x2(v.x, s) | (bf16x2_to_e4m3x2(v.y, s) << 16);
+    r.y = bf16x2_to_e4m3x2(v.z, s) | (bf16x2_to_e4m3x2(v.w, s) << 16);
+    return r;
+}
+
+__device__ __forceinline__ uint8_t cvt1(uint16_t b, float s)
+{
+    const float v = __fmul_rn(__uint_as_float(static_cast<uint32_t>(b) << 16), s);
+    return static_cast<uint8_t>(cvt2(v, 0.0f) & 0xFFu);
+}
+
+__global__ void __launch_bounds__(kCastThreads)
+cast_transpose_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
+                      const float *__restrict__ amax, float *__restrict__ scale_out,
+                      uint8_t *__restrict__ q, uint8_t *__restrict__ qt, int vector_ok)
+{
+    __shared__ __align__(16) uint8_t tile[kTile * kTile];
+    const float s = scale_from_amax(amax);
+    if (scale_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
+        *scale_out = s;
+
+    const int64_t tiles_c = (cols + kTile - 1) / kTile;
+    const int64_t tiles_r = (rows + kTile - 1) / kTile;
+    const int64_t ntiles = tiles_r * tiles_c;
+    const int t = threadIdx.x;
+
+    for (int64_t tix = blockIdx.x; tix < ntiles; tix += gridDim.x) {
+        const int64_t r0 = (tix / tiles_c) * kTile;
+        const int64_t c0 = (tix % tiles_c) * kTile;
+        const bool full = vector_ok && r0 + kTile <= rows && c0 + kTile <= cols;
+        if (full) {
+            // ---- phase 1: rows in, row-major codes out, park in smem
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int k = t + it * kCastThreads;  // 16-element chunk id in the tile
+                const int row = k >> 3, ch = k & 7;
+                const uint16_t *src = x + (r0 + row) * cols + c0 + ch * 16;
+                const uint4 v0 = __ldg(reinterpret_cast<const uint4 *>(src));
+                const uint4 v1 = __ldg(reinterpret_cast<const uint4 *>(src + 8));
+                const uint2 a = cvt8(v0, s), b = cvt8(v1, s);
+                const uint4 codes = make_uint4(a.x, a.y, b.x, b.y);
+                if (q != nullptr)
+                    *reinterpret_cast<uint4 *>(q + (r0 + row) * cols + c0 + ch * 16) = codes;
+                const int pch = ch ^ ((row >> 4) & 7);
+                *reinterpret_cast<uint4 *>(tile + row * kTile + pch * 16) = codes;
+            }
+            if (qt != nullptr) {
+                __syncthreads();
+                // ---- phase 2: 16 rows x 4 columns per thread, transposed out
+                const int rs = t & 7;          // 16-row segment
+                const int cg = t >> 3;         // 4-column group (0..31)
+                const int chunk = cg >> 2;     // 16-byte chunk holding the 4 columns
+                const int word = cg & 3;       // 4-byte word within the chunk
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int row = rs * 16 + i;
+                    const int pch = chunk ^ ((row >> 4) & 7);
+                    w[i] = *reinterpret_cast<const uint32_t *>(tile + row * kTile + pch * 16 + word * 4);
+                }
+                uint32_t col[4][4];
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const uint32_t a = w[4 * g], b = w[4 * g + 1], c = w[4 * g + 2], d = w[4 * g + 3];
+                    const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(c, d, 0x5140);
+                    const uint32_t t2 = __byte_perm(a, b, 0x7362), t3 = __byte_perm(c, d, 0x7362);
+                    col[0][g] = __byte_perm(t0, t1, 0x5410);
+                    col[1][g] = __byte_perm(t0, t1, 0x7632);
+                    col[2][g] = __byte_perm(t2, t3, 0x5410);
+                    col[3][g] = __byte_perm(t2, t3, 0x7632);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint8_t *dst = qt + (c0 + cg * 4 + j) * rows + r0 + rs * 16;
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
+                }
+            }
+            __syncthreads();
+        } else {
+            // ragged or unaligned tile: one element at a time
+            for (int e = t; e < kTile * kTile; e += kCastThreads) {
+                const int64_t r = r0 + e / kTile, c = c0 + e % kTile;
+                if (r < rows && c < cols) {
+                    const uint8_t b = cvt1(x[r * cols + c], s);
+                    if (q != nullptr)
+                        q[r * cols + c] = b;
+                    if (qt != nullptr)
+                        qt[c * rows + r] = b;
+                }
+            }
+        }
+    }
+}
+
+} // namespace
+
+cudaError_t launch_amax(const void *x, int64_t n, float *amax_out, const DeviceInfo &dev,
+                        cudaStream_t stream)
+{
+    cudaError_t err = cudaMemsetAsync(amax_out, 0, sizeof(float), stream);
+    if (err != cudaSuccess)
+        return err;
+    const int64_t nvec = n / 8;
+    const int ntail = static_cast<int>(n % 8);
+    const uint16_t *tail = static_cast<const uint16_t *>(x) + nvec * 8;
+    int64_t blocks = (nvec + kAmaxThreads * kAmaxUnroll - 1) / (kAmaxThreads * kAmaxUnroll);
+    const int64_t max_blocks = static_cast<int64_t>(dev.sm_count) * (2048 / kAmaxThreads);
+    if (blocks > max_blocks)
+        blocks = max_blocks;
+    if (blocks < 1)
+        blocks = 1;
+    amax_kernel<<<static_cast<unsigned>(blocks), kAmaxThreads, 0, stream>>>(
+        static_cast<const uint4 *>(x), nvec, tail, ntail, reinterpret_cast<unsigned *>(amax_out),
+        dev.status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, const float *amax,
+                                  float *scale_out, uint8_t *q, uint8_t *q_t,
+                                  const DeviceInfo &dev, cudaStream_t stream)
+{
+    const int64_t ntiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
+    int64_t blocks = ntiles;
+    const int64_t max_blocks = static_cast<int64_t>(dev.sm_count) * (2048 / kCastThreads);
+    if (blocks > max_blocks)
+        blocks = max_blocks;
+    if (blocks < 1)
+        blocks = 1;
+    const int vector_ok = (rows % 16 == 0) && (cols % 16 == 0);
+    cast_transpose_kernel<<<static_cast<unsigned>(blocks), kCastThreads, 0, stream>>>(
+        static_cast<const uint16_t *>(x), rows, cols, amax, scale_out, q, q_t, vector_ok);
+    return cudaGetLastError();
+}
+
+} // namespace f8

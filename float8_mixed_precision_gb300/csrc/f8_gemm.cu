@@ -1,0 +1,369 @@
+// E4M3 x E4M3 -> fp32 -> bf16 GEMM on the 5th-generation tensor cores:
+// C[M,N] = bf16( A[M,K] B[N,K]^T * 1/(sa sb) ), both operands K-major.
+//
+// One persistent CTA per SM (192 threads, warp-specialised):
+//   warp 0      TMA producer: 128 x 128-byte A tiles and BN x 128-byte B tiles
+//               (128-byte swizzle) into a STAGES-deep shared-memory ring,
+//               completion counted in transaction bytes on full[s];
+//   warp 1      TMEM allocator and MMA issuer: 4 tcgen05.mma kind::f8f6f4
+//               (128 x BN x 32) per stage into one of two TMEM accumulators;
+//               tcgen05.commit releases the stage (empty[s]) and, after the
+//               last K block, hands the accumulator to the epilogue (tfull);
+//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns, multiply by
+//               fl32(1/(sa sb)), round to bf16, store; then release the
+//               accumulator (tempty) so the MMA of tile i+1 overlaps the
+//               epilogue of tile i.
+// Tiles are visited in groups of `group_m` M-blocks so that concurrently
+// running CTAs share A and B tiles in L2.  Partial tiles at the M, N and K
+// edges are zero-filled by TMA and masked in the epilogue.
+//
+// Every wait is bounded (global-timer limit).  A wait that gives up sets a
+// CTA-wide abort flag and the device status word; the other roles leave
+// their loops, the producer waits for its own copies in flight, the MMA
+// thread waits for its own MMAs, and TMEM is released before the CTA exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "f8_internal.h"
+#include "f8_ptx.cuh"
+
+namespace f8 {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 128;  // bytes of K per stage = one 128-byte swizzle row
+constexpr int kThreads = 192;
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
+
+template <int BN, int STAGES>
+struct GemmCfg {
+    static constexpr int kABytes = kBM * kBK;
+    static constexpr int kBBytes = BN * kBK;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kTmemCols = (2 * BN <= 256) ? 256 : 512;
+    static constexpr int kBarBytes = 8 * (2 * STAGES + 5) + 16;
+    static constexpr int kSmemBytes = STAGES * kStageBytes + kBarBytes + 1024;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group_m, int &mb,
+                                            int &nb)
+{
+    const int per_group = group_m * num_n;
+    const int g = tile / per_group;
+    const int first_m = g * group_m;
+    const int gm = min(group_m, num_m - first_m);
+    const int r = tile - g * per_group;
+    mb = first_m + r % gm;
+    nb = r / gm;
+}
+
+__device__ __forceinline__ void note_timeout(volatile int *abort_flag, unsigned *status)
+{
+    *abort_flag = 1;
+    atomicOr(status, kStatusTimeout);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 h = __float22bfloat162_rn(make_float2(lo, hi));
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+            __nv_bfloat16 *__restrict__ c, int M, int N, int K, const float *__restrict__ sa,
+            const float *__restrict__ sb, unsigned *__restrict__ status, uint64_t limit_ns,
+            int group_m)
+{
+    using Cfg = GemmCfg<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *smA = smem;
+    uint8_t *smB = smem + STAGES * Cfg::kABytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::kStageBytes);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int num_m = (M + kBM - 1) / kBM;
+    const int num_n = (N + BN - 1) / BN;
+    const int tiles = num_m * num_n;
+    const int num_kb = (K + kBK - 1) / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tma_a);
+        tma_prefetch_desc(&tma_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            uint32_t stage = 0, phase = 0;
+            int64_t issued = 0;
+            bool stop = false;
+            for (int tile = blockIdx.x; tile < tiles && !stop; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords(tile, num_m, num_n, group_m, mb, nb);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, limit_ns)) {
+                        note_timeout(abort_flag, status);
+                        stop = true;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+                    tma_load_2d(smA + stage * Cfg::kABytes, &tma_a, &full[stage], kb * kBK, mb * kBM);
+                    tma_load_2d(smB + stage * Cfg::kBBytes, &tma_b, &full[stage], kb * kBK, nb * BN);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (*abort_flag) {
+                // wait for this CTA's copies still in flight before it exits
+                int64_t n = issued < STAGES ? issued : STAGES;
+                uint32_t s = stage, p = phase;
+                for (int64_t i = 0; i < n; ++i) {
+                    if (s == 0) {
+                        s = STAGES - 1;
+                        p ^= 1u;
+                    } else {
+                        --s;
+                    }
+                    mbar_wait(&full[s], p, nullptr, kDrainLimitNs);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            const uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+            uint32_t stage = 0, phase = 0;
+            bool stop = false;
+            int local = 0;
+            for (int tile = blockIdx.x; tile < tiles && !stop; tile += gridDim.x, ++local) {
+                const uint32_t acc = local & 1;
+                const uint32_t aph = (local >> 1) & 1;
+                if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, limit_ns)) {
+                    note_timeout(abort_flag, status);
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d = tmem_base + acc * BN;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, limit_ns)) {
+                        note_timeout(abort_flag, status);
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(smA + stage * Cfg::kABytes));
+                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(smB + stage * Cfg::kBBytes));
+#pragma unroll
+                    for (int k = 0; k < kBK / 32; ++k)
+                        tc_mma_f8(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+                    tc_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (stop)
+                    break;
+                tc_commit(&tfull[acc]);
+            }
+            if (*abort_flag) {
+                tc_commit(drain);
+                mbar_wait(drain, 0, nullptr, kDrainLimitNs);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int quad = warp & 3;  // the TMEM lane quarter this warp may read
+        const float inv = static_cast<float>(1.0 / (static_cast<double>(__ldg(sa)) *
+                                                     static_cast<double>(__ldg(sb))));
+        const bool vec_ok = (N % 8) == 0;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
+            const uint32_t acc = local & 1;
+            const uint32_t aph = (local >> 1) & 1;
+            bool ok = mbar_wait(&tfull[acc], aph, abort_flag, limit_ns);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) {
+                if (lane == 0)
+                    note_timeout(abort_flag, status);
+                break;
+            }
+            tc_fence_after_sync();
+            int mb, nb;
+            tile_coords(tile, num_m, num_n, group_m, mb, nb);
+            const int row = mb * kBM + quad * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int j = 0; j < BN / 32; ++j) {
+                uint32_t r[32];
+                tc_ld_32x32b_x32(taddr + j * 32, r);
+                tc_wait_ld();
+                const int col0 = nb * BN + j * 32;
+                if (row < M) {
+                    __nv_bfloat16 *dst = c + static_cast<int64_t>(row) * N + col0;
+                    if (vec_ok && col0 + 32 <= N) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 o;
+                            o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
+                            o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
+                            o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
+                            o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
+                            *reinterpret_cast<uint4 *>(dst + 8 * v) = o;
+                        }
+                    } else {
+                        for (int e = 0; e < 32; ++e)
+                            if (col0 + e < N)
+                                dst[e] = __float2bfloat16_rn(__uint_as_float(r[e]) * inv);
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&tempty[acc]);
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// K-major E4M3 matrix [rows, K] as a 2-D tensor map with a 128 x box_rows box.
+bool make_kmajor_map(CUtensorMap *map, const uint8_t *ptr, int64_t rows, int64_t K, int box_rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr)
+        return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES>
+cudaError_t run_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
+                     const float *sa, const float *sb, void *c, const DeviceInfo &dev,
+                     cudaStream_t stream)
+{
+    using Cfg = GemmCfg<BN, STAGES>;
+    CUtensorMap ma, mb;
+    if (!make_kmajor_map(&ma, a, M, K, kBM) || !make_kmajor_map(&mb, b, N, K, BN))
+        return cudaErrorNotSupported;
+    static std::once_flag attr_once[64];
+    static cudaError_t attr_err[64];
+    const int dv = dev.ordinal & 63;
+    std::call_once(attr_once[dv], [&] {
+        attr_err[dv] = cudaFuncSetAttribute(gemm_kernel<BN, STAGES>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            Cfg::kSmemBytes);
+    });
+    if (attr_err[dv] != cudaSuccess)
+        return attr_err[dv];
+    const int64_t num_m = (M + kBM - 1) / kBM, num_n = (N + BN - 1) / BN;
+    const int64_t tiles = num_m * num_n;
+    const int grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
+    const int group_m = 16;
+    gemm_kernel<BN, STAGES><<<grid, kThreads, Cfg::kSmemBytes, stream>>>(
+        ma, mb, static_cast<__nv_bfloat16 *>(c), static_cast<int>(M), static_cast<int>(N),
+        static_cast<int>(K), sa, sb, dev.status, wait_limit_ns(), group_m);
+    return cudaGetLastError();
+}
+
+__global__ void wait_selftest_kernel(unsigned *status, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, nullptr, limit_ns))
+        atomicOr(status, kStatusTimeout);
+}
+
+} // namespace
+
+cudaError_t launch_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
+                        const float *sa, const float *sb, void *c, const DeviceInfo &dev,
+                        cudaStream_t stream)
+{
+    return run_gemm<256, 4>(a, b, M, N, K, sa, sb, c, dev, stream);
+}
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, const DeviceInfo &dev, cudaStream_t stream)
+{
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(dev.status, limit_ns);
+    return cudaGetLastError();
+}
+
+} // namespace f8

@@ -1,0 +1,174 @@
+/*
+ * libf8 — Float8 training linear with dynamic tensorwise scaling, for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The method (torchtitan's Float8 training, provided by torchao):
+ *   "TorchTitan" paper summary (atlas.scime.ai), Approach and the ablation
+ *   table — Float8 is applied to the linears of Llama 3.1 8B on top of
+ *   torch.compile and FSDP2; wassimseifeddine.com/posts/torchtitan, section
+ *   "Float8 Training"; stanleyjacob.dev/oss/torchtitan, Part XI item 9 — the
+ *   E4M3 encoding of "FP8 Formats for Deep Learning".  The recipe itself is
+ *   not printed on those pages; this library implements the plainest
+ *   reading of "dynamic tensorwise scaling":
+ *
+ *     amax  = max |v| over the whole bf16 tensor                (fp32)
+ *     s     = 448 / max(amax, 1e-12)                 (one IEEE fp32 division)
+ *     q     = satfinite_rne_e4m3(fl32(v * s))          (byte per element)
+ *     Y  = bf16( (q(X)  q(W)^T)  / (s_x  s_w) )        forward
+ *     dX = bf16( (q(dY) q(W))    / (s_dy s_w) )        dgrad
+ *     dW = bf16( (q(dY)^T q(X))  / (s_dy s_x) )        wgrad
+ *   with the products accumulated in fp32 on the tensor cores.
+ *
+ * Conventions for every call:
+ *   - Tensors are dense and row-major.  X is [M,K] (tokens x in-features),
+ *     W is [N,K] (nn.Linear layout), dY and Y are [M,N], dX is [M,K], dW is
+ *     [N,K].  bf16 tensors are passed as `const void*`; E4M3 tensors as
+ *     `uint8_t*` holding float8_e4m3fn codes.
+ *   - Every pointer is a DEVICE pointer of the current CUDA device, owned by
+ *     the caller.  The library allocates nothing per call.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call only enqueues work on it and returns; scales and amax values stay
+ *     in device memory and are never read back by the library.
+ *   - Argument errors are found on the host before anything is launched and
+ *     are returned as a non-zero f8_status; nothing is enqueued then.
+ *     Pointers to bf16 or E4M3 tensors must be 16-byte aligned; pointers to
+ *     fp32 scalars 4-byte aligned.
+ *   - Errors found on the device (a non-finite amax, a wait that ran past its
+ *     time limit) are recorded in a per-device status word;
+ *     f8_last_device_status() reports and clears it.
+ */
+#ifndef F8_H_
+#define F8_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    F8_OK = 0,
+    F8_ERR_INVALID = 1,     /* NULL pointer, negative size, bad combination   */
+    F8_ERR_ALIGN = 2,       /* a pointer is not 16-byte (tensors) / 4-byte aligned */
+    F8_ERR_SHAPE = 3,       /* a size breaks a layout rule (e.g. K % 16 != 0) */
+    F8_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed           */
+    F8_ERR_TIMEOUT = 5,     /* a device-side wait exceeded its time limit     */
+    F8_ERR_NONFINITE = 6,   /* an amax input held +-inf or NaN                */
+    F8_ERR_UNSUPPORTED = 7  /* no sm_100-family device / driver entry point   */
+} f8_status;
+
+/*
+ * amax_out[0] = max_i |x[i]| over n bf16 values, as fp32 (exact).
+ *   x:        device, n bf16 values, 16-byte aligned.  n == 0 gives 0.
+ *   amax_out: device, one fp32; overwritten (the call zeroes it first).
+ * A NaN or +-inf input sets F8_ERR_NONFINITE in the device status word; the
+ * value written is then unspecified.
+ */
+f8_status f8_amax(const void *x, int64_t n, float *amax_out, void *stream);
+
+/*
+ * Scale and cast one bf16 tensor to E4M3, emitting both layouts in one pass.
+ *   x:          device bf16 [rows, cols], 16-byte aligned.
+ *   amax:       device fp32 scalar (e.g. from f8_amax).
+ *   scale_out:  device fp32 scalar receiving s = 448 / max(amax, 1e-12), or NULL.
+ *   q:          device uint8 [rows, cols] (row-major copy) or NULL.
+ *   q_t:        device uint8 [cols, rows] (column-major copy: q_t[c*rows + r]
+ *               == q[r*cols + c]) or NULL.
+ * Each element is q = satfinite_rne_e4m3(fl32(x * s)): one fp32 multiply,
+ * then round-to-nearest-even onto the E4M3 grid, |v| >= 448 -> +-448.
+ * Any rows, cols >= 0 are accepted; shapes with rows % 16 == 0 and
+ * cols % 16 == 0 take the vectorised path.
+ */
+f8_status f8_cast_transpose(const void *x, int64_t rows, int64_t cols, const float *amax,
+                            float *scale_out, uint8_t *q, uint8_t *q_t, void *stream);
+
+/*
+ * C = bf16( A B^T / (scale_a * scale_b) ), fp32 accumulation on tcgen05.
+ *   a:       device E4M3 [M, K] row-major (K contiguous), 16-byte aligned.
+ *   b:       device E4M3 [N, K] row-major (K contiguous), 16-byte aligned.
+ *   scale_a, scale_b: device fp32 scalars (the scales the operands were cast with).
+ *   c:       device bf16 [M, N] row-major, 16-byte aligned; fully overwritten.
+ * K must be a multiple of 16 (the E4M3 row pitch must be a multiple of 16
+ * bytes); M, N >= 0 are otherwise free.  K == 0 writes zeros.
+ */
+f8_status f8_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
+                  const float *scale_a, const float *scale_b, void *c, void *stream);
+
+/*
+ * What the forward pass leaves for the backward pass.  All members are
+ * caller-allocated device buffers.
+ *   x_t [K, M], w_t [K, N]: E4M3 column-major copies of q(X) and q(W);
+ *   amax_x, scale_x, amax_w, scale_w: device fp32 scalars.
+ */
+typedef struct {
+    uint8_t *x_t;
+    uint8_t *w_t;
+    float *amax_x;
+    float *scale_x;
+    float *amax_w;
+    float *scale_w;
+} f8_linear_saved;
+
+/*
+ * Device workspace (bytes) that f8_linear_fwd and f8_linear_bwd need for
+ * (M, N, K): the row-major E4M3 copies of X and W (forward) or of dY and
+ * dY^T plus two scalars (backward), each region 256-byte aligned.
+ */
+size_t f8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Forward of a Float8 linear: Y [M,N] = X [M,K] W[N,K]^T.
+ *   x, w: device bf16 inputs; y: device bf16 output.
+ *   saved: filled with q(X)^T, q(W)^T and the four scalars.
+ *   workspace: device scratch of at least f8_linear_workspace_bytes(M,N,K)
+ *   bytes, 256-byte aligned; its contents are not needed after the call.
+ * M, N, K must be multiples of 16 and > 0.
+ */
+f8_status f8_linear_fwd(const void *x, const void *w, int64_t M, int64_t N, int64_t K, void *y,
+                        const f8_linear_saved *saved, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
+/*
+ * Backward of the same linear: dX [M,K] = dY W, dW [N,K] = dY^T X, using the
+ * saved q(X)^T, q(W)^T and scales from f8_linear_fwd (which must have been
+ * enqueued earlier on the same stream, or otherwise completed).
+ *   dy: device bf16 [M,N]; dx, dw: device bf16 outputs (either may be NULL
+ *   to skip that GEMM).  Workspace as for the forward pass.
+ */
+f8_status f8_linear_bwd(const void *dy, const f8_linear_saved *saved, int64_t M, int64_t N,
+                        int64_t K, void *dx, void *dw, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word.  Returns F8_OK, F8_ERR_NONFINITE or F8_ERR_TIMEOUT (the first set
+ * bit in that order of severity: TIMEOUT wins), or F8_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+f8_status f8_last_device_status(void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *f8_status_string(f8_status status);
+
+/*
+ * Failure-path self-test: launches one CTA that waits on an mbarrier nothing
+ * ever arrives on, using the same bounded wait as the GEMM pipeline, with a
+ * limit of `limit_ns` nanoseconds.  The wait gives up, records
+ * F8_ERR_TIMEOUT in the status word and the kernel returns normally, so the
+ * context stays usable.  Read the result with f8_last_device_status().
+ */
+f8_status f8_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
+/*
+ * Time limit (nanoseconds) of every device-side wait of the GEMM pipeline;
+ * default 2e9.  A wait that exceeds it aborts its CTA cleanly and records
+ * F8_ERR_TIMEOUT.  0 restores the default.
+ */
+void f8_set_wait_limit_ns(uint64_t limit_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* F8_H_ */

@@ -1,0 +1,89 @@
+"""The C ABI without a GPU: the library loads, exports every function
+include/f8.h declares, and rejects bad arguments on the host before it
+touches the device (so these calls return without any CUDA work)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from float8_mixed_precision_gb300 import build
+    build.build()
+    import float8_mixed_precision_gb300 as f8
+    return f8.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "f8.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(f8_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_five_path_calls():
+    names = _declared()
+    for n in ("f8_amax", "f8_cast_transpose", "f8_gemm", "f8_linear_fwd", "f8_linear_bwd"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    import float8_mixed_precision_gb300 as f8
+    names = _declared()
+    assert set(names) == set(f8.EXPORTS)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    import float8_mixed_precision_gb300 as f8
+    for s in range(8):
+        assert f8.f8_status_string(s).startswith("F8_")
+    assert "UNKNOWN" in f8.f8_status_string(99)
+
+
+def test_workspace_bytes(L):
+    import float8_mixed_precision_gb300 as f8
+    M, N, K = 8192, 1024, 4096
+    ws = f8.f8_linear_workspace_bytes(M, N, K)
+    assert ws >= M * K + N * K and ws >= 2 * M * N
+    assert f8.f8_linear_workspace_bytes(0, 1, 1) == 0
+
+
+FAKE = 1 << 40          # an aligned address that is never dereferenced
+FAKE_MIS = FAKE + 8     # 8-byte aligned, not 16
+
+
+@pytest.mark.parametrize("args,want", [
+    ((FAKE, FAKE, 16, 16, 17, FAKE, FAKE, FAKE, None), 3),     # K % 16
+    ((FAKE, FAKE, -1, 16, 16, FAKE, FAKE, FAKE, None), 1),     # negative M
+    ((FAKE, FAKE, 16, 16, 16, None, FAKE, FAKE, None), 1),     # missing scale
+    ((FAKE_MIS, FAKE, 16, 16, 16, FAKE, FAKE, FAKE, None), 2), # misaligned A
+    ((FAKE, FAKE, 16, 16, 16, FAKE, FAKE, FAKE_MIS, None), 2), # misaligned C
+    ((None, FAKE, 16, 16, 16, FAKE, FAKE, FAKE, None), 1),     # NULL A
+])
+def test_gemm_rejects_bad_arguments_on_host(L, args, want):
+    assert L.f8_gemm(*args) == want
+
+
+def test_other_calls_reject_bad_arguments_on_host(L):
+    assert L.f8_amax(FAKE, -5, FAKE, None) == 1
+    assert L.f8_amax(FAKE_MIS, 5, FAKE, None) == 2
+    assert L.f8_amax(FAKE, 5, None, None) == 1
+    assert L.f8_cast_transpose(FAKE, 4, -1, FAKE, None, FAKE, FAKE, None) == 1
+    assert L.f8_cast_transpose(FAKE, 4, 4, None, None, FAKE, FAKE, None) == 1
+    assert L.f8_cast_transpose(FAKE, 4, 4, FAKE, None, FAKE_MIS, FAKE, None) == 2
+    from float8_mixed_precision_gb300.binding import _Saved
+    s = _Saved(FAKE, FAKE, FAKE, FAKE + 4, FAKE + 8, FAKE + 12)
+    ws = 1 << 30
+    assert L.f8_linear_fwd(FAKE, FAKE, 16, 16, 24, FAKE, ctypes.byref(s), FAKE, ws, None) == 3
+    assert L.f8_linear_fwd(FAKE, FAKE, 0, 16, 16, FAKE, ctypes.byref(s), FAKE, ws, None) == 1
+    assert L.f8_linear_fwd(FAKE, FAKE, 16, 16, 16, FAKE, None, FAKE, ws, None) == 1
+    assert L.f8_linear_fwd(FAKE, FAKE, 16, 16, 16, FAKE, ctypes.byref(s), FAKE, 10, None) == 1
+    assert L.f8_linear_fwd(FAKE, FAKE, 16, 16, 16, FAKE, ctypes.byref(s), FAKE + 16, ws, None) == 2
+    bad = _Saved(FAKE, None, FAKE, FAKE, FAKE, FAKE)
+    assert L.f8_linear_bwd(FAKE, ctypes.byref(bad), 16, 16, 16, FAKE, FAKE, FAKE, ws, None) == 1
+    assert L.f8_linear_bwd(FAKE, ctypes.byref(s), 16, 16, 16, FAKE_MIS, FAKE, FAKE, ws, None) == 2

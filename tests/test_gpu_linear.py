@@ -1,0 +1,128 @@
+"""GPU parity of the whole Float8 linear (f8_linear_fwd / f8_linear_bwd)
+against the oracle's step-by-step composition.
+
+Small shapes are compared in full.  The five workloads run at full size in
+the same launch configuration the benchmark times; there amax, scales and
+every E4M3 byte (q(X)^T, q(W)^T saved by the forward pass, plus the oracle's
+q of every tensor) are compared in full, and Y, dX, dW on one sampled row
+per 128-row band and one sampled column per 256-column band, so every
+output tile of every GEMM is visited.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from float8_mixed_precision_gb300 import workloads as wl
+from tolerance import check_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def f8():
+    import float8_mixed_precision_gb300 as m
+    from float8_mixed_precision_gb300 import build
+    build.build()
+    oracle.build()
+    m.lib()
+    return m
+
+
+def _run_gpu(f8, x, w, dy):
+    xd, wd, dyd = x.to(DEV), w.to(DEV), dy.to(DEV)
+    y, saved = f8.f8_linear_fwd(xd, wd)
+    dx, dw = f8.f8_linear_bwd(dyd, saved)
+    assert f8.f8_last_device_status() == 0
+    return y, dx, dw, saved
+
+
+def _check_saved(saved, fwd):
+    s = saved.scalars.cpu().numpy()
+    assert s[0] == fwd["x"]["amax"] and s[1] == fwd["x"]["scale"]
+    assert s[2] == fwd["w"]["amax"] and s[3] == fwd["w"]["scale"]
+    assert np.array_equal(saved.x_t.cpu().numpy(), fwd["x"]["qt"])
+    assert np.array_equal(saved.w_t.cpu().numpy(), fwd["w"]["qt"])
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 16, 16), (256, 512, 256), (272, 400, 528), (1024, 768, 640)])
+def test_linear_full_compare(f8, M, N, K):
+    d = wl.custom_linear(M, K, N, seed=M + N + K)
+    y, dx, dw, saved = _run_gpu(f8, d["x"], d["w"], d["dy"])
+    fwd = oracle.linear_fwd(wl.bits(d["x"]), wl.bits(d["w"]))
+    bwd = oracle.linear_bwd(wl.bits(d["dy"]), fwd)
+    _check_saved(saved, fwd)
+    check_close(y, fwd["y"], what="Y")
+    check_close(dx, bwd["dx"], what="dX")
+    check_close(dw, bwd["dw"], what="dW")
+
+
+def test_tiny_workload_full_compare(f8):
+    d = wl.linear_inputs(1, 0)
+    y, dx, dw, saved = _run_gpu(f8, d["x"], d["w"], d["dy"])
+    fwd = oracle.linear_fwd(wl.bits(d["x"]), wl.bits(d["w"]))
+    bwd = oracle.linear_bwd(wl.bits(d["dy"]), fwd)
+    _check_saved(saved, fwd)
+    check_close(y, fwd["y"], what="Y")
+    check_close(dx, bwd["dx"], what="dX")
+    check_close(dw, bwd["dw"], what="dW")
+
+
+def test_backward_without_dx_or_dw(f8):
+    d = wl.custom_linear(128, 256, 192, seed=5)
+    y, dx, dw, saved = _run_gpu(f8, d["x"], d["w"], d["dy"])
+    dx2, none = f8.f8_linear_bwd(d["dy"].to(DEV), saved, want_dw=False)
+    none2, dw2 = f8.f8_linear_bwd(d["dy"].to(DEV), saved, want_dx=False)
+    assert none is None and none2 is None
+    assert torch.equal(dx, dx2) and torch.equal(dw, dw2)
+
+
+def _bands(n, width, rng):
+    return np.array([b * width + rng.integers(0, min(width, n - b * width))
+                     for b in range((n + width - 1) // width)], np.int64)
+
+
+CASES = [(c, l) for c in (1, 2, 3, 4, 5) for l in range(len(wl.workload(c)[1]))]
+
+
+@pytest.mark.parametrize("c,l", CASES, ids=[f"w{c}-{wl.workload(c)[1][l].name}" for c, l in CASES])
+def test_workload_linear_full_size(f8, c, l):
+    lin = wl.workload(c)[1][l]
+    d = wl.linear_inputs(c, l)
+    y, dx, dw, saved = _run_gpu(f8, d["x"], d["w"], d["dy"])
+    qx = oracle.quantize(wl.bits(d["x"]))
+    qw = oracle.quantize(wl.bits(d["w"]))
+    qdy = oracle.quantize(wl.bits(d["dy"]))
+    _check_saved(saved, {"x": qx, "w": qw})
+    # the row-major copies and q(dY) come from the same cast kernel the linear launches
+    for t, q in (("x", qx), ("w", qw), ("dy", qdy)):
+        td = d[t].to(DEV)
+        gq, gqt, gs = f8.f8_cast_transpose(td, f8.f8_amax(td))
+        assert gs.item() == float(q["scale"])
+        assert np.array_equal(gq.cpu().numpy(), q["q"]) and np.array_equal(gqt.cpu().numpy(), q["qt"])
+        del td, gq, gqt
+    del d
+    rng = np.random.default_rng(1000 * c + l)
+    M, N, K = lin.M, lin.N, lin.K
+    # Y = q(X) q(W)^T
+    rows = _bands(M, 128, rng)
+    cols = _bands(N, 256, rng)
+    ref = oracle.gemm_rows(qx["q"], qw["q"], qx["scale"], qw["scale"], rows)
+    check_close(y[torch.from_numpy(rows).to(DEV)], ref, what="Y rows")
+    ref = oracle.gemm_cols(qx["q"], qw["q"], qx["scale"], qw["scale"], cols)
+    check_close(y[:, torch.from_numpy(cols).to(DEV)].t().contiguous(), ref, what="Y cols")
+    # dX = q(dY) q(W)  (B operand = q(W)^T [K, N])
+    rows = _bands(M, 128, rng)
+    cols = _bands(K, 256, rng)
+    ref = oracle.gemm_rows(qdy["q"], qw["qt"], qdy["scale"], qw["scale"], rows)
+    check_close(dx[torch.from_numpy(rows).to(DEV)], ref, what="dX rows")
+    ref = oracle.gemm_cols(qdy["q"], qw["qt"], qdy["scale"], qw["scale"], cols)
+    check_close(dx[:, torch.from_numpy(cols).to(DEV)].t().contiguous(), ref, what="dX cols")
+    # dW = q(dY)^T q(X)  (A = q(dY)^T [N, M], B = q(X)^T [K, M])
+    rows = _bands(N, 128, rng)
+    cols = _bands(K, 256, rng)
+    ref = oracle.gemm_rows(qdy["qt"], qx["qt"], qdy["scale"], qx["scale"], rows)
+    check_close(dw[torch.from_numpy(rows).to(DEV)], ref, what="dW rows")
+    ref = oracle.gemm_cols(qdy["qt"], qx["qt"], qdy["scale"], qx["scale"], cols)
+    check_close(dw[:, torch.from_numpy(cols).to(DEV)].t().contiguous(), ref, what="dW cols")
