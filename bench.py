@@ -1,0 +1,469 @@
+"""Benchmark: Float8 linear forward + backward (dynamic tensorwise scaling).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+
+One step = every linear of the workload through the whole path: amax(X),
+amax(W), cast_transpose(X), cast_transpose(W), GEMM Y = XW^T, amax(dY),
+cast_transpose(dY), GEMM dX = dY W, GEMM dW = dY^T X.  The metric is GEMM
+work (6 M N K flops per linear) over the whole step's time, in TFLOP/s.
+
+Inputs are seeded synthetic bf16 tensors (float8_mixed_precision_gb300.workloads),
+resident in HBM before timing.  A step's inputs (0.5 GB for the attention
+workload) exceed the 129 MB L2, so no L2 flush is inserted between steps.
+
+The JSON line carries, besides the contract keys:
+  roofline      the GEMM kernel: GEMM flops of the step over the summed
+                duration of its GEMM launches (CUDA events on the launch
+                stream, averaged over a timed run of the same steps), against
+                the measured bf16 peak x 2 (the FP8 : BF16 dense ratio);
+  kernels       the same per-kernel breakdown for amax and cast_transpose
+                (algorithmic bytes: 2 B/elem and 4 B/elem);
+  e2e           the same metric through the public API with pinned host
+                buffers: inputs copied in and Y, dX, dW copied out every step;
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload.
+With torchrun (N > 1) every rank runs an independent replica on its own GPU
+(no collective on the data path); value = all ranks' work / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP8 linear fwd+bwd TFLOP/s at Llama-3.1-8B shapes; % of GB300 FP8 peak"
+UNIT = "TFLOP/s"
+FP8_NOMINAL_TFLOPS = 4500.0
+FP8_PER_BF16 = 2.0          # nominal dense FP8 : BF16 tensor throughput
+HBM_NOMINAL_GBS = 8000.0
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a host float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+class Linear8:
+    """Device buffers of one linear: inputs, outputs, saved tensors, workspace."""
+
+    def __init__(self, f8, lin, inputs, device):
+        import torch
+        self.lin = lin
+        self.x = inputs["x"].to(device)
+        self.w = inputs["w"].to(device)
+        self.dy = inputs["dy"].to(device)
+        M, N, K = lin.M, lin.N, lin.K
+        self.y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=device)
+        self.dw = torch.empty((N, K), dtype=torch.bfloat16, device=device)
+        self.saved = f8.LinearSaved.empty(M, N, K, device)
+        self.ws = f8.workspace(M, N, K, device)
+        # the decomposed path (same kernels, launched one by one) for per-kernel timing
+        self.xq = torch.empty((M, K), dtype=torch.uint8, device=device)
+        self.wq = torch.empty((N, K), dtype=torch.uint8, device=device)
+        self.dyq = torch.empty((M, N), dtype=torch.uint8, device=device)
+        self.dyt = torch.empty((N, M), dtype=torch.uint8, device=device)
+        self.dys = torch.empty(2, dtype=torch.float32, device=device)
+
+    def step(self, f8):
+        f8.f8_linear_fwd(self.x, self.w, self.y, self.saved, self.ws)
+        f8.f8_linear_bwd(self.dy, self.saved, dx=self.dx, dw=self.dw, ws=self.ws)
+
+    def step_timed(self, f8, ev):
+        """The same launches as step(), one C call per kernel, bracketed by events."""
+        s = self.saved
+        ev("amax", 2 * self.x.numel(), lambda: f8.f8_amax(self.x, s.amax_x))
+        ev("amax", 2 * self.w.numel(), lambda: f8.f8_amax(self.w, s.amax_w))
+        ev("cast", 4 * self.x.numel(), lambda: f8.f8_cast_transpose(self.x, s.amax_x, s.scale_x, self.xq, s.x_t))
+        ev("cast", 4 * self.w.numel(), lambda: f8.f8_cast_transpose(self.w, s.amax_w, s.scale_w, self.wq, s.w_t))
+        M, N, K = self.lin.M, self.lin.N, self.lin.K
+        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.xq, self.wq, s.scale_x, s.scale_w, self.y))
+        ev("amax", 2 * self.dy.numel(), lambda: f8.f8_amax(self.dy, self.dys[0]))
+        ev("cast", 4 * self.dy.numel(), lambda: f8.f8_cast_transpose(self.dy, self.dys[0], self.dys[1], self.dyq, self.dyt))
+        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyq, s.w_t, self.dys[1], s.scale_w, self.dx))
+        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyt, s.x_t, self.dys[1], s.scale_x, self.dw))
+
+
+KERNELS_PER_LINEAR = 9  # 3 amax + 3 cast_transpose + 3 GEMM
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import float8_mixed_precision_gb300 as f8
+    from float8_mixed_precision_gb300 import workloads as wl
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    f8.lib()
+    name, lins = wl.workload(args.config)
+    layers = [Linear8(f8, lin, wl.linear_inputs(args.config, i), device) for i, lin in enumerate(lins)]
+    flops_step = sum(l.flops for l in lins)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- warm-up, then the timed region (library calls f8_linear_fwd/bwd)
+    for _ in range(args.warmup):
+        for L in layers:
+            L.step(f8)
+    st = f8.f8_last_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {f8.f8_status_string(st)}")
+    barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        t0.record(stream)
+        for _ in range(args.steps):
+            for L in layers:
+                L.step(f8)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = t0.elapsed_time(t1)
+    st = f8.f8_last_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after the timed region: {f8.f8_status_string(st)}")
+    ms_max = max_over_ranks(ms, world, device)
+    total_flops = sum_over_ranks(flops_step * args.steps, world, device)
+    value = total_flops / (ms_max * 1e-3) / 1e12
+
+    # ---- per-kernel breakdown: the same kernels, each bracketed by events
+    nsteps_k = max(1, min(args.steps, 100))
+    rec = []
+
+    def ev(kind, work, fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        rec.append((kind, work, a, b))
+
+    for _ in range(2):
+        for L in layers:
+            L.step_timed(f8, lambda k, w, fn: fn())
+    torch.cuda.synchronize()
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0.record(stream)
+    for _ in range(nsteps_k):
+        for L in layers:
+            L.step_timed(f8, ev)
+    k1.record(stream)
+    torch.cuda.synchronize()
+    breakdown_ms = k0.elapsed_time(k1) / nsteps_k
+    per = {}
+    for kind, work, a, b in rec:
+        d = per.setdefault(kind, {"launches": 0, "ms": 0.0, "work": 0.0})
+        d["launches"] += 1
+        d["ms"] += a.elapsed_time(b)
+        d["work"] += work
+    tot_ms = sum(d["ms"] for d in per.values())
+    peaks = load_peaks()
+    fp8_peak = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+    kernels = {}
+    for kind, d in per.items():
+        rate = d["work"] / (d["ms"] * 1e-3)
+        e = {"launches_per_step": d["launches"] // nsteps_k, "ms_per_step": d["ms"] / nsteps_k,
+             "share": d["ms"] / tot_ms}
+        if kind == "gemm":
+            e.update({"tflops": rate / 1e12, "frac_of_fp8_measured": rate / 1e12 / fp8_peak,
+                      "frac_of_fp8_nominal": rate / 1e12 / FP8_NOMINAL_TFLOPS})
+        else:
+            e.update({"gbs": rate / 1e9, "frac_of_hbm_measured": rate / 1e9 / peaks["hbm_gbs"]})
+        kernels[kind] = e
+    g = per["gemm"]
+    achieved = g["work"] / (g["ms"] * 1e-3) / 1e12
+    roofline = {"kernel": "gemm_kernel (tcgen05 kind::f8f6f4)", "bound": "tensor",
+                "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp8_peak,
+                "peak_note": f"{peaks['source']} bf16 sustained {peaks['bf16_tflops_sustained']} x {FP8_PER_BF16} (FP8:BF16 dense)",
+                "frac_of_nominal_4500": achieved / FP8_NOMINAL_TFLOPS,
+                "traffic": None}
+
+    # ---- end to end: pinned host buffers in, results out, every step
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = run_e2e(f8, layers, args, device, stream, flops_step, world)
+
+    return {"value": value, "ms_per_step": ms_max / args.steps, "name": name, "lins": lins,
+            "clocks": clocks.summary(), "kernels": kernels, "roofline": roofline,
+            "breakdown_ms_per_step": breakdown_ms, "e2e": e2e,
+            "gpu_launches": KERNELS_PER_LINEAR * len(layers) * args.steps}
+
+
+def run_e2e(f8, layers, args, device, stream, flops_step, world):
+    import torch
+    host = []
+    h2d = d2h = 0
+    for L in layers:
+        hx = L.x.cpu().pin_memory()
+        hw = L.w.cpu().pin_memory()
+        hdy = L.dy.cpu().pin_memory()
+        hy = torch.empty(L.y.shape, dtype=torch.bfloat16).pin_memory()
+        hdx = torch.empty(L.dx.shape, dtype=torch.bfloat16).pin_memory()
+        hdw = torch.empty(L.dw.shape, dtype=torch.bfloat16).pin_memory()
+        host.append((hx, hw, hdy, hy, hdx, hdw))
+        h2d += 2 * (hx.numel() + hw.numel() + hdy.numel())
+        d2h += 2 * (hy.numel() + hdx.numel() + hdw.numel())
+
+    def step():
+        for L, (hx, hw, hdy, hy, hdx, hdw) in zip(layers, host):
+            L.x.copy_(hx, non_blocking=True)
+            L.w.copy_(hw, non_blocking=True)
+            L.dy.copy_(hdy, non_blocking=True)
+            L.step(f8)
+            hy.copy_(L.y, non_blocking=True)
+            hdx.copy_(L.dx, non_blocking=True)
+            hdw.copy_(L.dw, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.e2e_steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1), world, device)
+    total = sum_over_ranks(flops_step * args.e2e_steps, world, device)
+    return {"value": total / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+            "ms_per_step": ms / args.e2e_steps}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(config: int, lin_index: int, rows: int):
+    """The oracle on a bounded sample of one linear: amax, scale and cast of X,
+    W and dY in full, then ``rows`` output rows of each of the three GEMMs.
+    Returns (GEMM flops of the sampled rows, seconds)."""
+    import numpy as np
+
+    import oracle
+    from float8_mixed_precision_gb300 import workloads as wl
+
+    lin = wl.workload(config)[1][lin_index]
+    d = wl.linear_inputs(config, lin_index)
+    xb, wb, dyb = wl.bits(d["x"]), wl.bits(d["w"]), wl.bits(d["dy"])
+    rng = np.random.default_rng(lin_index)
+    M, N, K = lin.M, lin.N, lin.K
+    r_m = np.sort(rng.choice(M, size=min(rows, M), replace=False))
+    r_n = np.sort(rng.choice(N, size=min(rows, N), replace=False))
+    t = time.perf_counter()
+    qx = oracle.quantize(xb)
+    qw = oracle.quantize(wb)
+    qdy = oracle.quantize(dyb)
+    oracle.gemm_rows(qx["q"], qw["q"], qx["scale"], qw["scale"], r_m)          # Y rows
+    oracle.gemm_rows(qdy["q"], qw["qt"], qdy["scale"], qw["scale"], r_m)       # dX rows
+    oracle.gemm_rows(qdy["qt"], qx["qt"], qdy["scale"], qx["scale"], r_n)      # dW rows
+    sec = time.perf_counter() - t
+    flops = 2 * (len(r_m) * N * K + len(r_m) * K * N + len(r_n) * K * M)
+    return flops, sec
+
+
+def cpu_baseline(config: int, rows: int):
+    import oracle
+    from float8_mixed_precision_gb300 import workloads as wl
+    flops, sec = oracle_sample(config, 0, rows)
+    lin = wl.workload(config)[1][0]
+    return {"value": flops / sec / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": sec,
+            "sample": (f"linear {lin.name} (M={lin.M}, K={lin.K}, N={lin.N}): amax, scale and "
+                       f"cast of X, W, dY in full, then {rows} sampled output rows of each of "
+                       f"Y, dX and dW; value = GEMM flops of the sampled rows / wall time")}
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the CPU oracle, as it stands, timed on the host cores."""
+    import oracle
+    from float8_mixed_precision_gb300 import workloads as wl
+    name, lins = wl.workload(args.config)
+    if rank != 0:
+        return 0
+    oracle.build()
+    rows = args.ref_rows
+    for i in range(args.warmup):
+        oracle_sample(args.config, i % len(lins), max(1, rows // 8))
+    flops = sec = 0.0
+    for i in range(args.steps):
+        f, s = oracle_sample(args.config, i % len(lins), rows)
+        flops += f
+        sec += s
+    value = flops / sec / 1e12
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": name, "linears": [l.name for l in lins], "M": lins[0].M},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": f"per step one linear (rotating): amax/scale/cast of X, W, dY "
+                                       f"in full + {rows} sampled rows of each GEMM"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ main
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-rows", type=int, default=1024)
+    ap.add_argument("--ref-rows", type=int, default=128)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    cpu = None
+    if rank == 0:
+        # the CPU oracle runs first, before any GPU work in this process
+        cpu = cpu_baseline(args.config, args.cpu_rows) if world == 1 else None
+    r = run_ours(args, world, rank, local)
+    if rank == 0:
+        lins = r["lins"]
+        line = {
+            "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3", "data": "synthetic (seeded; workloads.py)",
+            "config": {"workload": r["name"],
+                       "linears": [f"{l.name} M={l.M} K={l.K} N={l.N}" for l in lins],
+                       "flops_per_step": sum(l.flops for l in lins),
+                       "parallelism": "replicas" if world > 1 else "single-gpu",
+                       "l2": "no flush: a step's inputs exceed L2"},
+            "pct_of_fp8_peak_nominal": 100 * r["value"] / FP8_NOMINAL_TFLOPS,
+            "roofline": r["roofline"], "kernels": r["kernels"],
+            "breakdown_ms_per_step": r["breakdown_ms_per_step"],
+            "clocks": r["clocks"], "gpu_launches": r["gpu_launches"],
+            "e2e": r["e2e"], "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -289,24 +289,26 @@ void or_gemm_rows(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int6
                   float sa, float sb, const int64_t *rows, int64_t nrows, uint16_t *out)
 {
     (void)M;
+    int32_t *za = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nrows * K > 0 ? nrows * K : 1));
+    for (int64_t i = 0; i < nrows; ++i)
+        decode_row_z(a + rows[i] * K, K, za + i * K);
 #pragma omp parallel
     {
-        int32_t *za = (int32_t *)malloc(sizeof(int32_t) * (size_t)(K > 0 ? K : 1));
         int32_t *zr = (int32_t *)malloc(sizeof(int32_t) * (size_t)(K > 0 ? K : 1));
-#pragma omp for schedule(dynamic, 1)
+#pragma omp for schedule(dynamic, 16)
         for (int64_t n = 0; n < N; ++n) {
             decode_row_z(b + n * K, K, zr);
             for (int64_t i = 0; i < nrows; ++i) {
-                decode_row_z(a + rows[i] * K, K, za);
+                const int32_t *zi = za + i * K;
                 int64_t acc = 0;
                 for (int64_t k = 0; k < K; ++k)
-                    acc += (int64_t)za[k] * (int64_t)zr[k];
+                    acc += (int64_t)zi[k] * (int64_t)zr[k];
                 out[i * N + n] = finish(acc, sa, sb);
             }
         }
-        free(za);
         free(zr);
     }
+    free(za);
 }
 
 /* Selected columns: out[j, m] = C[m, cols[j]] for m < M. */
@@ -314,24 +316,26 @@ void or_gemm_cols(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int6
                   float sa, float sb, const int64_t *cols, int64_t ncols, uint16_t *out)
 {
     (void)N;
+    int32_t *zb = (int32_t *)malloc(sizeof(int32_t) * (size_t)(ncols * K > 0 ? ncols * K : 1));
+    for (int64_t j = 0; j < ncols; ++j)
+        decode_row_z(b + cols[j] * K, K, zb + j * K);
 #pragma omp parallel
     {
         int32_t *za = (int32_t *)malloc(sizeof(int32_t) * (size_t)(K > 0 ? K : 1));
-        int32_t *zr = (int32_t *)malloc(sizeof(int32_t) * (size_t)(K > 0 ? K : 1));
-#pragma omp for schedule(dynamic, 1)
+#pragma omp for schedule(dynamic, 16)
         for (int64_t m = 0; m < M; ++m) {
             decode_row_z(a + m * K, K, za);
             for (int64_t j = 0; j < ncols; ++j) {
-                decode_row_z(b + cols[j] * K, K, zr);
+                const int32_t *zj = zb + j * K;
                 int64_t acc = 0;
                 for (int64_t k = 0; k < K; ++k)
-                    acc += (int64_t)za[k] * (int64_t)zr[k];
+                    acc += (int64_t)za[k] * (int64_t)zj[k];
                 out[j * M + m] = finish(acc, sa, sb);
             }
         }
         free(za);
-        free(zr);
     }
+    free(zb);
 }
 
 /* Number of threads the parallel loops above use. */
