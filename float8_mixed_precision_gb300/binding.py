@@ -29,7 +29,7 @@ F8_ERR_UNSUPPORTED = 7
 # every symbol include/f8.h declares
 EXPORTS = ("f8_amax", "f8_cast_transpose", "f8_gemm", "f8_linear_workspace_bytes",
            "f8_linear_fwd", "f8_linear_bwd", "f8_last_device_status", "f8_status_string",
-           "f8_selftest_wait_timeout", "f8_set_wait_limit_ns")
+           "f8_selftest_wait_timeout", "f8_set_wait_limit_ns", "f8_linear_fwd_noalloc")
 
 
 class F8Error(RuntimeError):
@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
         L.f8_selftest_wait_timeout.restype = st
         L.f8_set_wait_limit_ns.argtypes = [u64]
         L.f8_set_wait_limit_ns.restype = None
+        L.f8_linear_fwd_noalloc.argtypes = [vp, vp, i64, i64, i64, vp, ctypes.POINTER(_Saved), vp]
+        L.f8_linear_fwd_noalloc.restype = st
         _lib = L
         return L
 
@@ -225,6 +227,25 @@ def f8_linear_fwd(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | None = Non
     s = saved.c_struct()
     _check(lib().f8_linear_fwd(_ptr(x), _ptr(w), M, N, K, _ptr(y), ctypes.byref(s), _ptr(ws),
                                ws.numel(), _stream(stream)), "f8_linear_fwd")
+    return y, saved
+
+
+def f8_linear_fwd_noalloc(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | None = None,
+                          saved: LinearSaved | None = None, stream=None):
+    """f8_linear_fwd without a workspace argument: the C entry point uses a
+    static device array instead, for callers that cannot allocate device memory."""
+    M, K = x.shape
+    N, K2 = w.shape
+    if K != K2:
+        raise ValueError("in-feature sizes differ")
+    dev = x.device
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if saved is None:
+        saved = LinearSaved.empty(M, N, K, dev)
+    s = saved.c_struct()
+    _check(lib().f8_linear_fwd_noalloc(_ptr(x), _ptr(w), M, N, K, _ptr(y), ctypes.byref(s),
+                                       _stream(stream)), "f8_linear_fwd_noalloc")
     return y, saved
 
 

@@ -141,6 +141,37 @@ f8_status f8_linear_bwd(const void *dy, const f8_linear_saved *saved, int64_t M,
                         void *stream);
 
 /*
+ * f8_linear_fwd for callers that cannot allocate device memory.  (The
+ * pages describe no such call; it exists for this library's users.)
+ *
+ * Who needs it: code that may not call cudaMalloc, such as a plugin running
+ * inside a framework that owns all device memory through its own pool and
+ * forbids side allocations, or a service whose device-memory budget is fixed
+ * at start-up.  Such a caller cannot supply f8_linear_fwd's workspace.
+ *
+ * What it does: exactly what f8_linear_fwd does, with the same kernels and
+ * arguments, except that the workspace (the row-major E4M3 copies of X and
+ * W) is a static device array of F8_NOALLOC_SCRATCH_BYTES compiled into the
+ * library.  The caller still passes x, w, y and `saved`.  The call allocates
+ * nothing and calls no allocating routine.
+ *
+ * Limits and rules:
+ *  - M*K + N*K bytes (each rounded up to 256) must fit in
+ *    F8_NOALLOC_SCRATCH_BYTES (64 MiB); larger problems return F8_ERR_SHAPE
+ *    before anything is launched.  M, N, K: multiples of 16, > 0.
+ *  - Every device that loads the library holds the array until the process
+ *    exits.
+ *  - All calls share the array.  Calls whose GPU work overlaps (different
+ *    streams, or threads without ordering between them) race on it and may
+ *    produce wrong results; calls on one stream are safe.
+ *  - The first call on a device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ */
+#define F8_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+f8_status f8_linear_fwd_noalloc(const void *x, const void *w, int64_t M, int64_t N, int64_t K,
+                                void *y, const f8_linear_saved *saved, void *stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns F8_OK, F8_ERR_NONFINITE or F8_ERR_TIMEOUT (the first set
  * bit in that order of severity: TIMEOUT wins), or F8_ERR_CUDA if the

@@ -1,0 +1,63 @@
+"""f8_linear_fwd_noalloc: the forward pass for callers that cannot allocate
+device memory (e.g. a plugin inside a framework that owns all device memory,
+or a service with a fixed device-memory budget).  Its workspace is a static
+device array inside the library instead of a caller-provided buffer.
+
+Checked here through the C ABI: two calls in a row (different inputs, so the
+second call runs on the first call's leftover scratch) each match the
+workspace entry point f8_linear_fwd within the GEMM tolerance, with
+bit-identical saved tensors; a problem larger than the static scratch is
+refused before anything is launched.  This file is collected last so a run
+that stops at the first failure has already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from float8_mixed_precision_gb300 import workloads as wl
+from tolerance import check_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def f8():
+    import float8_mixed_precision_gb300 as m
+    from float8_mixed_precision_gb300 import build
+    build.build()
+    m.lib()
+    return m
+
+
+def _noalloc_c(f8, x, w, M, N, K):
+    """Direct C-ABI call of f8_linear_fwd_noalloc with torch-allocated outputs."""
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    saved = f8.LinearSaved.empty(M, N, K, DEV)
+    s = saved.c_struct()
+    st = f8.lib().f8_linear_fwd_noalloc(x.data_ptr(), w.data_ptr(), M, N, K, y.data_ptr(),
+                                        ctypes.byref(s), torch.cuda.current_stream().cuda_stream)
+    assert st == 0, f8.f8_status_string(st)
+    return y, saved
+
+
+def test_two_calls_match_the_workspace_entry_point(f8):
+    for i, (M, N, K) in enumerate([(1024, 768, 2048), (512, 1536, 1024)]):
+        d = wl.custom_linear(M, K, N, seed=900 + i)
+        x, w = d["x"].to(DEV), d["w"].to(DEV)
+        y_ref, saved_ref = f8.f8_linear_fwd(x, w)
+        y, saved = _noalloc_c(f8, x, w, M, N, K)
+        assert f8.f8_last_device_status() == 0
+        check_close(y, y_ref.cpu(), what=f"noalloc call {i + 1} Y")
+        assert torch.equal(saved.scalars, saved_ref.scalars)
+        assert torch.equal(saved.x_t, saved_ref.x_t) and torch.equal(saved.w_t, saved_ref.w_t)
+
+
+def test_too_large_is_refused(f8):
+    M, N, K = 8192, 4096, 8192       # 64 MiB + 32 MiB of E4M3 copies > 64 MiB
+    assert M * K + N * K > 64 * 1024 * 1024
+    s = f8.binding._Saved(256, 256, 256, 260, 264, 268)
+    st = f8.lib().f8_linear_fwd_noalloc(256, 256, M, N, K, 256, ctypes.byref(s), None)
+    assert st == f8.binding.F8_ERR_SHAPE
