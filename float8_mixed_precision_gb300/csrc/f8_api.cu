@@ -39,25 +39,60 @@ f8_status from_cuda(cudaError_t e)
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Workspace of the forward pass: q(X) [M,K], q(W) [N,K], then the amax
+// partial maxima of X and of W.  Of the backward pass: q(dY) [M,N],
+// q(dY)^T [N,M], amax and scale of dY, then the partial maxima of dY.
+constexpr size_t kPartialsBytes = sizeof(unsigned) * kMaxAmaxPartials;
+
 struct FwdWs {
     uint8_t *x_q;
     uint8_t *w_q;
+    unsigned *parts_x;
+    unsigned *parts_w;
 };
 struct BwdWs {
     uint8_t *dy_q;
     uint8_t *dy_t;
     float *amax_dy;
     float *scale_dy;
+    unsigned *parts_dy;
 };
 
 size_t fwd_ws_bytes(int64_t M, int64_t N, int64_t K)
 {
-    return round256(static_cast<size_t>(M) * K) + round256(static_cast<size_t>(N) * K);
+    return round256(static_cast<size_t>(M) * K) + round256(static_cast<size_t>(N) * K) +
+           2 * kPartialsBytes;
 }
 
 size_t bwd_ws_bytes(int64_t M, int64_t N)
 {
-    return 2 * round256(static_cast<size_t>(M) * N) + 256;
+    return 2 * round256(static_cast<size_t>(M) * N) + 256 + kPartialsBytes;
+}
+
+FwdWs fwd_ws(void *workspace, int64_t M, int64_t N, int64_t K)
+{
+    uint8_t *p = static_cast<uint8_t *>(workspace);
+    FwdWs w;
+    w.x_q = p;
+    p += round256(static_cast<size_t>(M) * K);
+    w.w_q = p;
+    p += round256(static_cast<size_t>(N) * K);
+    w.parts_x = reinterpret_cast<unsigned *>(p);
+    w.parts_w = reinterpret_cast<unsigned *>(p + kPartialsBytes);
+    return w;
+}
+
+BwdWs bwd_ws(void *workspace, int64_t M, int64_t N)
+{
+    uint8_t *p = static_cast<uint8_t *>(workspace);
+    const size_t mn = round256(static_cast<size_t>(M) * N);
+    BwdWs w;
+    w.dy_q = p;
+    w.dy_t = p + mn;
+    w.amax_dy = reinterpret_cast<float *>(p + 2 * mn);
+    w.scale_dy = reinterpret_cast<float *>(p + 2 * mn + 128);
+    w.parts_dy = reinterpret_cast<unsigned *>(p + 2 * mn + 256);
+    return w;
 }
 
 } // namespace
@@ -209,8 +244,8 @@ f8_status f8_cast_transpose(const void *x, int64_t rows, int64_t cols, const flo
     F8_TRY(check_cast_args(x, rows, cols, amax, scale_out, q, q_t));
     const DeviceInfo *dev;
     F8_TRY(get_device(&dev));
-    return from_cuda(launch_cast_transpose(x, rows, cols, amax, scale_out, q, q_t, *dev,
-                                           static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_cast_transpose(x, rows, cols, amax, nullptr, 0, nullptr, scale_out, q,
+                                           q_t, *dev, static_cast<cudaStream_t>(stream)));
 }
 
 f8_status f8_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
@@ -250,13 +285,15 @@ f8_status f8_linear_fwd(const void *x, const void *w, int64_t M, int64_t N, int6
     const DeviceInfo *dev;
     F8_TRY(get_device(&dev));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    FwdWs fw{ws, ws + round256(static_cast<size_t>(M) * K)};
-
-    F8_TRY_CUDA(launch_amax(x, M * K, saved->amax_x, *dev, st));
-    F8_TRY_CUDA(launch_amax(w, N * K, saved->amax_w, *dev, st));
-    F8_TRY_CUDA(launch_cast_transpose(x, M, K, saved->amax_x, saved->scale_x, fw.x_q, saved->x_t, *dev, st));
-    F8_TRY_CUDA(launch_cast_transpose(w, N, K, saved->amax_w, saved->scale_w, fw.w_q, saved->w_t, *dev, st));
+    const FwdWs fw = fwd_ws(workspace, M, N, K);
+    int np = 0;
+    // each cast follows its own amax so that its re-read of the tensor hits L2
+    F8_TRY_CUDA(launch_amax_partials(x, M * K, fw.parts_x, &np, *dev, st));
+    F8_TRY_CUDA(launch_cast_transpose(x, M, K, nullptr, fw.parts_x, np, saved->amax_x,
+                                      saved->scale_x, fw.x_q, saved->x_t, *dev, st));
+    F8_TRY_CUDA(launch_amax_partials(w, N * K, fw.parts_w, &np, *dev, st));
+    F8_TRY_CUDA(launch_cast_transpose(w, N, K, nullptr, fw.parts_w, np, saved->amax_w,
+                                      saved->scale_w, fw.w_q, saved->w_t, *dev, st));
     return from_cuda(launch_gemm(fw.x_q, fw.w_q, M, N, K, saved->scale_x, saved->scale_w, y, *dev, st));
 }
 
@@ -275,14 +312,11 @@ f8_status f8_linear_bwd(const void *dy, const f8_linear_saved *saved, int64_t M,
     const DeviceInfo *dev;
     F8_TRY(get_device(&dev));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const size_t mn = round256(static_cast<size_t>(M) * N);
-    BwdWs bw{ws, ws + mn, reinterpret_cast<float *>(ws + 2 * mn),
-             reinterpret_cast<float *>(ws + 2 * mn + 128)};
-
-    F8_TRY_CUDA(launch_amax(dy, M * N, bw.amax_dy, *dev, st));
-    F8_TRY_CUDA(launch_cast_transpose(dy, M, N, bw.amax_dy, bw.scale_dy, dx ? bw.dy_q : nullptr,
-                                      dw ? bw.dy_t : nullptr, *dev, st));
+    const BwdWs bw = bwd_ws(workspace, M, N);
+    int np = 0;
+    F8_TRY_CUDA(launch_amax_partials(dy, M * N, bw.parts_dy, &np, *dev, st));
+    F8_TRY_CUDA(launch_cast_transpose(dy, M, N, nullptr, bw.parts_dy, np, bw.amax_dy, bw.scale_dy,
+                                      dx ? bw.dy_q : nullptr, dw ? bw.dy_t : nullptr, *dev, st));
     // dX [M,K] = q(dY) [M,N] . (q(W)^T [K,N])^T
     if (dx != nullptr)
         F8_TRY_CUDA(launch_gemm(bw.dy_q, saved->w_t, M, K, N, bw.scale_dy, saved->scale_w, dx, *dev, st));

@@ -7,7 +7,9 @@
 // numeric order, and inf/NaN sort above every finite value), reduces through
 // redux.sync within the warp and shared memory within the block, and folds
 // the block result into the output with one atomicMax on the fp32 bit
-// pattern (valid because the value is non-negative).
+// pattern (valid because the value is non-negative).  Inside a linear the
+// kernel instead writes one partial maximum per block (no output to zero
+// first) and the cast kernel reduces the partials in its prologue.
 //
 // cast_transpose: a CTA owns a 128 x 128 tile.  Phase 1 reads it with 16-byte
 // loads (each thread 16 consecutive bf16 of one row), scales in fp32,
@@ -20,6 +22,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "f8_internal.h"
 #include "f8_ptx.cuh"
@@ -39,24 +43,29 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t acc, uint4 v)
     return acc;
 }
 
-__global__ void __launch_bounds__(kAmaxThreads)
+template <bool kPartials>
+__global__ void __launch_bounds__(kAmaxThreads, 8)
 amax_kernel(const uint4 *__restrict__ x, int64_t nvec, const uint16_t *__restrict__ tail, int ntail,
             unsigned *__restrict__ out_bits, unsigned *__restrict__ status)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     uint32_t m2 = 0;
-    const int64_t S = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    for (; i + (kAmaxUnroll - 1) * S < nvec; i += kAmaxUnroll * S) {
+    const uint32_t S = gridDim.x * blockDim.x;  // grid <= 4096 x 256 threads
+    const uint4 *p = x + (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
+    const uint4 *const end = x + nvec;
+    while (p + (kAmaxUnroll - 1) * S < end) {
         uint4 v[kAmaxUnroll];
 #pragma unroll
         for (int u = 0; u < kAmaxUnroll; ++u)
-            v[u] = __ldg(x + i + u * S);
+            v[u] = __ldg(p + u * S);
 #pragma unroll
         for (int u = 0; u < kAmaxUnroll; ++u)
             m2 = max_u16x2(m2, v[u]);
+        p += kAmaxUnroll * S;
     }
-    for (; i < nvec; i += S)
-        m2 = max_u16x2(m2, __ldg(x + i));
+    for (; p < end; p += S)
+        m2 = max_u16x2(m2, __ldg(p));
     uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
     if (blockIdx.x == 0 && threadIdx.x < ntail)
         m = max(m, static_cast<uint32_t>(tail[threadIdx.x]) & 0x7FFFu);
@@ -73,7 +82,10 @@ amax_kernel(const uint4 *__restrict__ x, int64_t nvec, const uint16_t *__restric
         if (lane == 0) {
             if (m >= 0x7F80u)
                 atomicOr(status, kStatusNonfinite);
-            atomicMax(out_bits, m << 16);
+            if (kPartials)
+                out_bits[blockIdx.x] = m << 16;
+            else
+                atomicMax(out_bits, m << 16);
         }
     }
 }
@@ -81,10 +93,30 @@ amax_kernel(const uint4 *__restrict__ x, int64_t nvec, const uint16_t *__restric
 // ----------------------------------------------------------------- cast
 constexpr int kTile = 128;
 constexpr int kCastThreads = 256;
+constexpr int kCastThreadsMax = 256;
 
-__device__ __forceinline__ float scale_from_amax(const float *amax)
+__device__ __forceinline__ float scale_of(float amax)
 {
-    return __fdiv_rn(448.0f, fmaxf(__ldg(amax), 1e-12f));
+    return __fdiv_rn(448.0f, fmaxf(amax, 1e-12f));
+}
+
+// Maximum of the partial maxima (fp32 bit patterns of non-negative values),
+// reduced by the whole block; every thread gets the result.
+__device__ __forceinline__ float reduce_partials(const unsigned *partials, int n)
+{
+    __shared__ uint32_t red[kCastThreadsMax / 32];
+    uint32_t m = 0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+        m = max(m, partials[i]);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0)
+        red[warp] = m;
+    __syncthreads();
+    m = lane < static_cast<int>(blockDim.x >> 5) ? red[lane] : 0u;
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    __syncthreads();
+    return __uint_as_float(m);
 }
 
 __device__ __forceinline__ uint16_t cvt2(float lo, float hi)
@@ -117,13 +149,21 @@ __device__ __forceinline__ uint8_t cvt1(uint16_t b, float s)
 
 __global__ void __launch_bounds__(kCastThreads)
 cast_transpose_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
-                      const float *__restrict__ amax, float *__restrict__ scale_out,
+                      const float *__restrict__ amax, const unsigned *__restrict__ partials,
+                      int nparts, float *__restrict__ amax_out, float *__restrict__ scale_out,
                       uint8_t *__restrict__ q, uint8_t *__restrict__ qt, int vector_ok)
 {
     __shared__ __align__(16) uint8_t tile[kTile * kTile];
-    const float s = scale_from_amax(amax);
-    if (scale_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
-        *scale_out = s;
+    griddep_wait();
+    griddep_launch_dependents();
+    const float a = partials != nullptr ? reduce_partials(partials, nparts) : *amax;
+    const float s = scale_of(a);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (scale_out != nullptr)
+            *scale_out = s;
+        if (amax_out != nullptr)
+            *amax_out = a;
+    }
 
     const int64_t tiles_c = (cols + kTile - 1) / kTile;
     const int64_t tiles_r = (rows + kTile - 1) / kTile;
@@ -200,6 +240,44 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols
 
 } // namespace
 
+namespace {
+
+// Resident CTAs per SM of each kernel on each device (occupancy API, cached).
+struct Occupancy {
+    int amax_atomic = 0, amax_partials = 0, cast = 0;
+};
+std::mutex g_occ_mutex;
+Occupancy g_occ[64];
+
+const Occupancy &occupancy(const DeviceInfo &dev)
+{
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    Occupancy &o = g_occ[dev.ordinal & 63];
+    if (o.cast == 0) {
+        int n = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, amax_kernel<false>, kAmaxThreads, 0);
+        o.amax_atomic = n > 0 ? n : 1;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, amax_kernel<true>, kAmaxThreads, 0);
+        o.amax_partials = n > 0 ? n : 1;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cast_transpose_kernel, kCastThreads, 0);
+        o.cast = n > 0 ? n : 1;
+    }
+    return o;
+}
+
+int64_t amax_grid(int64_t nvec, int per_sm, const DeviceInfo &dev)
+{
+    int64_t blocks = (nvec + kAmaxThreads * kAmaxUnroll - 1) / (kAmaxThreads * kAmaxUnroll);
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * per_sm;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks > kMaxAmaxPartials)
+        blocks = kMaxAmaxPartials;
+    return blocks < 1 ? 1 : blocks;
+}
+
+} // namespace
+
 cudaError_t launch_amax(const void *x, int64_t n, float *amax_out, const DeviceInfo &dev,
                         cudaStream_t stream)
 {
@@ -209,33 +287,43 @@ cudaError_t launch_amax(const void *x, int64_t n, float *amax_out, const DeviceI
     const int64_t nvec = n / 8;
     const int ntail = static_cast<int>(n % 8);
     const uint16_t *tail = static_cast<const uint16_t *>(x) + nvec * 8;
-    int64_t blocks = (nvec + kAmaxThreads * kAmaxUnroll - 1) / (kAmaxThreads * kAmaxUnroll);
-    const int64_t max_blocks = static_cast<int64_t>(dev.sm_count) * (2048 / kAmaxThreads);
-    if (blocks > max_blocks)
-        blocks = max_blocks;
-    if (blocks < 1)
-        blocks = 1;
-    amax_kernel<<<static_cast<unsigned>(blocks), kAmaxThreads, 0, stream>>>(
+    const int64_t blocks = amax_grid(nvec, occupancy(dev).amax_atomic, dev);
+    // follows a memset, so it is launched without programmatic serialization
+    amax_kernel<false><<<static_cast<unsigned>(blocks), kAmaxThreads, 0, stream>>>(
         static_cast<const uint4 *>(x), nvec, tail, ntail, reinterpret_cast<unsigned *>(amax_out),
         dev.status);
     return cudaGetLastError();
 }
 
+cudaError_t launch_amax_partials(const void *x, int64_t n, unsigned *partials, int *nparts,
+                                 const DeviceInfo &dev, cudaStream_t stream)
+{
+    const int64_t nvec = n / 8;
+    const int ntail = static_cast<int>(n % 8);
+    const uint16_t *tail = static_cast<const uint16_t *>(x) + nvec * 8;
+    const int64_t blocks = amax_grid(nvec, occupancy(dev).amax_partials, dev);
+    *nparts = static_cast<int>(blocks);
+    return launch_pdl(amax_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(kAmaxThreads), 0,
+                      stream, static_cast<const uint4 *>(x), nvec, tail, ntail, partials,
+                      dev.status);
+}
+
 cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, const float *amax,
+                                  const unsigned *partials, int nparts, float *amax_out,
                                   float *scale_out, uint8_t *q, uint8_t *q_t,
                                   const DeviceInfo &dev, cudaStream_t stream)
 {
     const int64_t ntiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
     int64_t blocks = ntiles;
-    const int64_t max_blocks = static_cast<int64_t>(dev.sm_count) * (2048 / kCastThreads);
-    if (blocks > max_blocks)
-        blocks = max_blocks;
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * occupancy(dev).cast;
+    if (blocks > cap)
+        blocks = cap;
     if (blocks < 1)
         blocks = 1;
     const int vector_ok = (rows % 16 == 0) && (cols % 16 == 0);
-    cast_transpose_kernel<<<static_cast<unsigned>(blocks), kCastThreads, 0, stream>>>(
-        static_cast<const uint16_t *>(x), rows, cols, amax, scale_out, q, q_t, vector_ok);
-    return cudaGetLastError();
+    return launch_pdl(cast_transpose_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kCastThreads),
+                      0, stream, static_cast<const uint16_t *>(x), rows, cols, amax, partials, nparts,
+                      amax_out, scale_out, q, q_t, vector_ok);
 }
 
 } // namespace f8

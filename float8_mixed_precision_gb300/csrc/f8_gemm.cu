@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "f8_internal.h"
@@ -125,6 +126,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // everything above overlaps the previous kernel; operands and scales
+    // may come from it
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -214,8 +219,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
     } else {
         // ---------------------------------------------------- epilogue
         const int quad = warp & 3;  // the TMEM lane quarter this warp may read
-        const float inv = static_cast<float>(1.0 / (static_cast<double>(__ldg(sa)) *
-                                                     static_cast<double>(__ldg(sb))));
+        const float inv = static_cast<float>(1.0 / (static_cast<double>(*sa) *
+                                                     static_cast<double>(*sb)));
         const bool vec_ok = (N % 8) == 0;
         int local = 0;
         for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
@@ -270,6 +275,255 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------ CTA-pair kernel
+// The same pipeline over a cluster of two CTAs on neighbouring SMs, with
+// tcgen05.mma.cta_group::2: a 256 x BN tile per pair, each CTA loading its
+// own 128 rows of A and BN/2 rows of B, so every SM stages half the B tile
+// it would need alone.  The even CTA issues the MMAs; its full[s] barriers
+// count the TMA bytes of both CTAs; commits are multicast to the empty[s]
+// and tfull barriers of both CTAs; the epilogues of both CTAs arrive on the
+// even CTA's tempty barriers.
+template <int BN, int STAGES>
+struct PairCfg {
+    static constexpr int kABytes = 128 * kBK;
+    static constexpr int kBBytes = (BN / 2) * kBK;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kTmemCols = (2 * BN <= 256) ? 256 : 512;
+    static constexpr int kBarBytes = 8 * (2 * STAGES + 5) + 16;
+    static constexpr int kSmemBytes = STAGES * kStageBytes + kBarBytes + 1024;
+};
+
+template <int BN, int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                 __nv_bfloat16 *__restrict__ c, int M, int N, int K, const float *__restrict__ sa,
+                 const float *__restrict__ sb, unsigned *__restrict__ status, uint64_t limit_ns,
+                 int group_m)
+{
+    using Cfg = PairCfg<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *smA = smem;
+    uint8_t *smB = smem + STAGES * Cfg::kABytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::kStageBytes);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+    constexpr int kPM = 2 * kBM;  // rows of a pair tile
+    const int num_m = (M + kPM - 1) / kPM;
+    const int num_n = (N + BN - 1) / BN;
+    const int tiles = num_m * num_n;
+    const int num_kb = (K + kBK - 1) / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 8);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tma_a);
+        tma_prefetch_desc(&tma_b);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, Cfg::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    cluster_sync();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    griddep_wait();
+    griddep_launch_dependents();
+    const uint32_t full_leader = cluster_map(smem_addr(&full[0]), 0);
+    const uint32_t tempty_leader = cluster_map(smem_addr(&tempty[0]), 0);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // -------------------------------------------- TMA producer (both CTAs)
+            uint32_t stage = 0, phase = 0;
+            int64_t issued = 0;
+            bool stop = false;
+            for (int tile = pair; tile < tiles && !stop; tile += npairs) {
+                int mb, nb;
+                tile_coords(tile, num_m, num_n, group_m, mb, nb);
+                const int arow = mb * kPM + static_cast<int>(rank) * kBM;
+                const int brow = nb * BN + static_cast<int>(rank) * (BN / 2);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, limit_ns)) {
+                        note_timeout(abort_flag, status);
+                        stop = true;
+                        break;
+                    }
+                    if (leader)
+                        mbar_arrive_expect_tx(&full[stage], 2 * Cfg::kStageBytes);
+                    const uint32_t fb = full_leader + 8u * stage;
+                    tma_load_2d_pair(smA + stage * Cfg::kABytes, &tma_a, fb, kb * kBK, arow);
+                    tma_load_2d_pair(smB + stage * Cfg::kBBytes, &tma_b, fb, kb * kBK, brow);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!*abort_flag) {
+                // every stage this CTA filled must be released (its multicast
+                // arrivals landed) before the CTA may exit
+                for (int i = 0; i < STAGES; ++i) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, limit_ns)) {
+                        note_timeout(abort_flag, status);
+                        break;
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            } else if (leader) {
+                // copies of both CTAs still in flight land on these barriers
+                int64_t n = issued < STAGES ? issued : STAGES;
+                uint32_t s = stage, p = phase;
+                for (int64_t i = 0; i < n; ++i) {
+                    if (s == 0) {
+                        s = STAGES - 1;
+                        p ^= 1u;
+                    } else {
+                        --s;
+                    }
+                    mbar_wait(&full[s], p, nullptr, kDrainLimitNs);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (leader && lane == 0) {
+            // -------------------------------------------- MMA issuer (even CTA)
+            const uint32_t idesc = idesc_e4m3_f32(kPM, BN);
+            uint32_t stage = 0, phase = 0;
+            bool stop = false;
+            int local = 0;
+            for (int tile = pair; tile < tiles && !stop; tile += npairs, ++local) {
+                const uint32_t acc = local & 1;
+                const uint32_t aph = (local >> 1) & 1;
+                if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, limit_ns)) {
+                    note_timeout(abort_flag, status);
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d = tmem_base + acc * BN;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, limit_ns)) {
+                        note_timeout(abort_flag, status);
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(smA + stage * Cfg::kABytes));
+                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(smB + stage * Cfg::kBBytes));
+#pragma unroll
+                    for (int k = 0; k < kBK / 32; ++k)
+                        tc_mma_f8_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+                    tc_commit_pair_mc(&empty[stage], 0x3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (stop)
+                    break;
+                tc_commit_pair_mc(&tfull[acc], 0x3);
+            }
+            if (*abort_flag) {
+                tc_commit_pair(drain);
+                mbar_wait(drain, 0, nullptr, kDrainLimitNs);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- epilogue (both CTAs)
+        const int quad = warp & 3;
+        const float inv = static_cast<float>(1.0 / (static_cast<double>(*sa) *
+                                                     static_cast<double>(*sb)));
+        const bool vec_ok = (N % 8) == 0;
+        int local = 0;
+        for (int tile = pair; tile < tiles; tile += npairs, ++local) {
+            const uint32_t acc = local & 1;
+            const uint32_t aph = (local >> 1) & 1;
+            bool ok = mbar_wait(&tfull[acc], aph, abort_flag, limit_ns);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) {
+                if (lane == 0)
+                    note_timeout(abort_flag, status);
+                break;
+            }
+            tc_fence_after_sync();
+            int mb, nb;
+            tile_coords(tile, num_m, num_n, group_m, mb, nb);
+            const int row = mb * kPM + static_cast<int>(rank) * kBM + quad * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int j = 0; j < BN / 32; ++j) {
+                uint32_t r[32];
+                tc_ld_32x32b_x32(taddr + j * 32, r);
+                tc_wait_ld();
+                const int col0 = nb * BN + j * 32;
+                if (row < M) {
+                    __nv_bfloat16 *dst = c + static_cast<int64_t>(row) * N + col0;
+                    if (vec_ok && col0 + 32 <= N) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 o;
+                            o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
+                            o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
+                            o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
+                            o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
+                            *reinterpret_cast<uint4 *>(dst + 8 * v) = o;
+                        }
+                    } else {
+                        for (int e = 0; e < 32; ++e)
+                            if (col0 + e < N)
+                                dst[e] = __float2bfloat16_rn(__uint_as_float(r[e]) * inv);
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(&tempty[acc]);
+                else
+                    mbar_arrive_remote(tempty_leader + 8u * acc);
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
     }
 }
 
@@ -333,10 +587,58 @@ cudaError_t run_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, i
     const int64_t tiles = num_m * num_n;
     const int grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
     const int group_m = 16;
-    gemm_kernel<BN, STAGES><<<grid, kThreads, Cfg::kSmemBytes, stream>>>(
-        ma, mb, static_cast<__nv_bfloat16 *>(c), static_cast<int>(M), static_cast<int>(N),
-        static_cast<int>(K), sa, sb, dev.status, wait_limit_ns(), group_m);
-    return cudaGetLastError();
+    return launch_pdl(gemm_kernel<BN, STAGES>, dim3(grid), dim3(kThreads), Cfg::kSmemBytes, stream,
+                      ma, mb, static_cast<__nv_bfloat16 *>(c), static_cast<int>(M),
+                      static_cast<int>(N), static_cast<int>(K), sa, sb, dev.status,
+                      wait_limit_ns(), group_m);
+}
+
+template <int BN, int STAGES>
+cudaError_t run_pair(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
+                     const float *sa, const float *sb, void *c, const DeviceInfo &dev,
+                     cudaStream_t stream)
+{
+    using Cfg = PairCfg<BN, STAGES>;
+    CUtensorMap ma, mb;
+    if (!make_kmajor_map(&ma, a, M, K, kBM) || !make_kmajor_map(&mb, b, N, K, BN / 2))
+        return cudaErrorNotSupported;
+    static std::once_flag attr_once[64];
+    static cudaError_t attr_err[64];
+    const int dv = dev.ordinal & 63;
+    std::call_once(attr_once[dv], [&] {
+        attr_err[dv] = cudaFuncSetAttribute(gemm_pair_kernel<BN, STAGES>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            Cfg::kSmemBytes);
+    });
+    if (attr_err[dv] != cudaSuccess)
+        return attr_err[dv];
+    const int64_t num_m = (M + 2 * kBM - 1) / (2 * kBM), num_n = (N + BN - 1) / BN;
+    const int64_t tiles = num_m * num_n;
+    const int64_t max_pairs = dev.sm_count / 2;
+    const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
+    const int group_m = 8;
+    return launch_pdl(gemm_pair_kernel<BN, STAGES>, dim3(2 * pairs), dim3(kThreads),
+                      Cfg::kSmemBytes, stream, ma, mb, static_cast<__nv_bfloat16 *>(c),
+                      static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), sa, sb,
+                      dev.status, wait_limit_ns(), group_m);
+}
+
+constexpr int kVariantSingle = 1;
+constexpr int kVariantPair = 2;
+
+// Kernel choice: the CTA-pair kernel for every shape with at least two
+// 128-row blocks; F8_GEMM_VARIANT=1|2 forces one kernel (for measurement).
+int gemm_variant(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev)
+{
+    (void)N;
+    (void)K;
+    const char *e = std::getenv("F8_GEMM_VARIANT");
+    const int forced = e ? std::atoi(e) : 0;
+    if (forced == kVariantSingle || forced == kVariantPair)
+        return forced;
+    if (dev.sm_count < 2 || M < 2 * kBM)
+        return kVariantSingle;
+    return kVariantPair;
 }
 
 __global__ void wait_selftest_kernel(unsigned *status, uint64_t limit_ns)
@@ -357,7 +659,12 @@ cudaError_t launch_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N
                         const float *sa, const float *sb, void *c, const DeviceInfo &dev,
                         cudaStream_t stream)
 {
-    return run_gemm<256, 4>(a, b, M, N, K, sa, sb, c, dev, stream);
+    switch (gemm_variant(M, N, K, dev)) {
+    case kVariantPair:
+        return run_pair<256, 6>(a, b, M, N, K, sa, sb, c, dev, stream);
+    default:
+        return run_gemm<256, 4>(a, b, M, N, K, sa, sb, c, dev, stream);
+    }
 }
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, const DeviceInfo &dev, cudaStream_t stream)

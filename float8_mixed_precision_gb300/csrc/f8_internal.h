@@ -3,7 +3,9 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cstdlib>
 #include <cuda_runtime.h>
+#include <utility>
 
 namespace f8 {
 
@@ -22,12 +24,52 @@ const DeviceInfo *device_info();
 // Time limit of the GEMM pipeline's device waits.
 uint64_t wait_limit_ns();
 
-// amax over n bf16 values; n >= 1, x 16-byte aligned.
+// Programmatic dependent launch is on unless F8_PDL=0.
+inline bool pdl_enabled()
+{
+    const char *e = std::getenv("F8_PDL");
+    return e == nullptr || e[0] != '0';
+}
+
+// Launch with programmatic stream serialization, so the kernel's prologue
+// may overlap the tail of the previous kernel in the stream.  Every kernel
+// launched this way calls griddep_wait() before reading dependent data.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Most partial maxima one amax launch writes (its largest grid).
+constexpr int kMaxAmaxPartials = 4096;
+
+// amax over n bf16 values into one fp32 (zeroed here, then atomicMax);
+// n >= 1, x 16-byte aligned.
 cudaError_t launch_amax(const void *x, int64_t n, float *amax_out, const DeviceInfo &dev,
                         cudaStream_t stream);
 
-// Scale + cast + (optional) transpose of a [rows, cols] bf16 tensor.
+// amax over n bf16 values as per-block partial maxima (fp32 bit patterns),
+// no zeroing needed; *nparts receives the number written (<= kMaxAmaxPartials).
+cudaError_t launch_amax_partials(const void *x, int64_t n, unsigned *partials, int *nparts,
+                                 const DeviceInfo &dev, cudaStream_t stream);
+
+// Scale + cast + (optional) transpose of a [rows, cols] bf16 tensor.  The
+// amax comes either from `amax` (one fp32) or, if `partials` is non-null,
+// from the maximum of `nparts` partial maxima, which is then also stored to
+// `amax_out` (if non-null).
 cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, const float *amax,
+                                  const unsigned *partials, int nparts, float *amax_out,
                                   float *scale_out, uint8_t *q, uint8_t *q_t,
                                   const DeviceInfo &dev, cudaStream_t stream);
 
