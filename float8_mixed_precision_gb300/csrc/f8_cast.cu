@@ -1,8 +1,8 @@
 // amax reduction and fused scale + cast + transpose (bf16 -> E4M3), the two
 // HBM-bound steps of dynamic tensorwise scaling.
 //
-// amax: every thread streams 16-byte vectors of 8 bf16 values with four
-// independent loads in flight, keeps the maximum of the magnitude bits
+// amax: every thread streams 16-byte vectors of 8 bf16 values with eight
+// independent (predicated) loads in flight, also in the last round, keeps the maximum of the magnitude bits
 // (bits & 0x7FFF: for non-negative IEEE values the integer order is the
 // numeric order, and inf/NaN sort above every finite value), reduces through
 // redux.sync within the warp and shared memory within the block, and folds
@@ -32,7 +32,7 @@ namespace f8 {
 namespace {
 
 constexpr int kAmaxThreads = 256;
-constexpr int kAmaxUnroll = 4;
+constexpr int kAmaxUnroll = 8;
 
 __device__ __forceinline__ uint32_t max_u16x2(uint32_t acc, uint4 v)
 {
@@ -44,28 +44,26 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t acc, uint4 v)
 }
 
 template <bool kPartials>
-__global__ void __launch_bounds__(kAmaxThreads, 8)
+__global__ void __launch_bounds__(kAmaxThreads, 4)
 amax_kernel(const uint4 *__restrict__ x, int64_t nvec, const uint16_t *__restrict__ tail, int ntail,
             unsigned *__restrict__ out_bits, unsigned *__restrict__ status)
 {
     griddep_wait();
     griddep_launch_dependents();
     uint32_t m2 = 0;
-    const uint32_t S = gridDim.x * blockDim.x;  // grid <= 4096 x 256 threads
-    const uint4 *p = x + (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
-    const uint4 *const end = x + nvec;
-    while (p + (kAmaxUnroll - 1) * S < end) {
+    const int64_t S = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < nvec;
+         base += kAmaxUnroll * S) {
         uint4 v[kAmaxUnroll];
 #pragma unroll
-        for (int u = 0; u < kAmaxUnroll; ++u)
-            v[u] = __ldg(p + u * S);
+        for (int u = 0; u < kAmaxUnroll; ++u) {
+            const int64_t i = base + u * S;
+            v[u] = i < nvec ? __ldg(x + i) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
         for (int u = 0; u < kAmaxUnroll; ++u)
             m2 = max_u16x2(m2, v[u]);
-        p += kAmaxUnroll * S;
     }
-    for (; p < end; p += S)
-        m2 = max_u16x2(m2, __ldg(p));
     uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
     if (blockIdx.x == 0 && threadIdx.x < ntail)
         m = max(m, static_cast<uint32_t>(tail[threadIdx.x]) & 0x7FFFu);

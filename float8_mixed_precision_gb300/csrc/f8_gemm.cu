@@ -1,26 +1,38 @@
 // E4M3 x E4M3 -> fp32 -> bf16 GEMM on the 5th-generation tensor cores:
 // C[M,N] = bf16( A[M,K] B[N,K]^T * 1/(sa sb) ), both operands K-major.
 //
-// One persistent CTA per SM (192 threads, warp-specialised):
-//   warp 0      TMA producer: 128 x 128-byte A tiles and BN x 128-byte B tiles
-//               (128-byte swizzle) into a STAGES-deep shared-memory ring,
-//               completion counted in transaction bytes on full[s];
+// Persistent, warp-specialised, 192 threads per CTA, one CTA per SM:
+//   warp 0      TMA producer: A and B tiles of 128 bytes of K (128-byte
+//               swizzle) into a STAGES-deep shared-memory ring; completion
+//               is counted in transaction bytes on full[s];
 //   warp 1      TMEM allocator and MMA issuer: 4 tcgen05.mma kind::f8f6f4
-//               (128 x BN x 32) per stage into one of two TMEM accumulators;
+//               (K = 32 each) per stage into one of two TMEM accumulators;
 //               tcgen05.commit releases the stage (empty[s]) and, after the
-//               last K block, hands the accumulator to the epilogue (tfull);
-//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns, multiply by
-//               fl32(1/(sa sb)), round to bf16, store; then release the
-//               accumulator (tempty) so the MMA of tile i+1 overlaps the
-//               epilogue of tile i.
+//               last K block of a tile, hands the accumulator to the
+//               epilogue (tfull[a]);
+//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 64 columns, x fl32(1/(sa sb)),
+//               round to bf16, stage 32 rows x 128 bytes in swizzled shared
+//               memory and write it with one TMA tensor store; the
+//               accumulator is released (tempty[a]) as soon as it has been
+//               read, so the MMAs of tile i+1 overlap the epilogue of tile i.
+// Two shapes of the same kernel:
+//   PAIR = false  one CTA computes a 128 x BN tile (tcgen05 cta_group::1);
+//   PAIR = true   a cluster of two CTAs on neighbouring SMs computes a
+//                 256 x BN tile with cta_group::2: each CTA loads its own
+//                 128 rows of A and BN/2 rows of B, so each SM stages half
+//                 the B tile it would need alone.  The even CTA issues the
+//                 MMAs; its full[s] barriers count the bytes of both CTAs;
+//                 commits are multicast to the barriers of both CTAs; both
+//                 epilogues arrive on the even CTA's tempty barriers.
 // Tiles are visited in groups of `group_m` M-blocks so that concurrently
-// running CTAs share A and B tiles in L2.  Partial tiles at the M, N and K
-// edges are zero-filled by TMA and masked in the epilogue.
+// running CTAs share operand tiles in L2.  M, N and K edges are zero-filled
+// by TMA loads and clipped by TMA stores (or masked on the direct-store path
+// used when a C row is not a multiple of 16 bytes).
 //
 // Every wait is bounded (global-timer limit).  A wait that gives up sets a
-// CTA-wide abort flag and the device status word; the other roles leave
-// their loops, the producer waits for its own copies in flight, the MMA
-// thread waits for its own MMAs, and TMEM is released before the CTA exits.
+// CTA-wide abort flag and the device status word; the roles leave their
+// loops, the producer waits for copies still in flight, the MMA thread for
+// its own MMAs, and TMEM is released before the CTA exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -34,19 +46,27 @@
 namespace f8 {
 namespace {
 
-constexpr int kBM = 128;
-constexpr int kBK = 128;  // bytes of K per stage = one 128-byte swizzle row
+constexpr int kBM = 128;   // accumulator rows per CTA (TMEM lanes)
+constexpr int kBK = 128;   // bytes of K per stage = one 128-byte swizzle row
 constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kEpiCols = 64;                       // columns per epilogue step
+constexpr int kEpiBufBytes = 32 * kEpiCols * 2;    // 32 rows x 128 bytes
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
-template <int BN, int STAGES>
-struct GemmCfg {
+template <int BN, int STAGES, bool PAIR>
+struct Cfg {
+    static constexpr int kTileM = PAIR ? 2 * kBM : kBM;
+    static constexpr int kBRows = PAIR ? BN / 2 : BN;  // rows of B each CTA loads
     static constexpr int kABytes = kBM * kBK;
-    static constexpr int kBBytes = BN * kBK;
+    static constexpr int kBBytes = kBRows * kBK;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = (2 * BN <= 256) ? 256 : 512;
+    static constexpr int kStagingBytes = kEpiWarps * 2 * kEpiBufBytes;
     static constexpr int kBarBytes = 8 * (2 * STAGES + 5) + 16;
-    static constexpr int kSmemBytes = STAGES * kStageBytes + kBarBytes + 1024;
+    static constexpr int kSmemBytes = STAGES * kStageBytes + kStagingBytes + kBarBytes + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(BN % kEpiCols == 0, "epilogue steps");
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group_m, int &mb,
@@ -73,20 +93,83 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <int BN, int STAGES>
+__device__ __forceinline__ uint4 pack8(const uint32_t *r, float inv)
+{
+    uint4 o;
+    o.x = pack_bf16x2(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
+    o.y = pack_bf16x2(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
+    o.z = pack_bf16x2(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
+    o.w = pack_bf16x2(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
+    return o;
+}
+
+// One warp's share of an accumulator: TMEM lanes [32q, 32q + 32) x BN
+// columns starting at `taddr`, i.e. C rows row0 .. row0 + 31 and columns
+// col_base .. col_base + BN - 1.
+template <int BN>
+__device__ __forceinline__ void epilogue_rows(uint32_t taddr, int row0, int col_base, int M, int N,
+                                              float inv, __nv_bfloat16 *__restrict__ c,
+                                              const CUtensorMap *tma_c, bool tma_store,
+                                              uint8_t *stage, uint32_t &buf, int lane)
+{
+#pragma unroll 1
+    for (int j = 0; j < BN / kEpiCols; ++j) {
+        uint32_t r[kEpiCols];
+        tc_ld_32x32b_x32(taddr + j * kEpiCols, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tc_ld_32x32b_x32(taddr + j * kEpiCols + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tc_wait_ld();
+        const int col0 = col_base + j * kEpiCols;
+        if (tma_store) {
+            uint8_t *b = stage + buf * kEpiBufBytes;
+            if (lane == 0)
+                bulk_wait_group_read<1>();  // the store issued from b two steps ago has read it
+            __syncwarp();
+            // row `lane` of the box, 16-byte chunk q at (q ^ row % 8): the 128-byte swizzle
+#pragma unroll
+            for (int q = 0; q < kEpiCols / 8; ++q)
+                *reinterpret_cast<uint4 *>(b + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+                    pack8(&r[8 * q], inv);
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0 && row0 < M && col0 < N) {
+                tma_store_2d(tma_c, b, col0, row0);
+                bulk_commit_group();
+            }
+            buf ^= 1u;
+        } else {
+            const int row = row0 + lane;
+            if (row < M) {
+                __nv_bfloat16 *dst = c + static_cast<int64_t>(row) * N + col0;
+                const bool vec = (N % 8) == 0 && col0 + kEpiCols <= N;
+                if (vec) {
+#pragma unroll
+                    for (int q = 0; q < kEpiCols / 8; ++q)
+                        *reinterpret_cast<uint4 *>(dst + 8 * q) = pack8(&r[8 * q], inv);
+                } else {
+                    for (int e = 0; e < kEpiCols; ++e)
+                        if (col0 + e < N)
+                            dst[e] = __float2bfloat16_rn(__uint_as_float(r[e]) * inv);
+                }
+            }
+        }
+    }
+}
+
+template <int BN, int STAGES, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-            __nv_bfloat16 *__restrict__ c, int M, int N, int K, const float *__restrict__ sa,
-            const float *__restrict__ sb, unsigned *__restrict__ status, uint64_t limit_ns,
-            int group_m)
+            const __grid_constant__ CUtensorMap tma_c, __nv_bfloat16 *__restrict__ c, int M, int N,
+            int K, const float *__restrict__ sa, const float *__restrict__ sb,
+            unsigned *__restrict__ status, uint64_t limit_ns, int group_m, int tma_store)
 {
-    using Cfg = GemmCfg<BN, STAGES>;
+    using C = Cfg<BN, STAGES, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *smA = smem;
-    uint8_t *smB = smem + STAGES * Cfg::kABytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::kStageBytes);
+    uint8_t *smB = smem + STAGES * C::kABytes;
+    uint8_t *staging = smem + STAGES * C::kStageBytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(staging + C::kStagingBytes);
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
@@ -96,7 +179,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int num_m = (M + kBM - 1) / kBM;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int nunits = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const int num_m = (M + C::kTileM - 1) / C::kTileM;
     const int num_n = (N + BN - 1) / BN;
     const int tiles = num_m * num_n;
     const int num_kb = (K + kBK - 1) / kBK;
@@ -108,7 +195,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 4);
+            mbar_init(&tempty[a], PAIR ? 2 * kEpiWarps : kEpiWarps);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -117,270 +204,61 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tma_a);
         tma_prefetch_desc(&tma_b);
+        if (tma_store)
+            tma_prefetch_desc(&tma_c);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, Cfg::kTmemCols);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(tmem_slot, C::kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, C::kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if (PAIR)
+        cluster_sync();
+    else
+        __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    // everything above overlaps the previous kernel; operands and scales
-    // may come from it
+    // everything above overlaps the previous kernel in the stream; the
+    // operands and scales may come from it
     griddep_wait();
     griddep_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
+            const uint32_t full_leader = PAIR ? cluster_map(smem_addr(&full[0]), 0) : 0u;
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
             bool stop = false;
-            for (int tile = blockIdx.x; tile < tiles && !stop; tile += gridDim.x) {
+            for (int tile = unit; tile < tiles && !stop; tile += nunits) {
                 int mb, nb;
                 tile_coords(tile, num_m, num_n, group_m, mb, nb);
+                const int arow = mb * C::kTileM + static_cast<int>(rank) * kBM;
+                const int brow = nb * BN + static_cast<int>(rank) * C::kBRows;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, limit_ns)) {
                         note_timeout(abort_flag, status);
                         stop = true;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
-                    tma_load_2d(smA + stage * Cfg::kABytes, &tma_a, &full[stage], kb * kBK, mb * kBM);
-                    tma_load_2d(smB + stage * Cfg::kBBytes, &tma_b, &full[stage], kb * kBK, nb * BN);
-                    ++issued;
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            if (*abort_flag) {
-                // wait for this CTA's copies still in flight before it exits
-                int64_t n = issued < STAGES ? issued : STAGES;
-                uint32_t s = stage, p = phase;
-                for (int64_t i = 0; i < n; ++i) {
-                    if (s == 0) {
-                        s = STAGES - 1;
-                        p ^= 1u;
+                    uint8_t *sa_dst = smA + stage * C::kABytes;
+                    uint8_t *sb_dst = smB + stage * C::kBBytes;
+                    if (PAIR) {
+                        if (leader)
+                            mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
+                        const uint32_t fb = full_leader + 8u * stage;
+                        tma_load_2d_pair(sa_dst, &tma_a, fb, kb * kBK, arow);
+                        tma_load_2d_pair(sb_dst, &tma_b, fb, kb * kBK, brow);
                     } else {
-                        --s;
+                        mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+                        tma_load_2d(sa_dst, &tma_a, &full[stage], kb * kBK, arow);
+                        tma_load_2d(sb_dst, &tma_b, &full[stage], kb * kBK, brow);
                     }
-                    mbar_wait(&full[s], p, nullptr, kDrainLimitNs);
-                }
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            const uint32_t idesc = idesc_e4m3_f32(kBM, BN);
-            uint32_t stage = 0, phase = 0;
-            bool stop = false;
-            int local = 0;
-            for (int tile = blockIdx.x; tile < tiles && !stop; tile += gridDim.x, ++local) {
-                const uint32_t acc = local & 1;
-                const uint32_t aph = (local >> 1) & 1;
-                if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, limit_ns)) {
-                    note_timeout(abort_flag, status);
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint32_t d = tmem_base + acc * BN;
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, limit_ns)) {
-                        note_timeout(abort_flag, status);
-                        stop = true;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(smA + stage * Cfg::kABytes));
-                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(smB + stage * Cfg::kBBytes));
-#pragma unroll
-                    for (int k = 0; k < kBK / 32; ++k)
-                        tc_mma_f8(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
-                    tc_commit(&empty[stage]);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (stop)
-                    break;
-                tc_commit(&tfull[acc]);
-            }
-            if (*abort_flag) {
-                tc_commit(drain);
-                mbar_wait(drain, 0, nullptr, kDrainLimitNs);
-            }
-        }
-        __syncwarp();
-    } else {
-        // ---------------------------------------------------- epilogue
-        const int quad = warp & 3;  // the TMEM lane quarter this warp may read
-        const float inv = static_cast<float>(1.0 / (static_cast<double>(*sa) *
-                                                     static_cast<double>(*sb)));
-        const bool vec_ok = (N % 8) == 0;
-        int local = 0;
-        for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
-            const uint32_t acc = local & 1;
-            const uint32_t aph = (local >> 1) & 1;
-            bool ok = mbar_wait(&tfull[acc], aph, abort_flag, limit_ns);
-            ok = __all_sync(0xFFFFFFFFu, ok);
-            if (!ok) {
-                if (lane == 0)
-                    note_timeout(abort_flag, status);
-                break;
-            }
-            tc_fence_after_sync();
-            int mb, nb;
-            tile_coords(tile, num_m, num_n, group_m, mb, nb);
-            const int row = mb * kBM + quad * 32 + lane;
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
-#pragma unroll 1
-            for (int j = 0; j < BN / 32; ++j) {
-                uint32_t r[32];
-                tc_ld_32x32b_x32(taddr + j * 32, r);
-                tc_wait_ld();
-                const int col0 = nb * BN + j * 32;
-                if (row < M) {
-                    __nv_bfloat16 *dst = c + static_cast<int64_t>(row) * N + col0;
-                    if (vec_ok && col0 + 32 <= N) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 o;
-                            o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
-                            o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
-                            o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
-                            o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
-                            *reinterpret_cast<uint4 *>(dst + 8 * v) = o;
-                        }
-                    } else {
-                        for (int e = 0; e < 32; ++e)
-                            if (col0 + e < N)
-                                dst[e] = __float2bfloat16_rn(__uint_as_float(r[e]) * inv);
-                    }
-                }
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&tempty[acc]);
-        }
-    }
-
-    tc_fence_before_sync();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after_sync();
-        tmem_dealloc(tmem_base, Cfg::kTmemCols);
-    }
-}
-
-// ------------------------------------------------------------ CTA-pair kernel
-// The same pipeline over a cluster of two CTAs on neighbouring SMs, with
-// tcgen05.mma.cta_group::2: a 256 x BN tile per pair, each CTA loading its
-// own 128 rows of A and BN/2 rows of B, so every SM stages half the B tile
-// it would need alone.  The even CTA issues the MMAs; its full[s] barriers
-// count the TMA bytes of both CTAs; commits are multicast to the empty[s]
-// and tfull barriers of both CTAs; the epilogues of both CTAs arrive on the
-// even CTA's tempty barriers.
-template <int BN, int STAGES>
-struct PairCfg {
-    static constexpr int kABytes = 128 * kBK;
-    static constexpr int kBBytes = (BN / 2) * kBK;
-    static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kTmemCols = (2 * BN <= 256) ? 256 : 512;
-    static constexpr int kBarBytes = 8 * (2 * STAGES + 5) + 16;
-    static constexpr int kSmemBytes = STAGES * kStageBytes + kBarBytes + 1024;
-};
-
-template <int BN, int STAGES>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-                 __nv_bfloat16 *__restrict__ c, int M, int N, int K, const float *__restrict__ sa,
-                 const float *__restrict__ sb, unsigned *__restrict__ status, uint64_t limit_ns,
-                 int group_m)
-{
-    using Cfg = PairCfg<BN, STAGES>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
-    uint8_t *smA = smem;
-    uint8_t *smB = smem + STAGES * Cfg::kABytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::kStageBytes);
-    uint64_t *empty = full + STAGES;
-    uint64_t *tfull = empty + STAGES;
-    uint64_t *tempty = tfull + 2;
-    uint64_t *drain = tempty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const bool leader = rank == 0;
-    const int pair = blockIdx.x >> 1;
-    const int npairs = gridDim.x >> 1;
-    constexpr int kPM = 2 * kBM;  // rows of a pair tile
-    const int num_m = (M + kPM - 1) / kPM;
-    const int num_n = (N + BN - 1) / BN;
-    const int tiles = num_m * num_n;
-    const int num_kb = (K + kBK - 1) / kBK;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 8);
-        }
-        mbar_init(drain, 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tma_a);
-        tma_prefetch_desc(&tma_b);
-    }
-    if (warp == 1) {
-        tmem_alloc_pair(tmem_slot, Cfg::kTmemCols);
-        tmem_relinquish_pair();
-    }
-    tc_fence_before_sync();
-    cluster_sync();
-    tc_fence_after_sync();
-    const uint32_t tmem_base = *tmem_slot;
-    griddep_wait();
-    griddep_launch_dependents();
-    const uint32_t full_leader = cluster_map(smem_addr(&full[0]), 0);
-    const uint32_t tempty_leader = cluster_map(smem_addr(&tempty[0]), 0);
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // -------------------------------------------- TMA producer (both CTAs)
-            uint32_t stage = 0, phase = 0;
-            int64_t issued = 0;
-            bool stop = false;
-            for (int tile = pair; tile < tiles && !stop; tile += npairs) {
-                int mb, nb;
-                tile_coords(tile, num_m, num_n, group_m, mb, nb);
-                const int arow = mb * kPM + static_cast<int>(rank) * kBM;
-                const int brow = nb * BN + static_cast<int>(rank) * (BN / 2);
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, limit_ns)) {
-                        note_timeout(abort_flag, status);
-                        stop = true;
-                        break;
-                    }
-                    if (leader)
-                        mbar_arrive_expect_tx(&full[stage], 2 * Cfg::kStageBytes);
-                    const uint32_t fb = full_leader + 8u * stage;
-                    tma_load_2d_pair(smA + stage * Cfg::kABytes, &tma_a, fb, kb * kBK, arow);
-                    tma_load_2d_pair(smB + stage * Cfg::kBBytes, &tma_b, fb, kb * kBK, brow);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -389,8 +267,8 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
                 }
             }
             if (!*abort_flag) {
-                // every stage this CTA filled must be released (its multicast
-                // arrivals landed) before the CTA may exit
+                // every stage filled must be released (its commit arrivals
+                // have landed here) before the CTA may exit
                 for (int i = 0; i < STAGES; ++i) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, limit_ns)) {
                         note_timeout(abort_flag, status);
@@ -402,7 +280,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
                     }
                 }
             } else if (leader) {
-                // copies of both CTAs still in flight land on these barriers
+                // copies still in flight land on these barriers
                 int64_t n = issued < STAGES ? issued : STAGES;
                 uint32_t s = stage, p = phase;
                 for (int64_t i = 0; i < n; ++i) {
@@ -419,12 +297,12 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
         __syncwarp();
     } else if (warp == 1) {
         if (leader && lane == 0) {
-            // -------------------------------------------- MMA issuer (even CTA)
-            const uint32_t idesc = idesc_e4m3_f32(kPM, BN);
+            // ------------------------------------------------ MMA issuer
+            const uint32_t idesc = idesc_e4m3_f32(C::kTileM, BN);
             uint32_t stage = 0, phase = 0;
             bool stop = false;
             int local = 0;
-            for (int tile = pair; tile < tiles && !stop; tile += npairs, ++local) {
+            for (int tile = unit; tile < tiles && !stop; tile += nunits, ++local) {
                 const uint32_t acc = local & 1;
                 const uint32_t aph = (local >> 1) & 1;
                 if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, limit_ns)) {
@@ -440,12 +318,19 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(smA + stage * Cfg::kABytes));
-                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(smB + stage * Cfg::kBBytes));
+                    const uint64_t adesc = sdesc_kmajor_sw128(smem_addr(smA + stage * C::kABytes));
+                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_addr(smB + stage * C::kBBytes));
 #pragma unroll
-                    for (int k = 0; k < kBK / 32; ++k)
-                        tc_mma_f8_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
-                    tc_commit_pair_mc(&empty[stage], 0x3);
+                    for (int k = 0; k < kBK / 32; ++k) {
+                        if (PAIR)
+                            tc_mma_f8_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+                        else
+                            tc_mma_f8(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+                    }
+                    if (PAIR)
+                        tc_commit_pair_mc(&empty[stage], 0x3);
+                    else
+                        tc_commit(&empty[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -453,22 +338,30 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
                 }
                 if (stop)
                     break;
-                tc_commit_pair_mc(&tfull[acc], 0x3);
+                if (PAIR)
+                    tc_commit_pair_mc(&tfull[acc], 0x3);
+                else
+                    tc_commit(&tfull[acc]);
             }
             if (*abort_flag) {
-                tc_commit_pair(drain);
+                if (PAIR)
+                    tc_commit_pair(drain);
+                else
+                    tc_commit(drain);
                 mbar_wait(drain, 0, nullptr, kDrainLimitNs);
             }
         }
         __syncwarp();
     } else {
-        // ---------------------------------------------------- epilogue (both CTAs)
-        const int quad = warp & 3;
+        // ---------------------------------------------------- epilogue
+        const int quad = warp & 3;  // the TMEM lane quarter this warp may read
         const float inv = static_cast<float>(1.0 / (static_cast<double>(*sa) *
                                                      static_cast<double>(*sb)));
-        const bool vec_ok = (N % 8) == 0;
+        uint8_t *my_stage = staging + (warp - 2) * 2 * kEpiBufBytes;
+        const uint32_t tempty_leader = PAIR ? cluster_map(smem_addr(&tempty[0]), 0) : 0u;
+        uint32_t buf = 0;
         int local = 0;
-        for (int tile = pair; tile < tiles; tile += npairs, ++local) {
+        for (int tile = unit; tile < tiles; tile += nunits, ++local) {
             const uint32_t acc = local & 1;
             const uint32_t aph = (local >> 1) & 1;
             bool ok = mbar_wait(&tfull[acc], aph, abort_flag, limit_ns);
@@ -481,50 +374,48 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
             tc_fence_after_sync();
             int mb, nb;
             tile_coords(tile, num_m, num_n, group_m, mb, nb);
-            const int row = mb * kPM + static_cast<int>(rank) * kBM + quad * 32 + lane;
+            const int row0 = mb * C::kTileM + static_cast<int>(rank) * kBM + quad * 32;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
-#pragma unroll 1
-            for (int j = 0; j < BN / 32; ++j) {
-                uint32_t r[32];
-                tc_ld_32x32b_x32(taddr + j * 32, r);
-                tc_wait_ld();
-                const int col0 = nb * BN + j * 32;
-                if (row < M) {
-                    __nv_bfloat16 *dst = c + static_cast<int64_t>(row) * N + col0;
-                    if (vec_ok && col0 + 32 <= N) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 o;
-                            o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
-                            o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
-                            o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
-                            o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
-                            *reinterpret_cast<uint4 *>(dst + 8 * v) = o;
-                        }
-                    } else {
-                        for (int e = 0; e < 32; ++e)
-                            if (col0 + e < N)
-                                dst[e] = __float2bfloat16_rn(__uint_as_float(r[e]) * inv);
-                    }
-                }
-            }
+            epilogue_rows<BN>(taddr, row0, nb * BN, M, N, inv, c, &tma_c, tma_store != 0, my_stage,
+                              buf, lane);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
-                if (leader)
+                if (!PAIR || leader)
                     mbar_arrive(&tempty[acc]);
                 else
                     mbar_arrive_remote(tempty_leader + 8u * acc);
             }
         }
+        if (lane == 0)
+            bulk_wait_group_all();
+        __syncwarp();
     }
 
     tc_fence_before_sync();
-    cluster_sync();
+    if (PAIR)
+        cluster_sync();
+    else
+        __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, C::kTmemCols);
+        else
+            tmem_dealloc(tmem_base, C::kTmemCols);
     }
+}
+
+__global__ void wait_selftest_kernel(unsigned *status, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, nullptr, limit_ns))
+        atomicOr(status, kStatusTimeout);
 }
 
 // ------------------------------------------------------------ host side
@@ -548,79 +439,58 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// K-major E4M3 matrix [rows, K] as a 2-D tensor map with a 128 x box_rows box.
-bool make_kmajor_map(CUtensorMap *map, const uint8_t *ptr, int64_t rows, int64_t K, int box_rows)
+// 2-D row-major tensor [rows, cols] of `esize`-byte elements with a
+// box_cols x box_rows box and the 128-byte swizzle (box_cols * esize == 128).
+bool make_map(CUtensorMap *map, CUtensorMapDataType dtype, int esize, const void *ptr,
+              int64_t rows, int64_t cols, int box_cols, int box_rows)
 {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr)
         return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * esize)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(ptr), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = enc(map, dtype, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool PAIR>
 cudaError_t run_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
                      const float *sa, const float *sb, void *c, const DeviceInfo &dev,
                      cudaStream_t stream)
 {
-    using Cfg = GemmCfg<BN, STAGES>;
-    CUtensorMap ma, mb;
-    if (!make_kmajor_map(&ma, a, M, K, kBM) || !make_kmajor_map(&mb, b, N, K, BN))
+    using C = Cfg<BN, STAGES, PAIR>;
+    CUtensorMap ma, mb, mc;
+    if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a, M, K, kBK, kBM) ||
+        !make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, N, K, kBK, C::kBRows))
         return cudaErrorNotSupported;
+    // TMA stores need every C row to start on a 16-byte boundary
+    int tma_store = (N % 8 == 0) &&
+                    make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, M, N, kEpiCols, 32);
+    if (!tma_store)
+        mc = ma;  // not used by the kernel
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
     const int dv = dev.ordinal & 63;
     std::call_once(attr_once[dv], [&] {
-        attr_err[dv] = cudaFuncSetAttribute(gemm_kernel<BN, STAGES>,
+        attr_err[dv] = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, PAIR>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            Cfg::kSmemBytes);
+                                            C::kSmemBytes);
     });
     if (attr_err[dv] != cudaSuccess)
         return attr_err[dv];
-    const int64_t num_m = (M + kBM - 1) / kBM, num_n = (N + BN - 1) / BN;
-    const int64_t tiles = num_m * num_n;
-    const int grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
-    const int group_m = 16;
-    return launch_pdl(gemm_kernel<BN, STAGES>, dim3(grid), dim3(kThreads), Cfg::kSmemBytes, stream,
-                      ma, mb, static_cast<__nv_bfloat16 *>(c), static_cast<int>(M),
-                      static_cast<int>(N), static_cast<int>(K), sa, sb, dev.status,
-                      wait_limit_ns(), group_m);
-}
-
-template <int BN, int STAGES>
-cudaError_t run_pair(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
-                     const float *sa, const float *sb, void *c, const DeviceInfo &dev,
-                     cudaStream_t stream)
-{
-    using Cfg = PairCfg<BN, STAGES>;
-    CUtensorMap ma, mb;
-    if (!make_kmajor_map(&ma, a, M, K, kBM) || !make_kmajor_map(&mb, b, N, K, BN / 2))
-        return cudaErrorNotSupported;
-    static std::once_flag attr_once[64];
-    static cudaError_t attr_err[64];
-    const int dv = dev.ordinal & 63;
-    std::call_once(attr_once[dv], [&] {
-        attr_err[dv] = cudaFuncSetAttribute(gemm_pair_kernel<BN, STAGES>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            Cfg::kSmemBytes);
-    });
-    if (attr_err[dv] != cudaSuccess)
-        return attr_err[dv];
-    const int64_t num_m = (M + 2 * kBM - 1) / (2 * kBM), num_n = (N + BN - 1) / BN;
-    const int64_t tiles = num_m * num_n;
-    const int64_t max_pairs = dev.sm_count / 2;
-    const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
-    const int group_m = 8;
-    return launch_pdl(gemm_pair_kernel<BN, STAGES>, dim3(2 * pairs), dim3(kThreads),
-                      Cfg::kSmemBytes, stream, ma, mb, static_cast<__nv_bfloat16 *>(c),
-                      static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), sa, sb,
-                      dev.status, wait_limit_ns(), group_m);
+    const int64_t tiles = ((M + C::kTileM - 1) / C::kTileM) * ((N + BN - 1) / BN);
+    const int64_t max_units = PAIR ? dev.sm_count / 2 : dev.sm_count;
+    const int units = static_cast<int>(tiles < max_units ? tiles : max_units);
+    const int group_m = PAIR ? 8 : 16;
+    return launch_pdl_cluster(gemm_kernel<BN, STAGES, PAIR>, dim3((PAIR ? 2 : 1) * units),
+                              dim3(kThreads), C::kSmemBytes, stream, PAIR ? 2u : 1u, ma, mb, mc,
+                              static_cast<__nv_bfloat16 *>(c), static_cast<int>(M),
+                              static_cast<int>(N), static_cast<int>(K), sa, sb, dev.status,
+                              wait_limit_ns(), group_m, tma_store);
 }
 
 constexpr int kVariantSingle = 1;
@@ -628,10 +498,8 @@ constexpr int kVariantPair = 2;
 
 // Kernel choice: the CTA-pair kernel for every shape with at least two
 // 128-row blocks; F8_GEMM_VARIANT=1|2 forces one kernel (for measurement).
-int gemm_variant(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev)
+int gemm_variant(int64_t M, const DeviceInfo &dev)
 {
-    (void)N;
-    (void)K;
     const char *e = std::getenv("F8_GEMM_VARIANT");
     const int forced = e ? std::atoi(e) : 0;
     if (forced == kVariantSingle || forced == kVariantPair)
@@ -641,30 +509,15 @@ int gemm_variant(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev)
     return kVariantPair;
 }
 
-__global__ void wait_selftest_kernel(unsigned *status, uint64_t limit_ns)
-{
-    __shared__ uint64_t bar;
-    if (threadIdx.x == 0) {
-        mbar_init(&bar, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, nullptr, limit_ns))
-        atomicOr(status, kStatusTimeout);
-}
-
 } // namespace
 
 cudaError_t launch_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
                         const float *sa, const float *sb, void *c, const DeviceInfo &dev,
                         cudaStream_t stream)
 {
-    switch (gemm_variant(M, N, K, dev)) {
-    case kVariantPair:
-        return run_pair<256, 6>(a, b, M, N, K, sa, sb, c, dev, stream);
-    default:
-        return run_gemm<256, 4>(a, b, M, N, K, sa, sb, c, dev, stream);
-    }
+    if (gemm_variant(M, dev) == kVariantPair)
+        return run_gemm<256, 6, true>(a, b, M, N, K, sa, sb, c, dev, stream);
+    return run_gemm<256, 4, false>(a, b, M, N, K, sa, sb, c, dev, stream);
 }
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, const DeviceInfo &dev, cudaStream_t stream)
