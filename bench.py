@@ -283,6 +283,8 @@ def run_ours(args, world, rank, local):
                 "frac_of_nominal_4500": achieved / FP8_NOMINAL_TFLOPS,
                 "traffic": None}
 
+    iso = kernel_bench(f8, layers, device, stream) if args.kernel_bench else None
+
     # ---- end to end: pinned host buffers in, results out, every step
     e2e = None
     if args.e2e_steps > 0:
@@ -291,7 +293,71 @@ def run_ours(args, world, rank, local):
     return {"value": value, "ms_per_step": ms_max / args.steps, "name": name, "lins": lins,
             "clocks": clocks.summary(), "kernels": kernels, "roofline": roofline,
             "breakdown_ms_per_step": breakdown_ms, "e2e": e2e,
-            "gpu_launches": KERNELS_PER_LINEAR * len(layers) * args.steps}
+            "gpu_launches": KERNELS_PER_LINEAR * len(layers) * args.steps, "isolated": iso}
+
+
+def kernel_bench(f8, layers, device, stream, iters=20):
+    """Each kernel timed alone on the workload's tensors, L2 flushed (a
+    512 MB fill) before every launch, CUDA events around the launch only.
+    amax: 2 B/elem read; cast_transpose: 2 B/elem read + 2 x 1 B/elem
+    written; GEMM: 2 M N K flops.  f8_amax includes its 4-byte memset."""
+    import torch
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+    peaks = load_peaks()
+    fp8_burst = peaks["bf16_tflops"] * FP8_PER_BF16
+
+    def timed(fn):
+        ts = []
+        for _ in range(3):
+            fn()
+        for _ in range(iters):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    out = []
+    seen = set()
+    for L in layers:
+        s = L.saved
+        M, N, K = L.lin.M, L.lin.N, L.lin.K
+        for name, t in (("x", L.x), ("w", L.w), ("dy", L.dy)):
+            key = ("mem", tuple(t.shape))
+            if key in seen:
+                continue
+            seen.add(key)
+            amx = torch.empty((), dtype=torch.float32, device=device)
+            ms = timed(lambda: f8.f8_amax(t, amx))
+            out.append({"kernel": "amax", "tensor": f"{L.lin.name}.{name} {list(t.shape)}",
+                        "us": ms * 1e3, "gbs": 2 * t.numel() / ms / 1e6,
+                        "frac_of_hbm_measured": 2 * t.numel() / ms / 1e6 / peaks["hbm_gbs"]})
+            q = torch.empty(t.shape, dtype=torch.uint8, device=device)
+            qt = torch.empty((t.shape[1], t.shape[0]), dtype=torch.uint8, device=device)
+            sc = torch.empty((), dtype=torch.float32, device=device)
+            ms = timed(lambda: f8.f8_cast_transpose(t, amx, sc, q, qt))
+            out.append({"kernel": "cast_transpose", "tensor": f"{L.lin.name}.{name} {list(t.shape)}",
+                        "us": ms * 1e3, "gbs": 4 * t.numel() / ms / 1e6,
+                        "frac_of_hbm_measured": 4 * t.numel() / ms / 1e6 / peaks["hbm_gbs"]})
+            del q, qt
+        for gname, (a, b, sa, sb, c, mm, nn, kk) in (
+                ("fwd", (L.xq, L.wq, s.scale_x, s.scale_w, L.y, M, N, K)),
+                ("dgrad", (L.dyq, s.w_t, L.dys[1], s.scale_w, L.dx, M, K, N)),
+                ("wgrad", (L.dyt, s.x_t, L.dys[1], s.scale_x, L.dw, N, K, M))):
+            key = ("gemm", mm, nn, kk)
+            if key in seen:
+                continue
+            seen.add(key)
+            ms = timed(lambda: f8.f8_gemm(a, b, sa, sb, c))
+            tf = 2 * mm * nn * kk / ms / 1e9
+            out.append({"kernel": "gemm", "shape": f"{L.lin.name}.{gname} M={mm} N={nn} K={kk}",
+                        "us": ms * 1e3, "tflops": tf, "frac_of_fp8_measured_burst": tf / fp8_burst,
+                        "frac_of_fp8_nominal": tf / FP8_NOMINAL_TFLOPS})
+    del flush
+    return out
 
 
 def run_e2e(f8, layers, args, device, stream, flops_step, world):
@@ -414,13 +480,15 @@ def run_reference(args, world, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--ref-rows", type=int, default=128)
+    ap.add_argument("--kernel-bench", type=int, default=1,
+                    help="also time each kernel alone with L2 flushed (1) or not (0)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -455,6 +523,7 @@ def main(argv=None):
             "roofline": r["roofline"], "kernels": r["kernels"],
             "breakdown_ms_per_step": r["breakdown_ms_per_step"],
             "clocks": r["clocks"], "gpu_launches": r["gpu_launches"],
+            "kernels_isolated": r["isolated"],
             "e2e": r["e2e"], "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
