@@ -3,7 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
 
 One step = every linear of the workload through the whole path: amax(X),
-amax(W), cast_transpose(X), cast_transpose(W), GEMM Y = XW^T, amax(dY),
+cast_transpose(X), amax(W), cast_transpose(W), GEMM Y = XW^T, amax(dY),
 cast_transpose(dY), GEMM dX = dY W, GEMM dW = dY^T X.  The metric is GEMM
 work (6 M N K flops per linear) over the whole step's time, in TFLOP/s.
 
@@ -16,8 +16,11 @@ The JSON line carries, besides the contract keys:
                 duration of its GEMM launches (CUDA events on the launch
                 stream, averaged over a timed run of the same steps), against
                 the measured bf16 peak x 2 (the FP8 : BF16 dense ratio);
-  kernels       the same per-kernel breakdown for amax and cast_transpose
-                (algorithmic bytes: 2 B/elem and 4 B/elem);
+  kernels       the same breakdown for the quantisation of a tensor
+                (amax launch + cast_transpose launch, as the linear runs
+                them; algorithmic bytes 2 B/elem read + 2 x 1 B/elem
+                written, the cast's re-read of the tensor not counted);
+  kernels_isolated  each kernel alone on the workload's tensors, L2 flushed;
   e2e           the same metric through the public API with pinned host
                 buffers: inputs copied in and Y, dX, dW copied out every step;
   cpu_baseline  the CPU oracle on a bounded sample of the same workload.
@@ -163,6 +166,7 @@ class Linear8:
         self.dyq = torch.empty((M, N), dtype=torch.uint8, device=device)
         self.dyt = torch.empty((N, M), dtype=torch.uint8, device=device)
         self.dys = torch.empty(2, dtype=torch.float32, device=device)
+        self.qws = torch.empty(f8.f8_quantize_workspace_bytes(), dtype=torch.uint8, device=device)
 
     def step(self, f8):
         f8.f8_linear_fwd(self.x, self.w, self.y, self.saved, self.ws)
@@ -171,14 +175,14 @@ class Linear8:
     def step_timed(self, f8, ev):
         """The same launches as step(), one C call per kernel, bracketed by events."""
         s = self.saved
-        ev("amax", 2 * self.x.numel(), lambda: f8.f8_amax(self.x, s.amax_x))
-        ev("amax", 2 * self.w.numel(), lambda: f8.f8_amax(self.w, s.amax_w))
-        ev("cast", 4 * self.x.numel(), lambda: f8.f8_cast_transpose(self.x, s.amax_x, s.scale_x, self.xq, s.x_t))
-        ev("cast", 4 * self.w.numel(), lambda: f8.f8_cast_transpose(self.w, s.amax_w, s.scale_w, self.wq, s.w_t))
         M, N, K = self.lin.M, self.lin.N, self.lin.K
+        ev("quantize", 4 * self.x.numel(),
+           lambda: f8.f8_quantize(self.x, s.amax_x, s.scale_x, self.xq, s.x_t, self.qws))
+        ev("quantize", 4 * self.w.numel(),
+           lambda: f8.f8_quantize(self.w, s.amax_w, s.scale_w, self.wq, s.w_t, self.qws))
         ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.xq, self.wq, s.scale_x, s.scale_w, self.y))
-        ev("amax", 2 * self.dy.numel(), lambda: f8.f8_amax(self.dy, self.dys[0]))
-        ev("cast", 4 * self.dy.numel(), lambda: f8.f8_cast_transpose(self.dy, self.dys[0], self.dys[1], self.dyq, self.dyt))
+        ev("quantize", 4 * self.dy.numel(),
+           lambda: f8.f8_quantize(self.dy, self.dys[0], self.dys[1], self.dyq, self.dyt, self.qws))
         ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyq, s.w_t, self.dys[1], s.scale_w, self.dx))
         ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyt, s.x_t, self.dys[1], s.scale_x, self.dw))
 
@@ -297,12 +301,15 @@ def run_ours(args, world, rank, local):
 
 
 def kernel_bench(f8, layers, device, stream, iters=20):
-    """Each kernel timed alone on the workload's tensors, L2 flushed (a
-    512 MB fill) before every launch, CUDA events around the launch only.
+    """Each kernel timed alone on the workload's tensors, L2 flushed before
+    every launch (a 512 MB fill, then a 256 MB read so that the L2 holds
+    clean lines and the timed kernel pays no write-back for the flush), CUDA
+    events around the launch only.
     amax: 2 B/elem read; cast_transpose: 2 B/elem read + 2 x 1 B/elem
     written; GEMM: 2 M N K flops.  f8_amax includes its 4-byte memset."""
     import torch
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+    clean = torch.ones(256 * 1024 * 1024, dtype=torch.uint8, device=device)
     peaks = load_peaks()
     fp8_burst = peaks["bf16_tflops"] * FP8_PER_BF16
 
@@ -311,7 +318,8 @@ def kernel_bench(f8, layers, device, stream, iters=20):
         for _ in range(3):
             fn()
         for _ in range(iters):
-            flush.fill_(1)
+            flush.fill_(1)                # evicts everything from L2 ...
+            clean.max()                   # ... then fills it with clean lines
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()
@@ -342,7 +350,14 @@ def kernel_bench(f8, layers, device, stream, iters=20):
             out.append({"kernel": "cast_transpose", "tensor": f"{L.lin.name}.{name} {list(t.shape)}",
                         "us": ms * 1e3, "gbs": 4 * t.numel() / ms / 1e6,
                         "frac_of_hbm_measured": 4 * t.numel() / ms / 1e6 / peaks["hbm_gbs"]})
-            del q, qt
+            ws = torch.empty(f8.f8_quantize_workspace_bytes(), dtype=torch.uint8, device=device)
+            ms = timed(lambda: f8.f8_quantize(t, amx, sc, q, qt, ws))
+            out.append({"kernel": "quantize (amax + cast_transpose launches)",
+                        "tensor": f"{L.lin.name}.{name} {list(t.shape)}", "us": ms * 1e3,
+                        "gbs": 4 * t.numel() / ms / 1e6,
+                        "frac_of_hbm_measured": 4 * t.numel() / ms / 1e6 / peaks["hbm_gbs"],
+                        "note": "4 B/elem counted (2 read + 2 written); the cast's re-read is not"})
+            del q, qt, ws
         for gname, (a, b, sa, sb, c, mm, nn, kk) in (
                 ("fwd", (L.xq, L.wq, s.scale_x, s.scale_w, L.y, M, N, K)),
                 ("dgrad", (L.dyq, s.w_t, L.dys[1], s.scale_w, L.dx, M, K, N)),
@@ -356,7 +371,7 @@ def kernel_bench(f8, layers, device, stream, iters=20):
             out.append({"kernel": "gemm", "shape": f"{L.lin.name}.{gname} M={mm} N={nn} K={kk}",
                         "us": ms * 1e3, "tflops": tf, "frac_of_fp8_measured_burst": tf / fp8_burst,
                         "frac_of_fp8_nominal": tf / FP8_NOMINAL_TFLOPS})
-    del flush
+    del flush, clean
     return out
 
 

@@ -29,7 +29,8 @@ F8_ERR_UNSUPPORTED = 7
 # every symbol include/f8.h declares
 EXPORTS = ("f8_amax", "f8_cast_transpose", "f8_gemm", "f8_linear_workspace_bytes",
            "f8_linear_fwd", "f8_linear_bwd", "f8_last_device_status", "f8_status_string",
-           "f8_selftest_wait_timeout", "f8_set_wait_limit_ns", "f8_linear_fwd_noalloc")
+           "f8_selftest_wait_timeout", "f8_set_wait_limit_ns", "f8_linear_fwd_noalloc",
+           "f8_quantize", "f8_quantize_workspace_bytes")
 
 
 class F8Error(RuntimeError):
@@ -83,6 +84,10 @@ def lib() -> ctypes.CDLL:
         L.f8_selftest_wait_timeout.restype = st
         L.f8_set_wait_limit_ns.argtypes = [u64]
         L.f8_set_wait_limit_ns.restype = None
+        L.f8_quantize_workspace_bytes.argtypes = []
+        L.f8_quantize_workspace_bytes.restype = ctypes.c_size_t
+        L.f8_quantize.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        L.f8_quantize.restype = st
         L.f8_linear_fwd_noalloc.argtypes = [vp, vp, i64, i64, i64, vp, ctypes.POINTER(_Saved), vp]
         L.f8_linear_fwd_noalloc.restype = st
         _lib = L
@@ -156,6 +161,35 @@ def f8_cast_transpose(x: torch.Tensor, amax: torch.Tensor, scale_out: torch.Tens
     _check(lib().f8_cast_transpose(_ptr(x), rows, cols, _ptr(amax), _ptr(scale_out), _ptr(q),
                                    _ptr(q_t), _stream(stream)), "f8_cast_transpose")
     return q, q_t, scale_out
+
+
+def f8_quantize_workspace_bytes() -> int:
+    return int(lib().f8_quantize_workspace_bytes())
+
+
+def f8_quantize(x: torch.Tensor, amax_out: torch.Tensor | None = None,
+                scale_out: torch.Tensor | None = None, q: torch.Tensor | None = None,
+                q_t: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                want_q: bool = True, want_t: bool = True, stream=None):
+    """amax, scale and both E4M3 layouts of a 2-D bf16 tensor (the linear's
+    own two-launch quantisation): returns (q, q_t, scale, amax)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise TypeError("f8_quantize takes a 2-D bf16 tensor")
+    rows, cols = x.shape
+    dev = x.device
+    if amax_out is None:
+        amax_out = torch.empty((), dtype=torch.float32, device=dev)
+    if scale_out is None:
+        scale_out = torch.empty((), dtype=torch.float32, device=dev)
+    if q is None and want_q:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    if q_t is None and want_t:
+        q_t = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+    if ws is None:
+        ws = torch.empty(f8_quantize_workspace_bytes(), dtype=torch.uint8, device=dev)
+    _check(lib().f8_quantize(_ptr(x), rows, cols, _ptr(amax_out), _ptr(scale_out), _ptr(q),
+                             _ptr(q_t), _ptr(ws), ws.numel(), _stream(stream)), "f8_quantize")
+    return q, q_t, scale_out, amax_out
 
 
 def f8_gemm(a: torch.Tensor, b: torch.Tensor, scale_a: torch.Tensor, scale_b: torch.Tensor,

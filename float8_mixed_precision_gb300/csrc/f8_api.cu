@@ -248,6 +248,30 @@ f8_status f8_cast_transpose(const void *x, int64_t rows, int64_t cols, const flo
                                            q_t, *dev, static_cast<cudaStream_t>(stream)));
 }
 
+size_t f8_quantize_workspace_bytes(void) { return kPartialsBytes; }
+
+f8_status f8_quantize(const void *x, int64_t rows, int64_t cols, float *amax_out,
+                      float *scale_out, uint8_t *q, uint8_t *q_t, void *workspace,
+                      size_t workspace_bytes, void *stream)
+{
+    if (rows < 0 || cols < 0 || amax_out == nullptr || workspace == nullptr ||
+        (rows > 0 && cols > 0 && x == nullptr))
+        return F8_ERR_INVALID;
+    if (workspace_bytes < kPartialsBytes)
+        return F8_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(q, 16) || !aligned(q_t, 16) || !aligned(amax_out, 4) ||
+        !aligned(scale_out, 4) || !aligned(workspace, 16))
+        return F8_ERR_ALIGN;
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned *parts = static_cast<unsigned *>(workspace);
+    int np = 0;
+    F8_TRY_CUDA(launch_amax_partials(x, rows * cols, parts, &np, *dev, st));
+    return from_cuda(launch_cast_transpose(x, rows, cols, nullptr, parts, np, amax_out, scale_out,
+                                           q, q_t, *dev, st));
+}
+
 f8_status f8_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
                   const float *scale_a, const float *scale_b, void *c, void *stream)
 {

@@ -84,6 +84,28 @@ f8_status f8_cast_transpose(const void *x, int64_t rows, int64_t cols, const flo
                             float *scale_out, uint8_t *q, uint8_t *q_t, void *stream);
 
 /*
+ * f8_amax followed by f8_cast_transpose as two back-to-back launches with
+ * nothing in between: the amax launch leaves one partial maximum per CTA in
+ * `workspace` (so no output has to be zeroed first), the cast launch reduces
+ * them in its prologue, writes amax_out and scale_out, and casts; its re-read
+ * of the tensor comes mostly from L2.  Results are bit-identical to the two
+ * separate calls.  This is the quantisation f8_linear_fwd/bwd perform.
+ *   x:          device bf16 [rows, cols], 16-byte aligned.
+ *   amax_out:   device fp32 scalar receiving max |x|.
+ *   scale_out:  device fp32 scalar receiving s = 448 / max(amax, 1e-12), or NULL.
+ *   q, q_t:     as for f8_cast_transpose (either may be NULL).
+ *   workspace:  device scratch of f8_quantize_workspace_bytes() bytes,
+ *               16-byte aligned; its contents need not be initialised and
+ *               are meaningless after the call.  Two calls whose GPU work
+ *               overlaps must not share one workspace.
+ * A non-finite input sets F8_ERR_NONFINITE in the device status word.
+ */
+size_t f8_quantize_workspace_bytes(void);
+f8_status f8_quantize(const void *x, int64_t rows, int64_t cols, float *amax_out,
+                      float *scale_out, uint8_t *q, uint8_t *q_t, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/*
  * C = bf16( A B^T / (scale_a * scale_b) ), fp32 accumulation on tcgen05.
  *   a:       device E4M3 [M, K] row-major (K contiguous), 16-byte aligned.
  *   b:       device E4M3 [N, K] row-major (K contiguous), 16-byte aligned.
@@ -113,7 +135,9 @@ typedef struct {
 /*
  * Device workspace (bytes) that f8_linear_fwd and f8_linear_bwd need for
  * (M, N, K): the row-major E4M3 copies of X and W (forward) or of dY and
- * dY^T plus two scalars (backward), each region 256-byte aligned.
+ * dY^T plus two scalars (backward), and the per-CTA partial maxima of the
+ * amax launches; each region 256-byte aligned.  Its contents need not be
+ * initialised.
  */
 size_t f8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 

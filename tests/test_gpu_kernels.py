@@ -244,3 +244,39 @@ def test_gemm_single_and_pair_kernels(f8, M, N, K, monkeypatch):
         outs.append(c)
     assert f8.f8_last_device_status() == 0
     assert torch.equal(outs[0], outs[1])
+
+
+# ------------------------------------------------------------------ quantize (amax partials + cast)
+@pytest.mark.parametrize("shape", [(1, 1), (7, 33), (16, 16), (320, 528), (130, 260), (1024, 4096),
+                                   (4096, 8192), (8192, 1024)])
+def test_quantize_matches_oracle(f8, shape):
+    x = wl.normal(shape, 0.3, shape[0] + 11 * shape[1])
+    q, qt, s, a = f8.f8_quantize(x.to(DEV))
+    ref = oracle.quantize(_u16(x))
+    assert a.item() == float(ref["amax"]) and s.item() == float(ref["scale"])
+    assert np.array_equal(_u8(q), ref["q"]) and np.array_equal(_u8(qt), ref["qt"])
+    assert f8.f8_last_device_status() == 0
+
+
+def test_quantize_workspace_reuse_and_garbage(f8):
+    """The partial maxima need no clean workspace: back-to-back calls on one
+    workspace, and a workspace full of random bytes, both give the oracle's
+    bytes."""
+    ws = torch.randint(0, 256, (f8.f8_quantize_workspace_bytes(),), dtype=torch.uint8, device=DEV)
+    for i, (shape, std) in enumerate([((2048, 2048), 1.0), ((512, 4096), 1e-3), ((2048, 2048), 50.0)]):
+        x = wl.student_t_outliers(shape, 3, 1e-3, 100.0, 40 + i) if i == 2 else wl.normal(shape, std, 40 + i)
+        q, qt, s, a = f8.f8_quantize(x.to(DEV), ws=ws)
+        ref = oracle.quantize(_u16(x))
+        assert a.item() == float(ref["amax"]) and s.item() == float(ref["scale"])
+        assert np.array_equal(_u8(q), ref["q"]) and np.array_equal(_u8(qt), ref["qt"])
+    assert f8.f8_last_device_status() == 0
+
+
+def test_quantize_nonfinite_and_empty(f8):
+    t = torch.ones((64, 64), dtype=torch.bfloat16)
+    t[5, 6] = float("inf")
+    f8.f8_quantize(t.to(DEV))
+    assert f8.f8_last_device_status() == f8.binding.F8_ERR_NONFINITE
+    q, qt, s, a = f8.f8_quantize(torch.empty((0, 32), dtype=torch.bfloat16, device=DEV))
+    assert a.item() == 0.0 and s.item() == float(oracle.scale(0.0))
+    assert f8.f8_last_device_status() == 0
