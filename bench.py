@@ -376,6 +376,10 @@ def kernel_bench(f8, layers, device, stream, iters=20):
 
 
 def run_e2e(f8, layers, args, device, stream, flops_step, world):
+    """The whole step from pinned host buffers and back, through the public
+    API.  Three streams form a pipeline: the host-to-device copies of linear
+    i+1 and the device-to-host copies of linear i-1 run while linear i
+    computes; events keep each buffer's reuse ordered."""
     import torch
     host = []
     h2d = d2h = 0
@@ -389,16 +393,34 @@ def run_e2e(f8, layers, args, device, stream, flops_step, world):
         host.append((hx, hw, hdy, hy, hdx, hdw))
         h2d += 2 * (hx.numel() + hw.numel() + hdy.numel())
         d2h += 2 * (hy.numel() + hdx.numel() + hdw.numel())
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    n = len(layers)
+    ev_in = [torch.cuda.Event() for _ in range(n)]
+    ev_comp = [torch.cuda.Event() for _ in range(n)]
+    ev_out = [torch.cuda.Event() for _ in range(n)]
+    first = [True] * n
 
     def step():
-        for L, (hx, hw, hdy, hy, hdx, hdw) in zip(layers, host):
-            L.x.copy_(hx, non_blocking=True)
-            L.w.copy_(hw, non_blocking=True)
-            L.dy.copy_(hdy, non_blocking=True)
+        for i, (L, (hx, hw, hdy, hy, hdx, hdw)) in enumerate(zip(layers, host)):
+            with torch.cuda.stream(s_in):
+                if not first[i]:
+                    s_in.wait_event(ev_comp[i])      # last step's compute has read the inputs
+                L.x.copy_(hx, non_blocking=True)
+                L.w.copy_(hw, non_blocking=True)
+                L.dy.copy_(hdy, non_blocking=True)
+                ev_in[i].record(s_in)
+            stream.wait_event(ev_in[i])
+            if not first[i]:
+                stream.wait_event(ev_out[i])         # last step's outputs have been read back
             L.step(f8)
-            hy.copy_(L.y, non_blocking=True)
-            hdx.copy_(L.dx, non_blocking=True)
-            hdw.copy_(L.dw, non_blocking=True)
+            ev_comp[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[i])
+                hy.copy_(L.y, non_blocking=True)
+                hdx.copy_(L.dx, non_blocking=True)
+                hdw.copy_(L.dw, non_blocking=True)
+                ev_out[i].record(s_out)
+            first[i] = False
 
     for _ in range(2):
         step()
@@ -407,16 +429,20 @@ def run_e2e(f8, layers, args, device, stream, flops_step, world):
         import torch.distributed as dist
         dist.barrier()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
+    t0.record(s_in)
     for _ in range(args.e2e_steps):
         step()
-    t1.record(stream)
+    s_out.wait_stream(stream)
+    t1.record(s_out)
     torch.cuda.synchronize()
     ms = max_over_ranks(t0.elapsed_time(t1), world, device)
     total = sum_over_ranks(flops_step * args.e2e_steps, world, device)
+    # the results really came back: spot-check one output against its device copy
+    ok = torch.equal(host[-1][5][:4].to(device), layers[-1].dw[:4])
     return {"value": total / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-            "ms_per_step": ms / args.e2e_steps}
+            "ms_per_step": ms / args.e2e_steps, "pipelined": "3 streams (h2d, compute, d2h)",
+            "readback_check": bool(ok)}
 
 
 # ------------------------------------------------------------------ CPU oracle
