@@ -48,6 +48,20 @@ FP8_NOMINAL_TFLOPS = 4500.0
 FP8_PER_BF16 = 2.0          # nominal dense FP8 : BF16 tensor throughput
 HBM_NOMINAL_GBS = 8000.0
 
+# DRAM bytes (read + write) of the 12 GEMM launches of one attention fwd+bwd
+# step, from one ncu capture (profiles/gemm_traffic_attn8b.md), valid for the
+# GEMM sources whose hash is given; reported as null once they change.
+GEMM_TRAFFIC = {"workload": 2, "bytes_per_step": 696192256, "sources_sha256_16": "9ca37434df5e9d93"}
+
+
+def gemm_sources_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("f8_gemm.cu", "f8_ptx.cuh"):
+        with open(os.path.join(ROOT, "float8_mixed_precision_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
 
 # ------------------------------------------------------------------ helpers
 def dist_env():
@@ -285,7 +299,13 @@ def run_ours(args, world, rank, local):
                 "frac": achieved / fp8_peak,
                 "peak_note": f"{peaks['source']} bf16 sustained {peaks['bf16_tflops_sustained']} x {FP8_PER_BF16} (FP8:BF16 dense)",
                 "frac_of_nominal_4500": achieved / FP8_NOMINAL_TFLOPS,
-                "traffic": None}
+                "traffic": (GEMM_TRAFFIC["bytes_per_step"]
+                            if args.config == GEMM_TRAFFIC["workload"]
+                            and gemm_sources_hash() == GEMM_TRAFFIC["sources_sha256_16"] else None),
+                "traffic_unit": "bytes per step (all GEMM launches of the step, like achieved)",
+                # E4M3 operands read once + bf16 outputs written once, 3 GEMMs per linear
+                "algorithmic_bytes_per_step": sum(4 * (l.M * l.K + l.N * l.K + l.M * l.N)
+                                                  for l in lins)}
 
     iso = kernel_bench(f8, layers, device, stream) if args.kernel_bench else None
 
