@@ -89,6 +89,17 @@ def _load():
         lib.or_gemm_rows.restype = None
         lib.or_gemm_cols.argtypes = [u8p, u8p, i64, i64, i64, f32, f32, i64p, i64, u16p]
         lib.or_gemm_cols.restype = None
+        lib.or_e5m2_decode.argtypes = [ctypes.c_uint8]
+        lib.or_e5m2_decode.restype = ctypes.c_double
+        lib.or_e5m2_encode.argtypes = [f32]
+        lib.or_e5m2_encode.restype = ctypes.c_uint8
+        lib.or_scale_fmt.argtypes = [f32, ctypes.c_int]
+        lib.or_scale_fmt.restype = f32
+        lib.or_cast_transpose_fmt.argtypes = [u16p, i64, i64, f32, ctypes.c_int, u8p, u8p]
+        lib.or_cast_transpose_fmt.restype = None
+        lib.or_gemm_rows_fmt.argtypes = [u8p, ctypes.c_int, u8p, ctypes.c_int, i64, i64, i64, f32, f32,
+                                         i64p, i64, u16p]
+        lib.or_gemm_rows_fmt.restype = None
         lib.or_num_threads.argtypes = []
         lib.or_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -135,6 +146,19 @@ def e4m3_encode(v: float) -> int:
     return int(_load().or_e4m3_encode(float(np.float32(v))))
 
 
+E4M3, E5M2 = 0, 1
+FMT_MAX = {E4M3: 448.0, E5M2: 57344.0}
+
+
+def e5m2_decode(code: int) -> float:
+    return float(_load().or_e5m2_decode(int(code)))
+
+
+def e5m2_encode(v: float) -> int:
+    """v is taken as an fp32 value."""
+    return int(_load().or_e5m2_encode(float(np.float32(v))))
+
+
 def num_threads() -> int:
     return int(_load().or_num_threads())
 
@@ -164,6 +188,35 @@ def cast_transpose(x_bits: np.ndarray, s: float) -> tuple[np.ndarray, np.ndarray
     _load().or_cast_transpose(_ptr(x, ctypes.c_uint16), rows, cols, float(np.float32(s)),
                               _ptr(q, ctypes.c_uint8), _ptr(qt, ctypes.c_uint8))
     return q, qt
+
+
+def scale_fmt(a: float, fmt: int) -> np.float32:
+    return np.float32(_load().or_scale_fmt(float(np.float32(a)), int(fmt)))
+
+
+def cast_transpose_fmt(x_bits: np.ndarray, s: float, fmt: int) -> tuple[np.ndarray, np.ndarray]:
+    x = _u16(x_bits)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), np.uint8)
+    qt = np.empty((cols, rows), np.uint8)
+    _load().or_cast_transpose_fmt(_ptr(x, ctypes.c_uint16), rows, cols, float(np.float32(s)),
+                                  int(fmt), _ptr(q, ctypes.c_uint8), _ptr(qt, ctypes.c_uint8))
+    return q, qt
+
+
+def gemm_rows_fmt(a_q, fa: int, b_q, fb: int, sa, sb, rows=None) -> np.ndarray:
+    """Rows of C = bf16(A B^T / (sa sb)) with A codes in format fa and B in fb
+    (exact __int128 sums); all rows if ``rows`` is None."""
+    a = _u8(a_q)
+    b = _u8(b_q)
+    M, K = a.shape
+    N = b.shape[0]
+    r = np.arange(M, dtype=np.int64) if rows is None else np.ascontiguousarray(np.asarray(rows, np.int64))
+    out = np.empty((r.size, N), np.uint16)
+    _load().or_gemm_rows_fmt(_ptr(a, ctypes.c_uint8), int(fa), _ptr(b, ctypes.c_uint8), int(fb), M, N,
+                             K, float(np.float32(sa)), float(np.float32(sb)), _ptr(r, ctypes.c_int64),
+                             r.size, _ptr(out, ctypes.c_uint16))
+    return out
 
 
 def gemm(a_q: np.ndarray, b_q: np.ndarray, sa: float, sb: float, route: int = 0) -> np.ndarray:
@@ -214,12 +267,16 @@ def gemm_cols(a_q, b_q, sa, sb, cols) -> np.ndarray:
 # the linear layer, step by step
 # --------------------------------------------------------------------------
 
-def quantize(x_bits: np.ndarray) -> dict:
-    """amax -> scale -> (q, q^T) for one bf16 tensor."""
+def quantize(x_bits: np.ndarray, fmt: int = E4M3) -> dict:
+    """amax -> scale -> (q, q^T) for one bf16 tensor in format fmt."""
     a, nonfinite = amax(x_bits)
-    s = scale(a)
-    q, qt = cast_transpose(x_bits, s)
-    return {"amax": a, "scale": s, "q": q, "qt": qt, "nonfinite": nonfinite}
+    if fmt == E4M3:
+        s = scale(a)
+        q, qt = cast_transpose(x_bits, s)
+    else:
+        s = scale_fmt(a, fmt)
+        q, qt = cast_transpose_fmt(x_bits, s, fmt)
+    return {"amax": a, "scale": s, "q": q, "qt": qt, "nonfinite": nonfinite, "fmt": fmt}
 
 
 def linear_fwd(x_bits: np.ndarray, w_bits: np.ndarray) -> dict:
@@ -230,10 +287,15 @@ def linear_fwd(x_bits: np.ndarray, w_bits: np.ndarray) -> dict:
     return {"x": qx, "w": qw, "y": y}
 
 
-def linear_bwd(dy_bits: np.ndarray, fwd: dict) -> dict:
-    """dX = dY W, dW = dY^T X using the forward's quantised X and W."""
-    qdy = quantize(dy_bits)
+def linear_bwd(dy_bits: np.ndarray, fwd: dict, dy_fmt: int = E4M3) -> dict:
+    """dX = dY W, dW = dY^T X using the forward's quantised X and W; dY is
+    quantised in format dy_fmt (E4M3 or E5M2)."""
+    qdy = quantize(dy_bits, dy_fmt)
     qx, qw = fwd["x"], fwd["w"]
+    if dy_fmt != E4M3:
+        dx = gemm_rows_fmt(qdy["q"], dy_fmt, qw["qt"], E4M3, qdy["scale"], qw["scale"])
+        dw = gemm_rows_fmt(qdy["qt"], dy_fmt, qx["qt"], E4M3, qdy["scale"], qx["scale"])
+        return {"dy": qdy, "dx": dx, "dw": dw}
     # dX[m,k] = sum_n dY[m,n] W[n,k]: A = q(dY) [M,N], B = q(W)^T [K,N]
     dx = gemm(qdy["q"], qw["qt"], qdy["scale"], qw["scale"])
     # dW[n,k] = sum_m dY[m,n] X[m,k]: A = q(dY)^T [N,M], B = q(X)^T [K,M]

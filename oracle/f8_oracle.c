@@ -156,6 +156,68 @@ uint8_t or_e4m3_encode(float v)
 }
 
 /* ------------------------------------------------------------------------ */
+/* E5M2 ("float8_e5m2")                                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Value of an E5M2 byte S.EEEEE.MM (bias 15, IEEE-like): E=0 subnormals
+ * M * 2^-16; E=1..30 (4+M) * 2^(E-17); E=31: M=0 is +-inf, else NaN.
+ */
+double or_e5m2_decode(uint8_t c)
+{
+    int s = c >> 7;
+    int E = (c >> 2) & 0x1F;
+    int M = c & 0x3;
+    double mag;
+    if (E == 31)
+        mag = (M == 0) ? INFINITY : NAN;
+    else if (E == 0)
+        mag = (double)M * ldexp(1.0, -16);
+    else
+        mag = (double)(4 + M) * ldexp(1.0, E - 17);
+    return s ? -mag : mag;
+}
+
+/*
+ * Saturating round-to-nearest-even of an fp32 value to E5M2: |v| >= 57344
+ * (the largest finite value, 1.75 * 2^15) and +-inf give +-57344; NaN gives
+ * a NaN code; otherwise the nearest grid point, ties to the even code.  The
+ * spacing is 2^-16 below 2^-14 and 2^(E-2) in the binade [2^E, 2^(E+1)).
+ */
+uint8_t or_e5m2_encode(float v)
+{
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    if (isnan(v))
+        return (uint8_t)(sign | 0x7F);
+    double a = fabs((double)v);
+    if (a >= 57344.0)
+        return (uint8_t)(sign | 0x7B);
+
+    double ulp;
+    if (a < ldexp(1.0, -14)) {
+        ulp = ldexp(1.0, -16);
+    } else {
+        int e;
+        frexp(a, &e);
+        ulp = ldexp(1.0, (e - 1) - 2);
+    }
+    double n = a / ulp;
+    double fl = floor(n);
+    double r = n - fl;
+    if (r > 0.5 || (r == 0.5 && fmod(fl, 2.0) == 1.0))
+        fl += 1.0;
+    double q = fl * ulp;   /* a grid value in [0, 57344] */
+
+    if (q < ldexp(1.0, -14))
+        return (uint8_t)(sign | (uint8_t)(q / ldexp(1.0, -16)));
+    int e2;
+    frexp(q, &e2);
+    int E2 = e2 - 1;
+    int mant = (int)(q / ldexp(1.0, E2) * 4.0) - 4;
+    return (uint8_t)(sign | ((E2 + 15) << 2) | mant);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Dynamic tensorwise scaling                                                */
 /* ------------------------------------------------------------------------ */
 
@@ -188,6 +250,14 @@ float or_scale(float amax)
     return 448.0f / d;
 }
 
+/* The same with the largest finite value of the format: 448 (E4M3, fmt 0)
+ * or 57344 (E5M2, fmt 1). */
+float or_scale_fmt(float amax, int fmt)
+{
+    float d = (amax > 1e-12f) ? amax : 1e-12f;
+    return (fmt == 1 ? 57344.0f : 448.0f) / d;
+}
+
 /*
  * q = satfinite_rne_e4m3(fl32(x * s)) for a row-major bf16 [rows, cols]
  * tensor, written row-major into q [rows, cols] and column-major into
@@ -201,6 +271,23 @@ void or_cast_transpose(const uint16_t *x, int64_t rows, int64_t cols, float s,
         for (int64_t c = 0; c < cols; ++c) {
             float v = or_bf16_to_f32(x[r * cols + c]) * s;
             uint8_t b = or_e4m3_encode(v);
+            if (q)
+                q[r * cols + c] = b;
+            if (qt)
+                qt[c * rows + r] = b;
+        }
+    }
+}
+
+/* q = satfinite_rne_<fmt>(fl32(x * s)), both layouts, fmt 0 = E4M3, 1 = E5M2. */
+void or_cast_transpose_fmt(const uint16_t *x, int64_t rows, int64_t cols, float s, int fmt,
+                           uint8_t *q, uint8_t *qt)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < cols; ++c) {
+            float v = or_bf16_to_f32(x[r * cols + c]) * s;
+            uint8_t b = (fmt == 1) ? or_e5m2_encode(v) : or_e4m3_encode(v);
             if (q)
                 q[r * cols + c] = b;
             if (qt)
@@ -336,6 +423,59 @@ void or_gemm_cols(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int6
         free(za);
     }
     free(zb);
+}
+
+/*
+ * Mixed formats.  Every E5M2 value is an integer multiple of 2^-16 with
+ * magnitude at most 57344 * 2^16 < 2^32 and every E4M3 value one of 2^-9, so
+ * z = value * 2^16 (E5M2) or value * 2^9 (E4M3) is an exact int64, and the
+ * dot product is summed exactly in __int128 (a product is below 2^64 and a
+ * row has fewer than 2^31 terms).  The exact sum times 2^-(ea+eb) is then
+ * rounded to fp64 (exact while it stays below 2^53, one rounding beyond),
+ * divided by sa*sb (exact in fp64) with one more rounding, and rounded to
+ * nearest-even bf16.  fmt: 0 = E4M3, 1 = E5M2.
+ */
+static void decode_row_z64(const uint8_t *src, int64_t n, int fmt, int64_t *z)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        double v = fmt == 1 ? or_e5m2_decode(src[i]) : or_e4m3_decode(src[i]);
+        z[i] = (isnan(v) || isinf(v)) ? 0 : (int64_t)(v * (fmt == 1 ? 65536.0 : 512.0));
+    }
+}
+
+static uint16_t finish128(__int128 acc, int shift, float sa, float sb)
+{
+    double y = (double)acc * ldexp(1.0, -shift) / ((double)sa * (double)sb);
+    return or_f64_to_bf16(y);
+}
+
+/* Rows `rows` of C = A B^T with A in format fa, B in format fb. */
+void or_gemm_rows_fmt(const uint8_t *a, int fa, const uint8_t *b, int fb, int64_t M, int64_t N,
+                      int64_t K, float sa, float sb, const int64_t *rows, int64_t nrows,
+                      uint16_t *out)
+{
+    (void)M;
+    const int shift = (fa == 1 ? 16 : 9) + (fb == 1 ? 16 : 9);
+    int64_t *za = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nrows * K > 0 ? nrows * K : 1));
+    for (int64_t i = 0; i < nrows; ++i)
+        decode_row_z64(a + rows[i] * K, K, fa, za + i * K);
+#pragma omp parallel
+    {
+        int64_t *zr = (int64_t *)malloc(sizeof(int64_t) * (size_t)(K > 0 ? K : 1));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t n = 0; n < N; ++n) {
+            decode_row_z64(b + n * K, K, fb, zr);
+            for (int64_t i = 0; i < nrows; ++i) {
+                const int64_t *zi = za + i * K;
+                __int128 acc = 0;
+                for (int64_t k = 0; k < K; ++k)
+                    acc += (__int128)zi[k] * (__int128)zr[k];
+                out[i * N + n] = finish128(acc, shift, sa, sb);
+            }
+        }
+        free(zr);
+    }
+    free(za);
 }
 
 /* Number of threads the parallel loops above use. */
