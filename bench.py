@@ -162,9 +162,10 @@ class ClockSampler:
 class Linear8:
     """Device buffers of one linear: inputs, outputs, saved tensors, workspace."""
 
-    def __init__(self, f8, lin, inputs, device):
+    def __init__(self, f8, lin, inputs, device, dy_fmt=0):
         import torch
         self.lin = lin
+        self.dy_fmt = dy_fmt
         self.x = inputs["x"].to(device)
         self.w = inputs["w"].to(device)
         self.dy = inputs["dy"].to(device)
@@ -184,7 +185,7 @@ class Linear8:
 
     def step(self, f8):
         f8.f8_linear_fwd(self.x, self.w, self.y, self.saved, self.ws)
-        f8.f8_linear_bwd(self.dy, self.saved, dx=self.dx, dw=self.dw, ws=self.ws)
+        f8.f8_linear_bwd(self.dy, self.saved, dx=self.dx, dw=self.dw, ws=self.ws, dy_fmt=self.dy_fmt)
 
     def step_timed(self, f8, ev):
         """The same launches as step(), one C call per kernel, bracketed by events."""
@@ -196,9 +197,12 @@ class Linear8:
            lambda: f8.f8_quantize(self.w, s.amax_w, s.scale_w, self.wq, s.w_t, self.qws))
         ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.xq, self.wq, s.scale_x, s.scale_w, self.y))
         ev("quantize", 4 * self.dy.numel(),
-           lambda: f8.f8_quantize(self.dy, self.dys[0], self.dys[1], self.dyq, self.dyt, self.qws))
-        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyq, s.w_t, self.dys[1], s.scale_w, self.dx))
-        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyt, s.x_t, self.dys[1], s.scale_x, self.dw))
+           lambda: f8.f8_quantize(self.dy, self.dys[0], self.dys[1], self.dyq, self.dyt, self.qws,
+                                  fmt=self.dy_fmt))
+        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyq, s.w_t, self.dys[1], s.scale_w, self.dx,
+                                                     fmt_a=self.dy_fmt))
+        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyt, s.x_t, self.dys[1], s.scale_x, self.dw,
+                                                     fmt_a=self.dy_fmt))
 
 
 KERNELS_PER_LINEAR = 9  # 3 amax + 3 cast_transpose + 3 GEMM
@@ -214,7 +218,9 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(device)
     f8.lib()
     name, lins = wl.workload(args.config)
-    layers = [Linear8(f8, lin, wl.linear_inputs(args.config, i), device) for i, lin in enumerate(lins)]
+    dy_fmt = f8.F8_E5M2 if args.dy_format == "e5m2" else f8.F8_E4M3
+    layers = [Linear8(f8, lin, wl.linear_inputs(args.config, i), device, dy_fmt)
+              for i, lin in enumerate(lins)]
     flops_step = sum(l.flops for l in lins)
     stream = torch.cuda.current_stream()
 
@@ -386,7 +392,8 @@ def kernel_bench(f8, layers, device, stream, iters=20):
             if key in seen:
                 continue
             seen.add(key)
-            ms = timed(lambda: f8.f8_gemm(a, b, sa, sb, c))
+            fa = L.dy_fmt if gname != "fwd" else 0
+            ms = timed(lambda: f8.f8_gemm(a, b, sa, sb, c, fmt_a=fa))
             tf = 2 * mm * nn * kk / ms / 1e9
             out.append({"kernel": "gemm", "shape": f"{L.lin.name}.{gname} M={mm} N={nn} K={kk}",
                         "us": ms * 1e3, "tflops": tf, "frac_of_fp8_measured_burst": tf / fp8_burst,
@@ -548,6 +555,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--ref-rows", type=int, default=128)
+    ap.add_argument("--dy-format", default="e4m3", choices=["e4m3", "e5m2"],
+                    help="FP8 format of dY in the backward pass (X and W stay E4M3)")
     ap.add_argument("--kernel-bench", type=int, default=1,
                     help="also time each kernel alone with L2 flushed (1) or not (0)")
     args = ap.parse_args(argv)
@@ -574,7 +583,8 @@ def main(argv=None):
             "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3", "data": "synthetic (seeded; workloads.py)",
+            "dtype": "e4m3" if args.dy_format == "e4m3" else "e4m3 (X, W) / e5m2 (dY)",
+            "data": "synthetic (seeded; workloads.py)",
             "config": {"workload": r["name"],
                        "linears": [f"{l.name} M={l.M} K={l.K} N={l.N}" for l in lins],
                        "flops_per_step": sum(l.flops for l in lins),

@@ -30,7 +30,11 @@ F8_ERR_UNSUPPORTED = 7
 EXPORTS = ("f8_amax", "f8_cast_transpose", "f8_gemm", "f8_linear_workspace_bytes",
            "f8_linear_fwd", "f8_linear_bwd", "f8_last_device_status", "f8_status_string",
            "f8_selftest_wait_timeout", "f8_set_wait_limit_ns", "f8_linear_fwd_noalloc",
-           "f8_quantize", "f8_quantize_workspace_bytes")
+           "f8_quantize", "f8_quantize_workspace_bytes", "f8_quantize_fmt", "f8_gemm_fmt",
+           "f8_linear_bwd_fmt")
+
+F8_E4M3 = 0
+F8_E5M2 = 1
 
 
 class F8Error(RuntimeError):
@@ -88,6 +92,13 @@ def lib() -> ctypes.CDLL:
         L.f8_quantize_workspace_bytes.restype = ctypes.c_size_t
         L.f8_quantize.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         L.f8_quantize.restype = st
+        L.f8_quantize_fmt.argtypes = [vp, i64, i64, ctypes.c_int, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        L.f8_quantize_fmt.restype = st
+        L.f8_gemm_fmt.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, i64, i64, i64, vp, vp, vp, vp]
+        L.f8_gemm_fmt.restype = st
+        L.f8_linear_bwd_fmt.argtypes = [vp, ctypes.c_int, ctypes.POINTER(_Saved), i64, i64, i64, vp, vp,
+                                        vp, ctypes.c_size_t, vp]
+        L.f8_linear_bwd_fmt.restype = st
         L.f8_linear_fwd_noalloc.argtypes = [vp, vp, i64, i64, i64, vp, ctypes.POINTER(_Saved), vp]
         L.f8_linear_fwd_noalloc.restype = st
         _lib = L
@@ -170,9 +181,10 @@ def f8_quantize_workspace_bytes() -> int:
 def f8_quantize(x: torch.Tensor, amax_out: torch.Tensor | None = None,
                 scale_out: torch.Tensor | None = None, q: torch.Tensor | None = None,
                 q_t: torch.Tensor | None = None, ws: torch.Tensor | None = None,
-                want_q: bool = True, want_t: bool = True, stream=None):
-    """amax, scale and both E4M3 layouts of a 2-D bf16 tensor (the linear's
-    own two-launch quantisation): returns (q, q_t, scale, amax)."""
+                want_q: bool = True, want_t: bool = True, fmt: int = F8_E4M3, stream=None):
+    """amax, scale and both FP8 layouts of a 2-D bf16 tensor (the linear's
+    own two-launch quantisation): returns (q, q_t, scale, amax).  ``fmt``
+    picks E4M3 (f8_quantize) or E5M2 (f8_quantize_fmt)."""
     if x.dtype != torch.bfloat16 or x.dim() != 2:
         raise TypeError("f8_quantize takes a 2-D bf16 tensor")
     rows, cols = x.shape
@@ -187,22 +199,33 @@ def f8_quantize(x: torch.Tensor, amax_out: torch.Tensor | None = None,
         q_t = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
     if ws is None:
         ws = torch.empty(f8_quantize_workspace_bytes(), dtype=torch.uint8, device=dev)
-    _check(lib().f8_quantize(_ptr(x), rows, cols, _ptr(amax_out), _ptr(scale_out), _ptr(q),
-                             _ptr(q_t), _ptr(ws), ws.numel(), _stream(stream)), "f8_quantize")
+    if fmt == F8_E4M3:
+        _check(lib().f8_quantize(_ptr(x), rows, cols, _ptr(amax_out), _ptr(scale_out), _ptr(q),
+                                 _ptr(q_t), _ptr(ws), ws.numel(), _stream(stream)), "f8_quantize")
+    else:
+        _check(lib().f8_quantize_fmt(_ptr(x), rows, cols, int(fmt), _ptr(amax_out), _ptr(scale_out),
+                                     _ptr(q), _ptr(q_t), _ptr(ws), ws.numel(), _stream(stream)),
+               "f8_quantize_fmt")
     return q, q_t, scale_out, amax_out
 
 
 def f8_gemm(a: torch.Tensor, b: torch.Tensor, scale_a: torch.Tensor, scale_b: torch.Tensor,
-            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """bf16(a b^T / (scale_a scale_b)) for E4M3 codes a [M,K], b [N,K] (uint8)."""
+            out: torch.Tensor | None = None, fmt_a: int = F8_E4M3, fmt_b: int = F8_E4M3,
+            stream=None) -> torch.Tensor:
+    """bf16(a b^T / (scale_a scale_b)) for FP8 codes a [M,K], b [N,K] (uint8);
+    formats other than E4M3 go through f8_gemm_fmt."""
     M, K = a.shape
     N, K2 = b.shape
     if K != K2:
         raise ValueError("contraction sizes differ")
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
-    _check(lib().f8_gemm(_ptr(a), _ptr(b), M, N, K, _ptr(scale_a), _ptr(scale_b), _ptr(out),
-                         _stream(stream)), "f8_gemm")
+    if fmt_a == F8_E4M3 and fmt_b == F8_E4M3:
+        _check(lib().f8_gemm(_ptr(a), _ptr(b), M, N, K, _ptr(scale_a), _ptr(scale_b), _ptr(out),
+                             _stream(stream)), "f8_gemm")
+    else:
+        _check(lib().f8_gemm_fmt(_ptr(a), int(fmt_a), _ptr(b), int(fmt_b), M, N, K, _ptr(scale_a),
+                                 _ptr(scale_b), _ptr(out), _stream(stream)), "f8_gemm_fmt")
     return out
 
 
@@ -286,8 +309,9 @@ def f8_linear_fwd_noalloc(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | No
 def f8_linear_bwd(dy: torch.Tensor, saved: LinearSaved, K: int | None = None,
                   dx: torch.Tensor | None = None, dw: torch.Tensor | None = None,
                   ws: torch.Tensor | None = None, want_dx: bool = True, want_dw: bool = True,
-                  stream=None):
-    """(dX, dW) of the linear whose forward produced ``saved``."""
+                  dy_fmt: int = F8_E4M3, stream=None):
+    """(dX, dW) of the linear whose forward produced ``saved``; ``dy_fmt``
+    E5M2 routes through f8_linear_bwd_fmt."""
     M, N = dy.shape
     K = saved.x_t.shape[0]
     dev = dy.device
@@ -298,6 +322,11 @@ def f8_linear_bwd(dy: torch.Tensor, saved: LinearSaved, K: int | None = None,
     if ws is None:
         ws = workspace(M, N, K, dev)
     s = saved.c_struct()
-    _check(lib().f8_linear_bwd(_ptr(dy), ctypes.byref(s), M, N, K, _ptr(dx), _ptr(dw), _ptr(ws),
-                               ws.numel(), _stream(stream)), "f8_linear_bwd")
+    if dy_fmt == F8_E4M3:
+        _check(lib().f8_linear_bwd(_ptr(dy), ctypes.byref(s), M, N, K, _ptr(dx), _ptr(dw), _ptr(ws),
+                                   ws.numel(), _stream(stream)), "f8_linear_bwd")
+    else:
+        _check(lib().f8_linear_bwd_fmt(_ptr(dy), int(dy_fmt), ctypes.byref(s), M, N, K, _ptr(dx),
+                                       _ptr(dw), _ptr(ws), ws.numel(), _stream(stream)),
+               "f8_linear_bwd_fmt")
     return dx, dw

@@ -245,17 +245,17 @@ f8_status f8_cast_transpose(const void *x, int64_t rows, int64_t cols, const flo
     const DeviceInfo *dev;
     F8_TRY(get_device(&dev));
     return from_cuda(launch_cast_transpose(x, rows, cols, amax, nullptr, 0, nullptr, scale_out, q,
-                                           q_t, *dev, static_cast<cudaStream_t>(stream)));
+                                           q_t, 0, *dev, static_cast<cudaStream_t>(stream)));
 }
 
 size_t f8_quantize_workspace_bytes(void) { return kPartialsBytes; }
 
-f8_status f8_quantize(const void *x, int64_t rows, int64_t cols, float *amax_out,
-                      float *scale_out, uint8_t *q, uint8_t *q_t, void *workspace,
-                      size_t workspace_bytes, void *stream)
+static f8_status quantize_impl(const void *x, int64_t rows, int64_t cols, int fmt, float *amax_out,
+                               float *scale_out, uint8_t *q, uint8_t *q_t, void *workspace,
+                               size_t workspace_bytes, void *stream)
 {
     if (rows < 0 || cols < 0 || amax_out == nullptr || workspace == nullptr ||
-        (rows > 0 && cols > 0 && x == nullptr))
+        (rows > 0 && cols > 0 && x == nullptr) || (fmt != F8_E4M3 && fmt != F8_E5M2))
         return F8_ERR_INVALID;
     if (workspace_bytes < kPartialsBytes)
         return F8_ERR_INVALID;
@@ -269,12 +269,31 @@ f8_status f8_quantize(const void *x, int64_t rows, int64_t cols, float *amax_out
     int np = 0;
     F8_TRY_CUDA(launch_amax_partials(x, rows * cols, parts, &np, *dev, st));
     return from_cuda(launch_cast_transpose(x, rows, cols, nullptr, parts, np, amax_out, scale_out,
-                                           q, q_t, *dev, st));
+                                           q, q_t, fmt, *dev, st));
 }
 
-f8_status f8_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
-                  const float *scale_a, const float *scale_b, void *c, void *stream)
+f8_status f8_quantize(const void *x, int64_t rows, int64_t cols, float *amax_out,
+                      float *scale_out, uint8_t *q, uint8_t *q_t, void *workspace,
+                      size_t workspace_bytes, void *stream)
 {
+    return quantize_impl(x, rows, cols, F8_E4M3, amax_out, scale_out, q, q_t, workspace,
+                         workspace_bytes, stream);
+}
+
+f8_status f8_quantize_fmt(const void *x, int64_t rows, int64_t cols, f8_format fmt,
+                          float *amax_out, float *scale_out, uint8_t *q, uint8_t *q_t,
+                          void *workspace, size_t workspace_bytes, void *stream)
+{
+    return quantize_impl(x, rows, cols, fmt, amax_out, scale_out, q, q_t, workspace,
+                         workspace_bytes, stream);
+}
+
+static f8_status gemm_impl(const uint8_t *a, int fa, const uint8_t *b, int fb, int64_t M, int64_t N,
+                           int64_t K, const float *scale_a, const float *scale_b, void *c,
+                           void *stream)
+{
+    if ((fa != F8_E4M3 && fa != F8_E5M2) || (fb != F8_E4M3 && fb != F8_E5M2))
+        return F8_ERR_INVALID;
     F8_TRY(check_gemm_args(a, b, M, N, K, scale_a, scale_b, c));
     const DeviceInfo *dev;
     F8_TRY(get_device(&dev));
@@ -283,7 +302,20 @@ f8_status f8_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int6
         return F8_OK;
     if (K == 0)
         return from_cuda(cudaMemsetAsync(c, 0, static_cast<size_t>(M) * N * 2, st));
-    return from_cuda(launch_gemm(a, b, M, N, K, scale_a, scale_b, c, *dev, st));
+    return from_cuda(launch_gemm(a, b, M, N, K, scale_a, scale_b, c, *dev, st, fa, fb));
+}
+
+f8_status f8_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
+                  const float *scale_a, const float *scale_b, void *c, void *stream)
+{
+    return gemm_impl(a, F8_E4M3, b, F8_E4M3, M, N, K, scale_a, scale_b, c, stream);
+}
+
+f8_status f8_gemm_fmt(const uint8_t *a, f8_format fmt_a, const uint8_t *b, f8_format fmt_b,
+                      int64_t M, int64_t N, int64_t K, const float *scale_a, const float *scale_b,
+                      void *c, void *stream)
+{
+    return gemm_impl(a, fmt_a, b, fmt_b, M, N, K, scale_a, scale_b, c, stream);
 }
 
 size_t f8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K)
@@ -314,17 +346,19 @@ f8_status f8_linear_fwd(const void *x, const void *w, int64_t M, int64_t N, int6
     // each cast follows its own amax so that its re-read of the tensor hits L2
     F8_TRY_CUDA(launch_amax_partials(x, M * K, fw.parts_x, &np, *dev, st));
     F8_TRY_CUDA(launch_cast_transpose(x, M, K, nullptr, fw.parts_x, np, saved->amax_x,
-                                      saved->scale_x, fw.x_q, saved->x_t, *dev, st));
+                                      saved->scale_x, fw.x_q, saved->x_t, 0, *dev, st));
     F8_TRY_CUDA(launch_amax_partials(w, N * K, fw.parts_w, &np, *dev, st));
     F8_TRY_CUDA(launch_cast_transpose(w, N, K, nullptr, fw.parts_w, np, saved->amax_w,
-                                      saved->scale_w, fw.w_q, saved->w_t, *dev, st));
+                                      saved->scale_w, fw.w_q, saved->w_t, 0, *dev, st));
     return from_cuda(launch_gemm(fw.x_q, fw.w_q, M, N, K, saved->scale_x, saved->scale_w, y, *dev, st));
 }
 
-f8_status f8_linear_bwd(const void *dy, const f8_linear_saved *saved, int64_t M, int64_t N,
-                        int64_t K, void *dx, void *dw, void *workspace, size_t workspace_bytes,
-                        void *stream)
+static f8_status linear_bwd_impl(const void *dy, int fdy, const f8_linear_saved *saved, int64_t M,
+                                 int64_t N, int64_t K, void *dx, void *dw, void *workspace,
+                                 size_t workspace_bytes, void *stream)
 {
+    if (fdy != F8_E4M3 && fdy != F8_E5M2)
+        return F8_ERR_INVALID;
     F8_TRY(check_linear_shape(M, N, K));
     F8_TRY(check_saved(saved));
     if (dy == nullptr || workspace == nullptr)
@@ -340,14 +374,30 @@ f8_status f8_linear_bwd(const void *dy, const f8_linear_saved *saved, int64_t M,
     int np = 0;
     F8_TRY_CUDA(launch_amax_partials(dy, M * N, bw.parts_dy, &np, *dev, st));
     F8_TRY_CUDA(launch_cast_transpose(dy, M, N, nullptr, bw.parts_dy, np, bw.amax_dy, bw.scale_dy,
-                                      dx ? bw.dy_q : nullptr, dw ? bw.dy_t : nullptr, *dev, st));
+                                      dx ? bw.dy_q : nullptr, dw ? bw.dy_t : nullptr, fdy, *dev, st));
     // dX [M,K] = q(dY) [M,N] . (q(W)^T [K,N])^T
     if (dx != nullptr)
-        F8_TRY_CUDA(launch_gemm(bw.dy_q, saved->w_t, M, K, N, bw.scale_dy, saved->scale_w, dx, *dev, st));
+        F8_TRY_CUDA(launch_gemm(bw.dy_q, saved->w_t, M, K, N, bw.scale_dy, saved->scale_w, dx, *dev, st,
+                                fdy, F8_E4M3));
     // dW [N,K] = q(dY)^T [N,M] . (q(X)^T [K,M])^T
     if (dw != nullptr)
-        F8_TRY_CUDA(launch_gemm(bw.dy_t, saved->x_t, N, K, M, bw.scale_dy, saved->scale_x, dw, *dev, st));
+        F8_TRY_CUDA(launch_gemm(bw.dy_t, saved->x_t, N, K, M, bw.scale_dy, saved->scale_x, dw, *dev, st,
+                                fdy, F8_E4M3));
     return F8_OK;
+}
+
+f8_status f8_linear_bwd(const void *dy, const f8_linear_saved *saved, int64_t M, int64_t N,
+                        int64_t K, void *dx, void *dw, void *workspace, size_t workspace_bytes,
+                        void *stream)
+{
+    return linear_bwd_impl(dy, F8_E4M3, saved, M, N, K, dx, dw, workspace, workspace_bytes, stream);
+}
+
+f8_status f8_linear_bwd_fmt(const void *dy, f8_format fmt_dy, const f8_linear_saved *saved,
+                            int64_t M, int64_t N, int64_t K, void *dx, void *dw, void *workspace,
+                            size_t workspace_bytes, void *stream)
+{
+    return linear_bwd_impl(dy, fmt_dy, saved, M, N, K, dx, dw, workspace, workspace_bytes, stream);
 }
 
 f8_status f8_last_device_status(void *stream)

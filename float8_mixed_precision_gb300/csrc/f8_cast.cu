@@ -13,7 +13,7 @@
 //
 // cast_transpose: a CTA owns a 128 x 128 tile.  Phase 1 reads it with 16-byte
 // loads (each thread 16 consecutive bf16 of one row), scales in fp32,
-// converts with the hardware's saturating RNE E4M3 conversion, writes the
+// converts with the hardware's saturating RNE E4M3 (or E5M2) conversion, writes the
 // row-major codes with 16-byte stores and parks them in a 16 KB shared tile
 // whose 16-byte chunks are XOR-swizzled by (row / 16) % 8.  Phase 2 gives each
 // thread a 16-row x 4-column block: 16 conflict-free 4-byte shared loads,
@@ -93,9 +93,12 @@ constexpr int kTile = 128;
 constexpr int kCastThreads = 256;
 constexpr int kCastThreadsMax = 256;
 
+// Largest finite value of the target format: 448 (E4M3, FMT 0) or 57344
+// (E5M2, FMT 1).
+template <int FMT>
 __device__ __forceinline__ float scale_of(float amax)
 {
-    return __fdiv_rn(448.0f, fmaxf(amax, 1e-12f));
+    return __fdiv_rn(FMT == 1 ? 57344.0f : 448.0f, fmaxf(amax, 1e-12f));
 }
 
 // Maximum of the partial maxima (fp32 bit patterns of non-negative values),
@@ -117,34 +120,41 @@ __device__ __forceinline__ float reduce_partials(const unsigned *partials, int n
     return __uint_as_float(m);
 }
 
+// Saturating RNE conversion of two fp32 values to two FP8 codes (lo in the
+// low byte).
+template <int FMT>
 __device__ __forceinline__ uint16_t cvt2(float lo, float hi)
 {
-    return static_cast<uint16_t>(
-        __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+    return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE,
+                                                          FMT == 1 ? __NV_E5M2 : __NV_E4M3));
 }
 
-__device__ __forceinline__ uint32_t bf16x2_to_e4m3x2(uint32_t w, float s)
+template <int FMT>
+__device__ __forceinline__ uint32_t bf16x2_to_fp8x2(uint32_t w, float s)
 {
     const float lo = __uint_as_float(w << 16);
     const float hi = __uint_as_float(w & 0xFFFF0000u);
-    return cvt2(__fmul_rn(lo, s), __fmul_rn(hi, s));
+    return cvt2<FMT>(__fmul_rn(lo, s), __fmul_rn(hi, s));
 }
 
-// 8 bf16 (one uint4) -> 8 E4M3 codes (one uint2), element order preserved.
+// 8 bf16 (one uint4) -> 8 FP8 codes (one uint2), element order preserved.
+template <int FMT>
 __device__ __forceinline__ uint2 cvt8(uint4 v, float s)
 {
     uint2 r;
-    r.x = bf16x2_to_e4m3x2(v.x, s) | (bf16x2_to_e4m3x2(v.y, s) << 16);
-    r.y = bf16x2_to_e4m3x2(v.z, s) | (bf16x2_to_e4m3x2(v.w, s) << 16);
+    r.x = bf16x2_to_fp8x2<FMT>(v.x, s) | (bf16x2_to_fp8x2<FMT>(v.y, s) << 16);
+    r.y = bf16x2_to_fp8x2<FMT>(v.z, s) | (bf16x2_to_fp8x2<FMT>(v.w, s) << 16);
     return r;
 }
 
+template <int FMT>
 __device__ __forceinline__ uint8_t cvt1(uint16_t b, float s)
 {
     const float v = __fmul_rn(__uint_as_float(static_cast<uint32_t>(b) << 16), s);
-    return static_cast<uint8_t>(cvt2(v, 0.0f) & 0xFFu);
+    return static_cast<uint8_t>(cvt2<FMT>(v, 0.0f) & 0xFFu);
 }
 
+template <int FMT>
 __global__ void __launch_bounds__(kCastThreads)
 cast_transpose_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
                       const float *__restrict__ amax, const unsigned *__restrict__ partials,
@@ -155,7 +165,7 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols
     griddep_wait();
     griddep_launch_dependents();
     const float a = partials != nullptr ? reduce_partials(partials, nparts) : *amax;
-    const float s = scale_of(a);
+    const float s = scale_of<FMT>(a);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (scale_out != nullptr)
             *scale_out = s;
@@ -181,7 +191,7 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols
                 const uint16_t *src = x + (r0 + row) * cols + c0 + ch * 16;
                 const uint4 v0 = __ldg(reinterpret_cast<const uint4 *>(src));
                 const uint4 v1 = __ldg(reinterpret_cast<const uint4 *>(src + 8));
-                const uint2 a = cvt8(v0, s), b = cvt8(v1, s);
+                const uint2 a = cvt8<FMT>(v0, s), b = cvt8<FMT>(v1, s);
                 const uint4 codes = make_uint4(a.x, a.y, b.x, b.y);
                 if (q != nullptr)
                     *reinterpret_cast<uint4 *>(q + (r0 + row) * cols + c0 + ch * 16) = codes;
@@ -225,7 +235,7 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols
             for (int e = t; e < kTile * kTile; e += kCastThreads) {
                 const int64_t r = r0 + e / kTile, c = c0 + e % kTile;
                 if (r < rows && c < cols) {
-                    const uint8_t b = cvt1(x[r * cols + c], s);
+                    const uint8_t b = cvt1<FMT>(x[r * cols + c], s);
                     if (q != nullptr)
                         q[r * cols + c] = b;
                     if (qt != nullptr)
@@ -257,7 +267,7 @@ const Occupancy &occupancy(const DeviceInfo &dev)
         o.amax_atomic = n > 0 ? n : 1;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, amax_kernel<true>, kAmaxThreads, 0);
         o.amax_partials = n > 0 ? n : 1;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cast_transpose_kernel, kCastThreads, 0);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cast_transpose_kernel<0>, kCastThreads, 0);
         o.cast = n > 0 ? n : 1;
     }
     return o;
@@ -308,7 +318,7 @@ cudaError_t launch_amax_partials(const void *x, int64_t n, unsigned *partials, i
 
 cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, const float *amax,
                                   const unsigned *partials, int nparts, float *amax_out,
-                                  float *scale_out, uint8_t *q, uint8_t *q_t,
+                                  float *scale_out, uint8_t *q, uint8_t *q_t, int fmt,
                                   const DeviceInfo &dev, cudaStream_t stream)
 {
     const int64_t ntiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
@@ -319,7 +329,8 @@ cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, con
     if (blocks < 1)
         blocks = 1;
     const int vector_ok = (rows % 16 == 0) && (cols % 16 == 0);
-    return launch_pdl(cast_transpose_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kCastThreads),
+    return launch_pdl(fmt == 1 ? cast_transpose_kernel<1> : cast_transpose_kernel<0>,
+                      dim3(static_cast<unsigned>(blocks)), dim3(kCastThreads),
                       0, stream, static_cast<const uint16_t *>(x), rows, cols, amax, partials, nparts,
                       amax_out, scale_out, q, q_t, vector_ok);
 }

@@ -160,7 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
             const __grid_constant__ CUtensorMap tma_c, __nv_bfloat16 *__restrict__ c, int M, int N,
             int K, const float *__restrict__ sa, const float *__restrict__ sb,
-            unsigned *__restrict__ status, uint64_t limit_ns, int group_m, int tma_store)
+            unsigned *__restrict__ status, uint64_t limit_ns, int group_m, int tma_store,
+            uint32_t idesc)
 {
     using C = Cfg<BN, STAGES, PAIR>;
     extern __shared__ uint8_t smem_raw[];
@@ -298,7 +299,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
     } else if (warp == 1) {
         if (leader && lane == 0) {
             // ------------------------------------------------ MMA issuer
-            const uint32_t idesc = idesc_e4m3_f32(C::kTileM, BN);
             uint32_t stage = 0, phase = 0;
             bool stop = false;
             int local = 0;
@@ -460,7 +460,7 @@ bool make_map(CUtensorMap *map, CUtensorMapDataType dtype, int esize, const void
 template <int BN, int STAGES, bool PAIR>
 cudaError_t run_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
                      const float *sa, const float *sb, void *c, const DeviceInfo &dev,
-                     cudaStream_t stream)
+                     cudaStream_t stream, int fa, int fb)
 {
     using C = Cfg<BN, STAGES, PAIR>;
     CUtensorMap ma, mb, mc;
@@ -490,7 +490,9 @@ cudaError_t run_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, i
                               dim3(kThreads), C::kSmemBytes, stream, PAIR ? 2u : 1u, ma, mb, mc,
                               static_cast<__nv_bfloat16 *>(c), static_cast<int>(M),
                               static_cast<int>(N), static_cast<int>(K), sa, sb, dev.status,
-                              wait_limit_ns(), group_m, tma_store);
+                              wait_limit_ns(), group_m, tma_store,
+                              idesc_f8_f32(C::kTileM, BN, static_cast<uint32_t>(fa),
+                                           static_cast<uint32_t>(fb)));
 }
 
 constexpr int kVariantSingle = 1;
@@ -513,11 +515,11 @@ int gemm_variant(int64_t M, const DeviceInfo &dev)
 
 cudaError_t launch_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
                         const float *sa, const float *sb, void *c, const DeviceInfo &dev,
-                        cudaStream_t stream)
+                        cudaStream_t stream, int fa, int fb)
 {
     if (gemm_variant(M, dev) == kVariantPair)
-        return run_gemm<256, 6, true>(a, b, M, N, K, sa, sb, c, dev, stream);
-    return run_gemm<256, 4, false>(a, b, M, N, K, sa, sb, c, dev, stream);
+        return run_gemm<256, 6, true>(a, b, M, N, K, sa, sb, c, dev, stream, fa, fb);
+    return run_gemm<256, 4, false>(a, b, M, N, K, sa, sb, c, dev, stream, fa, fb);
 }
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, const DeviceInfo &dev, cudaStream_t stream)

@@ -87,16 +87,18 @@ cudaError_t launch_amax_partials(const void *x, int64_t n, unsigned *partials, i
 // amax comes either from `amax` (one fp32) or, if `partials` is non-null,
 // from the maximum of `nparts` partial maxima, which is then also stored to
 // `amax_out` (if non-null).
+// fmt: 0 = E4M3 (scale 448/amax), 1 = E5M2 (scale 57344/amax).
 cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, const float *amax,
                                   const unsigned *partials, int nparts, float *amax_out,
-                                  float *scale_out, uint8_t *q, uint8_t *q_t,
+                                  float *scale_out, uint8_t *q, uint8_t *q_t, int fmt,
                                   const DeviceInfo &dev, cudaStream_t stream);
 
 // C[M,N] = bf16(A[M,K] B[N,K]^T / (sa sb)); M, N, K >= 1, K % 16 == 0.
+// fa, fb: operand formats (0 = E4M3, 1 = E5M2).
 // Returns cudaErrorNotSupported if the tensor-map encoder is unavailable.
 cudaError_t launch_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
                         const float *sa, const float *sb, void *c, const DeviceInfo &dev,
-                        cudaStream_t stream);
+                        cudaStream_t stream, int fa = 0, int fb = 0);
 
 // One CTA waiting on an mbarrier that is never signalled (failure-path test).
 cudaError_t launch_wait_selftest(uint64_t limit_ns, const DeviceInfo &dev, cudaStream_t stream);

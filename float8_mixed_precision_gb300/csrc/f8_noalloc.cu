@@ -95,10 +95,10 @@ extern "C" f8_status f8_linear_fwd_noalloc(const void *x, const void *w, int64_t
         e = f8::launch_amax(w, N * K, saved->amax_w, *dev, st);
     if (e == cudaSuccess)
         e = f8::launch_cast_transpose(x, M, K, saved->amax_x, nullptr, 0, nullptr, saved->scale_x,
-                                      x_q, saved->x_t, *dev, st);
+                                      x_q, saved->x_t, 0, *dev, st);
     if (e == cudaSuccess)
         e = f8::launch_cast_transpose(w, N, K, saved->amax_w, nullptr, 0, nullptr, saved->scale_w,
-                                      w_q, saved->w_t, *dev, st);
+                                      w_q, saved->w_t, 0, *dev, st);
     if (e == cudaSuccess)
         e = f8::launch_gemm(x_q, w_q, M, N, K, saved->scale_x, saved->scale_w, y, *dev, st);
     if (e == cudaErrorNotSupported)

@@ -191,11 +191,12 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
 }
 
 // Instruction descriptor of kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B
-// E4M3 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 in
-// bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t m, uint32_t n)
+// formats in bits 7-9 and 10-12 (E4M3 = 0, E5M2 = 1), both K-major (bits 15,
+// 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f8_f32(uint32_t m, uint32_t n, uint32_t fa = 0,
+                                                    uint32_t fb = 0)
 {
-    return (1u << 4) | ((n >> 3) << 17) | ((m >> 4) << 24);
+    return (1u << 4) | (fa << 7) | (fb << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 } // namespace f8

@@ -59,6 +59,18 @@ typedef enum {
 } f8_status;
 
 /*
+ * FP8 formats of "FP8 Formats for Deep Learning" (the paper the torchtitan
+ * walkthrough, Part XI item 9, cites for torchtitan's Float8 training):
+ *   F8_E4M3  1-4-3, bias 7, no infinities, largest finite 448;
+ *   F8_E5M2  1-5-2, bias 15, IEEE-style inf/NaN, largest finite 57344.
+ * The five calls of the path use E4M3 for X, W and dY; the _fmt variants
+ * below also take E5M2, the wider-range format the paper suggests for
+ * gradients.  Scales are then fmax / max(amax, 1e-12), fmax the format's
+ * largest finite value, and conversions saturate to +-fmax.
+ */
+typedef enum { F8_E4M3 = 0, F8_E5M2 = 1 } f8_format;
+
+/*
  * amax_out[0] = max_i |x[i]| over n bf16 values, as fp32 (exact).
  *   x:        device, n bf16 values, 16-byte aligned.  n == 0 gives 0.
  *   amax_out: device, one fp32; overwritten (the call zeroes it first).
@@ -105,6 +117,11 @@ f8_status f8_quantize(const void *x, int64_t rows, int64_t cols, float *amax_out
                       float *scale_out, uint8_t *q, uint8_t *q_t, void *workspace,
                       size_t workspace_bytes, void *stream);
 
+/* f8_quantize into format `fmt` (E4M3: identical to f8_quantize). */
+f8_status f8_quantize_fmt(const void *x, int64_t rows, int64_t cols, f8_format fmt,
+                          float *amax_out, float *scale_out, uint8_t *q, uint8_t *q_t,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
 /*
  * C = bf16( A B^T / (scale_a * scale_b) ), fp32 accumulation on tcgen05.
  *   a:       device E4M3 [M, K] row-major (K contiguous), 16-byte aligned.
@@ -116,6 +133,12 @@ f8_status f8_quantize(const void *x, int64_t rows, int64_t cols, float *amax_out
  */
 f8_status f8_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
                   const float *scale_a, const float *scale_b, void *c, void *stream);
+
+/* f8_gemm with the operands' formats given (any mix of E4M3 and E5M2; one
+ * tcgen05.mma kind::f8f6f4 takes both). */
+f8_status f8_gemm_fmt(const uint8_t *a, f8_format fmt_a, const uint8_t *b, f8_format fmt_b,
+                      int64_t M, int64_t N, int64_t K, const float *scale_a,
+                      const float *scale_b, void *c, void *stream);
 
 /*
  * What the forward pass leaves for the backward pass.  All members are
@@ -194,6 +217,14 @@ f8_status f8_linear_bwd(const void *dy, const f8_linear_saved *saved, int64_t M,
 #define F8_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 f8_status f8_linear_fwd_noalloc(const void *x, const void *w, int64_t M, int64_t N, int64_t K,
                                 void *y, const f8_linear_saved *saved, void *stream);
+
+/*
+ * f8_linear_bwd with dY quantised to `fmt_dy` (E5M2: scale 57344/amax(dY);
+ * dgrad and wgrad then run E5M2 x E4M3 GEMMs).  X and W stay E4M3.
+ */
+f8_status f8_linear_bwd_fmt(const void *dy, f8_format fmt_dy, const f8_linear_saved *saved,
+                            int64_t M, int64_t N, int64_t K, void *dx, void *dw, void *workspace,
+                            size_t workspace_bytes, void *stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status
