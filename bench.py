@@ -219,8 +219,15 @@ def run_ours(args, world, rank, local):
     f8.lib()
     name, lins = wl.workload(args.config)
     dy_fmt = f8.F8_E5M2 if args.dy_format == "e5m2" else f8.F8_E4M3
-    layers = [Linear8(f8, lin, wl.linear_inputs(args.config, i), device, dy_fmt)
-              for i, lin in enumerate(lins)]
+    if args.fuse_shared_inputs:
+        groups = wl.fused_groups(args.config)
+        lins = [g for g, _ in groups]
+        name += " (shared inputs fused: " + ", ".join(l.name for l in lins) + ")"
+        layers = [Linear8(f8, g, wl.fused_group_inputs(args.config, idx), device, dy_fmt)
+                  for g, idx in groups]
+    else:
+        layers = [Linear8(f8, lin, wl.linear_inputs(args.config, i), device, dy_fmt)
+                  for i, lin in enumerate(lins)]
     flops_step = sum(l.flops for l in lins)
     stream = torch.cuda.current_stream()
 
@@ -555,6 +562,9 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--ref-rows", type=int, default=128)
+    ap.add_argument("--fuse-shared-inputs", action="store_true",
+                    help="merge the linears that read one input (q/k/v, w1/w3) into one linear "
+                         "with the concatenated weight and a tensorwise scale over it")
     ap.add_argument("--dy-format", default="e4m3", choices=["e4m3", "e5m2"],
                     help="FP8 format of dY in the backward pass (X and W stay E4M3)")
     ap.add_argument("--kernel-bench", type=int, default=1,

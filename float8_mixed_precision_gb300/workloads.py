@@ -23,6 +23,9 @@ torchtitan walkthrough's llama3_8b training run):
              the w2 input are Student-t(nu=3) with 0.1% of the entries
              (uniform, without replacement) multiplied by 100; W ~N(0,0.02)
 The second parameter of N(mu, sigma) is the standard deviation.
+Shared inputs (fused_groups): q, k, v read one X, as do w1 and w3; merging
+each group into one linear with the concatenated weight leaves the work
+unchanged and quantises the shared X once.
 Seed of tensor t (X=0, W=1, dY=2, a=3, b=4) of linear l in workload c:
 1000*(c-1) + 10*l + t, so workload 1 starts from seed 0.
 """
@@ -140,6 +143,36 @@ def linear_inputs(c: int, l: int, lin: Linear | None = None) -> dict[str, torch.
     w = normal((lin.N, lin.K), lin.w_std, seed_of(c, l, 1))
     dy = _activation(lin.dy_kind, (lin.M, lin.N), lin.dy_std, c, l, 2)
     return {"x": x, "w": w, "dy": dy}
+
+
+# Linears of a workload that read the same input in a Llama block: q, k and v
+# read the attention-norm output, w1 and w3 the FFN-norm output.
+SHARED_INPUT_GROUPS = {2: [["wq", "wk", "wv"], ["wo"]],
+                       3: [["w1", "w3"], ["w2"]],
+                       5: [["wq", "wk", "wv"], ["wo"], ["w1", "w3"], ["w2"]]}
+
+
+def fused_groups(c: int) -> list[tuple[Linear, list[int]]]:
+    """Workload ``c`` with the linears that share an input merged into one
+    linear with the concatenated weight [sum N_i, K] (same total work): each
+    entry is (merged Linear, indices of the member linears)."""
+    lins = WORKLOADS[c][1]
+    by_name = {l.name: i for i, l in enumerate(lins)}
+    out = []
+    for names in SHARED_INPUT_GROUPS[c]:
+        idx = [by_name[n] for n in names]
+        first = lins[idx[0]]
+        out.append((Linear("+".join(names), first.M, first.K, sum(lins[i].N for i in idx),
+                           first.x_kind, first.dy_kind, first.x_std, first.w_std, first.dy_std), idx))
+    return out
+
+
+def fused_group_inputs(c: int, idx: list[int]) -> dict[str, torch.Tensor]:
+    """X of the group's first linear (the shared input), the members' W
+    stacked along N, and their dY concatenated along N."""
+    parts = [linear_inputs(c, i) for i in idx]
+    return {"x": parts[0]["x"], "w": torch.cat([p["w"] for p in parts], 0),
+            "dy": torch.cat([p["dy"] for p in parts], 1)}
 
 
 def custom_linear(M: int, K: int, N: int, seed: int, x_std=1.0, w_std=0.02, dy_std=1.0):

@@ -126,3 +126,31 @@ def test_workload_linear_full_size(f8, c, l):
     check_close(dw[torch.from_numpy(rows).to(DEV)], ref, what="dW rows")
     ref = oracle.gemm_cols(qdy["qt"], qx["qt"], qdy["scale"], qx["scale"], cols)
     check_close(dw[:, torch.from_numpy(cols).to(DEV)].t().contiguous(), ref, what="dW cols")
+
+
+FUSED = [(c, gi) for c in (2, 3) for gi in range(len(wl.fused_groups(c)))
+         if len(wl.fused_groups(c)[gi][1]) > 1]
+
+
+@pytest.mark.parametrize("c,gi", FUSED, ids=[f"w{c}-{wl.fused_groups(c)[gi][0].name}" for c, gi in FUSED])
+def test_fused_shared_input_group_full_size(f8, c, gi):
+    """q/k/v (and w1/w3) read one input: merged into one linear with the
+    concatenated weight, the path is the same linear with a wider N."""
+    lin, idx = wl.fused_groups(c)[gi]
+    d = wl.fused_group_inputs(c, idx)
+    assert d["w"].shape == (lin.N, lin.K) and d["dy"].shape == (lin.M, lin.N)
+    y, dx, dw, saved = _run_gpu(f8, d["x"], d["w"], d["dy"])
+    qx = oracle.quantize(wl.bits(d["x"]))
+    qw = oracle.quantize(wl.bits(d["w"]))
+    qdy = oracle.quantize(wl.bits(d["dy"]))
+    _check_saved(saved, {"x": qx, "w": qw})
+    rng = np.random.default_rng(77 + gi)
+    M, N, K = lin.M, lin.N, lin.K
+    rows = _bands(M, 128, rng)
+    check_close(y[torch.from_numpy(rows).to(DEV)],
+                oracle.gemm_rows(qx["q"], qw["q"], qx["scale"], qw["scale"], rows), what="Y rows")
+    check_close(dx[torch.from_numpy(rows).to(DEV)],
+                oracle.gemm_rows(qdy["q"], qw["qt"], qdy["scale"], qw["scale"], rows), what="dX rows")
+    rows = _bands(N, 128, rng)
+    check_close(dw[torch.from_numpy(rows).to(DEV)],
+                oracle.gemm_rows(qdy["qt"], qx["qt"], qdy["scale"], qx["scale"], rows), what="dW rows")
