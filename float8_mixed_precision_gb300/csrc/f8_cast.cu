@@ -154,6 +154,42 @@ __device__ __forceinline__ uint8_t cvt1(uint16_t b, float s)
     return static_cast<uint8_t>(cvt2<FMT>(v, 0.0f) & 0xFFu);
 }
 
+// Phase 2 of a full tile: thread t takes a 16-row x 4-column block of the
+// parked codes (16 conflict-free 4-byte shared loads), transposes it with
+// PRMT and writes four 16-byte column segments of q^T (8 consecutive threads
+// write 128 contiguous bytes of one column).
+__device__ __forceinline__ void transpose_out(const uint8_t *tile, uint8_t *__restrict__ qt,
+                                              int64_t rows, int64_t r0, int64_t c0, int t)
+{
+    const int rs = t & 7;          // 16-row segment
+    const int cg = t >> 3;         // 4-column group (0..31)
+    const int chunk = cg >> 2;     // 16-byte chunk holding the 4 columns
+    const int word = cg & 3;       // 4-byte word within the chunk
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int row = rs * 16 + i;
+        const int pch = chunk ^ ((row >> 4) & 7);
+        w[i] = *reinterpret_cast<const uint32_t *>(tile + row * kTile + pch * 16 + word * 4);
+    }
+    uint32_t col[4][4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const uint32_t a = w[4 * g], b = w[4 * g + 1], c = w[4 * g + 2], d = w[4 * g + 3];
+        const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(c, d, 0x5140);
+        const uint32_t t2 = __byte_perm(a, b, 0x7362), t3 = __byte_perm(c, d, 0x7362);
+        col[0][g] = __byte_perm(t0, t1, 0x5410);
+        col[1][g] = __byte_perm(t0, t1, 0x7632);
+        col[2][g] = __byte_perm(t2, t3, 0x5410);
+        col[3][g] = __byte_perm(t2, t3, 0x7632);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint8_t *dst = qt + (c0 + cg * 4 + j) * rows + r0 + rs * 16;
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
+    }
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(kCastThreads)
 cast_transpose_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
@@ -200,34 +236,7 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols
             }
             if (qt != nullptr) {
                 __syncthreads();
-                // ---- phase 2: 16 rows x 4 columns per thread, transposed out
-                const int rs = t & 7;          // 16-row segment
-                const int cg = t >> 3;         // 4-column group (0..31)
-                const int chunk = cg >> 2;     // 16-byte chunk holding the 4 columns
-                const int word = cg & 3;       // 4-byte word within the chunk
-                uint32_t w[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int row = rs * 16 + i;
-                    const int pch = chunk ^ ((row >> 4) & 7);
-                    w[i] = *reinterpret_cast<const uint32_t *>(tile + row * kTile + pch * 16 + word * 4);
-                }
-                uint32_t col[4][4];
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const uint32_t a = w[4 * g], b = w[4 * g + 1], c = w[4 * g + 2], d = w[4 * g + 3];
-                    const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(c, d, 0x5140);
-                    const uint32_t t2 = __byte_perm(a, b, 0x7362), t3 = __byte_perm(c, d, 0x7362);
-                    col[0][g] = __byte_perm(t0, t1, 0x5410);
-                    col[1][g] = __byte_perm(t0, t1, 0x7632);
-                    col[2][g] = __byte_perm(t2, t3, 0x5410);
-                    col[3][g] = __byte_perm(t2, t3, 0x7632);
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint8_t *dst = qt + (c0 + cg * 4 + j) * rows + r0 + rs * 16;
-                    *reinterpret_cast<uint4 *>(dst) = make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
-                }
+                transpose_out(tile, qt, rows, r0, c0, t);
             }
             __syncthreads();
         } else {
@@ -246,13 +255,111 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols
     }
 }
 
+// The same cast for tensors whose sides are multiples of 128, with the bf16
+// tiles brought in by TMA: a CTA keeps kInStages 32 KB input buffers and
+// loads tiles k+1 .. k+kInStages-1 while it converts and transposes tile k,
+// so the work of a tile overlaps the latency of the next ones.  Phase 1
+// reads the tile from shared memory (16 bytes per thread, consecutive
+// threads on consecutive bytes).  Two CTAs fit on an SM.
+constexpr int kInBytes = kTile * kTile * 2;
+constexpr int kInStages = 3;
+constexpr int kTmaCastSmem = kInStages * kInBytes + kTile * kTile + 64 + 128;
+
+template <int FMT>
+__global__ void __launch_bounds__(kCastThreads)
+cast_transpose_tma_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t rows, int64_t cols,
+                          const float *__restrict__ amax, const unsigned *__restrict__ partials,
+                          int nparts, float *__restrict__ amax_out, float *__restrict__ scale_out,
+                          uint8_t *__restrict__ q, uint8_t *__restrict__ qt,
+                          unsigned *__restrict__ status, uint64_t limit_ns)
+{
+    extern __shared__ uint8_t cast_smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(cast_smem_raw) + 127) &
+                                              ~static_cast<uintptr_t>(127));
+    uint8_t *tile = sm + kInStages * kInBytes;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(tile + kTile * kTile);
+    __shared__ int abort_flag;
+    const int t = threadIdx.x;
+    if (t == 0) {
+        for (int b = 0; b < kInStages; ++b)
+            mbar_init(&bar[b], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmap_x);
+    }
+    __syncthreads();
+    griddep_wait();
+    griddep_launch_dependents();
+    const float a = partials != nullptr ? reduce_partials(partials, nparts) : *amax;
+    const float s = scale_of<FMT>(a);
+    if (blockIdx.x == 0 && t == 0) {
+        if (scale_out != nullptr)
+            *scale_out = s;
+        if (amax_out != nullptr)
+            *amax_out = a;
+    }
+
+    const int64_t tiles_c = cols / kTile;
+    const int64_t ntiles = (rows / kTile) * tiles_c;
+    const int64_t nmine = ntiles > blockIdx.x ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    auto issue = [&](int64_t k) {
+        const int64_t tix = blockIdx.x + k * gridDim.x;
+        const int b = static_cast<int>(k % kInStages);
+        fence_proxy_async_shared();  // earlier generic reads of this buffer come first
+        mbar_arrive_expect_tx(&bar[b], kInBytes);
+        tma_load_2d(sm + b * kInBytes, &tmap_x, &bar[b], static_cast<int32_t>((tix % tiles_c) * kTile),
+                    static_cast<int32_t>((tix / tiles_c) * kTile));
+    };
+    if (t == 0)
+        for (int64_t j = 0; j < nmine && j < kInStages - 1; ++j)
+            issue(j);
+    int64_t k = 0;
+    for (; k < nmine; ++k) {
+        if (t == 0 && k + kInStages - 1 < nmine)
+            issue(k + kInStages - 1);  // its buffer was released at the end of iteration k - 1
+        const int b = static_cast<int>(k % kInStages);
+        if (!mbar_wait(&bar[b], static_cast<uint32_t>((k / kInStages) & 1), &abort_flag, limit_ns)) {
+            abort_flag = 1;
+            atomicOr(status, kStatusTimeout);
+        }
+        if (__syncthreads_or(abort_flag))
+            break;
+        const int64_t tix = blockIdx.x + k * gridDim.x;
+        const int64_t r0 = (tix / tiles_c) * kTile;
+        const int64_t c0 = (tix % tiles_c) * kTile;
+        const uint8_t *src = sm + b * kInBytes;
+        // ---- phase 1: 8 passes of 16 rows; thread t converts 8 consecutive bf16
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const int idx = p * kCastThreads + t;
+            const int row = idx >> 4, c8 = idx & 15;
+            const uint4 v = *reinterpret_cast<const uint4 *>(src + row * (kTile * 2) + c8 * 16);
+            const uint2 codes = cvt8<FMT>(v, s);
+            if (q != nullptr)
+                *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + c8 * 8) = codes;
+            const int pch = (c8 >> 1) ^ ((row >> 4) & 7);
+            *reinterpret_cast<uint2 *>(tile + row * kTile + pch * 16 + (c8 & 1) * 8) = codes;
+        }
+        __syncthreads();
+        if (qt != nullptr)
+            transpose_out(tile, qt, rows, r0, c0, t);
+        __syncthreads();  // the input buffer and the parked tile are free again
+    }
+    if (k < nmine && t == 0) {
+        // gave up: the loads still in flight must land before the CTA exits
+        for (int64_t j = k; j < nmine && j < k + kInStages; ++j)
+            mbar_wait(&bar[j % kInStages], static_cast<uint32_t>((j / kInStages) & 1), nullptr,
+                      limit_ns);
+    }
+}
+
 } // namespace
 
 namespace {
 
 // Resident CTAs per SM of each kernel on each device (occupancy API, cached).
 struct Occupancy {
-    int amax_atomic = 0, amax_partials = 0, cast = 0;
+    int amax_atomic = 0, amax_partials = 0, cast = 0, cast_tma = 0;
 };
 std::mutex g_occ_mutex;
 Occupancy g_occ[64];
@@ -269,6 +376,13 @@ const Occupancy &occupancy(const DeviceInfo &dev)
         o.amax_partials = n > 0 ? n : 1;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cast_transpose_kernel<0>, kCastThreads, 0);
         o.cast = n > 0 ? n : 1;
+        cudaFuncSetAttribute(cast_transpose_tma_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTmaCastSmem);
+        cudaFuncSetAttribute(cast_transpose_tma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTmaCastSmem);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cast_transpose_tma_kernel<0>, kCastThreads,
+                                                      kTmaCastSmem);
+        o.cast_tma = n > 0 ? n : 1;
     }
     return o;
 }
@@ -322,6 +436,19 @@ cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, con
                                   const DeviceInfo &dev, cudaStream_t stream)
 {
     const int64_t ntiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
+    CUtensorMap map;
+    if (rows % kTile == 0 && cols % kTile == 0 && rows > 0 && cols > 0 && cast_tma_enabled() &&
+        make_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, rows, cols, kTile, kTile,
+                           CU_TENSOR_MAP_SWIZZLE_NONE)) {
+        int64_t blocks = ntiles;
+        const int64_t cap = static_cast<int64_t>(dev.sm_count) * occupancy(dev).cast_tma;
+        if (blocks > cap)
+            blocks = cap;
+        return launch_pdl(fmt == 1 ? cast_transpose_tma_kernel<1> : cast_transpose_tma_kernel<0>,
+                          dim3(static_cast<unsigned>(blocks)), dim3(kCastThreads), kTmaCastSmem,
+                          stream, map, rows, cols, amax, partials, nparts, amax_out, scale_out, q,
+                          q_t, dev.status, wait_limit_ns());
+    }
     int64_t blocks = ntiles;
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * occupancy(dev).cast;
     if (blocks > cap)

@@ -513,6 +513,22 @@ int gemm_variant(int64_t M, const DeviceInfo &dev)
 
 } // namespace
 
+bool make_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, int esize, const void *ptr,
+                        int64_t rows, int64_t cols, int box_cols, int box_rows,
+                        CUtensorMapSwizzle swizzle)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr)
+        return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * esize)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, dtype, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
                         const float *sa, const float *sb, void *c, const DeviceInfo &dev,
                         cudaStream_t stream, int fa, int fb)

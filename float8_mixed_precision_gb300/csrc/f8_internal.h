@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cstdlib>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <utility>
 
@@ -23,6 +24,20 @@ const DeviceInfo *device_info();
 
 // Time limit of the GEMM pipeline's device waits.
 uint64_t wait_limit_ns();
+
+// 2-D row-major tensor [rows, cols] of `esize`-byte elements as a TMA tensor
+// map with a box_cols x box_rows box; false if the driver entry point is
+// missing or the encoding is refused.
+bool make_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, int esize, const void *ptr,
+                        int64_t rows, int64_t cols, int box_cols, int box_rows,
+                        CUtensorMapSwizzle swizzle);
+
+// The TMA-fed cast is used unless F8_CAST_TMA=0 (for measurement).
+inline bool cast_tma_enabled()
+{
+    const char *e = std::getenv("F8_CAST_TMA");
+    return e == nullptr || e[0] != '0';
+}
 
 // Programmatic dependent launch is on unless F8_PDL=0.
 inline bool pdl_enabled()
