@@ -47,6 +47,7 @@ UNIT = "TFLOP/s"
 FP8_NOMINAL_TFLOPS = 4500.0
 FP8_PER_BF16 = 2.0          # nominal dense FP8 : BF16 tensor throughput
 HBM_NOMINAL_GBS = 8000.0
+REF_BUDGET_S = 60.0   # timed seconds of the CPU reference arm
 
 # DRAM bytes (read + write) of the 12 GEMM launches of one attention fwd+bwd
 # step, from one ncu capture (profiles/gemm_traffic_attn8b.md), valid for the
@@ -520,32 +521,89 @@ def cpu_baseline(config: int, rows: int):
                        f"Y, dX and dW; value = GEMM flops of the sampled rows / wall time")}
 
 
+class OracleSampler:
+    """Bounded samples of the oracle's work on one workload, for the CPU
+    reference arm.  Inputs and their full quantisation are built once per
+    linear (untimed); a timed sample is the oracle's amax + scale + cast of
+    the first `frac` of the rows of X, W and dY plus `rows` sampled output
+    rows of each of the three GEMMs, so the sample keeps the step's mix of
+    quantisation and GEMM work."""
+
+    def __init__(self, config: int):
+        from float8_mixed_precision_gb300 import workloads as wl
+        self.config = config
+        self.lins = wl.workload(config)[1]
+        self.cache = {}
+
+    def _prep(self, i):
+        if i not in self.cache:
+            import oracle
+            from float8_mixed_precision_gb300 import workloads as wl
+            d = wl.linear_inputs(self.config, i)
+            b = {k: wl.bits(v) for k, v in d.items()}
+            self.cache[i] = (b, {k: oracle.quantize(v) for k, v in b.items()})
+        return self.cache[i]
+
+    def sample(self, i: int, rows: int):
+        import numpy as np
+
+        import oracle
+        b, q = self._prep(i)
+        lin = self.lins[i]
+        M, N, K = lin.M, lin.N, lin.K
+        rng = np.random.default_rng(rows + 7 * i)
+        r_m = np.sort(rng.choice(M, size=min(rows, M), replace=False))
+        r_n = np.sort(rng.choice(N, size=min(rows, N), replace=False))
+        frac = len(r_m) / M
+        t = time.perf_counter()
+        for key in ("x", "w", "dy"):
+            part = b[key][: max(1, int(round(frac * b[key].shape[0])))]
+            oracle.quantize(part)
+        qx, qw, qdy = q["x"], q["w"], q["dy"]
+        oracle.gemm_rows(qx["q"], qw["q"], qx["scale"], qw["scale"], r_m)
+        oracle.gemm_rows(qdy["q"], qw["qt"], qdy["scale"], qw["scale"], r_m)
+        oracle.gemm_rows(qdy["qt"], qx["qt"], qdy["scale"], qx["scale"], r_n)
+        sec = time.perf_counter() - t
+        flops = 2 * (len(r_m) * N * K + len(r_m) * K * N + len(r_n) * K * M)
+        return flops, sec
+
+
 def run_reference(args, world, rank):
-    """--impl reference: the CPU oracle, as it stands, timed on the host cores."""
+    """--impl reference: the CPU oracle, as it stands, timed on the host cores.
+    The per-step sample is sized so that the timed steps take about
+    REF_BUDGET_S seconds whatever --steps is."""
     import oracle
     from float8_mixed_precision_gb300 import workloads as wl
     name, lins = wl.workload(args.config)
     if rank != 0:
         return 0
     oracle.build()
-    rows = args.ref_rows
+    sampler = OracleSampler(args.config)
+    for i in range(len(lins)):
+        sampler._prep(i)
+    # calibrate: seconds per sampled row on this host
+    f0, t0 = sampler.sample(0, 16)
+    per_row = t0 / 16
+    target = max(0.02, min(5.0, REF_BUDGET_S / max(1, args.steps)))
+    rows = int(max(1, min(lins[0].M, target / per_row)))
     for i in range(args.warmup):
-        oracle_sample(args.config, i % len(lins), max(1, rows // 8))
+        sampler.sample(i % len(lins), max(1, rows // 4))
     flops = sec = 0.0
     for i in range(args.steps):
-        f, s = oracle_sample(args.config, i % len(lins), rows)
+        f, s_ = sampler.sample(i % len(lins), rows)
         flops += f
-        sec += s
+        sec += s_
     value = flops / sec / 1e12
+    sample = (f"per step one linear (rotating over {', '.join(l.name for l in lins)}): amax, scale "
+              f"and cast of the first {rows}/{lins[0].M} of the rows of X, W, dY and {rows} sampled "
+              f"output rows of each of Y, dX, dW; value = GEMM flops of the sampled rows / time")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
             "data": "synthetic", "impl": "reference",
             "config": {"workload": name, "linears": [l.name for l in lins], "M": lins[0].M},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
-                             "kind": "oracle",
-                             "sample": f"per step one linear (rotating): amax/scale/cast of X, W, dY "
-                                       f"in full + {rows} sampled rows of each GEMM"},
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
