@@ -52,7 +52,7 @@ REF_BUDGET_S = 60.0   # timed seconds of the CPU reference arm
 # DRAM bytes (read + write) of the 12 GEMM launches of one attention fwd+bwd
 # step, from one ncu capture (profiles/gemm_traffic_attn8b.md), valid for the
 # GEMM sources whose hash is given; reported as null once they change.
-GEMM_TRAFFIC = {"workload": 2, "bytes_per_step": 696192256, "sources_sha256_16": "9ca37434df5e9d93"}
+GEMM_TRAFFIC = {"workload": 2, "bytes_per_step": 697309952, "sources_sha256_16": "955986f4b70b25e0"}
 
 
 def gemm_sources_hash() -> str:
