@@ -8,7 +8,9 @@ cast_transpose(dY), GEMM dX = dY W, GEMM dW = dY^T X.  The metric is GEMM
 work (6 M N K flops per linear) over the whole step's time, in TFLOP/s.
 
 Inputs are seeded synthetic bf16 tensors (float8_mixed_precision_gb300.workloads),
-resident in HBM before timing.  A step's inputs (0.5 GB for the attention
+resident in HBM before timing.  By default the step (every launch of every
+linear, made through f8_linear_fwd / f8_linear_bwd) is captured once as a
+CUDA graph and replayed each timed step (--graph 0: called each step).  A step's inputs (0.5 GB for the attention
 workload) exceed the 129 MB L2, so no L2 flush is inserted between steps.
 
 The JSON line carries, besides the contract keys:
@@ -241,6 +243,20 @@ def run_ours(args, world, rank, local):
     for _ in range(args.warmup):
         for L in layers:
             L.step(f8)
+    graph = None
+    if args.graph:
+        # one whole step (every launch of every linear) captured once and replayed
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                for L in layers:
+                    L.step(f8)
+        stream.wait_stream(cap)
+        for _ in range(2):
+            graph.replay()
     st = f8.f8_last_device_status()
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {f8.f8_status_string(st)}")
@@ -250,8 +266,11 @@ def run_ours(args, world, rank, local):
     with ClockSampler(local) as clocks:
         t0.record(stream)
         for _ in range(args.steps):
-            for L in layers:
-                L.step(f8)
+            if graph is not None:
+                graph.replay()
+            else:
+                for L in layers:
+                    L.step(f8)
         t1.record(stream)
         torch.cuda.synchronize()
     barrier()
@@ -620,6 +639,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--ref-rows", type=int, default=128)
+    ap.add_argument("--graph", type=int, default=1,
+                    help="replay the step as one captured CUDA graph (1) or launch it call by call (0)")
     ap.add_argument("--fuse-shared-inputs", action="store_true",
                     help="merge the linears that read one input (q/k/v, w1/w3) into one linear "
                          "with the concatenated weight and a tensorwise scale over it")
@@ -657,7 +678,8 @@ def main(argv=None):
                        "linears": [f"{l.name} M={l.M} K={l.K} N={l.N}" for l in lins],
                        "flops_per_step": sum(l.flops for l in lins),
                        "parallelism": "replicas" if world > 1 else "single-gpu",
-                       "l2": "no flush: a step's inputs exceed L2"},
+                       "l2": "no flush: a step's inputs exceed L2",
+                       "launch": "one captured CUDA graph per step" if args.graph else "call by call"},
             "pct_of_fp8_peak_nominal": 100 * r["value"] / FP8_NOMINAL_TFLOPS,
             "roofline": r["roofline"], "kernels": r["kernels"],
             "breakdown_ms_per_step": r["breakdown_ms_per_step"],

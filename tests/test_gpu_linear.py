@@ -154,3 +154,40 @@ def test_fused_shared_input_group_full_size(f8, c, gi):
     rows = _bands(N, 128, rng)
     check_close(dw[torch.from_numpy(rows).to(DEV)],
                 oracle.gemm_rows(qdy["qt"], qx["qt"], qdy["scale"], qx["scale"], rows), what="dW rows")
+
+
+def test_linear_in_cuda_graph_matches_eager(f8):
+    """Forward + backward captured once in a CUDA graph (as the benchmark
+    replays a step) give the same bits as eager calls, replay after replay."""
+    d = wl.custom_linear(1024, 768, 640, seed=3, dy_std=0.5)
+    x, w, dy = d["x"].to(DEV), d["w"].to(DEV), d["dy"].to(DEV)
+    M, K = x.shape
+    N = w.shape[0]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
+    dw = torch.empty((N, K), dtype=torch.bfloat16, device=DEV)
+    saved = f8.LinearSaved.empty(M, N, K, DEV)
+    ws = f8.workspace(M, N, K, DEV)
+
+    def step():
+        f8.f8_linear_fwd(x, w, y, saved, ws)
+        f8.f8_linear_bwd(dy, saved, dx=dx, dw=dw, ws=ws)
+
+    step()
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (y, dx, dw, saved.x_t, saved.w_t, saved.scalars)]
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    for t in (y, dx, dw):
+        t.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert f8.f8_last_device_status() == 0
+    for a, b in zip((y, dx, dw, saved.x_t, saved.w_t, saved.scalars), ref):
+        assert torch.equal(a, b)
