@@ -100,6 +100,12 @@ def _load():
         lib.or_gemm_rows_fmt.argtypes = [u8p, ctypes.c_int, u8p, ctypes.c_int, i64, i64, i64, f32, f32,
                                          i64p, i64, u16p]
         lib.or_gemm_rows_fmt.restype = None
+        lib.or_exp_cw.argtypes = [f32]
+        lib.or_exp_cw.restype = f32
+        lib.or_silu.argtypes = [f32]
+        lib.or_silu.restype = f32
+        lib.or_swiglu_h.argtypes = [u16p, u16p, i64, u16p]
+        lib.or_swiglu_h.restype = None
         lib.or_num_threads.argtypes = []
         lib.or_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -263,6 +269,26 @@ def gemm_cols(a_q, b_q, sa, sb, cols) -> np.ndarray:
     return out
 
 
+def exp_cw(x: float) -> float:
+    return float(_load().or_exp_cw(float(np.float32(x))))
+
+
+def silu(x: float) -> float:
+    return float(_load().or_silu(float(np.float32(x))))
+
+
+def swiglu_h(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
+    """bf16 bits of h = bf16(silu(a) * b) (fp32 arithmetic, exp by Cody-Waite
+    reduction + degree-7 Taylor polynomial)."""
+    a = _u16(a_bits)
+    b = _u16(b_bits)
+    assert a.shape == b.shape
+    h = np.empty(a.shape, np.uint16)
+    _load().or_swiglu_h(_ptr(a, ctypes.c_uint16), _ptr(b, ctypes.c_uint16), a.size,
+                        _ptr(h, ctypes.c_uint16))
+    return h
+
+
 # --------------------------------------------------------------------------
 # the linear layer, step by step
 # --------------------------------------------------------------------------
@@ -285,6 +311,15 @@ def linear_fwd(x_bits: np.ndarray, w_bits: np.ndarray) -> dict:
     qw = quantize(w_bits)
     y = gemm(qx["q"], qw["q"], qx["scale"], qw["scale"])
     return {"x": qx, "w": qw, "y": y}
+
+
+def linear_fwd_swiglu(a_bits: np.ndarray, b_bits: np.ndarray, w_bits: np.ndarray) -> dict:
+    """The forward of a linear whose input is h = silu(a) * b: h is formed
+    elementwise, then quantised and multiplied exactly as linear_fwd does."""
+    h = swiglu_h(a_bits, b_bits)
+    out = linear_fwd(h, w_bits)
+    out["h"] = h
+    return out
 
 
 def linear_bwd(dy_bits: np.ndarray, fwd: dict, dy_fmt: int = E4M3) -> dict:

@@ -478,6 +478,80 @@ void or_gemm_rows_fmt(const uint8_t *a, int fa, const uint8_t *b, int fb, int64_
     free(za);
 }
 
+/* ------------------------------------------------------------------------ */
+/* SwiGLU input of the w2 linear: h = bf16( silu(a) * b )                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * exp(x) in fp32 by Cody and Waite's range reduction (x = n ln2 + r with ln2
+ * split into a head exact in fp32 and a tail, |r| <= ln2/2) and the Taylor
+ * polynomial of degree 7 of exp(r) in Horner form, scaled by 2^n.  Every
+ * step is one IEEE fp32 operation (fmaf, add, multiply, round to integer),
+ * so any IEEE fp32 machine that performs the same steps gets the same bits.
+ * Error below 2 ulp over the finite range.
+ */
+static float f32_exp_cw(float x)
+{
+    if (isnan(x))
+        return x;
+    if (x > 88.0f)
+        return INFINITY;
+    if (x < -87.0f)
+        return 0.0f;
+    const float log2e = 1.44269502f;        /* fp32(1/ln 2) */
+    const float ln2_hi = 0.693145751953125f; /* ln 2 to 16 bits: n * ln2_hi is exact */
+    const float ln2_lo = 1.42860677e-06f;    /* fp32(ln 2 - ln2_hi) */
+    const float n = nearbyintf(x * log2e);
+    float r = fmaf(-n, ln2_hi, x);
+    r = fmaf(-n, ln2_lo, r);
+    float p = 1.0f / 5040.0f;
+    p = fmaf(p, r, 1.0f / 720.0f);
+    p = fmaf(p, r, 1.0f / 120.0f);
+    p = fmaf(p, r, 1.0f / 24.0f);
+    p = fmaf(p, r, 1.0f / 6.0f);
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    /* 2^n for n in [-126, 127] as an fp32 bit pattern */
+    const int ni = (int)n;
+    uint32_t bits = (uint32_t)(ni + 127) << 23;
+    float two_n;
+    memcpy(&two_n, &bits, sizeof two_n);
+    return p * two_n;
+}
+
+float or_exp_cw(float x) { return f32_exp_cw(x); }
+
+/* silu(a) = a / (1 + exp(-a)), each step one fp32 operation. */
+float or_silu(float a)
+{
+    const float e = f32_exp_cw(-a);
+    const float d = 1.0f + e;
+    return a / d;
+}
+
+/* RNE fp32 -> bf16 (bit patterns); NaN stays NaN. */
+static uint16_t f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u)
+        return (uint16_t)((u >> 16) | 0x40);
+    const uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* h = bf16(fl32(silu(fp32(a)) * fp32(b))) elementwise over n values. */
+void or_swiglu_h(const uint16_t *a, const uint16_t *b, int64_t n, uint16_t *h)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        const float s = or_silu(or_bf16_to_f32(a[i]));
+        h[i] = f32_to_bf16(s * or_bf16_to_f32(b[i]));
+    }
+}
+
 /* Number of threads the parallel loops above use. */
 int or_num_threads(void)
 {
