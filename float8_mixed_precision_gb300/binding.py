@@ -31,7 +31,7 @@ EXPORTS = ("f8_amax", "f8_cast_transpose", "f8_gemm", "f8_linear_workspace_bytes
            "f8_linear_fwd", "f8_linear_bwd", "f8_last_device_status", "f8_status_string",
            "f8_selftest_wait_timeout", "f8_set_wait_limit_ns", "f8_linear_fwd_noalloc",
            "f8_quantize", "f8_quantize_workspace_bytes", "f8_quantize_fmt", "f8_gemm_fmt",
-           "f8_linear_bwd_fmt")
+           "f8_linear_bwd_fmt", "f8_quantize_swiglu", "f8_linear_fwd_swiglu")
 
 F8_E4M3 = 0
 F8_E5M2 = 1
@@ -99,6 +99,11 @@ def lib() -> ctypes.CDLL:
         L.f8_linear_bwd_fmt.argtypes = [vp, ctypes.c_int, ctypes.POINTER(_Saved), i64, i64, i64, vp, vp,
                                         vp, ctypes.c_size_t, vp]
         L.f8_linear_bwd_fmt.restype = st
+        L.f8_quantize_swiglu.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        L.f8_quantize_swiglu.restype = st
+        L.f8_linear_fwd_swiglu.argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.POINTER(_Saved), vp,
+                                           ctypes.c_size_t, vp]
+        L.f8_linear_fwd_swiglu.restype = st
         L.f8_linear_fwd_noalloc.argtypes = [vp, vp, i64, i64, i64, vp, ctypes.POINTER(_Saved), vp]
         L.f8_linear_fwd_noalloc.restype = st
         _lib = L
@@ -303,6 +308,47 @@ def f8_linear_fwd_noalloc(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | No
     s = saved.c_struct()
     _check(lib().f8_linear_fwd_noalloc(_ptr(x), _ptr(w), M, N, K, _ptr(y), ctypes.byref(s),
                                        _stream(stream)), "f8_linear_fwd_noalloc")
+    return y, saved
+
+
+def f8_quantize_swiglu(a: torch.Tensor, b: torch.Tensor, amax_out=None, scale_out=None, q=None,
+                       q_t=None, ws=None, stream=None):
+    """E4M3 quantisation of h = bf16(silu(a) * b) without storing h:
+    returns (q, q_t, scale, amax)."""
+    if a.shape != b.shape or a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16 or a.dim() != 2:
+        raise TypeError("f8_quantize_swiglu takes two 2-D bf16 tensors of one shape")
+    rows, cols = a.shape
+    dev = a.device
+    amax_out = torch.empty((), dtype=torch.float32, device=dev) if amax_out is None else amax_out
+    scale_out = torch.empty((), dtype=torch.float32, device=dev) if scale_out is None else scale_out
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=dev) if q is None else q
+    q_t = torch.empty((cols, rows), dtype=torch.uint8, device=dev) if q_t is None else q_t
+    if ws is None:
+        ws = torch.empty(f8_quantize_workspace_bytes(), dtype=torch.uint8, device=dev)
+    _check(lib().f8_quantize_swiglu(_ptr(a), _ptr(b), rows, cols, _ptr(amax_out), _ptr(scale_out),
+                                    _ptr(q), _ptr(q_t), _ptr(ws), ws.numel(), _stream(stream)),
+           "f8_quantize_swiglu")
+    return q, q_t, scale_out, amax_out
+
+
+def f8_linear_fwd_swiglu(a: torch.Tensor, b: torch.Tensor, w: torch.Tensor,
+                         y: torch.Tensor | None = None, saved: LinearSaved | None = None,
+                         ws: torch.Tensor | None = None, stream=None):
+    """Y = h W^T with h = silu(a) * b formed inside the quantisation; returns (Y, saved)."""
+    M, K = a.shape
+    N, K2 = w.shape
+    if K != K2 or a.shape != b.shape:
+        raise ValueError("shapes do not match")
+    dev = a.device
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if saved is None:
+        saved = LinearSaved.empty(M, N, K, dev)
+    if ws is None:
+        ws = workspace(M, N, K, dev)
+    s = saved.c_struct()
+    _check(lib().f8_linear_fwd_swiglu(_ptr(a), _ptr(b), _ptr(w), M, N, K, _ptr(y), ctypes.byref(s),
+                                      _ptr(ws), ws.numel(), _stream(stream)), "f8_linear_fwd_swiglu")
     return y, saved
 
 

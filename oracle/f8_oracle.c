@@ -504,11 +504,12 @@ static float f32_exp_cw(float x)
     const float n = nearbyintf(x * log2e);
     float r = fmaf(-n, ln2_hi, x);
     r = fmaf(-n, ln2_lo, r);
-    float p = 1.0f / 5040.0f;
-    p = fmaf(p, r, 1.0f / 720.0f);
-    p = fmaf(p, r, 1.0f / 120.0f);
-    p = fmaf(p, r, 1.0f / 24.0f);
-    p = fmaf(p, r, 1.0f / 6.0f);
+    /* 1/k! rounded to fp32: 1/5040, 1/720, 1/120, 1/24, 1/6 */
+    float p = 0x1.a01a02p-13f;
+    p = fmaf(p, r, 0x1.6c16c2p-10f);
+    p = fmaf(p, r, 0x1.111112p-7f);
+    p = fmaf(p, r, 0x1.555556p-5f);
+    p = fmaf(p, r, 0x1.555556p-3f);
     p = fmaf(p, r, 0.5f);
     p = fmaf(p, r, 1.0f);
     p = fmaf(p, r, 1.0f);

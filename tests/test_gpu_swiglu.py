@@ -1,0 +1,95 @@
+"""GPU parity of the fused SwiGLU quantisation (h = bf16(silu(a) b) formed on
+the fly in both launches): scale and every E4M3 byte of q(h), q(h)^T
+bit-exact against the oracle's same-step definition, and the w2 linear fed by
+it (forward and backward) within the GEMM bar, small in full and at the
+Llama-3.1-8B FFN size on sampled rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from float8_mixed_precision_gb300 import workloads as wl
+from tolerance import check_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def f8():
+    import float8_mixed_precision_gb300 as m
+    from float8_mixed_precision_gb300 import build
+    build.build()
+    oracle.build()
+    m.lib()
+    return m
+
+
+def _ab(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    a = (torch.randn(shape, generator=g) * scale).to(torch.bfloat16)
+    b = torch.randn(shape, generator=g).to(torch.bfloat16)
+    return a, b
+
+
+@pytest.mark.parametrize("shape,scale", [((1, 1), 1.0), ((7, 33), 1.0), ((130, 260), 3.0),
+                                         ((320, 528), 1.0), ((1024, 4096), 1.0), ((256, 512), 40.0)])
+def test_quantize_swiglu_bytes(f8, shape, scale):
+    a, b = _ab(shape, shape[0] + shape[1], scale)
+    q, qt, s, amax = f8.f8_quantize_swiglu(a.to(DEV), b.to(DEV))
+    h = oracle.swiglu_h(wl.bits(a), wl.bits(b))
+    ref = oracle.quantize(h)
+    assert amax.item() == float(ref["amax"]) and s.item() == float(ref["scale"])
+    assert np.array_equal(q.cpu().numpy(), ref["q"]) and np.array_equal(qt.cpu().numpy(), ref["qt"])
+    assert f8.f8_last_device_status() == 0
+
+
+def test_quantize_swiglu_special_values(f8):
+    vals = [0.0, -0.0, 1.0, -1.0, 20.0, -20.0, 87.5, -87.5, 88.5, -88.5, 100.0, -100.0, 1e-30, 1e30]
+    a = torch.tensor(vals * 16, dtype=torch.bfloat16).reshape(14, 16)
+    b = torch.tensor([1.0, -2.0, 0.5, 0.0] * 56, dtype=torch.bfloat16).reshape(14, 16)
+    q, qt, s, amax = f8.f8_quantize_swiglu(a.to(DEV), b.to(DEV))
+    ref = oracle.quantize(oracle.swiglu_h(wl.bits(a), wl.bits(b)))
+    assert amax.item() == float(ref["amax"]) and s.item() == float(ref["scale"])
+    assert np.array_equal(q.cpu().numpy(), ref["q"])
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (272, 400, 528)])
+def test_linear_fwd_swiglu_full_compare(f8, M, N, K):
+    a, b = _ab((M, K), M + K)
+    w = (torch.randn(N, K, generator=torch.Generator().manual_seed(N)) * 0.02).to(torch.bfloat16)
+    dy = torch.randn(M, N, generator=torch.Generator().manual_seed(M)).to(torch.bfloat16)
+    y, saved = f8.f8_linear_fwd_swiglu(a.to(DEV), b.to(DEV), w.to(DEV))
+    dx, dw = f8.f8_linear_bwd(dy.to(DEV), saved)
+    assert f8.f8_last_device_status() == 0
+    fwd = oracle.linear_fwd_swiglu(wl.bits(a), wl.bits(b), wl.bits(w))
+    bwd = oracle.linear_bwd(wl.bits(dy), fwd)
+    assert np.array_equal(saved.x_t.cpu().numpy(), fwd["x"]["qt"])
+    assert saved.scalars[1].item() == float(fwd["x"]["scale"])
+    check_close(y, fwd["y"], what="Y")
+    check_close(dx, bwd["dx"], what="dX")
+    check_close(dw, bwd["dw"], what="dW")
+
+
+def test_linear_fwd_swiglu_llama8b_w2(f8):
+    """The w2 linear of the Llama-3.1-8B FFN workload (M=8192, K=14336 ->
+    N=4096) with its input given as the a, b of the SwiGLU."""
+    c, l = 3, 2
+    lin = wl.workload(c)[1][l]
+    shape = (lin.M, lin.K)
+    g_a = torch.Generator().manual_seed(wl.seed_of(c, l, 3))
+    g_b = torch.Generator().manual_seed(wl.seed_of(c, l, 4))
+    a = torch.randn(shape, generator=g_a).to(torch.bfloat16)
+    b = torch.randn(shape, generator=g_b).to(torch.bfloat16)
+    w = wl.normal((lin.N, lin.K), lin.w_std, wl.seed_of(c, l, 1))
+    y, saved = f8.f8_linear_fwd_swiglu(a.to(DEV), b.to(DEV), w.to(DEV))
+    assert f8.f8_last_device_status() == 0
+    h = oracle.swiglu_h(wl.bits(a), wl.bits(b))
+    qh = oracle.quantize(h)
+    qw = oracle.quantize(wl.bits(w))
+    assert saved.scalars[1].item() == float(qh["scale"])
+    assert np.array_equal(saved.x_t.cpu().numpy(), qh["qt"])
+    rng = np.random.default_rng(4)
+    rows = np.array([r * 128 + rng.integers(0, 128) for r in range(lin.M // 128)], np.int64)
+    check_close(y[torch.from_numpy(rows).to(DEV)],
+                oracle.gemm_rows(qh["q"], qw["q"], qh["scale"], qw["scale"], rows), what="Y rows")
