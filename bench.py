@@ -165,10 +165,16 @@ class ClockSampler:
 class Linear8:
     """Device buffers of one linear: inputs, outputs, saved tensors, workspace."""
 
-    def __init__(self, f8, lin, inputs, device, dy_fmt=0):
+    def __init__(self, f8, lin, inputs, device, dy_fmt=0, swiglu=None, ab=None):
         import torch
         self.lin = lin
         self.dy_fmt = dy_fmt
+        # swiglu: None (X given), "materialized" (h = silu(a) * b by torch each
+        # step, then the linear) or "fused" (f8_linear_fwd_swiglu on a, b)
+        self.swiglu = swiglu
+        if swiglu is not None:
+            self.a, self.b = ab[0].to(device), ab[1].to(device)
+            self.h = torch.empty_like(self.a)
         self.x = inputs["x"].to(device)
         self.w = inputs["w"].to(device)
         self.dy = inputs["dy"].to(device)
@@ -187,15 +193,30 @@ class Linear8:
         self.qws = torch.empty(f8.f8_quantize_workspace_bytes(), dtype=torch.uint8, device=device)
 
     def step(self, f8):
-        f8.f8_linear_fwd(self.x, self.w, self.y, self.saved, self.ws)
+        if self.swiglu == "fused":
+            f8.f8_linear_fwd_swiglu(self.a, self.b, self.w, self.y, self.saved, self.ws, h=self.h)
+        else:
+            if self.swiglu == "materialized":
+                import torch
+                torch.mul(torch.nn.functional.silu(self.a), self.b, out=self.x)
+            f8.f8_linear_fwd(self.x, self.w, self.y, self.saved, self.ws)
         f8.f8_linear_bwd(self.dy, self.saved, dx=self.dx, dw=self.dw, ws=self.ws, dy_fmt=self.dy_fmt)
 
     def step_timed(self, f8, ev):
         """The same launches as step(), one C call per kernel, bracketed by events."""
         s = self.saved
         M, N, K = self.lin.M, self.lin.N, self.lin.K
-        ev("quantize", 4 * self.x.numel(),
-           lambda: f8.f8_quantize(self.x, s.amax_x, s.scale_x, self.xq, s.x_t, self.qws))
+        if self.swiglu == "fused":
+            ev("quantize", 4 * self.x.numel(),
+               lambda: f8.f8_quantize_swiglu(self.a, self.b, self.h, s.amax_x, s.scale_x, self.xq, s.x_t,
+                                             self.qws))
+        else:
+            if self.swiglu == "materialized":
+                import torch
+                ev("swiglu (torch)", 6 * self.x.numel(),
+                   lambda: torch.mul(torch.nn.functional.silu(self.a), self.b, out=self.x))
+            ev("quantize", 4 * self.x.numel(),
+               lambda: f8.f8_quantize(self.x, s.amax_x, s.scale_x, self.xq, s.x_t, self.qws))
         ev("quantize", 4 * self.w.numel(),
            lambda: f8.f8_quantize(self.w, s.amax_w, s.scale_w, self.wq, s.w_t, self.qws))
         ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.xq, self.wq, s.scale_x, s.scale_w, self.y))
@@ -229,8 +250,13 @@ def run_ours(args, world, rank, local):
         layers = [Linear8(f8, g, wl.fused_group_inputs(args.config, idx), device, dy_fmt)
                   for g, idx in groups]
     else:
-        layers = [Linear8(f8, lin, wl.linear_inputs(args.config, i), device, dy_fmt)
-                  for i, lin in enumerate(lins)]
+        layers = []
+        for i, lin in enumerate(lins):
+            sw = args.swiglu_input if (lin.x_kind == "swiglu" and args.swiglu_input != "given") else None
+            layers.append(Linear8(f8, lin, wl.linear_inputs(args.config, i), device, dy_fmt, sw,
+                                  wl.swiglu_ab(args.config, i) if sw else None))
+        if any(L.swiglu for L in layers):
+            name += f" (w2 input: silu(a) * b, {args.swiglu_input})"
     flops_step = sum(l.flops for l in lins)
     stream = torch.cuda.current_stream()
 
@@ -319,7 +345,9 @@ def run_ours(args, world, rank, local):
         rate = d["work"] / (d["ms"] * 1e-3)
         e = {"launches_per_step": d["launches"] // nsteps_k, "ms_per_step": d["ms"] / nsteps_k,
              "share": d["ms"] / tot_ms}
-        if kind == "gemm":
+        if kind == "swiglu (torch)":
+            e.update({"gbs": rate / 1e9})
+        elif kind == "gemm":
             e.update({"tflops": rate / 1e12, "frac_of_fp8_measured": rate / 1e12 / fp8_peak,
                       "frac_of_fp8_nominal": rate / 1e12 / FP8_NOMINAL_TFLOPS})
         else:
@@ -644,6 +672,9 @@ def main(argv=None):
     ap.add_argument("--fuse-shared-inputs", action="store_true",
                     help="merge the linears that read one input (q/k/v, w1/w3) into one linear "
                          "with the concatenated weight and a tensorwise scale over it")
+    ap.add_argument("--swiglu-input", default="given", choices=["given", "materialized", "fused"],
+                    help="for linears fed by silu(a) * b: the bf16 product given (default), "
+                         "formed by torch each step, or formed inside the quantisation")
     ap.add_argument("--dy-format", default="e4m3", choices=["e4m3", "e5m2"],
                     help="FP8 format of dY in the backward pass (X and W stay E4M3)")
     ap.add_argument("--kernel-bench", type=int, default=1,

@@ -99,10 +99,10 @@ def lib() -> ctypes.CDLL:
         L.f8_linear_bwd_fmt.argtypes = [vp, ctypes.c_int, ctypes.POINTER(_Saved), i64, i64, i64, vp, vp,
                                         vp, ctypes.c_size_t, vp]
         L.f8_linear_bwd_fmt.restype = st
-        L.f8_quantize_swiglu.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        L.f8_quantize_swiglu.argtypes = [vp, vp, vp, i64, i64, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         L.f8_quantize_swiglu.restype = st
-        L.f8_linear_fwd_swiglu.argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.POINTER(_Saved), vp,
-                                           ctypes.c_size_t, vp]
+        L.f8_linear_fwd_swiglu.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, ctypes.POINTER(_Saved),
+                                           vp, ctypes.c_size_t, vp]
         L.f8_linear_fwd_swiglu.restype = st
         L.f8_linear_fwd_noalloc.argtypes = [vp, vp, i64, i64, i64, vp, ctypes.POINTER(_Saved), vp]
         L.f8_linear_fwd_noalloc.restype = st
@@ -311,10 +311,10 @@ def f8_linear_fwd_noalloc(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | No
     return y, saved
 
 
-def f8_quantize_swiglu(a: torch.Tensor, b: torch.Tensor, amax_out=None, scale_out=None, q=None,
-                       q_t=None, ws=None, stream=None):
-    """E4M3 quantisation of h = bf16(silu(a) * b) without storing h:
-    returns (q, q_t, scale, amax)."""
+def f8_quantize_swiglu(a: torch.Tensor, b: torch.Tensor, h: torch.Tensor | None = None,
+                       amax_out=None, scale_out=None, q=None, q_t=None, ws=None, stream=None):
+    """h = bf16(silu(a) * b) with its amax from the producing pass, then its
+    E4M3 cast: returns (q, q_t, scale, amax, h)."""
     if a.shape != b.shape or a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16 or a.dim() != 2:
         raise TypeError("f8_quantize_swiglu takes two 2-D bf16 tensors of one shape")
     rows, cols = a.shape
@@ -325,16 +325,17 @@ def f8_quantize_swiglu(a: torch.Tensor, b: torch.Tensor, amax_out=None, scale_ou
     q_t = torch.empty((cols, rows), dtype=torch.uint8, device=dev) if q_t is None else q_t
     if ws is None:
         ws = torch.empty(f8_quantize_workspace_bytes(), dtype=torch.uint8, device=dev)
-    _check(lib().f8_quantize_swiglu(_ptr(a), _ptr(b), rows, cols, _ptr(amax_out), _ptr(scale_out),
-                                    _ptr(q), _ptr(q_t), _ptr(ws), ws.numel(), _stream(stream)),
-           "f8_quantize_swiglu")
-    return q, q_t, scale_out, amax_out
+    h = torch.empty_like(a) if h is None else h
+    _check(lib().f8_quantize_swiglu(_ptr(a), _ptr(b), _ptr(h), rows, cols, _ptr(amax_out),
+                                    _ptr(scale_out), _ptr(q), _ptr(q_t), _ptr(ws), ws.numel(),
+                                    _stream(stream)), "f8_quantize_swiglu")
+    return q, q_t, scale_out, amax_out, h
 
 
 def f8_linear_fwd_swiglu(a: torch.Tensor, b: torch.Tensor, w: torch.Tensor,
                          y: torch.Tensor | None = None, saved: LinearSaved | None = None,
-                         ws: torch.Tensor | None = None, stream=None):
-    """Y = h W^T with h = silu(a) * b formed inside the quantisation; returns (Y, saved)."""
+                         ws: torch.Tensor | None = None, h: torch.Tensor | None = None, stream=None):
+    """Y = h W^T with h = silu(a) * b produced with its amax; returns (Y, saved)."""
     M, K = a.shape
     N, K2 = w.shape
     if K != K2 or a.shape != b.shape:
@@ -346,9 +347,11 @@ def f8_linear_fwd_swiglu(a: torch.Tensor, b: torch.Tensor, w: torch.Tensor,
         saved = LinearSaved.empty(M, N, K, dev)
     if ws is None:
         ws = workspace(M, N, K, dev)
+    h = torch.empty_like(a) if h is None else h
     s = saved.c_struct()
-    _check(lib().f8_linear_fwd_swiglu(_ptr(a), _ptr(b), _ptr(w), M, N, K, _ptr(y), ctypes.byref(s),
-                                      _ptr(ws), ws.numel(), _stream(stream)), "f8_linear_fwd_swiglu")
+    _check(lib().f8_linear_fwd_swiglu(_ptr(a), _ptr(b), _ptr(h), _ptr(w), M, N, K, _ptr(y),
+                                      ctypes.byref(s), _ptr(ws), ws.numel(), _stream(stream)),
+           "f8_linear_fwd_swiglu")
     return y, saved
 
 

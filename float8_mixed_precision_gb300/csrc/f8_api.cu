@@ -400,44 +400,46 @@ f8_status f8_linear_bwd_fmt(const void *dy, f8_format fmt_dy, const f8_linear_sa
     return linear_bwd_impl(dy, fmt_dy, saved, M, N, K, dx, dw, workspace, workspace_bytes, stream);
 }
 
-f8_status f8_quantize_swiglu(const void *a, const void *b, int64_t rows, int64_t cols,
+f8_status f8_quantize_swiglu(const void *a, const void *b, void *h, int64_t rows, int64_t cols,
                              float *amax_out, float *scale_out, uint8_t *q, uint8_t *q_t,
                              void *workspace, size_t workspace_bytes, void *stream)
 {
     if (rows < 0 || cols < 0 || amax_out == nullptr || workspace == nullptr ||
-        (rows > 0 && cols > 0 && (a == nullptr || b == nullptr)))
+        (rows > 0 && cols > 0 && (a == nullptr || b == nullptr || h == nullptr)))
         return F8_ERR_INVALID;
     if (workspace_bytes < kPartialsBytes)
         return F8_ERR_INVALID;
-    if (!aligned(a, 16) || !aligned(b, 16) || !aligned(q, 16) || !aligned(q_t, 16) ||
-        !aligned(amax_out, 4) || !aligned(scale_out, 4) || !aligned(workspace, 16))
+    if (!aligned(a, 16) || !aligned(b, 16) || !aligned(h, 16) || !aligned(q, 16) ||
+        !aligned(q_t, 16) || !aligned(amax_out, 4) || !aligned(scale_out, 4) ||
+        !aligned(workspace, 16))
         return F8_ERR_ALIGN;
     const DeviceInfo *dev;
     F8_TRY(get_device(&dev));
-    return from_cuda(launch_quantize_swiglu(a, b, rows, cols, static_cast<unsigned *>(workspace),
+    return from_cuda(launch_quantize_swiglu(a, b, h, rows, cols, static_cast<unsigned *>(workspace),
                                             amax_out, scale_out, q, q_t, *dev,
                                             static_cast<cudaStream_t>(stream)));
 }
 
-f8_status f8_linear_fwd_swiglu(const void *a, const void *b, const void *w, int64_t M, int64_t N,
-                               int64_t K, void *y, const f8_linear_saved *saved, void *workspace,
-                               size_t workspace_bytes, void *stream)
+f8_status f8_linear_fwd_swiglu(const void *a, const void *b, void *h, const void *w, int64_t M,
+                               int64_t N, int64_t K, void *y, const f8_linear_saved *saved,
+                               void *workspace, size_t workspace_bytes, void *stream)
 {
     F8_TRY(check_linear_shape(M, N, K));
     F8_TRY(check_saved(saved));
-    if (a == nullptr || b == nullptr || w == nullptr || y == nullptr || workspace == nullptr)
+    if (a == nullptr || b == nullptr || h == nullptr || w == nullptr || y == nullptr ||
+        workspace == nullptr)
         return F8_ERR_INVALID;
     if (workspace_bytes < fwd_ws_bytes(M, N, K))
         return F8_ERR_INVALID;
-    if (!aligned(a, 16) || !aligned(b, 16) || !aligned(w, 16) || !aligned(y, 16) ||
-        !aligned(workspace, 256))
+    if (!aligned(a, 16) || !aligned(b, 16) || !aligned(h, 16) || !aligned(w, 16) ||
+        !aligned(y, 16) || !aligned(workspace, 256))
         return F8_ERR_ALIGN;
     const DeviceInfo *dev;
     F8_TRY(get_device(&dev));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const FwdWs fw = fwd_ws(workspace, M, N, K);
     int np = 0;
-    F8_TRY_CUDA(launch_quantize_swiglu(a, b, M, K, fw.parts_x, saved->amax_x, saved->scale_x,
+    F8_TRY_CUDA(launch_quantize_swiglu(a, b, h, M, K, fw.parts_x, saved->amax_x, saved->scale_x,
                                        fw.x_q, saved->x_t, *dev, st));
     F8_TRY_CUDA(launch_amax_partials(w, N * K, fw.parts_w, &np, *dev, st));
     F8_TRY_CUDA(launch_cast_transpose(w, N, K, nullptr, fw.parts_w, np, saved->amax_w,

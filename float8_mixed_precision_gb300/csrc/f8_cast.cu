@@ -154,13 +154,19 @@ __device__ __forceinline__ uint8_t cvt1(uint16_t b, float s)
     return static_cast<uint8_t>(cvt2<FMT>(v, 0.0f) & 0xFFu);
 }
 
-// ---- the SwiGLU input of the w2 linear, h = bf16(silu(a) * b), formed on
-// the fly.  exp(x) is Cody and Waite's range reduction (x = n ln2 + r, ln2
-// split into a head exact in fp32 and a tail) with the degree-7 Taylor
-// polynomial of exp(r) in Horner form, scaled by 2^n; silu(a) = a/(1+exp(-a)).
-// Every step is one IEEE fp32 operation with round-to-nearest-even, so the
-// bits are those of the same steps on any IEEE machine.
-__device__ __forceinline__ float exp_cw(float x)
+// ---- the SwiGLU input of the w2 linear, h = bf16(silu(a) * b).  exp(x)
+// is Cody and Waite's range reduction (x = n ln2 + r, ln2 split into a head
+// exact in fp32 and a tail) with the degree-7 Taylor polynomial of exp(r) in
+// Horner form, scaled by 2^n; silu(a) = a * (1 / (1 + exp(-a))) with the
+// correctly rounded reciprocal.  Every step is one IEEE fp32 operation with
+// round-to-nearest-even, so the bits are those of the same steps on any IEEE
+// machine.  Two elements go through each packed fp32x2 instruction (per lane
+// the numerics of the scalar _rn operation).  n = rint(x log2e) is taken as
+// (p + 1.5 2^23) - 1.5 2^23, exact round-to-nearest-even for |p| < 2^22, and
+// 2^n is read off the low mantissa bits of the rounded sum.
+__device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
+
+__device__ __forceinline__ float exp_special(float x, float e)
 {
     if (x != x)
         return x;
@@ -168,46 +174,71 @@ __device__ __forceinline__ float exp_cw(float x)
         return __int_as_float(0x7F800000);
     if (x < -87.0f)
         return 0.0f;
-    const float n = rintf(__fmul_rn(x, 1.44269502f));
-    float r = __fmaf_rn(-n, 0.693145751953125f, x);
-    r = __fmaf_rn(-n, 1.42860677e-06f, r);
-    float p = 0x1.a01a02p-13f;
-    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);
-    p = __fmaf_rn(p, r, 0x1.111112p-7f);
-    p = __fmaf_rn(p, r, 0x1.555556p-5f);
-    p = __fmaf_rn(p, r, 0x1.555556p-3f);
-    p = __fmaf_rn(p, r, 0.5f);
-    p = __fmaf_rn(p, r, 1.0f);
-    p = __fmaf_rn(p, r, 1.0f);
-    return __fmul_rn(p, __int_as_float((static_cast<int>(n) + 127) << 23));
+    return e;
 }
 
-__device__ __forceinline__ uint32_t swiglu_bf16(uint32_t a_bits, uint32_t b_bits)
+// kChecked = false: the caller has shown -87 <= x <= 87 for both lanes (no
+// NaN), where the special cases cannot arise and n stays in [-126, 126].
+template <bool kChecked>
+__device__ __forceinline__ float2 exp_cw2(float2 x)
 {
-    const float a = __uint_as_float(a_bits << 16);
-    const float s = __fdiv_rn(a, __fadd_rn(1.0f, exp_cw(-a)));
-    const __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(s, __uint_as_float(b_bits << 16)));
-    return static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&h));
+    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+    const float2 p = __fmul2_rn(x, splat(1.44269502f));
+    const float2 t = __fadd2_rn(p, splat(kRound));
+    const float2 mn = __fadd2_rn(splat(kRound), make_float2(-t.x, -t.y));  // -rint(p)
+    float2 r = __ffma2_rn(mn, splat(0.693145751953125f), x);
+    r = __ffma2_rn(mn, splat(1.42860677e-06f), r);
+    float2 q = __ffma2_rn(splat(0x1.a01a02p-13f), r, splat(0x1.6c16c2p-10f));
+    q = __ffma2_rn(q, r, splat(0x1.111112p-7f));
+    q = __ffma2_rn(q, r, splat(0x1.555556p-5f));
+    q = __ffma2_rn(q, r, splat(0x1.555556p-3f));
+    q = __ffma2_rn(q, r, splat(0.5f));
+    q = __ffma2_rn(q, r, splat(1.0f));
+    q = __ffma2_rn(q, r, splat(1.0f));
+    // bits(t) = 0x4B400000 + n, and 0x4B400000 << 23 vanishes mod 2^32
+    const float2 two_n = make_float2(__int_as_float((__float_as_int(t.x) << 23) + 0x3F800000),
+                                     __int_as_float((__float_as_int(t.y) << 23) + 0x3F800000));
+    const float2 e = __fmul2_rn(q, two_n);
+    if (!kChecked)
+        return e;
+    return make_float2(exp_special(x.x, e.x), exp_special(x.y, e.y));
 }
 
 // two packed bf16 of a and of b -> two packed bf16 of h
+template <bool kChecked>
 __device__ __forceinline__ uint32_t swiglu_x2(uint32_t a, uint32_t b)
 {
-    return swiglu_bf16(a & 0xFFFFu, b & 0xFFFFu) | (swiglu_bf16(a >> 16, b >> 16) << 16);
+    const float2 fa = make_float2(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
+    const float2 fb = make_float2(__uint_as_float(b << 16), __uint_as_float(b & 0xFFFF0000u));
+    const float2 e = exp_cw2<kChecked>(make_float2(-fa.x, -fa.y));
+    const float2 d = __fadd2_rn(splat(1.0f), e);
+    const float2 sl = __fmul2_rn(fa, make_float2(__frcp_rn(d.x), __frcp_rn(d.y)));
+    const float2 hf = __fmul2_rn(sl, fb);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(hf.x, hf.y);
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// Eight elements; the special-value selects of exp are skipped when every
+// |a| <= 87 (bf16 0x42AE), the case for all but pathological inputs.
 __device__ __forceinline__ uint4 swiglu_x8(uint4 a, uint4 b)
 {
-    return make_uint4(swiglu_x2(a.x, b.x), swiglu_x2(a.y, b.y), swiglu_x2(a.z, b.z),
-                      swiglu_x2(a.w, b.w));
+    constexpr uint32_t kMag = 0x7FFF7FFFu;
+    const uint32_t m = __vmaxu2(__vmaxu2(a.x & kMag, a.y & kMag), __vmaxu2(a.z & kMag, a.w & kMag));
+    if (__vcmpgtu2(m, 0x42AE42AEu) == 0)
+        return make_uint4(swiglu_x2<false>(a.x, b.x), swiglu_x2<false>(a.y, b.y),
+                          swiglu_x2<false>(a.z, b.z), swiglu_x2<false>(a.w, b.w));
+    return make_uint4(swiglu_x2<true>(a.x, b.x), swiglu_x2<true>(a.y, b.y), swiglu_x2<true>(a.z, b.z),
+                      swiglu_x2<true>(a.w, b.w));
 }
 
-// amax partials of h over the whole [n] tensor given by a and b (no h is
-// written): one partial maximum per CTA, as amax_kernel<true>.
+// h = silu(a) * b for the whole [n] tensors, written once as bf16, with one
+// partial maximum of |h| per CTA (as amax_kernel<true>): the amax comes out
+// of the pass that produces h, so h is read only by the cast.
 __global__ void __launch_bounds__(kAmaxThreads)
-amax_swiglu_kernel(const uint4 *__restrict__ a, const uint4 *__restrict__ b, int64_t nvec,
-                   const uint16_t *__restrict__ a_tail, const uint16_t *__restrict__ b_tail,
-                   int ntail, unsigned *__restrict__ partials, unsigned *__restrict__ status)
+swiglu_amax_kernel(const uint4 *__restrict__ a, const uint4 *__restrict__ b, uint4 *__restrict__ h,
+                   int64_t nvec, const uint16_t *__restrict__ a_tail, const uint16_t *__restrict__ b_tail,
+                   uint16_t *__restrict__ h_tail, int ntail, unsigned *__restrict__ partials,
+                   unsigned *__restrict__ status)
 {
     griddep_wait();
     griddep_launch_dependents();
@@ -224,12 +255,21 @@ amax_swiglu_kernel(const uint4 *__restrict__ a, const uint4 *__restrict__ b, int
             vb[u] = i < nvec ? __ldg(b + i) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int u = 0; u < kU; ++u)
-            m2 = max_u16x2(m2, swiglu_x8(va[u], vb[u]));
+        for (int u = 0; u < kU; ++u) {
+            const int64_t i = base + u * S;
+            const uint4 hv = swiglu_x8(va[u], vb[u]);
+            if (i < nvec) {
+                h[i] = hv;
+                m2 = max_u16x2(m2, hv);
+            }
+        }
     }
     uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-    if (blockIdx.x == 0 && threadIdx.x < ntail)
-        m = max(m, swiglu_bf16(a_tail[threadIdx.x], b_tail[threadIdx.x]) & 0x7FFFu);
+    if (blockIdx.x == 0 && threadIdx.x < ntail) {
+        const uint32_t hv = swiglu_x2<true>(a_tail[threadIdx.x], b_tail[threadIdx.x]) & 0xFFFFu;
+        h_tail[threadIdx.x] = static_cast<uint16_t>(hv);
+        m = max(m, hv & 0x7FFFu);
+    }
     m = __reduce_max_sync(0xFFFFFFFFu, m);
     __shared__ uint32_t warp_max[kAmaxThreads / 32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -283,14 +323,12 @@ __device__ __forceinline__ void transpose_out(const uint8_t *tile, uint8_t *__re
     }
 }
 
-// SWIGLU: the tensor is h = silu(x) * xb formed on the fly from x and xb.
-template <int FMT, bool SWIGLU = false>
+template <int FMT>
 __global__ void __launch_bounds__(kCastThreads)
 cast_transpose_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
                       const float *__restrict__ amax, const unsigned *__restrict__ partials,
                       int nparts, float *__restrict__ amax_out, float *__restrict__ scale_out,
-                      uint8_t *__restrict__ q, uint8_t *__restrict__ qt, int vector_ok,
-                      const uint16_t *__restrict__ xb = nullptr)
+                      uint8_t *__restrict__ q, uint8_t *__restrict__ qt, int vector_ok)
 {
     __shared__ __align__(16) uint8_t tile[kTile * kTile];
     griddep_wait();
@@ -320,13 +358,8 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols
                 const int k = t + it * kCastThreads;  // 16-element chunk id in the tile
                 const int row = k >> 3, ch = k & 7;
                 const uint16_t *src = x + (r0 + row) * cols + c0 + ch * 16;
-                uint4 v0 = __ldg(reinterpret_cast<const uint4 *>(src));
-                uint4 v1 = __ldg(reinterpret_cast<const uint4 *>(src + 8));
-                if (SWIGLU) {
-                    const uint16_t *srcb = xb + (r0 + row) * cols + c0 + ch * 16;
-                    v0 = swiglu_x8(v0, __ldg(reinterpret_cast<const uint4 *>(srcb)));
-                    v1 = swiglu_x8(v1, __ldg(reinterpret_cast<const uint4 *>(srcb + 8)));
-                }
+                const uint4 v0 = __ldg(reinterpret_cast<const uint4 *>(src));
+                const uint4 v1 = __ldg(reinterpret_cast<const uint4 *>(src + 8));
                 const uint2 a = cvt8<FMT>(v0, s), b = cvt8<FMT>(v1, s);
                 const uint4 codes = make_uint4(a.x, a.y, b.x, b.y);
                 if (q != nullptr)
@@ -344,10 +377,7 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols
             for (int e = t; e < kTile * kTile; e += kCastThreads) {
                 const int64_t r = r0 + e / kTile, c = c0 + e % kTile;
                 if (r < rows && c < cols) {
-                    const uint16_t v = SWIGLU ? static_cast<uint16_t>(swiglu_bf16(x[r * cols + c],
-                                                                                  xb[r * cols + c]))
-                                              : x[r * cols + c];
-                    const uint8_t b = cvt1<FMT>(v, s);
+                    const uint8_t b = cvt1<FMT>(x[r * cols + c], s);
                     if (q != nullptr)
                         q[r * cols + c] = b;
                     if (qt != nullptr)
@@ -462,7 +492,7 @@ namespace {
 
 // Resident CTAs per SM of each kernel on each device (occupancy API, cached).
 struct Occupancy {
-    int amax_atomic = 0, amax_partials = 0, cast = 0, cast_tma = 0;
+    int amax_atomic = 0, amax_partials = 0, cast = 0, cast_tma = 0, swiglu = 0;
 };
 std::mutex g_occ_mutex;
 Occupancy g_occ[64];
@@ -477,7 +507,7 @@ const Occupancy &occupancy(const DeviceInfo &dev)
         o.amax_atomic = n > 0 ? n : 1;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, amax_kernel<true>, kAmaxThreads, 0);
         o.amax_partials = n > 0 ? n : 1;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cast_transpose_kernel<0, true>, kCastThreads, 0);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cast_transpose_kernel<0>, kCastThreads, 0);
         o.cast = n > 0 ? n : 1;
         cudaFuncSetAttribute(cast_transpose_tma_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kTmaCastSmem);
@@ -486,6 +516,8 @@ const Occupancy &occupancy(const DeviceInfo &dev)
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cast_transpose_tma_kernel<0>, kCastThreads,
                                                       kTmaCastSmem);
         o.cast_tma = n > 0 ? n : 1;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, swiglu_amax_kernel, kAmaxThreads, 0);
+        o.swiglu = n > 0 ? n : 1;
     }
     return o;
 }
@@ -562,19 +594,19 @@ cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, con
     return launch_pdl(fmt == 1 ? cast_transpose_kernel<1> : cast_transpose_kernel<0>,
                       dim3(static_cast<unsigned>(blocks)), dim3(kCastThreads),
                       0, stream, static_cast<const uint16_t *>(x), rows, cols, amax, partials, nparts,
-                      amax_out, scale_out, q, q_t, vector_ok, static_cast<const uint16_t *>(nullptr));
+                      amax_out, scale_out, q, q_t, vector_ok);
 }
 
-cudaError_t launch_quantize_swiglu(const void *a, const void *b, int64_t rows, int64_t cols,
-                                   unsigned *partials, float *amax_out, float *scale_out,
-                                   uint8_t *q, uint8_t *q_t, const DeviceInfo &dev,
+cudaError_t launch_quantize_swiglu(const void *a, const void *b, void *h, int64_t rows,
+                                   int64_t cols, unsigned *partials, float *amax_out,
+                                   float *scale_out, uint8_t *q, uint8_t *q_t, const DeviceInfo &dev,
                                    cudaStream_t stream)
 {
     const int64_t n = rows * cols;
     const int64_t nvec = n / 8;
     const int ntail = static_cast<int>(n % 8);
     int64_t blocks = (nvec + kAmaxThreads * 4 - 1) / (kAmaxThreads * 4);
-    const int64_t cap = static_cast<int64_t>(dev.sm_count) * occupancy(dev).amax_partials;
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * occupancy(dev).swiglu;
     if (blocks > cap)
         blocks = cap;
     if (blocks > kMaxAmaxPartials)
@@ -582,24 +614,16 @@ cudaError_t launch_quantize_swiglu(const void *a, const void *b, int64_t rows, i
     if (blocks < 1)
         blocks = 1;
     const uint16_t *a16 = static_cast<const uint16_t *>(a), *b16 = static_cast<const uint16_t *>(b);
-    cudaError_t e = launch_pdl(amax_swiglu_kernel, dim3(static_cast<unsigned>(blocks)),
+    uint16_t *h16 = static_cast<uint16_t *>(h);
+    cudaError_t e = launch_pdl(swiglu_amax_kernel, dim3(static_cast<unsigned>(blocks)),
                                dim3(kAmaxThreads), 0, stream, static_cast<const uint4 *>(a),
-                               static_cast<const uint4 *>(b), nvec, a16 + nvec * 8, b16 + nvec * 8,
-                               ntail, partials, dev.status);
+                               static_cast<const uint4 *>(b), static_cast<uint4 *>(h), nvec,
+                               a16 + nvec * 8, b16 + nvec * 8, h16 + nvec * 8, ntail, partials,
+                               dev.status);
     if (e != cudaSuccess)
         return e;
-    const int64_t ntiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
-    int64_t cblocks = ntiles;
-    const int64_t ccap = static_cast<int64_t>(dev.sm_count) * occupancy(dev).cast;
-    if (cblocks > ccap)
-        cblocks = ccap;
-    if (cblocks < 1)
-        cblocks = 1;
-    const int vector_ok = (rows % 16 == 0) && (cols % 16 == 0);
-    return launch_pdl(cast_transpose_kernel<0, true>, dim3(static_cast<unsigned>(cblocks)),
-                      dim3(kCastThreads), 0, stream, a16, rows, cols, static_cast<const float *>(nullptr),
-                      static_cast<const unsigned *>(partials), static_cast<int>(blocks), amax_out,
-                      scale_out, q, q_t, vector_ok, b16);
+    return launch_cast_transpose(h, rows, cols, nullptr, partials, static_cast<int>(blocks), amax_out,
+                                 scale_out, q, q_t, 0, dev, stream);
 }
 
 } // namespace f8

@@ -108,11 +108,11 @@ cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, con
                                   float *scale_out, uint8_t *q, uint8_t *q_t, int fmt,
                                   const DeviceInfo &dev, cudaStream_t stream);
 
-// amax (partials) and E4M3 cast of h = bf16(silu(a) * b) for two [rows, cols]
-// bf16 tensors, h formed on the fly in both launches and never stored.
-cudaError_t launch_quantize_swiglu(const void *a, const void *b, int64_t rows, int64_t cols,
-                                   unsigned *partials, float *amax_out, float *scale_out,
-                                   uint8_t *q, uint8_t *q_t, const DeviceInfo &dev,
+// h = bf16(silu(a) * b) for two [rows, cols] bf16 tensors written to `h`
+// together with its amax partials (one pass), then its E4M3 cast.
+cudaError_t launch_quantize_swiglu(const void *a, const void *b, void *h, int64_t rows,
+                                   int64_t cols, unsigned *partials, float *amax_out,
+                                   float *scale_out, uint8_t *q, uint8_t *q_t, const DeviceInfo &dev,
                                    cudaStream_t stream);
 
 // C[M,N] = bf16(A[M,K] B[N,K]^T / (sa sb)); M, N, K >= 1, K % 16 == 0.

@@ -125,6 +125,16 @@ def student_t_outliers(shape, nu: int, frac: float, factor: float, seed: int) ->
     return t.reshape(shape).to(torch.bfloat16)
 
 
+def swiglu_ab(c: int, l: int) -> tuple[torch.Tensor, torch.Tensor]:
+    """The a and b (bf16) whose silu(a) * b is the input of linear l of
+    workload c, for linears with x_kind "swiglu"."""
+    lin = WORKLOADS[c][1][l]
+    shape = (lin.M, lin.K)
+    a = torch.randn(shape, generator=_gen(seed_of(c, l, 3)), dtype=torch.float32)
+    b = torch.randn(shape, generator=_gen(seed_of(c, l, 4)), dtype=torch.float32)
+    return a.to(torch.bfloat16), b.to(torch.bfloat16)
+
+
 def _activation(kind: str, shape, std: float, c: int, l: int, t: int) -> torch.Tensor:
     if kind == "normal":
         return normal(shape, std, seed_of(c, l, t))

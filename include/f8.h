@@ -227,29 +227,33 @@ f8_status f8_linear_bwd_fmt(const void *dy, f8_format fmt_dy, const f8_linear_sa
                             size_t workspace_bytes, void *stream);
 
 /*
- * The w2 input of a SwiGLU FFN, h = bf16(silu(a) * b), quantised to E4M3
- * without ever being stored: the amax launch and the cast launch both form
- * h from a and b on the fly (2 x 2 B/elem read per launch, 2 x 1 B/elem
- * written: h costs no HBM pass of its own).  silu(a) = a / (1 + exp(-a))
- * in fp32 with exp by Cody-Waite range reduction and the degree-7 Taylor
- * polynomial (each step one IEEE fp32 operation), then one RNE to bf16.
- * The pages name the SwiGLU FFN of Llama 3.1 (torchtitan's llama3 model)
- * and credit Float8 on top of torch.compile, which fuses such neighbours.
+ * The w2 input of a SwiGLU FFN, h = bf16(silu(a) * b), produced and
+ * quantised to E4M3 with its amax taken in the producing pass: launch one
+ * reads a and b, writes h and one partial maximum of |h| per CTA; launch two
+ * is f8_quantize's cast of h.  Against forming h separately and then
+ * running f8_quantize, the amax re-read of h (2 B/elem) is gone.
+ * silu(a) = a * (1 / (1 + exp(-a))) in fp32, exp by Cody-Waite range
+ * reduction and the degree-7 Taylor polynomial, the reciprocal correctly
+ * rounded; each step one IEEE fp32 operation, then one RNE to bf16.  The
+ * pages name the SwiGLU FFN of torchtitan's Llama 3.1 and credit Float8 on
+ * top of torch.compile, which fuses such neighbouring elementwise work.
  *   a, b:     device bf16 [rows, cols], 16-byte aligned.
+ *   h:        device bf16 [rows, cols] receiving h.
  *   amax_out, scale_out, q, q_t, workspace: as for f8_quantize.
  */
-f8_status f8_quantize_swiglu(const void *a, const void *b, int64_t rows, int64_t cols,
+f8_status f8_quantize_swiglu(const void *a, const void *b, void *h, int64_t rows, int64_t cols,
                              float *amax_out, float *scale_out, uint8_t *q, uint8_t *q_t,
                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * f8_linear_fwd of the w2 linear fed by h = silu(a) * b (a, b: device bf16
- * [M, K]): h is quantised by f8_quantize_swiglu's two launches instead of
- * being given.  `saved` receives q(h)^T, so f8_linear_bwd applies unchanged.
+ * f8_linear_fwd of the w2 linear fed by h = silu(a) * b (a, b, h: device
+ * bf16 [M, K]; h receives the product): the input is produced and quantised
+ * by f8_quantize_swiglu's two launches.  `saved` receives q(h)^T, so
+ * f8_linear_bwd applies unchanged.
  */
-f8_status f8_linear_fwd_swiglu(const void *a, const void *b, const void *w, int64_t M, int64_t N,
-                               int64_t K, void *y, const f8_linear_saved *saved, void *workspace,
-                               size_t workspace_bytes, void *stream);
+f8_status f8_linear_fwd_swiglu(const void *a, const void *b, void *h, const void *w, int64_t M,
+                               int64_t N, int64_t K, void *y, const f8_linear_saved *saved,
+                               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status

@@ -523,12 +523,14 @@ static float f32_exp_cw(float x)
 
 float or_exp_cw(float x) { return f32_exp_cw(x); }
 
-/* silu(a) = a / (1 + exp(-a)), each step one fp32 operation. */
+/* silu(a) = a * (1 / (1 + exp(-a))), each step one fp32 operation (the
+ * reciprocal is the correctly rounded 1/d, then one multiply). */
 float or_silu(float a)
 {
     const float e = f32_exp_cw(-a);
     const float d = 1.0f + e;
-    return a / d;
+    const float r = 1.0f / d;
+    return a * r;
 }
 
 /* RNE fp32 -> bf16 (bit patterns); NaN stays NaN. */
