@@ -54,7 +54,7 @@ REF_BUDGET_S = 60.0   # timed seconds of the CPU reference arm
 # DRAM bytes (read + write) of the 12 GEMM launches of one attention fwd+bwd
 # step, from one ncu capture (profiles/gemm_traffic_attn8b.md), valid for the
 # GEMM sources whose hash is given; reported as null once they change.
-GEMM_TRAFFIC = {"workload": 2, "bytes_per_step": 697309952, "sources_sha256_16": "955986f4b70b25e0"}
+GEMM_TRAFFIC = {"workload": 2, "bytes_per_step": 696449024, "sources_sha256_16": "ef8eef719b567c8c"}
 
 
 def gemm_sources_hash() -> str:
@@ -165,6 +165,8 @@ class ClockSampler:
 class Linear8:
     """Device buffers of one linear: inputs, outputs, saved tensors, workspace."""
 
+    launches = 9  # our kernels per step: amax + cast of X, W, dY; 3 GEMMs
+
     def __init__(self, f8, lin, inputs, device, dy_fmt=0, swiglu=None, ab=None):
         import torch
         self.lin = lin
@@ -220,6 +222,11 @@ class Linear8:
         ev("quantize", 4 * self.w.numel(),
            lambda: f8.f8_quantize(self.w, s.amax_w, s.scale_w, self.wq, s.w_t, self.qws))
         ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.xq, self.wq, s.scale_x, s.scale_w, self.y))
+        self.bwd_timed(f8, ev)
+
+    def bwd_timed(self, f8, ev):
+        s = self.saved
+        M, N, K = self.lin.M, self.lin.N, self.lin.K
         ev("quantize", 4 * self.dy.numel(),
            lambda: f8.f8_quantize(self.dy, self.dys[0], self.dys[1], self.dyq, self.dyt, self.qws,
                                   fmt=self.dy_fmt))
@@ -229,7 +236,108 @@ class Linear8:
                                                      fmt_a=self.dy_fmt))
 
 
-KERNELS_PER_LINEAR = 9  # 3 amax + 3 cast_transpose + 3 GEMM
+class FfnIn8(Linear8):
+    """The group {w1, w3} of a SwiGLU FFN (W13 interleaved by 128 rows) with
+    the SwiGLU epilogue: f8_linear_fwd_w13_swiglu writes AB (into y), h and
+    q(h), q(h)^T and h's amax and scale for the W2Q8 that follows, then the
+    group's backward."""
+
+    launches = 10  # amax + cast of X, W13; the GEMM; cast of h; amax + cast of dY; 2 GEMMs
+
+    def __init__(self, f8, lin, inputs, device, dy_fmt=0):
+        import torch
+        super().__init__(f8, lin, inputs, device, dy_fmt)
+        M, F = lin.M, lin.N // 2
+        self.h = torch.empty((M, F), dtype=torch.bfloat16, device=device)
+        self.h_q = torch.empty((M, F), dtype=torch.uint8, device=device)
+        self.next = None  # the W2Q8 whose saved tensors receive q(h)^T and h's scalars
+
+    def step(self, f8):
+        s2 = self.next.saved
+        f8.f8_linear_fwd_w13_swiglu(self.x, self.w, self.y, self.h, self.saved, s2.scalars[0:1],
+                                    s2.scalars[1:2], self.h_q, s2.x_t, self.ws)
+        f8.f8_linear_bwd(self.dy, self.saved, dx=self.dx, dw=self.dw, ws=self.ws, dy_fmt=self.dy_fmt)
+
+    def step_timed(self, f8, ev):
+        s, s2 = self.saved, self.next.saved
+        M, N, K = self.lin.M, self.lin.N, self.lin.K
+        ev("quantize", 4 * self.x.numel(),
+           lambda: f8.f8_quantize(self.x, s.amax_x, s.scale_x, self.xq, s.x_t, self.qws))
+        ev("quantize", 4 * self.w.numel(),
+           lambda: f8.f8_quantize(self.w, s.amax_w, s.scale_w, self.wq, s.w_t, self.qws))
+        ev("gemm", 2 * M * N * K,
+           lambda: f8.f8_gemm_w13_swiglu(self.xq, self.wq, s.scale_x, s.scale_w, self.y, self.h,
+                                         s2.scalars[0:1]))
+        ev("quantize", 4 * self.h.numel(),
+           lambda: f8.f8_cast_transpose(self.h, s2.scalars[0:1], s2.scalars[1:2], self.h_q, s2.x_t))
+        self.bwd_timed(f8, ev)
+
+
+class W2Q8(Linear8):
+    """The w2 linear fed by the q(h) that its FfnIn8 produced: W2 quantised
+    (f8_quantize), the GEMM on q(h) (f8_gemm), then the linear's backward."""
+
+    launches = 7  # amax + cast of W2; the GEMM; amax + cast of dY; 2 GEMMs
+
+    def __init__(self, f8, lin, inputs, device, dy_fmt, src: FfnIn8):
+        super().__init__(f8, lin, inputs, device, dy_fmt)
+        self.src = src
+        src.next = self
+
+    def step(self, f8):
+        s = self.saved
+        f8.f8_quantize(self.w, s.amax_w, s.scale_w, self.wq, s.w_t, self.qws)
+        f8.f8_gemm(self.src.h_q, self.wq, s.scale_x, s.scale_w, self.y)
+        f8.f8_linear_bwd(self.dy, self.saved, dx=self.dx, dw=self.dw, ws=self.ws, dy_fmt=self.dy_fmt)
+
+    def step_timed(self, f8, ev):
+        s = self.saved
+        M, N, K = self.lin.M, self.lin.N, self.lin.K
+        ev("quantize", 4 * self.w.numel(),
+           lambda: f8.f8_quantize(self.w, s.amax_w, s.scale_w, self.wq, s.w_t, self.qws))
+        ev("gemm", 2 * M * N * K,
+           lambda: f8.f8_gemm(self.src.h_q, self.wq, s.scale_x, s.scale_w, self.y))
+        self.bwd_timed(f8, ev)
+
+
+def build_layers(f8, wl, args, device, dy_fmt):
+    """The workload's linears as layer objects, and the workload's name."""
+    name, lins = wl.workload(args.config)
+    if args.swiglu_input == "epilogue":
+        if args.config not in wl.SHARED_INPUT_GROUPS:
+            raise SystemExit("--swiglu-input epilogue needs a workload with a SwiGLU FFN (3, 4, 5)")
+        layers, ffn = [], None
+        for g, idx in wl.fused_groups(args.config):
+            if g.name == "w1+w3":
+                ffn = FfnIn8(f8, g, wl.w13_group_inputs(args.config, idx), device, dy_fmt)
+                layers.append(ffn)
+            elif g.name == "w2" and ffn is not None:
+                layers.append(W2Q8(f8, g, wl.fused_group_inputs(args.config, idx), device, dy_fmt,
+                                   ffn))
+            else:
+                layers.append(Linear8(f8, g, wl.fused_group_inputs(args.config, idx), device,
+                                      dy_fmt))
+        if ffn is None:
+            raise SystemExit("--swiglu-input epilogue needs a workload with a SwiGLU FFN (3, 4, 5)")
+        return (name + " (shared inputs fused; w2 input silu(a) * b from the w1+w3 GEMM "
+                "epilogue)"), layers
+    if args.fuse_shared_inputs:
+        layers = []
+        for g, idx in wl.fused_groups(args.config):
+            sw = (args.swiglu_input if g.x_kind == "swiglu" and args.swiglu_input != "given"
+                  else None)
+            layers.append(Linear8(f8, g, wl.fused_group_inputs(args.config, idx), device, dy_fmt,
+                                  sw, wl.swiglu_ab(args.config, idx[0]) if sw else None))
+        name += " (shared inputs fused: " + ", ".join(L.lin.name for L in layers) + ")"
+    else:
+        layers = []
+        for i, lin in enumerate(lins):
+            sw = args.swiglu_input if (lin.x_kind == "swiglu" and args.swiglu_input != "given") else None
+            layers.append(Linear8(f8, lin, wl.linear_inputs(args.config, i), device, dy_fmt, sw,
+                                  wl.swiglu_ab(args.config, i) if sw else None))
+    if any(L.swiglu for L in layers):
+        name += f" (w2 input: silu(a) * b, {args.swiglu_input})"
+    return name, layers
 
 
 def run_ours(args, world, rank, local):
@@ -241,22 +349,9 @@ def run_ours(args, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     f8.lib()
-    name, lins = wl.workload(args.config)
     dy_fmt = f8.F8_E5M2 if args.dy_format == "e5m2" else f8.F8_E4M3
-    if args.fuse_shared_inputs:
-        groups = wl.fused_groups(args.config)
-        lins = [g for g, _ in groups]
-        name += " (shared inputs fused: " + ", ".join(l.name for l in lins) + ")"
-        layers = [Linear8(f8, g, wl.fused_group_inputs(args.config, idx), device, dy_fmt)
-                  for g, idx in groups]
-    else:
-        layers = []
-        for i, lin in enumerate(lins):
-            sw = args.swiglu_input if (lin.x_kind == "swiglu" and args.swiglu_input != "given") else None
-            layers.append(Linear8(f8, lin, wl.linear_inputs(args.config, i), device, dy_fmt, sw,
-                                  wl.swiglu_ab(args.config, i) if sw else None))
-        if any(L.swiglu for L in layers):
-            name += f" (w2 input: silu(a) * b, {args.swiglu_input})"
+    name, layers = build_layers(f8, wl, args, device, dy_fmt)
+    lins = [L.lin for L in layers]
     flops_step = sum(l.flops for l in lins)
     stream = torch.cuda.current_stream()
 
@@ -368,17 +463,19 @@ def run_ours(args, world, rank, local):
                 "algorithmic_bytes_per_step": sum(4 * (l.M * l.K + l.N * l.K + l.M * l.N)
                                                   for l in lins)}
 
-    iso = kernel_bench(f8, layers, device, stream) if args.kernel_bench else None
+    # the chained FFN's w2 reads a device-made input: no isolated or host-fed runs
+    chained = args.swiglu_input == "epilogue"
+    iso = kernel_bench(f8, layers, device, stream) if args.kernel_bench and not chained else None
 
     # ---- end to end: pinned host buffers in, results out, every step
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and not chained:
         e2e = run_e2e(f8, layers, args, device, stream, flops_step, world)
 
     return {"value": value, "ms_per_step": ms_max / args.steps, "name": name, "lins": lins,
             "clocks": clocks.summary(), "kernels": kernels, "roofline": roofline,
             "breakdown_ms_per_step": breakdown_ms, "e2e": e2e,
-            "gpu_launches": KERNELS_PER_LINEAR * len(layers) * args.steps, "isolated": iso}
+            "gpu_launches": sum(L.launches for L in layers) * args.steps, "isolated": iso}
 
 
 def kernel_bench(f8, layers, device, stream, iters=20):
@@ -521,10 +618,33 @@ def run_e2e(f8, layers, args, device, stream, flops_step, world):
     total = sum_over_ranks(flops_step * args.e2e_steps, world, device)
     # the results really came back: spot-check one output against its device copy
     ok = torch.equal(host[-1][5][:4].to(device), layers[-1].dw[:4])
+    link = host_link_gbs(device, s_in, s_out)
+    moved = (h2d + d2h) * args.e2e_steps / (ms * 1e-3) / 1e9
     return {"value": total / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
             "ms_per_step": ms / args.e2e_steps, "pipelined": "3 streams (h2d, compute, d2h)",
-            "readback_check": bool(ok)}
+            "readback_check": bool(ok), "host_bytes_gbs": moved,
+            "host_link_gbs_measured": link, "frac_of_host_link": moved / link if link else None}
+
+
+def host_link_gbs(device, s_in, s_out, nbytes=256 << 20, reps=5):
+    """Pinned host<->device bandwidth of this machine with both directions busy
+    at once (as in the e2e step): bytes moved both ways / time."""
+    import torch
+    hs = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    hd = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    ds = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    dd = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        with torch.cuda.stream(s_in):
+            ds.copy_(hs, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            hd.copy_(dd, non_blocking=True)
+    torch.cuda.synchronize()
+    sec = time.perf_counter() - t0
+    return 2 * nbytes * reps / sec / 1e9
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -672,9 +792,12 @@ def main(argv=None):
     ap.add_argument("--fuse-shared-inputs", action="store_true",
                     help="merge the linears that read one input (q/k/v, w1/w3) into one linear "
                          "with the concatenated weight and a tensorwise scale over it")
-    ap.add_argument("--swiglu-input", default="given", choices=["given", "materialized", "fused"],
+    ap.add_argument("--swiglu-input", default="given",
+                    choices=["given", "materialized", "fused", "epilogue"],
                     help="for linears fed by silu(a) * b: the bf16 product given (default), "
-                         "formed by torch each step, or formed inside the quantisation")
+                         "formed by torch each step, produced from given a, b with its amax "
+                         "(f8_linear_fwd_swiglu), or formed in the epilogue of the w1+w3 "
+                         "group's GEMM and fed to w2 (implies --fuse-shared-inputs)")
     ap.add_argument("--dy-format", default="e4m3", choices=["e4m3", "e5m2"],
                     help="FP8 format of dY in the backward pass (X and W stay E4M3)")
     ap.add_argument("--kernel-bench", type=int, default=1,

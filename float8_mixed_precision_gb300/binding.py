@@ -31,7 +31,8 @@ EXPORTS = ("f8_amax", "f8_cast_transpose", "f8_gemm", "f8_linear_workspace_bytes
            "f8_linear_fwd", "f8_linear_bwd", "f8_last_device_status", "f8_status_string",
            "f8_selftest_wait_timeout", "f8_set_wait_limit_ns", "f8_linear_fwd_noalloc",
            "f8_quantize", "f8_quantize_workspace_bytes", "f8_quantize_fmt", "f8_gemm_fmt",
-           "f8_linear_bwd_fmt", "f8_quantize_swiglu", "f8_linear_fwd_swiglu")
+           "f8_linear_bwd_fmt", "f8_quantize_swiglu", "f8_linear_fwd_swiglu",
+           "f8_linear_fwd_w13_swiglu", "f8_gemm_w13_swiglu")
 
 F8_E4M3 = 0
 F8_E5M2 = 1
@@ -104,6 +105,11 @@ def lib() -> ctypes.CDLL:
         L.f8_linear_fwd_swiglu.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, ctypes.POINTER(_Saved),
                                            vp, ctypes.c_size_t, vp]
         L.f8_linear_fwd_swiglu.restype = st
+        L.f8_linear_fwd_w13_swiglu.argtypes = [vp, vp, i64, i64, i64, vp, vp, ctypes.POINTER(_Saved),
+                                               vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        L.f8_linear_fwd_w13_swiglu.restype = st
+        L.f8_gemm_w13_swiglu.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp]
+        L.f8_gemm_w13_swiglu.restype = st
         L.f8_linear_fwd_noalloc.argtypes = [vp, vp, i64, i64, i64, vp, ctypes.POINTER(_Saved), vp]
         L.f8_linear_fwd_noalloc.restype = st
         _lib = L
@@ -353,6 +359,73 @@ def f8_linear_fwd_swiglu(a: torch.Tensor, b: torch.Tensor, w: torch.Tensor,
                                       ctypes.byref(s), _ptr(ws), ws.numel(), _stream(stream)),
            "f8_linear_fwd_swiglu")
     return y, saved
+
+
+def interleave_w13(w1: torch.Tensor, w3: torch.Tensor) -> torch.Tensor:
+    """W13 [2F, K] in the row order f8_linear_fwd_w13_swiglu takes: blocks of
+    128 rows of W1 and of W3, alternating (a layout copy, no arithmetic)."""
+    F, K = w1.shape
+    if w3.shape != w1.shape or F % 128:
+        raise ValueError("w1 and w3 must both be [F, K] with F % 128 == 0")
+    return torch.stack((w1.reshape(F // 128, 128, K), w3.reshape(F // 128, 128, K)),
+                       dim=1).reshape(2 * F, K)
+
+
+def split_ab(ab: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
+    """Views a, b [M, F] (strided) of an interleaved AB [M, 2F]."""
+    M, N = ab.shape
+    v = ab.view(M, N // 256, 2, 128)
+    return v[:, :, 0, :].reshape(M, N // 2), v[:, :, 1, :].reshape(M, N // 2)
+
+
+def f8_linear_fwd_w13_swiglu(x: torch.Tensor, w13: torch.Tensor, ab: torch.Tensor | None = None,
+                             h: torch.Tensor | None = None, saved: LinearSaved | None = None,
+                             amax_h: torch.Tensor | None = None,
+                             scale_h: torch.Tensor | None = None, h_q: torch.Tensor | None = None,
+                             h_t: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                             stream=None):
+    """AB = X W13^T (Float8 linear), h = silu(a) * b and its E4M3 copies from
+    the GEMM epilogue; returns (ab, h, saved, h_q, h_t, scale_h, amax_h)."""
+    M, K = x.shape
+    N, K2 = w13.shape
+    if K != K2 or N % 256:
+        raise ValueError("w13 must be [2F, K] with F % 128 == 0")
+    F = N // 2
+    dev = x.device
+    ab = torch.empty((M, N), dtype=torch.bfloat16, device=dev) if ab is None else ab
+    h = torch.empty((M, F), dtype=torch.bfloat16, device=dev) if h is None else h
+    saved = LinearSaved.empty(M, N, K, dev) if saved is None else saved
+    amax_h = torch.empty(1, dtype=torch.float32, device=dev) if amax_h is None else amax_h
+    scale_h = torch.empty(1, dtype=torch.float32, device=dev) if scale_h is None else scale_h
+    h_q = torch.empty((M, F), dtype=torch.uint8, device=dev) if h_q is None else h_q
+    h_t = torch.empty((F, M), dtype=torch.uint8, device=dev) if h_t is None else h_t
+    ws = workspace(M, N, K, dev) if ws is None else ws
+    s = saved.c_struct()
+    _check(lib().f8_linear_fwd_w13_swiglu(_ptr(x), _ptr(w13), M, F, K, _ptr(ab), _ptr(h),
+                                          ctypes.byref(s), _ptr(amax_h), _ptr(scale_h), _ptr(h_q),
+                                          _ptr(h_t), _ptr(ws), ws.numel(), _stream(stream)),
+           "f8_linear_fwd_w13_swiglu")
+    return ab, h, saved, h_q, h_t, scale_h, amax_h
+
+
+def f8_gemm_w13_swiglu(x_q: torch.Tensor, w13_q: torch.Tensor, scale_x: torch.Tensor,
+                       scale_w13: torch.Tensor, ab: torch.Tensor | None = None,
+                       h: torch.Tensor | None = None, amax_h: torch.Tensor | None = None,
+                       stream=None):
+    """AB = q(X) q(W13)^T / (s_x s_w13) and h = silu(a) * b with max |h|;
+    returns (ab, h, amax_h)."""
+    M, K = x_q.shape
+    N, K2 = w13_q.shape
+    if K != K2 or N % 256:
+        raise ValueError("w13_q must be [2F, K] with F % 128 == 0")
+    dev = x_q.device
+    ab = torch.empty((M, N), dtype=torch.bfloat16, device=dev) if ab is None else ab
+    h = torch.empty((M, N // 2), dtype=torch.bfloat16, device=dev) if h is None else h
+    amax_h = torch.empty(1, dtype=torch.float32, device=dev) if amax_h is None else amax_h
+    _check(lib().f8_gemm_w13_swiglu(_ptr(x_q), _ptr(w13_q), M, N // 2, K, _ptr(scale_x),
+                                    _ptr(scale_w13), _ptr(ab), _ptr(h), _ptr(amax_h),
+                                    _stream(stream)), "f8_gemm_w13_swiglu")
+    return ab, h, amax_h
 
 
 def f8_linear_bwd(dy: torch.Tensor, saved: LinearSaved, K: int | None = None,

@@ -447,6 +447,72 @@ f8_status f8_linear_fwd_swiglu(const void *a, const void *b, void *h, const void
     return from_cuda(launch_gemm(fw.x_q, fw.w_q, M, N, K, saved->scale_x, saved->scale_w, y, *dev, st));
 }
 
+f8_status f8_linear_fwd_w13_swiglu(const void *x, const void *w13, int64_t M, int64_t F,
+                                   int64_t K, void *ab, void *h, const f8_linear_saved *saved,
+                                   float *amax_h, float *scale_h, uint8_t *h_q, uint8_t *h_t,
+                                   void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (M <= 0 || F <= 0 || K <= 0)
+        return F8_ERR_INVALID;
+    if (F % 128 || F > INT32_MAX / 4)
+        return F8_ERR_SHAPE;
+    const int64_t N = 2 * F;
+    F8_TRY(check_linear_shape(M, N, K));
+    F8_TRY(check_saved(saved));
+    if (x == nullptr || w13 == nullptr || ab == nullptr || h == nullptr || amax_h == nullptr ||
+        scale_h == nullptr || h_q == nullptr || h_t == nullptr || workspace == nullptr)
+        return F8_ERR_INVALID;
+    if (workspace_bytes < fwd_ws_bytes(M, N, K))
+        return F8_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(ab, 16) || !aligned(h, 16) ||
+        !aligned(h_q, 16) || !aligned(h_t, 16) || !aligned(amax_h, 4) || !aligned(scale_h, 4) ||
+        !aligned(workspace, 256))
+        return F8_ERR_ALIGN;
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const FwdWs fw = fwd_ws(workspace, M, N, K);
+    int np = 0;
+    F8_TRY_CUDA(launch_amax_partials(x, M * K, fw.parts_x, &np, *dev, st));
+    F8_TRY_CUDA(launch_cast_transpose(x, M, K, nullptr, fw.parts_x, np, saved->amax_x,
+                                      saved->scale_x, fw.x_q, saved->x_t, 0, *dev, st));
+    F8_TRY_CUDA(launch_amax_partials(w13, N * K, fw.parts_w, &np, *dev, st));
+    F8_TRY_CUDA(launch_cast_transpose(w13, N, K, nullptr, fw.parts_w, np, saved->amax_w,
+                                      saved->scale_w, fw.w_q, saved->w_t, 0, *dev, st));
+    // the X partials were consumed by the cast of X, which the GEMM's
+    // dependency wait orders before it: they take h's partials
+    int nh = 0;
+    F8_TRY_CUDA(launch_gemm_w13_swiglu(fw.x_q, fw.w_q, M, F, K, saved->scale_x, saved->scale_w, ab,
+                                       h, fw.parts_x, &nh, *dev, st));
+    return from_cuda(launch_cast_transpose(h, M, F, nullptr, fw.parts_x, nh, amax_h, scale_h, h_q,
+                                           h_t, 0, *dev, st));
+}
+
+f8_status f8_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int64_t M, int64_t F,
+                             int64_t K, const float *scale_x, const float *scale_w13, void *ab,
+                             void *h, float *amax_h, void *stream)
+{
+    if (M <= 0 || F <= 0 || K <= 0)
+        return F8_ERR_INVALID;
+    if (F % 128 || F > INT32_MAX / 4)
+        return F8_ERR_SHAPE;
+    F8_TRY(check_linear_shape(M, 2 * F, K));
+    if (x_q == nullptr || w13_q == nullptr || scale_x == nullptr || scale_w13 == nullptr ||
+        ab == nullptr || h == nullptr || amax_h == nullptr)
+        return F8_ERR_INVALID;
+    if (!aligned(x_q, 16) || !aligned(w13_q, 16) || !aligned(ab, 16) || !aligned(h, 16) ||
+        !aligned(scale_x, 4) || !aligned(scale_w13, 4) || !aligned(amax_h, 4))
+        return F8_ERR_ALIGN;
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    F8_TRY_CUDA(cudaMemsetAsync(amax_h, 0, sizeof(float), st));
+    int nh = 0;
+    return from_cuda(launch_gemm_w13_swiglu(x_q, w13_q, M, F, K, scale_x, scale_w13, ab, h,
+                                            reinterpret_cast<unsigned *>(amax_h), &nh, *dev, st,
+                                            true));
+}
+
 f8_status f8_last_device_status(void *stream)
 {
     const DeviceInfo *dev = device_info();

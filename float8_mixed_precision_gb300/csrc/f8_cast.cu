@@ -27,9 +27,12 @@
 
 #include "f8_internal.h"
 #include "f8_ptx.cuh"
+#include "f8_swiglu.cuh"
 
 namespace f8 {
 namespace {
+
+using swiglu::swiglu_x2;
 
 constexpr int kAmaxThreads = 256;
 constexpr int kAmaxUnroll = 8;
@@ -154,83 +157,6 @@ __device__ __forceinline__ uint8_t cvt1(uint16_t b, float s)
     return static_cast<uint8_t>(cvt2<FMT>(v, 0.0f) & 0xFFu);
 }
 
-// ---- the SwiGLU input of the w2 linear, h = bf16(silu(a) * b).  exp(x)
-// is Cody and Waite's range reduction (x = n ln2 + r, ln2 split into a head
-// exact in fp32 and a tail) with the degree-7 Taylor polynomial of exp(r) in
-// Horner form, scaled by 2^n; silu(a) = a * (1 / (1 + exp(-a))) with the
-// correctly rounded reciprocal.  Every step is one IEEE fp32 operation with
-// round-to-nearest-even, so the bits are those of the same steps on any IEEE
-// machine.  Two elements go through each packed fp32x2 instruction (per lane
-// the numerics of the scalar _rn operation).  n = rint(x log2e) is taken as
-// (p + 1.5 2^23) - 1.5 2^23, exact round-to-nearest-even for |p| < 2^22, and
-// 2^n is read off the low mantissa bits of the rounded sum.
-__device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
-
-__device__ __forceinline__ float exp_special(float x, float e)
-{
-    if (x != x)
-        return x;
-    if (x > 88.0f)
-        return __int_as_float(0x7F800000);
-    if (x < -87.0f)
-        return 0.0f;
-    return e;
-}
-
-// kChecked = false: the caller has shown -87 <= x <= 87 for both lanes (no
-// NaN), where the special cases cannot arise and n stays in [-126, 126].
-template <bool kChecked>
-__device__ __forceinline__ float2 exp_cw2(float2 x)
-{
-    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-    const float2 p = __fmul2_rn(x, splat(1.44269502f));
-    const float2 t = __fadd2_rn(p, splat(kRound));
-    const float2 mn = __fadd2_rn(splat(kRound), make_float2(-t.x, -t.y));  // -rint(p)
-    float2 r = __ffma2_rn(mn, splat(0.693145751953125f), x);
-    r = __ffma2_rn(mn, splat(1.42860677e-06f), r);
-    float2 q = __ffma2_rn(splat(0x1.a01a02p-13f), r, splat(0x1.6c16c2p-10f));
-    q = __ffma2_rn(q, r, splat(0x1.111112p-7f));
-    q = __ffma2_rn(q, r, splat(0x1.555556p-5f));
-    q = __ffma2_rn(q, r, splat(0x1.555556p-3f));
-    q = __ffma2_rn(q, r, splat(0.5f));
-    q = __ffma2_rn(q, r, splat(1.0f));
-    q = __ffma2_rn(q, r, splat(1.0f));
-    // bits(t) = 0x4B400000 + n, and 0x4B400000 << 23 vanishes mod 2^32
-    const float2 two_n = make_float2(__int_as_float((__float_as_int(t.x) << 23) + 0x3F800000),
-                                     __int_as_float((__float_as_int(t.y) << 23) + 0x3F800000));
-    const float2 e = __fmul2_rn(q, two_n);
-    if (!kChecked)
-        return e;
-    return make_float2(exp_special(x.x, e.x), exp_special(x.y, e.y));
-}
-
-// two packed bf16 of a and of b -> two packed bf16 of h
-template <bool kChecked>
-__device__ __forceinline__ uint32_t swiglu_x2(uint32_t a, uint32_t b)
-{
-    const float2 fa = make_float2(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
-    const float2 fb = make_float2(__uint_as_float(b << 16), __uint_as_float(b & 0xFFFF0000u));
-    const float2 e = exp_cw2<kChecked>(make_float2(-fa.x, -fa.y));
-    const float2 d = __fadd2_rn(splat(1.0f), e);
-    const float2 sl = __fmul2_rn(fa, make_float2(__frcp_rn(d.x), __frcp_rn(d.y)));
-    const float2 hf = __fmul2_rn(sl, fb);
-    const __nv_bfloat162 h = __floats2bfloat162_rn(hf.x, hf.y);
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
-
-// Eight elements; the special-value selects of exp are skipped when every
-// |a| <= 87 (bf16 0x42AE), the case for all but pathological inputs.
-__device__ __forceinline__ uint4 swiglu_x8(uint4 a, uint4 b)
-{
-    constexpr uint32_t kMag = 0x7FFF7FFFu;
-    const uint32_t m = __vmaxu2(__vmaxu2(a.x & kMag, a.y & kMag), __vmaxu2(a.z & kMag, a.w & kMag));
-    if (__vcmpgtu2(m, 0x42AE42AEu) == 0)
-        return make_uint4(swiglu_x2<false>(a.x, b.x), swiglu_x2<false>(a.y, b.y),
-                          swiglu_x2<false>(a.z, b.z), swiglu_x2<false>(a.w, b.w));
-    return make_uint4(swiglu_x2<true>(a.x, b.x), swiglu_x2<true>(a.y, b.y), swiglu_x2<true>(a.z, b.z),
-                      swiglu_x2<true>(a.w, b.w));
-}
-
 // h = silu(a) * b for the whole [n] tensors, written once as bf16, with one
 // partial maximum of |h| per CTA (as amax_kernel<true>): the amax comes out
 // of the pass that produces h, so h is read only by the cast.
@@ -254,13 +180,27 @@ swiglu_amax_kernel(const uint4 *__restrict__ a, const uint4 *__restrict__ b, uin
             va[u] = i < nvec ? __ldg(a + i) : make_uint4(0, 0, 0, 0);
             vb[u] = i < nvec ? __ldg(b + i) : make_uint4(0, 0, 0, 0);
         }
+        uint32_t amag = 0;
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            amag = swiglu::fold_abs(amag, va[u]);
+        uint4 hv[kU];
+        // one branch per 32 elements, so that their chains interleave
+        if (swiglu::small87(amag)) {
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                hv[u] = swiglu::swiglu8<false>(va[u], vb[u]);
+        } else {
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                hv[u] = swiglu::swiglu8<true>(va[u], vb[u]);
+        }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const int64_t i = base + u * S;
-            const uint4 hv = swiglu_x8(va[u], vb[u]);
             if (i < nvec) {
-                h[i] = hv;
-                m2 = max_u16x2(m2, hv);
+                h[i] = hv[u];
+                m2 = max_u16x2(m2, hv[u]);
             }
         }
     }

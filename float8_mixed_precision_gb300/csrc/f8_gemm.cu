@@ -15,6 +15,13 @@
 //               memory and write it with one TMA tensor store; the
 //               accumulator is released (tempty[a]) as soon as it has been
 //               read, so the MMAs of tile i+1 overlap the epilogue of tile i.
+// GLU = true is the W13 GEMM of a SwiGLU FFN: B holds W1 and W3 interleaved
+// by 128 rows, so the 256 columns of a tile are 128 columns of a = X W1^T and
+// the matching 128 of b = X W3^T.  The epilogue stores a and b (bf16) and
+// h = bf16(silu(a) b), formed from those bf16 values, into a second [M, N/2]
+// output, all by TMA stores, and keeps the largest |h|: one partial maximum
+// per CTA is written at the end for the cast of h (or, with hatomic, one
+// atomicMax per CTA into a zeroed fp32 amax).
 // Two shapes of the same kernel:
 //   PAIR = false  one CTA computes a 128 x BN tile (tcgen05 cta_group::1);
 //   PAIR = true   a cluster of two CTAs on neighbouring SMs computes a
@@ -42,19 +49,21 @@
 
 #include "f8_internal.h"
 #include "f8_ptx.cuh"
+#include "f8_swiglu.cuh"
 
 namespace f8 {
 namespace {
 
 constexpr int kBM = 128;   // accumulator rows per CTA (TMEM lanes)
 constexpr int kBK = 128;   // bytes of K per stage = one 128-byte swizzle row
-constexpr int kThreads = 192;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 4;       // one per TMEM lane quarter
+constexpr int kGluCols = 32;       // GLU: h columns per epilogue step
+constexpr int kGluBoxBytes = 32 * kGluCols * 2;  // one 32 x 64-byte box, 64-byte swizzle
 constexpr int kEpiCols = 64;                       // columns per epilogue step
 constexpr int kEpiBufBytes = 32 * kEpiCols * 2;    // 32 rows x 128 bytes
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
-template <int BN, int STAGES, bool PAIR>
+template <int BN, int STAGES, bool PAIR, bool GLU = false>
 struct Cfg {
     static constexpr int kTileM = PAIR ? 2 * kBM : kBM;
     static constexpr int kBRows = PAIR ? BN / 2 : BN;  // rows of B each CTA loads
@@ -62,11 +71,16 @@ struct Cfg {
     static constexpr int kBBytes = kBRows * kBK;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = (2 * BN <= 256) ? 256 : 512;
-    static constexpr int kStagingBytes = kEpiWarps * 2 * kEpiBufBytes;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
+    // per epilogue warp: plain, two 32 x 128-byte swizzled store buffers;
+    // GLU, one set of three 32 x 64-byte boxes (a, b, h)
+    static constexpr int kWarpStaging = GLU ? 3 * kGluBoxBytes : 2 * kEpiBufBytes;
+    static constexpr int kStagingBytes = kEpiWarps * kWarpStaging;
     static constexpr int kBarBytes = 8 * (2 * STAGES + 5) + 16;
     static constexpr int kSmemBytes = STAGES * kStageBytes + kStagingBytes + kBarBytes + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(BN % kEpiCols == 0, "epilogue steps");
+    static_assert(!GLU || BN == 256, "a GLU tile is 128 columns of a and 128 of b");
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group_m, int &mb,
@@ -93,14 +107,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// eight fp32 accumulators x inv (one packed fp32x2 multiply per pair, per
+// lane the scalar round-to-nearest product), rounded to bf16 and packed
+__device__ __forceinline__ uint32_t scale2(const uint32_t *r, float2 inv2)
+{
+    const float2 v = __fmul2_rn(make_float2(__uint_as_float(r[0]), __uint_as_float(r[1])), inv2);
+    return pack_bf16x2(v.x, v.y);
+}
+
 __device__ __forceinline__ uint4 pack8(const uint32_t *r, float inv)
 {
-    uint4 o;
-    o.x = pack_bf16x2(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
-    o.y = pack_bf16x2(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
-    o.z = pack_bf16x2(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
-    o.w = pack_bf16x2(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
-    return o;
+    const float2 inv2 = make_float2(inv, inv);
+    return make_uint4(scale2(r, inv2), scale2(r + 2, inv2), scale2(r + 4, inv2),
+                      scale2(r + 6, inv2));
 }
 
 // One warp's share of an accumulator: TMEM lanes [32q, 32q + 32) x BN
@@ -155,15 +174,85 @@ __device__ __forceinline__ void epilogue_rows(uint32_t taddr, int row0, int col_
     }
 }
 
-template <int BN, int STAGES, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
-gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-            const __grid_constant__ CUtensorMap tma_c, __nv_bfloat16 *__restrict__ c, int M, int N,
-            int K, const float *__restrict__ sa, const float *__restrict__ sb,
-            unsigned *__restrict__ status, uint64_t limit_ns, int group_m, int tma_store,
-            uint32_t idesc)
+// The GLU epilogue of one warp: TMEM lanes [32q, 32q + 32) of a W13 tile,
+// accumulator columns [0, 128) = a and [128, 256) = the matching b.  Per
+// step of 32 h columns: a and b are scaled and rounded exactly as in
+// epilogue_rows, h = bf16(silu(a) b) is formed from those bf16 values, and
+// the three 32 x 32 blocks (row = lane, 64 bytes each) are staged in boxes
+// laid out in the TMA 64-byte swizzle (16-byte chunk q of row r at chunk
+// q ^ ((r / 2) % 4), which keeps each 8-lane phase of a 16-byte shared store
+// on 8 distinct bank groups) and written with three TMA stores (AB columns col_base +
+// c and col_base + 128 + c, h columns col_base / 2 + c): whole-line bulk
+// writes, which keep the L2 request rate of the epilogue at the plain
+// epilogue's.  The box set is reused once the previous step's stores have
+// read it; the next accumulator load is issued before that wait.
+__device__ __forceinline__ void epilogue_rows_glu(uint32_t taddr, int row0, int col_base, int M,
+                                                  float inv, const CUtensorMap *tma_ab,
+                                                  const CUtensorMap *tma_h, uint8_t *stage,
+                                                  uint32_t &hmax2, int lane)
 {
-    using C = Cfg<BN, STAGES, PAIR>;
+    uint8_t *sa = stage;
+    uint8_t *sb = stage + kGluBoxBytes;
+    uint8_t *sh = stage + 2 * kGluBoxBytes;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += kGluCols) {
+        uint32_t ra[32], rb[32];
+        tc_ld_32x32b_x32(taddr + c, ra);
+        tc_ld_32x32b_x32(taddr + 128 + c, rb);
+        if (lane == 0)
+            bulk_wait_group_read<0>();  // the previous step's stores have read the boxes
+        __syncwarp();
+        tc_wait_ld();
+        uint4 a8[4], b8[4], h8[4];
+        uint32_t amag = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            a8[q] = pack8(&ra[8 * q], inv);
+            b8[q] = pack8(&rb[8 * q], inv);
+            amag = swiglu::fold_abs(amag, a8[q]);
+        }
+        // one branch per 32 elements, so that their chains interleave
+        if (swiglu::small87(amag)) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                h8[q] = swiglu::swiglu8<false>(a8[q], b8[q]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                h8[q] = swiglu::swiglu8<true>(a8[q], b8[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            hmax2 = swiglu::max_abs2(hmax2, h8[q].x);
+            hmax2 = swiglu::max_abs2(hmax2, h8[q].y);
+            hmax2 = swiglu::max_abs2(hmax2, h8[q].z);
+            hmax2 = swiglu::max_abs2(hmax2, h8[q].w);
+            const int off = lane * (kGluCols * 2) + ((q ^ ((lane >> 1) & 3)) << 4);
+            *reinterpret_cast<uint4 *>(sa + off) = a8[q];
+            *reinterpret_cast<uint4 *>(sb + off) = b8[q];
+            *reinterpret_cast<uint4 *>(sh + off) = h8[q];
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0 && row0 < M) {
+            tma_store_2d(tma_ab, sa, col_base + c, row0);
+            tma_store_2d(tma_ab, sb, col_base + 128 + c, row0);
+            tma_store_2d(tma_h, sh, col_base / 2 + c, row0);
+            bulk_commit_group();
+        }
+    }
+}
+
+template <int BN, int STAGES, bool PAIR, bool GLU>
+__global__ void __launch_bounds__(Cfg<BN, STAGES, PAIR, GLU>::kThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+            const __grid_constant__ CUtensorMap tma_c, const __grid_constant__ CUtensorMap tma_h,
+            __nv_bfloat16 *__restrict__ c, int M, int N, int K, const float *__restrict__ sa,
+            const float *__restrict__ sb, unsigned *__restrict__ status, uint64_t limit_ns,
+            int group_m, int tma_store, uint32_t idesc, unsigned *__restrict__ hparts,
+            int hatomic)
+{
+    using C = Cfg<BN, STAGES, PAIR, GLU>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -177,6 +266,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
     uint64_t *drain = tempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    unsigned *hmax_cta = reinterpret_cast<unsigned *>(tmem_slot + 2);  // GLU: largest |h| bits
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -200,6 +290,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
+        *hmax_cta = 0u;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -207,6 +298,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
         tma_prefetch_desc(&tma_b);
         if (tma_store)
             tma_prefetch_desc(&tma_c);
+        if (GLU)
+            tma_prefetch_desc(&tma_h);
     }
     if (warp == 1) {
         if (PAIR) {
@@ -357,7 +450,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
         const int quad = warp & 3;  // the TMEM lane quarter this warp may read
         const float inv = static_cast<float>(1.0 / (static_cast<double>(*sa) *
                                                      static_cast<double>(*sb)));
-        uint8_t *my_stage = staging + (warp - 2) * 2 * kEpiBufBytes;
+        uint8_t *my_stage = staging + (warp - 2) * C::kWarpStaging;
+        uint32_t hmax2 = 0;
         const uint32_t tempty_leader = PAIR ? cluster_map(smem_addr(&tempty[0]), 0) : 0u;
         uint32_t buf = 0;
         int local = 0;
@@ -376,8 +470,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
             tile_coords(tile, num_m, num_n, group_m, mb, nb);
             const int row0 = mb * C::kTileM + static_cast<int>(rank) * kBM + quad * 32;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
-            epilogue_rows<BN>(taddr, row0, nb * BN, M, N, inv, c, &tma_c, tma_store != 0, my_stage,
-                              buf, lane);
+            if (GLU)
+                epilogue_rows_glu(taddr, row0, nb * BN, M, inv, &tma_c, &tma_h, my_stage, hmax2,
+                                  lane);
+            else
+                epilogue_rows<BN>(taddr, row0, nb * BN, M, N, inv, c, &tma_c, tma_store != 0,
+                                  my_stage, buf, lane);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
@@ -390,6 +488,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
         if (lane == 0)
             bulk_wait_group_all();
         __syncwarp();
+        if (GLU) {
+            const unsigned m = __reduce_max_sync(0xFFFFFFFFu, max(hmax2 & 0xFFFFu, hmax2 >> 16));
+            if (lane == 0)
+                atomicMax(hmax_cta, m);
+        }
     }
 
     tc_fence_before_sync();
@@ -397,6 +500,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
         cluster_sync();
     else
         __syncthreads();
+    if (GLU && threadIdx.x == 0) {
+        const unsigned m = *hmax_cta;
+        if (m >= 0x7F80u)
+            atomicOr(status, kStatusNonfinite);
+        if (hatomic)
+            atomicMax(hparts, m << 16);  // fp32 bits of the bf16 |h|: integer order = numeric
+        else
+            hparts[blockIdx.x] = m << 16;
+    }
     if (warp == 1) {
         tc_fence_after_sync();
         if (PAIR)
@@ -457,26 +569,40 @@ bool make_map(CUtensorMap *map, CUtensorMapDataType dtype, int esize, const void
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, bool PAIR>
+template <int BN, int STAGES, bool PAIR, bool GLU = false>
 cudaError_t run_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
                      const float *sa, const float *sb, void *c, const DeviceInfo &dev,
-                     cudaStream_t stream, int fa, int fb)
+                     cudaStream_t stream, int fa, int fb, void *h = nullptr,
+                     unsigned *hparts = nullptr, int *nparts = nullptr, int hatomic = 0)
 {
-    using C = Cfg<BN, STAGES, PAIR>;
-    CUtensorMap ma, mb, mc;
+    using C = Cfg<BN, STAGES, PAIR, GLU>;
+    CUtensorMap ma, mb, mc, mh;
     if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a, M, K, kBK, kBM) ||
         !make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, N, K, kBK, C::kBRows))
         return cudaErrorNotSupported;
     // TMA stores need every C row to start on a 16-byte boundary
-    int tma_store = (N % 8 == 0) &&
+    int tma_store;
+    if (GLU) {
+        // AB and h through 32-row x 32-column boxes in the 64-byte swizzle
+        tma_store = 1;
+        if (N % 256 != 0 ||
+            !make_tensor_map_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, M, N, kGluCols, 32,
+                                CU_TENSOR_MAP_SWIZZLE_64B) ||
+            !make_tensor_map_2d(&mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, M, N / 2, kGluCols,
+                                32, CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorNotSupported;
+    } else {
+        tma_store = (N % 8 == 0) &&
                     make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, M, N, kEpiCols, 32);
-    if (!tma_store)
-        mc = ma;  // not used by the kernel
+        if (!tma_store)
+            mc = ma;  // not used by the kernel
+        mh = ma;      // not used by the kernel
+    }
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
     const int dv = dev.ordinal & 63;
     std::call_once(attr_once[dv], [&] {
-        attr_err[dv] = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, PAIR>,
+        attr_err[dv] = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, PAIR, GLU>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             C::kSmemBytes);
     });
@@ -486,13 +612,16 @@ cudaError_t run_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, i
     const int64_t max_units = PAIR ? dev.sm_count / 2 : dev.sm_count;
     const int units = static_cast<int>(tiles < max_units ? tiles : max_units);
     const int group_m = PAIR ? 8 : 16;
-    return launch_pdl_cluster(gemm_kernel<BN, STAGES, PAIR>, dim3((PAIR ? 2 : 1) * units),
-                              dim3(kThreads), C::kSmemBytes, stream, PAIR ? 2u : 1u, ma, mb, mc,
-                              static_cast<__nv_bfloat16 *>(c), static_cast<int>(M),
+    if (nparts != nullptr)
+        *nparts = (PAIR ? 2 : 1) * units;
+    return launch_pdl_cluster(gemm_kernel<BN, STAGES, PAIR, GLU>, dim3((PAIR ? 2 : 1) * units),
+                              dim3(C::kThreads), C::kSmemBytes, stream, PAIR ? 2u : 1u, ma, mb, mc,
+                              mh, static_cast<__nv_bfloat16 *>(c), static_cast<int>(M),
                               static_cast<int>(N), static_cast<int>(K), sa, sb, dev.status,
                               wait_limit_ns(), group_m, tma_store,
                               idesc_f8_f32(C::kTileM, BN, static_cast<uint32_t>(fa),
-                                           static_cast<uint32_t>(fb)));
+                                           static_cast<uint32_t>(fb)),
+                              hparts, hatomic);
 }
 
 constexpr int kVariantSingle = 1;
@@ -536,6 +665,20 @@ cudaError_t launch_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N
     if (gemm_variant(M, dev) == kVariantPair)
         return run_gemm<256, 6, true>(a, b, M, N, K, sa, sb, c, dev, stream, fa, fb);
     return run_gemm<256, 4, false>(a, b, M, N, K, sa, sb, c, dev, stream, fa, fb);
+}
+
+cudaError_t launch_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int64_t M, int64_t F,
+                                   int64_t K, const float *sx, const float *sw, void *ab, void *h,
+                                   unsigned *hparts, int *nparts, const DeviceInfo &dev,
+                                   cudaStream_t stream, bool hatomic)
+{
+    if (F % 128 != 0)
+        return cudaErrorInvalidValue;
+    if (gemm_variant(M, dev) == kVariantPair)
+        return run_gemm<256, 6, true, true>(x_q, w13_q, M, 2 * F, K, sx, sw, ab, dev, stream, 0, 0,
+                                            h, hparts, nparts, hatomic ? 1 : 0);
+    return run_gemm<256, 4, false, true>(x_q, w13_q, M, 2 * F, K, sx, sw, ab, dev, stream, 0, 0, h,
+                                         hparts, nparts, hatomic ? 1 : 0);
 }
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, const DeviceInfo &dev, cudaStream_t stream)

@@ -122,6 +122,16 @@ cudaError_t launch_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N
                         const float *sa, const float *sb, void *c, const DeviceInfo &dev,
                         cudaStream_t stream, int fa = 0, int fb = 0);
 
+// The W13 GEMM of a SwiGLU FFN: AB[M, 2F] = bf16(X W13^T / (sx sw)) with
+// W13 interleaved by 128 rows (W1 block, W3 block, ...), and h[M, F] =
+// bf16(silu(a) b) from its epilogue with one |h| partial maximum per CTA in
+// hparts (*nparts receives their count), or with hatomic one atomicMax per
+// CTA into hparts[0] (a zeroed fp32 amax).  F % 128 == 0.
+cudaError_t launch_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int64_t M, int64_t F,
+                                   int64_t K, const float *sx, const float *sw, void *ab, void *h,
+                                   unsigned *hparts, int *nparts, const DeviceInfo &dev,
+                                   cudaStream_t stream, bool hatomic = false);
+
 // One CTA waiting on an mbarrier that is never signalled (failure-path test).
 cudaError_t launch_wait_selftest(uint64_t limit_ns, const DeviceInfo &dev, cudaStream_t stream);
 

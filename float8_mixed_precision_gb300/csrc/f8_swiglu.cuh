@@ -1,0 +1,141 @@
+// SwiGLU of bf16 pairs, shared by the producing pass (f8_cast.cu) and the
+// W13 GEMM epilogue (f8_gemm.cu).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace f8 {
+namespace swiglu {
+
+// ---- the SwiGLU input of the w2 linear, h = bf16(silu(a) * b).  exp(x)
+// is Cody and Waite's range reduction (x = n ln2 + r, ln2 split into a head
+// exact in fp32 and a tail) with the degree-7 Taylor polynomial of exp(r) in
+// Horner form, scaled by 2^n; silu(a) = a * (1 / (1 + exp(-a))) with the
+// correctly rounded reciprocal.  Every step is one IEEE fp32 operation with
+// round-to-nearest-even, so the bits are those of the same steps on any IEEE
+// machine.  Two elements go through each packed fp32x2 instruction (per lane
+// the numerics of the scalar _rn operation).  n = rint(x log2e) is taken as
+// (p + 1.5 2^23) - 1.5 2^23, exact round-to-nearest-even for |p| < 2^22, and
+// 2^n is read off the low mantissa bits of the rounded sum.
+__device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
+
+__device__ __forceinline__ float exp_special(float x, float e)
+{
+    if (x != x)
+        return x;
+    if (x > 88.0f)
+        return __int_as_float(0x7F800000);
+    if (x < -87.0f)
+        return 0.0f;
+    return e;
+}
+
+// kChecked = false: the caller has shown -87 <= x <= 87 for both lanes (no
+// NaN), where the special cases cannot arise and n stays in [-126, 126].
+template <bool kChecked>
+__device__ __forceinline__ float2 exp_cw2(float2 x)
+{
+    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+    const float2 p = __fmul2_rn(x, splat(1.44269502f));
+    const float2 t = __fadd2_rn(p, splat(kRound));
+    const float2 mn = __fadd2_rn(splat(kRound), make_float2(-t.x, -t.y));  // -rint(p)
+    float2 r = __ffma2_rn(mn, splat(0.693145751953125f), x);
+    r = __ffma2_rn(mn, splat(1.42860677e-06f), r);
+    float2 q = __ffma2_rn(splat(0x1.a01a02p-13f), r, splat(0x1.6c16c2p-10f));
+    q = __ffma2_rn(q, r, splat(0x1.111112p-7f));
+    q = __ffma2_rn(q, r, splat(0x1.555556p-5f));
+    q = __ffma2_rn(q, r, splat(0x1.555556p-3f));
+    q = __ffma2_rn(q, r, splat(0.5f));
+    q = __ffma2_rn(q, r, splat(1.0f));
+    q = __ffma2_rn(q, r, splat(1.0f));
+    // bits(t) = 0x4B400000 + n, and 0x4B400000 << 23 vanishes mod 2^32
+    const float2 two_n = make_float2(__int_as_float((__float_as_int(t.x) << 23) + 0x3F800000),
+                                     __int_as_float((__float_as_int(t.y) << 23) + 0x3F800000));
+    const float2 e = __fmul2_rn(q, two_n);
+    if (!kChecked)
+        return e;
+    return make_float2(exp_special(x.x, e.x), exp_special(x.y, e.y));
+}
+
+// 1/d correctly rounded, two lanes, for d in [1, 2^126): the hardware's
+// approximate reciprocal refined by two Newton-Raphson steps in Markstein's
+// residual form (e = 1 - d y by one FMA, then y + y e), and d = (2 - 2^-23)
+// 2^k, the one input class the refinement can leave one ulp off, set to its
+// correctly rounded reciprocal (1 + 2^-23) 2^-(k+1) directly.  Every
+// significand of d has been checked against IEEE division with seeds up to
+// 8 ulp off.  Branch-free, so consecutive elements interleave.
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ float fix_all_ones(float d, float y)
+{
+    const uint32_t bd = __float_as_uint(d);
+    return (bd & 0x7FFFFFu) == 0x7FFFFFu ? __uint_as_float(0x7E800001u - (bd & 0x7F800000u)) : y;
+}
+
+__device__ __forceinline__ float2 rcp2_refined(float2 d)
+{
+    const float2 nd = make_float2(-d.x, -d.y);
+    float2 y = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+    float2 e = __ffma2_rn(nd, y, splat(1.0f));
+    y = __ffma2_rn(y, e, y);
+    e = __ffma2_rn(nd, y, splat(1.0f));
+    y = __ffma2_rn(y, e, y);
+    return make_float2(fix_all_ones(d.x, y.x), fix_all_ones(d.y, y.y));
+}
+
+// two packed bf16 of a and of b -> two packed bf16 of h.  kChecked = false
+// requires |a| <= 87 in both lanes: exp needs no special values and
+// 1 + exp(-a) lies in [1, 2^126), the refined reciprocal's range.
+template <bool kChecked>
+__device__ __forceinline__ uint32_t swiglu_x2(uint32_t a, uint32_t b)
+{
+    const float2 fa = make_float2(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
+    const float2 fb = make_float2(__uint_as_float(b << 16), __uint_as_float(b & 0xFFFF0000u));
+    const float2 e = exp_cw2<kChecked>(make_float2(-fa.x, -fa.y));
+    const float2 d = __fadd2_rn(splat(1.0f), e);
+    const float2 r = kChecked ? make_float2(__frcp_rn(d.x), __frcp_rn(d.y)) : rcp2_refined(d);
+    const float2 hf = __fmul2_rn(__fmul2_rn(fa, r), fb);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(hf.x, hf.y);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+template <bool kChecked>
+__device__ __forceinline__ uint4 swiglu8(uint4 a, uint4 b)
+{
+    return make_uint4(swiglu_x2<kChecked>(a.x, b.x), swiglu_x2<kChecked>(a.y, b.y),
+                      swiglu_x2<kChecked>(a.z, b.z), swiglu_x2<kChecked>(a.w, b.w));
+}
+
+// Packed maximum of |a| over eight bf16, to gate a group onto the fast path
+// (every |a| <= 87, bf16 0x42AE, when small87 of the fold is true).
+__device__ __forceinline__ uint32_t fold_abs(uint32_t m, uint4 a)
+{
+    constexpr uint32_t kMag = 0x7FFF7FFFu;
+    return __vmaxu2(__vmaxu2(m, __vmaxu2(a.x & kMag, a.y & kMag)), __vmaxu2(a.z & kMag, a.w & kMag));
+}
+
+__device__ __forceinline__ bool small87(uint32_t m) { return __vcmpgtu2(m, 0x42AE42AEu) == 0; }
+
+// Eight elements with their own gate.
+__device__ __forceinline__ uint4 swiglu_x8(uint4 a, uint4 b)
+{
+    return small87(fold_abs(0u, a)) ? swiglu8<false>(a, b) : swiglu8<true>(a, b);
+}
+
+// |h| of a packed bf16 pair folded into a running packed maximum (bit order
+// is numeric order for non-negative bf16; NaN and inf sort above all finite).
+__device__ __forceinline__ uint32_t max_abs2(uint32_t m, uint32_t h2)
+{
+    return __vmaxu2(m, h2 & 0x7FFF7FFFu);
+}
+
+} // namespace swiglu
+} // namespace f8

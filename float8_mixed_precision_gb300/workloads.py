@@ -159,6 +159,7 @@ def linear_inputs(c: int, l: int, lin: Linear | None = None) -> dict[str, torch.
 # read the attention-norm output, w1 and w3 the FFN-norm output.
 SHARED_INPUT_GROUPS = {2: [["wq", "wk", "wv"], ["wo"]],
                        3: [["w1", "w3"], ["w2"]],
+                       4: [["w1", "w3"], ["w2"]],
                        5: [["wq", "wk", "wv"], ["wo"], ["w1", "w3"], ["w2"]]}
 
 
@@ -183,6 +184,26 @@ def fused_group_inputs(c: int, idx: list[int]) -> dict[str, torch.Tensor]:
     parts = [linear_inputs(c, i) for i in idx]
     return {"x": parts[0]["x"], "w": torch.cat([p["w"] for p in parts], 0),
             "dy": torch.cat([p["dy"] for p in parts], 1)}
+
+
+def interleave_128(t1: torch.Tensor, t3: torch.Tensor, dim: int) -> torch.Tensor:
+    """Blocks of 128 along `dim` taken from t1 and t3 alternately (the row
+    order of W13, and the column order of AB and its gradient): a copy, no
+    arithmetic."""
+    n = t1.shape[dim]
+    assert t3.shape == t1.shape and n % 128 == 0
+    a = t1.unflatten(dim, (n // 128, 128))
+    b = t3.unflatten(dim, (n // 128, 128))
+    return torch.stack((a, b), dim=dim + 1).flatten(dim, dim + 2)
+
+
+def w13_group_inputs(c: int, idx: list[int]) -> dict[str, torch.Tensor]:
+    """The group {w1, w3} of workload c for the SwiGLU-epilogue linear: X of
+    w1, W13 with W1 and W3 rows interleaved by 128, and the group's dY
+    [M, 2F] with dY1 and dY3 columns interleaved the same way."""
+    p1, p3 = linear_inputs(c, idx[0]), linear_inputs(c, idx[1])
+    return {"x": p1["x"], "w": interleave_128(p1["w"], p3["w"], 0),
+            "dy": interleave_128(p1["dy"], p3["dy"], 1)}
 
 
 def custom_linear(M: int, K: int, N: int, seed: int, x_std=1.0, w_std=0.02, dy_std=1.0):

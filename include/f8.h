@@ -256,6 +256,63 @@ f8_status f8_linear_fwd_swiglu(const void *a, const void *b, void *h, const void
                                void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The input side of a SwiGLU FFN (the FeedForward of torchtitan's Llama 3.1:
+ * w2(silu(w1(x)) * w3(x))) as one Float8 linear whose GEMM epilogue also
+ * forms the w2 input and its amax:
+ *   AB = bf16(q(X) q(W13)^T / (s_x s_w13)), the Float8 linear of the group
+ *        {w1, w3} that shares X (one tensorwise scale over W13, as for every
+ *        concatenated weight);
+ *   h  = bf16(silu(a) * b), formed in the epilogue from the bf16 a and b just
+ *        rounded, with silu as in f8_quantize_swiglu;
+ *   amax(h) taken in the same epilogue (one partial per CTA), then h cast to
+ *        E4M3 with both copies.
+ * Against f8_linear_fwd on W13 followed by f8_quantize_swiglu, a and b are
+ * not read back (4 B per element of h) and the SiLU arithmetic runs under
+ * the GEMM's main loop.  Launches: amax and cast of X, amax and cast of W13,
+ * the GEMM, the cast of h.
+ *   x:     device bf16 [M, K].
+ *   w13:   device bf16 [2F, K], W1 and W3 interleaved by 128 rows: rows
+ *          [256j, 256j + 128) are W1 rows [128j, 128j + 128) and rows
+ *          [256j + 128, 256j + 256) are W3 rows [128j, 128j + 128).
+ *          F % 128 == 0, K % 16 == 0, M % 16 == 0.
+ *   ab:    device bf16 [M, 2F] receiving a and b, interleaved like W13 (a
+ *          tensor of the forward kept for the SwiGLU backward).
+ *   h:     device bf16 [M, F] receiving h.
+ *   saved: receives q(X)^T, q(W13)^T, their amax and scales, as f8_linear_fwd
+ *          with N = 2F does, so f8_linear_bwd (N = 2F, dY interleaved like
+ *          AB) is the group's backward.
+ *   amax_h, scale_h: device fp32 scalars receiving h's amax and scale.
+ *   h_q:   device E4M3 [M, F], q(h) row-major: the A operand of the w2 GEMM
+ *          (f8_gemm(h_q, q(W2), ..., scale_h, s_w2)).
+ *   h_t:   device E4M3 [F, M], q(h)^T: the w2 linear's saved input.
+ *   workspace: f8_linear_workspace_bytes(M, 2F, K) bytes, 256-byte aligned.
+ * All device pointers 16-byte aligned (amax_h, scale_h: 4).  F8_ERR_SHAPE
+ * if F is not a positive multiple of 128.
+ */
+f8_status f8_linear_fwd_w13_swiglu(const void *x, const void *w13, int64_t M, int64_t F,
+                                   int64_t K, void *ab, void *h, const f8_linear_saved *saved,
+                                   float *amax_h, float *scale_h, uint8_t *h_q, uint8_t *h_t,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The GEMM of f8_linear_fwd_w13_swiglu alone, for callers that quantise X
+ * and W13 themselves (e.g. a W13 quantised once per optimiser step):
+ * AB = bf16(q(X) q(W13)^T / (scale_x scale_w13)) and h = bf16(silu(a) * b)
+ * from the epilogue, with max |h| written to amax_h.
+ *   x_q:   device E4M3 [M, K]; w13_q: device E4M3 [2F, K], rows interleaved
+ *          as for f8_linear_fwd_w13_swiglu; F % 128 == 0, M % 16 == 0,
+ *          K % 16 == 0.
+ *   scale_x, scale_w13: device fp32 scalars.
+ *   ab:    device bf16 [M, 2F]; h: device bf16 [M, F].
+ *   amax_h: device fp32, zeroed by this call (a 4-byte memset on `stream`)
+ *          and then raised by one atomicMax per CTA; it is ready for
+ *          f8_cast_transpose(h, ...).  A non-finite h sets F8_ERR_NONFINITE.
+ */
+f8_status f8_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int64_t M, int64_t F,
+                             int64_t K, const float *scale_x, const float *scale_w13, void *ab,
+                             void *h, float *amax_h, void *stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns F8_OK, F8_ERR_NONFINITE or F8_ERR_TIMEOUT (the first set
  * bit in that order of severity: TIMEOUT wins), or F8_ERR_CUDA if the

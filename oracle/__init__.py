@@ -322,6 +322,29 @@ def linear_fwd_swiglu(a_bits: np.ndarray, b_bits: np.ndarray, w_bits: np.ndarray
     return out
 
 
+def split_ab(ab_bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """a, b [M, F] of the group {w1, w3}'s output AB [M, 2F] when W13 takes
+    its rows from W1 and W3 alternately in blocks of 128: column c of a is
+    column 256 (c // 128) + c % 128 of AB, column c of b the one 128 to its
+    right."""
+    ab = _u16(ab_bits)
+    M, N = ab.shape
+    v = ab.reshape(M, N // 256, 2, 128)
+    return (np.ascontiguousarray(v[:, :, 0, :].reshape(M, N // 2)),
+            np.ascontiguousarray(v[:, :, 1, :].reshape(M, N // 2)))
+
+
+def linear_fwd_w13_swiglu(x_bits: np.ndarray, w13_bits: np.ndarray) -> dict:
+    """The input side of a SwiGLU FFN: AB = linear_fwd(X, W13) (one Float8
+    linear for the group {w1, w3}, one scale over W13), then h = bf16(silu(a)
+    * b) from AB's bf16 a and b, then h quantised for the w2 linear."""
+    out = linear_fwd(x_bits, w13_bits)
+    a, b = split_ab(out["y"])
+    out["h"] = swiglu_h(a, b)
+    out["qh"] = quantize(out["h"])
+    return out
+
+
 def linear_bwd(dy_bits: np.ndarray, fwd: dict, dy_fmt: int = E4M3) -> dict:
     """dX = dY W, dW = dY^T X using the forward's quantised X and W; dY is
     quantised in format dy_fmt (E4M3 or E5M2)."""

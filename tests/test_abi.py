@@ -87,3 +87,50 @@ def test_other_calls_reject_bad_arguments_on_host(L):
     bad = _Saved(FAKE, None, FAKE, FAKE, FAKE, FAKE)
     assert L.f8_linear_bwd(FAKE, ctypes.byref(bad), 16, 16, 16, FAKE, FAKE, FAKE, ws, None) == 1
     assert L.f8_linear_bwd(FAKE, ctypes.byref(s), 16, 16, 16, FAKE_MIS, FAKE, FAKE, ws, None) == 2
+
+
+def test_w13_swiglu_rejects_bad_arguments_on_host(L):
+    from float8_mixed_precision_gb300.binding import _Saved
+    s = _Saved(FAKE, FAKE, FAKE, FAKE + 4, FAKE + 8, FAKE + 12)
+    ws = 1 << 30
+    f = L.f8_linear_fwd_w13_swiglu
+    ok = (FAKE, FAKE, 256, 128, 64, FAKE, FAKE, ctypes.byref(s), FAKE, FAKE + 4, FAKE, FAKE, FAKE,
+          ws, None)
+
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+
+    assert call(a3=192) == 3            # F % 128
+    assert call(a3=0) == 1              # F = 0
+    assert call(a2=24) == 3             # M % 16
+    assert call(a4=40) == 3             # K % 16
+    assert call(a5=None) == 1           # AB missing
+    assert call(a6=None) == 1           # h missing
+    assert call(a7=None) == 1           # saved missing
+    assert call(a10=None) == 1          # h_q missing
+    assert call(a13=10) == 1            # workspace too small
+    assert call(a6=FAKE_MIS) == 2       # h misaligned
+    assert call(a12=FAKE + 16) == 2     # workspace not 256-byte aligned
+
+
+def test_gemm_w13_swiglu_rejects_bad_arguments_on_host(L):
+    f = L.f8_gemm_w13_swiglu
+    assert f(FAKE, FAKE, 256, 192, 64, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 3   # F % 128
+    assert f(FAKE, FAKE, 256, 128, 0, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 1    # K = 0
+    assert f(FAKE, FAKE, 256, 128, 64, FAKE, FAKE, FAKE, FAKE, None, None) == 1   # amax_h
+    assert f(FAKE, FAKE, 256, 128, 64, FAKE, FAKE, FAKE_MIS, FAKE, FAKE, None) == 2
+
+
+def test_package_exposes_every_binding_wrapper():
+    """Each C entry point that has a Python wrapper is reachable from the
+    package itself (no GPU needed: nothing is called)."""
+    import float8_mixed_precision_gb300 as f8
+    from float8_mixed_precision_gb300 import binding
+    for n in binding.EXPORTS:
+        if hasattr(binding, n):
+            assert hasattr(f8, n), n
+    for n in ("interleave_w13", "split_ab", "LinearSaved", "workspace"):
+        assert hasattr(f8, n), n

@@ -1,0 +1,72 @@
+"""The Python binding's marshalling, without a GPU: every wrapper is called on
+small CPU tensors against a stand-in for libf8 that checks the argument count
+of each C call against the argtypes the real library was given, records the
+call and returns F8_OK.  Nothing runs on a device; this catches wrappers whose
+C call no longer matches include/f8.h."""
+import ctypes
+
+import pytest
+import torch
+
+from float8_mixed_precision_gb300 import binding
+
+
+class _Recorder:
+    def __init__(self, real):
+        self.real = real
+        self.calls = []
+
+    def __getattr__(self, name):
+        fn = getattr(self.real, name)
+
+        def call(*args):
+            assert len(args) == len(fn.argtypes), (name, len(args), len(fn.argtypes))
+            self.calls.append(name)
+            if fn.restype is ctypes.c_size_t:
+                return 4096
+            return 0
+        return call
+
+
+@pytest.fixture()
+def rec(monkeypatch):
+    from float8_mixed_precision_gb300 import build
+    build.build()
+    real = binding.lib()
+    r = _Recorder(real)
+    monkeypatch.setattr(binding, "lib", lambda: r)
+    monkeypatch.setattr(binding, "_ptr", lambda t: None if t is None else t.data_ptr())
+    monkeypatch.setattr(binding, "_stream", lambda s: 0)
+    return r
+
+
+def _bf(*shape):
+    return torch.zeros(shape, dtype=torch.bfloat16)
+
+
+def test_every_wrapper_marshals(rec):
+    M, N, K, F = 32, 48, 64, 128
+    x, w, dy = _bf(M, K), _bf(N, K), _bf(M, N)
+    binding.f8_amax(x)
+    binding.f8_cast_transpose(x, torch.ones(1), torch.ones(1))
+    binding.f8_quantize(x)
+    binding.f8_quantize(x, fmt=binding.F8_E5M2)
+    q = torch.zeros((M, K), dtype=torch.uint8)
+    binding.f8_gemm(q, torch.zeros((N, K), dtype=torch.uint8), torch.ones(1), torch.ones(1))
+    binding.f8_gemm(q, torch.zeros((N, K), dtype=torch.uint8), torch.ones(1), torch.ones(1),
+                    fmt_a=binding.F8_E5M2)
+    y, saved = binding.f8_linear_fwd(x, w)
+    binding.f8_linear_fwd_noalloc(x, w)
+    binding.f8_linear_bwd(dy, saved)
+    binding.f8_linear_bwd(dy, saved, dy_fmt=binding.F8_E5M2)
+    binding.f8_quantize_swiglu(x, x)
+    binding.f8_linear_fwd_swiglu(x, x, w)
+    binding.f8_linear_fwd_w13_swiglu(x, _bf(2 * F, K))
+    binding.f8_gemm_w13_swiglu(q, torch.zeros((2 * F, K), dtype=torch.uint8), torch.ones(1),
+                               torch.ones(1))
+    binding.f8_selftest_wait_timeout(1000)
+    wrapped = {n for n in binding.EXPORTS if hasattr(binding, n)}
+    called = set(rec.calls)
+    assert wrapped - {"f8_status_string", "f8_last_device_status", "f8_set_wait_limit_ns",
+                      "f8_linear_workspace_bytes", "f8_quantize_workspace_bytes"} <= called, \
+        sorted(wrapped - called)

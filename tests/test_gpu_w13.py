@@ -1,0 +1,165 @@
+"""GPU parity of f8_linear_fwd_w13_swiglu: the group {w1, w3} of a SwiGLU FFN
+as one Float8 linear whose GEMM epilogue also forms h = bf16(silu(a) b) and
+takes its amax.
+
+- AB (a and b, interleaved by 128 columns) meets the GEMM bar against the
+  oracle's linear_fwd of X and W13.
+- h is bit-exact against the oracle's swiglu_h of the GPU's own a and b (the
+  GEMM's fp32 accumulation order decides a and b to within the GEMM bar; h is
+  defined from the bf16 a, b).
+- amax(h), the scale and every E4M3 byte of q(h), q(h)^T are bit-exact
+  against the oracle's quantize of the GPU's h, and the saved q(X)^T, q(W13)^T
+  and scalars against the oracle's quantize of X and W13.
+- The CTA-pair kernel (M >= 256) and the single-CTA kernel (M < 256), M and K
+  tails, several waves of tiles, the Llama-3.1-8B FFN size (sampled rows),
+  and the chain into the w2 GEMM and the group's backward.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from float8_mixed_precision_gb300 import workloads as wl
+from tolerance import check_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def f8():
+    import float8_mixed_precision_gb300 as m
+    from float8_mixed_precision_gb300 import build
+    build.build()
+    oracle.build()
+    m.lib()
+    return m
+
+
+def _interleave(w1, w3):
+    """W13 per the entry point's definition, written out here: rows [256j,
+    256j + 128) from W1 rows [128j, 128j + 128), the next 128 from W3."""
+    F = w1.shape[0]
+    parts = []
+    for j in range(F // 128):
+        parts += [w1[128 * j:128 * (j + 1)], w3[128 * j:128 * (j + 1)]]
+    return torch.cat(parts)
+
+
+def _inputs(M, F, K, seed, x_std=1.0):
+    g = torch.Generator().manual_seed(seed)
+    x = (torch.randn((M, K), generator=g) * x_std).to(torch.bfloat16)
+    w1 = (torch.randn((F, K), generator=g) * 0.02).to(torch.bfloat16)
+    w3 = (torch.randn((F, K), generator=g) * 0.02).to(torch.bfloat16)
+    return x, w1, w3
+
+
+def _check_h_and_quant(f8, ab, h, h_q, h_t, scale_h, amax_h):
+    a_g, b_g = oracle.split_ab(wl.bits(ab.cpu()))
+    h_g = wl.bits(h.cpu())
+    assert np.array_equal(h_g, oracle.swiglu_h(a_g, b_g))
+    qh = oracle.quantize(h_g)
+    assert amax_h.item() == float(qh["amax"]) and scale_h.item() == float(qh["scale"])
+    assert np.array_equal(h_q.cpu().numpy(), qh["q"])
+    assert np.array_equal(h_t.cpu().numpy(), qh["qt"])
+    return h_g, qh
+
+
+def test_interleave_helper_matches_definition(f8):
+    x, w1, w3 = _inputs(16, 384, 32, 3)
+    assert torch.equal(f8.interleave_w13(w1, w3), _interleave(w1, w3))
+    ab = torch.arange(5 * 768, dtype=torch.int16).view(5, 768).view(torch.bfloat16)
+    a, b = f8.split_ab(ab)
+    ao, bo = oracle.split_ab(wl.bits(ab))
+    assert np.array_equal(wl.bits(a.contiguous()), ao) and np.array_equal(wl.bits(b.contiguous()), bo)
+
+
+@pytest.mark.parametrize("M,F,K", [(256, 128, 256), (272, 256, 528), (128, 384, 512),
+                                   (48, 128, 64), (1040, 640, 1024)])
+def test_w13_swiglu_full_compare(f8, M, F, K):
+    x, w1, w3 = _inputs(M, F, K, M + F + K)
+    w13 = _interleave(w1, w3)
+    ab, h, saved, h_q, h_t, scale_h, amax_h = f8.f8_linear_fwd_w13_swiglu(x.to(DEV), w13.to(DEV))
+    assert f8.f8_last_device_status() == 0
+    ref = oracle.linear_fwd(wl.bits(x), wl.bits(w13))
+    assert np.array_equal(saved.x_t.cpu().numpy(), ref["x"]["qt"])
+    assert np.array_equal(saved.w_t.cpu().numpy(), ref["w"]["qt"])
+    assert saved.scalars.cpu().tolist() == [float(ref["x"]["amax"]), float(ref["x"]["scale"]),
+                                            float(ref["w"]["amax"]), float(ref["w"]["scale"])]
+    check_close(ab, ref["y"], what="AB")
+    _check_h_and_quant(f8, ab, h, h_q, h_t, scale_h, amax_h)
+
+
+def test_w13_swiglu_large_activations(f8):
+    """X scaled so that |a| reaches the tens: silu's negative tail and exp's
+    reduction over a wide range, still bit-exact in h."""
+    M, F, K = 256, 256, 256
+    x, w1, w3 = _inputs(M, F, K, 99, x_std=300.0)
+    w13 = _interleave(w1, w3)
+    ab, h, saved, h_q, h_t, scale_h, amax_h = f8.f8_linear_fwd_w13_swiglu(x.to(DEV), w13.to(DEV))
+    assert f8.f8_last_device_status() == 0
+    assert float(ab.float().abs().max()) > 20.0
+    check_close(ab, oracle.linear_fwd(wl.bits(x), wl.bits(w13))["y"], what="AB")
+    _check_h_and_quant(f8, ab, h, h_q, h_t, scale_h, amax_h)
+
+
+def test_w13_chain_into_w2_and_group_backward(f8):
+    """q(h) from the epilogue feeds the w2 GEMM (f8_quantize of W2, then
+    f8_gemm), and the group's backward is f8_linear_bwd with N = 2F."""
+    M, F, K, D = 256, 256, 256, 384
+    x, w1, w3 = _inputs(M, F, K, 5)
+    w13 = _interleave(w1, w3)
+    g = torch.Generator().manual_seed(6)
+    w2 = (torch.randn((D, F), generator=g) * 0.02).to(torch.bfloat16)
+    dy13 = (torch.randn((M, 2 * F), generator=g) * 0.01).to(torch.bfloat16)
+    ab, h, saved, h_q, h_t, scale_h, amax_h = f8.f8_linear_fwd_w13_swiglu(x.to(DEV), w13.to(DEV))
+    w2_q, w2_t, scale_w2, amax_w2 = f8.f8_quantize(w2.to(DEV))
+    y = f8.f8_gemm(h_q, w2_q, scale_h, scale_w2)
+    dx, dw = f8.f8_linear_bwd(dy13.to(DEV), saved)
+    assert f8.f8_last_device_status() == 0
+    h_g = wl.bits(h.cpu())
+    ref2 = oracle.linear_fwd(h_g, wl.bits(w2))
+    check_close(y, ref2["y"], what="Y of w2")
+    fwd = oracle.linear_fwd(wl.bits(x), wl.bits(w13))
+    bwd = oracle.linear_bwd(wl.bits(dy13), fwd)
+    check_close(dx, bwd["dx"], what="dX of the group")
+    check_close(dw, bwd["dw"], what="dW13")
+
+
+def test_w13_swiglu_llama8b(f8):
+    """The Llama-3.1-8B FFN input side at full size: M=8192, K=4096, F=14336.
+    AB on one sampled row per 128-row block against the oracle; h and q(h)
+    bit-exact in full."""
+    M, F, K = 8192, 14336, 4096
+    x = wl.normal((M, K), 1.0, wl.seed_of(3, 0, 0))
+    w1 = wl.normal((F, K), 0.02, wl.seed_of(3, 0, 1))
+    w3 = wl.normal((F, K), 0.02, wl.seed_of(3, 1, 1))
+    w13 = _interleave(w1, w3)
+    ab, h, saved, h_q, h_t, scale_h, amax_h = f8.f8_linear_fwd_w13_swiglu(x.to(DEV), w13.to(DEV))
+    assert f8.f8_last_device_status() == 0
+    qx = oracle.quantize(wl.bits(x))
+    qw = oracle.quantize(wl.bits(w13))
+    assert saved.scalars.cpu().tolist() == [float(qx["amax"]), float(qx["scale"]),
+                                            float(qw["amax"]), float(qw["scale"])]
+    rng = np.random.default_rng(13)
+    rows = np.array([r * 128 + rng.integers(0, 128) for r in range(M // 128)], np.int64)
+    check_close(ab[torch.from_numpy(rows).to(DEV)],
+                oracle.gemm_rows(qx["q"], qw["q"], qx["scale"], qw["scale"], rows), what="AB rows")
+    _check_h_and_quant(f8, ab, h, h_q, h_t, scale_h, amax_h)
+
+
+@pytest.mark.parametrize("M,F,K", [(272, 256, 528), (128, 128, 256)])
+def test_gemm_w13_swiglu_alone_equals_fused_call(f8, M, F, K):
+    """The standalone GEMM entry point on q(X), q(W13) gives the same AB and
+    h bits as the fused call, and amax_h = max |h| of the oracle."""
+    x, w1, w3 = _inputs(M, F, K, 17)
+    w13 = _interleave(w1, w3).to(DEV)
+    xd = x.to(DEV)
+    ab, h, saved, h_q, h_t, scale_h, amax_h = f8.f8_linear_fwd_w13_swiglu(xd, w13)
+    x_q, _, sx, _ = f8.f8_quantize(xd)
+    w_q, _, sw, _ = f8.f8_quantize(w13)
+    ab2, h2, amax2 = f8.f8_gemm_w13_swiglu(x_q, w_q, sx, sw)
+    assert f8.f8_last_device_status() == 0
+    assert torch.equal(ab.view(torch.int16), ab2.view(torch.int16))
+    assert torch.equal(h.view(torch.int16), h2.view(torch.int16))
+    assert amax2.item() == amax_h.item() == float(oracle.quantize(wl.bits(h.cpu()))["amax"])
