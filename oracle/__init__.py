@@ -106,6 +106,8 @@ def _load():
         lib.or_silu.restype = f32
         lib.or_swiglu_h.argtypes = [u16p, u16p, i64, u16p]
         lib.or_swiglu_h.restype = None
+        lib.or_swiglu_bwd.argtypes = [u16p, u16p, u16p, i64, u16p, u16p]
+        lib.or_swiglu_bwd.restype = None
         lib.or_num_threads.argtypes = []
         lib.or_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -289,6 +291,20 @@ def swiglu_h(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
     return h
 
 
+def swiglu_bwd(dh_bits: np.ndarray, a_bits: np.ndarray, b_bits: np.ndarray):
+    """bf16 bits of (da, db), the gradient of h = bf16(silu(a) * b) for an
+    upstream dh: db = bf16(dh * silu(a)), da = bf16(dh * b * silu'(a)) with
+    silu'(a) = sigma (1 + a (1 - sigma)), fp32 steps as in or_swiglu_bwd."""
+    dh, a, b = _u16(dh_bits), _u16(a_bits), _u16(b_bits)
+    assert dh.shape == a.shape == b.shape
+    da = np.empty(a.shape, np.uint16)
+    db = np.empty(a.shape, np.uint16)
+    _load().or_swiglu_bwd(_ptr(dh, ctypes.c_uint16), _ptr(a, ctypes.c_uint16),
+                          _ptr(b, ctypes.c_uint16), a.size, _ptr(da, ctypes.c_uint16),
+                          _ptr(db, ctypes.c_uint16))
+    return da, db
+
+
 # --------------------------------------------------------------------------
 # the linear layer, step by step
 # --------------------------------------------------------------------------
@@ -342,6 +358,29 @@ def linear_fwd_w13_swiglu(x_bits: np.ndarray, w13_bits: np.ndarray) -> dict:
     a, b = split_ab(out["y"])
     out["h"] = swiglu_h(a, b)
     out["qh"] = quantize(out["h"])
+    return out
+
+
+def merge_ab(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
+    """The inverse of split_ab: a and b [M, F] into one [M, 2F] whose column
+    blocks of 128 come from a and b alternately."""
+    a, b = _u16(a_bits), _u16(b_bits)
+    M, F = a.shape
+    out = np.empty((M, F // 128, 2, 128), np.uint16)
+    out[:, :, 0, :] = a.reshape(M, F // 128, 128)
+    out[:, :, 1, :] = b.reshape(M, F // 128, 128)
+    return out.reshape(M, 2 * F)
+
+
+def linear_bwd_w13_swiglu(dh_bits: np.ndarray, fwd: dict) -> dict:
+    """The backward of linear_fwd_w13_swiglu for the gradient dh of h: the
+    SwiGLU gradient (da, db) from dh and the forward's bf16 a and b, merged
+    into d(AB) in AB's column order, then linear_bwd of the group."""
+    a, b = split_ab(fwd["y"])
+    da, db = swiglu_bwd(dh_bits, a, b)
+    dab = merge_ab(da, db)
+    out = linear_bwd(dab, fwd)
+    out["dab"] = dab
     return out
 
 

@@ -555,6 +555,38 @@ void or_swiglu_h(const uint16_t *a, const uint16_t *b, int64_t n, uint16_t *h)
     }
 }
 
+/* The gradient of h = bf16(silu(a) * b) (the step above) for an upstream
+ * gradient dh, elementwise over n values, each step one fp32 operation:
+ *   sigma = 1 / (1 + exp(-a))      (as in or_silu: correctly rounded reciprocal)
+ *   s     = a * sigma              (silu(a), as in the forward)
+ *   db    = bf16(dh * s)           (d h / d b = silu(a))
+ *   t     = 1 - sigma
+ *   w     = fma(a, t, 1)           (one rounding: 1 + a (1 - sigma))
+ *   ds    = sigma * w              (silu'(a) = sigma (1 + a (1 - sigma)))
+ *   g     = dh * b                 (the gradient reaching silu(a))
+ *   da    = bf16(g * ds)
+ */
+void or_swiglu_bwd(const uint16_t *dh, const uint16_t *a, const uint16_t *b, int64_t n,
+                   uint16_t *da, uint16_t *db)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        const float fa = or_bf16_to_f32(a[i]);
+        const float fb = or_bf16_to_f32(b[i]);
+        const float fdh = or_bf16_to_f32(dh[i]);
+        const float e = f32_exp_cw(-fa);
+        const float d = 1.0f + e;
+        const float sigma = 1.0f / d;
+        const float s = fa * sigma;
+        db[i] = f32_to_bf16(fdh * s);
+        const float t = 1.0f - sigma;
+        const float w = fmaf(fa, t, 1.0f);
+        const float ds = sigma * w;
+        const float g = fdh * fb;
+        da[i] = f32_to_bf16(g * ds);
+    }
+}
+
 /* Number of threads the parallel loops above use. */
 int or_num_threads(void)
 {

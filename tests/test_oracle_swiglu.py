@@ -120,3 +120,83 @@ def test_w13_group_rows_are_w1_and_w3(oracle_mod):
     assert np.array_equal(wl.bits(w13)[256:384], wl.bits(w1)[128:256])
     assert np.array_equal(wl.bits(w13)[384:512], wl.bits(w3)[128:256])
     assert np.array_equal(out["h"], oracle_mod.swiglu_h(a, b))
+
+
+def _bf(x):
+    return torch.tensor(x, dtype=torch.float32).to(torch.bfloat16)
+
+
+def _f(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy()).view(torch.bfloat16).double()
+
+
+def test_swiglu_bwd_against_float64_autograd(oracle_mod):
+    """(da, db) against torch autograd of h = silu(a) * b in float64 on the
+    same bf16 inputs: equal to the float64 gradient rounded once to bf16
+    except within fp32 rounding of a bf16 boundary, and then by one ulp."""
+    shape = (200, 300)
+    g = torch.Generator().manual_seed(31)
+    a = (torch.randn(shape, generator=g) * 2).to(torch.bfloat16)
+    b = torch.randn(shape, generator=g).to(torch.bfloat16)
+    dh = torch.randn(shape, generator=g).to(torch.bfloat16)
+    da, db = oracle_mod.swiglu_bwd(wl.bits(dh), wl.bits(a), wl.bits(b))
+    ad = a.double().requires_grad_()
+    bd = b.double().requires_grad_()
+    (torch.nn.functional.silu(ad) * bd).backward(dh.double())
+    for got, ref in ((_f(da), ad.grad), (_f(db), bd.grad)):
+        ref_bf = ref.to(torch.bfloat16).double()
+        ulp = torch.from_numpy(np.spacing(np.abs(ref_bf.float().numpy())).astype(np.float64)) * 2 ** 16
+        diff = (got - ref_bf).abs()
+        assert bool((diff <= ulp * (1 + 1e-9)).all()), float((diff / ulp).max())
+        assert float((diff > 0).double().mean()) < 0.02
+
+
+def test_silu_derivative_by_finite_differences(oracle_mod):
+    """With dh = b = 1, da is bf16(silu'(a)): checked against a central
+    difference of the float64 silu (independent of the formula the oracle
+    uses), to within one bf16 ulp."""
+    xs = np.concatenate([np.linspace(-12, 12, 241), [-0.5, -1e-3, 1e-3, 0.25]])
+    a = _bf(xs)
+    one = _bf(np.ones_like(xs))
+    da, db = oracle_mod.swiglu_bwd(wl.bits(one), wl.bits(a), wl.bits(one))
+    silu = lambda v: v / (1.0 + np.exp(-v))
+    for v, got in zip(a.double().numpy(), _f(da).numpy()):
+        hstep = 1e-6 * max(1.0, abs(v))
+        fd = (silu(v + hstep) - silu(v - hstep)) / (2 * hstep)
+        ulp = np.spacing(np.float32(abs(fd))) * 2 ** 16 if fd != 0 else 1e-30
+        assert abs(got - fd) <= ulp + 1e-9, (v, got, fd)
+    # db with dh = 1 is bf16(silu(a))
+    for v, got in zip(a.double().numpy(), _f(db).numpy()):
+        ref = silu(v)
+        assert abs(got - ref) <= np.spacing(np.float32(abs(ref))) * 2 ** 16 + 1e-30, (v, got, ref)
+
+
+def test_swiglu_bwd_special_cases(oracle_mod):
+    """a = 0: sigma = 1/2 and silu'(0) = 1/2 exactly, so da = bf16(dh b / 2)
+    and db = 0.  a = 20: 1 + exp(-20) rounds to 1 in fp32, so sigma = 1,
+    silu' = 1 and da = bf16(dh b), db = bf16(dh a).  dh = 0 gives zeros.
+    a = -30: both gradients tiny and of the sign of -dh b and -dh."""
+    dh = _bf([1.5, -2.0, 0.0, 1.0, 3.0])
+    a = _bf([0.0, 20.0, 5.0, -30.0, 0.0])
+    b = _bf([3.0, 0.5, 7.0, 2.0, -1.0])
+    da, db = oracle_mod.swiglu_bwd(wl.bits(dh), wl.bits(a), wl.bits(b))
+    da, db = _f(da).numpy(), _f(db).numpy()
+    assert da[0] == 2.25 and db[0] == 0.0
+    assert da[1] == -1.0 and db[1] == -40.0
+    assert da[2] == 0.0 and db[2] == 0.0
+    assert da[3] < 0 and abs(da[3]) < 1e-10 and db[3] < 0 and abs(db[3]) < 1e-10
+    assert da[4] == -1.5 and db[4] == 0.0
+
+
+def test_merge_ab_inverts_split_ab(oracle_mod):
+    M, F = 4, 384
+    rng = np.random.default_rng(5)
+    a = rng.integers(0, 1 << 16, (M, F), dtype=np.uint16)
+    b = rng.integers(0, 1 << 16, (M, F), dtype=np.uint16)
+    ab = oracle_mod.merge_ab(a, b)
+    assert ab.shape == (M, 2 * F)
+    a2, b2 = oracle_mod.split_ab(ab)
+    assert np.array_equal(a, a2) and np.array_equal(b, b2)
+    for c in range(F):
+        src = 256 * (c // 128) + c % 128
+        assert np.array_equal(ab[:, src], a[:, c]) and np.array_equal(ab[:, src + 128], b[:, c])
