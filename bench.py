@@ -244,19 +244,41 @@ class FfnIn8(Linear8):
 
     launches = 10  # amax + cast of X, W13; the GEMM; cast of h; amax + cast of dY; 2 GEMMs
 
-    def __init__(self, f8, lin, inputs, device, dy_fmt=0):
+    def __init__(self, f8, lin, inputs, device, dy_fmt=0, chain=False):
         import torch
         super().__init__(f8, lin, inputs, device, dy_fmt)
         M, F = lin.M, lin.N // 2
         self.h = torch.empty((M, F), dtype=torch.bfloat16, device=device)
         self.h_q = torch.empty((M, F), dtype=torch.uint8, device=device)
         self.next = None  # the W2Q8 whose saved tensors receive q(h)^T and h's scalars
+        # chain: the group's dY is not given but formed from dh by the SwiGLU
+        # backward, which the W2Q8 runs after its own backward
+        self.chain = chain
+        if chain:
+            self.launches = 6
+            self.dy = torch.empty_like(self.y)  # d(AB), written each step
 
     def step(self, f8):
         s2 = self.next.saved
         f8.f8_linear_fwd_w13_swiglu(self.x, self.w, self.y, self.h, self.saved, s2.scalars[0:1],
                                     s2.scalars[1:2], self.h_q, s2.x_t, self.ws)
-        f8.f8_linear_bwd(self.dy, self.saved, dx=self.dx, dw=self.dw, ws=self.ws, dy_fmt=self.dy_fmt)
+        if not self.chain:
+            f8.f8_linear_bwd(self.dy, self.saved, dx=self.dx, dw=self.dw, ws=self.ws,
+                             dy_fmt=self.dy_fmt)
+
+    def bwd_from_dh(self, f8, dh):
+        f8.f8_linear_bwd_w13_swiglu(dh, self.y, self.saved, dab=self.dy, dx=self.dx, dw=self.dw,
+                                    ws=self.ws)
+
+    def bwd_from_dh_timed(self, f8, ev, dh):
+        s = self.saved
+        M, N, K = self.lin.M, self.lin.N, self.lin.K
+        # reads dh, a, b (6 B per element of h) and writes d(AB) (4 B), then the cast
+        ev("quantize", 10 * dh.numel() + 4 * self.dy.numel(),
+           lambda: f8.f8_quantize_swiglu_bwd(dh, self.y, self.dy, self.dys[0], self.dys[1], self.dyq,
+                                             self.dyt, self.qws))
+        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyq, s.w_t, self.dys[1], s.scale_w, self.dx))
+        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyt, s.x_t, self.dys[1], s.scale_x, self.dw))
 
     def step_timed(self, f8, ev):
         s, s2 = self.saved, self.next.saved
@@ -270,7 +292,8 @@ class FfnIn8(Linear8):
                                          s2.scalars[0:1]))
         ev("quantize", 4 * self.h.numel(),
            lambda: f8.f8_cast_transpose(self.h, s2.scalars[0:1], s2.scalars[1:2], self.h_q, s2.x_t))
-        self.bwd_timed(f8, ev)
+        if not self.chain:
+            self.bwd_timed(f8, ev)
 
 
 class W2Q8(Linear8):
@@ -283,12 +306,16 @@ class W2Q8(Linear8):
         super().__init__(f8, lin, inputs, device, dy_fmt)
         self.src = src
         src.next = self
+        if src.chain:
+            self.launches = 7 + 4  # ... then the SwiGLU backward, cast of d(AB), 2 GEMMs
 
     def step(self, f8):
         s = self.saved
         f8.f8_quantize(self.w, s.amax_w, s.scale_w, self.wq, s.w_t, self.qws)
         f8.f8_gemm(self.src.h_q, self.wq, s.scale_x, s.scale_w, self.y)
         f8.f8_linear_bwd(self.dy, self.saved, dx=self.dx, dw=self.dw, ws=self.ws, dy_fmt=self.dy_fmt)
+        if self.src.chain:
+            self.src.bwd_from_dh(f8, self.dx)  # dX of w2 is dh
 
     def step_timed(self, f8, ev):
         s = self.saved
@@ -298,18 +325,21 @@ class W2Q8(Linear8):
         ev("gemm", 2 * M * N * K,
            lambda: f8.f8_gemm(self.src.h_q, self.wq, s.scale_x, s.scale_w, self.y))
         self.bwd_timed(f8, ev)
+        if self.src.chain:
+            self.src.bwd_from_dh_timed(f8, ev, self.dx)
 
 
 def build_layers(f8, wl, args, device, dy_fmt):
     """The workload's linears as layer objects, and the workload's name."""
     name, lins = wl.workload(args.config)
-    if args.swiglu_input == "epilogue":
+    if args.swiglu_input in ("epilogue", "chain"):
+        chain = args.swiglu_input == "chain"
         if args.config not in wl.SHARED_INPUT_GROUPS:
             raise SystemExit("--swiglu-input epilogue needs a workload with a SwiGLU FFN (3, 4, 5)")
         layers, ffn = [], None
         for g, idx in wl.fused_groups(args.config):
             if g.name == "w1+w3":
-                ffn = FfnIn8(f8, g, wl.w13_group_inputs(args.config, idx), device, dy_fmt)
+                ffn = FfnIn8(f8, g, wl.w13_group_inputs(args.config, idx), device, dy_fmt, chain)
                 layers.append(ffn)
             elif g.name == "w2" and ffn is not None:
                 layers.append(W2Q8(f8, g, wl.fused_group_inputs(args.config, idx), device, dy_fmt,
@@ -319,8 +349,8 @@ def build_layers(f8, wl, args, device, dy_fmt):
                                       dy_fmt))
         if ffn is None:
             raise SystemExit("--swiglu-input epilogue needs a workload with a SwiGLU FFN (3, 4, 5)")
-        return (name + " (shared inputs fused; w2 input silu(a) * b from the w1+w3 GEMM "
-                "epilogue)"), layers
+        return (name + " (shared inputs fused; w2 input silu(a) * b from the w1+w3 GEMM epilogue"
+                + ("; dY of w1+w3 from the SwiGLU backward of dX of w2)" if chain else ")")), layers
     if args.fuse_shared_inputs:
         layers = []
         for g, idx in wl.fused_groups(args.config):
@@ -464,7 +494,7 @@ def run_ours(args, world, rank, local):
                                                   for l in lins)}
 
     # the chained FFN's w2 reads a device-made input: no isolated or host-fed runs
-    chained = args.swiglu_input == "epilogue"
+    chained = args.swiglu_input in ("epilogue", "chain")
     iso = kernel_bench(f8, layers, device, stream) if args.kernel_bench and not chained else None
 
     # ---- end to end: pinned host buffers in, results out, every step
@@ -793,11 +823,13 @@ def main(argv=None):
                     help="merge the linears that read one input (q/k/v, w1/w3) into one linear "
                          "with the concatenated weight and a tensorwise scale over it")
     ap.add_argument("--swiglu-input", default="given",
-                    choices=["given", "materialized", "fused", "epilogue"],
+                    choices=["given", "materialized", "fused", "epilogue", "chain"],
                     help="for linears fed by silu(a) * b: the bf16 product given (default), "
                          "formed by torch each step, produced from given a, b with its amax "
                          "(f8_linear_fwd_swiglu), or formed in the epilogue of the w1+w3 "
-                         "group's GEMM and fed to w2 (implies --fuse-shared-inputs)")
+                         "group's GEMM and fed to w2 (implies --fuse-shared-inputs); chain: "
+                         "epilogue, and the group's dY formed from dX of w2 by the SwiGLU "
+                         "backward (only dY of w2 given)")
     ap.add_argument("--dy-format", default="e4m3", choices=["e4m3", "e5m2"],
                     help="FP8 format of dY in the backward pass (X and W stay E4M3)")
     ap.add_argument("--kernel-bench", type=int, default=1,

@@ -32,7 +32,8 @@ EXPORTS = ("f8_amax", "f8_cast_transpose", "f8_gemm", "f8_linear_workspace_bytes
            "f8_selftest_wait_timeout", "f8_set_wait_limit_ns", "f8_linear_fwd_noalloc",
            "f8_quantize", "f8_quantize_workspace_bytes", "f8_quantize_fmt", "f8_gemm_fmt",
            "f8_linear_bwd_fmt", "f8_quantize_swiglu", "f8_linear_fwd_swiglu",
-           "f8_linear_fwd_w13_swiglu", "f8_gemm_w13_swiglu")
+           "f8_linear_fwd_w13_swiglu", "f8_gemm_w13_swiglu", "f8_linear_bwd_w13_swiglu",
+           "f8_quantize_swiglu_bwd")
 
 F8_E4M3 = 0
 F8_E5M2 = 1
@@ -108,6 +109,12 @@ def lib() -> ctypes.CDLL:
         L.f8_linear_fwd_w13_swiglu.argtypes = [vp, vp, i64, i64, i64, vp, vp, ctypes.POINTER(_Saved),
                                                vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         L.f8_linear_fwd_w13_swiglu.restype = st
+        L.f8_linear_bwd_w13_swiglu.argtypes = [vp, vp, ctypes.POINTER(_Saved), i64, i64, i64, vp,
+                                               vp, vp, vp, ctypes.c_size_t, vp]
+        L.f8_linear_bwd_w13_swiglu.restype = st
+        L.f8_quantize_swiglu_bwd.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, vp, vp,
+                                             ctypes.c_size_t, vp]
+        L.f8_quantize_swiglu_bwd.restype = st
         L.f8_gemm_w13_swiglu.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp]
         L.f8_gemm_w13_swiglu.restype = st
         L.f8_linear_fwd_noalloc.argtypes = [vp, vp, i64, i64, i64, vp, ctypes.POINTER(_Saved), vp]
@@ -406,6 +413,51 @@ def f8_linear_fwd_w13_swiglu(x: torch.Tensor, w13: torch.Tensor, ab: torch.Tenso
                                           _ptr(h_t), _ptr(ws), ws.numel(), _stream(stream)),
            "f8_linear_fwd_w13_swiglu")
     return ab, h, saved, h_q, h_t, scale_h, amax_h
+
+
+def f8_linear_bwd_w13_swiglu(dh: torch.Tensor, ab: torch.Tensor, saved: LinearSaved,
+                             dab: torch.Tensor | None = None, dx: torch.Tensor | None = None,
+                             dw: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                             want_dx: bool = True, want_dw: bool = True, stream=None):
+    """d(AB) from dh and the forward's AB, then dX, dW13 of the w1+w3 group;
+    returns (dx, dw, dab)."""
+    M, F = dh.shape
+    K = saved.x_t.shape[0]
+    if ab.shape != (M, 2 * F):
+        raise ValueError("ab must be [M, 2F] for dh [M, F]")
+    dev = dh.device
+    dab = torch.empty_like(ab) if dab is None else dab
+    if dx is None and want_dx:
+        dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    if dw is None and want_dw:
+        dw = torch.empty((2 * F, K), dtype=torch.bfloat16, device=dev)
+    ws = workspace(M, 2 * F, K, dev) if ws is None else ws
+    s = saved.c_struct()
+    _check(lib().f8_linear_bwd_w13_swiglu(_ptr(dh), _ptr(ab), ctypes.byref(s), M, F, K, _ptr(dab),
+                                          _ptr(dx), _ptr(dw), _ptr(ws), ws.numel(),
+                                          _stream(stream)), "f8_linear_bwd_w13_swiglu")
+    return dx, dw, dab
+
+
+def f8_quantize_swiglu_bwd(dh: torch.Tensor, ab: torch.Tensor, dab: torch.Tensor | None = None,
+                           amax_out=None, scale_out=None, q=None, q_t=None, ws=None, stream=None):
+    """d(AB) from dh and the forward's AB with its amax, then its E4M3 cast:
+    returns (q, q_t, scale, amax, dab)."""
+    M, F = dh.shape
+    if ab.shape != (M, 2 * F):
+        raise ValueError("ab must be [M, 2F] for dh [M, F]")
+    dev = dh.device
+    dab = torch.empty_like(ab) if dab is None else dab
+    amax_out = torch.empty((), dtype=torch.float32, device=dev) if amax_out is None else amax_out
+    scale_out = torch.empty((), dtype=torch.float32, device=dev) if scale_out is None else scale_out
+    q = torch.empty((M, 2 * F), dtype=torch.uint8, device=dev) if q is None else q
+    q_t = torch.empty((2 * F, M), dtype=torch.uint8, device=dev) if q_t is None else q_t
+    if ws is None:
+        ws = torch.empty(f8_quantize_workspace_bytes(), dtype=torch.uint8, device=dev)
+    _check(lib().f8_quantize_swiglu_bwd(_ptr(dh), _ptr(ab), M, F, _ptr(dab), _ptr(amax_out),
+                                        _ptr(scale_out), _ptr(q), _ptr(q_t), _ptr(ws), ws.numel(),
+                                        _stream(stream)), "f8_quantize_swiglu_bwd")
+    return q, q_t, scale_out, amax_out, dab
 
 
 def f8_gemm_w13_swiglu(x_q: torch.Tensor, w13_q: torch.Tensor, scale_x: torch.Tensor,

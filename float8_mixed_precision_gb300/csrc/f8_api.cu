@@ -488,6 +488,70 @@ f8_status f8_linear_fwd_w13_swiglu(const void *x, const void *w13, int64_t M, in
                                            h_t, 0, *dev, st));
 }
 
+f8_status f8_quantize_swiglu_bwd(const void *dh, const void *ab, int64_t M, int64_t F, void *dab,
+                                 float *amax_out, float *scale_out, uint8_t *q, uint8_t *q_t,
+                                 void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (M <= 0 || F <= 0)
+        return F8_ERR_INVALID;
+    if (F % 128 || F > INT32_MAX / 4 || M > INT32_MAX / 2)
+        return F8_ERR_SHAPE;
+    if (dh == nullptr || ab == nullptr || dab == nullptr || amax_out == nullptr ||
+        workspace == nullptr)
+        return F8_ERR_INVALID;
+    if (workspace_bytes < kPartialsBytes)
+        return F8_ERR_INVALID;
+    if (!aligned(dh, 16) || !aligned(ab, 16) || !aligned(dab, 16) || !aligned(q, 16) ||
+        !aligned(q_t, 16) || !aligned(amax_out, 4) || !aligned(scale_out, 4) ||
+        !aligned(workspace, 16))
+        return F8_ERR_ALIGN;
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned *parts = static_cast<unsigned *>(workspace);
+    int np = 0;
+    F8_TRY_CUDA(launch_swiglu_bwd_amax(dh, ab, dab, M, F, parts, &np, *dev, st));
+    return from_cuda(launch_cast_transpose(dab, M, 2 * F, nullptr, parts, np, amax_out, scale_out, q,
+                                           q_t, F8_E4M3, *dev, st));
+}
+
+f8_status f8_linear_bwd_w13_swiglu(const void *dh, const void *ab, const f8_linear_saved *saved,
+                                   int64_t M, int64_t F, int64_t K, void *dab, void *dx,
+                                   void *dw13, void *workspace, size_t workspace_bytes,
+                                   void *stream)
+{
+    if (M <= 0 || F <= 0 || K <= 0)
+        return F8_ERR_INVALID;
+    if (F % 128 || F > INT32_MAX / 4)
+        return F8_ERR_SHAPE;
+    const int64_t N = 2 * F;
+    F8_TRY(check_linear_shape(M, N, K));
+    F8_TRY(check_saved(saved));
+    if (dh == nullptr || ab == nullptr || dab == nullptr || workspace == nullptr)
+        return F8_ERR_INVALID;
+    if (workspace_bytes < bwd_ws_bytes(M, N))
+        return F8_ERR_INVALID;
+    if (!aligned(dh, 16) || !aligned(ab, 16) || !aligned(dab, 16) || !aligned(dx, 16) ||
+        !aligned(dw13, 16) || !aligned(workspace, 256))
+        return F8_ERR_ALIGN;
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const BwdWs bw = bwd_ws(workspace, M, N);
+    int np = 0;
+    F8_TRY_CUDA(launch_swiglu_bwd_amax(dh, ab, dab, M, F, bw.parts_dy, &np, *dev, st));
+    F8_TRY_CUDA(launch_cast_transpose(dab, M, N, nullptr, bw.parts_dy, np, bw.amax_dy, bw.scale_dy,
+                                      dx ? bw.dy_q : nullptr, dw13 ? bw.dy_t : nullptr, F8_E4M3,
+                                      *dev, st));
+    if (dx != nullptr)
+        F8_TRY_CUDA(launch_gemm(bw.dy_q, saved->w_t, M, K, N, bw.scale_dy, saved->scale_w, dx, *dev,
+                                st));
+    if (dw13 != nullptr)
+        F8_TRY_CUDA(launch_gemm(bw.dy_t, saved->x_t, N, K, M, bw.scale_dy, saved->scale_x, dw13,
+                                *dev, st));
+    return F8_OK;
+}
+
 f8_status f8_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int64_t M, int64_t F,
                              int64_t K, const float *scale_x, const float *scale_w13, void *ab,
                              void *h, float *amax_h, void *stream)

@@ -227,6 +227,76 @@ swiglu_amax_kernel(const uint4 *__restrict__ a, const uint4 *__restrict__ b, uin
     }
 }
 
+// d(AB) of the w1+w3 group from the gradient dh [M, F] of h and the
+// forward's AB [M, 2F] (a and b in column blocks of 128, alternating): for
+// the 16-byte vector v of dh, a is vector v + 16 (v / 16) of AB and b the
+// one 16 vectors further; da and db are written at those same places of
+// dAB.  One partial maximum of |d(AB)| per CTA, as amax_kernel<true>.
+__global__ void __launch_bounds__(kAmaxThreads)
+swiglu_bwd_amax_kernel(const uint4 *__restrict__ dh, const uint4 *__restrict__ ab,
+                       uint4 *__restrict__ dab, int64_t nvec, unsigned *__restrict__ partials,
+                       unsigned *__restrict__ status)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    constexpr int kU = 2;
+    uint32_t m2 = 0;
+    const int64_t S = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < nvec;
+         base += kU * S) {
+        uint4 vd[kU], va[kU], vb[kU];
+        int64_t ia[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int64_t i = base + u * S;
+            ia[u] = i + ((i >> 4) << 4);
+            const bool in = i < nvec;
+            vd[u] = in ? __ldg(dh + i) : make_uint4(0, 0, 0, 0);
+            va[u] = in ? __ldg(ab + ia[u]) : make_uint4(0, 0, 0, 0);
+            vb[u] = in ? __ldg(ab + ia[u] + 16) : make_uint4(0, 0, 0, 0);
+        }
+        uint32_t amag = 0;
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            amag = swiglu::fold_abs(amag, va[u]);
+        uint4 ga[kU], gb[kU];
+        // one branch per 16 elements, so that their chains interleave
+        if (swiglu::small87(amag)) {
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                swiglu::swiglu_bwd8<false>(vd[u], va[u], vb[u], ga[u], gb[u]);
+        } else {
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                swiglu::swiglu_bwd8<true>(vd[u], va[u], vb[u], ga[u], gb[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (base + u * S < nvec) {
+                dab[ia[u]] = ga[u];
+                dab[ia[u] + 16] = gb[u];
+                m2 = max_u16x2(max_u16x2(m2, ga[u]), gb[u]);
+            }
+        }
+    }
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    __shared__ uint32_t warp_max[kAmaxThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0)
+        warp_max[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        m = lane < kAmaxThreads / 32 ? warp_max[lane] : 0u;
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if (lane == 0) {
+            if (m >= 0x7F80u)
+                atomicOr(status, kStatusNonfinite);
+            partials[blockIdx.x] = m << 16;
+        }
+    }
+}
+
 // Phase 2 of a full tile: thread t takes a 16-row x 4-column block of the
 // parked codes (16 conflict-free 4-byte shared loads), transposes it with
 // PRMT and writes four 16-byte column segments of q^T (8 consecutive threads
@@ -432,7 +502,7 @@ namespace {
 
 // Resident CTAs per SM of each kernel on each device (occupancy API, cached).
 struct Occupancy {
-    int amax_atomic = 0, amax_partials = 0, cast = 0, cast_tma = 0, swiglu = 0;
+    int amax_atomic = 0, amax_partials = 0, cast = 0, cast_tma = 0, swiglu = 0, swiglu_bwd = 0;
 };
 std::mutex g_occ_mutex;
 Occupancy g_occ[64];
@@ -458,6 +528,8 @@ const Occupancy &occupancy(const DeviceInfo &dev)
         o.cast_tma = n > 0 ? n : 1;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, swiglu_amax_kernel, kAmaxThreads, 0);
         o.swiglu = n > 0 ? n : 1;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, swiglu_bwd_amax_kernel, kAmaxThreads, 0);
+        o.swiglu_bwd = n > 0 ? n : 1;
     }
     return o;
 }
@@ -564,6 +636,25 @@ cudaError_t launch_quantize_swiglu(const void *a, const void *b, void *h, int64_
         return e;
     return launch_cast_transpose(h, rows, cols, nullptr, partials, static_cast<int>(blocks), amax_out,
                                  scale_out, q, q_t, 0, dev, stream);
+}
+
+cudaError_t launch_swiglu_bwd_amax(const void *dh, const void *ab, void *dab, int64_t M, int64_t F,
+                                   unsigned *partials, int *nparts, const DeviceInfo &dev,
+                                   cudaStream_t stream)
+{
+    const int64_t nvec = M * F / 8;
+    int64_t blocks = (nvec + kAmaxThreads * 2 - 1) / (kAmaxThreads * 2);
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * occupancy(dev).swiglu_bwd;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks > kMaxAmaxPartials)
+        blocks = kMaxAmaxPartials;
+    if (blocks < 1)
+        blocks = 1;
+    *nparts = static_cast<int>(blocks);
+    return launch_pdl(swiglu_bwd_amax_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kAmaxThreads),
+                      0, stream, static_cast<const uint4 *>(dh), static_cast<const uint4 *>(ab),
+                      static_cast<uint4 *>(dab), nvec, partials, dev.status);
 }
 
 } // namespace f8

@@ -132,6 +132,13 @@ cudaError_t launch_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int
                                    unsigned *hparts, int *nparts, const DeviceInfo &dev,
                                    cudaStream_t stream, bool hatomic = false);
 
+// d(AB) [M, 2F] (AB's column order) of the w1+w3 group from the gradient dh
+// [M, F] of h = silu(a) b and the forward's AB, with one |d(AB)| partial
+// maximum per CTA in partials (*nparts receives their count).  F % 128 == 0.
+cudaError_t launch_swiglu_bwd_amax(const void *dh, const void *ab, void *dab, int64_t M, int64_t F,
+                                   unsigned *partials, int *nparts, const DeviceInfo &dev,
+                                   cudaStream_t stream);
+
 // One CTA waiting on an mbarrier that is never signalled (failure-path test).
 cudaError_t launch_wait_selftest(uint64_t limit_ns, const DeviceInfo &dev, cudaStream_t stream);
 

@@ -130,6 +130,39 @@ __device__ __forceinline__ uint4 swiglu_x8(uint4 a, uint4 b)
     return small87(fold_abs(0u, a)) ? swiglu8<false>(a, b) : swiglu8<true>(a, b);
 }
 
+// The gradient of swiglu_x2's h for two packed bf16 lanes of the upstream
+// gradient dh: db = bf16(dh s) with s = a sigma, and da = bf16((dh b) ds)
+// with ds = sigma fma(a, 1 - sigma, 1) = silu'(a); sigma as in the forward.
+// Each step one fp32 operation, as written.  kChecked as for swiglu_x2.
+template <bool kChecked>
+__device__ __forceinline__ void swiglu_bwd_x2(uint32_t dh, uint32_t a, uint32_t b, uint32_t &da,
+                                              uint32_t &db)
+{
+    const float2 fa = make_float2(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
+    const float2 fb = make_float2(__uint_as_float(b << 16), __uint_as_float(b & 0xFFFF0000u));
+    const float2 fd = make_float2(__uint_as_float(dh << 16), __uint_as_float(dh & 0xFFFF0000u));
+    const float2 e = exp_cw2<kChecked>(make_float2(-fa.x, -fa.y));
+    const float2 d = __fadd2_rn(splat(1.0f), e);
+    const float2 sg = kChecked ? make_float2(__frcp_rn(d.x), __frcp_rn(d.y)) : rcp2_refined(d);
+    const float2 vdb = __fmul2_rn(fd, __fmul2_rn(fa, sg));
+    const float2 t = __fadd2_rn(splat(1.0f), make_float2(-sg.x, -sg.y));
+    const float2 ds = __fmul2_rn(sg, __ffma2_rn(fa, t, splat(1.0f)));
+    const float2 vda = __fmul2_rn(__fmul2_rn(fd, fb), ds);
+    const __nv_bfloat162 ha = __floats2bfloat162_rn(vda.x, vda.y);
+    const __nv_bfloat162 hb = __floats2bfloat162_rn(vdb.x, vdb.y);
+    da = *reinterpret_cast<const uint32_t *>(&ha);
+    db = *reinterpret_cast<const uint32_t *>(&hb);
+}
+
+template <bool kChecked>
+__device__ __forceinline__ void swiglu_bwd8(uint4 dh, uint4 a, uint4 b, uint4 &da, uint4 &db)
+{
+    swiglu_bwd_x2<kChecked>(dh.x, a.x, b.x, da.x, db.x);
+    swiglu_bwd_x2<kChecked>(dh.y, a.y, b.y, da.y, db.y);
+    swiglu_bwd_x2<kChecked>(dh.z, a.z, b.z, da.z, db.z);
+    swiglu_bwd_x2<kChecked>(dh.w, a.w, b.w, da.w, db.w);
+}
+
 // |h| of a packed bf16 pair folded into a running packed maximum (bit order
 // is numeric order for non-negative bf16; NaN and inf sort above all finite).
 __device__ __forceinline__ uint32_t max_abs2(uint32_t m, uint32_t h2)

@@ -295,6 +295,43 @@ f8_status f8_linear_fwd_w13_swiglu(const void *x, const void *w13, int64_t M, in
                                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The first half of f8_linear_bwd_w13_swiglu alone: d(AB) from dh and the
+ * forward's AB with its amax (one pass), then its E4M3 cast, as
+ * f8_quantize does for a given tensor.
+ *   dh:  device bf16 [M, F]; ab: device bf16 [M, 2F]; F % 128 == 0.
+ *   dab: device bf16 [M, 2F] receiving d(AB).
+ *   amax_out, scale_out, q ([M, 2F]), q_t ([2F, M]), workspace
+ *   (f8_quantize_workspace_bytes()): as for f8_quantize.
+ */
+f8_status f8_quantize_swiglu_bwd(const void *dh, const void *ab, int64_t M, int64_t F, void *dab,
+                                 float *amax_out, float *scale_out, uint8_t *q, uint8_t *q_t,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The backward of f8_linear_fwd_w13_swiglu for the gradient dh of h (in a
+ * Llama FFN, the dX of the w2 linear):
+ *   d(AB) = the gradient of h = silu(a) * b: db = bf16(dh * silu(a)),
+ *           da = bf16(dh * b * silu'(a)) with silu'(a) = sigma fma(a, 1 - sigma,
+ *           1), sigma and silu(a) as in the forward, each step one IEEE fp32
+ *           operation; written in AB's column order, with its amax taken in
+ *           the same pass (one partial per CTA);
+ *   then the group's backward as f8_linear_bwd with dY = d(AB): cast of
+ *           d(AB), dX = q(dAB) q(W13), dW13 = q(dAB)^T q(X).
+ *   dh:    device bf16 [M, F].
+ *   ab:    device bf16 [M, 2F], the forward's AB.
+ *   saved: the forward's saved tensors.
+ *   dab:   device bf16 [M, 2F] receiving d(AB).
+ *   dx:    device bf16 [M, K] or NULL; dw13: device bf16 [2F, K] or NULL.
+ *   workspace: f8_linear_workspace_bytes(M, 2F, K) bytes, 256-byte aligned.
+ * All device pointers 16-byte aligned.  F8_ERR_SHAPE if F is not a positive
+ * multiple of 128.
+ */
+f8_status f8_linear_bwd_w13_swiglu(const void *dh, const void *ab, const f8_linear_saved *saved,
+                                   int64_t M, int64_t F, int64_t K, void *dab, void *dx,
+                                   void *dw13, void *workspace, size_t workspace_bytes,
+                                   void *stream);
+
+/*
  * The GEMM of f8_linear_fwd_w13_swiglu alone, for callers that quantise X
  * and W13 themselves (e.g. a W13 quantised once per optimiser step):
  * AB = bf16(q(X) q(W13)^T / (scale_x scale_w13)) and h = bf16(silu(a) * b)

@@ -64,6 +64,9 @@ def test_every_wrapper_marshals(rec):
     binding.f8_linear_fwd_w13_swiglu(x, _bf(2 * F, K))
     binding.f8_gemm_w13_swiglu(q, torch.zeros((2 * F, K), dtype=torch.uint8), torch.ones(1),
                                torch.ones(1))
+    _, _, saved13, _, _, _, _ = binding.f8_linear_fwd_w13_swiglu(x, _bf(2 * F, K))
+    binding.f8_linear_bwd_w13_swiglu(_bf(M, F), _bf(M, 2 * F), saved13)
+    binding.f8_quantize_swiglu_bwd(_bf(M, F), _bf(M, 2 * F))
     binding.f8_selftest_wait_timeout(1000)
     wrapped = {n for n in binding.EXPORTS if hasattr(binding, n)}
     called = set(rec.calls)

@@ -163,3 +163,100 @@ def test_gemm_w13_swiglu_alone_equals_fused_call(f8, M, F, K):
     assert torch.equal(ab.view(torch.int16), ab2.view(torch.int16))
     assert torch.equal(h.view(torch.int16), h2.view(torch.int16))
     assert amax2.item() == amax_h.item() == float(oracle.quantize(wl.bits(h.cpu()))["amax"])
+
+
+def _split(ab):
+    return oracle.split_ab(wl.bits(ab.cpu()))
+
+
+@pytest.mark.parametrize("M,F,K", [(256, 256, 256), (272, 384, 528), (128, 128, 64)])
+def test_w13_swiglu_bwd_full_compare(f8, M, F, K):
+    """Forward, then the backward for a random dh: d(AB) bit-exact against
+    the oracle's swiglu_bwd of dh and the GPU's own a, b (merged in AB's
+    order); dX and dW13 within the GEMM bar against the oracle's linear_bwd
+    of that d(AB)."""
+    x, w1, w3 = _inputs(M, F, K, 3 * M + F)
+    w13 = _interleave(w1, w3)
+    dh = (torch.randn((M, F), generator=torch.Generator().manual_seed(M + 7)) * 0.01).to(torch.bfloat16)
+    ab, h, saved, h_q, h_t, scale_h, amax_h = f8.f8_linear_fwd_w13_swiglu(x.to(DEV), w13.to(DEV))
+    dx, dw, dab = f8.f8_linear_bwd_w13_swiglu(dh.to(DEV), ab, saved)
+    assert f8.f8_last_device_status() == 0
+    a_g, b_g = _split(ab)
+    da, db = oracle.swiglu_bwd(wl.bits(dh), a_g, b_g)
+    dab_or = oracle.merge_ab(da, db)
+    assert np.array_equal(wl.bits(dab.cpu()), dab_or)
+    fwd = oracle.linear_fwd(wl.bits(x), wl.bits(w13))
+    bwd = oracle.linear_bwd(dab_or, fwd)
+    check_close(dx, bwd["dx"], what="dX of the group")
+    check_close(dw, bwd["dw"], what="dW13")
+
+
+@pytest.mark.parametrize("order", ["sorted", "shuffled"])
+def test_w13_swiglu_bwd_every_bf16_a(f8, order):
+    """d(AB) for every one of the 65536 bf16 values of a (inf and NaN
+    included) with random b and dh: bit-exact, except that a NaN only has to
+    stay a NaN."""
+    M, F, K = 256, 256, 64
+    codes = np.arange(65536, dtype=np.uint16)
+    if order == "shuffled":
+        codes = codes[np.random.default_rng(9).permutation(65536)]
+    a = codes.reshape(M, F)
+    rng = torch.Generator().manual_seed(10)
+    b = wl.bits(torch.randn((M, F), generator=rng).to(torch.bfloat16))
+    dh = torch.randn((M, F), generator=rng).to(torch.bfloat16)
+    ab = torch.from_numpy(oracle.merge_ab(a, b).view(np.int16).copy()).view(torch.bfloat16)
+    x, w1, w3 = _inputs(M, F, K, 11)
+    _, _, saved, _, _, _, _ = f8.f8_linear_fwd_w13_swiglu(x.to(DEV), _interleave(w1, w3).to(DEV))
+    _, _, dab = f8.f8_linear_bwd_w13_swiglu(dh.to(DEV), ab.to(DEV), saved)
+    f8.f8_last_device_status()   # NaN inputs flag the amax non-finite; clear it
+    da, db = oracle.swiglu_bwd(wl.bits(dh), a, b)
+    ref = oracle.merge_ab(da, db).ravel()
+    got = wl.bits(dab.cpu()).ravel()
+    nan_ref = (ref & 0x7FFF) > 0x7F80
+    assert np.array_equal(nan_ref, (got & 0x7FFF) > 0x7F80)
+    assert np.array_equal(got[~nan_ref], ref[~nan_ref])
+
+
+def test_w13_swiglu_bwd_llama8b(f8):
+    """The Llama-3.1-8B FFN backward through the group at full size
+    (M=8192, K=4096, F=14336): d(AB) bit-exact in full; dX and dW13 on one
+    sampled row per 128-row block."""
+    M, F, K = 8192, 14336, 4096
+    x = wl.normal((M, K), 1.0, wl.seed_of(3, 0, 0))
+    w13 = _interleave(wl.normal((F, K), 0.02, wl.seed_of(3, 0, 1)),
+                      wl.normal((F, K), 0.02, wl.seed_of(3, 1, 1)))
+    dh = wl.normal((M, F), 0.01, wl.seed_of(3, 2, 5))
+    ab, h, saved, h_q, h_t, scale_h, amax_h = f8.f8_linear_fwd_w13_swiglu(x.to(DEV), w13.to(DEV))
+    dx, dw, dab = f8.f8_linear_bwd_w13_swiglu(dh.to(DEV), ab, saved)
+    assert f8.f8_last_device_status() == 0
+    a_g, b_g = _split(ab)
+    da, db = oracle.swiglu_bwd(wl.bits(dh), a_g, b_g)
+    dab_or = oracle.merge_ab(da, db)
+    assert np.array_equal(wl.bits(dab.cpu()), dab_or)
+    q = oracle.quantize(dab_or)
+    qx = oracle.quantize(wl.bits(x))
+    qw = oracle.quantize(wl.bits(w13))
+    rng = np.random.default_rng(14)
+    rows = np.array([r * 128 + rng.integers(0, 128) for r in range(M // 128)], np.int64)
+    check_close(dx[torch.from_numpy(rows).to(DEV)],
+                oracle.gemm_rows(q["q"], qw["qt"], q["scale"], qw["scale"], rows), what="dX rows")
+    rows_n = np.array([r * 128 + rng.integers(0, 128) for r in range(2 * F // 128)], np.int64)
+    check_close(dw[torch.from_numpy(rows_n).to(DEV)],
+                oracle.gemm_rows(q["qt"], qx["qt"], q["scale"], qx["scale"], rows_n), what="dW13 rows")
+
+
+def test_quantize_swiglu_bwd_alone(f8):
+    """f8_quantize_swiglu_bwd gives the d(AB) of the full backward and the
+    oracle's quantize of it: amax, scale, q and q^T bit-exact."""
+    M, F = 272, 384
+    g = torch.Generator().manual_seed(23)
+    ab = torch.randn((M, 2 * F), generator=g).to(torch.bfloat16)
+    dh = (torch.randn((M, F), generator=g) * 0.01).to(torch.bfloat16)
+    q, qt, s, amax, dab = f8.f8_quantize_swiglu_bwd(dh.to(DEV), ab.to(DEV))
+    assert f8.f8_last_device_status() == 0
+    a, b = oracle.split_ab(wl.bits(ab))
+    ref_dab = oracle.merge_ab(*oracle.swiglu_bwd(wl.bits(dh), a, b))
+    assert np.array_equal(wl.bits(dab.cpu()), ref_dab)
+    ref = oracle.quantize(ref_dab)
+    assert amax.item() == float(ref["amax"]) and s.item() == float(ref["scale"])
+    assert np.array_equal(q.cpu().numpy(), ref["q"]) and np.array_equal(qt.cpu().numpy(), ref["qt"])
