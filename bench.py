@@ -711,11 +711,13 @@ def cpu_baseline(config: int, rows: int):
     from float8_mixed_precision_gb300 import workloads as wl
     flops, sec = oracle_sample(config, 0, rows)
     lin = wl.workload(config)[1][0]
+    rm, rn = min(rows, lin.M), min(rows, lin.N)
     return {"value": flops / sec / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
             "kind": "oracle", "seconds": sec,
             "sample": (f"linear {lin.name} (M={lin.M}, K={lin.K}, N={lin.N}): amax, scale and "
-                       f"cast of X, W, dY in full, then {rows} sampled output rows of each of "
-                       f"Y, dX and dW; value = GEMM flops of the sampled rows / wall time")}
+                       f"cast of X, W, dY in full, then {rm} of {lin.M} output rows of Y and of "
+                       f"dX and {rn} of {lin.N} rows of dW; value = GEMM flops of those rows / "
+                       f"wall time")}
 
 
 class OracleSampler:
@@ -815,7 +817,7 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--cpu-rows", type=int, default=1024)
+    ap.add_argument("--cpu-rows", type=int, default=8192)
     ap.add_argument("--ref-rows", type=int, default=128)
     ap.add_argument("--graph", type=int, default=1,
                     help="replay the step as one captured CUDA graph (1) or launch it call by call (0)")
