@@ -508,7 +508,7 @@ def run_ours(args, world, rank, local):
             "gpu_launches": sum(L.launches for L in layers) * args.steps, "isolated": iso}
 
 
-def kernel_bench(f8, layers, device, stream, iters=20):
+def kernel_bench(f8, layers, device, stream, iters=50):
     """Each kernel timed alone on the workload's tensors, L2 flushed before
     every launch (a 512 MB fill, then a 256 MB read so that the L2 holds
     clean lines and the timed kernel pays no write-back for the flush), CUDA
