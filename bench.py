@@ -165,7 +165,6 @@ class ClockSampler:
 class Linear8:
     """Device buffers of one linear: inputs, outputs, saved tensors, workspace."""
 
-    launches = 9  # our kernels per step: amax + cast of X, W, dY; 3 GEMMs
 
     def __init__(self, f8, lin, inputs, device, dy_fmt=0, swiglu=None, ab=None):
         import torch
@@ -242,8 +241,6 @@ class FfnIn8(Linear8):
     q(h), q(h)^T and h's amax and scale for the W2Q8 that follows, then the
     group's backward."""
 
-    launches = 10  # amax + cast of X, W13; the GEMM; cast of h; amax + cast of dY; 2 GEMMs
-
     def __init__(self, f8, lin, inputs, device, dy_fmt=0, chain=False):
         import torch
         super().__init__(f8, lin, inputs, device, dy_fmt)
@@ -255,7 +252,6 @@ class FfnIn8(Linear8):
         # backward, which the W2Q8 runs after its own backward
         self.chain = chain
         if chain:
-            self.launches = 6
             self.dy = torch.empty_like(self.y)  # d(AB), written each step
 
     def step(self, f8):
@@ -300,14 +296,10 @@ class W2Q8(Linear8):
     """The w2 linear fed by the q(h) that its FfnIn8 produced: W2 quantised
     (f8_quantize), the GEMM on q(h) (f8_gemm), then the linear's backward."""
 
-    launches = 7  # amax + cast of W2; the GEMM; amax + cast of dY; 2 GEMMs
-
     def __init__(self, f8, lin, inputs, device, dy_fmt, src: FfnIn8):
         super().__init__(f8, lin, inputs, device, dy_fmt)
         self.src = src
         src.next = self
-        if src.chain:
-            self.launches = 7 + 4  # ... then the SwiGLU backward, cast of d(AB), 2 GEMMs
 
     def step(self, f8):
         s = self.saved
@@ -392,8 +384,10 @@ def run_ours(args, world, rank, local):
 
     # ---- warm-up, then the timed region (library calls f8_linear_fwd/bwd)
     for _ in range(args.warmup):
+        n0 = f8.f8_kernel_launches()
         for L in layers:
             L.step(f8)
+        launches_per_step = f8.f8_kernel_launches() - n0  # counted by libf8 itself
     graph = None
     if args.graph:
         # one whole step (every launch of every linear) captured once and replayed
@@ -505,7 +499,7 @@ def run_ours(args, world, rank, local):
     return {"value": value, "ms_per_step": ms_max / args.steps, "name": name, "lins": lins,
             "clocks": clocks.summary(), "kernels": kernels, "roofline": roofline,
             "breakdown_ms_per_step": breakdown_ms, "e2e": e2e,
-            "gpu_launches": sum(L.launches for L in layers) * args.steps, "isolated": iso}
+            "gpu_launches": launches_per_step * args.steps, "isolated": iso}
 
 
 def kernel_bench(f8, layers, device, stream, iters=50):

@@ -33,7 +33,7 @@ EXPORTS = ("f8_amax", "f8_cast_transpose", "f8_gemm", "f8_linear_workspace_bytes
            "f8_quantize", "f8_quantize_workspace_bytes", "f8_quantize_fmt", "f8_gemm_fmt",
            "f8_linear_bwd_fmt", "f8_quantize_swiglu", "f8_linear_fwd_swiglu",
            "f8_linear_fwd_w13_swiglu", "f8_gemm_w13_swiglu", "f8_linear_bwd_w13_swiglu",
-           "f8_quantize_swiglu_bwd")
+           "f8_quantize_swiglu_bwd", "f8_kernel_launches")
 
 F8_E4M3 = 0
 F8_E5M2 = 1
@@ -115,6 +115,8 @@ def lib() -> ctypes.CDLL:
         L.f8_quantize_swiglu_bwd.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, vp, vp,
                                              ctypes.c_size_t, vp]
         L.f8_quantize_swiglu_bwd.restype = st
+        L.f8_kernel_launches.argtypes = []
+        L.f8_kernel_launches.restype = ctypes.c_ulonglong
         L.f8_gemm_w13_swiglu.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp]
         L.f8_gemm_w13_swiglu.restype = st
         L.f8_linear_fwd_noalloc.argtypes = [vp, vp, i64, i64, i64, vp, ctypes.POINTER(_Saved), vp]
@@ -144,6 +146,11 @@ def _ptr(t: torch.Tensor | None):
 def _check(status: int, where: str):
     if status != F8_OK:
         raise F8Error(status, where)
+
+
+def f8_kernel_launches() -> int:
+    """Kernels libf8 has launched in this process so far."""
+    return int(lib().f8_kernel_launches())
 
 
 def f8_status_string(status: int) -> str:

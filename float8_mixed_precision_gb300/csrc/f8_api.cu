@@ -16,6 +16,10 @@
 __device__ unsigned g_f8_status_word;
 
 namespace f8 {
+std::atomic<unsigned long long> g_kernel_launches{0};
+} // namespace f8
+
+namespace f8 {
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -43,6 +47,8 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // partial maxima of X and of W.  Of the backward pass: q(dY) [M,N],
 // q(dY)^T [N,M], amax and scale of dY, then the partial maxima of dY.
 constexpr size_t kPartialsBytes = sizeof(unsigned) * kMaxAmaxPartials;
+// X + W (bf16) up to which f8_linear_fwd quantises the two in shared launches
+constexpr int64_t kPairMaxBytes = 112ll << 20;
 
 struct FwdWs {
     uint8_t *x_q;
@@ -342,14 +348,28 @@ f8_status f8_linear_fwd(const void *x, const void *w, int64_t M, int64_t N, int6
     F8_TRY(get_device(&dev));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const FwdWs fw = fwd_ws(workspace, M, N, K);
-    int np = 0;
-    // each cast follows its own amax so that its re-read of the tensor hits L2
-    F8_TRY_CUDA(launch_amax_partials(x, M * K, fw.parts_x, &np, *dev, st));
-    F8_TRY_CUDA(launch_cast_transpose(x, M, K, nullptr, fw.parts_x, np, saved->amax_x,
-                                      saved->scale_x, fw.x_q, saved->x_t, 0, *dev, st));
-    F8_TRY_CUDA(launch_amax_partials(w, N * K, fw.parts_w, &np, *dev, st));
-    F8_TRY_CUDA(launch_cast_transpose(w, N, K, nullptr, fw.parts_w, np, saved->amax_w,
-                                      saved->scale_w, fw.w_q, saved->w_t, 0, *dev, st));
+    // X and W together when they fit in L2 with room to spare (the cast
+    // re-reads what the amax launch just read): two launches instead of four
+    bool pair = quant_pair_enabled() && 2 * (M * K + N * K) <= kPairMaxBytes;
+    if (pair) {
+        const cudaError_t e = launch_quantize_pair(
+            x, M, K, w, N, K, fw.parts_x, fw.parts_w, saved->amax_x, saved->scale_x, fw.x_q,
+            saved->x_t, saved->amax_w, saved->scale_w, fw.w_q, saved->w_t, *dev, st);
+        if (e == cudaErrorNotSupported)
+            pair = false;  // nothing was launched
+        else
+            F8_TRY_CUDA(e);
+    }
+    if (!pair) {
+        int np = 0;
+        // each cast follows its own amax so that its re-read of the tensor hits L2
+        F8_TRY_CUDA(launch_amax_partials(x, M * K, fw.parts_x, &np, *dev, st));
+        F8_TRY_CUDA(launch_cast_transpose(x, M, K, nullptr, fw.parts_x, np, saved->amax_x,
+                                          saved->scale_x, fw.x_q, saved->x_t, 0, *dev, st));
+        F8_TRY_CUDA(launch_amax_partials(w, N * K, fw.parts_w, &np, *dev, st));
+        F8_TRY_CUDA(launch_cast_transpose(w, N, K, nullptr, fw.parts_w, np, saved->amax_w,
+                                          saved->scale_w, fw.w_q, saved->w_t, 0, *dev, st));
+    }
     return from_cuda(launch_gemm(fw.x_q, fw.w_q, M, N, K, saved->scale_x, saved->scale_w, y, *dev, st));
 }
 
@@ -575,6 +595,11 @@ f8_status f8_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int64_t M
     return from_cuda(launch_gemm_w13_swiglu(x_q, w13_q, M, F, K, scale_x, scale_w13, ab, h,
                                             reinterpret_cast<unsigned *>(amax_h), &nh, *dev, st,
                                             true));
+}
+
+unsigned long long f8_kernel_launches(void)
+{
+    return g_kernel_launches.load(std::memory_order_relaxed);
 }
 
 f8_status f8_last_device_status(void *stream)

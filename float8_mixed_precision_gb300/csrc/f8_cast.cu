@@ -91,6 +91,53 @@ amax_kernel(const uint4 *__restrict__ x, int64_t nvec, const uint16_t *__restric
     }
 }
 
+// Partial maxima of two tensors in one launch (no tails: both lengths are
+// multiples of 8): blocks [0, b0) take x0, the rest x1, each with its own
+// grid stride; block i of a tensor writes that tensor's partial i.
+__global__ void __launch_bounds__(kAmaxThreads, 4)
+amax_pair_kernel(const uint4 *__restrict__ x0, int64_t nvec0, const uint4 *__restrict__ x1,
+                 int64_t nvec1, int b0, unsigned *__restrict__ parts0, unsigned *__restrict__ parts1,
+                 unsigned *__restrict__ status)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    const bool second = static_cast<int>(blockIdx.x) >= b0;
+    const uint4 *__restrict__ x = second ? x1 : x0;
+    const int64_t nvec = second ? nvec1 : nvec0;
+    const int bid = second ? static_cast<int>(blockIdx.x) - b0 : static_cast<int>(blockIdx.x);
+    const int nblk = second ? static_cast<int>(gridDim.x) - b0 : b0;
+    uint32_t m2 = 0;
+    const int64_t S = static_cast<int64_t>(nblk) * blockDim.x;
+    for (int64_t base = static_cast<int64_t>(bid) * blockDim.x + threadIdx.x; base < nvec;
+         base += kAmaxUnroll * S) {
+        uint4 v[kAmaxUnroll];
+#pragma unroll
+        for (int u = 0; u < kAmaxUnroll; ++u) {
+            const int64_t i = base + u * S;
+            v[u] = i < nvec ? __ldg(x + i) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kAmaxUnroll; ++u)
+            m2 = max_u16x2(m2, v[u]);
+    }
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    __shared__ uint32_t warp_max[kAmaxThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0)
+        warp_max[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        m = lane < kAmaxThreads / 32 ? warp_max[lane] : 0u;
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if (lane == 0) {
+            if (m >= 0x7F80u)
+                atomicOr(status, kStatusNonfinite);
+            (second ? parts1 : parts0)[bid] = m << 16;
+        }
+    }
+}
+
 // ----------------------------------------------------------------- cast
 constexpr int kTile = 128;
 constexpr int kCastThreads = 256;
@@ -408,12 +455,24 @@ constexpr int kInBytes = kTile * kTile * 2;
 constexpr int kInStages = 3;
 constexpr int kTmaCastSmem = kInStages * kInBytes + kTile * kTile + 64 + 128;
 
-template <int FMT>
+// One tensor's share of a cast launch: shape, where its amax comes from and
+// where its outputs go (outputs may be NULL).
+struct CastSeg {
+    int64_t rows, cols;
+    const float *amax;
+    const unsigned *partials;
+    int nparts;
+    float *amax_out, *scale_out;
+    uint8_t *q, *qt;
+};
+
+// NSEG = 2: the tiles of the second tensor follow those of the first in one
+// persistent loop, each tile with its own tensor's map, scale and outputs.
+template <int FMT, int NSEG>
 __global__ void __launch_bounds__(kCastThreads)
-cast_transpose_tma_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t rows, int64_t cols,
-                          const float *__restrict__ amax, const unsigned *__restrict__ partials,
-                          int nparts, float *__restrict__ amax_out, float *__restrict__ scale_out,
-                          uint8_t *__restrict__ q, uint8_t *__restrict__ qt,
+cast_transpose_tma_kernel(const __grid_constant__ CUtensorMap tmap0,
+                          const __grid_constant__ CUtensorMap tmap1,
+                          const __grid_constant__ CastSeg seg0, const __grid_constant__ CastSeg seg1,
                           unsigned *__restrict__ status, uint64_t limit_ns)
 {
     extern __shared__ uint8_t cast_smem_raw[];
@@ -428,30 +487,56 @@ cast_transpose_tma_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t ro
             mbar_init(&bar[b], 1);
         abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmap_x);
+        tma_prefetch_desc(&tmap0);
+        if (NSEG == 2)
+            tma_prefetch_desc(&tmap1);
     }
     __syncthreads();
     griddep_wait();
     griddep_launch_dependents();
-    const float a = partials != nullptr ? reduce_partials(partials, nparts) : *amax;
-    const float s = scale_of<FMT>(a);
+    const float a0 = seg0.partials != nullptr ? reduce_partials(seg0.partials, seg0.nparts) : *seg0.amax;
+    const float s0 = scale_of<FMT>(a0);
+    float a1 = 0.0f, s1 = 0.0f;
+    if (NSEG == 2) {
+        a1 = seg1.partials != nullptr ? reduce_partials(seg1.partials, seg1.nparts) : *seg1.amax;
+        s1 = scale_of<FMT>(a1);
+    }
     if (blockIdx.x == 0 && t == 0) {
-        if (scale_out != nullptr)
-            *scale_out = s;
-        if (amax_out != nullptr)
-            *amax_out = a;
+        if (seg0.scale_out != nullptr)
+            *seg0.scale_out = s0;
+        if (seg0.amax_out != nullptr)
+            *seg0.amax_out = a0;
+        if (NSEG == 2) {
+            if (seg1.scale_out != nullptr)
+                *seg1.scale_out = s1;
+            if (seg1.amax_out != nullptr)
+                *seg1.amax_out = a1;
+        }
     }
 
-    const int64_t tiles_c = cols / kTile;
-    const int64_t ntiles = (rows / kTile) * tiles_c;
+    const int64_t tiles_c0 = seg0.cols / kTile;
+    const int64_t ntiles0 = (seg0.rows / kTile) * tiles_c0;
+    const int64_t tiles_c1 = NSEG == 2 ? seg1.cols / kTile : 1;
+    const int64_t ntiles = ntiles0 + (NSEG == 2 ? (seg1.rows / kTile) * tiles_c1 : 0);
     const int64_t nmine = ntiles > blockIdx.x ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    // tile tix of the launch -> (tensor, tile row start, tile column start)
+    auto locate = [&](int64_t tix, bool &second, int64_t &r0, int64_t &c0) {
+        second = NSEG == 2 && tix >= ntiles0;
+        const int64_t lt = second ? tix - ntiles0 : tix;
+        const int64_t tc = second ? tiles_c1 : tiles_c0;
+        r0 = (lt / tc) * kTile;
+        c0 = (lt % tc) * kTile;
+    };
     auto issue = [&](int64_t k) {
         const int64_t tix = blockIdx.x + k * gridDim.x;
+        bool second;
+        int64_t r0, c0;
+        locate(tix, second, r0, c0);
         const int b = static_cast<int>(k % kInStages);
         fence_proxy_async_shared();  // earlier generic reads of this buffer come first
         mbar_arrive_expect_tx(&bar[b], kInBytes);
-        tma_load_2d(sm + b * kInBytes, &tmap_x, &bar[b], static_cast<int32_t>((tix % tiles_c) * kTile),
-                    static_cast<int32_t>((tix / tiles_c) * kTile));
+        tma_load_2d(sm + b * kInBytes, second ? &tmap1 : &tmap0, &bar[b], static_cast<int32_t>(c0),
+                    static_cast<int32_t>(r0));
     };
     if (t == 0)
         for (int64_t j = 0; j < nmine && j < kInStages - 1; ++j)
@@ -467,9 +552,14 @@ cast_transpose_tma_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t ro
         }
         if (__syncthreads_or(abort_flag))
             break;
-        const int64_t tix = blockIdx.x + k * gridDim.x;
-        const int64_t r0 = (tix / tiles_c) * kTile;
-        const int64_t c0 = (tix % tiles_c) * kTile;
+        bool second;
+        int64_t r0, c0;
+        locate(blockIdx.x + k * gridDim.x, second, r0, c0);
+        const float s = second ? s1 : s0;
+        const int64_t rows = second ? seg1.rows : seg0.rows;
+        const int64_t cols = second ? seg1.cols : seg0.cols;
+        uint8_t *q = second ? seg1.q : seg0.q;
+        uint8_t *qt = second ? seg1.qt : seg0.qt;
         const uint8_t *src = sm + b * kInBytes;
         // ---- phase 1: 8 passes of 16 rows; thread t converts 8 consecutive bf16
 #pragma unroll
@@ -495,7 +585,6 @@ cast_transpose_tma_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t ro
                       limit_ns);
     }
 }
-
 } // namespace
 
 namespace {
@@ -519,12 +608,14 @@ const Occupancy &occupancy(const DeviceInfo &dev)
         o.amax_partials = n > 0 ? n : 1;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cast_transpose_kernel<0>, kCastThreads, 0);
         o.cast = n > 0 ? n : 1;
-        cudaFuncSetAttribute(cast_transpose_tma_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kTmaCastSmem);
-        cudaFuncSetAttribute(cast_transpose_tma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kTmaCastSmem);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cast_transpose_tma_kernel<0>, kCastThreads,
-                                                      kTmaCastSmem);
+        cudaFuncSetAttribute(cast_transpose_tma_kernel<0, 1>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaCastSmem);
+        cudaFuncSetAttribute(cast_transpose_tma_kernel<1, 1>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaCastSmem);
+        cudaFuncSetAttribute(cast_transpose_tma_kernel<0, 2>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaCastSmem);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cast_transpose_tma_kernel<0, 1>,
+                                                      kCastThreads, kTmaCastSmem);
         o.cast_tma = n > 0 ? n : 1;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, swiglu_amax_kernel, kAmaxThreads, 0);
         o.swiglu = n > 0 ? n : 1;
@@ -532,6 +623,11 @@ const Occupancy &occupancy(const DeviceInfo &dev)
         o.swiglu_bwd = n > 0 ? n : 1;
     }
     return o;
+}
+
+bool tma_castable(int64_t rows, int64_t cols)
+{
+    return rows % kTile == 0 && cols % kTile == 0 && rows > 0 && cols > 0 && cast_tma_enabled();
 }
 
 int64_t amax_grid(int64_t nvec, int per_sm, const DeviceInfo &dev)
@@ -558,6 +654,7 @@ cudaError_t launch_amax(const void *x, int64_t n, float *amax_out, const DeviceI
     const uint16_t *tail = static_cast<const uint16_t *>(x) + nvec * 8;
     const int64_t blocks = amax_grid(nvec, occupancy(dev).amax_atomic, dev);
     // follows a memset, so it is launched without programmatic serialization
+    count_launch();
     amax_kernel<false><<<static_cast<unsigned>(blocks), kAmaxThreads, 0, stream>>>(
         static_cast<const uint4 *>(x), nvec, tail, ntail, reinterpret_cast<unsigned *>(amax_out),
         dev.status);
@@ -584,17 +681,17 @@ cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, con
 {
     const int64_t ntiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
     CUtensorMap map;
-    if (rows % kTile == 0 && cols % kTile == 0 && rows > 0 && cols > 0 && cast_tma_enabled() &&
+    if (tma_castable(rows, cols) &&
         make_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, rows, cols, kTile, kTile,
                            CU_TENSOR_MAP_SWIZZLE_NONE)) {
         int64_t blocks = ntiles;
         const int64_t cap = static_cast<int64_t>(dev.sm_count) * occupancy(dev).cast_tma;
         if (blocks > cap)
             blocks = cap;
-        return launch_pdl(fmt == 1 ? cast_transpose_tma_kernel<1> : cast_transpose_tma_kernel<0>,
+        const CastSeg seg{rows, cols, amax, partials, nparts, amax_out, scale_out, q, q_t};
+        return launch_pdl(fmt == 1 ? cast_transpose_tma_kernel<1, 1> : cast_transpose_tma_kernel<0, 1>,
                           dim3(static_cast<unsigned>(blocks)), dim3(kCastThreads), kTmaCastSmem,
-                          stream, map, rows, cols, amax, partials, nparts, amax_out, scale_out, q,
-                          q_t, dev.status, wait_limit_ns());
+                          stream, map, map, seg, seg, dev.status, wait_limit_ns());
     }
     int64_t blocks = ntiles;
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * occupancy(dev).cast;
@@ -655,6 +752,47 @@ cudaError_t launch_swiglu_bwd_amax(const void *dh, const void *ab, void *dab, in
     return launch_pdl(swiglu_bwd_amax_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kAmaxThreads),
                       0, stream, static_cast<const uint4 *>(dh), static_cast<const uint4 *>(ab),
                       static_cast<uint4 *>(dab), nvec, partials, dev.status);
+}
+
+cudaError_t launch_quantize_pair(const void *x0, int64_t rows0, int64_t cols0, const void *x1,
+                                 int64_t rows1, int64_t cols1, unsigned *parts0, unsigned *parts1,
+                                 float *amax0, float *scale0, uint8_t *q0, uint8_t *qt0,
+                                 float *amax1, float *scale1, uint8_t *q1, uint8_t *qt1,
+                                 const DeviceInfo &dev, cudaStream_t stream)
+{
+    if (!tma_castable(rows0, cols0) || !tma_castable(rows1, cols1))
+        return cudaErrorNotSupported;
+    CUtensorMap m0, m1;
+    if (!make_tensor_map_2d(&m0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x0, rows0, cols0, kTile, kTile,
+                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tensor_map_2d(&m1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x1, rows1, cols1, kTile, kTile,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorNotSupported;
+    const int64_t nvec0 = rows0 * cols0 / 8, nvec1 = rows1 * cols1 / 8;
+    const Occupancy &occ = occupancy(dev);
+    // the amax blocks, shared in proportion to the tensors' sizes
+    const int64_t total = amax_grid(nvec0 + nvec1, occ.amax_partials, dev);
+    if (total < 2)
+        return cudaErrorNotSupported;
+    int64_t b0 = (total * nvec0 + (nvec0 + nvec1) / 2) / (nvec0 + nvec1);
+    b0 = b0 < 1 ? 1 : (b0 > total - 1 ? total - 1 : b0);
+    cudaError_t e = launch_pdl(amax_pair_kernel, dim3(static_cast<unsigned>(total)),
+                               dim3(kAmaxThreads), 0, stream, static_cast<const uint4 *>(x0), nvec0,
+                               static_cast<const uint4 *>(x1), nvec1, static_cast<int>(b0), parts0,
+                               parts1, dev.status);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t ntiles = (rows0 / kTile) * (cols0 / kTile) + (rows1 / kTile) * (cols1 / kTile);
+    int64_t blocks = ntiles;
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * occ.cast_tma;
+    if (blocks > cap)
+        blocks = cap;
+    const CastSeg s0{rows0, cols0, nullptr, parts0, static_cast<int>(b0), amax0, scale0, q0, qt0};
+    const CastSeg s1{rows1, cols1, nullptr, parts1, static_cast<int>(total - b0), amax1, scale1, q1,
+                     qt1};
+    return launch_pdl(cast_transpose_tma_kernel<0, 2>, dim3(static_cast<unsigned>(blocks)),
+                      dim3(kCastThreads), kTmaCastSmem, stream, m0, m1, s0, s1, dev.status,
+                      wait_limit_ns());
 }
 
 } // namespace f8

@@ -683,6 +683,7 @@ cudaError_t launch_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, const DeviceInfo &dev, cudaStream_t stream)
 {
+    count_launch();
     wait_selftest_kernel<<<1, 32, 0, stream>>>(dev.status, limit_ns);
     return cudaGetLastError();
 }

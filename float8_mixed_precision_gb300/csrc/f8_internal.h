@@ -6,6 +6,7 @@
 #include <cstdlib>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <utility>
 
 namespace f8 {
@@ -38,6 +39,20 @@ inline bool cast_tma_enabled()
     const char *e = std::getenv("F8_CAST_TMA");
     return e == nullptr || e[0] != '0';
 }
+
+// X and W of a small linear are quantised together (one amax launch, one
+// cast launch) unless F8_QUANT_PAIR=0.
+inline bool quant_pair_enabled()
+{
+    const char *e = std::getenv("F8_QUANT_PAIR");
+    return e == nullptr || e[0] != '0';
+}
+
+// Kernels this library has launched in this process (every launch site adds
+// one; defined in f8_api.cu).
+extern std::atomic<unsigned long long> g_kernel_launches;
+
+inline void count_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
 
 // Programmatic dependent launch is on unless F8_PDL=0.
 inline bool pdl_enabled()
@@ -75,6 +90,7 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
+    count_launch();
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
@@ -138,6 +154,17 @@ cudaError_t launch_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int
 cudaError_t launch_swiglu_bwd_amax(const void *dh, const void *ab, void *dab, int64_t M, int64_t F,
                                    unsigned *partials, int *nparts, const DeviceInfo &dev,
                                    cudaStream_t stream);
+
+// E4M3 quantisation of two bf16 tensors in two launches instead of four:
+// one amax launch writing each tensor's partial maxima (parts0, parts1), then
+// one TMA cast launch over the tiles of both.  cudaErrorNotSupported (and
+// nothing launched) unless both shapes are multiples of 128 and the TMA cast
+// is enabled.
+cudaError_t launch_quantize_pair(const void *x0, int64_t rows0, int64_t cols0, const void *x1,
+                                 int64_t rows1, int64_t cols1, unsigned *parts0, unsigned *parts1,
+                                 float *amax0, float *scale0, uint8_t *q0, uint8_t *qt0,
+                                 float *amax1, float *scale1, uint8_t *q1, uint8_t *qt1,
+                                 const DeviceInfo &dev, cudaStream_t stream);
 
 // One CTA waiting on an mbarrier that is never signalled (failure-path test).
 cudaError_t launch_wait_selftest(uint64_t limit_ns, const DeviceInfo &dev, cudaStream_t stream);

@@ -350,6 +350,14 @@ f8_status f8_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int64_t M
                              void *h, float *amax_h, void *stream);
 
 /*
+ * Number of kernels this library has launched (enqueued) in this process so
+ * far, over all devices and streams; host-side, no synchronisation.  The
+ * difference across a sequence of calls is the number of GPU kernels those
+ * calls launched (memsets are not counted).
+ */
+unsigned long long f8_kernel_launches(void);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns F8_OK, F8_ERR_NONFINITE or F8_ERR_TIMEOUT (the first set
  * bit in that order of severity: TIMEOUT wins), or F8_ERR_CUDA if the

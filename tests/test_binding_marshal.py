@@ -71,5 +71,6 @@ def test_every_wrapper_marshals(rec):
     wrapped = {n for n in binding.EXPORTS if hasattr(binding, n)}
     called = set(rec.calls)
     assert wrapped - {"f8_status_string", "f8_last_device_status", "f8_set_wait_limit_ns",
+                      "f8_kernel_launches",
                       "f8_linear_workspace_bytes", "f8_quantize_workspace_bytes"} <= called, \
         sorted(wrapped - called)
