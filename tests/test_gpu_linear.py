@@ -6,7 +6,9 @@ the same launch configuration the benchmark times; there amax, scales and
 every E4M3 byte (q(X)^T, q(W)^T saved by the forward pass, plus the oracle's
 q of every tensor) are compared in full, and Y, dX, dW on one sampled row
 per 128-row band and one sampled column per 256-column band, so every
-output tile of every GEMM is visited.
+output tile of every GEMM is visited.  The attention projections (2.06
+TFLOP, in workloads 2 and 5) are also compared on every output element
+against the oracle's full GEMMs.
 """
 import numpy as np
 import pytest
@@ -191,3 +193,24 @@ def test_linear_in_cuda_graph_matches_eager(f8):
     assert f8.f8_last_device_status() == 0
     for a, b in zip((y, dx, dw, saved.x_t, saved.w_t, saved.scalars), ref):
         assert torch.equal(a, b)
+
+
+ATTN = [(c, l) for c in (2, 5) for l in range(4)]
+
+
+@pytest.mark.parametrize("c,l", ATTN, ids=[f"w{c}-{n}" for c in (2, 5) for n in ("wq", "wk", "wv", "wo")])
+def test_attention_workload_every_output(f8, c, l):
+    """The Llama-3.1-8B attention projections at full size (M=8192), with
+    normal inputs (workload 2) and with Student-t inputs carrying x100
+    outliers (workload 5): every element of Y, dX and dW against the
+    oracle's full GEMMs (about 25 s of oracle time on 16 host cores per
+    workload)."""
+    d = wl.linear_inputs(c, l)
+    y, dx, dw, saved = _run_gpu(f8, d["x"], d["w"], d["dy"])
+    qx = oracle.quantize(wl.bits(d["x"]))
+    qw = oracle.quantize(wl.bits(d["w"]))
+    qdy = oracle.quantize(wl.bits(d["dy"]))
+    _check_saved(saved, {"x": qx, "w": qw})
+    check_close(y, oracle.gemm(qx["q"], qw["q"], qx["scale"], qw["scale"]), what="Y")
+    check_close(dx, oracle.gemm(qdy["q"], qw["qt"], qdy["scale"], qw["scale"]), what="dX")
+    check_close(dw, oracle.gemm(qdy["qt"], qx["qt"], qdy["scale"], qx["scale"]), what="dW")
