@@ -15,7 +15,9 @@ from dataclasses import dataclass
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_lib", "libf8.so")
+# F8_LIBRARY selects another build of the same library (the checked build,
+# _lib/libf8_checked.so); it must exist like the default one.
+LIB_PATH = os.environ.get("F8_LIBRARY") or os.path.join(_HERE, "_lib", "libf8.so")
 
 F8_OK = 0
 F8_ERR_INVALID = 1
@@ -25,6 +27,7 @@ F8_ERR_CUDA = 4
 F8_ERR_TIMEOUT = 5
 F8_ERR_NONFINITE = 6
 F8_ERR_UNSUPPORTED = 7
+F8_ERR_BOUNDS = 8
 
 # every symbol include/f8.h declares
 EXPORTS = ("f8_amax", "f8_cast_transpose", "f8_gemm", "f8_linear_workspace_bytes",
@@ -33,7 +36,7 @@ EXPORTS = ("f8_amax", "f8_cast_transpose", "f8_gemm", "f8_linear_workspace_bytes
            "f8_quantize", "f8_quantize_workspace_bytes", "f8_quantize_fmt", "f8_gemm_fmt",
            "f8_linear_bwd_fmt", "f8_quantize_swiglu", "f8_linear_fwd_swiglu",
            "f8_linear_fwd_w13_swiglu", "f8_gemm_w13_swiglu", "f8_linear_bwd_w13_swiglu",
-           "f8_quantize_swiglu_bwd", "f8_kernel_launches")
+           "f8_quantize_swiglu_bwd", "f8_kernel_launches", "f8_selftest_bounds")
 
 F8_E4M3 = 0
 F8_E5M2 = 1
@@ -115,6 +118,8 @@ def lib() -> ctypes.CDLL:
         L.f8_quantize_swiglu_bwd.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, vp, vp,
                                              ctypes.c_size_t, vp]
         L.f8_quantize_swiglu_bwd.restype = st
+        L.f8_selftest_bounds.argtypes = [vp]
+        L.f8_selftest_bounds.restype = st
         L.f8_kernel_launches.argtypes = []
         L.f8_kernel_launches.restype = ctypes.c_ulonglong
         L.f8_gemm_w13_swiglu.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp]
@@ -146,6 +151,12 @@ def _ptr(t: torch.Tensor | None):
 def _check(status: int, where: str):
     if status != F8_OK:
         raise F8Error(status, where)
+
+
+def f8_selftest_bounds(stream=None) -> int:
+    """F8_OK in the checked build (the next status read is F8_ERR_BOUNDS),
+    F8_ERR_UNSUPPORTED in a release build; returns the status, never raises."""
+    return int(lib().f8_selftest_bounds(_stream(stream)))
 
 
 def f8_kernel_launches() -> int:

@@ -1,6 +1,6 @@
 """Build libf8.so in-tree with nvcc for sm_103a.
 
-    python -m float8_mixed_precision_gb300.build [--force] [--ptxas-verbose]
+    python -m float8_mixed_precision_gb300.build [--force] [--ptxas-verbose] [--checked]
 
 Each .cu file under csrc/ is compiled in parallel to an object file, then
 linked into ``_lib/libf8.so`` (CUDA runtime linked statically, so the library
@@ -21,6 +21,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libf8.so")
+# the checked build: device bounds checks compiled in (-DF8_BOUNDS_CHECK)
+LIB_CHECKED = os.path.join(OUT_DIR, "libf8_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -40,25 +42,31 @@ def _deps():
         os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, checked: bool = False) -> str:
+    """Build libf8.so (or, with checked=True, libf8_checked.so with the
+    device bounds checks) unless it is newer than every source."""
+    lib = LIB_CHECKED if checked else LIB
+    if not force and up_to_date(lib):
+        return lib
+    obj_dir = os.path.join(OUT_DIR, "checked") if checked else OUT_DIR
+    os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
                      "-I", CSRC]
+    if checked:
+        common += ["-DF8_BOUNDS_CHECK"]
     if verbose_ptxas:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         r = subprocess.run([cc, *common, "-c", src, "-o", obj], capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -70,13 +78,14 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         for _, err in results:
             sys.stderr.write(err)
     objs = [o for o, _ in results]
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="--ptxas-verbose" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="--ptxas-verbose" in sys.argv,
+                checked="--checked" in sys.argv))

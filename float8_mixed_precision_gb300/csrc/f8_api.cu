@@ -221,6 +221,7 @@ const char *f8_status_string(f8_status s)
     case F8_ERR_TIMEOUT: return "F8_ERR_TIMEOUT: device wait exceeded its time limit";
     case F8_ERR_NONFINITE: return "F8_ERR_NONFINITE: non-finite value in an amax input";
     case F8_ERR_UNSUPPORTED: return "F8_ERR_UNSUPPORTED: needs an sm_103 device and driver";
+    case F8_ERR_BOUNDS: return "F8_ERR_BOUNDS: an index left its buffer (checked build)";
     }
     return "F8_ERR_UNKNOWN";
 }
@@ -615,11 +616,22 @@ f8_status f8_last_device_status(void *stream)
     const unsigned zero = 0;
     if (cudaMemcpy(dev->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
         return F8_ERR_CUDA;
+    if (word & kStatusBounds)
+        return F8_ERR_BOUNDS;
     if (word & kStatusTimeout)
         return F8_ERR_TIMEOUT;
     if (word & kStatusNonfinite)
         return F8_ERR_NONFINITE;
     return F8_OK;
+}
+
+f8_status f8_selftest_bounds(void *stream)
+{
+    if (!bounds_checked_build())
+        return F8_ERR_UNSUPPORTED;
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    return from_cuda(launch_bounds_selftest(*dev, static_cast<cudaStream_t>(stream)));
 }
 
 f8_status f8_selftest_wait_timeout(uint64_t limit_ns, void *stream)

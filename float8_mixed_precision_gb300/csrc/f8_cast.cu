@@ -61,14 +61,14 @@ amax_kernel(const uint4 *__restrict__ x, int64_t nvec, const uint16_t *__restric
 #pragma unroll
         for (int u = 0; u < kAmaxUnroll; ++u) {
             const int64_t i = base + u * S;
-            v[u] = i < nvec ? __ldg(x + i) : make_uint4(0, 0, 0, 0);
+            v[u] = i < nvec && in_range(i, 1, nvec, status) ? __ldg(x + i) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kAmaxUnroll; ++u)
             m2 = max_u16x2(m2, v[u]);
     }
     uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-    if (blockIdx.x == 0 && threadIdx.x < ntail)
+    if (blockIdx.x == 0 && threadIdx.x < ntail && in_range(threadIdx.x, 1, ntail, status))
         m = max(m, static_cast<uint32_t>(tail[threadIdx.x]) & 0x7FFFu);
 
     m = __reduce_max_sync(0xFFFFFFFFu, m);
@@ -114,7 +114,7 @@ amax_pair_kernel(const uint4 *__restrict__ x0, int64_t nvec0, const uint4 *__res
 #pragma unroll
         for (int u = 0; u < kAmaxUnroll; ++u) {
             const int64_t i = base + u * S;
-            v[u] = i < nvec ? __ldg(x + i) : make_uint4(0, 0, 0, 0);
+            v[u] = i < nvec && in_range(i, 1, nvec, status) ? __ldg(x + i) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kAmaxUnroll; ++u)
@@ -224,8 +224,9 @@ swiglu_amax_kernel(const uint4 *__restrict__ a, const uint4 *__restrict__ b, uin
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const int64_t i = base + u * S;
-            va[u] = i < nvec ? __ldg(a + i) : make_uint4(0, 0, 0, 0);
-            vb[u] = i < nvec ? __ldg(b + i) : make_uint4(0, 0, 0, 0);
+            const bool in = i < nvec && in_range(i, 1, nvec, status);
+            va[u] = in ? __ldg(a + i) : make_uint4(0, 0, 0, 0);
+            vb[u] = in ? __ldg(b + i) : make_uint4(0, 0, 0, 0);
         }
         uint32_t amag = 0;
 #pragma unroll
@@ -245,14 +246,14 @@ swiglu_amax_kernel(const uint4 *__restrict__ a, const uint4 *__restrict__ b, uin
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const int64_t i = base + u * S;
-            if (i < nvec) {
+            if (i < nvec && in_range(i, 1, nvec, status)) {
                 h[i] = hv[u];
                 m2 = max_u16x2(m2, hv[u]);
             }
         }
     }
     uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-    if (blockIdx.x == 0 && threadIdx.x < ntail) {
+    if (blockIdx.x == 0 && threadIdx.x < ntail && in_range(threadIdx.x, 1, ntail, status)) {
         const uint32_t hv = swiglu_x2<true>(a_tail[threadIdx.x], b_tail[threadIdx.x]) & 0xFFFFu;
         h_tail[threadIdx.x] = static_cast<uint16_t>(hv);
         m = max(m, hv & 0x7FFFu);
@@ -297,7 +298,9 @@ swiglu_bwd_amax_kernel(const uint4 *__restrict__ dh, const uint4 *__restrict__ a
         for (int u = 0; u < kU; ++u) {
             const int64_t i = base + u * S;
             ia[u] = i + ((i >> 4) << 4);
-            const bool in = i < nvec;
+            const bool in = i < nvec && in_range(i, 1, nvec, status) &&
+                            in_range(ia[u], 1, 2 * nvec, status) &&
+                            in_range(ia[u] + 16, 1, 2 * nvec, status);
             vd[u] = in ? __ldg(dh + i) : make_uint4(0, 0, 0, 0);
             va[u] = in ? __ldg(ab + ia[u]) : make_uint4(0, 0, 0, 0);
             vb[u] = in ? __ldg(ab + ia[u] + 16) : make_uint4(0, 0, 0, 0);
@@ -319,7 +322,7 @@ swiglu_bwd_amax_kernel(const uint4 *__restrict__ dh, const uint4 *__restrict__ a
         }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-            if (base + u * S < nvec) {
+            if (base + u * S < nvec && in_range(ia[u] + 16, 1, 2 * nvec, status)) {
                 dab[ia[u]] = ga[u];
                 dab[ia[u] + 16] = gb[u];
                 m2 = max_u16x2(max_u16x2(m2, ga[u]), gb[u]);
@@ -349,7 +352,8 @@ swiglu_bwd_amax_kernel(const uint4 *__restrict__ dh, const uint4 *__restrict__ a
 // PRMT and writes four 16-byte column segments of q^T (8 consecutive threads
 // write 128 contiguous bytes of one column).
 __device__ __forceinline__ void transpose_out(const uint8_t *tile, uint8_t *__restrict__ qt,
-                                              int64_t rows, int64_t r0, int64_t c0, int t)
+                                              int64_t rows, int64_t cols, int64_t r0, int64_t c0,
+                                              int t, unsigned *status)
 {
     const int rs = t & 7;          // 16-row segment
     const int cg = t >> 3;         // 4-column group (0..31)
@@ -375,8 +379,10 @@ __device__ __forceinline__ void transpose_out(const uint8_t *tile, uint8_t *__re
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        uint8_t *dst = qt + (c0 + cg * 4 + j) * rows + r0 + rs * 16;
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
+        const int64_t o = (c0 + cg * 4 + j) * rows + r0 + rs * 16;
+        if (in_range(o, 16, rows * cols, status))
+            *reinterpret_cast<uint4 *>(qt + o) =
+                make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
     }
 }
 
@@ -385,7 +391,8 @@ __global__ void __launch_bounds__(kCastThreads)
 cast_transpose_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
                       const float *__restrict__ amax, const unsigned *__restrict__ partials,
                       int nparts, float *__restrict__ amax_out, float *__restrict__ scale_out,
-                      uint8_t *__restrict__ q, uint8_t *__restrict__ qt, int vector_ok)
+                      uint8_t *__restrict__ q, uint8_t *__restrict__ qt, int vector_ok,
+                      unsigned *__restrict__ status)
 {
     __shared__ __align__(16) uint8_t tile[kTile * kTile];
     griddep_wait();
@@ -414,26 +421,29 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols
             for (int it = 0; it < 4; ++it) {
                 const int k = t + it * kCastThreads;  // 16-element chunk id in the tile
                 const int row = k >> 3, ch = k & 7;
-                const uint16_t *src = x + (r0 + row) * cols + c0 + ch * 16;
-                const uint4 v0 = __ldg(reinterpret_cast<const uint4 *>(src));
-                const uint4 v1 = __ldg(reinterpret_cast<const uint4 *>(src + 8));
+                const int64_t o = (r0 + row) * cols + c0 + ch * 16;
+                const bool ok = in_range(o, 16, rows * cols, status);
+                const uint16_t *src = x + o;
+                const uint4 v0 = ok ? __ldg(reinterpret_cast<const uint4 *>(src)) : make_uint4(0, 0, 0, 0);
+                const uint4 v1 = ok ? __ldg(reinterpret_cast<const uint4 *>(src + 8)) : make_uint4(0, 0, 0, 0);
                 const uint2 a = cvt8<FMT>(v0, s), b = cvt8<FMT>(v1, s);
                 const uint4 codes = make_uint4(a.x, a.y, b.x, b.y);
-                if (q != nullptr)
-                    *reinterpret_cast<uint4 *>(q + (r0 + row) * cols + c0 + ch * 16) = codes;
+                if (q != nullptr && ok)
+                    *reinterpret_cast<uint4 *>(q + o) = codes;
                 const int pch = ch ^ ((row >> 4) & 7);
                 *reinterpret_cast<uint4 *>(tile + row * kTile + pch * 16) = codes;
             }
             if (qt != nullptr) {
                 __syncthreads();
-                transpose_out(tile, qt, rows, r0, c0, t);
+                transpose_out(tile, qt, rows, cols, r0, c0, t, status);
             }
             __syncthreads();
         } else {
             // ragged or unaligned tile: one element at a time
             for (int e = t; e < kTile * kTile; e += kCastThreads) {
                 const int64_t r = r0 + e / kTile, c = c0 + e % kTile;
-                if (r < rows && c < cols) {
+                if (r < rows && c < cols && in_range(r * cols + c, 1, rows * cols, status) &&
+                    in_range(c * rows + r, 1, rows * cols, status)) {
                     const uint8_t b = cvt1<FMT>(x[r * cols + c], s);
                     if (q != nullptr)
                         q[r * cols + c] = b;
@@ -568,14 +578,15 @@ cast_transpose_tma_kernel(const __grid_constant__ CUtensorMap tmap0,
             const int row = idx >> 4, c8 = idx & 15;
             const uint4 v = *reinterpret_cast<const uint4 *>(src + row * (kTile * 2) + c8 * 16);
             const uint2 codes = cvt8<FMT>(v, s);
-            if (q != nullptr)
-                *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + c8 * 8) = codes;
+            const int64_t o = (r0 + row) * cols + c0 + c8 * 8;
+            if (q != nullptr && in_range(o, 8, rows * cols, status))
+                *reinterpret_cast<uint2 *>(q + o) = codes;
             const int pch = (c8 >> 1) ^ ((row >> 4) & 7);
             *reinterpret_cast<uint2 *>(tile + row * kTile + pch * 16 + (c8 & 1) * 8) = codes;
         }
         __syncthreads();
         if (qt != nullptr)
-            transpose_out(tile, qt, rows, r0, c0, t);
+            transpose_out(tile, qt, rows, cols, r0, c0, t, status);
         __syncthreads();  // the input buffer and the parked tile are free again
     }
     if (k < nmine && t == 0) {
@@ -703,7 +714,7 @@ cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, con
     return launch_pdl(fmt == 1 ? cast_transpose_kernel<1> : cast_transpose_kernel<0>,
                       dim3(static_cast<unsigned>(blocks)), dim3(kCastThreads),
                       0, stream, static_cast<const uint16_t *>(x), rows, cols, amax, partials, nparts,
-                      amax_out, scale_out, q, q_t, vector_ok);
+                      amax_out, scale_out, q, q_t, vector_ok, dev.status);
 }
 
 cudaError_t launch_quantize_swiglu(const void *a, const void *b, void *h, int64_t rows,
@@ -793,6 +804,21 @@ cudaError_t launch_quantize_pair(const void *x0, int64_t rows0, int64_t cols0, c
     return launch_pdl(cast_transpose_tma_kernel<0, 2>, dim3(static_cast<unsigned>(blocks)),
                       dim3(kCastThreads), kTmaCastSmem, stream, m0, m1, s0, s1, dev.status,
                       wait_limit_ns());
+}
+
+namespace {
+// One thread asks in_range about an element past the end of a 1-element
+// buffer and touches no memory: the checked build records kStatusBounds.
+__global__ void bounds_selftest_kernel(unsigned *status) { (void)in_range(1, 1, 1, status); }
+} // namespace
+
+bool bounds_checked_build() { return kBoundsCheck; }
+
+cudaError_t launch_bounds_selftest(const DeviceInfo &dev, cudaStream_t stream)
+{
+    count_launch();
+    bounds_selftest_kernel<<<1, 1, 0, stream>>>(dev.status);
+    return cudaGetLastError();
 }
 
 } // namespace f8

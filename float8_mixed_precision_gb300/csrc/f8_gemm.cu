@@ -129,7 +129,8 @@ template <int BN>
 __device__ __forceinline__ void epilogue_rows(uint32_t taddr, int row0, int col_base, int M, int N,
                                               float inv, __nv_bfloat16 *__restrict__ c,
                                               const CUtensorMap *tma_c, bool tma_store,
-                                              uint8_t *stage, uint32_t &buf, int lane)
+                                              uint8_t *stage, uint32_t &buf, int lane,
+                                              unsigned *status)
 {
 #pragma unroll 1
     for (int j = 0; j < BN / kEpiCols; ++j) {
@@ -160,13 +161,16 @@ __device__ __forceinline__ void epilogue_rows(uint32_t taddr, int row0, int col_
             if (row < M) {
                 __nv_bfloat16 *dst = c + static_cast<int64_t>(row) * N + col0;
                 const bool vec = (N % 8) == 0 && col0 + kEpiCols <= N;
+                const int64_t o = static_cast<int64_t>(row) * N + col0;
+                const int64_t mn = static_cast<int64_t>(M) * N;
                 if (vec) {
 #pragma unroll
                     for (int q = 0; q < kEpiCols / 8; ++q)
-                        *reinterpret_cast<uint4 *>(dst + 8 * q) = pack8(&r[8 * q], inv);
+                        if (in_range(o + 8 * q, 8, mn, status))
+                            *reinterpret_cast<uint4 *>(dst + 8 * q) = pack8(&r[8 * q], inv);
                 } else {
                     for (int e = 0; e < kEpiCols; ++e)
-                        if (col0 + e < N)
+                        if (col0 + e < N && in_range(o + e, 1, mn, status))
                             dst[e] = __float2bfloat16_rn(__uint_as_float(r[e]) * inv);
                 }
             }
@@ -475,7 +479,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
                                   lane);
             else
                 epilogue_rows<BN>(taddr, row0, nb * BN, M, N, inv, c, &tma_c, tma_store != 0,
-                                  my_stage, buf, lane);
+                                  my_stage, buf, lane, status);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {

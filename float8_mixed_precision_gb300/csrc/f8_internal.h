@@ -166,6 +166,12 @@ cudaError_t launch_quantize_pair(const void *x0, int64_t rows0, int64_t cols0, c
                                  float *amax1, float *scale1, uint8_t *q1, uint8_t *qt1,
                                  const DeviceInfo &dev, cudaStream_t stream);
 
+// Whether this library was built with the device bounds checks
+// (-DF8_BOUNDS_CHECK), and a one-thread kernel that makes one such check
+// fail without touching memory (it sets kStatusBounds in a checked build).
+bool bounds_checked_build();
+cudaError_t launch_bounds_selftest(const DeviceInfo &dev, cudaStream_t stream);
+
 // One CTA waiting on an mbarrier that is never signalled (failure-path test).
 cudaError_t launch_wait_selftest(uint64_t limit_ns, const DeviceInfo &dev, cudaStream_t stream);
 

@@ -11,6 +11,29 @@ namespace f8 {
 // Bits of the per-device status word (host maps them to f8_status).
 constexpr unsigned kStatusNonfinite = 1u << 0;
 constexpr unsigned kStatusTimeout = 1u << 1;
+constexpr unsigned kStatusBounds = 1u << 2;
+
+// Bounds checks of the manual global-memory indexing, compiled in only with
+// -DF8_BOUNDS_CHECK (the checked build).  In that build an access of `len`
+// elements at element i of a buffer of n elements must satisfy
+// 0 <= i and i + len <= n; otherwise the access is skipped and the status
+// word gets kStatusBounds (reported as F8_ERR_BOUNDS).  Release builds
+// compile every check to `true`.
+#if defined(F8_BOUNDS_CHECK)
+constexpr bool kBoundsCheck = true;
+#else
+constexpr bool kBoundsCheck = false;
+#endif
+
+__device__ __forceinline__ bool in_range(int64_t i, int64_t len, int64_t n, unsigned *status)
+{
+    if (!kBoundsCheck)
+        return true;
+    if (i >= 0 && len >= 0 && i + len <= n)
+        return true;
+    atomicOr(status, kStatusBounds);
+    return false;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {

@@ -34,7 +34,8 @@
  *     Pointers to bf16 or E4M3 tensors must be 16-byte aligned; pointers to
  *     fp32 scalars 4-byte aligned.
  *   - Errors found on the device (a non-finite amax, a wait that ran past its
- *     time limit) are recorded in a per-device status word;
+ *     time limit, in the checked build an index outside its buffer) are
+ *     recorded in a per-device status word;
  *     f8_last_device_status() reports and clears it.
  */
 #ifndef F8_H_
@@ -55,7 +56,8 @@ typedef enum {
     F8_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed           */
     F8_ERR_TIMEOUT = 5,     /* a device-side wait exceeded its time limit     */
     F8_ERR_NONFINITE = 6,   /* an amax input held +-inf or NaN                */
-    F8_ERR_UNSUPPORTED = 7  /* no sm_100-family device / driver entry point   */
+    F8_ERR_UNSUPPORTED = 7, /* no sm_100-family device / driver entry point   */
+    F8_ERR_BOUNDS = 8       /* checked build only: an index left its buffer   */
 } f8_status;
 
 /*
@@ -358,10 +360,23 @@ f8_status f8_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int64_t M
 unsigned long long f8_kernel_launches(void);
 
 /*
+ * The checked build (compiled with -DF8_BOUNDS_CHECK) tests every manually
+ * indexed global load and store of the amax, cast and SwiGLU kernels and of
+ * the GEMM's direct-store epilogue against its buffer before making it; an
+ * index outside the buffer skips the access and sets F8_ERR_BOUNDS in the
+ * device status word (in place of a sanitizer, which this build does not
+ * rely on).  f8_selftest_bounds launches one thread that makes one such
+ * check fail without touching memory: in the checked build it returns F8_OK
+ * and the next f8_last_device_status() gives F8_ERR_BOUNDS; in a release
+ * build it launches nothing and returns F8_ERR_UNSUPPORTED.
+ */
+f8_status f8_selftest_bounds(void *stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
- * word.  Returns F8_OK, F8_ERR_NONFINITE or F8_ERR_TIMEOUT (the first set
- * bit in that order of severity: TIMEOUT wins), or F8_ERR_CUDA if the
- * synchronisation itself failed.
+ * word.  Returns F8_OK, F8_ERR_NONFINITE, F8_ERR_TIMEOUT or F8_ERR_BOUNDS
+ * (the most severe bit set, BOUNDS over TIMEOUT over NONFINITE), or
+ * F8_ERR_CUDA if the synchronisation itself failed.
  */
 f8_status f8_last_device_status(void *stream);
 

@@ -68,6 +68,7 @@ def test_every_wrapper_marshals(rec):
     binding.f8_linear_bwd_w13_swiglu(_bf(M, F), _bf(M, 2 * F), saved13)
     binding.f8_quantize_swiglu_bwd(_bf(M, F), _bf(M, 2 * F))
     binding.f8_selftest_wait_timeout(1000)
+    binding.f8_selftest_bounds()
     wrapped = {n for n in binding.EXPORTS if hasattr(binding, n)}
     called = set(rec.calls)
     assert wrapped - {"f8_status_string", "f8_last_device_status", "f8_set_wait_limit_ns",
