@@ -214,3 +214,52 @@ def test_attention_workload_every_output(f8, c, l):
     check_close(y, oracle.gemm(qx["q"], qw["q"], qx["scale"], qw["scale"]), what="Y")
     check_close(dx, oracle.gemm(qdy["q"], qw["qt"], qdy["scale"], qw["scale"]), what="dX")
     check_close(dw, oracle.gemm(qdy["qt"], qx["qt"], qdy["scale"], qx["scale"]), what="dW")
+
+
+def test_two_streams_share_no_state(f8):
+    """Two linears of different shapes run forward and backward at the same
+    time on two streams, each with its own workspace and outputs (the calls
+    interleaved on the host).  Every output is bit-identical to running them
+    one after the other: the library keeps no per-call state between calls
+    other than the device status word."""
+    shapes = [(2048, 1536, 1024, 21), (1024, 2048, 512, 22)]
+    bufs = []
+    for M, N, K, seed in shapes:
+        d = wl.custom_linear(M, K, N, seed=seed, dy_std=0.5)
+        bufs.append({"x": d["x"].to(DEV), "w": d["w"].to(DEV), "dy": d["dy"].to(DEV),
+                     "y": torch.empty((M, N), dtype=torch.bfloat16, device=DEV),
+                     "dx": torch.empty((M, K), dtype=torch.bfloat16, device=DEV),
+                     "dw": torch.empty((N, K), dtype=torch.bfloat16, device=DEV),
+                     "saved": f8.LinearSaved.empty(M, N, K, DEV), "ws": f8.workspace(M, N, K, DEV)})
+
+    def fwd(b, stream=None):
+        f8.f8_linear_fwd(b["x"], b["w"], b["y"], b["saved"], b["ws"], stream=stream)
+
+    def bwd(b, stream=None):
+        f8.f8_linear_bwd(b["dy"], b["saved"], dx=b["dx"], dw=b["dw"], ws=b["ws"], stream=stream)
+
+    def outs(b):
+        return [t.clone() for t in (b["y"], b["dx"], b["dw"], b["saved"].x_t, b["saved"].w_t,
+                                    b["saved"].scalars)]
+
+    for b in bufs:
+        fwd(b)
+        bwd(b)
+    torch.cuda.synchronize()
+    ref = [outs(b) for b in bufs]
+    for b in bufs:
+        for t in (b["y"], b["dx"], b["dw"]):
+            t.zero_()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for _ in range(3):
+        fwd(bufs[0], streams[0])
+        fwd(bufs[1], streams[1])
+        bwd(bufs[0], streams[0])
+        bwd(bufs[1], streams[1])
+    torch.cuda.synchronize()
+    assert f8.f8_last_device_status() == 0
+    for b, r in zip(bufs, ref):
+        for got, want in zip(outs(b), r):
+            assert torch.equal(got.view(torch.uint8), want.view(torch.uint8))
