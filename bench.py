@@ -264,7 +264,7 @@ class FfnIn8(Linear8):
 
     def bwd_from_dh(self, f8, dh):
         f8.f8_linear_bwd_w13_swiglu(dh, self.y, self.saved, dab=self.dy, dx=self.dx, dw=self.dw,
-                                    ws=self.ws)
+                                    ws=self.ws, dy_fmt=self.dy_fmt)
 
     def bwd_from_dh_timed(self, f8, ev, dh):
         s = self.saved
@@ -272,9 +272,11 @@ class FfnIn8(Linear8):
         # reads dh, a, b (6 B per element of h) and writes d(AB) (4 B), then the cast
         ev("quantize", 10 * dh.numel() + 4 * self.dy.numel(),
            lambda: f8.f8_quantize_swiglu_bwd(dh, self.y, self.dy, self.dys[0], self.dys[1], self.dyq,
-                                             self.dyt, self.qws))
-        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyq, s.w_t, self.dys[1], s.scale_w, self.dx))
-        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyt, s.x_t, self.dys[1], s.scale_x, self.dw))
+                                             self.dyt, self.qws, fmt=self.dy_fmt))
+        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyq, s.w_t, self.dys[1], s.scale_w, self.dx,
+                                                     fmt_a=self.dy_fmt))
+        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyt, s.x_t, self.dys[1], s.scale_x, self.dw,
+                                                     fmt_a=self.dy_fmt))
 
     def step_timed(self, f8, ev):
         s, s2 = self.saved, self.next.saved

@@ -113,9 +113,9 @@ def lib() -> ctypes.CDLL:
                                                vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         L.f8_linear_fwd_w13_swiglu.restype = st
         L.f8_linear_bwd_w13_swiglu.argtypes = [vp, vp, ctypes.POINTER(_Saved), i64, i64, i64, vp,
-                                               vp, vp, vp, ctypes.c_size_t, vp]
+                                               ctypes.c_int, vp, vp, vp, ctypes.c_size_t, vp]
         L.f8_linear_bwd_w13_swiglu.restype = st
-        L.f8_quantize_swiglu_bwd.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, vp, vp,
+        L.f8_quantize_swiglu_bwd.argtypes = [vp, vp, i64, i64, vp, ctypes.c_int, vp, vp, vp, vp, vp,
                                              ctypes.c_size_t, vp]
         L.f8_quantize_swiglu_bwd.restype = st
         L.f8_selftest_bounds.argtypes = [vp]
@@ -436,9 +436,10 @@ def f8_linear_fwd_w13_swiglu(x: torch.Tensor, w13: torch.Tensor, ab: torch.Tenso
 def f8_linear_bwd_w13_swiglu(dh: torch.Tensor, ab: torch.Tensor, saved: LinearSaved,
                              dab: torch.Tensor | None = None, dx: torch.Tensor | None = None,
                              dw: torch.Tensor | None = None, ws: torch.Tensor | None = None,
-                             want_dx: bool = True, want_dw: bool = True, stream=None):
-    """d(AB) from dh and the forward's AB, then dX, dW13 of the w1+w3 group;
-    returns (dx, dw, dab)."""
+                             want_dx: bool = True, want_dw: bool = True, dy_fmt: int = F8_E4M3,
+                             stream=None):
+    """d(AB) from dh and the forward's AB (quantised in format dy_fmt), then
+    dX, dW13 of the w1+w3 group; returns (dx, dw, dab)."""
     M, F = dh.shape
     K = saved.x_t.shape[0]
     if ab.shape != (M, 2 * F):
@@ -452,15 +453,16 @@ def f8_linear_bwd_w13_swiglu(dh: torch.Tensor, ab: torch.Tensor, saved: LinearSa
     ws = workspace(M, 2 * F, K, dev) if ws is None else ws
     s = saved.c_struct()
     _check(lib().f8_linear_bwd_w13_swiglu(_ptr(dh), _ptr(ab), ctypes.byref(s), M, F, K, _ptr(dab),
-                                          _ptr(dx), _ptr(dw), _ptr(ws), ws.numel(),
+                                          int(dy_fmt), _ptr(dx), _ptr(dw), _ptr(ws), ws.numel(),
                                           _stream(stream)), "f8_linear_bwd_w13_swiglu")
     return dx, dw, dab
 
 
 def f8_quantize_swiglu_bwd(dh: torch.Tensor, ab: torch.Tensor, dab: torch.Tensor | None = None,
-                           amax_out=None, scale_out=None, q=None, q_t=None, ws=None, stream=None):
-    """d(AB) from dh and the forward's AB with its amax, then its E4M3 cast:
-    returns (q, q_t, scale, amax, dab)."""
+                           amax_out=None, scale_out=None, q=None, q_t=None, ws=None,
+                           fmt: int = F8_E4M3, stream=None):
+    """d(AB) from dh and the forward's AB with its amax, then its cast to
+    format fmt: returns (q, q_t, scale, amax, dab)."""
     M, F = dh.shape
     if ab.shape != (M, 2 * F):
         raise ValueError("ab must be [M, 2F] for dh [M, F]")
@@ -472,9 +474,10 @@ def f8_quantize_swiglu_bwd(dh: torch.Tensor, ab: torch.Tensor, dab: torch.Tensor
     q_t = torch.empty((2 * F, M), dtype=torch.uint8, device=dev) if q_t is None else q_t
     if ws is None:
         ws = torch.empty(f8_quantize_workspace_bytes(), dtype=torch.uint8, device=dev)
-    _check(lib().f8_quantize_swiglu_bwd(_ptr(dh), _ptr(ab), M, F, _ptr(dab), _ptr(amax_out),
-                                        _ptr(scale_out), _ptr(q), _ptr(q_t), _ptr(ws), ws.numel(),
-                                        _stream(stream)), "f8_quantize_swiglu_bwd")
+    _check(lib().f8_quantize_swiglu_bwd(_ptr(dh), _ptr(ab), M, F, _ptr(dab), int(fmt),
+                                        _ptr(amax_out), _ptr(scale_out), _ptr(q), _ptr(q_t),
+                                        _ptr(ws), ws.numel(), _stream(stream)),
+           "f8_quantize_swiglu_bwd")
     return q, q_t, scale_out, amax_out, dab
 
 

@@ -510,10 +510,11 @@ f8_status f8_linear_fwd_w13_swiglu(const void *x, const void *w13, int64_t M, in
 }
 
 f8_status f8_quantize_swiglu_bwd(const void *dh, const void *ab, int64_t M, int64_t F, void *dab,
-                                 float *amax_out, float *scale_out, uint8_t *q, uint8_t *q_t,
-                                 void *workspace, size_t workspace_bytes, void *stream)
+                                 f8_format fmt, float *amax_out, float *scale_out, uint8_t *q,
+                                 uint8_t *q_t, void *workspace, size_t workspace_bytes,
+                                 void *stream)
 {
-    if (M <= 0 || F <= 0)
+    if (M <= 0 || F <= 0 || (fmt != F8_E4M3 && fmt != F8_E5M2))
         return F8_ERR_INVALID;
     if (F % 128 || F > INT32_MAX / 4 || M > INT32_MAX / 2)
         return F8_ERR_SHAPE;
@@ -533,15 +534,15 @@ f8_status f8_quantize_swiglu_bwd(const void *dh, const void *ab, int64_t M, int6
     int np = 0;
     F8_TRY_CUDA(launch_swiglu_bwd_amax(dh, ab, dab, M, F, parts, &np, *dev, st));
     return from_cuda(launch_cast_transpose(dab, M, 2 * F, nullptr, parts, np, amax_out, scale_out, q,
-                                           q_t, F8_E4M3, *dev, st));
+                                           q_t, fmt, *dev, st));
 }
 
 f8_status f8_linear_bwd_w13_swiglu(const void *dh, const void *ab, const f8_linear_saved *saved,
-                                   int64_t M, int64_t F, int64_t K, void *dab, void *dx,
-                                   void *dw13, void *workspace, size_t workspace_bytes,
+                                   int64_t M, int64_t F, int64_t K, void *dab, f8_format fmt_dab,
+                                   void *dx, void *dw13, void *workspace, size_t workspace_bytes,
                                    void *stream)
 {
-    if (M <= 0 || F <= 0 || K <= 0)
+    if (M <= 0 || F <= 0 || K <= 0 || (fmt_dab != F8_E4M3 && fmt_dab != F8_E5M2))
         return F8_ERR_INVALID;
     if (F % 128 || F > INT32_MAX / 4)
         return F8_ERR_SHAPE;
@@ -562,14 +563,14 @@ f8_status f8_linear_bwd_w13_swiglu(const void *dh, const void *ab, const f8_line
     int np = 0;
     F8_TRY_CUDA(launch_swiglu_bwd_amax(dh, ab, dab, M, F, bw.parts_dy, &np, *dev, st));
     F8_TRY_CUDA(launch_cast_transpose(dab, M, N, nullptr, bw.parts_dy, np, bw.amax_dy, bw.scale_dy,
-                                      dx ? bw.dy_q : nullptr, dw13 ? bw.dy_t : nullptr, F8_E4M3,
+                                      dx ? bw.dy_q : nullptr, dw13 ? bw.dy_t : nullptr, fmt_dab,
                                       *dev, st));
     if (dx != nullptr)
         F8_TRY_CUDA(launch_gemm(bw.dy_q, saved->w_t, M, K, N, bw.scale_dy, saved->scale_w, dx, *dev,
-                                st));
+                                st, fmt_dab, F8_E4M3));
     if (dw13 != nullptr)
         F8_TRY_CUDA(launch_gemm(bw.dy_t, saved->x_t, N, K, M, bw.scale_dy, saved->scale_x, dw13,
-                                *dev, st));
+                                *dev, st, fmt_dab, F8_E4M3));
     return F8_OK;
 }
 

@@ -302,12 +302,14 @@ f8_status f8_linear_fwd_w13_swiglu(const void *x, const void *w13, int64_t M, in
  * f8_quantize does for a given tensor.
  *   dh:  device bf16 [M, F]; ab: device bf16 [M, 2F]; F % 128 == 0.
  *   dab: device bf16 [M, 2F] receiving d(AB).
+ *   fmt: F8_E4M3 or F8_E5M2 (as f8_quantize_fmt).
  *   amax_out, scale_out, q ([M, 2F]), q_t ([2F, M]), workspace
  *   (f8_quantize_workspace_bytes()): as for f8_quantize.
  */
 f8_status f8_quantize_swiglu_bwd(const void *dh, const void *ab, int64_t M, int64_t F, void *dab,
-                                 float *amax_out, float *scale_out, uint8_t *q, uint8_t *q_t,
-                                 void *workspace, size_t workspace_bytes, void *stream);
+                                 f8_format fmt, float *amax_out, float *scale_out, uint8_t *q,
+                                 uint8_t *q_t, void *workspace, size_t workspace_bytes,
+                                 void *stream);
 
 /*
  * The backward of f8_linear_fwd_w13_swiglu for the gradient dh of h (in a
@@ -323,14 +325,16 @@ f8_status f8_quantize_swiglu_bwd(const void *dh, const void *ab, int64_t M, int6
  *   ab:    device bf16 [M, 2F], the forward's AB.
  *   saved: the forward's saved tensors.
  *   dab:   device bf16 [M, 2F] receiving d(AB).
+ *   fmt_dab: F8_E4M3, or F8_E5M2 for the E5M2-gradient recipe (d(AB) cast
+ *          with scale 57344/amax; E5M2 x E4M3 GEMMs), as f8_linear_bwd_fmt.
  *   dx:    device bf16 [M, K] or NULL; dw13: device bf16 [2F, K] or NULL.
  *   workspace: f8_linear_workspace_bytes(M, 2F, K) bytes, 256-byte aligned.
  * All device pointers 16-byte aligned.  F8_ERR_SHAPE if F is not a positive
  * multiple of 128.
  */
 f8_status f8_linear_bwd_w13_swiglu(const void *dh, const void *ab, const f8_linear_saved *saved,
-                                   int64_t M, int64_t F, int64_t K, void *dab, void *dx,
-                                   void *dw13, void *workspace, size_t workspace_bytes,
+                                   int64_t M, int64_t F, int64_t K, void *dab, f8_format fmt_dab,
+                                   void *dx, void *dw13, void *workspace, size_t workspace_bytes,
                                    void *stream);
 
 /*

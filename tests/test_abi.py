@@ -141,8 +141,9 @@ def test_w13_swiglu_bwd_rejects_bad_arguments_on_host(L):
     s = _Saved(FAKE, FAKE, FAKE, FAKE + 4, FAKE + 8, FAKE + 12)
     f = L.f8_linear_bwd_w13_swiglu
     ws = 1 << 30
-    assert f(FAKE, FAKE, ctypes.byref(s), 256, 192, 64, FAKE, FAKE, FAKE, FAKE, ws, None) == 3
-    assert f(FAKE, FAKE, ctypes.byref(s), 256, 128, 64, None, FAKE, FAKE, FAKE, ws, None) == 1
-    assert f(FAKE, FAKE, None, 256, 128, 64, FAKE, FAKE, FAKE, FAKE, ws, None) == 1
-    assert f(FAKE, FAKE, ctypes.byref(s), 256, 128, 64, FAKE, FAKE, FAKE, FAKE, 10, None) == 1
-    assert f(FAKE_MIS, FAKE, ctypes.byref(s), 256, 128, 64, FAKE, FAKE, FAKE, FAKE, ws, None) == 2
+    assert f(FAKE, FAKE, ctypes.byref(s), 256, 192, 64, FAKE, 0, FAKE, FAKE, FAKE, ws, None) == 3
+    assert f(FAKE, FAKE, ctypes.byref(s), 256, 128, 64, None, 0, FAKE, FAKE, FAKE, ws, None) == 1
+    assert f(FAKE, FAKE, None, 256, 128, 64, FAKE, 0, FAKE, FAKE, FAKE, ws, None) == 1
+    assert f(FAKE, FAKE, ctypes.byref(s), 256, 128, 64, FAKE, 0, FAKE, FAKE, FAKE, 10, None) == 1
+    assert f(FAKE_MIS, FAKE, ctypes.byref(s), 256, 128, 64, FAKE, 0, FAKE, FAKE, FAKE, ws, None) == 2
+    assert f(FAKE, FAKE, ctypes.byref(s), 256, 128, 64, FAKE, 2, FAKE, FAKE, FAKE, ws, None) == 1

@@ -260,3 +260,28 @@ def test_quantize_swiglu_bwd_alone(f8):
     ref = oracle.quantize(ref_dab)
     assert amax.item() == float(ref["amax"]) and s.item() == float(ref["scale"])
     assert np.array_equal(q.cpu().numpy(), ref["q"]) and np.array_equal(qt.cpu().numpy(), ref["qt"])
+
+
+def test_w13_swiglu_bwd_e5m2(f8):
+    """The group's backward with d(AB) in E5M2 (scale 57344/amax, E5M2 x E4M3
+    GEMMs): d(AB) still bit-exact; q(d(AB)) and its scale bit-exact against
+    the oracle's E5M2 quantize; dX and dW13 within the GEMM bar against the
+    oracle's linear_bwd with dy_fmt = E5M2."""
+    M, F, K = 272, 256, 528
+    x, w1, w3 = _inputs(M, F, K, 41)
+    w13 = _interleave(w1, w3)
+    dh = (torch.randn((M, F), generator=torch.Generator().manual_seed(42)) * 0.01).to(torch.bfloat16)
+    ab, h, saved, h_q, h_t, scale_h, amax_h = f8.f8_linear_fwd_w13_swiglu(x.to(DEV), w13.to(DEV))
+    dx, dw, dab = f8.f8_linear_bwd_w13_swiglu(dh.to(DEV), ab, saved, dy_fmt=f8.F8_E5M2)
+    q, qt, s, amax, dab2 = f8.f8_quantize_swiglu_bwd(dh.to(DEV), ab, fmt=f8.F8_E5M2)
+    assert f8.f8_last_device_status() == 0
+    a_g, b_g = _split(ab)
+    dab_or = oracle.merge_ab(*oracle.swiglu_bwd(wl.bits(dh), a_g, b_g))
+    assert np.array_equal(wl.bits(dab.cpu()), dab_or) and np.array_equal(wl.bits(dab2.cpu()), dab_or)
+    qref = oracle.quantize(dab_or, oracle.E5M2)
+    assert s.item() == float(qref["scale"])
+    assert np.array_equal(q.cpu().numpy(), qref["q"]) and np.array_equal(qt.cpu().numpy(), qref["qt"])
+    fwd = oracle.linear_fwd(wl.bits(x), wl.bits(w13))
+    bwd = oracle.linear_bwd(dab_or, fwd, dy_fmt=oracle.E5M2)
+    check_close(dx, bwd["dx"], what="dX (E5M2 d(AB))")
+    check_close(dw, bwd["dw"], what="dW13 (E5M2 d(AB))")
