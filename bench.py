@@ -677,7 +677,7 @@ def host_link_gbs(device, s_in, s_out, nbytes=256 << 20, reps=5):
 def oracle_sample(config: int, lin_index: int, rows: int):
     """The oracle on a bounded sample of one linear: amax, scale and cast of X,
     W and dY in full, then ``rows`` output rows of each of the three GEMMs.
-    Returns (GEMM flops of the sampled rows, seconds)."""
+    Returns (GEMM flops of the sampled rows, seconds, seconds per phase)."""
     import numpy as np
 
     import oracle
@@ -690,26 +690,43 @@ def oracle_sample(config: int, lin_index: int, rows: int):
     M, N, K = lin.M, lin.N, lin.K
     r_m = np.sort(rng.choice(M, size=min(rows, M), replace=False))
     r_n = np.sort(rng.choice(N, size=min(rows, N), replace=False))
-    t = time.perf_counter()
-    qx = oracle.quantize(xb)
-    qw = oracle.quantize(wb)
-    qdy = oracle.quantize(dyb)
-    oracle.gemm_rows(qx["q"], qw["q"], qx["scale"], qw["scale"], r_m)          # Y rows
-    oracle.gemm_rows(qdy["q"], qw["qt"], qdy["scale"], qw["scale"], r_m)       # dX rows
-    oracle.gemm_rows(qdy["qt"], qx["qt"], qdy["scale"], qx["scale"], r_n)      # dW rows
-    sec = time.perf_counter() - t
+    t0 = time.perf_counter()
+    amaxes = [oracle.amax(b)[0] for b in (xb, wb, dyb)]
+    t1 = time.perf_counter()
+    scales = [oracle.scale(a) for a in amaxes]
+    (xq, xt), (wq, wt), (dyq, dyt) = [oracle.cast_transpose(b, sc)
+                                      for b, sc in zip((xb, wb, dyb), scales)]
+    t2 = time.perf_counter()
+    sx, sw, sdy = scales
+    oracle.gemm_rows(xq, wq, sx, sw, r_m)          # Y rows
+    oracle.gemm_rows(dyq, wt, sdy, sw, r_m)        # dX rows
+    oracle.gemm_rows(dyt, xt, sdy, sx, r_n)        # dW rows
+    t3 = time.perf_counter()
     flops = 2 * (len(r_m) * N * K + len(r_m) * K * N + len(r_n) * K * M)
-    return flops, sec
+    return flops, t3 - t0, {"amax": t1 - t0, "scale+cast_transpose": t2 - t1, "gemm": t3 - t2}
 
 
 def cpu_baseline(config: int, rows: int):
     import oracle
     from float8_mixed_precision_gb300 import workloads as wl
-    flops, sec = oracle_sample(config, 0, rows)
-    lin = wl.workload(config)[1][0]
+    flops, sec, phases = oracle_sample(config, 0, rows)
+    lins = wl.workload(config)[1]
+    lin = lins[0]
     rm, rn = min(rows, lin.M), min(rows, lin.N)
+    # the whole step on the same cores, from the measured rates: the GEMMs at
+    # the sample's GEMM rate, the quantisation at its measured bf16 bytes/s
+    gemm_rate = flops / phases["gemm"]
+    q_rate = 2 * (lin.M * lin.K + lin.N * lin.K + lin.M * lin.N) / (
+        phases["amax"] + phases["scale+cast_transpose"])
+    step_s = sum(l.flops / gemm_rate + 2 * (l.M * l.K + l.N * l.K + l.M * l.N) / q_rate
+                 for l in lins)
     return {"value": flops / sec / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
             "kind": "oracle", "seconds": sec,
+            "seconds_by_phase": phases,
+            "gemm_gflops": gemm_rate / 1e9,
+            "extrapolated_step_seconds": step_s,
+            "extrapolated_note": ("extrapolated: the whole workload step on these cores at the "
+                                  "sample's measured GEMM and quantisation rates"),
             "sample": (f"linear {lin.name} (M={lin.M}, K={lin.K}, N={lin.N}): amax, scale and "
                        f"cast of X, W, dY in full, then {rm} of {lin.M} output rows of Y and of "
                        f"dX and {rn} of {lin.N} rows of dW; value = GEMM flops of those rows / "
