@@ -715,15 +715,15 @@ def cpu_baseline(config: int, rows: int):
     rm, rn = min(rows, lin.M), min(rows, lin.N)
     # the whole step on the same cores, from the measured rates: the GEMMs at
     # the sample's GEMM rate, the quantisation at its measured bf16 bytes/s
-    gemm_rate = flops / phases["gemm"]
-    q_rate = 2 * (lin.M * lin.K + lin.N * lin.K + lin.M * lin.N) / (
-        phases["amax"] + phases["scale+cast_transpose"])
-    step_s = sum(l.flops / gemm_rate + 2 * (l.M * l.K + l.N * l.K + l.M * l.N) / q_rate
-                 for l in lins)
+    gemm_rate = flops / phases["gemm"] if flops > 0 and phases["gemm"] > 0 else None
+    q_s = phases["amax"] + phases["scale+cast_transpose"]
+    q_rate = 2 * (lin.M * lin.K + lin.N * lin.K + lin.M * lin.N) / q_s if q_s > 0 else None
+    step_s = (sum(l.flops / gemm_rate + 2 * (l.M * l.K + l.N * l.K + l.M * l.N) / q_rate
+                  for l in lins) if gemm_rate and q_rate else None)
     return {"value": flops / sec / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
             "kind": "oracle", "seconds": sec,
             "seconds_by_phase": phases,
-            "gemm_gflops": gemm_rate / 1e9,
+            "gemm_gflops": gemm_rate / 1e9 if gemm_rate else None,
             "extrapolated_step_seconds": step_s,
             "extrapolated_note": ("extrapolated: the whole workload step on these cores at the "
                                   "sample's measured GEMM and quantisation rates"),
