@@ -285,3 +285,54 @@ def test_w13_swiglu_bwd_e5m2(f8):
     bwd = oracle.linear_bwd(dab_or, fwd, dy_fmt=oracle.E5M2)
     check_close(dx, bwd["dx"], what="dX (E5M2 d(AB))")
     check_close(dw, bwd["dw"], what="dW13 (E5M2 d(AB))")
+
+
+def test_w13_swiglu_smallest_shape(f8):
+    """M = 16 rows (single-CTA kernel, one partial tile), F = 128, K = 16."""
+    M, F, K = 16, 128, 16
+    x, w1, w3 = _inputs(M, F, K, 51)
+    w13 = _interleave(w1, w3)
+    ab, h, saved, h_q, h_t, scale_h, amax_h = f8.f8_linear_fwd_w13_swiglu(x.to(DEV), w13.to(DEV))
+    dh = (torch.randn((M, F), generator=torch.Generator().manual_seed(52)) * 0.01).to(torch.bfloat16)
+    dx, dw, dab = f8.f8_linear_bwd_w13_swiglu(dh.to(DEV), ab, saved)
+    assert f8.f8_last_device_status() == 0
+    check_close(ab, oracle.linear_fwd(wl.bits(x), wl.bits(w13))["y"], what="AB")
+    _check_h_and_quant(f8, ab, h, h_q, h_t, scale_h, amax_h)
+    a_g, b_g = _split(ab)
+    assert np.array_equal(wl.bits(dab.cpu()), oracle.merge_ab(*oracle.swiglu_bwd(wl.bits(dh), a_g, b_g)))
+
+
+def test_w13_swiglu_bwd_flags_nonfinite_dh(f8):
+    """An infinite dh makes d(AB) non-finite: the pass still writes every
+    finite element bit-exact and the status reads F8_ERR_NONFINITE."""
+    M, F, K = 256, 128, 64
+    x, w1, w3 = _inputs(M, F, K, 61)
+    ab, h, saved, *_ = f8.f8_linear_fwd_w13_swiglu(x.to(DEV), _interleave(w1, w3).to(DEV))
+    assert f8.f8_last_device_status() == 0
+    dh = (torch.randn((M, F), generator=torch.Generator().manual_seed(62)) * 0.01).to(torch.bfloat16)
+    dh[5, 17] = float("inf")
+    _, _, dab = f8.f8_linear_bwd_w13_swiglu(dh.to(DEV), ab, saved)
+    assert f8.f8_last_device_status() == f8.binding.F8_ERR_NONFINITE
+    a_g, b_g = _split(ab)
+    ref = oracle.merge_ab(*oracle.swiglu_bwd(wl.bits(dh), a_g, b_g)).ravel()
+    got = wl.bits(dab.cpu()).ravel()
+    finite = (ref & 0x7FFF) < 0x7F80
+    assert np.array_equal(got[finite], ref[finite])
+    assert np.array_equal((got & 0x7FFF) >= 0x7F80, ~finite)
+
+
+@pytest.mark.parametrize("want", ["dx", "dw"])
+def test_w13_swiglu_bwd_one_output(f8, want):
+    """dX only or dW13 only: the one asked for equals the full backward's."""
+    M, F, K = 256, 256, 128
+    x, w1, w3 = _inputs(M, F, K, 71)
+    ab, h, saved, *_ = f8.f8_linear_fwd_w13_swiglu(x.to(DEV), _interleave(w1, w3).to(DEV))
+    dh = (torch.randn((M, F), generator=torch.Generator().manual_seed(72)) * 0.01).to(torch.bfloat16)
+    dx, dw, _ = f8.f8_linear_bwd_w13_swiglu(dh.to(DEV), ab, saved)
+    dx1, dw1, _ = f8.f8_linear_bwd_w13_swiglu(dh.to(DEV), ab, saved, want_dx=(want == "dx"),
+                                              want_dw=(want == "dw"))
+    assert f8.f8_last_device_status() == 0
+    if want == "dx":
+        assert dw1 is None and torch.equal(dx1.view(torch.int16), dx.view(torch.int16))
+    else:
+        assert dx1 is None and torch.equal(dw1.view(torch.int16), dw.view(torch.int16))
