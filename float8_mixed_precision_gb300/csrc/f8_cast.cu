@@ -1,24 +1,34 @@
-// amax reduction and fused scale + cast + transpose (bf16 -> E4M3), the two
-// HBM-bound steps of dynamic tensorwise scaling.
+// The HBM-bound steps of dynamic tensorwise scaling: amax, and the fused
+// scale + cast + transpose (bf16 -> E4M3 or E5M2); also the SwiGLU passes
+// that produce a tensor together with its amax.
 //
-// amax: every thread streams 16-byte vectors of 8 bf16 values with eight
-// independent (predicated) loads in flight, also in the last round, keeps the maximum of the magnitude bits
-// (bits & 0x7FFF: for non-negative IEEE values the integer order is the
-// numeric order, and inf/NaN sort above every finite value), reduces through
-// redux.sync within the warp and shared memory within the block, and folds
-// the block result into the output with one atomicMax on the fp32 bit
-// pattern (valid because the value is non-negative).  Inside a linear the
-// kernel instead writes one partial maximum per block (no output to zero
-// first) and the cast kernel reduces the partials in its prologue.
+// amax_kernel: every thread streams 16-byte vectors of 8 bf16 values with
+// eight independent (predicated) loads in flight, also in the last round,
+// and keeps the maximum of the magnitude bits (bits & 0x7FFF: for
+// non-negative IEEE values the integer order is the numeric order, and
+// inf/NaN sort above every finite value).  It reduces through redux.sync
+// within the warp and shared memory within the block, then either folds the
+// block result into the output with one atomicMax on the fp32 bit pattern,
+// or (inside a linear) writes one partial maximum per block, so that no
+// output has to be zeroed first; the cast kernel reduces the partials in its
+// prologue.  amax_pair_kernel does the same for two tensors in one launch,
+// its blocks split between them in proportion to their sizes.
 //
-// cast_transpose: a CTA owns a 128 x 128 tile.  Phase 1 reads it with 16-byte
-// loads (each thread 16 consecutive bf16 of one row), scales in fp32,
-// converts with the hardware's saturating RNE E4M3 (or E5M2) conversion, writes the
+// cast_transpose_kernel: a CTA owns a 128 x 128 tile.  Phase 1 reads it with
+// 16-byte loads (each thread 16 consecutive bf16 of one row), scales in
+// fp32, converts with the hardware's saturating RNE conversion, writes the
 // row-major codes with 16-byte stores and parks them in a 16 KB shared tile
-// whose 16-byte chunks are XOR-swizzled by (row / 16) % 8.  Phase 2 gives each
-// thread a 16-row x 4-column block: 16 conflict-free 4-byte shared loads,
-// a byte transpose with PRMT, and four 16-byte stores of the column-major
-// copy (8 consecutive threads write 128 contiguous bytes of one column).
+// whose 16-byte chunks are XOR-swizzled by (row / 16) % 8.  Phase 2 gives
+// each thread a 16-row x 4-column block: 16 conflict-free 4-byte shared
+// loads, a byte transpose with PRMT, and four 16-byte stores of the
+// column-major copy (8 consecutive threads write 128 contiguous bytes of one
+// column).  cast_transpose_tma_kernel does the same with the bf16 tiles
+// brought in by TMA through a 3-stage ring, for one or two tensors whose
+// sides are multiples of 128; the register kernel takes the other shapes.
+//
+// swiglu_amax_kernel / swiglu_bwd_amax_kernel: h = silu(a) b, and the
+// gradient d(AB) of the w1+w3 group, each produced in one pass that also
+// writes one partial maximum per CTA for the cast that follows.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>

@@ -124,12 +124,6 @@ __device__ __forceinline__ uint32_t fold_abs(uint32_t m, uint4 a)
 
 __device__ __forceinline__ bool small87(uint32_t m) { return __vcmpgtu2(m, 0x42AE42AEu) == 0; }
 
-// Eight elements with their own gate.
-__device__ __forceinline__ uint4 swiglu_x8(uint4 a, uint4 b)
-{
-    return small87(fold_abs(0u, a)) ? swiglu8<false>(a, b) : swiglu8<true>(a, b);
-}
-
 // The gradient of swiglu_x2's h for two packed bf16 lanes of the upstream
 // gradient dh: db = bf16(dh s) with s = a sigma, and da = bf16((dh b) ds)
 // with ds = sigma fma(a, 1 - sigma, 1) = silu'(a); sigma as in the forward.
