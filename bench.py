@@ -506,13 +506,13 @@ def run_ours(args, world, rank, local):
 
 def kernel_bench(f8, layers, device, stream, iters=50):
     """Each kernel timed alone on the workload's tensors, L2 flushed before
-    every launch (a 512 MB fill, then a 256 MB read so that the L2 holds
+    every launch (a 1 GiB fill, then a 256 MB read so that the L2 holds
     clean lines and the timed kernel pays no write-back for the flush), CUDA
     events around the launch only.
     amax: 2 B/elem read; cast_transpose: 2 B/elem read + 2 x 1 B/elem
     written; GEMM: 2 M N K flops.  f8_amax includes its 4-byte memset."""
     import torch
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+    flush = torch.empty(1024 * 1024 * 1024, dtype=torch.uint8, device=device)
     clean = torch.ones(256 * 1024 * 1024, dtype=torch.uint8, device=device)
     peaks = load_peaks()
     fp8_burst = peaks["bf16_tflops"] * FP8_PER_BF16
