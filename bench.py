@@ -54,13 +54,13 @@ REF_BUDGET_S = 60.0   # timed seconds of the CPU reference arm
 # DRAM bytes (read + write) of the 12 GEMM launches of one attention fwd+bwd
 # step, from one ncu capture (profiles/gemm_traffic_attn8b.md), valid for the
 # GEMM sources whose hash is given; reported as null once they change.
-GEMM_TRAFFIC = {"workload": 2, "bytes_per_step": 696834816, "sources_sha256_16": "2308a51fcb709b8b"}
+GEMM_TRAFFIC = {"workload": 2, "bytes_per_step": 761316864, "sources_sha256_16": "a205204bb5365e82"}
 
 
 def gemm_sources_hash() -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("f8_gemm.cu", "f8_ptx.cuh"):
+    for f in ("f8_gemm.cu", "f8_ptx.cuh", "f8_sched.h"):
         with open(os.path.join(ROOT, "float8_mixed_precision_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -229,10 +229,10 @@ class Linear8:
         ev("quantize", 4 * self.dy.numel(),
            lambda: f8.f8_quantize(self.dy, self.dys[0], self.dys[1], self.dyq, self.dyt, self.qws,
                                   fmt=self.dy_fmt))
-        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyq, s.w_t, self.dys[1], s.scale_w, self.dx,
-                                                     fmt_a=self.dy_fmt))
-        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyt, s.x_t, self.dys[1], s.scale_x, self.dw,
-                                                     fmt_a=self.dy_fmt))
+        # dgrad and wgrad in one launch, as f8_linear_bwd runs them
+        ev("gemm", 4 * M * N * K, lambda: f8.f8_gemm_grouped(
+            [(self.dyq, s.w_t, self.dys[1], s.scale_w, self.dx, self.dy_fmt),
+             (self.dyt, s.x_t, self.dys[1], s.scale_x, self.dw, self.dy_fmt)]))
 
 
 class FfnIn8(Linear8):
@@ -273,10 +273,10 @@ class FfnIn8(Linear8):
         ev("quantize", 10 * dh.numel() + 4 * self.dy.numel(),
            lambda: f8.f8_quantize_swiglu_bwd(dh, self.y, self.dy, self.dys[0], self.dys[1], self.dyq,
                                              self.dyt, self.qws, fmt=self.dy_fmt))
-        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyq, s.w_t, self.dys[1], s.scale_w, self.dx,
-                                                     fmt_a=self.dy_fmt))
-        ev("gemm", 2 * M * N * K, lambda: f8.f8_gemm(self.dyt, s.x_t, self.dys[1], s.scale_x, self.dw,
-                                                     fmt_a=self.dy_fmt))
+        # dgrad and wgrad in one launch, as f8_linear_bwd runs them
+        ev("gemm", 4 * M * N * K, lambda: f8.f8_gemm_grouped(
+            [(self.dyq, s.w_t, self.dys[1], s.scale_w, self.dx, self.dy_fmt),
+             (self.dyt, s.x_t, self.dys[1], s.scale_x, self.dw, self.dy_fmt)]))
 
     def step_timed(self, f8, ev):
         s, s2 = self.saved, self.next.saved

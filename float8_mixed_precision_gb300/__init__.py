@@ -5,7 +5,7 @@ include/f8.h); ``binding`` marshals torch tensors into it.  ``workloads``
 draws the seeded synthetic inputs.
 """
 from .binding import (EXPORTS, F8_E4M3, F8_E5M2, F8Error, LinearSaved, f8_amax, f8_cast_transpose, f8_gemm,  # noqa: F401
-                      f8_last_device_status, f8_linear_bwd, f8_linear_fwd,
+                      f8_gemm_grouped, f8_last_device_status, f8_linear_bwd, f8_linear_fwd,
                       f8_linear_workspace_bytes, f8_quantize, f8_quantize_workspace_bytes,
                       f8_quantize_swiglu, f8_linear_fwd_swiglu, f8_linear_fwd_w13_swiglu,
                       f8_gemm_w13_swiglu, interleave_w13, split_ab, f8_linear_fwd_noalloc,

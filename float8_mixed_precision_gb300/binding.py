@@ -36,7 +36,8 @@ EXPORTS = ("f8_amax", "f8_cast_transpose", "f8_gemm", "f8_linear_workspace_bytes
            "f8_quantize", "f8_quantize_workspace_bytes", "f8_quantize_fmt", "f8_gemm_fmt",
            "f8_linear_bwd_fmt", "f8_quantize_swiglu", "f8_linear_fwd_swiglu",
            "f8_linear_fwd_w13_swiglu", "f8_gemm_w13_swiglu", "f8_linear_bwd_w13_swiglu",
-           "f8_quantize_swiglu_bwd", "f8_kernel_launches", "f8_selftest_bounds")
+           "f8_quantize_swiglu_bwd", "f8_kernel_launches", "f8_selftest_bounds",
+           "f8_gemm_grouped")
 
 F8_E4M3 = 0
 F8_E5M2 = 1
@@ -52,6 +53,13 @@ class _Saved(ctypes.Structure):
     _fields_ = [("x_t", ctypes.c_void_p), ("w_t", ctypes.c_void_p),
                 ("amax_x", ctypes.c_void_p), ("scale_x", ctypes.c_void_p),
                 ("amax_w", ctypes.c_void_p), ("scale_w", ctypes.c_void_p)]
+
+
+class _GemmProblem(ctypes.Structure):
+    _fields_ = [("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("M", ctypes.c_int64),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("scale_a", ctypes.c_void_p),
+                ("scale_b", ctypes.c_void_p), ("c", ctypes.c_void_p), ("fmt_a", ctypes.c_int),
+                ("fmt_b", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -126,6 +134,8 @@ def lib() -> ctypes.CDLL:
         L.f8_gemm_w13_swiglu.restype = st
         L.f8_linear_fwd_noalloc.argtypes = [vp, vp, i64, i64, i64, vp, ctypes.POINTER(_Saved), vp]
         L.f8_linear_fwd_noalloc.restype = st
+        L.f8_gemm_grouped.argtypes = [ctypes.POINTER(_GemmProblem), ctypes.c_int, vp]
+        L.f8_gemm_grouped.restype = st
         _lib = L
         return L
 
@@ -263,6 +273,30 @@ def f8_gemm(a: torch.Tensor, b: torch.Tensor, scale_a: torch.Tensor, scale_b: to
         _check(lib().f8_gemm_fmt(_ptr(a), int(fmt_a), _ptr(b), int(fmt_b), M, N, K, _ptr(scale_a),
                                  _ptr(scale_b), _ptr(out), _stream(stream)), "f8_gemm_fmt")
     return out
+
+
+def f8_gemm_grouped(problems, stream=None) -> list:
+    """One or two GEMMs in one launch (f8_gemm_grouped).  Each problem is
+    (a, b, scale_a, scale_b, out, fmt_a, fmt_b) as for f8_gemm (out, fmt_a
+    and fmt_b may be None / omitted); returns the outputs."""
+    arr = (_GemmProblem * len(problems))()
+    outs = []
+    for i, p in enumerate(problems):
+        a, b, sa, sb = p[:4]
+        out = p[4] if len(p) > 4 else None
+        fa = p[5] if len(p) > 5 else F8_E4M3
+        fb = p[6] if len(p) > 6 else F8_E4M3
+        M, K = a.shape
+        N, K2 = b.shape
+        if K != K2:
+            raise ValueError("contraction sizes differ")
+        if out is None:
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+        arr[i] = _GemmProblem(_ptr(a), _ptr(b), M, N, K, _ptr(sa), _ptr(sb), _ptr(out), int(fa),
+                              int(fb))
+        outs.append(out)
+    _check(lib().f8_gemm_grouped(arr, len(problems), _stream(stream)), "f8_gemm_grouped")
+    return outs
 
 
 def f8_linear_workspace_bytes(M: int, N: int, K: int) -> int:

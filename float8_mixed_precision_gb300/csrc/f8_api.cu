@@ -101,6 +101,26 @@ BwdWs bwd_ws(void *workspace, int64_t M, int64_t N)
     return w;
 }
 
+// The backward GEMMs of a linear from q(dY) (format fdy) and the saved
+// q(X)^T, q(W)^T; both in one launch when both are wanted:
+//   dX [M,K] = q(dY) [M,N] . (q(W)^T [K,N])^T
+//   dW [N,K] = q(dY)^T [N,M] . (q(X)^T [K,M])^T
+cudaError_t launch_bwd_gemms(const BwdWs &bw, const f8_linear_saved *saved, int64_t M, int64_t N,
+                             int64_t K, int fdy, void *dx, void *dw, const DeviceInfo &dev,
+                             cudaStream_t st)
+{
+    const GemmDesc gdx{bw.dy_q, saved->w_t, M, K, N, bw.scale_dy, saved->scale_w, dx,
+                       fdy, F8_E4M3};
+    const GemmDesc gdw{bw.dy_t, saved->x_t, N, K, M, bw.scale_dy, saved->scale_x, dw,
+                       fdy, F8_E4M3};
+    if (dx != nullptr && dw != nullptr)
+        return launch_gemm2(gdx, gdw, dev, st);
+    const GemmDesc &g = dx != nullptr ? gdx : gdw;
+    if (g.c == nullptr)
+        return cudaSuccess;
+    return launch_gemm(g.a, g.b, g.M, g.N, g.K, g.sa, g.sb, g.c, dev, st, g.fa, g.fb);
+}
+
 } // namespace
 
 const DeviceInfo *device_info()
@@ -325,6 +345,38 @@ f8_status f8_gemm_fmt(const uint8_t *a, f8_format fmt_a, const uint8_t *b, f8_fo
     return gemm_impl(a, fmt_a, b, fmt_b, M, N, K, scale_a, scale_b, c, stream);
 }
 
+f8_status f8_gemm_grouped(const f8_gemm_problem *problems, int count, void *stream)
+{
+    if (problems == nullptr || count < 1 || count > 2)
+        return F8_ERR_INVALID;
+    bool separate = count == 1;
+    for (int i = 0; i < count; ++i) {
+        const f8_gemm_problem &p = problems[i];
+        if ((p.fmt_a != F8_E4M3 && p.fmt_a != F8_E5M2) ||
+            (p.fmt_b != F8_E4M3 && p.fmt_b != F8_E5M2))
+            return F8_ERR_INVALID;
+        F8_TRY(check_gemm_args(p.a, p.b, p.M, p.N, p.K, p.scale_a, p.scale_b, p.c));
+        if (p.M == 0 || p.N == 0 || p.K == 0)
+            separate = true;
+    }
+    if (separate) {
+        for (int i = 0; i < count; ++i) {
+            const f8_gemm_problem &p = problems[i];
+            F8_TRY(gemm_impl(p.a, p.fmt_a, p.b, p.fmt_b, p.M, p.N, p.K, p.scale_a, p.scale_b, p.c,
+                             stream));
+        }
+        return F8_OK;
+    }
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    GemmDesc g[2];
+    for (int i = 0; i < 2; ++i) {
+        const f8_gemm_problem &p = problems[i];
+        g[i] = GemmDesc{p.a, p.b, p.M, p.N, p.K, p.scale_a, p.scale_b, p.c, p.fmt_a, p.fmt_b};
+    }
+    return from_cuda(launch_gemm2(g[0], g[1], *dev, static_cast<cudaStream_t>(stream)));
+}
+
 size_t f8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K)
 {
     if (M <= 0 || N <= 0 || K <= 0)
@@ -396,15 +448,7 @@ static f8_status linear_bwd_impl(const void *dy, int fdy, const f8_linear_saved 
     F8_TRY_CUDA(launch_amax_partials(dy, M * N, bw.parts_dy, &np, *dev, st));
     F8_TRY_CUDA(launch_cast_transpose(dy, M, N, nullptr, bw.parts_dy, np, bw.amax_dy, bw.scale_dy,
                                       dx ? bw.dy_q : nullptr, dw ? bw.dy_t : nullptr, fdy, *dev, st));
-    // dX [M,K] = q(dY) [M,N] . (q(W)^T [K,N])^T
-    if (dx != nullptr)
-        F8_TRY_CUDA(launch_gemm(bw.dy_q, saved->w_t, M, K, N, bw.scale_dy, saved->scale_w, dx, *dev, st,
-                                fdy, F8_E4M3));
-    // dW [N,K] = q(dY)^T [N,M] . (q(X)^T [K,M])^T
-    if (dw != nullptr)
-        F8_TRY_CUDA(launch_gemm(bw.dy_t, saved->x_t, N, K, M, bw.scale_dy, saved->scale_x, dw, *dev, st,
-                                fdy, F8_E4M3));
-    return F8_OK;
+    return from_cuda(launch_bwd_gemms(bw, saved, M, N, K, fdy, dx, dw, *dev, st));
 }
 
 f8_status f8_linear_bwd(const void *dy, const f8_linear_saved *saved, int64_t M, int64_t N,
@@ -565,13 +609,7 @@ f8_status f8_linear_bwd_w13_swiglu(const void *dh, const void *ab, const f8_line
     F8_TRY_CUDA(launch_cast_transpose(dab, M, N, nullptr, bw.parts_dy, np, bw.amax_dy, bw.scale_dy,
                                       dx ? bw.dy_q : nullptr, dw13 ? bw.dy_t : nullptr, fmt_dab,
                                       *dev, st));
-    if (dx != nullptr)
-        F8_TRY_CUDA(launch_gemm(bw.dy_q, saved->w_t, M, K, N, bw.scale_dy, saved->scale_w, dx, *dev,
-                                st, fmt_dab, F8_E4M3));
-    if (dw13 != nullptr)
-        F8_TRY_CUDA(launch_gemm(bw.dy_t, saved->x_t, N, K, M, bw.scale_dy, saved->scale_x, dw13,
-                                *dev, st, fmt_dab, F8_E4M3));
-    return F8_OK;
+    return from_cuda(launch_bwd_gemms(bw, saved, M, N, K, fmt_dab, dx, dw13, *dev, st));
 }
 
 f8_status f8_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int64_t M, int64_t F,

@@ -31,6 +31,10 @@
 //                 MMAs; its full[s] barriers count the bytes of both CTAs;
 //                 commits are multicast to the barriers of both CTAs; both
 //                 epilogues arrive on the even CTA's tempty barriers.
+// A launch runs one GEMM, or two independent ones (a linear's dgrad and
+// wgrad) whose tiles share the persistent CTAs under the static list
+// schedule of f8_sched.h: every role of every CTA derives the same tile
+// sequence from (CTA, i), so nothing is communicated.
 // Tiles are visited in groups of `group_m` M-blocks so that concurrently
 // running CTAs share operand tiles in L2.  M, N and K edges are zero-filled
 // by TMA loads and clipped by TMA stores (or masked on the direct-store path
@@ -49,6 +53,7 @@
 
 #include "f8_internal.h"
 #include "f8_ptx.cuh"
+#include "f8_sched.h"
 #include "f8_swiglu.cuh"
 
 namespace f8 {
@@ -151,8 +156,12 @@ __device__ __forceinline__ void epilogue_rows(uint32_t taddr, int row0, int col_
                     pack8(&r[8 * q], inv);
             fence_proxy_async_shared();
             __syncwarp();
-            if (lane == 0 && row0 < M && col0 < N) {
-                tma_store_2d(tma_c, b, col0, row0);
+            // one bulk group per step, empty where the box lies outside C,
+            // so that the read wait above always refers to this buffer's
+            // last store
+            if (lane == 0) {
+                if (row0 < M && col0 < N)
+                    tma_store_2d(tma_c, b, col0, row0);
                 bulk_commit_group();
             }
             buf ^= 1u;
@@ -247,14 +256,27 @@ __device__ __forceinline__ void epilogue_rows_glu(uint32_t taddr, int row0, int 
     }
 }
 
+// One GEMM problem of a launch.  A launch runs one problem, or two
+// independent ones (the dgrad and wgrad GEMMs of a linear's backward pass)
+// whose tiles share the persistent CTAs through the schedule of f8_sched.h.
+struct GemmProb {
+    __nv_bfloat16 *c;
+    const float *sa;
+    const float *sb;
+    int M, N;
+    int num_m, num_n, num_kb;
+    int tma_store;
+    uint32_t idesc;
+};
+
 template <int BN, int STAGES, bool PAIR, bool GLU>
 __global__ void __launch_bounds__(Cfg<BN, STAGES, PAIR, GLU>::kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
             const __grid_constant__ CUtensorMap tma_c, const __grid_constant__ CUtensorMap tma_h,
-            __nv_bfloat16 *__restrict__ c, int M, int N, int K, const float *__restrict__ sa,
-            const float *__restrict__ sb, unsigned *__restrict__ status, uint64_t limit_ns,
-            int group_m, int tma_store, uint32_t idesc, unsigned *__restrict__ hparts,
-            int hatomic)
+            const __grid_constant__ CUtensorMap tma_a1, const __grid_constant__ CUtensorMap tma_b1,
+            const __grid_constant__ CUtensorMap tma_c1, const GemmProb p0, const GemmProb p1,
+            const TileSched sched, unsigned *__restrict__ status, uint64_t limit_ns, int group_m,
+            unsigned *__restrict__ hparts, int hatomic)
 {
     using C = Cfg<BN, STAGES, PAIR, GLU>;
     extern __shared__ uint8_t smem_raw[];
@@ -277,11 +299,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
     const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const int nunits = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-    const int num_m = (M + C::kTileM - 1) / C::kTileM;
-    const int num_n = (N + BN - 1) / BN;
-    const int tiles = num_m * num_n;
-    const int num_kb = (K + kBK - 1) / kBK;
+    const bool two = sched.tiles1 > 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -300,10 +318,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tma_a);
         tma_prefetch_desc(&tma_b);
-        if (tma_store)
+        if (p0.tma_store)
             tma_prefetch_desc(&tma_c);
         if (GLU)
             tma_prefetch_desc(&tma_h);
+        if (two) {
+            tma_prefetch_desc(&tma_a1);
+            tma_prefetch_desc(&tma_b1);
+            if (p1.tma_store)
+                tma_prefetch_desc(&tma_c1);
+        }
     }
     if (warp == 1) {
         if (PAIR) {
@@ -333,9 +357,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
             bool stop = false;
-            for (int tile = unit; tile < tiles && !stop; tile += nunits) {
+            for (int i = 0; !stop; ++i) {
+                int tile = sched_tile(sched, unit, i);
+                if (tile < 0)
+                    break;
+                const bool second = tile >= sched.tiles0;
+                if (second)
+                    tile -= sched.tiles0;
+                const CUtensorMap *ma = second ? &tma_a1 : &tma_a;
+                const CUtensorMap *mb_ = second ? &tma_b1 : &tma_b;
+                const int num_kb = second ? p1.num_kb : p0.num_kb;
                 int mb, nb;
-                tile_coords(tile, num_m, num_n, group_m, mb, nb);
+                tile_coords(tile, second ? p1.num_m : p0.num_m, second ? p1.num_n : p0.num_n,
+                            group_m, mb, nb);
                 const int arow = mb * C::kTileM + static_cast<int>(rank) * kBM;
                 const int brow = nb * BN + static_cast<int>(rank) * C::kBRows;
                 for (int kb = 0; kb < num_kb; ++kb) {
@@ -350,12 +384,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
                         if (leader)
                             mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
                         const uint32_t fb = full_leader + 8u * stage;
-                        tma_load_2d_pair(sa_dst, &tma_a, fb, kb * kBK, arow);
-                        tma_load_2d_pair(sb_dst, &tma_b, fb, kb * kBK, brow);
+                        tma_load_2d_pair(sa_dst, ma, fb, kb * kBK, arow);
+                        tma_load_2d_pair(sb_dst, mb_, fb, kb * kBK, brow);
                     } else {
                         mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-                        tma_load_2d(sa_dst, &tma_a, &full[stage], kb * kBK, arow);
-                        tma_load_2d(sb_dst, &tma_b, &full[stage], kb * kBK, brow);
+                        tma_load_2d(sa_dst, ma, &full[stage], kb * kBK, arow);
+                        tma_load_2d(sb_dst, mb_, &full[stage], kb * kBK, brow);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -399,7 +433,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
             uint32_t stage = 0, phase = 0;
             bool stop = false;
             int local = 0;
-            for (int tile = unit; tile < tiles && !stop; tile += nunits, ++local) {
+            for (;; ++local) {
+                const int tile = sched_tile(sched, unit, local);
+                if (tile < 0)
+                    break;
+                const bool second = tile >= sched.tiles0;
+                const int num_kb = second ? p1.num_kb : p0.num_kb;
+                const uint32_t idesc = second ? p1.idesc : p0.idesc;
                 const uint32_t acc = local & 1;
                 const uint32_t aph = (local >> 1) & 1;
                 if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, limit_ns)) {
@@ -452,14 +492,22 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
     } else {
         // ---------------------------------------------------- epilogue
         const int quad = warp & 3;  // the TMEM lane quarter this warp may read
-        const float inv = static_cast<float>(1.0 / (static_cast<double>(*sa) *
-                                                     static_cast<double>(*sb)));
+        const float inv0 = static_cast<float>(1.0 / (static_cast<double>(*p0.sa) *
+                                                      static_cast<double>(*p0.sb)));
+        const float inv1 = two ? static_cast<float>(1.0 / (static_cast<double>(*p1.sa) *
+                                                            static_cast<double>(*p1.sb)))
+                               : inv0;
         uint8_t *my_stage = staging + (warp - 2) * C::kWarpStaging;
         uint32_t hmax2 = 0;
         const uint32_t tempty_leader = PAIR ? cluster_map(smem_addr(&tempty[0]), 0) : 0u;
         uint32_t buf = 0;
-        int local = 0;
-        for (int tile = unit; tile < tiles; tile += nunits, ++local) {
+        for (int local = 0;; ++local) {
+            int tile = sched_tile(sched, unit, local);
+            if (tile < 0)
+                break;
+            const bool second = tile >= sched.tiles0;
+            if (second)
+                tile -= sched.tiles0;
             const uint32_t acc = local & 1;
             const uint32_t aph = (local >> 1) & 1;
             bool ok = mbar_wait(&tfull[acc], aph, abort_flag, limit_ns);
@@ -471,15 +519,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
             }
             tc_fence_after_sync();
             int mb, nb;
-            tile_coords(tile, num_m, num_n, group_m, mb, nb);
+            tile_coords(tile, second ? p1.num_m : p0.num_m, second ? p1.num_n : p0.num_n, group_m,
+                        mb, nb);
             const int row0 = mb * C::kTileM + static_cast<int>(rank) * kBM + quad * 32;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
             if (GLU)
-                epilogue_rows_glu(taddr, row0, nb * BN, M, inv, &tma_c, &tma_h, my_stage, hmax2,
-                                  lane);
+                epilogue_rows_glu(taddr, row0, nb * BN, p0.M, inv0, &tma_c, &tma_h, my_stage,
+                                  hmax2, lane);
+            else if (second)
+                epilogue_rows<BN>(taddr, row0, nb * BN, p1.M, p1.N, inv1, p1.c, &tma_c1,
+                                  p1.tma_store != 0, my_stage, buf, lane, status);
             else
-                epilogue_rows<BN>(taddr, row0, nb * BN, M, N, inv, c, &tma_c, tma_store != 0,
-                                  my_stage, buf, lane, status);
+                epilogue_rows<BN>(taddr, row0, nb * BN, p0.M, p0.N, inv0, p0.c, &tma_c,
+                                  p0.tma_store != 0, my_stage, buf, lane, status);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
@@ -573,34 +625,89 @@ bool make_map(CUtensorMap *map, CUtensorMapDataType dtype, int esize, const void
     return r == CUDA_SUCCESS;
 }
 
+// Per-tile cost in the schedule of a two-problem launch, in K blocks: the
+// tile's K blocks plus a fixed share for handing over the accumulator and
+// draining it (measured: a short-K tile costs about four K blocks more than
+// its MMAs).
+constexpr int kTileOverheadKb = 4;
+
+// Smallest gain, in percent of the two launches' predicted time, for which
+// launch_gemm2 puts two GEMMs in one launch.  Measured: the attention
+// projections' backward GEMMs (predicted 6-8%) gain 3-10%; the FFN ones
+// (predicted 0-2%, power-capped) lose up to 2% when grouped.
+constexpr int kGroupMinGainPct = 4;
+
+// The schedule of one launch over `nprob` problems with tile_m x bn tiles
+// on at most max_units workers; `first` is the index of the problem dealt
+// round-robin (the one with the costlier tiles).
+struct SchedPlan {
+    TileSched s;
+    int first;
+};
+
+SchedPlan plan_schedule(const GemmDesc *probs, int nprob, int tile_m, int bn, int64_t max_units)
+{
+    int tiles[2] = {0, 0};
+    int cost[2] = {1, 1};
+    for (int i = 0; i < nprob; ++i) {
+        const GemmDesc &p = probs[i];
+        tiles[i] = static_cast<int>(((p.M + tile_m - 1) / tile_m) * ((p.N + bn - 1) / bn));
+        cost[i] = static_cast<int>((p.K + kBK - 1) / kBK) + kTileOverheadKb;
+    }
+    const int64_t total = static_cast<int64_t>(tiles[0]) + tiles[1];
+    const int units = static_cast<int>(total < max_units ? total : max_units);
+    const int first = (nprob == 2 && cost[1] > cost[0]) ? 1 : 0;
+    const int second = nprob == 2 ? 1 - first : first;
+    return SchedPlan{TileSched{units, tiles[first], nprob == 2 ? tiles[second] : 0, cost[first],
+                               cost[second]},
+                     first};
+}
+
 template <int BN, int STAGES, bool PAIR, bool GLU = false>
-cudaError_t run_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
-                     const float *sa, const float *sb, void *c, const DeviceInfo &dev,
-                     cudaStream_t stream, int fa, int fb, void *h = nullptr,
-                     unsigned *hparts = nullptr, int *nparts = nullptr, int hatomic = 0)
+cudaError_t run_gemm(const GemmDesc *probs, int nprob, const DeviceInfo &dev, cudaStream_t stream,
+                     void *h = nullptr, unsigned *hparts = nullptr, int *nparts = nullptr,
+                     int hatomic = 0)
 {
     using C = Cfg<BN, STAGES, PAIR, GLU>;
-    CUtensorMap ma, mb, mc, mh;
-    if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a, M, K, kBK, kBM) ||
-        !make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, N, K, kBK, C::kBRows))
-        return cudaErrorNotSupported;
-    // TMA stores need every C row to start on a 16-byte boundary
-    int tma_store;
-    if (GLU) {
-        // AB and h through 32-row x 32-column boxes in the 64-byte swizzle
-        tma_store = 1;
-        if (N % 256 != 0 ||
-            !make_tensor_map_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, M, N, kGluCols, 32,
-                                CU_TENSOR_MAP_SWIZZLE_64B) ||
-            !make_tensor_map_2d(&mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, M, N / 2, kGluCols,
-                                32, CU_TENSOR_MAP_SWIZZLE_64B))
+    CUtensorMap ma[2], mb[2], mc[2], mh;
+    GemmProb gp[2];
+    for (int i = 0; i < nprob; ++i) {
+        const GemmDesc &p = probs[i];
+        if (!make_map(&ma[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.a, p.M, p.K, kBK, kBM) ||
+            !make_map(&mb[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.b, p.N, p.K, kBK, C::kBRows))
             return cudaErrorNotSupported;
-    } else {
-        tma_store = (N % 8 == 0) &&
-                    make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, M, N, kEpiCols, 32);
-        if (!tma_store)
-            mc = ma;  // not used by the kernel
-        mh = ma;      // not used by the kernel
+        // TMA stores need every C row to start on a 16-byte boundary
+        int tma_store;
+        if (GLU) {
+            // AB and h through 32-row x 32-column boxes in the 64-byte swizzle
+            tma_store = 1;
+            if (p.N % 256 != 0 ||
+                !make_tensor_map_2d(&mc[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.c, p.M, p.N,
+                                    kGluCols, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+                !make_tensor_map_2d(&mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, p.M, p.N / 2,
+                                    kGluCols, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+                return cudaErrorNotSupported;
+        } else {
+            tma_store = (p.N % 8 == 0) && make_map(&mc[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                                   p.c, p.M, p.N, kEpiCols, 32);
+            if (!tma_store)
+                mc[i] = ma[i];  // not used by the kernel
+        }
+        const int num_m = static_cast<int>((p.M + C::kTileM - 1) / C::kTileM);
+        const int num_n = static_cast<int>((p.N + BN - 1) / BN);
+        const int num_kb = static_cast<int>((p.K + kBK - 1) / kBK);
+        gp[i] = GemmProb{static_cast<__nv_bfloat16 *>(p.c), p.sa, p.sb, static_cast<int>(p.M),
+                         static_cast<int>(p.N), num_m, num_n, num_kb, tma_store,
+                         idesc_f8_f32(C::kTileM, BN, static_cast<uint32_t>(p.fa),
+                                      static_cast<uint32_t>(p.fb))};
+    }
+    if (!GLU)
+        mh = ma[0];  // not used by the kernel
+    if (nprob == 1) {
+        ma[1] = ma[0];
+        mb[1] = mb[0];
+        mc[1] = mc[0];
+        gp[1] = gp[0];
     }
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
@@ -612,20 +719,20 @@ cudaError_t run_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, i
     });
     if (attr_err[dv] != cudaSuccess)
         return attr_err[dv];
-    const int64_t tiles = ((M + C::kTileM - 1) / C::kTileM) * ((N + BN - 1) / BN);
-    const int64_t max_units = PAIR ? dev.sm_count / 2 : dev.sm_count;
-    const int units = static_cast<int>(tiles < max_units ? tiles : max_units);
+    const SchedPlan plan =
+        plan_schedule(probs, nprob, C::kTileM, BN, PAIR ? dev.sm_count / 2 : dev.sm_count);
+    const TileSched &sched = plan.s;
+    const int units = sched.units;
+    const int first = plan.first;
+    const int second = nprob == 2 ? 1 - first : first;
     const int group_m = PAIR ? 8 : 16;
     if (nparts != nullptr)
         *nparts = (PAIR ? 2 : 1) * units;
     return launch_pdl_cluster(gemm_kernel<BN, STAGES, PAIR, GLU>, dim3((PAIR ? 2 : 1) * units),
-                              dim3(C::kThreads), C::kSmemBytes, stream, PAIR ? 2u : 1u, ma, mb, mc,
-                              mh, static_cast<__nv_bfloat16 *>(c), static_cast<int>(M),
-                              static_cast<int>(N), static_cast<int>(K), sa, sb, dev.status,
-                              wait_limit_ns(), group_m, tma_store,
-                              idesc_f8_f32(C::kTileM, BN, static_cast<uint32_t>(fa),
-                                           static_cast<uint32_t>(fb)),
-                              hparts, hatomic);
+                              dim3(C::kThreads), C::kSmemBytes, stream, PAIR ? 2u : 1u,
+                              ma[first], mb[first], mc[first], mh, ma[second], mb[second],
+                              mc[second], gp[first], gp[second], sched, dev.status,
+                              wait_limit_ns(), group_m, hparts, hatomic);
 }
 
 constexpr int kVariantSingle = 1;
@@ -666,9 +773,39 @@ cudaError_t launch_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N
                         const float *sa, const float *sb, void *c, const DeviceInfo &dev,
                         cudaStream_t stream, int fa, int fb)
 {
+    const GemmDesc g{a, b, M, N, K, sa, sb, c, fa, fb};
     if (gemm_variant(M, dev) == kVariantPair)
-        return run_gemm<256, 6, true>(a, b, M, N, K, sa, sb, c, dev, stream, fa, fb);
-    return run_gemm<256, 4, false>(a, b, M, N, K, sa, sb, c, dev, stream, fa, fb);
+        return run_gemm<256, 6, true>(&g, 1, dev, stream);
+    return run_gemm<256, 4, false>(&g, 1, dev, stream);
+}
+
+cudaError_t launch_gemm2(const GemmDesc &g0, const GemmDesc &g1, const DeviceInfo &dev,
+                         cudaStream_t stream)
+{
+    const int v = gemm_variant(g0.M, dev);
+    const int mode = gemm_group_mode();
+    bool group = mode != kGroupNever && v == gemm_variant(g1.M, dev);
+    if (group && mode == kGroupAuto) {
+        const int tile_m = v == kVariantPair ? 2 * kBM : kBM;
+        const int64_t max_units = v == kVariantPair ? dev.sm_count / 2 : dev.sm_count;
+        const GemmDesc both[2] = {g0, g1};
+        const int64_t grouped = sched_makespan(plan_schedule(both, 2, tile_m, 256, max_units).s);
+        const int64_t apart = sched_makespan(plan_schedule(&g0, 1, tile_m, 256, max_units).s) +
+                              sched_makespan(plan_schedule(&g1, 1, tile_m, 256, max_units).s);
+        group = grouped * 100 <= apart * (100 - kGroupMinGainPct);
+    }
+    if (!group) {
+        cudaError_t e = launch_gemm(g0.a, g0.b, g0.M, g0.N, g0.K, g0.sa, g0.sb, g0.c, dev, stream,
+                                    g0.fa, g0.fb);
+        if (e != cudaSuccess)
+            return e;
+        return launch_gemm(g1.a, g1.b, g1.M, g1.N, g1.K, g1.sa, g1.sb, g1.c, dev, stream, g1.fa,
+                           g1.fb);
+    }
+    const GemmDesc g[2] = {g0, g1};
+    if (v == kVariantPair)
+        return run_gemm<256, 6, true>(g, 2, dev, stream);
+    return run_gemm<256, 4, false>(g, 2, dev, stream);
 }
 
 cudaError_t launch_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int64_t M, int64_t F,
@@ -678,11 +815,11 @@ cudaError_t launch_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int
 {
     if (F % 128 != 0)
         return cudaErrorInvalidValue;
+    const GemmDesc g{x_q, w13_q, M, 2 * F, K, sx, sw, ab, 0, 0};
     if (gemm_variant(M, dev) == kVariantPair)
-        return run_gemm<256, 6, true, true>(x_q, w13_q, M, 2 * F, K, sx, sw, ab, dev, stream, 0, 0,
-                                            h, hparts, nparts, hatomic ? 1 : 0);
-    return run_gemm<256, 4, false, true>(x_q, w13_q, M, 2 * F, K, sx, sw, ab, dev, stream, 0, 0, h,
-                                         hparts, nparts, hatomic ? 1 : 0);
+        return run_gemm<256, 6, true, true>(&g, 1, dev, stream, h, hparts, nparts,
+                                            hatomic ? 1 : 0);
+    return run_gemm<256, 4, false, true>(&g, 1, dev, stream, h, hparts, nparts, hatomic ? 1 : 0);
 }
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, const DeviceInfo &dev, cudaStream_t stream)

@@ -48,6 +48,22 @@ inline bool quant_pair_enabled()
     return e == nullptr || e[0] != '0';
 }
 
+// Whether launch_gemm2 puts two GEMMs in one launch: F8_GEMM_GROUP=0 never,
+// =2 always, otherwise (1 or unset) when the schedule's predicted makespan
+// beats two launches by the margin launch_gemm2 asks for.
+constexpr int kGroupNever = 0;
+constexpr int kGroupAuto = 1;
+constexpr int kGroupAlways = 2;
+inline int gemm_group_mode()
+{
+    const char *e = std::getenv("F8_GEMM_GROUP");
+    if (e == nullptr)
+        return kGroupAuto;
+    if (e[0] == '0')
+        return kGroupNever;
+    return e[0] == '2' ? kGroupAlways : kGroupAuto;
+}
+
 // Kernels this library has launched in this process (every launch site adds
 // one; defined in f8_api.cu).
 extern std::atomic<unsigned long long> g_kernel_launches;
@@ -137,6 +153,26 @@ cudaError_t launch_quantize_swiglu(const void *a, const void *b, void *h, int64_
 cudaError_t launch_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
                         const float *sa, const float *sb, void *c, const DeviceInfo &dev,
                         cudaStream_t stream, int fa = 0, int fb = 0);
+
+// One GEMM as launch_gemm2 takes it: C[M,N] = bf16(A[M,K] B[N,K]^T / (sa sb)).
+struct GemmDesc {
+    const uint8_t *a;
+    const uint8_t *b;
+    int64_t M, N, K;
+    const float *sa;
+    const float *sb;
+    void *c;
+    int fa, fb;
+};
+
+// Two independent GEMMs in one persistent launch: the problem with the
+// costlier tiles is dealt round-robin over the CTAs, the other's tiles then
+// go, in order, to the CTA that frees up first (a static list schedule each
+// CTA evaluates in closed form).  Two plain launches if the shapes need
+// different kernels, or if the schedule does not promise a clear gain over
+// two launches (gemm_group_mode).
+cudaError_t launch_gemm2(const GemmDesc &g0, const GemmDesc &g1, const DeviceInfo &dev,
+                         cudaStream_t stream);
 
 // The W13 GEMM of a SwiGLU FFN: AB[M, 2F] = bf16(X W13^T / (sx sw)) with
 // W13 interleaved by 128 rows (W1 block, W3 block, ...), and h[M, F] =

@@ -143,6 +143,37 @@ f8_status f8_gemm_fmt(const uint8_t *a, f8_format fmt_a, const uint8_t *b, f8_fo
                       const float *scale_b, void *c, void *stream);
 
 /*
+ * One GEMM of f8_gemm_grouped: c = bf16( a b^T / (scale_a * scale_b) ),
+ * with the arguments of f8_gemm_fmt.
+ */
+typedef struct {
+    const uint8_t *a;       /* device [M, K], K contiguous, format fmt_a */
+    const uint8_t *b;       /* device [N, K], K contiguous, format fmt_b */
+    int64_t M, N, K;
+    const float *scale_a;   /* device fp32 scalars */
+    const float *scale_b;
+    void *c;                /* device bf16 [M, N] row-major */
+    f8_format fmt_a, fmt_b;
+} f8_gemm_problem;
+
+/*
+ * `count` (1 or 2) independent GEMMs in one persistent launch.  Their
+ * tiles share the CTA pairs under a static list schedule: the problem with
+ * more K per tile is dealt round-robin, then the other problem's tiles go
+ * in order to whichever pair frees up first.  One problem's last, partial
+ * wave is thus filled with the other's tiles.  Each c is bit-identical to
+ * f8_gemm_fmt on its problem (same tiles, same K order).  f8_linear_bwd
+ * runs its dgrad and wgrad GEMMs this way: they are the two products of
+ * the Float8 linear's backward pass, both reading q(dY).
+ *   problems: host array of `count` problems, each checked as by
+ *   f8_gemm_fmt (F8_ERR_INVALID for count outside 1..2 or a NULL array).
+ *   The c buffers must not overlap one another or any operand.
+ * Problems that need different kernels (M < 256 for one, M >= 256 for the
+ * other) or have a zero extent run as separate launches, in array order.
+ */
+f8_status f8_gemm_grouped(const f8_gemm_problem *problems, int count, void *stream);
+
+/*
  * What the forward pass leaves for the backward pass.  All members are
  * caller-allocated device buffers.
  *   x_t [K, M], w_t [K, N]: E4M3 column-major copies of q(X) and q(W);
@@ -181,7 +212,9 @@ f8_status f8_linear_fwd(const void *x, const void *w, int64_t M, int64_t N, int6
 /*
  * Backward of the same linear: dX [M,K] = dY W, dW [N,K] = dY^T X, using the
  * saved q(X)^T, q(W)^T and scales from f8_linear_fwd (which must have been
- * enqueued earlier on the same stream, or otherwise completed).
+ * enqueued earlier on the same stream, or otherwise completed).  dY is
+ * quantised (amax launch, cast launch), then both GEMMs run as one launch
+ * (f8_gemm_grouped).
  *   dy: device bf16 [M,N]; dx, dw: device bf16 outputs (either may be NULL
  *   to skip that GEMM).  Workspace as for the forward pass.
  */

@@ -1,0 +1,118 @@
+// Checks the closed-form two-problem tile schedule (f8_sched.h) against a
+// direct simulation of the list scheduler it stands for: problem 0 dealt
+// round-robin, then each problem-1 tile, in order, to the worker that is
+// free first (lowest worker index among equals).  Every worker's tile list
+// must be identical, which also makes every tile appear exactly once, and
+// sched_makespan must equal the simulated busiest worker's finishing time.
+// Usage: sched_check [cases]; prints "<n> cases, <m> mismatches".
+#include <cstdio>
+#include <cstdlib>
+#include <queue>
+#include <utility>
+#include <vector>
+
+#include "../../float8_mixed_precision_gb300/csrc/f8_sched.h"
+
+using f8::TileSched;
+
+static std::vector<std::vector<int>> simulate(const TileSched &s)
+{
+    std::vector<std::vector<int>> lists(s.units);
+    std::vector<long long> free_at(s.units, 0);
+    for (int t = 0; t < s.tiles0; ++t) {
+        lists[t % s.units].push_back(t);
+        free_at[t % s.units] += s.cost0;
+    }
+    typedef std::pair<long long, int> Ev;  // (free time, worker): smallest first
+    std::priority_queue<Ev, std::vector<Ev>, std::greater<Ev>> q;
+    for (int u = 0; u < s.units; ++u)
+        q.push(Ev(free_at[u], u));
+    for (int t = 0; t < s.tiles1; ++t) {
+        Ev e = q.top();
+        q.pop();
+        lists[e.second].push_back(s.tiles0 + t);
+        q.push(Ev(e.first + s.cost1, e.second));
+    }
+    return lists;
+}
+
+static std::vector<std::vector<int>> closed_form(const TileSched &s)
+{
+    std::vector<std::vector<int>> lists(s.units);
+    for (int u = 0; u < s.units; ++u)
+        for (int i = 0;; ++i) {
+            const int g = f8::sched_tile(s, u, i);
+            if (g < 0)
+                break;
+            lists[u].push_back(g);
+            if (i > s.tiles0 + s.tiles1)  // a runaway list is a mismatch
+                break;
+        }
+    return lists;
+}
+
+static long long simulated_makespan(const TileSched &s, const std::vector<std::vector<int>> &l)
+{
+    long long worst = 0;
+    for (const std::vector<int> &v : l) {
+        long long t = 0;
+        for (int g : v)
+            t += g < s.tiles0 ? s.cost0 : s.cost1;
+        worst = t > worst ? t : worst;
+    }
+    return worst;
+}
+
+static int check(const TileSched &s)
+{
+    const std::vector<std::vector<int>> sim = simulate(s);
+    if (sim == closed_form(s) && simulated_makespan(s, sim) == f8::sched_makespan(s))
+        return 0;
+    std::printf("mismatch: U=%d T0=%d T1=%d c0=%d c1=%d\n", s.units, s.tiles0, s.tiles1, s.cost0,
+                s.cost1);
+    return 1;
+}
+
+int main(int argc, char **argv)
+{
+    const int cases = argc > 1 ? std::atoi(argv[1]) : 20000;
+    int bad = 0, n = 0;
+    // the launches a linear's backward pass makes on 76 CTA pairs, with the
+    // tile cost model K blocks + 4 (Llama-3.1 8B/70B attention and FFN shapes)
+    const TileSched shapes[] = {
+        {76, 256, 512, 68, 36},   {76, 64, 512, 68, 12},    {76, 512, 896, 116, 68},
+        {76, 448, 512, 68, 60},   {76, 1792, 1024, 228, 68}, {76, 1024, 1792, 68, 228},
+        {76, 0, 100, 1, 5},       {76, 100, 0, 5, 1},        {1, 7, 9, 3, 2},
+        {152, 512, 512, 36, 36},
+    };
+    for (const TileSched &s : shapes) {
+        bad += check(s);
+        ++n;
+    }
+    // exhaustive over small parameters (equal-time ties of both classes)
+    for (int U = 1; U <= 9; ++U)
+        for (int t0 = 0; t0 <= 20; ++t0)
+            for (int t1 = 0; t1 <= 20; t1 += 3)
+                for (int c0 = 1; c0 <= 6; ++c0)
+                    for (int c1 = 1; c1 <= 6; ++c1) {
+                        bad += check(TileSched{U, t0, t1, c0, c1});
+                        ++n;
+                    }
+    unsigned r = 12345u;
+    for (int i = 0; i < cases; ++i) {
+        r = r * 1103515245u + 12345u;
+        const int U = 1 + static_cast<int>((r >> 8) % 160u);
+        r = r * 1103515245u + 12345u;
+        const int t0 = static_cast<int>((r >> 8) % 2000u);
+        r = r * 1103515245u + 12345u;
+        const int t1 = static_cast<int>((r >> 8) % 2000u);
+        r = r * 1103515245u + 12345u;
+        const int c0 = 1 + static_cast<int>((r >> 8) % 300u);
+        r = r * 1103515245u + 12345u;
+        const int c1 = 1 + static_cast<int>((r >> 8) % 300u);
+        bad += check(TileSched{U, t0, t1, c0, c1});
+        ++n;
+    }
+    std::printf("%d cases, %d mismatches\n", n, bad);
+    return bad != 0;
+}

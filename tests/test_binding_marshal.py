@@ -55,6 +55,9 @@ def test_every_wrapper_marshals(rec):
     binding.f8_gemm(q, torch.zeros((N, K), dtype=torch.uint8), torch.ones(1), torch.ones(1))
     binding.f8_gemm(q, torch.zeros((N, K), dtype=torch.uint8), torch.ones(1), torch.ones(1),
                     fmt_a=binding.F8_E5M2)
+    qb = torch.zeros((N, K), dtype=torch.uint8)
+    binding.f8_gemm_grouped([(q, qb, torch.ones(1), torch.ones(1)),
+                             (qb, q, torch.ones(1), torch.ones(1), None, binding.F8_E5M2)])
     y, saved = binding.f8_linear_fwd(x, w)
     binding.f8_linear_fwd_noalloc(x, w)
     binding.f8_linear_bwd(dy, saved)

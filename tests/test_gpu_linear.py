@@ -263,3 +263,65 @@ def test_two_streams_share_no_state(f8):
     for b, r in zip(bufs, ref):
         for got, want in zip(outs(b), r):
             assert torch.equal(got.view(torch.uint8), want.view(torch.uint8))
+
+
+GROUP_CASES = [
+    (8192, 1024, 4096, 0),   # wk/wv: 64 wgrad tiles (fewer than the CTA pairs), 512 dgrad
+    (8192, 4096, 4096, 0),   # wq/wo: 256 wgrad tiles of twice the K of the 512 dgrad tiles
+    (4352, 1040, 1552, 1),   # ragged M, N, K; E5M2 dY
+    (512, 4112, 4096, 0),    # 34 dgrad tiles, 17 x 16 wgrad tiles
+    (1024, 256, 16384, 0),   # dgrad tiles costlier than wgrad tiles
+    (128, 192, 512, 0),      # single-CTA kernel for both
+    (128, 512, 256, 1),      # pair kernel for wgrad only: two launches
+]
+
+
+@pytest.mark.parametrize("M,N,K,fmt", GROUP_CASES)
+def test_grouped_backward_matches_two_launches(f8, monkeypatch, M, N, K, fmt):
+    """dgrad and wgrad in one launch (the tiles of both under one static
+    schedule) give the bits of two separate launches: each output tile is
+    accumulated in the same K order by the same kernel.  The grouped path
+    makes one launch fewer whenever both GEMMs take the same kernel."""
+    d = wl.custom_linear(M, K, N, seed=M + 3 * N + 7 * K, dy_std=0.3)
+    y, saved = f8.f8_linear_fwd(d["x"].to(DEV), d["w"].to(DEV))
+    dy = d["dy"].to(DEV)
+    dy_fmt = f8.F8_E5M2 if fmt else f8.F8_E4M3
+    out = {}
+    for grouped in ("0", "2"):   # never / always one launch
+        monkeypatch.setenv("F8_GEMM_GROUP", grouped)
+        torch.cuda.synchronize()
+        n0 = f8.f8_kernel_launches()
+        dx, dw = f8.f8_linear_bwd(dy, saved, dy_fmt=dy_fmt)
+        torch.cuda.synchronize()
+        out[grouped] = (dx, dw, f8.f8_kernel_launches() - n0)
+        assert f8.f8_last_device_status() == 0
+    assert torch.equal(out["0"][0].view(torch.int16), out["2"][0].view(torch.int16))
+    assert torch.equal(out["0"][1].view(torch.int16), out["2"][1].view(torch.int16))
+    same_kernel = (M >= 256) == (N >= 256)
+    assert out["2"][2] == out["0"][2] - (1 if same_kernel else 0)
+    if M * N * K <= 10 ** 10:
+        fwd = oracle.linear_fwd(wl.bits(d["x"]), wl.bits(d["w"]))
+        bwd = oracle.linear_bwd(wl.bits(d["dy"]), fwd, dy_fmt=oracle.E5M2 if fmt else oracle.E4M3)
+        check_close(out["2"][0], bwd["dx"], what="dX")
+        check_close(out["2"][1], bwd["dw"], what="dW")
+
+
+@pytest.mark.parametrize("M,N,K,grouped", [
+    (8192, 4096, 4096, True),     # wq/wo: 6% predicted from the schedule
+    (8192, 1024, 4096, True),     # wk/wv: 8%
+    (8192, 14336, 4096, False),   # w1/w3: nothing to gain
+    (8192, 4096, 14336, False),   # w2
+])
+def test_backward_groups_where_the_schedule_gains(f8, M, N, K, grouped):
+    """By default f8_linear_bwd runs dgrad and wgrad as one launch only where
+    the static schedule's predicted time beats two launches by at least 4%:
+    the attention projections of Llama-3.1 8B, not its FFN linears."""
+    d = wl.custom_linear(M, K, N, seed=11)
+    y, saved = f8.f8_linear_fwd(d["x"].to(DEV), d["w"].to(DEV))
+    dy = d["dy"].to(DEV)
+    torch.cuda.synchronize()
+    n0 = f8.f8_kernel_launches()
+    f8.f8_linear_bwd(dy, saved)
+    torch.cuda.synchronize()
+    assert f8.f8_kernel_launches() - n0 == (3 if grouped else 4)
+    assert f8.f8_last_device_status() == 0

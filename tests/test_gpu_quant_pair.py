@@ -81,10 +81,11 @@ def test_pair_path_flags_nonfinite(f8, which):
         del os.environ["F8_QUANT_PAIR"]
 
 
-def test_kernel_launch_counts(f8):
+def test_kernel_launch_counts(f8, monkeypatch):
     """libf8's own launch counter: the forward of a linear that fits in L2
     is 3 kernels (paired amax, paired cast, GEMM), 5 on the four-launch path
-    or for a shape the TMA cast does not take; the backward is 4."""
+    or for a shape the TMA cast does not take; the backward is 3 (amax and
+    cast of dY, dgrad and wgrad in one GEMM launch), 4 with F8_GEMM_GROUP=0."""
     def count(fn):
         torch.cuda.synchronize()
         n0 = f8.f8_kernel_launches()
@@ -97,7 +98,11 @@ def test_kernel_launch_counts(f8):
     n, _ = count(lambda: _fwd(f8, x, w, False))
     assert n == 5
     n, _ = count(lambda: f8.f8_linear_bwd(dy, saved))
+    assert n == 3
+    monkeypatch.setenv("F8_GEMM_GROUP", "0")
+    n, _ = count(lambda: f8.f8_linear_bwd(dy, saved))
     assert n == 4
+    monkeypatch.delenv("F8_GEMM_GROUP")
     d = wl.custom_linear(272, 528, 400, seed=4)      # not multiples of 128
     n, _ = count(lambda: _fwd(f8, d["x"].to(DEV), d["w"].to(DEV), True))
     assert n == 5
