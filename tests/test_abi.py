@@ -147,3 +147,25 @@ def test_w13_swiglu_bwd_rejects_bad_arguments_on_host(L):
     assert f(FAKE, FAKE, ctypes.byref(s), 256, 128, 64, FAKE, 0, FAKE, FAKE, FAKE, 10, None) == 1
     assert f(FAKE_MIS, FAKE, ctypes.byref(s), 256, 128, 64, FAKE, 0, FAKE, FAKE, FAKE, ws, None) == 2
     assert f(FAKE, FAKE, ctypes.byref(s), 256, 128, 64, FAKE, 2, FAKE, FAKE, FAKE, ws, None) == 1
+
+
+def test_gemm_grouped_rejects_bad_arguments_on_host(L):
+    from float8_mixed_precision_gb300.binding import _GemmProblem
+    ok = _GemmProblem(FAKE, FAKE, 256, 256, 256, FAKE, FAKE + 4, FAKE, 0, 0)
+    arr = (_GemmProblem * 3)(ok, ok, ok)
+    f = L.f8_gemm_grouped
+    assert f(None, 1, None) == 1                  # no array
+    assert f(arr, 0, None) == 1                   # count outside 1..2
+    assert f(arr, 3, None) == 1
+
+    def with_field(name, value):
+        p = _GemmProblem(FAKE, FAKE, 256, 256, 256, FAKE, FAKE + 4, FAKE, 0, 0)
+        setattr(p, name, value)
+        return (_GemmProblem * 2)(ok, p)
+
+    assert f(with_field("K", 24), 2, None) == 3       # K % 16
+    assert f(with_field("M", -1), 2, None) == 1
+    assert f(with_field("fmt_a", 2), 2, None) == 1    # no such format
+    assert f(with_field("scale_b", None), 2, None) == 1
+    assert f(with_field("c", None), 2, None) == 1
+    assert f(with_field("b", FAKE_MIS), 2, None) == 2

@@ -117,3 +117,39 @@ def test_linear_backward_e5m2_llama_wq_full_size(f8):
     rows = np.array([b * 128 + rng.integers(0, 128) for b in range(lin.N // 128)], np.int64)
     ref = oracle.gemm_rows_fmt(qdy["qt"], oracle.E5M2, qx["qt"], oracle.E4M3, qdy["scale"], qx["scale"], rows)
     check_close(dw[torch.from_numpy(rows).to(DEV)], ref, what="dW rows (E5M2 dY)")
+
+
+@pytest.mark.parametrize("shapes", [
+    ((300, 520, 400, E5, E4), (640, 1024, 2048, E4, E4)),   # ragged + costlier second problem
+    ((1024, 256, 4096, E4, E5), (256, 1536, 512, E5, E5)),  # costlier first problem
+    ((37, 50, 48, E5, E4), (100, 60, 32, E4, E4)),          # both on the single-CTA kernel
+    ((512, 384, 1024, E4, E4), (0, 64, 64, E4, E4)),        # an empty problem: separate launches
+])
+def test_gemm_grouped_matches_single_launches(f8, shapes, monkeypatch):
+    """f8_gemm_grouped on two problems of different shapes and formats (the
+    grouping forced on) writes the bits f8_gemm writes for each alone, and
+    both match the oracle."""
+    monkeypatch.setenv("F8_GEMM_GROUP", "2")
+    probs, refs, singles = [], [], []
+    for i, (M, N, K, fa, fb) in enumerate(shapes):
+        a, b = _codes((M, K), 11 * i + M + K, fa), _codes((N, K), 13 * i + N + K, fb)
+        sa, sb = np.float32(2.0 if fa == E4 else 1e-3), np.float32(0.25 if fb == E4 else 4e-3)
+        ad, bd = a.to(DEV), b.to(DEV)
+        sad, sbd = torch.tensor(sa, device=DEV), torch.tensor(sb, device=DEV)
+        probs.append((ad, bd, sad, sbd, None, fa, fb))
+        refs.append(oracle.gemm_rows_fmt(a.numpy(), fa, b.numpy(), fb, sa, sb) if M else None)
+        singles.append(f8.f8_gemm(ad, bd, sad, sbd, fmt_a=fa, fmt_b=fb))
+    outs = f8.f8_gemm_grouped(probs)
+    assert f8.f8_last_device_status() == 0
+    for out, single, ref, (M, N, K, fa, fb) in zip(outs, singles, refs, shapes):
+        assert torch.equal(out.view(torch.int16), single.view(torch.int16))
+        if ref is not None:
+            check_close(out, ref, what=f"grouped gemm {M}x{N}x{K}")
+
+
+def test_gemm_grouped_one_problem_is_f8_gemm(f8):
+    a, b = _codes((512, 1024), 1, E4), _codes((768, 1024), 2, E4)
+    s = torch.tensor(1.5, device=DEV)
+    one = f8.f8_gemm_grouped([(a.to(DEV), b.to(DEV), s, s)])[0]
+    assert torch.equal(one, f8.f8_gemm(a.to(DEV), b.to(DEV), s, s))
+    assert f8.f8_last_device_status() == 0
