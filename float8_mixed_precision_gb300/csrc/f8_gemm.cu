@@ -145,9 +145,13 @@ __device__ __forceinline__ void epilogue_rows(uint32_t taddr, int row0, int col_
         tc_wait_ld();
         const int col0 = col_base + j * kEpiCols;
         if (tma_store) {
+            // nothing of this box lies in C: no staging, no store, no bulk
+            // group (row0 and col0 are warp-uniform)
+            if (row0 >= M || col0 >= N)
+                continue;
             uint8_t *b = stage + buf * kEpiBufBytes;
             if (lane == 0)
-                bulk_wait_group_read<1>();  // the store issued from b two steps ago has read it
+                bulk_wait_group_read<1>();  // the store issued from b two stores ago has read it
             __syncwarp();
             // row `lane` of the box, 16-byte chunk q at (q ^ row % 8): the 128-byte swizzle
 #pragma unroll
@@ -156,12 +160,10 @@ __device__ __forceinline__ void epilogue_rows(uint32_t taddr, int row0, int col_
                     pack8(&r[8 * q], inv);
             fence_proxy_async_shared();
             __syncwarp();
-            // one bulk group per step, empty where the box lies outside C,
-            // so that the read wait above always refers to this buffer's
-            // last store
+            // every use of a buffer ends in one store and one bulk group, so
+            // the read wait above always refers to this buffer's last store
             if (lane == 0) {
-                if (row0 < M && col0 < N)
-                    tma_store_2d(tma_c, b, col0, row0);
+                tma_store_2d(tma_c, b, col0, row0);
                 bulk_commit_group();
             }
             buf ^= 1u;
@@ -269,7 +271,20 @@ struct GemmProb {
     uint32_t idesc;
 };
 
-template <int BN, int STAGES, bool PAIR, bool GLU>
+// This unit's i-th tile as a global index ([0, tiles0) problem 0, then
+// problem 1), or -1.  One problem (TWO = false): plain round-robin, the
+// code of a single-GEMM launch; two: the list schedule of f8_sched.h.
+template <bool TWO>
+__device__ __forceinline__ int unit_tile(const TileSched &s, int unit, int i)
+{
+    if (!TWO) {
+        const int t = unit + i * s.units;
+        return t < s.tiles0 ? t : -1;
+    }
+    return sched_tile(s, unit, i);
+}
+
+template <int BN, int STAGES, bool PAIR, bool GLU, bool TWO>
 __global__ void __launch_bounds__(Cfg<BN, STAGES, PAIR, GLU>::kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
             const __grid_constant__ CUtensorMap tma_c, const __grid_constant__ CUtensorMap tma_h,
@@ -299,7 +314,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
     const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const bool two = sched.tiles1 > 0;
+    const bool two = TWO && sched.tiles1 > 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -358,10 +373,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
             int64_t issued = 0;
             bool stop = false;
             for (int i = 0; !stop; ++i) {
-                int tile = sched_tile(sched, unit, i);
+                int tile = unit_tile<TWO>(sched, unit, i);
                 if (tile < 0)
                     break;
-                const bool second = tile >= sched.tiles0;
+                const bool second = TWO && tile >= sched.tiles0;
                 if (second)
                     tile -= sched.tiles0;
                 const CUtensorMap *ma = second ? &tma_a1 : &tma_a;
@@ -434,10 +449,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
             bool stop = false;
             int local = 0;
             for (;; ++local) {
-                const int tile = sched_tile(sched, unit, local);
+                const int tile = unit_tile<TWO>(sched, unit, local);
                 if (tile < 0)
                     break;
-                const bool second = tile >= sched.tiles0;
+                const bool second = TWO && tile >= sched.tiles0;
                 const int num_kb = second ? p1.num_kb : p0.num_kb;
                 const uint32_t idesc = second ? p1.idesc : p0.idesc;
                 const uint32_t acc = local & 1;
@@ -502,10 +517,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
         const uint32_t tempty_leader = PAIR ? cluster_map(smem_addr(&tempty[0]), 0) : 0u;
         uint32_t buf = 0;
         for (int local = 0;; ++local) {
-            int tile = sched_tile(sched, unit, local);
+            int tile = unit_tile<TWO>(sched, unit, local);
             if (tile < 0)
                 break;
-            const bool second = tile >= sched.tiles0;
+            const bool second = TWO && tile >= sched.tiles0;
             if (second)
                 tile -= sched.tiles0;
             const uint32_t acc = local & 1;
@@ -663,7 +678,7 @@ SchedPlan plan_schedule(const GemmDesc *probs, int nprob, int tile_m, int bn, in
                      first};
 }
 
-template <int BN, int STAGES, bool PAIR, bool GLU = false>
+template <int BN, int STAGES, bool PAIR, bool GLU = false, bool TWO = false>
 cudaError_t run_gemm(const GemmDesc *probs, int nprob, const DeviceInfo &dev, cudaStream_t stream,
                      void *h = nullptr, unsigned *hparts = nullptr, int *nparts = nullptr,
                      int hatomic = 0)
@@ -713,7 +728,7 @@ cudaError_t run_gemm(const GemmDesc *probs, int nprob, const DeviceInfo &dev, cu
     static cudaError_t attr_err[64];
     const int dv = dev.ordinal & 63;
     std::call_once(attr_once[dv], [&] {
-        attr_err[dv] = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, PAIR, GLU>,
+        attr_err[dv] = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, PAIR, GLU, TWO>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             C::kSmemBytes);
     });
@@ -728,7 +743,7 @@ cudaError_t run_gemm(const GemmDesc *probs, int nprob, const DeviceInfo &dev, cu
     const int group_m = PAIR ? 8 : 16;
     if (nparts != nullptr)
         *nparts = (PAIR ? 2 : 1) * units;
-    return launch_pdl_cluster(gemm_kernel<BN, STAGES, PAIR, GLU>, dim3((PAIR ? 2 : 1) * units),
+    return launch_pdl_cluster(gemm_kernel<BN, STAGES, PAIR, GLU, TWO>, dim3((PAIR ? 2 : 1) * units),
                               dim3(C::kThreads), C::kSmemBytes, stream, PAIR ? 2u : 1u,
                               ma[first], mb[first], mc[first], mh, ma[second], mb[second],
                               mc[second], gp[first], gp[second], sched, dev.status,
@@ -804,8 +819,8 @@ cudaError_t launch_gemm2(const GemmDesc &g0, const GemmDesc &g1, const DeviceInf
     }
     const GemmDesc g[2] = {g0, g1};
     if (v == kVariantPair)
-        return run_gemm<256, 6, true>(g, 2, dev, stream);
-    return run_gemm<256, 4, false>(g, 2, dev, stream);
+        return run_gemm<256, 6, true, false, true>(g, 2, dev, stream);
+    return run_gemm<256, 4, false, false, true>(g, 2, dev, stream);
 }
 
 cudaError_t launch_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int64_t M, int64_t F,
