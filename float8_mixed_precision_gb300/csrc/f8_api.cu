@@ -179,12 +179,18 @@ f8_status check_cast_args(const void *x, int64_t rows, int64_t cols, const float
     return F8_OK;
 }
 
+// The GEMM kernels number the output tiles of a launch (128 x 256 at the
+// smallest) in 32-bit ints.
+bool tiles_fit(int64_t M, int64_t N) { return ((M + 127) / 128) * ((N + 255) / 256) <= INT32_MAX / 2; }
+
 f8_status check_gemm_args(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
                           const float *sa, const float *sb, const void *c)
 {
     if (M < 0 || N < 0 || K < 0 || sa == nullptr || sb == nullptr)
         return F8_ERR_INVALID;
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2)
+        return F8_ERR_SHAPE;
+    if (!tiles_fit(M, N))
         return F8_ERR_SHAPE;
     if (M > 0 && N > 0 && (c == nullptr || (K > 0 && (a == nullptr || b == nullptr))))
         return F8_ERR_INVALID;
@@ -202,6 +208,9 @@ f8_status check_linear_shape(int64_t M, int64_t N, int64_t K)
     if (M % 16 || N % 16 || K % 16)
         return F8_ERR_SHAPE;
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2)
+        return F8_ERR_SHAPE;
+    // Y [M,N], dX [M,K], dW [N,K]
+    if (!tiles_fit(M, N) || !tiles_fit(M, K) || !tiles_fit(N, K))
         return F8_ERR_SHAPE;
     return F8_OK;
 }

@@ -64,6 +64,7 @@ FAKE_MIS = FAKE + 8     # 8-byte aligned, not 16
     ((FAKE_MIS, FAKE, 16, 16, 16, FAKE, FAKE, FAKE, None), 2), # misaligned A
     ((FAKE, FAKE, 16, 16, 16, FAKE, FAKE, FAKE_MIS, None), 2), # misaligned C
     ((None, FAKE, 16, 16, 16, FAKE, FAKE, FAKE, None), 1),     # NULL A
+    ((FAKE, FAKE, 1 << 29, 1 << 29, 16, FAKE, FAKE, FAKE, None), 3),  # 2^36 tiles
 ])
 def test_gemm_rejects_bad_arguments_on_host(L, args, want):
     assert L.f8_gemm(*args) == want
@@ -80,6 +81,8 @@ def test_other_calls_reject_bad_arguments_on_host(L):
     s = _Saved(FAKE, FAKE, FAKE, FAKE + 4, FAKE + 8, FAKE + 12)
     ws = 1 << 30
     assert L.f8_linear_fwd(FAKE, FAKE, 16, 16, 24, FAKE, ctypes.byref(s), FAKE, ws, None) == 3
+    big = 1 << 29                                      # dX would have 2^35 tiles
+    assert L.f8_linear_fwd(FAKE, FAKE, big, 16, big, FAKE, ctypes.byref(s), FAKE, ws, None) == 3
     assert L.f8_linear_fwd(FAKE, FAKE, 0, 16, 16, FAKE, ctypes.byref(s), FAKE, ws, None) == 1
     assert L.f8_linear_fwd(FAKE, FAKE, 16, 16, 16, FAKE, None, FAKE, ws, None) == 1
     assert L.f8_linear_fwd(FAKE, FAKE, 16, 16, 16, FAKE, ctypes.byref(s), FAKE, 10, None) == 1
