@@ -640,42 +640,15 @@ bool make_map(CUtensorMap *map, CUtensorMapDataType dtype, int esize, const void
     return r == CUDA_SUCCESS;
 }
 
-// Per-tile cost in the schedule of a two-problem launch, in K blocks: the
-// tile's K blocks plus a fixed share for handing over the accumulator and
-// draining it (measured: a short-K tile costs about four K blocks more than
-// its MMAs).
-constexpr int kTileOverheadKb = 4;
+static_assert(kBK == kSchedBlockK, "the schedule's tile costs count the kernel's K blocks");
 
-// Smallest gain, in percent of the two launches' predicted time, for which
-// launch_gemm2 puts two GEMMs in one launch.  Measured: the attention
-// projections' backward GEMMs (predicted 6-8%) gain 3-10%; the FFN ones
-// (predicted 0-2%, power-capped) lose up to 2% when grouped.
-constexpr int kGroupMinGainPct = 4;
-
-// The schedule of one launch over `nprob` problems with tile_m x bn tiles
-// on at most max_units workers; `first` is the index of the problem dealt
-// round-robin (the one with the costlier tiles).
-struct SchedPlan {
-    TileSched s;
-    int first;
-};
-
-SchedPlan plan_schedule(const GemmDesc *probs, int nprob, int tile_m, int bn, int64_t max_units)
+// The schedule planner's view of a launch's problems.
+SchedPlan plan_launch(const GemmDesc *probs, int nprob, int tile_m, int bn, int64_t max_units)
 {
-    int tiles[2] = {0, 0};
-    int cost[2] = {1, 1};
-    for (int i = 0; i < nprob; ++i) {
-        const GemmDesc &p = probs[i];
-        tiles[i] = static_cast<int>(((p.M + tile_m - 1) / tile_m) * ((p.N + bn - 1) / bn));
-        cost[i] = static_cast<int>((p.K + kBK - 1) / kBK) + kTileOverheadKb;
-    }
-    const int64_t total = static_cast<int64_t>(tiles[0]) + tiles[1];
-    const int units = static_cast<int>(total < max_units ? total : max_units);
-    const int first = (nprob == 2 && cost[1] > cost[0]) ? 1 : 0;
-    const int second = nprob == 2 ? 1 - first : first;
-    return SchedPlan{TileSched{units, tiles[first], nprob == 2 ? tiles[second] : 0, cost[first],
-                               cost[second]},
-                     first};
+    SchedProblem p[2];
+    for (int i = 0; i < nprob; ++i)
+        p[i] = SchedProblem{probs[i].M, probs[i].N, probs[i].K};
+    return sched_plan(p, nprob, tile_m, bn, max_units);
 }
 
 template <int BN, int STAGES, bool PAIR, bool GLU = false, bool TWO = false>
@@ -735,7 +708,7 @@ cudaError_t run_gemm(const GemmDesc *probs, int nprob, const DeviceInfo &dev, cu
     if (attr_err[dv] != cudaSuccess)
         return attr_err[dv];
     const SchedPlan plan =
-        plan_schedule(probs, nprob, C::kTileM, BN, PAIR ? dev.sm_count / 2 : dev.sm_count);
+        plan_launch(probs, nprob, C::kTileM, BN, PAIR ? dev.sm_count / 2 : dev.sm_count);
     const TileSched &sched = plan.s;
     const int units = sched.units;
     const int first = plan.first;
@@ -803,11 +776,8 @@ cudaError_t launch_gemm2(const GemmDesc &g0, const GemmDesc &g1, const DeviceInf
     if (group && mode == kGroupAuto) {
         const int tile_m = v == kVariantPair ? 2 * kBM : kBM;
         const int64_t max_units = v == kVariantPair ? dev.sm_count / 2 : dev.sm_count;
-        const GemmDesc both[2] = {g0, g1};
-        const int64_t grouped = sched_makespan(plan_schedule(both, 2, tile_m, 256, max_units).s);
-        const int64_t apart = sched_makespan(plan_schedule(&g0, 1, tile_m, 256, max_units).s) +
-                              sched_makespan(plan_schedule(&g1, 1, tile_m, 256, max_units).s);
-        group = grouped * 100 <= apart * (100 - kGroupMinGainPct);
+        group = sched_should_group(SchedProblem{g0.M, g0.N, g0.K}, SchedProblem{g1.M, g1.N, g1.K},
+                                   tile_m, 256, max_units);
     }
     if (!group) {
         cudaError_t e = launch_gemm(g0.a, g0.b, g0.M, g0.N, g0.K, g0.sa, g0.sb, g0.c, dev, stream,

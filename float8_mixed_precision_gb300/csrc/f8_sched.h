@@ -96,4 +96,69 @@ static inline int64_t sched_makespan(const TileSched &s)
     return worst;
 }
 
+// ------------------------------------------------------------ host planning
+
+// Bytes of K per pipeline stage (one K block), as the GEMM kernel stages them.
+constexpr int kSchedBlockK = 128;
+
+// Per-tile cost in the schedule, in K blocks: the tile's K blocks plus a
+// fixed share for handing over the accumulator and draining it (measured: a
+// short-K tile costs about four K blocks more than its MMAs).
+constexpr int kSchedTileOverheadKb = 4;
+
+// Smallest gain, in percent of the two launches' predicted time, for which
+// two GEMMs share one launch.  Measured: the attention projections'
+// backward GEMMs (predicted 6-8%) gain 2-10%; the FFN ones (predicted
+// 0-2%, power-capped) lose up to 2% when grouped.
+constexpr int kSchedMinGainPct = 4;
+
+// The extents of one GEMM C[M,N] = A[M,K] B[N,K]^T.
+struct SchedProblem {
+    int64_t M, N, K;
+};
+
+// The schedule of one launch over `nprob` (1 or 2) problems in tile_m x bn
+// output tiles on at most max_units workers; `first` is the index of the
+// problem dealt round-robin (the one with the costlier tiles).
+struct SchedPlan {
+    TileSched s;
+    int first;
+};
+
+static inline SchedPlan sched_plan(const SchedProblem *p, int nprob, int tile_m, int bn,
+                                   int64_t max_units)
+{
+    int tiles[2] = {0, 0};
+    int cost[2] = {1, 1};
+    for (int i = 0; i < nprob; ++i) {
+        tiles[i] = static_cast<int>(((p[i].M + tile_m - 1) / tile_m) * ((p[i].N + bn - 1) / bn));
+        cost[i] = static_cast<int>((p[i].K + kSchedBlockK - 1) / kSchedBlockK) +
+                  kSchedTileOverheadKb;
+    }
+    const int64_t total = static_cast<int64_t>(tiles[0]) + tiles[1];
+    const int units = static_cast<int>(total < max_units ? total : max_units);
+    const int first = (nprob == 2 && cost[1] > cost[0]) ? 1 : 0;
+    const int second = nprob == 2 ? 1 - first : first;
+    SchedPlan plan;
+    plan.s.units = units;
+    plan.s.tiles0 = tiles[first];
+    plan.s.tiles1 = nprob == 2 ? tiles[second] : 0;
+    plan.s.cost0 = cost[first];
+    plan.s.cost1 = cost[second];
+    plan.first = first;
+    return plan;
+}
+
+// Whether two GEMMs should share one launch: the schedule's predicted
+// makespan beats the two launches' by at least kSchedMinGainPct percent.
+static inline bool sched_should_group(const SchedProblem &p0, const SchedProblem &p1, int tile_m,
+                                      int bn, int64_t max_units)
+{
+    const SchedProblem both[2] = {p0, p1};
+    const int64_t grouped = sched_makespan(sched_plan(both, 2, tile_m, bn, max_units).s);
+    const int64_t apart = sched_makespan(sched_plan(&p0, 1, tile_m, bn, max_units).s) +
+                          sched_makespan(sched_plan(&p1, 1, tile_m, bn, max_units).s);
+    return grouped * 100 <= apart * (100 - kSchedMinGainPct);
+}
+
 }  // namespace f8

@@ -4,6 +4,9 @@
 // free first (lowest worker index among equals).  Every worker's tile list
 // must be identical, which also makes every tile appear exactly once, and
 // sched_makespan must equal the simulated busiest worker's finishing time.
+// The planner's tile counts, costs and grouping decisions for the Llama-3.1
+// linears' backward passes are checked against the values worked out by
+// hand (a launch is shared only where that is predicted to gain >= 4%).
 // Usage: sched_check [cases]; prints "<n> cases, <m> mismatches".
 #include <cstdio>
 #include <cstdlib>
@@ -112,6 +115,47 @@ int main(int argc, char **argv)
         const int c1 = 1 + static_cast<int>((r >> 8) % 300u);
         bad += check(TileSched{U, t0, t1, c0, c1});
         ++n;
+    }
+    // the planner on the backward pass of the Llama-3.1 linears (M = 8192
+    // tokens; dgrad [M, K] over N, wgrad [N, K] over M; 256 x 256 tiles on 76
+    // CTA pairs): tile counts and costs, and the decision to share a launch
+    struct Lin {
+        const char *name;
+        int64_t N, K;
+        bool group;
+    };
+    const Lin lins[] = {{"wq/wo", 4096, 4096, true},      {"wk/wv", 1024, 4096, true},
+                        {"8B w1/w3", 14336, 4096, false}, {"8B w2", 4096, 14336, false},
+                        {"70B w1/w3", 28672, 8192, false}, {"70B w2", 8192, 28672, false}};
+    for (const Lin &l : lins) {
+        const f8::SchedProblem dgrad{8192, l.K, l.N}, wgrad{l.N, l.K, 8192};
+        const bool g = f8::sched_should_group(dgrad, wgrad, 256, 256, 76);
+        if (g != l.group) {
+            std::printf("decision mismatch: %s grouped=%d\n", l.name, g);
+            ++bad;
+        }
+        ++n;
+    }
+    {
+        // wq: wgrad (K = 8192: 64 K blocks + 4) is dealt first, 256 tiles;
+        // then dgrad's 512 tiles of 32 + 4
+        const f8::SchedProblem p[2] = {{8192, 4096, 4096}, {4096, 4096, 8192}};
+        const f8::SchedPlan pl = f8::sched_plan(p, 2, 256, 256, 76);
+        if (!(pl.first == 1 && pl.s.units == 76 && pl.s.tiles0 == 256 && pl.s.cost0 == 68 &&
+              pl.s.tiles1 == 512 && pl.s.cost1 == 36)) {
+            std::printf("plan mismatch (wq)\n");
+            ++bad;
+        }
+        // one small problem: round-robin over as many workers as tiles
+        const f8::SchedPlan one = f8::sched_plan(p + 1, 1, 256, 256, 76);
+        const f8::SchedProblem tiny{300, 520, 400};
+        const f8::SchedPlan t = f8::sched_plan(&tiny, 1, 256, 256, 76);
+        if (!(one.s.tiles1 == 0 && one.s.units == 76 && t.s.units == 6 && t.s.tiles0 == 6 &&
+              t.s.cost0 == 8)) {
+            std::printf("plan mismatch (one problem)\n");
+            ++bad;
+        }
+        n += 2;
     }
     std::printf("%d cases, %d mismatches\n", n, bad);
     return bad != 0;

@@ -8,7 +8,10 @@ Each CTA evaluates its own share of that list schedule in closed form
 compares every worker's tile list with a direct simulation of the list
 scheduler (a priority queue of free times), on the launch shapes of the
 Llama-3.1 8B and 70B linears, exhaustively over small parameters, and on
-random ones; identical lists also mean every tile is run exactly once."""
+random ones; identical lists also mean every tile is run exactly once.  The
+planner's tile counts, costs and decisions to share a launch are pinned for
+the backward passes of the Llama-3.1 8B and 70B linears (grouped: the
+attention projections; not grouped: the FFN linears)."""
 import os
 import shutil
 import subprocess
