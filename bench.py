@@ -4,8 +4,10 @@
 
 One step = every linear of the workload through the whole path: amax(X),
 cast_transpose(X), amax(W), cast_transpose(W), GEMM Y = XW^T, amax(dY),
-cast_transpose(dY), GEMM dX = dY W, GEMM dW = dY^T X.  The metric is GEMM
-work (6 M N K flops per linear) over the whole step's time, in TFLOP/s.
+cast_transpose(dY), GEMM dX = dY W, GEMM dW = dY^T X (the last two in one
+launch where the tile schedule gains, as f8_linear_bwd runs them).  The
+metric is GEMM work (6 M N K flops per linear) over the whole step's time,
+in TFLOP/s.
 
 Inputs are seeded synthetic bf16 tensors (float8_mixed_precision_gb300.workloads),
 resident in HBM before timing.  By default the step (every launch of every
