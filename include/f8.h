@@ -56,7 +56,7 @@ typedef enum {
     F8_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed           */
     F8_ERR_TIMEOUT = 5,     /* a device-side wait exceeded its time limit     */
     F8_ERR_NONFINITE = 6,   /* an amax input held +-inf or NaN                */
-    F8_ERR_UNSUPPORTED = 7, /* no sm_100-family device / driver entry point   */
+    F8_ERR_UNSUPPORTED = 7, /* not an sm_103 device, or no driver entry point */
     F8_ERR_BOUNDS = 8       /* checked build only: an index left its buffer   */
 } f8_status;
 

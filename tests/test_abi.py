@@ -172,3 +172,37 @@ def test_gemm_grouped_rejects_bad_arguments_on_host(L):
     assert f(with_field("scale_b", None), 2, None) == 1
     assert f(with_field("c", None), 2, None) == 1
     assert f(with_field("b", FAKE_MIS), 2, None) == 2
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """The ctypes mirrors of f8_linear_saved and f8_gemm_problem have the
+    size and field offsets that a C compiler gives the header's structs
+    (compiled here against include/f8.h; no CUDA headers needed)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    from float8_mixed_precision_gb300.binding import _GemmProblem, _Saved
+    structs = {"f8_linear_saved": _Saved, "f8_gemm_problem": _GemmProblem}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "f8.h"', "int main(void) {"]
+    for cname, cls in structs.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for field, _ in cls._fields_:
+            lines.append(f'printf("{cname} {field} %zu\\n", offsetof({cname}, {field}));')
+    lines.append('printf("f8_format size %zu\\n", sizeof(f8_format));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)],
+                   check=True)
+    got = {}
+    for ln in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines():
+        name, field, value = ln.split()
+        got[(name, field)] = int(value)
+    for cname, cls in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for field, _ in cls._fields_:
+            assert got[(cname, field)] == getattr(cls, field).offset, (cname, field)
+    assert got[("f8_format", "size")] == ctypes.sizeof(ctypes.c_int)
