@@ -10,16 +10,22 @@
 namespace f8 {
 namespace swiglu {
 
-// ---- the SwiGLU input of the w2 linear, h = bf16(silu(a) * b).  exp(x)
-// is Cody and Waite's range reduction (x = n ln2 + r, ln2 split into a head
-// exact in fp32 and a tail) with the degree-7 Taylor polynomial of exp(r) in
-// Horner form, scaled by 2^n; silu(a) = a * (1 / (1 + exp(-a))) with the
-// correctly rounded reciprocal.  Every step is one IEEE fp32 operation with
-// round-to-nearest-even, so the bits are those of the same steps on any IEEE
-// machine.  Two elements go through each packed fp32x2 instruction (per lane
-// the numerics of the scalar _rn operation).  n = rint(x log2e) is taken as
+// ---- the SwiGLU input of the w2 linear, h = bf16(silu(a) * b), and its
+// gradient, evaluated in fp32 to within one bf16 ulp of the definition
+// (silu(a) = a / (1 + exp(-a)) and its derivative in exact arithmetic,
+// rounded once to bf16).  exp(x) is Cody and Waite's range reduction
+// (x = n ln2 + r, ln2 split into a head exact in fp32 and a tail) with the
+// degree-7 Taylor polynomial of exp(r) in Horner form, scaled by 2^n;
+// silu(a) = a * (1 / (1 + exp(-a))) with the correctly rounded reciprocal.
+// Two elements go through each packed fp32x2 instruction (per lane the
+// numerics of the scalar _rn operation).  n = rint(x log2e) is taken as
 // (p + 1.5 2^23) - 1.5 2^23, exact round-to-nearest-even for |p| < 2^22, and
 // 2^n is read off the low mantissa bits of the rounded sum.
+// Below a = -87, sigma(a) = e^a / (1 + e^a) rounds to e^a in fp32 and falls
+// into fp32's subnormal range, where forming it would lose the bits that
+// a sigma(a) b (a bf16 normal down to a = -92) still needs: there e^a =
+// p 2^n is applied as 2^(n+64) before the products and 2^-64 after them
+// (neg_tail), so every intermediate stays a normal fp32.
 __device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
 
 __device__ __forceinline__ float exp_special(float x, float e)
@@ -91,6 +97,36 @@ __device__ __forceinline__ float2 rcp2_refined(float2 d)
     return make_float2(fix_all_ones(d.x, y.x), fix_all_ones(d.y, y.y));
 }
 
+// For a in [-110, -87): p 2^(n + 64) with e^a = p 2^n (n in [-159, -125],
+// so 2^(n + 64) is a normal fp32).  Below -110, e^a < 2^-158 and 0 is
+// returned: every product that uses it is then a signed zero (or NaN for an
+// infinite factor), as the definition's is after rounding.
+__device__ __forceinline__ float neg_tail_exp_scaled(float a)
+{
+    if (a < -110.0f)
+        return 0.0f;
+    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+    const float t = __fadd_rn(__fmul_rn(a, 1.44269502f), kRound);
+    const float n = __fadd_rn(t, -kRound);
+    float r = __fmaf_rn(-n, 0.693145751953125f, a);
+    r = __fmaf_rn(-n, 1.42860677e-06f, r);
+    float q = __fmaf_rn(0x1.a01a02p-13f, r, 0x1.6c16c2p-10f);
+    q = __fmaf_rn(q, r, 0x1.111112p-7f);
+    q = __fmaf_rn(q, r, 0x1.555556p-5f);
+    q = __fmaf_rn(q, r, 0x1.555556p-3f);
+    q = __fmaf_rn(q, r, 0.5f);
+    q = __fmaf_rn(q, r, 1.0f);
+    q = __fmaf_rn(q, r, 1.0f);
+    const int ni = static_cast<int>(n);
+    return __fmul_rn(q, __int_as_float((ni + 64 + 127) << 23));
+}
+
+// h for a < -87: (a e^a b), e^a applied as 2^(n+64) p, then 2^-64.
+__device__ __forceinline__ float neg_tail_h(float a, float b)
+{
+    return __fmul_rn(__fmul_rn(__fmul_rn(a, neg_tail_exp_scaled(a)), b), 0x1p-64f);
+}
+
 // two packed bf16 of a and of b -> two packed bf16 of h.  kChecked = false
 // requires |a| <= 87 in both lanes: exp needs no special values and
 // 1 + exp(-a) lies in [1, 2^126), the refined reciprocal's range.
@@ -102,7 +138,13 @@ __device__ __forceinline__ uint32_t swiglu_x2(uint32_t a, uint32_t b)
     const float2 e = exp_cw2<kChecked>(make_float2(-fa.x, -fa.y));
     const float2 d = __fadd2_rn(splat(1.0f), e);
     const float2 r = kChecked ? make_float2(__frcp_rn(d.x), __frcp_rn(d.y)) : rcp2_refined(d);
-    const float2 hf = __fmul2_rn(__fmul2_rn(fa, r), fb);
+    float2 hf = __fmul2_rn(__fmul2_rn(fa, r), fb);
+    if (kChecked) {
+        if (fa.x < -87.0f)
+            hf.x = neg_tail_h(fa.x, fb.x);
+        if (fa.y < -87.0f)
+            hf.y = neg_tail_h(fa.y, fb.y);
+    }
     const __nv_bfloat162 h = __floats2bfloat162_rn(hf.x, hf.y);
     return *reinterpret_cast<const uint32_t *>(&h);
 }
@@ -124,10 +166,13 @@ __device__ __forceinline__ uint32_t fold_abs(uint32_t m, uint4 a)
 
 __device__ __forceinline__ bool small87(uint32_t m) { return __vcmpgtu2(m, 0x42AE42AEu) == 0; }
 
-// The gradient of swiglu_x2's h for two packed bf16 lanes of the upstream
+// The gradient of h = silu(a) b for two packed bf16 lanes of the upstream
 // gradient dh: db = bf16(dh s) with s = a sigma, and da = bf16((dh b) ds)
 // with ds = sigma fma(a, 1 - sigma, 1) = silu'(a); sigma as in the forward.
-// Each step one fp32 operation, as written.  kChecked as for swiglu_x2.
+// Below a = -87 (kChecked only), sigma = e^a and 1 - sigma = 1 in fp32, so
+// db = (a e^a) dh and da = ((1 + a) e^a) (dh b), with e^a applied as in
+// neg_tail_h.  dh b is formed first in every case (exact in fp32 for
+// bf16 factors unless it leaves fp32's range).
 template <bool kChecked>
 __device__ __forceinline__ void swiglu_bwd_x2(uint32_t dh, uint32_t a, uint32_t b, uint32_t &da,
                                               uint32_t &db)
@@ -138,10 +183,23 @@ __device__ __forceinline__ void swiglu_bwd_x2(uint32_t dh, uint32_t a, uint32_t 
     const float2 e = exp_cw2<kChecked>(make_float2(-fa.x, -fa.y));
     const float2 d = __fadd2_rn(splat(1.0f), e);
     const float2 sg = kChecked ? make_float2(__frcp_rn(d.x), __frcp_rn(d.y)) : rcp2_refined(d);
-    const float2 vdb = __fmul2_rn(fd, __fmul2_rn(fa, sg));
+    float2 vdb = __fmul2_rn(fd, __fmul2_rn(fa, sg));
     const float2 t = __fadd2_rn(splat(1.0f), make_float2(-sg.x, -sg.y));
     const float2 ds = __fmul2_rn(sg, __ffma2_rn(fa, t, splat(1.0f)));
-    const float2 vda = __fmul2_rn(__fmul2_rn(fd, fb), ds);
+    const float2 g = __fmul2_rn(fd, fb);
+    float2 vda = __fmul2_rn(g, ds);
+    if (kChecked) {
+        if (fa.x < -87.0f) {
+            const float s = neg_tail_exp_scaled(fa.x);
+            vdb.x = __fmul_rn(__fmul_rn(__fmul_rn(fa.x, s), fd.x), 0x1p-64f);
+            vda.x = __fmul_rn(__fmul_rn(__fmul_rn(__fadd_rn(1.0f, fa.x), s), g.x), 0x1p-64f);
+        }
+        if (fa.y < -87.0f) {
+            const float s = neg_tail_exp_scaled(fa.y);
+            vdb.y = __fmul_rn(__fmul_rn(__fmul_rn(fa.y, s), fd.y), 0x1p-64f);
+            vda.y = __fmul_rn(__fmul_rn(__fmul_rn(__fadd_rn(1.0f, fa.y), s), g.y), 0x1p-64f);
+        }
+    }
     const __nv_bfloat162 ha = __floats2bfloat162_rn(vda.x, vda.y);
     const __nv_bfloat162 hb = __floats2bfloat162_rn(vdb.x, vdb.y);
     da = *reinterpret_cast<const uint32_t *>(&ha);

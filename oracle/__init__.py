@@ -100,10 +100,8 @@ def _load():
         lib.or_gemm_rows_fmt.argtypes = [u8p, ctypes.c_int, u8p, ctypes.c_int, i64, i64, i64, f32, f32,
                                          i64p, i64, u16p]
         lib.or_gemm_rows_fmt.restype = None
-        lib.or_exp_cw.argtypes = [f32]
-        lib.or_exp_cw.restype = f32
-        lib.or_silu.argtypes = [f32]
-        lib.or_silu.restype = f32
+        lib.or_silu.argtypes = [ctypes.c_double]
+        lib.or_silu.restype = ctypes.c_double
         lib.or_swiglu_h.argtypes = [u16p, u16p, i64, u16p]
         lib.or_swiglu_h.restype = None
         lib.or_swiglu_bwd.argtypes = [u16p, u16p, u16p, i64, u16p, u16p]
@@ -271,17 +269,14 @@ def gemm_cols(a_q, b_q, sa, sb, cols) -> np.ndarray:
     return out
 
 
-def exp_cw(x: float) -> float:
-    return float(_load().or_exp_cw(float(np.float32(x))))
-
-
 def silu(x: float) -> float:
-    return float(_load().or_silu(float(np.float32(x))))
+    """silu(x) = x / (1 + exp(-x)) in fp64."""
+    return float(_load().or_silu(float(x)))
 
 
 def swiglu_h(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
-    """bf16 bits of h = bf16(silu(a) * b) (fp32 arithmetic, exp by Cody-Waite
-    reduction + degree-7 Taylor polynomial)."""
+    """bf16 bits of h = bf16(silu(a) * b): the product formed in fp64 from the
+    bf16 inputs and rounded once to bf16."""
     a = _u16(a_bits)
     b = _u16(b_bits)
     assert a.shape == b.shape
@@ -292,9 +287,10 @@ def swiglu_h(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
 
 
 def swiglu_bwd(dh_bits: np.ndarray, a_bits: np.ndarray, b_bits: np.ndarray):
-    """bf16 bits of (da, db), the gradient of h = bf16(silu(a) * b) for an
-    upstream dh: db = bf16(dh * silu(a)), da = bf16(dh * b * silu'(a)) with
-    silu'(a) = sigma (1 + a (1 - sigma)), fp32 steps as in or_swiglu_bwd."""
+    """bf16 bits of (da, db), the gradient of h = silu(a) * b for an upstream
+    dh: db = bf16(dh * silu(a)), da = bf16(dh * b * silu'(a)) with
+    silu'(a) = sigma (1 + a (1 - sigma)), each formed in fp64 and rounded
+    once to bf16."""
     dh, a, b = _u16(dh_bits), _u16(a_bits), _u16(b_bits)
     assert dh.shape == a.shape == b.shape
     da = np.empty(a.shape, np.uint16)

@@ -483,107 +483,53 @@ void or_gemm_rows_fmt(const uint8_t *a, int fa, const uint8_t *b, int fb, int64_
 /* ------------------------------------------------------------------------ */
 
 /*
- * exp(x) in fp32 by Cody and Waite's range reduction (x = n ln2 + r with ln2
- * split into a head exact in fp32 and a tail, |r| <= ln2/2) and the Taylor
- * polynomial of degree 7 of exp(r) in Horner form, scaled by 2^n.  Every
- * step is one IEEE fp32 operation (fmaf, add, multiply, round to integer),
- * so any IEEE fp32 machine that performs the same steps gets the same bits.
- * Error below 2 ulp over the finite range.
+ * The pages name the SwiGLU FFN of Llama 3.1 (the ablation table's model)
+ * but print no arithmetic for it, so the oracle takes the definition itself:
+ * silu(a) = a / (1 + exp(-a)) = a * sigma(a), with h = silu(a) * b, each
+ * formed in fp64 from the exact bf16 inputs (libm exp) and rounded once to
+ * bf16.  fp64 carries 29 more bits than the bf16 result needs, so this is
+ * the correctly rounded h except within ~2^-50 (relative) of a bf16
+ * rounding boundary.  exp(-a) overflows fp64 only for a < -709, where
+ * a / inf gives the correctly signed zero (and -inf / inf the NaN of
+ * -inf * sigma(-inf) = -inf * 0).
  */
-static float f32_exp_cw(float x)
+double or_silu(double a)
 {
-    if (isnan(x))
-        return x;
-    if (x > 88.0f)
-        return INFINITY;
-    if (x < -87.0f)
-        return 0.0f;
-    const float log2e = 1.44269502f;        /* fp32(1/ln 2) */
-    const float ln2_hi = 0.693145751953125f; /* ln 2 to 16 bits: n * ln2_hi is exact */
-    const float ln2_lo = 1.42860677e-06f;    /* fp32(ln 2 - ln2_hi) */
-    const float n = nearbyintf(x * log2e);
-    float r = fmaf(-n, ln2_hi, x);
-    r = fmaf(-n, ln2_lo, r);
-    /* 1/k! rounded to fp32: 1/5040, 1/720, 1/120, 1/24, 1/6 */
-    float p = 0x1.a01a02p-13f;
-    p = fmaf(p, r, 0x1.6c16c2p-10f);
-    p = fmaf(p, r, 0x1.111112p-7f);
-    p = fmaf(p, r, 0x1.555556p-5f);
-    p = fmaf(p, r, 0x1.555556p-3f);
-    p = fmaf(p, r, 0.5f);
-    p = fmaf(p, r, 1.0f);
-    p = fmaf(p, r, 1.0f);
-    /* 2^n for n in [-126, 127] as an fp32 bit pattern */
-    const int ni = (int)n;
-    uint32_t bits = (uint32_t)(ni + 127) << 23;
-    float two_n;
-    memcpy(&two_n, &bits, sizeof two_n);
-    return p * two_n;
+    return a / (1.0 + exp(-a));
 }
 
-float or_exp_cw(float x) { return f32_exp_cw(x); }
-
-/* silu(a) = a * (1 / (1 + exp(-a))), each step one fp32 operation (the
- * reciprocal is the correctly rounded 1/d, then one multiply). */
-float or_silu(float a)
-{
-    const float e = f32_exp_cw(-a);
-    const float d = 1.0f + e;
-    const float r = 1.0f / d;
-    return a * r;
-}
-
-/* RNE fp32 -> bf16 (bit patterns); NaN stays NaN. */
-static uint16_t f32_to_bf16(float f)
-{
-    uint32_t u;
-    memcpy(&u, &f, sizeof u);
-    if ((u & 0x7FFFFFFFu) > 0x7F800000u)
-        return (uint16_t)((u >> 16) | 0x40);
-    const uint32_t lsb = (u >> 16) & 1u;
-    u += 0x7FFFu + lsb;
-    return (uint16_t)(u >> 16);
-}
-
-/* h = bf16(fl32(silu(fp32(a)) * fp32(b))) elementwise over n values. */
+/* h = bf16(silu(a) * b) elementwise over n values, in fp64. */
 void or_swiglu_h(const uint16_t *a, const uint16_t *b, int64_t n, uint16_t *h)
 {
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i) {
-        const float s = or_silu(or_bf16_to_f32(a[i]));
-        h[i] = f32_to_bf16(s * or_bf16_to_f32(b[i]));
+        const double fa = (double)or_bf16_to_f32(a[i]);
+        const double fb = (double)or_bf16_to_f32(b[i]);
+        h[i] = or_f64_to_bf16(or_silu(fa) * fb);
     }
 }
 
-/* The gradient of h = bf16(silu(a) * b) (the step above) for an upstream
- * gradient dh, elementwise over n values, each step one fp32 operation:
- *   sigma = 1 / (1 + exp(-a))      (as in or_silu: correctly rounded reciprocal)
- *   s     = a * sigma              (silu(a), as in the forward)
- *   db    = bf16(dh * s)           (d h / d b = silu(a))
- *   t     = 1 - sigma
- *   w     = fma(a, t, 1)           (one rounding: 1 + a (1 - sigma))
- *   ds    = sigma * w              (silu'(a) = sigma (1 + a (1 - sigma)))
- *   g     = dh * b                 (the gradient reaching silu(a))
- *   da    = bf16(g * ds)
+/*
+ * The gradient of h = silu(a) * b for an upstream gradient dh, elementwise
+ * over n values, from the derivative of the definition above:
+ *   sigma    = 1 / (1 + exp(-a))
+ *   dh/db    = silu(a) = a sigma
+ *   dh/da    = b silu'(a),   silu'(a) = sigma (1 + a (1 - sigma))
+ *   db = bf16(dh * a * sigma),  da = bf16(dh * b * silu'(a))
+ * all in fp64, each output rounded once to bf16.
  */
 void or_swiglu_bwd(const uint16_t *dh, const uint16_t *a, const uint16_t *b, int64_t n,
                    uint16_t *da, uint16_t *db)
 {
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i) {
-        const float fa = or_bf16_to_f32(a[i]);
-        const float fb = or_bf16_to_f32(b[i]);
-        const float fdh = or_bf16_to_f32(dh[i]);
-        const float e = f32_exp_cw(-fa);
-        const float d = 1.0f + e;
-        const float sigma = 1.0f / d;
-        const float s = fa * sigma;
-        db[i] = f32_to_bf16(fdh * s);
-        const float t = 1.0f - sigma;
-        const float w = fmaf(fa, t, 1.0f);
-        const float ds = sigma * w;
-        const float g = fdh * fb;
-        da[i] = f32_to_bf16(g * ds);
+        const double fa = (double)or_bf16_to_f32(a[i]);
+        const double fb = (double)or_bf16_to_f32(b[i]);
+        const double fdh = (double)or_bf16_to_f32(dh[i]);
+        const double sigma = 1.0 / (1.0 + exp(-fa));
+        const double dsilu = sigma * (1.0 + fa * (1.0 - sigma));
+        db[i] = or_f64_to_bf16(fdh * (fa * sigma));
+        da[i] = or_f64_to_bf16(fdh * fb * dsilu);
     }
 }
 
