@@ -160,7 +160,100 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi, 100 ms"}
+
+
+class NvmlClockSampler:
+    """SM clock, clock-event reasons and power read through NVML (libnvidia-ml,
+    read-only queries) every `period_s` by a thread while the timed region
+    runs: a region of tens of milliseconds gets tens of samples, where
+    nvidia-smi's 100 ms loop gives one.  Falls back to ClockSampler if NVML
+    cannot be loaded or the device cannot be found."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_index: int, period_s: float = 0.002):
+        self.gpu = gpu_index
+        self.period = period_s
+        self.samples = []
+        self.fallback = None
+        self.nvml = None
+        self.max_mhz = None
+
+    def _open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        found = False
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(self.gpu).uuid)
+            name = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            found = lib.nvmlDeviceGetHandleByUUID(name.encode(), ctypes.byref(h)) == 0
+        except Exception:
+            found = False
+        if not found and lib.nvmlDeviceGetHandleByIndex_v2(self.gpu, ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1 = NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        self.nvml, self.h, self.ct = lib, h, ctypes
+
+    def _run(self):
+        ct, lib, h = self.ct, self.nvml, self.h
+        clk, rs, mw = ct.c_uint(), ct.c_ulonglong(), ct.c_uint()
+        while not self.stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) == 0:
+                r = rs.value if self.reason_fn(h, ct.byref(rs)) == 0 else 0
+                p = mw.value / 1000.0 if lib.nvmlDeviceGetPowerUsage(h, ct.byref(mw)) == 0 else None
+                self.samples.append((float(clk.value), int(r), p))
+            self.stop.wait(self.period)
+
+    def __enter__(self):
+        try:
+            self._open()
+        except Exception:
+            self.fallback = ClockSampler(self.gpu).__enter__()
+            return self
+        self.stop = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.fallback is not None:
+            return self.fallback.__exit__(*exc)
+        self.stop.set()
+        self.thread.join(timeout=2)
+
+    def summary(self):
+        if self.fallback is not None:
+            return self.fallback.summary()
+        sm = [c for c, _, _ in self.samples]
+        reasons = set()
+        for _, r, _ in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        power = [p for _, _, p in self.samples if p is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(sm) if sm else None, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None,
+                "source": f"NVML, every {self.period * 1e3:g} ms"}
+
+
+def fp8_peak_for(seconds: float, peaks: dict) -> tuple[float, str]:
+    """The FP8 dense peak a rate measured over a region of `seconds` is held
+    to: the measured bf16 GEMM peak x 2 (the FP8 : BF16 dense ratio), burst
+    for a region shorter than a second, sustained (the power-capped
+    seconds-long loop) otherwise."""
+    if seconds < 1.0:
+        return peaks["bf16_tflops"] * FP8_PER_BF16, "burst"
+    return peaks["bf16_tflops_sustained"] * FP8_PER_BF16, "sustained"
 
 
 # ------------------------------------------------------------------ our arm
@@ -194,6 +287,22 @@ class Linear8:
         self.dyt = torch.empty((N, M), dtype=torch.uint8, device=device)
         self.dys = torch.empty(2, dtype=torch.float32, device=device)
         self.qws = torch.empty(f8.f8_quantize_workspace_bytes(), dtype=torch.uint8, device=device)
+
+    @property
+    def lins(self):
+        return [self.lin]
+
+    def inputs(self):
+        """Device tensors a step reads (filled from the host in the e2e run)."""
+        return [self.x, self.w, self.dy]
+
+    def outputs(self):
+        """Device tensors a step writes (read back in the e2e run)."""
+        return [self.y, self.dx, self.dw]
+
+    def iso_items(self):
+        """(linear, X, W, dY) of each linear, for the isolated kernel timings."""
+        return [(self.lin, self.x, self.w, self.dy)]
 
     def step(self, f8):
         if self.swiglu == "fused":
@@ -235,6 +344,79 @@ class Linear8:
         ev("gemm", 4 * M * N * K, lambda: f8.f8_gemm_grouped(
             [(self.dyq, s.w_t, self.dys[1], s.scale_w, self.dx, self.dy_fmt),
              (self.dyt, s.x_t, self.dys[1], s.scale_x, self.dw, self.dy_fmt)]))
+
+
+class GroupLinear8:
+    """Linears that read one input X (q, k, v; w1, w3) as one group:
+    f8_linear_fwd_group quantises X once and every W_i with its own scale
+    (two launches for all of them), then runs the members' GEMMs under the
+    grouped-launch planner; f8_linear_bwd_group quantises every dY_i (two
+    launches) and runs the members' dgrad and wgrad GEMMs the same way.
+    Every output is bit-identical to f8_linear_fwd / f8_linear_bwd on that
+    member with the same X."""
+
+    def __init__(self, f8, lins, x, ws, dys, device, dy_fmt=0):
+        import torch
+        self.members = lins
+        self.dy_fmt = dy_fmt
+        M, K = lins[0].M, lins[0].K
+        self.M, self.K = M, K
+        self.Ns = [l.N for l in lins]
+        self.lin = type(lins[0])("+".join(l.name for l in lins), M, K, sum(self.Ns))
+        self.x = x.to(device)
+        self.w = [w.to(device) for w in ws]
+        self.dy = [d.to(device) for d in dys]
+        self.y = [torch.empty((M, N), dtype=torch.bfloat16, device=device) for N in self.Ns]
+        self.dx = [torch.empty((M, K), dtype=torch.bfloat16, device=device) for _ in self.Ns]
+        self.dw = [torch.empty((N, K), dtype=torch.bfloat16, device=device) for N in self.Ns]
+        self.saved = f8.group_saved(M, K, self.Ns, device)
+        self.ws = f8.group_workspace(M, K, self.Ns, device)
+        # the decomposed path (same kernels, one C call per phase) for per-phase timing
+        self.xq = torch.empty((M, K), dtype=torch.uint8, device=device)
+        self.wq = [torch.empty((N, K), dtype=torch.uint8, device=device) for N in self.Ns]
+        self.dyq = [torch.empty((M, N), dtype=torch.uint8, device=device) for N in self.Ns]
+        self.dyt = [torch.empty((N, M), dtype=torch.uint8, device=device) for N in self.Ns]
+        self.dys = [torch.empty(2, dtype=torch.float32, device=device) for _ in self.Ns]
+        self.qws = torch.empty(f8.f8_quantize_multi_workspace_bytes(), dtype=torch.uint8,
+                               device=device)
+
+    @property
+    def lins(self):
+        return list(self.members)
+
+    def inputs(self):
+        return [self.x] + self.w + self.dy
+
+    def outputs(self):
+        return self.y + self.dx + self.dw
+
+    def iso_items(self):
+        return [(l, self.x, w, dy) for l, w, dy in zip(self.members, self.w, self.dy)]
+
+    def step(self, f8):
+        f8.f8_linear_fwd_group(self.x, self.w, ys=self.y, saved=self.saved, ws=self.ws)
+        f8.f8_linear_bwd_group(self.dy, self.saved, self.K, dxs=self.dx, dws=self.dw, ws=self.ws,
+                               fmt=self.dy_fmt)
+
+    def step_timed(self, f8, ev):
+        s = self.saved
+        M, K = self.M, self.K
+        xs = s[0].x_scalars
+        outs = [(self.xq, s[0].x_t, xs[1], xs[0])] + [
+            (wq, si.w_t, si.scalars[3], si.scalars[2]) for wq, si in zip(self.wq, s)]
+        ev("quantize", 4 * (self.x.numel() + sum(w.numel() for w in self.w)),
+           lambda: f8.f8_quantize_multi([self.x] + self.w, outs=outs, ws=self.qws))
+        ev("gemm", sum(2 * M * N * K for N in self.Ns), lambda: f8.f8_gemm_grouped(
+            [(self.xq, wq, xs[1], si.scalars[3], y) for wq, si, y in zip(self.wq, s, self.y)]))
+        douts = [(q, t, d[1], d[0]) for q, t, d in zip(self.dyq, self.dyt, self.dys)]
+        ev("quantize", 4 * sum(d.numel() for d in self.dy),
+           lambda: f8.f8_quantize_multi(self.dy, fmt=self.dy_fmt, outs=douts, ws=self.qws))
+        probs = []
+        for i in range(len(self.Ns)):
+            probs.append((self.dyq[i], s[i].w_t, self.dys[i][1], s[i].scalars[3], self.dx[i],
+                          self.dy_fmt))
+            probs.append((self.dyt[i], s[i].x_t, self.dys[i][1], xs[1], self.dw[i], self.dy_fmt))
+        ev("gemm", sum(4 * M * N * K for N in self.Ns), lambda: f8.f8_gemm_grouped(probs))
 
 
 class FfnIn8(Linear8):
@@ -325,9 +507,51 @@ class W2Q8(Linear8):
             self.src.bwd_from_dh_timed(f8, ev, self.dx)
 
 
+def describe_workload(wl, args):
+    """The workload's name and the linears one step runs (as build_layers
+    makes them), from the arguments alone: both arms print it as `config`."""
+    name, lins = wl.workload(args.config)
+    if args.swiglu_input in ("epilogue", "chain"):
+        if args.config not in wl.SHARED_INPUT_GROUPS:
+            raise SystemExit("--swiglu-input epilogue needs a workload with a SwiGLU FFN (3, 4, 5)")
+        chain = args.swiglu_input == "chain"
+        return (name + " (shared inputs fused; w2 input silu(a) * b from the w1+w3 GEMM epilogue"
+                + ("; dY of w1+w3 from the SwiGLU backward of dX of w2)" if chain else ")"),
+                [g for g, _ in wl.fused_groups(args.config)])
+    if args.fuse_shared_inputs:
+        groups = [g for g, _ in wl.fused_groups(args.config)]
+        name += " (shared inputs fused: " + ", ".join(g.name for g in groups) + ")"
+        lins = groups
+    elif use_groups(wl, args):
+        name += (" (linears that share X as groups: " +
+                 ", ".join("+".join(g) for g in wl.SHARED_INPUT_GROUPS[args.config] if len(g) > 1) +
+                 "; X quantised once, one scale per tensor)")
+    if args.swiglu_input != "given" and any(l.x_kind == "swiglu" for l in lins):
+        name += f" (w2 input: silu(a) * b, {args.swiglu_input})"
+    return name, lins
+
+
+def use_groups(wl, args) -> bool:
+    """Whether the step runs the linears that share X as groups
+    (f8_linear_fwd_group / f8_linear_bwd_group)."""
+    return (args.groups and args.config in wl.SHARED_INPUT_GROUPS and not args.fuse_shared_inputs
+            and args.swiglu_input == "given")
+
+
+def config_dict(wl, args, world):
+    name, lins = describe_workload(wl, args)
+    return {"workload": name,
+            "linears": [f"{l.name} M={l.M} K={l.K} N={l.N}" for l in lins],
+            "flops_per_step": sum(l.flops for l in lins),
+            "parallelism": "replicas" if world > 1 else "single-gpu",
+            "l2": "no flush: a step's inputs exceed L2",
+            "launch": "one captured CUDA graph per step" if args.graph else "call by call"}
+
+
 def build_layers(f8, wl, args, device, dy_fmt):
     """The workload's linears as layer objects, and the workload's name."""
-    name, lins = wl.workload(args.config)
+    name, _ = describe_workload(wl, args)
+    lins = wl.workload(args.config)[1]
     if args.swiglu_input in ("epilogue", "chain"):
         chain = args.swiglu_input == "chain"
         if args.config not in wl.SHARED_INPUT_GROUPS:
@@ -345,8 +569,21 @@ def build_layers(f8, wl, args, device, dy_fmt):
                                       dy_fmt))
         if ffn is None:
             raise SystemExit("--swiglu-input epilogue needs a workload with a SwiGLU FFN (3, 4, 5)")
-        return (name + " (shared inputs fused; w2 input silu(a) * b from the w1+w3 GEMM epilogue"
-                + ("; dY of w1+w3 from the SwiGLU backward of dX of w2)" if chain else ")")), layers
+        return name, layers
+    if use_groups(wl, args):
+        by_name = {l.name: i for i, l in enumerate(lins)}
+        layers = []
+        for names in wl.SHARED_INPUT_GROUPS[args.config]:
+            idx = [by_name[n] for n in names]
+            if len(idx) == 1:
+                layers.append(Linear8(f8, lins[idx[0]], wl.linear_inputs(args.config, idx[0]),
+                                      device, dy_fmt))
+                continue
+            ins = [wl.linear_inputs(args.config, i) for i in idx]
+            layers.append(GroupLinear8(f8, [lins[i] for i in idx], ins[0]["x"],
+                                       [d["w"] for d in ins], [d["dy"] for d in ins], device,
+                                       dy_fmt))
+        return name, layers
     if args.fuse_shared_inputs:
         layers = []
         for g, idx in wl.fused_groups(args.config):
@@ -354,15 +591,12 @@ def build_layers(f8, wl, args, device, dy_fmt):
                   else None)
             layers.append(Linear8(f8, g, wl.fused_group_inputs(args.config, idx), device, dy_fmt,
                                   sw, wl.swiglu_ab(args.config, idx[0]) if sw else None))
-        name += " (shared inputs fused: " + ", ".join(L.lin.name for L in layers) + ")"
     else:
         layers = []
         for i, lin in enumerate(lins):
             sw = args.swiglu_input if (lin.x_kind == "swiglu" and args.swiglu_input != "given") else None
             layers.append(Linear8(f8, lin, wl.linear_inputs(args.config, i), device, dy_fmt, sw,
                                   wl.swiglu_ab(args.config, i) if sw else None))
-    if any(L.swiglu for L in layers):
-        name += f" (w2 input: silu(a) * b, {args.swiglu_input})"
     return name, layers
 
 
@@ -377,7 +611,7 @@ def run_ours(args, world, rank, local):
     f8.lib()
     dy_fmt = f8.F8_E5M2 if args.dy_format == "e5m2" else f8.F8_E4M3
     name, layers = build_layers(f8, wl, args, device, dy_fmt)
-    lins = [L.lin for L in layers]
+    lins = [l for L in layers for l in L.lins]
     flops_step = sum(l.flops for l in lins)
     stream = torch.cuda.current_stream()
 
@@ -412,7 +646,8 @@ def run_ours(args, world, rank, local):
     barrier()
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
+    busy_t0 = time.perf_counter()
+    with NvmlClockSampler(local) as clocks:
         t0.record(stream)
         for _ in range(args.steps):
             if graph is not None:
@@ -462,7 +697,10 @@ def run_ours(args, world, rank, local):
         d["work"] += work
     tot_ms = sum(d["ms"] for d in per.values())
     peaks = load_peaks()
-    fp8_peak = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+    # the GPU has been busy from the start of the timed region to here: the
+    # burst peak applies to a region under a second, the sustained one beyond
+    busy_s = time.perf_counter() - busy_t0
+    fp8_peak, regime = fp8_peak_for(busy_s, peaks)
     kernels = {}
     for kind, d in per.items():
         rate = d["work"] / (d["ms"] * 1e-3)
@@ -472,6 +710,7 @@ def run_ours(args, world, rank, local):
             e.update({"gbs": rate / 1e9})
         elif kind == "gemm":
             e.update({"tflops": rate / 1e12, "frac_of_fp8_measured": rate / 1e12 / fp8_peak,
+                      "fp8_peak_regime": regime,
                       "frac_of_fp8_nominal": rate / 1e12 / FP8_NOMINAL_TFLOPS})
         else:
             e.update({"gbs": rate / 1e9, "frac_of_hbm_measured": rate / 1e9 / peaks["hbm_gbs"]})
@@ -481,7 +720,14 @@ def run_ours(args, world, rank, local):
     roofline = {"kernel": "gemm_kernel (tcgen05 kind::f8f6f4)", "bound": "tensor",
                 "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak,
-                "peak_note": f"{peaks['source']} bf16 sustained {peaks['bf16_tflops_sustained']} x {FP8_PER_BF16} (FP8:BF16 dense)",
+                "peak_regime": regime,
+                "peak_note": (f"{peaks['source']} bf16 {regime} "
+                              f"{peaks['bf16_tflops' if regime == 'burst' else 'bf16_tflops_sustained']}"
+                              f" x {FP8_PER_BF16} (FP8:BF16 dense); {regime} because the GPU was busy "
+                              f"{busy_s:.2f} s from the start of the timed region to the end of the "
+                              f"per-kernel replay (burst below 1 s)"),
+                "frac_of_burst": achieved / (peaks["bf16_tflops"] * FP8_PER_BF16),
+                "frac_of_sustained": achieved / (peaks["bf16_tflops_sustained"] * FP8_PER_BF16),
                 "frac_of_nominal_4500": achieved / FP8_NOMINAL_TFLOPS,
                 "traffic": (GEMM_TRAFFIC["bytes_per_step"]
                             if args.config == GEMM_TRAFFIC["workload"]
@@ -537,47 +783,57 @@ def kernel_bench(f8, layers, device, stream, iters=50):
     out = []
     seen = set()
     for L in layers:
-        s = L.saved
-        M, N, K = L.lin.M, L.lin.N, L.lin.K
-        for name, t in (("x", L.x), ("w", L.w), ("dy", L.dy)):
-            key = ("mem", tuple(t.shape))
-            if key in seen:
-                continue
-            seen.add(key)
-            amx = torch.empty((), dtype=torch.float32, device=device)
-            ms = timed(lambda: f8.f8_amax(t, amx))
-            out.append({"kernel": "amax", "tensor": f"{L.lin.name}.{name} {list(t.shape)}",
-                        "us": ms * 1e3, "gbs": 2 * t.numel() / ms / 1e6,
-                        "frac_of_hbm_measured": 2 * t.numel() / ms / 1e6 / peaks["hbm_gbs"]})
-            q = torch.empty(t.shape, dtype=torch.uint8, device=device)
-            qt = torch.empty((t.shape[1], t.shape[0]), dtype=torch.uint8, device=device)
-            sc = torch.empty((), dtype=torch.float32, device=device)
-            ms = timed(lambda: f8.f8_cast_transpose(t, amx, sc, q, qt))
-            out.append({"kernel": "cast_transpose", "tensor": f"{L.lin.name}.{name} {list(t.shape)}",
-                        "us": ms * 1e3, "gbs": 4 * t.numel() / ms / 1e6,
-                        "frac_of_hbm_measured": 4 * t.numel() / ms / 1e6 / peaks["hbm_gbs"]})
-            ws = torch.empty(f8.f8_quantize_workspace_bytes(), dtype=torch.uint8, device=device)
-            ms = timed(lambda: f8.f8_quantize(t, amx, sc, q, qt, ws))
-            out.append({"kernel": "quantize (amax + cast_transpose launches)",
-                        "tensor": f"{L.lin.name}.{name} {list(t.shape)}", "us": ms * 1e3,
-                        "gbs": 4 * t.numel() / ms / 1e6,
-                        "frac_of_hbm_measured": 4 * t.numel() / ms / 1e6 / peaks["hbm_gbs"],
-                        "note": "4 B/elem counted (2 read + 2 written); the cast's re-read is not"})
-            del q, qt, ws
-        for gname, (a, b, sa, sb, c, mm, nn, kk) in (
-                ("fwd", (L.xq, L.wq, s.scale_x, s.scale_w, L.y, M, N, K)),
-                ("dgrad", (L.dyq, s.w_t, L.dys[1], s.scale_w, L.dx, M, K, N)),
-                ("wgrad", (L.dyt, s.x_t, L.dys[1], s.scale_x, L.dw, N, K, M))):
-            key = ("gemm", mm, nn, kk)
-            if key in seen:
-                continue
-            seen.add(key)
-            fa = L.dy_fmt if gname != "fwd" else 0
-            ms = timed(lambda: f8.f8_gemm(a, b, sa, sb, c, fmt_a=fa))
-            tf = 2 * mm * nn * kk / ms / 1e9
-            out.append({"kernel": "gemm", "shape": f"{L.lin.name}.{gname} M={mm} N={nn} K={kk}",
-                        "us": ms * 1e3, "tflops": tf, "frac_of_fp8_measured_burst": tf / fp8_burst,
-                        "frac_of_fp8_nominal": tf / FP8_NOMINAL_TFLOPS})
+        for lin, x, w, dy in L.iso_items():
+            M, N, K = lin.M, lin.N, lin.K
+            dy_fmt = L.dy_fmt
+            amx = {}
+            ops = {}
+            for name, t in (("x", x), ("w", w), ("dy", dy)):
+                amx[name] = torch.empty((), dtype=torch.float32, device=device)
+                q = torch.empty(t.shape, dtype=torch.uint8, device=device)
+                qt = torch.empty((t.shape[1], t.shape[0]), dtype=torch.uint8, device=device)
+                sc = torch.empty((), dtype=torch.float32, device=device)
+                ws = torch.empty(f8.f8_quantize_workspace_bytes(), dtype=torch.uint8, device=device)
+                fmt = dy_fmt if name == "dy" else 0
+                f8.f8_quantize(t, amx[name], sc, q, qt, ws, fmt=fmt)   # operands for the GEMMs
+                ops[name] = (q, qt, sc)
+                key = ("mem", tuple(t.shape))
+                if key in seen:
+                    continue
+                seen.add(key)
+                a1 = amx[name]
+                ms = timed(lambda: f8.f8_amax(t, a1))
+                out.append({"kernel": "amax", "tensor": f"{lin.name}.{name} {list(t.shape)}",
+                            "us": ms * 1e3, "gbs": 2 * t.numel() / ms / 1e6,
+                            "frac_of_hbm_measured": 2 * t.numel() / ms / 1e6 / peaks["hbm_gbs"]})
+                ms = timed(lambda: f8.f8_cast_transpose(t, a1, sc, q, qt))
+                out.append({"kernel": "cast_transpose", "tensor": f"{lin.name}.{name} {list(t.shape)}",
+                            "us": ms * 1e3, "gbs": 4 * t.numel() / ms / 1e6,
+                            "frac_of_hbm_measured": 4 * t.numel() / ms / 1e6 / peaks["hbm_gbs"]})
+                ms = timed(lambda: f8.f8_quantize(t, a1, sc, q, qt, ws, fmt=fmt))
+                out.append({"kernel": "quantize (amax + cast_transpose launches)",
+                            "tensor": f"{lin.name}.{name} {list(t.shape)}", "us": ms * 1e3,
+                            "gbs": 4 * t.numel() / ms / 1e6,
+                            "frac_of_hbm_measured": 4 * t.numel() / ms / 1e6 / peaks["hbm_gbs"],
+                            "note": "4 B/elem counted (2 read + 2 written); the cast's re-read is not"})
+            (xq, xt, sx), (wq, wt, sw), (dyq, dyt, sdy) = ops["x"], ops["w"], ops["dy"]
+            for gname, (a, b, sa, sb, mm, nn, kk) in (
+                    ("fwd", (xq, wq, sx, sw, M, N, K)),
+                    ("dgrad", (dyq, wt, sdy, sw, M, K, N)),
+                    ("wgrad", (dyt, xt, sdy, sx, N, K, M))):
+                key = ("gemm", mm, nn, kk)
+                if key in seen:
+                    continue
+                seen.add(key)
+                fa = dy_fmt if gname != "fwd" else 0
+                c = torch.empty((mm, nn), dtype=torch.bfloat16, device=device)
+                ms = timed(lambda: f8.f8_gemm(a, b, sa, sb, c, fmt_a=fa))
+                tf = 2 * mm * nn * kk / ms / 1e9
+                out.append({"kernel": "gemm", "shape": f"{lin.name}.{gname} M={mm} N={nn} K={kk}",
+                            "us": ms * 1e3, "tflops": tf, "frac_of_fp8_measured_burst": tf / fp8_burst,
+                            "frac_of_fp8_nominal": tf / FP8_NOMINAL_TFLOPS})
+                del c
+            del ops
     del flush, clean
     return out
 
@@ -591,15 +847,11 @@ def run_e2e(f8, layers, args, device, stream, flops_step, world):
     host = []
     h2d = d2h = 0
     for L in layers:
-        hx = L.x.cpu().pin_memory()
-        hw = L.w.cpu().pin_memory()
-        hdy = L.dy.cpu().pin_memory()
-        hy = torch.empty(L.y.shape, dtype=torch.bfloat16).pin_memory()
-        hdx = torch.empty(L.dx.shape, dtype=torch.bfloat16).pin_memory()
-        hdw = torch.empty(L.dw.shape, dtype=torch.bfloat16).pin_memory()
-        host.append((hx, hw, hdy, hy, hdx, hdw))
-        h2d += 2 * (hx.numel() + hw.numel() + hdy.numel())
-        d2h += 2 * (hy.numel() + hdx.numel() + hdw.numel())
+        hin = [t.cpu().pin_memory() for t in L.inputs()]
+        hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in L.outputs()]
+        host.append((hin, hout))
+        h2d += sum(t.numel() * t.element_size() for t in hin)
+        d2h += sum(t.numel() * t.element_size() for t in hout)
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     n = len(layers)
     ev_in = [torch.cuda.Event() for _ in range(n)]
@@ -608,13 +860,12 @@ def run_e2e(f8, layers, args, device, stream, flops_step, world):
     first = [True] * n
 
     def step():
-        for i, (L, (hx, hw, hdy, hy, hdx, hdw)) in enumerate(zip(layers, host)):
+        for i, (L, (hin, hout)) in enumerate(zip(layers, host)):
             with torch.cuda.stream(s_in):
                 if not first[i]:
                     s_in.wait_event(ev_comp[i])      # last step's compute has read the inputs
-                L.x.copy_(hx, non_blocking=True)
-                L.w.copy_(hw, non_blocking=True)
-                L.dy.copy_(hdy, non_blocking=True)
+                for d, h in zip(L.inputs(), hin):
+                    d.copy_(h, non_blocking=True)
                 ev_in[i].record(s_in)
             stream.wait_event(ev_in[i])
             if not first[i]:
@@ -623,9 +874,8 @@ def run_e2e(f8, layers, args, device, stream, flops_step, world):
             ev_comp[i].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_comp[i])
-                hy.copy_(L.y, non_blocking=True)
-                hdx.copy_(L.dx, non_blocking=True)
-                hdw.copy_(L.dw, non_blocking=True)
+                for h, d in zip(hout, L.outputs()):
+                    h.copy_(d, non_blocking=True)
                 ev_out[i].record(s_out)
             first[i] = False
 
@@ -645,7 +895,7 @@ def run_e2e(f8, layers, args, device, stream, flops_step, world):
     ms = max_over_ranks(t0.elapsed_time(t1), world, device)
     total = sum_over_ranks(flops_step * args.e2e_steps, world, device)
     # the results really came back: spot-check one output against its device copy
-    ok = torch.equal(host[-1][5][:4].to(device), layers[-1].dw[:4])
+    ok = torch.equal(host[-1][1][-1][:4].to(device), layers[-1].outputs()[-1][:4])
     link = host_link_gbs(device, s_in, s_out)
     moved = (h2d + d2h) * args.e2e_steps / (ms * 1e-3) / 1e9
     return {"value": total / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -815,7 +1065,7 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": name, "linears": [l.name for l in lins], "M": lins[0].M},
+            "config": config_dict(wl, args, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -829,13 +1079,18 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5],
+                    help="workload (default 5: the full Llama-3.1-8B block, all seven linears)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-rows", type=int, default=8192)
     ap.add_argument("--ref-rows", type=int, default=128)
     ap.add_argument("--graph", type=int, default=1,
                     help="replay the step as one captured CUDA graph (1) or launch it call by call (0)")
+    ap.add_argument("--groups", type=int, default=1,
+                    help="run the linears that share X (q, k, v; w1, w3) as groups: X quantised "
+                         "once, one scale per tensor, GEMMs in shared launches (1, default) or "
+                         "every linear alone (0)")
     ap.add_argument("--fuse-shared-inputs", action="store_true",
                     help="merge the linears that read one input (q/k/v, w1/w3) into one linear "
                          "with the concatenated weight and a tensorwise scale over it")
@@ -870,19 +1125,14 @@ def main(argv=None):
         cpu = cpu_baseline(args.config, args.cpu_rows) if world == 1 else None
     r = run_ours(args, world, rank, local)
     if rank == 0:
-        lins = r["lins"]
+        from float8_mixed_precision_gb300 import workloads as wl
         line = {
             "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3" if args.dy_format == "e4m3" else "e4m3 (X, W) / e5m2 (dY)",
             "data": "synthetic (seeded; workloads.py)",
-            "config": {"workload": r["name"],
-                       "linears": [f"{l.name} M={l.M} K={l.K} N={l.N}" for l in lins],
-                       "flops_per_step": sum(l.flops for l in lins),
-                       "parallelism": "replicas" if world > 1 else "single-gpu",
-                       "l2": "no flush: a step's inputs exceed L2",
-                       "launch": "one captured CUDA graph per step" if args.graph else "call by call"},
+            "config": config_dict(wl, args, world),
             "pct_of_fp8_peak_nominal": 100 * r["value"] / FP8_NOMINAL_TFLOPS,
             "roofline": r["roofline"], "kernels": r["kernels"],
             "breakdown_ms_per_step": r["breakdown_ms_per_step"],

@@ -37,7 +37,13 @@ EXPORTS = ("f8_amax", "f8_cast_transpose", "f8_gemm", "f8_linear_workspace_bytes
            "f8_linear_bwd_fmt", "f8_quantize_swiglu", "f8_linear_fwd_swiglu",
            "f8_linear_fwd_w13_swiglu", "f8_gemm_w13_swiglu", "f8_linear_bwd_w13_swiglu",
            "f8_quantize_swiglu_bwd", "f8_kernel_launches", "f8_selftest_bounds",
-           "f8_gemm_grouped")
+           "f8_gemm_grouped", "f8_quantize_multi", "f8_quantize_multi_workspace_bytes",
+           "f8_linear_group_workspace_bytes", "f8_linear_fwd_group", "f8_linear_bwd_group",
+           "f8_transpose_u8", "f8_linear_fwd_qw", "f8_linear_fwd_qw_workspace_bytes")
+
+F8_MAX_GROUPED_GEMMS = 8
+F8_MAX_MULTI_TENSORS = 8
+F8_MAX_GROUP_LINEARS = 4
 
 F8_E4M3 = 0
 F8_E5M2 = 1
@@ -60,6 +66,18 @@ class _GemmProblem(ctypes.Structure):
                 ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("scale_a", ctypes.c_void_p),
                 ("scale_b", ctypes.c_void_p), ("c", ctypes.c_void_p), ("fmt_a", ctypes.c_int),
                 ("fmt_b", ctypes.c_int)]
+
+
+class _QuantTensor(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("amax_out", ctypes.c_void_p), ("scale_out", ctypes.c_void_p),
+                ("q", ctypes.c_void_p), ("q_t", ctypes.c_void_p)]
+
+
+class _GroupLinear(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int64), ("w", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("dy", ctypes.c_void_p), ("dx", ctypes.c_void_p), ("dw", ctypes.c_void_p),
+                ("saved", _Saved)]
 
 
 _lock = threading.Lock()
@@ -136,6 +154,26 @@ def lib() -> ctypes.CDLL:
         L.f8_linear_fwd_noalloc.restype = st
         L.f8_gemm_grouped.argtypes = [ctypes.POINTER(_GemmProblem), ctypes.c_int, vp]
         L.f8_gemm_grouped.restype = st
+        L.f8_quantize_multi_workspace_bytes.argtypes = []
+        L.f8_quantize_multi_workspace_bytes.restype = ctypes.c_size_t
+        L.f8_quantize_multi.argtypes = [ctypes.POINTER(_QuantTensor), ctypes.c_int, ctypes.c_int, vp,
+                                        ctypes.c_size_t, vp]
+        L.f8_quantize_multi.restype = st
+        L.f8_linear_group_workspace_bytes.argtypes = [i64, i64, ctypes.POINTER(i64), ctypes.c_int]
+        L.f8_linear_group_workspace_bytes.restype = ctypes.c_size_t
+        L.f8_linear_fwd_group.argtypes = [vp, i64, i64, ctypes.POINTER(_GroupLinear), ctypes.c_int, vp,
+                                          ctypes.c_size_t, vp]
+        L.f8_linear_fwd_group.restype = st
+        L.f8_linear_bwd_group.argtypes = [ctypes.POINTER(_GroupLinear), ctypes.c_int, i64, i64,
+                                          ctypes.c_int, vp, ctypes.c_size_t, vp]
+        L.f8_linear_bwd_group.restype = st
+        L.f8_transpose_u8.argtypes = [vp, i64, i64, vp, vp]
+        L.f8_transpose_u8.restype = st
+        L.f8_linear_fwd_qw_workspace_bytes.argtypes = [i64, i64]
+        L.f8_linear_fwd_qw_workspace_bytes.restype = ctypes.c_size_t
+        L.f8_linear_fwd_qw.argtypes = [vp, vp, i64, i64, i64, vp, ctypes.POINTER(_Saved), vp,
+                                       ctypes.c_size_t, vp]
+        L.f8_linear_fwd_qw.restype = st
         _lib = L
         return L
 
@@ -276,7 +314,8 @@ def f8_gemm(a: torch.Tensor, b: torch.Tensor, scale_a: torch.Tensor, scale_b: to
 
 
 def f8_gemm_grouped(problems, stream=None) -> list:
-    """One or two GEMMs in one launch (f8_gemm_grouped).  Each problem is
+    """Up to F8_MAX_GROUPED_GEMMS GEMMs under the grouped-launch planner
+    (f8_gemm_grouped).  Each problem is
     (a, b, scale_a, scale_b, out, fmt_a, fmt_b) as for f8_gemm (out, fmt_a
     and fmt_b may be None / omitted); returns the outputs."""
     arr = (_GemmProblem * len(problems))()
@@ -305,10 +344,13 @@ def f8_linear_workspace_bytes(M: int, N: int, K: int) -> int:
 
 @dataclass
 class LinearSaved:
-    """Device buffers the forward pass leaves for the backward pass."""
+    """Device buffers the forward pass leaves for the backward pass.  A
+    member of a group (group_saved) shares x_t and x_scalars with the
+    group's other members; its scalars[0:2] are then unused."""
     x_t: torch.Tensor      # [K, M] uint8
     w_t: torch.Tensor      # [K, N] uint8
     scalars: torch.Tensor  # [4] fp32: amax_x, scale_x, amax_w, scale_w
+    x_scalars: torch.Tensor | None = None  # [2] fp32 amax_x, scale_x shared by a group
 
     @classmethod
     def empty(cls, M: int, N: int, K: int, device) -> "LinearSaved":
@@ -318,13 +360,16 @@ class LinearSaved:
 
     def c_struct(self) -> _Saved:
         p = self.scalars.data_ptr()
-        return _Saved(self.x_t.data_ptr(), self.w_t.data_ptr(), p, p + 4, p + 8, p + 12)
+        px = self.x_scalars.data_ptr() if self.x_scalars is not None else p
+        return _Saved(self.x_t.data_ptr(), self.w_t.data_ptr(), px, px + 4, p + 8, p + 12)
 
     @property
-    def amax_x(self): return self.scalars[0]
+    def amax_x(self):
+        return (self.x_scalars if self.x_scalars is not None else self.scalars)[0]
 
     @property
-    def scale_x(self): return self.scalars[1]
+    def scale_x(self):
+        return (self.x_scalars if self.x_scalars is not None else self.scalars)[1]
 
     @property
     def amax_w(self): return self.scalars[2]
@@ -335,6 +380,110 @@ class LinearSaved:
 
 def workspace(M: int, N: int, K: int, device) -> torch.Tensor:
     return torch.empty(max(f8_linear_workspace_bytes(M, N, K), 1), dtype=torch.uint8, device=device)
+
+
+def f8_quantize_multi_workspace_bytes() -> int:
+    return int(lib().f8_quantize_multi_workspace_bytes())
+
+
+def f8_quantize_multi(xs, fmt: int = F8_E4M3, outs=None, ws: torch.Tensor | None = None,
+                      want_q: bool = True, want_t: bool = True, stream=None) -> list:
+    """Each 2-D bf16 tensor of ``xs`` quantised with its own amax and scale
+    (f8_quantize_multi): returns [(q, q_t, scale, amax), ...].  ``outs`` may
+    give those buffers per tensor."""
+    n = len(xs)
+    arr = (_QuantTensor * n)()
+    res = []
+    for i, x in enumerate(xs):
+        if x.dtype != torch.bfloat16 or x.dim() != 2:
+            raise TypeError("f8_quantize_multi takes 2-D bf16 tensors")
+        rows, cols = x.shape
+        dev = x.device
+        if outs is not None:
+            q, q_t, sc, am = outs[i]
+        else:
+            q = torch.empty((rows, cols), dtype=torch.uint8, device=dev) if want_q else None
+            q_t = torch.empty((cols, rows), dtype=torch.uint8, device=dev) if want_t else None
+            sc = torch.empty((), dtype=torch.float32, device=dev)
+            am = torch.empty((), dtype=torch.float32, device=dev)
+        arr[i] = _QuantTensor(_ptr(x), rows, cols, _ptr(am), _ptr(sc), _ptr(q), _ptr(q_t))
+        res.append((q, q_t, sc, am))
+    if ws is None:
+        ws = torch.empty(f8_quantize_multi_workspace_bytes(), dtype=torch.uint8, device=xs[0].device)
+    _check(lib().f8_quantize_multi(arr, n, int(fmt), _ptr(ws), ws.numel(), _stream(stream)),
+           "f8_quantize_multi")
+    return res
+
+
+def f8_linear_group_workspace_bytes(M: int, K: int, Ns) -> int:
+    arr = (ctypes.c_int64 * len(Ns))(*Ns)
+    return int(lib().f8_linear_group_workspace_bytes(M, K, arr, len(Ns)))
+
+
+def group_workspace(M: int, K: int, Ns, device) -> torch.Tensor:
+    return torch.empty(max(f8_linear_group_workspace_bytes(M, K, Ns), 1), dtype=torch.uint8,
+                       device=device)
+
+
+def group_saved(M: int, K: int, Ns, device) -> list:
+    """Saved buffers of a group of linears sharing X [M, K]: one q(X)^T and
+    one (amax_x, scale_x) shared, q(W_i)^T and (amax_w, scale_w) per member."""
+    x_t = torch.empty((K, M), dtype=torch.uint8, device=device)
+    xs = torch.empty(2, dtype=torch.float32, device=device)
+    return [LinearSaved(x_t, torch.empty((K, N), dtype=torch.uint8, device=device),
+                        torch.empty(4, dtype=torch.float32, device=device), xs) for N in Ns]
+
+
+def _group_array(saved, Ns, w=None, y=None, dy=None, dx=None, dw=None):
+    n = len(saved)
+    arr = (_GroupLinear * n)()
+    for i in range(n):
+        arr[i] = _GroupLinear(Ns[i], _ptr(w[i]) if w else None, _ptr(y[i]) if y else None,
+                              _ptr(dy[i]) if dy else None, _ptr(dx[i]) if dx else None,
+                              _ptr(dw[i]) if dw else None, saved[i].c_struct())
+    return arr
+
+
+def f8_linear_fwd_group(x: torch.Tensor, ws_: list, ys: list | None = None, saved: list | None = None,
+                        ws: torch.Tensor | None = None, stream=None):
+    """Y_i = X W_i^T for linears sharing X (f8_linear_fwd_group): X quantised
+    once, each W_i with its own scale; returns (ys, saved)."""
+    M, K = x.shape
+    Ns = [w.shape[0] for w in ws_]
+    for w in ws_:
+        if w.shape[1] != K:
+            raise ValueError("in-feature sizes differ")
+    dev = x.device
+    if ys is None:
+        ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for N in Ns]
+    if saved is None:
+        saved = group_saved(M, K, Ns, dev)
+    if ws is None:
+        ws = group_workspace(M, K, Ns, dev)
+    arr = _group_array(saved, Ns, w=ws_, y=ys)
+    _check(lib().f8_linear_fwd_group(_ptr(x), M, K, arr, len(Ns), _ptr(ws), ws.numel(),
+                                     _stream(stream)), "f8_linear_fwd_group")
+    return ys, saved
+
+
+def f8_linear_bwd_group(dys: list, saved: list, K: int, dxs: list | None = None,
+                        dws: list | None = None, ws: torch.Tensor | None = None,
+                        fmt: int = F8_E4M3, want_dx: bool = True, want_dw: bool = True, stream=None):
+    """dX_i = dY_i W_i, dW_i = dY_i^T X for the group of f8_linear_fwd_group
+    (f8_linear_bwd_group); returns (dxs, dws) (lists, or None if not wanted)."""
+    M = dys[0].shape[0]
+    Ns = [dy.shape[1] for dy in dys]
+    dev = dys[0].device
+    if want_dx and dxs is None:
+        dxs = [torch.empty((M, K), dtype=torch.bfloat16, device=dev) for _ in Ns]
+    if want_dw and dws is None:
+        dws = [torch.empty((N, K), dtype=torch.bfloat16, device=dev) for N in Ns]
+    if ws is None:
+        ws = group_workspace(M, K, Ns, dev)
+    arr = _group_array(saved, Ns, dy=dys, dx=dxs if want_dx else None, dw=dws if want_dw else None)
+    _check(lib().f8_linear_bwd_group(arr, len(Ns), M, K, int(fmt), _ptr(ws), ws.numel(),
+                                     _stream(stream)), "f8_linear_bwd_group")
+    return (dxs if want_dx else None), (dws if want_dw else None)
 
 
 def f8_linear_fwd(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | None = None,
@@ -559,3 +708,38 @@ def f8_linear_bwd(dy: torch.Tensor, saved: LinearSaved, K: int | None = None,
                                        _ptr(dw), _ptr(ws), ws.numel(), _stream(stream)),
                "f8_linear_bwd_fmt")
     return dx, dw
+
+
+def f8_transpose_u8(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[c, r] = x[r, c] for a 2-D uint8 tensor (f8_transpose_u8)."""
+    if x.dtype != torch.uint8 or x.dim() != 2:
+        raise TypeError("f8_transpose_u8 takes a 2-D uint8 tensor")
+    rows, cols = x.shape
+    if out is None:
+        out = torch.empty((cols, rows), dtype=torch.uint8, device=x.device)
+    _check(lib().f8_transpose_u8(_ptr(x), rows, cols, _ptr(out), _stream(stream)), "f8_transpose_u8")
+    return out
+
+
+def f8_linear_fwd_qw_workspace_bytes(M: int, K: int) -> int:
+    return int(lib().f8_linear_fwd_qw_workspace_bytes(M, K))
+
+
+def f8_linear_fwd_qw(x: torch.Tensor, w_q: torch.Tensor, saved: LinearSaved,
+                     y: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None):
+    """Y = X W^T for a weight that arrives quantised (w_q [N, K] uint8, with
+    saved.w_t = q(W)^T and saved's amax_w / scale_w set by the caller);
+    writes saved's X part; returns Y."""
+    M, K = x.shape
+    N, K2 = w_q.shape
+    if K != K2:
+        raise ValueError("in-feature sizes differ")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = torch.empty(max(f8_linear_fwd_qw_workspace_bytes(M, K), 1), dtype=torch.uint8,
+                         device=x.device)
+    s = saved.c_struct()
+    _check(lib().f8_linear_fwd_qw(_ptr(x), _ptr(w_q), M, N, K, _ptr(y), ctypes.byref(s), _ptr(ws),
+                                  ws.numel(), _stream(stream)), "f8_linear_fwd_qw")
+    return y

@@ -43,6 +43,10 @@ f8_status from_cuda(cudaError_t e)
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// The GEMM kernels number the output tiles of a launch (128 x 256 at the
+// smallest) in 32-bit ints.
+bool tiles_fit(int64_t M, int64_t N) { return ((M + 127) / 128) * ((N + 255) / 256) <= INT32_MAX / 2; }
+
 // Workspace of the forward pass: q(X) [M,K], q(W) [N,K], then the amax
 // partial maxima of X and of W.  Of the backward pass: q(dY) [M,N],
 // q(dY)^T [N,M], amax and scale of dY, then the partial maxima of dY.
@@ -148,6 +152,33 @@ const DeviceInfo *device_info()
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
+f8_status check_linear_shape(int64_t M, int64_t N, int64_t K)
+{
+    if (M <= 0 || N <= 0 || K <= 0)
+        return F8_ERR_INVALID;
+    if (M % 16 || N % 16 || K % 16)
+        return F8_ERR_SHAPE;
+    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2)
+        return F8_ERR_SHAPE;
+    // Y [M,N], dX [M,K], dW [N,K]
+    if (!tiles_fit(M, N) || !tiles_fit(M, K) || !tiles_fit(N, K))
+        return F8_ERR_SHAPE;
+    return F8_OK;
+}
+
+f8_status check_saved(const f8_linear_saved *s)
+{
+    if (s == nullptr || s->x_t == nullptr || s->w_t == nullptr || s->amax_x == nullptr ||
+        s->scale_x == nullptr || s->amax_w == nullptr || s->scale_w == nullptr)
+        return F8_ERR_INVALID;
+    if (!aligned(s->x_t, 16) || !aligned(s->w_t, 16) || !aligned(s->amax_x, 4) ||
+        !aligned(s->scale_x, 4) || !aligned(s->amax_w, 4) || !aligned(s->scale_w, 4))
+        return F8_ERR_ALIGN;
+    return F8_OK;
+}
+
+size_t linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K) { return fwd_ws_bytes(M, N, K); }
+
 } // namespace f8
 
 using namespace f8;
@@ -179,9 +210,6 @@ f8_status check_cast_args(const void *x, int64_t rows, int64_t cols, const float
     return F8_OK;
 }
 
-// The GEMM kernels number the output tiles of a launch (128 x 256 at the
-// smallest) in 32-bit ints.
-bool tiles_fit(int64_t M, int64_t N) { return ((M + 127) / 128) * ((N + 255) / 256) <= INT32_MAX / 2; }
 
 f8_status check_gemm_args(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
                           const float *sa, const float *sb, const void *c)
@@ -201,31 +229,6 @@ f8_status check_gemm_args(const uint8_t *a, const uint8_t *b, int64_t M, int64_t
     return F8_OK;
 }
 
-f8_status check_linear_shape(int64_t M, int64_t N, int64_t K)
-{
-    if (M <= 0 || N <= 0 || K <= 0)
-        return F8_ERR_INVALID;
-    if (M % 16 || N % 16 || K % 16)
-        return F8_ERR_SHAPE;
-    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2)
-        return F8_ERR_SHAPE;
-    // Y [M,N], dX [M,K], dW [N,K]
-    if (!tiles_fit(M, N) || !tiles_fit(M, K) || !tiles_fit(N, K))
-        return F8_ERR_SHAPE;
-    return F8_OK;
-}
-
-f8_status check_saved(const f8_linear_saved *s)
-{
-    if (s == nullptr || s->x_t == nullptr || s->w_t == nullptr || s->amax_x == nullptr ||
-        s->scale_x == nullptr || s->amax_w == nullptr || s->scale_w == nullptr)
-        return F8_ERR_INVALID;
-    if (!aligned(s->x_t, 16) || !aligned(s->w_t, 16) || !aligned(s->amax_x, 4) ||
-        !aligned(s->scale_x, 4) || !aligned(s->amax_w, 4) || !aligned(s->scale_w, 4))
-        return F8_ERR_ALIGN;
-    return F8_OK;
-}
-
 #define F8_TRY(expr)                                                                               \
     do {                                                                                           \
         f8_status st_ = (expr);                                                                    \
@@ -236,6 +239,42 @@ f8_status check_saved(const f8_linear_saved *s)
 #define F8_TRY_CUDA(expr) F8_TRY(from_cuda(expr))
 
 } // namespace
+
+f8_status f8::linear_fwd_impl(const void *x, const void *w, int64_t M, int64_t N, int64_t K,
+                              void *y, const f8_linear_saved *saved, void *workspace,
+                              size_t workspace_bytes, cudaStream_t st)
+{
+    F8_TRY(check_linear_shape(M, N, K));
+    F8_TRY(check_saved(saved));
+    if (x == nullptr || w == nullptr || y == nullptr || workspace == nullptr)
+        return F8_ERR_INVALID;
+    if (workspace_bytes < fwd_ws_bytes(M, N, K))
+        return F8_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(workspace, 256))
+        return F8_ERR_ALIGN;
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    const FwdWs fw = fwd_ws(workspace, M, N, K);
+    // X and W together when they fit in L2 with room to spare (the cast
+    // re-reads what the amax launch just read): two launches instead of four
+    bool pair = quant_pair_enabled() && 2 * (M * K + N * K) <= kPairMaxBytes;
+    const QuantDesc xw[2] = {{x, M, K, saved->amax_x, saved->scale_x, fw.x_q, saved->x_t},
+                             {w, N, K, saved->amax_w, saved->scale_w, fw.w_q, saved->w_t}};
+    pair = pair && quantize_multi_castable(xw, 2);
+    if (pair) {
+        F8_TRY_CUDA(launch_quantize_multi(xw, 2, F8_E4M3, fw.parts_x, *dev, st));
+    } else {
+        int np = 0;
+        // each cast follows its own amax so that its re-read of the tensor hits L2
+        F8_TRY_CUDA(launch_amax_partials(x, M * K, fw.parts_x, &np, *dev, st));
+        F8_TRY_CUDA(launch_cast_transpose(x, M, K, nullptr, fw.parts_x, np, saved->amax_x,
+                                          saved->scale_x, fw.x_q, saved->x_t, 0, *dev, st, true));
+        F8_TRY_CUDA(launch_amax_partials(w, N * K, fw.parts_w, &np, *dev, st));
+        F8_TRY_CUDA(launch_cast_transpose(w, N, K, nullptr, fw.parts_w, np, saved->amax_w,
+                                          saved->scale_w, fw.w_q, saved->w_t, 0, *dev, st, true));
+    }
+    return from_cuda(launch_gemm(fw.x_q, fw.w_q, M, N, K, saved->scale_x, saved->scale_w, y, *dev, st));
+}
 
 extern "C" {
 
@@ -305,7 +344,7 @@ static f8_status quantize_impl(const void *x, int64_t rows, int64_t cols, int fm
     int np = 0;
     F8_TRY_CUDA(launch_amax_partials(x, rows * cols, parts, &np, *dev, st));
     return from_cuda(launch_cast_transpose(x, rows, cols, nullptr, parts, np, amax_out, scale_out,
-                                           q, q_t, fmt, *dev, st));
+                                           q, q_t, fmt, *dev, st, true));
 }
 
 f8_status f8_quantize(const void *x, int64_t rows, int64_t cols, float *amax_out,
@@ -356,7 +395,7 @@ f8_status f8_gemm_fmt(const uint8_t *a, f8_format fmt_a, const uint8_t *b, f8_fo
 
 f8_status f8_gemm_grouped(const f8_gemm_problem *problems, int count, void *stream)
 {
-    if (problems == nullptr || count < 1 || count > 2)
+    if (problems == nullptr || count < 1 || count > F8_MAX_GROUPED_GEMMS)
         return F8_ERR_INVALID;
     bool separate = count == 1;
     for (int i = 0; i < count; ++i) {
@@ -378,12 +417,53 @@ f8_status f8_gemm_grouped(const f8_gemm_problem *problems, int count, void *stre
     }
     const DeviceInfo *dev;
     F8_TRY(get_device(&dev));
-    GemmDesc g[2];
-    for (int i = 0; i < 2; ++i) {
+    GemmDesc g[F8_MAX_GROUPED_GEMMS];
+    for (int i = 0; i < count; ++i) {
         const f8_gemm_problem &p = problems[i];
         g[i] = GemmDesc{p.a, p.b, p.M, p.N, p.K, p.scale_a, p.scale_b, p.c, p.fmt_a, p.fmt_b};
     }
-    return from_cuda(launch_gemm2(g[0], g[1], *dev, static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_gemm_multi(g, count, *dev, static_cast<cudaStream_t>(stream)));
+}
+
+size_t f8_quantize_multi_workspace_bytes(void) { return kPartialsBytes; }
+
+static f8_status check_quant_tensor(const f8_quant_tensor &t)
+{
+    if (t.rows < 0 || t.cols < 0 || t.amax_out == nullptr || (t.rows > 0 && t.cols > 0 && t.x == nullptr))
+        return F8_ERR_INVALID;
+    if (!aligned(t.x, 16) || !aligned(t.q, 16) || !aligned(t.q_t, 16) || !aligned(t.amax_out, 4) ||
+        !aligned(t.scale_out, 4))
+        return F8_ERR_ALIGN;
+    return F8_OK;
+}
+
+f8_status f8_quantize_multi(const f8_quant_tensor *tensors, int count, f8_format fmt,
+                            void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (tensors == nullptr || count < 1 || count > F8_MAX_MULTI_TENSORS || workspace == nullptr ||
+        (fmt != F8_E4M3 && fmt != F8_E5M2))
+        return F8_ERR_INVALID;
+    if (workspace_bytes < kPartialsBytes)
+        return F8_ERR_INVALID;
+    if (!aligned(workspace, 16))
+        return F8_ERR_ALIGN;
+    for (int i = 0; i < count; ++i)
+        F8_TRY(check_quant_tensor(tensors[i]));
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    QuantDesc d[F8_MAX_MULTI_TENSORS];
+    for (int i = 0; i < count; ++i) {
+        const f8_quant_tensor &t = tensors[i];
+        d[i] = QuantDesc{t.x, t.rows, t.cols, t.amax_out, t.scale_out, t.q, t.q_t};
+    }
+    if (quantize_multi_castable(d, count))
+        return from_cuda(launch_quantize_multi(d, count, fmt, static_cast<unsigned *>(workspace),
+                                               *dev, st));
+    for (int i = 0; i < count; ++i)
+        F8_TRY(quantize_impl(d[i].x, d[i].rows, d[i].cols, fmt, d[i].amax_out, d[i].scale_out,
+                             d[i].q, d[i].q_t, workspace, workspace_bytes, stream));
+    return F8_OK;
 }
 
 size_t f8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K)
@@ -398,41 +478,8 @@ f8_status f8_linear_fwd(const void *x, const void *w, int64_t M, int64_t N, int6
                         const f8_linear_saved *saved, void *workspace, size_t workspace_bytes,
                         void *stream)
 {
-    F8_TRY(check_linear_shape(M, N, K));
-    F8_TRY(check_saved(saved));
-    if (x == nullptr || w == nullptr || y == nullptr || workspace == nullptr)
-        return F8_ERR_INVALID;
-    if (workspace_bytes < fwd_ws_bytes(M, N, K))
-        return F8_ERR_INVALID;
-    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(workspace, 256))
-        return F8_ERR_ALIGN;
-    const DeviceInfo *dev;
-    F8_TRY(get_device(&dev));
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const FwdWs fw = fwd_ws(workspace, M, N, K);
-    // X and W together when they fit in L2 with room to spare (the cast
-    // re-reads what the amax launch just read): two launches instead of four
-    bool pair = quant_pair_enabled() && 2 * (M * K + N * K) <= kPairMaxBytes;
-    if (pair) {
-        const cudaError_t e = launch_quantize_pair(
-            x, M, K, w, N, K, fw.parts_x, fw.parts_w, saved->amax_x, saved->scale_x, fw.x_q,
-            saved->x_t, saved->amax_w, saved->scale_w, fw.w_q, saved->w_t, *dev, st);
-        if (e == cudaErrorNotSupported)
-            pair = false;  // nothing was launched
-        else
-            F8_TRY_CUDA(e);
-    }
-    if (!pair) {
-        int np = 0;
-        // each cast follows its own amax so that its re-read of the tensor hits L2
-        F8_TRY_CUDA(launch_amax_partials(x, M * K, fw.parts_x, &np, *dev, st));
-        F8_TRY_CUDA(launch_cast_transpose(x, M, K, nullptr, fw.parts_x, np, saved->amax_x,
-                                          saved->scale_x, fw.x_q, saved->x_t, 0, *dev, st));
-        F8_TRY_CUDA(launch_amax_partials(w, N * K, fw.parts_w, &np, *dev, st));
-        F8_TRY_CUDA(launch_cast_transpose(w, N, K, nullptr, fw.parts_w, np, saved->amax_w,
-                                          saved->scale_w, fw.w_q, saved->w_t, 0, *dev, st));
-    }
-    return from_cuda(launch_gemm(fw.x_q, fw.w_q, M, N, K, saved->scale_x, saved->scale_w, y, *dev, st));
+    return linear_fwd_impl(x, w, M, N, K, y, saved, workspace, workspace_bytes,
+                           static_cast<cudaStream_t>(stream));
 }
 
 static f8_status linear_bwd_impl(const void *dy, int fdy, const f8_linear_saved *saved, int64_t M,
@@ -456,7 +503,8 @@ static f8_status linear_bwd_impl(const void *dy, int fdy, const f8_linear_saved 
     int np = 0;
     F8_TRY_CUDA(launch_amax_partials(dy, M * N, bw.parts_dy, &np, *dev, st));
     F8_TRY_CUDA(launch_cast_transpose(dy, M, N, nullptr, bw.parts_dy, np, bw.amax_dy, bw.scale_dy,
-                                      dx ? bw.dy_q : nullptr, dw ? bw.dy_t : nullptr, fdy, *dev, st));
+                                      dx ? bw.dy_q : nullptr, dw ? bw.dy_t : nullptr, fdy, *dev, st,
+                                      true));
     return from_cuda(launch_bwd_gemms(bw, saved, M, N, K, fdy, dx, dw, *dev, st));
 }
 
@@ -472,6 +520,215 @@ f8_status f8_linear_bwd_fmt(const void *dy, f8_format fmt_dy, const f8_linear_sa
                             size_t workspace_bytes, void *stream)
 {
     return linear_bwd_impl(dy, fmt_dy, saved, M, N, K, dx, dw, workspace, workspace_bytes, stream);
+}
+
+// Workspace of a group forward: q(X) [M, K], q(W_i) [N_i, K], partial
+// maxima.  Of a group backward: per member q(dY_i) [M, N_i], q(dY_i)^T and
+// 256 bytes of scalars (amax, scale), then partial maxima.
+static size_t group_fwd_ws_bytes(int64_t M, int64_t K, const int64_t *N, int count)
+{
+    size_t b = round256(static_cast<size_t>(M) * K) + kPartialsBytes;
+    for (int i = 0; i < count; ++i)
+        b += round256(static_cast<size_t>(N[i]) * K);
+    return b;
+}
+
+static size_t group_bwd_ws_bytes(int64_t M, const int64_t *N, int count)
+{
+    size_t b = kPartialsBytes;
+    for (int i = 0; i < count; ++i)
+        b += 2 * round256(static_cast<size_t>(M) * N[i]) + 256;
+    return b;
+}
+
+// Shapes and the shared-X rule of a group; fills N[].
+static f8_status check_group(const f8_group_linear *m, int count, int64_t M, int64_t K, int64_t *N)
+{
+    if (m == nullptr || count < 1 || count > F8_MAX_GROUP_LINEARS)
+        return F8_ERR_INVALID;
+    for (int i = 0; i < count; ++i) {
+        F8_TRY(check_linear_shape(M, m[i].N, K));
+        F8_TRY(check_saved(&m[i].saved));
+        const f8_linear_saved &s0 = m[0].saved, &si = m[i].saved;
+        if (si.x_t != s0.x_t || si.amax_x != s0.amax_x || si.scale_x != s0.scale_x)
+            return F8_ERR_INVALID;
+        N[i] = m[i].N;
+    }
+    return F8_OK;
+}
+
+size_t f8_linear_group_workspace_bytes(int64_t M, int64_t K, const int64_t *N, int count)
+{
+    if (N == nullptr || count < 1 || count > F8_MAX_GROUP_LINEARS || M <= 0 || K <= 0)
+        return 0;
+    for (int i = 0; i < count; ++i)
+        if (N[i] <= 0)
+            return 0;
+    const size_t f = group_fwd_ws_bytes(M, K, N, count), b = group_bwd_ws_bytes(M, N, count);
+    return f > b ? f : b;
+}
+
+f8_status f8_linear_fwd_group(const void *x, int64_t M, int64_t K, const f8_group_linear *members,
+                              int count, void *workspace, size_t workspace_bytes, void *stream)
+{
+    int64_t N[F8_MAX_GROUP_LINEARS];
+    F8_TRY(check_group(members, count, M, K, N));
+    if (x == nullptr || workspace == nullptr)
+        return F8_ERR_INVALID;
+    for (int i = 0; i < count; ++i)
+        if (members[i].w == nullptr || members[i].y == nullptr)
+            return F8_ERR_INVALID;
+    if (workspace_bytes < group_fwd_ws_bytes(M, K, N, count))
+        return F8_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(workspace, 256))
+        return F8_ERR_ALIGN;
+    for (int i = 0; i < count; ++i)
+        if (!aligned(members[i].w, 16) || !aligned(members[i].y, 16))
+            return F8_ERR_ALIGN;
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // workspace: q(X), q(W_0), ..., partials
+    uint8_t *p = static_cast<uint8_t *>(workspace);
+    uint8_t *x_q = p;
+    p += round256(static_cast<size_t>(M) * K);
+    uint8_t *w_q[F8_MAX_GROUP_LINEARS];
+    for (int i = 0; i < count; ++i) {
+        w_q[i] = p;
+        p += round256(static_cast<size_t>(N[i]) * K);
+    }
+    unsigned *parts = reinterpret_cast<unsigned *>(p);
+    const f8_linear_saved &s0 = members[0].saved;
+    QuantDesc d[1 + F8_MAX_GROUP_LINEARS];
+    d[0] = QuantDesc{x, M, K, s0.amax_x, s0.scale_x, x_q, s0.x_t};
+    for (int i = 0; i < count; ++i) {
+        const f8_linear_saved &si = members[i].saved;
+        d[1 + i] = QuantDesc{members[i].w, N[i], K, si.amax_w, si.scale_w, w_q[i], si.w_t};
+    }
+    if (quantize_multi_castable(d, 1 + count)) {
+        F8_TRY_CUDA(launch_quantize_multi(d, 1 + count, F8_E4M3, parts, *dev, st));
+    } else {
+        for (int i = 0; i <= count; ++i) {
+            int np = 0;
+            F8_TRY_CUDA(launch_amax_partials(d[i].x, d[i].rows * d[i].cols, parts, &np, *dev, st));
+            F8_TRY_CUDA(launch_cast_transpose(d[i].x, d[i].rows, d[i].cols, nullptr, parts, np,
+                                              d[i].amax_out, d[i].scale_out, d[i].q, d[i].q_t, 0,
+                                              *dev, st, true));
+        }
+    }
+    GemmDesc g[F8_MAX_GROUP_LINEARS];
+    for (int i = 0; i < count; ++i)
+        g[i] = GemmDesc{x_q, w_q[i], M, N[i], K, s0.scale_x, members[i].saved.scale_w,
+                        members[i].y, F8_E4M3, F8_E4M3};
+    return from_cuda(launch_gemm_multi(g, count, *dev, st));
+}
+
+f8_status f8_linear_bwd_group(const f8_group_linear *members, int count, int64_t M, int64_t K,
+                              f8_format fmt_dy, void *workspace, size_t workspace_bytes,
+                              void *stream)
+{
+    int64_t N[F8_MAX_GROUP_LINEARS];
+    F8_TRY(check_group(members, count, M, K, N));
+    if (workspace == nullptr || (fmt_dy != F8_E4M3 && fmt_dy != F8_E5M2))
+        return F8_ERR_INVALID;
+    for (int i = 0; i < count; ++i)
+        if (members[i].dy == nullptr)
+            return F8_ERR_INVALID;
+    if (workspace_bytes < group_bwd_ws_bytes(M, N, count))
+        return F8_ERR_INVALID;
+    if (!aligned(workspace, 256))
+        return F8_ERR_ALIGN;
+    for (int i = 0; i < count; ++i)
+        if (!aligned(members[i].dy, 16) || !aligned(members[i].dx, 16) ||
+            !aligned(members[i].dw, 16))
+            return F8_ERR_ALIGN;
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *p = static_cast<uint8_t *>(workspace);
+    uint8_t *dy_q[F8_MAX_GROUP_LINEARS], *dy_t[F8_MAX_GROUP_LINEARS];
+    float *amax[F8_MAX_GROUP_LINEARS], *scale[F8_MAX_GROUP_LINEARS];
+    for (int i = 0; i < count; ++i) {
+        const size_t mn = round256(static_cast<size_t>(M) * N[i]);
+        dy_q[i] = p;
+        dy_t[i] = p + mn;
+        amax[i] = reinterpret_cast<float *>(p + 2 * mn);
+        scale[i] = reinterpret_cast<float *>(p + 2 * mn + 128);
+        p += 2 * mn + 256;
+    }
+    unsigned *parts = reinterpret_cast<unsigned *>(p);
+    QuantDesc d[F8_MAX_GROUP_LINEARS];
+    for (int i = 0; i < count; ++i)
+        d[i] = QuantDesc{members[i].dy, M, N[i], amax[i], scale[i],
+                         members[i].dx ? dy_q[i] : nullptr, members[i].dw ? dy_t[i] : nullptr};
+    if (quantize_multi_castable(d, count)) {
+        F8_TRY_CUDA(launch_quantize_multi(d, count, fmt_dy, parts, *dev, st));
+    } else {
+        for (int i = 0; i < count; ++i) {
+            int np = 0;
+            F8_TRY_CUDA(launch_amax_partials(d[i].x, M * N[i], parts, &np, *dev, st));
+            F8_TRY_CUDA(launch_cast_transpose(d[i].x, M, N[i], nullptr, parts, np, d[i].amax_out,
+                                              d[i].scale_out, d[i].q, d[i].q_t, fmt_dy, *dev, st,
+                                              true));
+        }
+    }
+    // dX_i [M,K] = q(dY_i) [M,N_i] . (q(W_i)^T [K,N_i])^T;  dW_i [N_i,K] = q(dY_i)^T . (q(X)^T [K,M])^T
+    GemmDesc g[2 * F8_MAX_GROUP_LINEARS];
+    int n = 0;
+    for (int i = 0; i < count; ++i) {
+        const f8_linear_saved &si = members[i].saved;
+        if (members[i].dx != nullptr)
+            g[n++] = GemmDesc{dy_q[i], si.w_t, M, K, N[i], scale[i], si.scale_w, members[i].dx,
+                              fmt_dy, F8_E4M3};
+        if (members[i].dw != nullptr)
+            g[n++] = GemmDesc{dy_t[i], si.x_t, N[i], K, M, scale[i], si.scale_x, members[i].dw,
+                              fmt_dy, F8_E4M3};
+    }
+    if (n == 0)
+        return F8_OK;
+    return from_cuda(launch_gemm_multi(g, n, *dev, st));
+}
+
+f8_status f8_transpose_u8(const uint8_t *in, int64_t rows, int64_t cols, uint8_t *out, void *stream)
+{
+    if (rows < 0 || cols < 0 || (rows > 0 && cols > 0 && (in == nullptr || out == nullptr)))
+        return F8_ERR_INVALID;
+    if (rows == 0 || cols == 0)
+        return F8_OK;
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    return from_cuda(launch_transpose_u8(in, rows, cols, out, *dev, static_cast<cudaStream_t>(stream)));
+}
+
+size_t f8_linear_fwd_qw_workspace_bytes(int64_t M, int64_t K)
+{
+    if (M <= 0 || K <= 0)
+        return 0;
+    return round256(static_cast<size_t>(M) * K) + kPartialsBytes;
+}
+
+f8_status f8_linear_fwd_qw(const void *x, const uint8_t *w_q, int64_t M, int64_t N, int64_t K,
+                           void *y, const f8_linear_saved *saved, void *workspace,
+                           size_t workspace_bytes, void *stream)
+{
+    F8_TRY(check_linear_shape(M, N, K));
+    F8_TRY(check_saved(saved));
+    if (x == nullptr || w_q == nullptr || y == nullptr || workspace == nullptr)
+        return F8_ERR_INVALID;
+    if (workspace_bytes < f8_linear_fwd_qw_workspace_bytes(M, K))
+        return F8_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(w_q, 16) || !aligned(y, 16) || !aligned(workspace, 256))
+        return F8_ERR_ALIGN;
+    const DeviceInfo *dev;
+    F8_TRY(get_device(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *x_q = static_cast<uint8_t *>(workspace);
+    unsigned *parts = reinterpret_cast<unsigned *>(x_q + round256(static_cast<size_t>(M) * K));
+    int np = 0;
+    F8_TRY_CUDA(launch_amax_partials(x, M * K, parts, &np, *dev, st));
+    F8_TRY_CUDA(launch_cast_transpose(x, M, K, nullptr, parts, np, saved->amax_x, saved->scale_x,
+                                      x_q, saved->x_t, 0, *dev, st, true));
+    return from_cuda(launch_gemm(x_q, w_q, M, N, K, saved->scale_x, saved->scale_w, y, *dev, st));
 }
 
 f8_status f8_quantize_swiglu(const void *a, const void *b, void *h, int64_t rows, int64_t cols,
@@ -517,7 +774,7 @@ f8_status f8_linear_fwd_swiglu(const void *a, const void *b, void *h, const void
                                        fw.x_q, saved->x_t, *dev, st));
     F8_TRY_CUDA(launch_amax_partials(w, N * K, fw.parts_w, &np, *dev, st));
     F8_TRY_CUDA(launch_cast_transpose(w, N, K, nullptr, fw.parts_w, np, saved->amax_w,
-                                      saved->scale_w, fw.w_q, saved->w_t, 0, *dev, st));
+                                      saved->scale_w, fw.w_q, saved->w_t, 0, *dev, st, true));
     return from_cuda(launch_gemm(fw.x_q, fw.w_q, M, N, K, saved->scale_x, saved->scale_w, y, *dev, st));
 }
 
@@ -549,10 +806,10 @@ f8_status f8_linear_fwd_w13_swiglu(const void *x, const void *w13, int64_t M, in
     int np = 0;
     F8_TRY_CUDA(launch_amax_partials(x, M * K, fw.parts_x, &np, *dev, st));
     F8_TRY_CUDA(launch_cast_transpose(x, M, K, nullptr, fw.parts_x, np, saved->amax_x,
-                                      saved->scale_x, fw.x_q, saved->x_t, 0, *dev, st));
+                                      saved->scale_x, fw.x_q, saved->x_t, 0, *dev, st, true));
     F8_TRY_CUDA(launch_amax_partials(w13, N * K, fw.parts_w, &np, *dev, st));
     F8_TRY_CUDA(launch_cast_transpose(w13, N, K, nullptr, fw.parts_w, np, saved->amax_w,
-                                      saved->scale_w, fw.w_q, saved->w_t, 0, *dev, st));
+                                      saved->scale_w, fw.w_q, saved->w_t, 0, *dev, st, true));
     // the X partials were consumed by the cast of X, which the GEMM's
     // dependency wait orders before it: they take h's partials
     int nh = 0;

@@ -101,21 +101,31 @@ amax_kernel(const uint4 *__restrict__ x, int64_t nvec, const uint16_t *__restric
     }
 }
 
-// Partial maxima of two tensors in one launch (no tails: both lengths are
-// multiples of 8): blocks [0, b0) take x0, the rest x1, each with its own
-// grid stride; block i of a tensor writes that tensor's partial i.
+// Partial maxima of up to kMaxQuantTensors tensors in one launch (no tails:
+// every length is a multiple of 8): blocks [first_block[i],
+// first_block[i + 1]) take tensor i, each tensor with its own grid stride;
+// block j of a tensor writes that tensor's partial j.
+struct AmaxSegs {
+    const uint4 *x[kMaxQuantTensors];
+    int64_t nvec[kMaxQuantTensors];
+    unsigned *parts[kMaxQuantTensors];
+    int first_block[kMaxQuantTensors + 1];
+    int nseg;
+};
+
 __global__ void __launch_bounds__(kAmaxThreads, 4)
-amax_pair_kernel(const uint4 *__restrict__ x0, int64_t nvec0, const uint4 *__restrict__ x1,
-                 int64_t nvec1, int b0, unsigned *__restrict__ parts0, unsigned *__restrict__ parts1,
-                 unsigned *__restrict__ status)
+amax_multi_kernel(const __grid_constant__ AmaxSegs segs, unsigned *__restrict__ status)
 {
     griddep_wait();
     griddep_launch_dependents();
-    const bool second = static_cast<int>(blockIdx.x) >= b0;
-    const uint4 *__restrict__ x = second ? x1 : x0;
-    const int64_t nvec = second ? nvec1 : nvec0;
-    const int bid = second ? static_cast<int>(blockIdx.x) - b0 : static_cast<int>(blockIdx.x);
-    const int nblk = second ? static_cast<int>(gridDim.x) - b0 : b0;
+    int seg = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxQuantTensors; ++i)
+        seg += (i < segs.nseg && static_cast<int>(blockIdx.x) >= segs.first_block[i]) ? 1 : 0;
+    const uint4 *__restrict__ x = segs.x[seg];
+    const int64_t nvec = segs.nvec[seg];
+    const int bid = static_cast<int>(blockIdx.x) - segs.first_block[seg];
+    const int nblk = segs.first_block[seg + 1] - segs.first_block[seg];
     uint32_t m2 = 0;
     const int64_t S = static_cast<int64_t>(nblk) * blockDim.x;
     for (int64_t base = static_cast<int64_t>(bid) * blockDim.x + threadIdx.x; base < nvec;
@@ -143,7 +153,7 @@ amax_pair_kernel(const uint4 *__restrict__ x0, int64_t nvec0, const uint4 *__res
         if (lane == 0) {
             if (m >= 0x7F80u)
                 atomicOr(status, kStatusNonfinite);
-            (second ? parts1 : parts0)[bid] = m << 16;
+            segs.parts[seg][bid] = m << 16;
         }
     }
 }
@@ -486,14 +496,26 @@ struct CastSeg {
     uint8_t *q, *qt;
 };
 
-// NSEG = 2: the tiles of the second tensor follow those of the first in one
-// persistent loop, each tile with its own tensor's map, scale and outputs.
-template <int FMT, int NSEG>
+// The tensors of one TMA cast launch: NS = 1, one tensor; NS =
+// kMaxQuantTensors, nseg tensors whose tiles are numbered one after the
+// other (first_tile[i] = tensor i's first tile).
+template <int NS>
+struct CastSet {
+    CUtensorMap map[NS];
+    CastSeg seg[NS];
+    int64_t first_tile[NS + 1];
+    int nseg;
+    int early;   // 1: the inputs are complete before the dependency wait (the
+                 // previous launch only read them: their amax pass)
+};
+
+// Tiles are taken in reverse launch order (the last tile first): the amax
+// pass that precedes a cast walks each tensor front to back, so the tail of
+// a tensor larger than L2 is what L2 still holds when the cast starts.
+template <int FMT, int NS>
 __global__ void __launch_bounds__(kCastThreads)
-cast_transpose_tma_kernel(const __grid_constant__ CUtensorMap tmap0,
-                          const __grid_constant__ CUtensorMap tmap1,
-                          const __grid_constant__ CastSeg seg0, const __grid_constant__ CastSeg seg1,
-                          unsigned *__restrict__ status, uint64_t limit_ns)
+cast_transpose_tma_kernel(const __grid_constant__ CastSet<NS> set, unsigned *__restrict__ status,
+                          uint64_t limit_ns)
 {
     extern __shared__ uint8_t cast_smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(cast_smem_raw) + 127) &
@@ -501,66 +523,84 @@ cast_transpose_tma_kernel(const __grid_constant__ CUtensorMap tmap0,
     uint8_t *tile = sm + kInStages * kInBytes;
     uint64_t *bar = reinterpret_cast<uint64_t *>(tile + kTile * kTile);
     __shared__ int abort_flag;
+    __shared__ float s_scale[NS];
     const int t = threadIdx.x;
+    const int nseg = NS == 1 ? 1 : set.nseg;
+    const int64_t ntiles = set.first_tile[nseg];
+    const int64_t nmine = ntiles > blockIdx.x ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    // the k-th tile of this CTA -> (tensor, tile row start, tile column start)
+    auto locate = [&](int64_t k, int &sg, int64_t &r0, int64_t &c0) {
+        const int64_t tix = ntiles - 1 - (blockIdx.x + k * gridDim.x);
+        sg = 0;
+#pragma unroll
+        for (int i = 1; i < NS; ++i)
+            sg += (i < nseg && tix >= set.first_tile[i]) ? 1 : 0;
+        const int64_t lt = tix - set.first_tile[sg];
+        const int64_t tc = set.seg[sg].cols / kTile;
+        r0 = (lt / tc) * kTile;
+        c0 = (lt % tc) * kTile;
+    };
+    auto issue = [&](int64_t k) {
+        int sg;
+        int64_t r0, c0;
+        locate(k, sg, r0, c0);
+        const int b = static_cast<int>(k % kInStages);
+        fence_proxy_async_shared();  // earlier generic reads of this buffer come first
+        mbar_arrive_expect_tx(&bar[b], kInBytes);
+        tma_load_2d(sm + b * kInBytes, &set.map[sg], &bar[b], static_cast<int32_t>(c0),
+                    static_cast<int32_t>(r0));
+    };
     if (t == 0) {
         for (int b = 0; b < kInStages; ++b)
             mbar_init(&bar[b], 1);
         abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmap0);
-        if (NSEG == 2)
-            tma_prefetch_desc(&tmap1);
+        for (int i = 0; i < nseg; ++i)
+            tma_prefetch_desc(&set.map[i]);
+        if (set.early)
+            for (int64_t j = 0; j < nmine && j < kInStages - 1; ++j)
+                issue(j);
     }
     __syncthreads();
     griddep_wait();
     griddep_launch_dependents();
-    const float a0 = seg0.partials != nullptr ? reduce_partials(seg0.partials, seg0.nparts) : *seg0.amax;
-    const float s0 = scale_of<FMT>(a0);
-    float a1 = 0.0f, s1 = 0.0f;
-    if (NSEG == 2) {
-        a1 = seg1.partials != nullptr ? reduce_partials(seg1.partials, seg1.nparts) : *seg1.amax;
-        s1 = scale_of<FMT>(a1);
-    }
-    if (blockIdx.x == 0 && t == 0) {
-        if (seg0.scale_out != nullptr)
-            *seg0.scale_out = s0;
-        if (seg0.amax_out != nullptr)
-            *seg0.amax_out = a0;
-        if (NSEG == 2) {
-            if (seg1.scale_out != nullptr)
-                *seg1.scale_out = s1;
-            if (seg1.amax_out != nullptr)
-                *seg1.amax_out = a1;
-        }
-    }
-
-    const int64_t tiles_c0 = seg0.cols / kTile;
-    const int64_t ntiles0 = (seg0.rows / kTile) * tiles_c0;
-    const int64_t tiles_c1 = NSEG == 2 ? seg1.cols / kTile : 1;
-    const int64_t ntiles = ntiles0 + (NSEG == 2 ? (seg1.rows / kTile) * tiles_c1 : 0);
-    const int64_t nmine = ntiles > blockIdx.x ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    // tile tix of the launch -> (tensor, tile row start, tile column start)
-    auto locate = [&](int64_t tix, bool &second, int64_t &r0, int64_t &c0) {
-        second = NSEG == 2 && tix >= ntiles0;
-        const int64_t lt = second ? tix - ntiles0 : tix;
-        const int64_t tc = second ? tiles_c1 : tiles_c0;
-        r0 = (lt / tc) * kTile;
-        c0 = (lt % tc) * kTile;
-    };
-    auto issue = [&](int64_t k) {
-        const int64_t tix = blockIdx.x + k * gridDim.x;
-        bool second;
-        int64_t r0, c0;
-        locate(tix, second, r0, c0);
-        const int b = static_cast<int>(k % kInStages);
-        fence_proxy_async_shared();  // earlier generic reads of this buffer come first
-        mbar_arrive_expect_tx(&bar[b], kInBytes);
-        tma_load_2d(sm + b * kInBytes, second ? &tmap1 : &tmap0, &bar[b], static_cast<int32_t>(c0),
-                    static_cast<int32_t>(r0));
-    };
-    if (t == 0)
+    if (t == 0 && !set.early)
         for (int64_t j = 0; j < nmine && j < kInStages - 1; ++j)
             issue(j);
+    // each tensor's amax: the block reduces its partial maxima (fp32 bit
+    // patterns of non-negative values, so integer order is numeric order),
+    // then its scale
+    __shared__ unsigned s_amax[NS];
+    if (t < nseg)
+        s_amax[t] = 0u;
+    __syncthreads();
+    for (int i = 0; i < nseg; ++i) {
+        const CastSeg &sg = set.seg[i];
+        uint32_t m = 0;
+        if (sg.partials != nullptr) {
+            for (int j = t; j < sg.nparts; j += kCastThreads)
+                m = max(m, sg.partials[j]);
+        } else if (t == 0) {
+            m = __float_as_uint(*sg.amax);
+        }
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if ((t & 31) == 0 && m != 0u)
+            atomicMax(&s_amax[i], m);
+    }
+    __syncthreads();
+    if (t < nseg) {
+        const float a = __uint_as_float(s_amax[t]);
+        const float sc = scale_of<FMT>(a);
+        s_scale[t] = sc;
+        if (blockIdx.x == 0) {
+            if (set.seg[t].scale_out != nullptr)
+                *set.seg[t].scale_out = sc;
+            if (set.seg[t].amax_out != nullptr)
+                *set.seg[t].amax_out = a;
+        }
+    }
+    __syncthreads();
+
     int64_t k = 0;
     for (; k < nmine; ++k) {
         if (t == 0 && k + kInStages - 1 < nmine)
@@ -572,14 +612,15 @@ cast_transpose_tma_kernel(const __grid_constant__ CUtensorMap tmap0,
         }
         if (__syncthreads_or(abort_flag))
             break;
-        bool second;
+        int sg;
         int64_t r0, c0;
-        locate(blockIdx.x + k * gridDim.x, second, r0, c0);
-        const float s = second ? s1 : s0;
-        const int64_t rows = second ? seg1.rows : seg0.rows;
-        const int64_t cols = second ? seg1.cols : seg0.cols;
-        uint8_t *q = second ? seg1.q : seg0.q;
-        uint8_t *qt = second ? seg1.qt : seg0.qt;
+        locate(k, sg, r0, c0);
+        const CastSeg &seg = set.seg[sg];
+        const float s = s_scale[sg];
+        const int64_t rows = seg.rows;
+        const int64_t cols = seg.cols;
+        uint8_t *q = seg.q;
+        uint8_t *qt = seg.qt;
         const uint8_t *src = sm + b * kInBytes;
         // ---- phase 1: 8 passes of 16 rows; thread t converts 8 consecutive bf16
 #pragma unroll
@@ -599,11 +640,13 @@ cast_transpose_tma_kernel(const __grid_constant__ CUtensorMap tmap0,
             transpose_out(tile, qt, rows, cols, r0, c0, t, status);
         __syncthreads();  // the input buffer and the parked tile are free again
     }
-    if (k < nmine && t == 0) {
+    if (t == 0) {
         // gave up: the loads still in flight must land before the CTA exits
+        // (loads are issued up to kInStages - 1 tiles ahead of k)
         for (int64_t j = k; j < nmine && j < k + kInStages; ++j)
-            mbar_wait(&bar[j % kInStages], static_cast<uint32_t>((j / kInStages) & 1), nullptr,
-                      limit_ns);
+            if (k < nmine)
+                mbar_wait(&bar[j % kInStages], static_cast<uint32_t>((j / kInStages) & 1), nullptr,
+                          limit_ns);
     }
 }
 } // namespace
@@ -633,7 +676,9 @@ const Occupancy &occupancy(const DeviceInfo &dev)
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaCastSmem);
         cudaFuncSetAttribute(cast_transpose_tma_kernel<1, 1>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaCastSmem);
-        cudaFuncSetAttribute(cast_transpose_tma_kernel<0, 2>,
+        cudaFuncSetAttribute(cast_transpose_tma_kernel<0, kMaxQuantTensors>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaCastSmem);
+        cudaFuncSetAttribute(cast_transpose_tma_kernel<1, kMaxQuantTensors>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaCastSmem);
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cast_transpose_tma_kernel<0, 1>,
                                                       kCastThreads, kTmaCastSmem);
@@ -698,7 +743,7 @@ cudaError_t launch_amax_partials(const void *x, int64_t n, unsigned *partials, i
 cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, const float *amax,
                                   const unsigned *partials, int nparts, float *amax_out,
                                   float *scale_out, uint8_t *q, uint8_t *q_t, int fmt,
-                                  const DeviceInfo &dev, cudaStream_t stream)
+                                  const DeviceInfo &dev, cudaStream_t stream, bool early)
 {
     const int64_t ntiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
     CUtensorMap map;
@@ -709,10 +754,16 @@ cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, con
         const int64_t cap = static_cast<int64_t>(dev.sm_count) * occupancy(dev).cast_tma;
         if (blocks > cap)
             blocks = cap;
-        const CastSeg seg{rows, cols, amax, partials, nparts, amax_out, scale_out, q, q_t};
+        CastSet<1> set;
+        set.map[0] = map;
+        set.seg[0] = CastSeg{rows, cols, amax, partials, nparts, amax_out, scale_out, q, q_t};
+        set.first_tile[0] = 0;
+        set.first_tile[1] = ntiles;
+        set.nseg = 1;
+        set.early = early ? 1 : 0;
         return launch_pdl(fmt == 1 ? cast_transpose_tma_kernel<1, 1> : cast_transpose_tma_kernel<0, 1>,
                           dim3(static_cast<unsigned>(blocks)), dim3(kCastThreads), kTmaCastSmem,
-                          stream, map, map, seg, seg, dev.status, wait_limit_ns());
+                          stream, set, dev.status, wait_limit_ns());
     }
     int64_t blocks = ntiles;
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * occupancy(dev).cast;
@@ -775,45 +826,123 @@ cudaError_t launch_swiglu_bwd_amax(const void *dh, const void *ab, void *dab, in
                       static_cast<uint4 *>(dab), nvec, partials, dev.status);
 }
 
-cudaError_t launch_quantize_pair(const void *x0, int64_t rows0, int64_t cols0, const void *x1,
-                                 int64_t rows1, int64_t cols1, unsigned *parts0, unsigned *parts1,
-                                 float *amax0, float *scale0, uint8_t *q0, uint8_t *qt0,
-                                 float *amax1, float *scale1, uint8_t *q1, uint8_t *qt1,
-                                 const DeviceInfo &dev, cudaStream_t stream)
+cudaError_t launch_quantize_multi(const QuantDesc *t, int n, int fmt, unsigned *parts,
+                                  const DeviceInfo &dev, cudaStream_t stream)
 {
-    if (!tma_castable(rows0, cols0) || !tma_castable(rows1, cols1))
-        return cudaErrorNotSupported;
-    CUtensorMap m0, m1;
-    if (!make_tensor_map_2d(&m0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x0, rows0, cols0, kTile, kTile,
-                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_tensor_map_2d(&m1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x1, rows1, cols1, kTile, kTile,
-                            CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorNotSupported;
-    const int64_t nvec0 = rows0 * cols0 / 8, nvec1 = rows1 * cols1 / 8;
+    if (n < 1 || n > kMaxQuantTensors || (fmt != 0 && fmt != 1))
+        return cudaErrorInvalidValue;
+    CastSet<kMaxQuantTensors> set;
+    AmaxSegs segs;
+    int64_t nvec_total = 0;
+    for (int i = 0; i < n; ++i) {
+        if (!tma_castable(t[i].rows, t[i].cols) ||
+            !make_tensor_map_2d(&set.map[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, t[i].x, t[i].rows,
+                                t[i].cols, kTile, kTile, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorNotSupported;
+        segs.x[i] = static_cast<const uint4 *>(t[i].x);
+        segs.nvec[i] = t[i].rows * t[i].cols / 8;
+        nvec_total += segs.nvec[i];
+    }
     const Occupancy &occ = occupancy(dev);
-    // the amax blocks, shared in proportion to the tensors' sizes
-    const int64_t total = amax_grid(nvec0 + nvec1, occ.amax_partials, dev);
-    if (total < 2)
-        return cudaErrorNotSupported;
-    int64_t b0 = (total * nvec0 + (nvec0 + nvec1) / 2) / (nvec0 + nvec1);
-    b0 = b0 < 1 ? 1 : (b0 > total - 1 ? total - 1 : b0);
-    cudaError_t e = launch_pdl(amax_pair_kernel, dim3(static_cast<unsigned>(total)),
-                               dim3(kAmaxThreads), 0, stream, static_cast<const uint4 *>(x0), nvec0,
-                               static_cast<const uint4 *>(x1), nvec1, static_cast<int>(b0), parts0,
-                               parts1, dev.status);
+    // the amax blocks, shared in proportion to the tensors' sizes (each at
+    // least one, at most kMaxAmaxPartials / kMaxQuantTensors)
+    const int64_t total = amax_grid(nvec_total, occ.amax_partials, dev);
+    constexpr int kPartsPer = kMaxAmaxPartials / kMaxQuantTensors;
+    segs.first_block[0] = 0;
+    set.first_tile[0] = 0;
+    for (int i = 0; i < n; ++i) {
+        int64_t b = (total * segs.nvec[i] + nvec_total / 2) / nvec_total;
+        b = b < 1 ? 1 : (b > kPartsPer ? kPartsPer : b);
+        segs.first_block[i + 1] = segs.first_block[i] + static_cast<int>(b);
+        segs.parts[i] = parts + static_cast<size_t>(i) * kPartsPer;
+        set.seg[i] = CastSeg{t[i].rows, t[i].cols, nullptr, segs.parts[i], static_cast<int>(b),
+                             t[i].amax_out, t[i].scale_out, t[i].q, t[i].q_t};
+        set.first_tile[i + 1] = set.first_tile[i] + (t[i].rows / kTile) * (t[i].cols / kTile);
+    }
+    for (int i = n; i < kMaxQuantTensors; ++i) {  // unused entries: copies, never read
+        segs.x[i] = segs.x[0];
+        segs.nvec[i] = 0;
+        segs.parts[i] = segs.parts[0];
+        segs.first_block[i + 1] = segs.first_block[n];
+        set.map[i] = set.map[0];
+        set.seg[i] = set.seg[0];
+        set.first_tile[i + 1] = set.first_tile[n];
+    }
+    segs.nseg = n;
+    set.nseg = n;
+    set.early = 1;  // the amax launch just before only reads the inputs
+    cudaError_t e = launch_pdl(amax_multi_kernel, dim3(static_cast<unsigned>(segs.first_block[n])),
+                               dim3(kAmaxThreads), 0, stream, segs, dev.status);
     if (e != cudaSuccess)
         return e;
-    const int64_t ntiles = (rows0 / kTile) * (cols0 / kTile) + (rows1 / kTile) * (cols1 / kTile);
-    int64_t blocks = ntiles;
+    int64_t blocks = set.first_tile[n];
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * occ.cast_tma;
     if (blocks > cap)
         blocks = cap;
-    const CastSeg s0{rows0, cols0, nullptr, parts0, static_cast<int>(b0), amax0, scale0, q0, qt0};
-    const CastSeg s1{rows1, cols1, nullptr, parts1, static_cast<int>(total - b0), amax1, scale1, q1,
-                     qt1};
-    return launch_pdl(cast_transpose_tma_kernel<0, 2>, dim3(static_cast<unsigned>(blocks)),
-                      dim3(kCastThreads), kTmaCastSmem, stream, m0, m1, s0, s1, dev.status,
-                      wait_limit_ns());
+    return launch_pdl(fmt == 1 ? cast_transpose_tma_kernel<1, kMaxQuantTensors>
+                               : cast_transpose_tma_kernel<0, kMaxQuantTensors>,
+                      dim3(static_cast<unsigned>(blocks)), dim3(kCastThreads), kTmaCastSmem, stream,
+                      set, dev.status, wait_limit_ns());
+}
+
+bool quantize_multi_castable(const QuantDesc *t, int n)
+{
+    for (int i = 0; i < n; ++i)
+        if (!tma_castable(t[i].rows, t[i].cols))
+            return false;
+    return n >= 1 && n <= kMaxQuantTensors;
+}
+
+namespace {
+// Byte transpose out[c, r] = in[r, c] of a [rows, cols] uint8 tensor, 64 x 64
+// tiles through shared memory (a padded row pitch keeps the column reads
+// conflict-free); byte-wide, coalesced accesses.  Used on the FP8 weight
+// all-gather path (q(W)^T of a gathered q(W)), not inside the linear.
+constexpr int kTrTile = 64;
+constexpr int kTrThreads = 256;
+
+__global__ void __launch_bounds__(kTrThreads)
+transpose_u8_kernel(const uint8_t *__restrict__ in, int64_t rows, int64_t cols,
+                    uint8_t *__restrict__ out, unsigned *__restrict__ status)
+{
+    __shared__ uint8_t tile[kTrTile][kTrTile + 1];
+    griddep_wait();
+    griddep_launch_dependents();
+    const int64_t tiles_c = (cols + kTrTile - 1) / kTrTile;
+    const int64_t ntiles = ((rows + kTrTile - 1) / kTrTile) * tiles_c;
+    const int64_t n = rows * cols;
+    for (int64_t tix = blockIdx.x; tix < ntiles; tix += gridDim.x) {
+        const int64_t r0 = (tix / tiles_c) * kTrTile, c0 = (tix % tiles_c) * kTrTile;
+        for (int e = threadIdx.x; e < kTrTile * kTrTile; e += kTrThreads) {
+            const int r = e / kTrTile, c = e % kTrTile;
+            const int64_t o = (r0 + r) * cols + c0 + c;
+            if (r0 + r < rows && c0 + c < cols && in_range(o, 1, n, status))
+                tile[r][c] = in[o];
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < kTrTile * kTrTile; e += kTrThreads) {
+            const int c = e / kTrTile, r = e % kTrTile;
+            const int64_t o = (c0 + c) * rows + r0 + r;
+            if (r0 + r < rows && c0 + c < cols && in_range(o, 1, n, status))
+                out[o] = tile[r][c];
+        }
+        __syncthreads();
+    }
+}
+} // namespace
+
+cudaError_t launch_transpose_u8(const uint8_t *in, int64_t rows, int64_t cols, uint8_t *out,
+                                const DeviceInfo &dev, cudaStream_t stream)
+{
+    const int64_t ntiles = ((rows + kTrTile - 1) / kTrTile) * ((cols + kTrTile - 1) / kTrTile);
+    int64_t blocks = ntiles;
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * 8;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    return launch_pdl(transpose_u8_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kTrThreads), 0,
+                      stream, in, rows, cols, out, dev.status);
 }
 
 namespace {

@@ -31,8 +31,9 @@
 //                 MMAs; its full[s] barriers count the bytes of both CTAs;
 //                 commits are multicast to the barriers of both CTAs; both
 //                 epilogues arrive on the even CTA's tempty barriers.
-// A launch runs one GEMM, or two independent ones (a linear's dgrad and
-// wgrad) whose tiles share the persistent CTAs under the static list
+// A launch runs one GEMM (NP = 1), or up to four independent ones (NP = 4:
+// a linear's dgrad and wgrad; the forward GEMMs of linears that share their
+// input) whose tiles share the persistent CTAs under the static list
 // schedule of f8_sched.h: every role of every CTA derives the same tile
 // sequence from (CTA, i), so nothing is communicated.
 // Tiles are visited in groups of `group_m` M-blocks so that concurrently
@@ -258,9 +259,7 @@ __device__ __forceinline__ void epilogue_rows_glu(uint32_t taddr, int row0, int 
     }
 }
 
-// One GEMM problem of a launch.  A launch runs one problem, or two
-// independent ones (the dgrad and wgrad GEMMs of a linear's backward pass)
-// whose tiles share the persistent CTAs through the schedule of f8_sched.h.
+// One GEMM problem of a launch.
 struct GemmProb {
     __nv_bfloat16 *c;
     const float *sa;
@@ -271,29 +270,61 @@ struct GemmProb {
     uint32_t idesc;
 };
 
-// This unit's i-th tile as a global index ([0, tiles0) problem 0, then
-// problem 1), or -1.  One problem (TWO = false): plain round-robin, the
-// code of a single-GEMM launch; two: the list schedule of f8_sched.h.
-template <bool TWO>
-__device__ __forceinline__ int unit_tile(const TileSched &s, int unit, int i)
+// The problems of one launch and their tensor maps (C's map unused when the
+// problem stores directly).  NP = 1: one problem, its tiles dealt
+// round-robin.  NP > 1: nprob problems in the slot order of f8_sched.h's
+// LaunchPlan; first_tile[i] is slot i's first launch-global tile and sched
+// the list schedule over them.
+template <int NP>
+struct GemmSet {
+    CUtensorMap a[NP], b[NP], c[NP];
+    GemmProb p[NP];
+    int first_tile[NP + 1];
+    int nprob;
+    TileSched sched;
+};
+
+// This unit's i-th tile as a launch-global index, or -1.
+template <int NP>
+__device__ __forceinline__ int unit_tile(const GemmSet<NP> &set, int unit, int i)
 {
-    if (!TWO) {
-        const int t = unit + i * s.units;
-        return t < s.tiles0 ? t : -1;
+    if (NP == 1) {
+        const int t = unit + i * set.sched.units;
+        return t < set.sched.tiles0 ? t : -1;
     }
-    return sched_tile(s, unit, i);
+    return sched_tile(set.sched, unit, i);
 }
 
-template <int BN, int STAGES, bool PAIR, bool GLU, bool TWO>
+// The slot of launch-global tile g, and g's tile index within that problem.
+template <int NP>
+__device__ __forceinline__ int tile_slot(const GemmSet<NP> &set, int g, int &local)
+{
+    if (NP == 1) {
+        local = g;
+        return 0;
+    }
+    return sched_slot(set.first_tile, set.nprob, g, local);
+}
+
+// v[slot] for a slot held in a register, by selects (no local memory).
+template <int NP>
+__device__ __forceinline__ float pick(const float (&v)[NP], int slot)
+{
+    float r = v[0];
+#pragma unroll
+    for (int j = 1; j < NP; ++j)
+        r = slot == j ? v[j] : r;
+    return r;
+}
+
+template <int BN, int STAGES, bool PAIR, bool GLU, int NP>
 __global__ void __launch_bounds__(Cfg<BN, STAGES, PAIR, GLU>::kThreads, 1)
-gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-            const __grid_constant__ CUtensorMap tma_c, const __grid_constant__ CUtensorMap tma_h,
-            const __grid_constant__ CUtensorMap tma_a1, const __grid_constant__ CUtensorMap tma_b1,
-            const __grid_constant__ CUtensorMap tma_c1, const GemmProb p0, const GemmProb p1,
-            const TileSched sched, unsigned *__restrict__ status, uint64_t limit_ns, int group_m,
+gemm_kernel(const __grid_constant__ GemmSet<NP> set, const __grid_constant__ CUtensorMap tma_h,
+            unsigned *__restrict__ status, uint64_t limit_ns, int group_m,
             unsigned *__restrict__ hparts, int hatomic)
 {
     using C = Cfg<BN, STAGES, PAIR, GLU>;
+    static_assert(!GLU || NP == 1, "the SwiGLU epilogue runs single-problem launches");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -314,7 +345,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
     const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const bool two = TWO && sched.tiles1 > 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -331,18 +361,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tma_a);
-        tma_prefetch_desc(&tma_b);
-        if (p0.tma_store)
-            tma_prefetch_desc(&tma_c);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            if (j < set.nprob) {
+                tma_prefetch_desc(&set.a[j]);
+                tma_prefetch_desc(&set.b[j]);
+                if (set.p[j].tma_store)
+                    tma_prefetch_desc(&set.c[j]);
+            }
+        }
         if (GLU)
             tma_prefetch_desc(&tma_h);
-        if (two) {
-            tma_prefetch_desc(&tma_a1);
-            tma_prefetch_desc(&tma_b1);
-            if (p1.tma_store)
-                tma_prefetch_desc(&tma_c1);
-        }
     }
     if (warp == 1) {
         if (PAIR) {
@@ -373,18 +402,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
             int64_t issued = 0;
             bool stop = false;
             for (int i = 0; !stop; ++i) {
-                int tile = unit_tile<TWO>(sched, unit, i);
-                if (tile < 0)
+                const int g = unit_tile<NP>(set, unit, i);
+                if (g < 0)
                     break;
-                const bool second = TWO && tile >= sched.tiles0;
-                if (second)
-                    tile -= sched.tiles0;
-                const CUtensorMap *ma = second ? &tma_a1 : &tma_a;
-                const CUtensorMap *mb_ = second ? &tma_b1 : &tma_b;
-                const int num_kb = second ? p1.num_kb : p0.num_kb;
+                int tile;
+                const int slot = tile_slot<NP>(set, g, tile);
+                const CUtensorMap *ma = &set.a[slot];
+                const CUtensorMap *mb_ = &set.b[slot];
+                const GemmProb &pr = set.p[slot];
+                const int num_kb = pr.num_kb;
                 int mb, nb;
-                tile_coords(tile, second ? p1.num_m : p0.num_m, second ? p1.num_n : p0.num_n,
-                            group_m, mb, nb);
+                tile_coords(tile, pr.num_m, pr.num_n, group_m, mb, nb);
                 const int arow = mb * C::kTileM + static_cast<int>(rank) * kBM;
                 const int brow = nb * BN + static_cast<int>(rank) * C::kBRows;
                 for (int kb = 0; kb < num_kb; ++kb) {
@@ -449,12 +477,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
             bool stop = false;
             int local = 0;
             for (;; ++local) {
-                const int tile = unit_tile<TWO>(sched, unit, local);
-                if (tile < 0)
+                const int g = unit_tile<NP>(set, unit, local);
+                if (g < 0)
                     break;
-                const bool second = TWO && tile >= sched.tiles0;
-                const int num_kb = second ? p1.num_kb : p0.num_kb;
-                const uint32_t idesc = second ? p1.idesc : p0.idesc;
+                int tile;
+                const int slot = tile_slot<NP>(set, g, tile);
+                const int num_kb = set.p[slot].num_kb;
+                const uint32_t idesc = set.p[slot].idesc;
                 const uint32_t acc = local & 1;
                 const uint32_t aph = (local >> 1) & 1;
                 if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, limit_ns)) {
@@ -507,22 +536,23 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
     } else {
         // ---------------------------------------------------- epilogue
         const int quad = warp & 3;  // the TMEM lane quarter this warp may read
-        const float inv0 = static_cast<float>(1.0 / (static_cast<double>(*p0.sa) *
-                                                      static_cast<double>(*p0.sb)));
-        const float inv1 = two ? static_cast<float>(1.0 / (static_cast<double>(*p1.sa) *
-                                                            static_cast<double>(*p1.sb)))
-                               : inv0;
+        float inv[NP];
+#pragma unroll
+        for (int j = 0; j < NP; ++j)
+            inv[j] = j < set.nprob ? static_cast<float>(1.0 / (static_cast<double>(*set.p[j].sa) *
+                                                               static_cast<double>(*set.p[j].sb)))
+                                   : 0.0f;
         uint8_t *my_stage = staging + (warp - 2) * C::kWarpStaging;
         uint32_t hmax2 = 0;
         const uint32_t tempty_leader = PAIR ? cluster_map(smem_addr(&tempty[0]), 0) : 0u;
         uint32_t buf = 0;
         for (int local = 0;; ++local) {
-            int tile = unit_tile<TWO>(sched, unit, local);
-            if (tile < 0)
+            const int g = unit_tile<NP>(set, unit, local);
+            if (g < 0)
                 break;
-            const bool second = TWO && tile >= sched.tiles0;
-            if (second)
-                tile -= sched.tiles0;
+            int tile;
+            const int slot = tile_slot<NP>(set, g, tile);
+            const GemmProb &pr = set.p[slot];
             const uint32_t acc = local & 1;
             const uint32_t aph = (local >> 1) & 1;
             bool ok = mbar_wait(&tfull[acc], aph, abort_flag, limit_ns);
@@ -534,19 +564,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ C
             }
             tc_fence_after_sync();
             int mb, nb;
-            tile_coords(tile, second ? p1.num_m : p0.num_m, second ? p1.num_n : p0.num_n, group_m,
-                        mb, nb);
+            tile_coords(tile, pr.num_m, pr.num_n, group_m, mb, nb);
             const int row0 = mb * C::kTileM + static_cast<int>(rank) * kBM + quad * 32;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
             if (GLU)
-                epilogue_rows_glu(taddr, row0, nb * BN, p0.M, inv0, &tma_c, &tma_h, my_stage,
+                epilogue_rows_glu(taddr, row0, nb * BN, pr.M, inv[0], &set.c[0], &tma_h, my_stage,
                                   hmax2, lane);
-            else if (second)
-                epilogue_rows<BN>(taddr, row0, nb * BN, p1.M, p1.N, inv1, p1.c, &tma_c1,
-                                  p1.tma_store != 0, my_stage, buf, lane, status);
             else
-                epilogue_rows<BN>(taddr, row0, nb * BN, p0.M, p0.N, inv0, p0.c, &tma_c,
-                                  p0.tma_store != 0, my_stage, buf, lane, status);
+                epilogue_rows<BN>(taddr, row0, nb * BN, pr.M, pr.N, pick<NP>(inv, slot), pr.c,
+                                  &set.c[slot], pr.tma_store != 0, my_stage, buf, lane, status);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
@@ -642,27 +668,22 @@ bool make_map(CUtensorMap *map, CUtensorMapDataType dtype, int esize, const void
 
 static_assert(kBK == kSchedBlockK, "the schedule's tile costs count the kernel's K blocks");
 
-// The schedule planner's view of a launch's problems.
-SchedPlan plan_launch(const GemmDesc *probs, int nprob, int tile_m, int bn, int64_t max_units)
-{
-    SchedProblem p[2];
-    for (int i = 0; i < nprob; ++i)
-        p[i] = SchedProblem{probs[i].M, probs[i].N, probs[i].K};
-    return sched_plan(p, nprob, tile_m, bn, max_units);
-}
-
-template <int BN, int STAGES, bool PAIR, bool GLU = false, bool TWO = false>
-cudaError_t run_gemm(const GemmDesc *probs, int nprob, const DeviceInfo &dev, cudaStream_t stream,
-                     void *h = nullptr, unsigned *hparts = nullptr, int *nparts = nullptr,
-                     int hatomic = 0)
+// One launch of gemm_kernel over the problems probs[plan.order[0 .. n)]
+// (n = 1 for NP = 1), in the plan's slot order.
+template <int BN, int STAGES, bool PAIR, bool GLU = false, int NP = 1>
+cudaError_t run_gemm(const GemmDesc *probs, const LaunchPlan &plan, const DeviceInfo &dev,
+                     cudaStream_t stream, void *h = nullptr, unsigned *hparts = nullptr,
+                     int *nparts = nullptr, int hatomic = 0)
 {
     using C = Cfg<BN, STAGES, PAIR, GLU>;
-    CUtensorMap ma[2], mb[2], mc[2], mh;
-    GemmProb gp[2];
-    for (int i = 0; i < nprob; ++i) {
-        const GemmDesc &p = probs[i];
-        if (!make_map(&ma[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.a, p.M, p.K, kBK, kBM) ||
-            !make_map(&mb[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.b, p.N, p.K, kBK, C::kBRows))
+    if (!plan.ok || plan.nprob < 1 || plan.nprob > NP)
+        return cudaErrorInvalidValue;
+    GemmSet<NP> set;
+    CUtensorMap mh;
+    for (int i = 0; i < plan.nprob; ++i) {
+        const GemmDesc &p = probs[plan.order[i]];
+        if (!make_map(&set.a[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.a, p.M, p.K, kBK, kBM) ||
+            !make_map(&set.b[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.b, p.N, p.K, kBK, C::kBRows))
             return cudaErrorNotSupported;
         // TMA stores need every C row to start on a 16-byte boundary
         int tma_store;
@@ -670,57 +691,54 @@ cudaError_t run_gemm(const GemmDesc *probs, int nprob, const DeviceInfo &dev, cu
             // AB and h through 32-row x 32-column boxes in the 64-byte swizzle
             tma_store = 1;
             if (p.N % 256 != 0 ||
-                !make_tensor_map_2d(&mc[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.c, p.M, p.N,
+                !make_tensor_map_2d(&set.c[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.c, p.M, p.N,
                                     kGluCols, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
                 !make_tensor_map_2d(&mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, p.M, p.N / 2,
                                     kGluCols, 32, CU_TENSOR_MAP_SWIZZLE_64B))
                 return cudaErrorNotSupported;
         } else {
-            tma_store = (p.N % 8 == 0) && make_map(&mc[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            tma_store = (p.N % 8 == 0) && make_map(&set.c[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                                                    p.c, p.M, p.N, kEpiCols, 32);
             if (!tma_store)
-                mc[i] = ma[i];  // not used by the kernel
+                set.c[i] = set.a[i];  // not used by the kernel
         }
         const int num_m = static_cast<int>((p.M + C::kTileM - 1) / C::kTileM);
         const int num_n = static_cast<int>((p.N + BN - 1) / BN);
         const int num_kb = static_cast<int>((p.K + kBK - 1) / kBK);
-        gp[i] = GemmProb{static_cast<__nv_bfloat16 *>(p.c), p.sa, p.sb, static_cast<int>(p.M),
-                         static_cast<int>(p.N), num_m, num_n, num_kb, tma_store,
-                         idesc_f8_f32(C::kTileM, BN, static_cast<uint32_t>(p.fa),
-                                      static_cast<uint32_t>(p.fb))};
+        set.p[i] = GemmProb{static_cast<__nv_bfloat16 *>(p.c), p.sa, p.sb, static_cast<int>(p.M),
+                            static_cast<int>(p.N), num_m, num_n, num_kb, tma_store,
+                            idesc_f8_f32(C::kTileM, BN, static_cast<uint32_t>(p.fa),
+                                         static_cast<uint32_t>(p.fb))};
     }
+    for (int i = plan.nprob; i < NP; ++i) {  // unused slots: copies, never read
+        set.a[i] = set.a[0];
+        set.b[i] = set.b[0];
+        set.c[i] = set.c[0];
+        set.p[i] = set.p[0];
+    }
+    for (int i = 0; i <= NP; ++i)
+        set.first_tile[i] = i <= plan.nprob ? plan.first_tile[i] : plan.first_tile[plan.nprob];
+    set.nprob = plan.nprob;
+    set.sched = plan.s;
     if (!GLU)
-        mh = ma[0];  // not used by the kernel
-    if (nprob == 1) {
-        ma[1] = ma[0];
-        mb[1] = mb[0];
-        mc[1] = mc[0];
-        gp[1] = gp[0];
-    }
+        mh = set.a[0];  // not used by the kernel
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
     const int dv = dev.ordinal & 63;
     std::call_once(attr_once[dv], [&] {
-        attr_err[dv] = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, PAIR, GLU, TWO>,
+        attr_err[dv] = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, PAIR, GLU, NP>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             C::kSmemBytes);
     });
     if (attr_err[dv] != cudaSuccess)
         return attr_err[dv];
-    const SchedPlan plan =
-        plan_launch(probs, nprob, C::kTileM, BN, PAIR ? dev.sm_count / 2 : dev.sm_count);
-    const TileSched &sched = plan.s;
-    const int units = sched.units;
-    const int first = plan.first;
-    const int second = nprob == 2 ? 1 - first : first;
+    const int units = plan.s.units;
     const int group_m = PAIR ? 8 : 16;
     if (nparts != nullptr)
         *nparts = (PAIR ? 2 : 1) * units;
-    return launch_pdl_cluster(gemm_kernel<BN, STAGES, PAIR, GLU, TWO>, dim3((PAIR ? 2 : 1) * units),
-                              dim3(C::kThreads), C::kSmemBytes, stream, PAIR ? 2u : 1u,
-                              ma[first], mb[first], mc[first], mh, ma[second], mb[second],
-                              mc[second], gp[first], gp[second], sched, dev.status,
-                              wait_limit_ns(), group_m, hparts, hatomic);
+    return launch_pdl_cluster(gemm_kernel<BN, STAGES, PAIR, GLU, NP>, dim3((PAIR ? 2 : 1) * units),
+                              dim3(C::kThreads), C::kSmemBytes, stream, PAIR ? 2u : 1u, set, mh,
+                              dev.status, wait_limit_ns(), group_m, hparts, hatomic);
 }
 
 constexpr int kVariantSingle = 1;
@@ -757,40 +775,99 @@ bool make_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, int esize, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+
+// Tile geometry of a kernel variant.
+int variant_tile_m(int v) { return v == kVariantPair ? 2 * kBM : kBM; }
+
+int64_t variant_units(int v, const DeviceInfo &dev)
+{
+    return v == kVariantPair ? dev.sm_count / 2 : dev.sm_count;
+}
+
+SchedProblem sched_problem(const GemmDesc &g) { return SchedProblem{g.M, g.N, g.K}; }
+
+// One launch over probs[idx[0 .. n)], all of kernel variant v.
+cudaError_t launch_set(const GemmDesc *probs, const int *idx, int n, int v, const DeviceInfo &dev,
+                       cudaStream_t stream)
+{
+    SchedProblem sp[kMaxLaunchProblems];
+    for (int i = 0; i < n; ++i)
+        sp[i] = sched_problem(probs[idx[i]]);
+    int local[kMaxLaunchProblems];
+    for (int i = 0; i < n; ++i)
+        local[i] = i;
+    LaunchPlan plan = sched_plan_idx(sp, local, n, variant_tile_m(v), 256, variant_units(v, dev));
+    if (!plan.ok)
+        return cudaErrorInvalidValue;
+    GemmDesc g[kMaxLaunchProblems];
+    for (int i = 0; i < n; ++i)
+        g[i] = probs[idx[i]];
+    if (n == 1)
+        return v == kVariantPair ? run_gemm<256, 6, true>(g, plan, dev, stream)
+                                 : run_gemm<256, 4, false>(g, plan, dev, stream);
+    return v == kVariantPair ? run_gemm<256, 6, true, false, kMaxLaunchProblems>(g, plan, dev, stream)
+                             : run_gemm<256, 4, false, false, kMaxLaunchProblems>(g, plan, dev, stream);
+}
+
+} // namespace
+
 cudaError_t launch_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N, int64_t K,
                         const float *sa, const float *sb, void *c, const DeviceInfo &dev,
                         cudaStream_t stream, int fa, int fb)
 {
     const GemmDesc g{a, b, M, N, K, sa, sb, c, fa, fb};
-    if (gemm_variant(M, dev) == kVariantPair)
-        return run_gemm<256, 6, true>(&g, 1, dev, stream);
-    return run_gemm<256, 4, false>(&g, 1, dev, stream);
+    const int idx = 0;
+    return launch_set(&g, &idx, 1, gemm_variant(M, dev), dev, stream);
+}
+
+cudaError_t launch_gemm_multi(const GemmDesc *g, int n, const DeviceInfo &dev, cudaStream_t stream)
+{
+    if (n < 1 || n > kMaxPartitionProblems)
+        return cudaErrorInvalidValue;
+    // problems of different kernel variants never share a launch
+    const int v0 = gemm_variant(g[0].M, dev);
+    bool same = true;
+    for (int i = 1; i < n; ++i)
+        same = same && gemm_variant(g[i].M, dev) == v0;
+    const int mode = gemm_group_mode();
+    if (n == 1 || !same || mode == kGroupNever) {
+        for (int i = 0; i < n; ++i) {
+            const cudaError_t e = launch_set(g, &i, 1, gemm_variant(g[i].M, dev), dev, stream);
+            if (e != cudaSuccess)
+                return e;
+        }
+        return cudaSuccess;
+    }
+    SchedProblem sp[kMaxPartitionProblems];
+    for (int i = 0; i < n; ++i)
+        sp[i] = sched_problem(g[i]);
+    Partition part;
+    int all[kMaxLaunchProblems];
+    for (int i = 0; i < n && i < kMaxLaunchProblems; ++i)
+        all[i] = i;
+    if (mode == kGroupAlways && n <= kMaxLaunchProblems &&
+        sched_plan_idx(sp, all, n, variant_tile_m(v0), 256, variant_units(v0, dev)).ok) {
+        part.nlaunch = 1;
+        part.nprob[0] = n;
+        for (int i = 0; i < n; ++i)
+            part.idx[0][i] = i;
+    } else {
+        part = sched_partition(sp, n, variant_tile_m(v0), 256, variant_units(v0, dev));
+    }
+    for (int j = 0; j < part.nlaunch; ++j) {
+        const cudaError_t e = launch_set(g, part.idx[j], part.nprob[j], v0, dev, stream);
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_gemm2(const GemmDesc &g0, const GemmDesc &g1, const DeviceInfo &dev,
                          cudaStream_t stream)
 {
-    const int v = gemm_variant(g0.M, dev);
-    const int mode = gemm_group_mode();
-    bool group = mode != kGroupNever && v == gemm_variant(g1.M, dev);
-    if (group && mode == kGroupAuto) {
-        const int tile_m = v == kVariantPair ? 2 * kBM : kBM;
-        const int64_t max_units = v == kVariantPair ? dev.sm_count / 2 : dev.sm_count;
-        group = sched_should_group(SchedProblem{g0.M, g0.N, g0.K}, SchedProblem{g1.M, g1.N, g1.K},
-                                   tile_m, 256, max_units);
-    }
-    if (!group) {
-        cudaError_t e = launch_gemm(g0.a, g0.b, g0.M, g0.N, g0.K, g0.sa, g0.sb, g0.c, dev, stream,
-                                    g0.fa, g0.fb);
-        if (e != cudaSuccess)
-            return e;
-        return launch_gemm(g1.a, g1.b, g1.M, g1.N, g1.K, g1.sa, g1.sb, g1.c, dev, stream, g1.fa,
-                           g1.fb);
-    }
     const GemmDesc g[2] = {g0, g1};
-    if (v == kVariantPair)
-        return run_gemm<256, 6, true, false, true>(g, 2, dev, stream);
-    return run_gemm<256, 4, false, false, true>(g, 2, dev, stream);
+    return launch_gemm_multi(g, 2, dev, stream);
 }
 
 cudaError_t launch_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int64_t M, int64_t F,
@@ -801,10 +878,13 @@ cudaError_t launch_gemm_w13_swiglu(const uint8_t *x_q, const uint8_t *w13_q, int
     if (F % 128 != 0)
         return cudaErrorInvalidValue;
     const GemmDesc g{x_q, w13_q, M, 2 * F, K, sx, sw, ab, 0, 0};
-    if (gemm_variant(M, dev) == kVariantPair)
-        return run_gemm<256, 6, true, true>(&g, 1, dev, stream, h, hparts, nparts,
+    const int v = gemm_variant(M, dev);
+    const SchedProblem sp = sched_problem(g);
+    const LaunchPlan plan = sched_plan(&sp, 1, variant_tile_m(v), 256, variant_units(v, dev));
+    if (v == kVariantPair)
+        return run_gemm<256, 6, true, true>(&g, plan, dev, stream, h, hparts, nparts,
                                             hatomic ? 1 : 0);
-    return run_gemm<256, 4, false, true>(&g, 1, dev, stream, h, hparts, nparts, hatomic ? 1 : 0);
+    return run_gemm<256, 4, false, true>(&g, plan, dev, stream, h, hparts, nparts, hatomic ? 1 : 0);
 }
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, const DeviceInfo &dev, cudaStream_t stream)

@@ -9,6 +9,8 @@
 #include <atomic>
 #include <utility>
 
+#include "f8.h"
+
 namespace f8 {
 
 struct DeviceInfo {
@@ -48,9 +50,11 @@ inline bool quant_pair_enabled()
     return e == nullptr || e[0] != '0';
 }
 
-// Whether launch_gemm2 puts two GEMMs in one launch: F8_GEMM_GROUP=0 never,
-// =2 always, otherwise (1 or unset) when the schedule's predicted makespan
-// beats two launches by the margin launch_gemm2 asks for.
+// Whether launch_gemm_multi puts several GEMMs in one launch:
+// F8_GEMM_GROUP=0 never, =2 always (all in one launch where one launch can
+// take them), otherwise (1 or unset) as sched_partition plans it: shared
+// launches only where the predicted time beats one launch per GEMM by the
+// planner's margin.
 constexpr int kGroupNever = 0;
 constexpr int kGroupAuto = 1;
 constexpr int kGroupAlways = 2;
@@ -135,9 +139,37 @@ cudaError_t launch_amax_partials(const void *x, int64_t n, unsigned *partials, i
 // from the maximum of `nparts` partial maxima, which is then also stored to
 // `amax_out` (if non-null).
 // fmt: 0 = E4M3 (scale 448/amax), 1 = E5M2 (scale 57344/amax).
+// early: the launch just before this one on the stream only read x (its
+// amax pass), so x is complete when this kernel starts and its first tiles
+// may be loaded before the dependency wait.  Leave it false after a kernel
+// that writes x.
 cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, const float *amax,
                                   const unsigned *partials, int nparts, float *amax_out,
                                   float *scale_out, uint8_t *q, uint8_t *q_t, int fmt,
+                                  const DeviceInfo &dev, cudaStream_t stream, bool early = false);
+
+// Most tensors one multi-tensor quantisation launch pair takes.
+constexpr int kMaxQuantTensors = 8;
+
+// One tensor of a multi-tensor quantisation: bf16 [rows, cols] in, its amax
+// and scale (device fp32) and its codes (either may be null) out.
+struct QuantDesc {
+    const void *x;
+    int64_t rows, cols;
+    float *amax_out, *scale_out;
+    uint8_t *q, *q_t;
+};
+
+// Whether launch_quantize_multi takes these tensors (every side a multiple
+// of 128, the TMA cast enabled, 1 <= n <= kMaxQuantTensors).
+bool quantize_multi_castable(const QuantDesc *t, int n);
+
+// Dynamic tensorwise quantisation of n tensors, each with its own amax and
+// scale, in two launches: one amax launch whose blocks are split between the
+// tensors in proportion to their sizes (partial maxima in `parts`, which
+// holds kMaxAmaxPartials), then one TMA cast launch over all their tiles.
+// cudaErrorNotSupported (nothing launched) unless quantize_multi_castable.
+cudaError_t launch_quantize_multi(const QuantDesc *t, int n, int fmt, unsigned *parts,
                                   const DeviceInfo &dev, cudaStream_t stream);
 
 // h = bf16(silu(a) * b) for two [rows, cols] bf16 tensors written to `h`
@@ -154,7 +186,7 @@ cudaError_t launch_gemm(const uint8_t *a, const uint8_t *b, int64_t M, int64_t N
                         const float *sa, const float *sb, void *c, const DeviceInfo &dev,
                         cudaStream_t stream, int fa = 0, int fb = 0);
 
-// One GEMM as launch_gemm2 takes it: C[M,N] = bf16(A[M,K] B[N,K]^T / (sa sb)).
+// One GEMM as launch_gemm_multi takes it: C[M,N] = bf16(A[M,K] B[N,K]^T / (sa sb)).
 struct GemmDesc {
     const uint8_t *a;
     const uint8_t *b;
@@ -165,12 +197,17 @@ struct GemmDesc {
     int fa, fb;
 };
 
-// Two independent GEMMs in one persistent launch: the problem with the
-// costlier tiles is dealt round-robin over the CTAs, the other's tiles then
+// n (<= 8) independent GEMMs in as few persistent launches as pay:
+// f8_sched.h's sched_partition groups problems of at most two tile costs
+// (K extents) into launches of up to four; within a launch the costlier
+// class is dealt round-robin over the CTAs and the other class's tiles then
 // go, in order, to the CTA that frees up first (a static list schedule each
-// CTA evaluates in closed form).  Two plain launches if the shapes need
-// different kernels, or if the schedule does not promise a clear gain over
-// two launches (gemm_group_mode).
+// CTA evaluates in closed form).  Problems that need different kernels (the
+// CTA-pair kernel for M >= 256, the single-CTA one below) never share a
+// launch.
+cudaError_t launch_gemm_multi(const GemmDesc *g, int n, const DeviceInfo &dev, cudaStream_t stream);
+
+// launch_gemm_multi of two problems.
 cudaError_t launch_gemm2(const GemmDesc &g0, const GemmDesc &g1, const DeviceInfo &dev,
                          cudaStream_t stream);
 
@@ -191,16 +228,24 @@ cudaError_t launch_swiglu_bwd_amax(const void *dh, const void *ab, void *dab, in
                                    unsigned *partials, int *nparts, const DeviceInfo &dev,
                                    cudaStream_t stream);
 
-// E4M3 quantisation of two bf16 tensors in two launches instead of four:
-// one amax launch writing each tensor's partial maxima (parts0, parts1), then
-// one TMA cast launch over the tiles of both.  cudaErrorNotSupported (and
-// nothing launched) unless both shapes are multiples of 128 and the TMA cast
-// is enabled.
-cudaError_t launch_quantize_pair(const void *x0, int64_t rows0, int64_t cols0, const void *x1,
-                                 int64_t rows1, int64_t cols1, unsigned *parts0, unsigned *parts1,
-                                 float *amax0, float *scale0, uint8_t *q0, uint8_t *qt0,
-                                 float *amax1, float *scale1, uint8_t *q1, uint8_t *qt1,
-                                 const DeviceInfo &dev, cudaStream_t stream);
+// out[c, r] = in[r, c] for a [rows, cols] uint8 tensor (rows, cols >= 1).
+cudaError_t launch_transpose_u8(const uint8_t *in, int64_t rows, int64_t cols, uint8_t *out,
+                                const DeviceInfo &dev, cudaStream_t stream);
+
+// The argument rules of a linear (M, N, K multiples of 16 and > 0, tile
+// counts within the kernels' 32-bit index) and of its saved tensors, as
+// f8_linear_fwd / f8_linear_bwd apply them.
+f8_status check_linear_shape(int64_t M, int64_t N, int64_t K);
+f8_status check_saved(const f8_linear_saved *s);
+
+// Workspace bytes f8_linear_fwd needs (its row-major E4M3 copies of X and W
+// and the amax partial maxima), for a shape that passed check_linear_shape.
+size_t linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K);
+
+// f8_linear_fwd itself: argument checks, then its launches with `workspace`.
+f8_status linear_fwd_impl(const void *x, const void *w, int64_t M, int64_t N, int64_t K, void *y,
+                          const f8_linear_saved *saved, void *workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
 
 // Whether this library was built with the device bounds checks
 // (-DF8_BOUNDS_CHECK), and a one-thread kernel that makes one such check

@@ -1,17 +1,20 @@
-// Static tile schedule for one persistent GEMM launch that runs two
-// independent problems (the dgrad and wgrad GEMMs of a linear's backward
-// pass, which both read q(dY)).  Plain integer code, usable from host and
-// device.
+// Static tile schedule for one persistent GEMM launch that runs several
+// independent problems (a linear's dgrad and wgrad, which both read q(dY);
+// the forward GEMMs of linears that share their input X).  Plain integer
+// code, usable from host and device.
 //
-// U workers (CTAs, or CTA pairs) share T0 tiles of problem 0, each costing
-// c0, and T1 tiles of problem 1, each costing c1 (a model of the tile's run
-// time; the host puts the problem with the larger cost first).  Problem 0 is
-// dealt round-robin: worker u takes tiles u, u + U, u + 2U, ...  and is then
-// free at T_u = n0(u) c0.  Problem 1's tiles are then handed out in order,
-// each to the worker that is free first (ties: lower worker index first);
-// a worker is free again c1 after it took one.  That is list scheduling of
-// the second problem behind the first, and it keeps consecutive tiles of
-// problem 1 on concurrently running workers (the raster order's L2 reuse).
+// The problems of a launch fall into two cost classes: every tile of class
+// 0 costs c0, every tile of class 1 costs c1 (a model of the tile's run
+// time: its K blocks plus a fixed share; the host puts the costlier class
+// first).  Within a class the problems' tiles are numbered one after the
+// other.  U workers (CTAs, or CTA pairs) share the T0 tiles of class 0 and
+// the T1 tiles of class 1.  Class 0 is dealt round-robin: worker u takes
+// tiles u, u + U, u + 2U, ...  and is then free at T_u = n0(u) c0.  Class
+// 1's tiles are then handed out in order, each to the worker that is free
+// first (ties: lower worker index first); a worker is free again c1 after it
+// took one.  That is list scheduling of the second class behind the first,
+// and it keeps consecutive tiles on concurrently running workers (the raster
+// order's L2 reuse).
 //
 // Nothing is communicated: the free-time events form two arithmetic
 // sequences (workers u < T0 mod U start at (q0 + 1) c0, the rest at q0 c0,
@@ -36,6 +39,21 @@ struct TileSched {
     int cost0;    // c0 >= 1
     int cost1;    // c1 >= 1
 };
+
+// Most problems one launch runs.
+constexpr int kMaxLaunchProblems = 4;
+
+// Problem slot of a launch-global tile index g, and g's index within that
+// problem: first_tile[i] is the global index of slot i's first tile
+// (first_tile[nprob] = the launch's tile count).
+F8_SCHED_FN int sched_slot(const int *first_tile, int nprob, int g, int &local)
+{
+    int slot = 0;
+    for (int i = 1; i < kMaxLaunchProblems; ++i)
+        slot += (i < nprob && g >= first_tile[i]) ? 1 : 0;
+    local = g - first_tile[slot];
+    return slot;
+}
 
 // events start, start + c, start + 2c, ... that fall strictly before t
 F8_SCHED_FN int64_t sched_events_before(int64_t t, int64_t start, int64_t c)
@@ -112,41 +130,108 @@ constexpr int kSchedTileOverheadKb = 4;
 // 0-2%, power-capped) lose up to 2% when grouped.
 constexpr int kSchedMinGainPct = 4;
 
+// Per-launch cost in the same unit (K blocks): the ramp of a persistent
+// launch (pipeline fill, the first tiles' loads) and its drain (the last
+// tiles' epilogues).  Measured: the 128 tiles of an 8192 x 1024 x 4096 GEMM
+// take 28.8 us alone, two rounds of 36 K blocks, where the 512-tile
+// 8192 x 4096 x 4096 GEMM spends 11.4 us a round: about 6 us, 19 K blocks,
+// more than its rounds.
+constexpr int kSchedLaunchOverheadKb = 16;
+
 // The extents of one GEMM C[M,N] = A[M,K] B[N,K]^T.
 struct SchedProblem {
     int64_t M, N, K;
 };
 
-// The schedule of one launch over `nprob` (1 or 2) problems in tile_m x bn
-// output tiles on at most max_units workers; `first` is the index of the
-// problem dealt round-robin (the one with the costlier tiles).
-struct SchedPlan {
+// One launch over nprob (1 .. kMaxLaunchProblems) problems in tile_m x bn
+// output tiles: the schedule, the caller's problem index of each slot
+// (class 0's problems first, each class in the caller's order), and the
+// first global tile of each slot.
+struct LaunchPlan {
     TileSched s;
-    int first;
+    int nprob;
+    int nclass0;                          // slots [0, nclass0) are class 0
+    int order[kMaxLaunchProblems];
+    int first_tile[kMaxLaunchProblems + 1];
+    bool ok;                              // false: more than two tile costs
 };
 
-static inline SchedPlan sched_plan(const SchedProblem *p, int nprob, int tile_m, int bn,
-                                   int64_t max_units)
+static inline int64_t sched_tiles(const SchedProblem &p, int tile_m, int bn)
 {
-    int tiles[2] = {0, 0};
-    int cost[2] = {1, 1};
-    for (int i = 0; i < nprob; ++i) {
-        tiles[i] = static_cast<int>(((p[i].M + tile_m - 1) / tile_m) * ((p[i].N + bn - 1) / bn));
-        cost[i] = static_cast<int>((p[i].K + kSchedBlockK - 1) / kSchedBlockK) +
-                  kSchedTileOverheadKb;
+    return ((p.M + tile_m - 1) / tile_m) * ((p.N + bn - 1) / bn);
+}
+
+static inline int sched_cost(const SchedProblem &p)
+{
+    return static_cast<int>((p.K + kSchedBlockK - 1) / kSchedBlockK) + kSchedTileOverheadKb;
+}
+
+// The plan of one launch over problems p[idx[0 .. n)] on at most max_units
+// workers.  ok = false if their tiles have more than two costs.
+static inline LaunchPlan sched_plan_idx(const SchedProblem *p, const int *idx, int n, int tile_m,
+                                        int bn, int64_t max_units)
+{
+    LaunchPlan pl;
+    pl.nprob = n;
+    pl.nclass0 = 0;
+    pl.ok = n >= 1 && n <= kMaxLaunchProblems;
+    // the distinct tile costs: at most two
+    int c_hi = 0, c_lo = 0;
+    for (int i = 0; i < n && pl.ok; ++i) {
+        const int c = sched_cost(p[idx[i]]);
+        if (c == c_hi || c == c_lo)
+            continue;
+        if (c_hi == 0)
+            c_hi = c;
+        else if (c_lo == 0)
+            c_lo = c;
+        else
+            pl.ok = false;
     }
-    const int64_t total = static_cast<int64_t>(tiles[0]) + tiles[1];
-    const int units = static_cast<int>(total < max_units ? total : max_units);
-    const int first = (nprob == 2 && cost[1] > cost[0]) ? 1 : 0;
-    const int second = nprob == 2 ? 1 - first : first;
-    SchedPlan plan;
-    plan.s.units = units;
-    plan.s.tiles0 = tiles[first];
-    plan.s.tiles1 = nprob == 2 ? tiles[second] : 0;
-    plan.s.cost0 = cost[first];
-    plan.s.cost1 = cost[second];
-    plan.first = first;
-    return plan;
+    if (c_lo > c_hi) {
+        const int t = c_hi;
+        c_hi = c_lo;
+        c_lo = t;
+    }
+    int k = 0;
+    int64_t t0 = 0, t1 = 0;
+    pl.first_tile[0] = 0;
+    for (int pass = 0; pass < 2 && pl.ok; ++pass) {
+        for (int i = 0; i < n; ++i) {
+            const bool hi = sched_cost(p[idx[i]]) == c_hi;
+            if (hi != (pass == 0))
+                continue;
+            const int64_t t = sched_tiles(p[idx[i]], tile_m, bn);
+            pl.order[k] = idx[i];
+            pl.first_tile[k + 1] = static_cast<int>(pl.first_tile[k] + t);
+            (pass == 0 ? t0 : t1) += t;
+            ++k;
+        }
+        if (pass == 0)
+            pl.nclass0 = k;
+    }
+    const int64_t total = t0 + t1;
+    pl.s.units = static_cast<int>(total < max_units ? (total > 0 ? total : 1) : max_units);
+    pl.s.tiles0 = static_cast<int>(t0);
+    pl.s.tiles1 = static_cast<int>(t1);
+    pl.s.cost0 = c_hi > 0 ? c_hi : 1;
+    pl.s.cost1 = c_lo > 0 ? c_lo : pl.s.cost0;
+    return pl;
+}
+
+static inline LaunchPlan sched_plan(const SchedProblem *p, int n, int tile_m, int bn,
+                                    int64_t max_units)
+{
+    int idx[kMaxLaunchProblems];
+    for (int i = 0; i < n && i < kMaxLaunchProblems; ++i)
+        idx[i] = i;
+    return sched_plan_idx(p, idx, n, tile_m, bn, max_units);
+}
+
+// Predicted time of a launch: its busiest worker plus the launch's own cost.
+static inline int64_t sched_launch_time(const LaunchPlan &pl)
+{
+    return sched_makespan(pl.s) + kSchedLaunchOverheadKb;
 }
 
 // Whether two GEMMs should share one launch: the schedule's predicted
@@ -155,10 +240,121 @@ static inline bool sched_should_group(const SchedProblem &p0, const SchedProblem
                                       int bn, int64_t max_units)
 {
     const SchedProblem both[2] = {p0, p1};
-    const int64_t grouped = sched_makespan(sched_plan(both, 2, tile_m, bn, max_units).s);
-    const int64_t apart = sched_makespan(sched_plan(&p0, 1, tile_m, bn, max_units).s) +
-                          sched_makespan(sched_plan(&p1, 1, tile_m, bn, max_units).s);
+    const int64_t grouped = sched_launch_time(sched_plan(both, 2, tile_m, bn, max_units));
+    const int64_t apart = sched_launch_time(sched_plan(&p0, 1, tile_m, bn, max_units)) +
+                          sched_launch_time(sched_plan(&p1, 1, tile_m, bn, max_units));
     return grouped * 100 <= apart * (100 - kSchedMinGainPct);
+}
+
+// ------------------------------------------------ partition into launches
+
+// Most problems a partition takes (e.g. the dgrad and wgrad GEMMs of four
+// linears).
+constexpr int kMaxPartitionProblems = 8;
+
+struct Partition {
+    int nlaunch;
+    int nprob[kMaxPartitionProblems];                   // problems of launch j
+    int idx[kMaxPartitionProblems][kMaxLaunchProblems];  // their caller indices
+    int64_t predicted;                                  // sum of launch times
+};
+
+// Splits n (<= kMaxPartitionProblems) independent GEMMs into launches.
+// Problems of equal tile cost form a class (split into chunks of at most
+// kMaxLaunchProblems); a launch takes one class chunk or two of different
+// costs.  Every pairing of the chunks is tried and the one with the least
+// predicted time kept, provided it beats one launch per problem by at least
+// kSchedMinGainPct percent; otherwise every problem gets its own launch.
+static inline Partition sched_partition(const SchedProblem *p, int n, int tile_m, int bn,
+                                        int64_t max_units)
+{
+    Partition alone;
+    alone.nlaunch = n;
+    alone.predicted = 0;
+    for (int i = 0; i < n; ++i) {
+        alone.nprob[i] = 1;
+        alone.idx[i][0] = i;
+        alone.predicted += sched_launch_time(sched_plan_idx(p, &i, 1, tile_m, bn, max_units));
+    }
+    if (n <= 1 || n > kMaxPartitionProblems)
+        return alone;
+    // chunks: problems of one cost, at most kMaxLaunchProblems each
+    int nch = 0, ch_n[kMaxPartitionProblems], ch_idx[kMaxPartitionProblems][kMaxLaunchProblems],
+        ch_cost[kMaxPartitionProblems];
+    bool used[kMaxPartitionProblems] = {};
+    for (int i = 0; i < n; ++i) {
+        if (used[i])
+            continue;
+        const int c = sched_cost(p[i]);
+        ch_n[nch] = 0;
+        ch_cost[nch] = c;
+        for (int j = i; j < n; ++j) {
+            if (!used[j] && sched_cost(p[j]) == c) {
+                if (ch_n[nch] == kMaxLaunchProblems) {
+                    ++nch;
+                    ch_n[nch] = 0;
+                    ch_cost[nch] = c;
+                }
+                ch_idx[nch][ch_n[nch]++] = j;
+                used[j] = true;
+            }
+        }
+        ++nch;
+    }
+    // every matching of the chunks (a chunk alone, or with one of another
+    // cost whose problems fit in the launch), by depth-first search
+    Partition best = alone;
+    Partition cur;
+    cur.nlaunch = 0;
+    cur.predicted = 0;
+    bool taken[kMaxPartitionProblems] = {};
+    struct Search {
+        static void go(const SchedProblem *p, int tile_m, int bn, int64_t max_units, int nch,
+                       const int *ch_n, const int (*ch_idx)[kMaxLaunchProblems], const int *ch_cost,
+                       bool *taken, Partition &cur, Partition &best)
+        {
+            int first = -1;
+            for (int c = 0; c < nch && first < 0; ++c)
+                if (!taken[c])
+                    first = c;
+            if (first < 0) {
+                if (cur.predicted < best.predicted)
+                    best = cur;
+                return;
+            }
+            taken[first] = true;
+            for (int other = -1; other < nch; ++other) {
+                if (other >= 0 && (taken[other] || ch_cost[other] == ch_cost[first] ||
+                                   ch_n[first] + ch_n[other] > kMaxLaunchProblems))
+                    continue;
+                int idx[kMaxLaunchProblems], k = 0;
+                for (int i = 0; i < ch_n[first]; ++i)
+                    idx[k++] = ch_idx[first][i];
+                if (other >= 0)
+                    for (int i = 0; i < ch_n[other]; ++i)
+                        idx[k++] = ch_idx[other][i];
+                const LaunchPlan pl = sched_plan_idx(p, idx, k, tile_m, bn, max_units);
+                const int64_t t = sched_launch_time(pl);
+                if (other >= 0)
+                    taken[other] = true;
+                const int j = cur.nlaunch++;
+                cur.nprob[j] = k;
+                for (int i = 0; i < k; ++i)
+                    cur.idx[j][i] = idx[i];
+                cur.predicted += t;
+                go(p, tile_m, bn, max_units, nch, ch_n, ch_idx, ch_cost, taken, cur, best);
+                cur.predicted -= t;
+                --cur.nlaunch;
+                if (other >= 0)
+                    taken[other] = false;
+            }
+            taken[first] = false;
+        }
+    };
+    Search::go(p, tile_m, bn, max_units, nch, ch_n, ch_idx, ch_cost, taken, cur, best);
+    if (best.predicted * 100 <= alone.predicted * (100 - kSchedMinGainPct))
+        return best;
+    return alone;
 }
 
 }  // namespace f8

@@ -73,6 +73,14 @@ typedef enum {
 typedef enum { F8_E4M3 = 0, F8_E5M2 = 1 } f8_format;
 
 /*
+ * Step 1 of dynamic tensorwise scaling: the tensor's absolute maximum.
+ * Source: wassimseifeddine.com/posts/torchtitan, section "Float8 Training"
+ * (torchtitan's Float8 is torchao's Float8 training) and the atlas summary
+ * of the TorchTitan paper, Approach (Float8 is one of the composable
+ * training transformations).  The pages name neither the scaling recipe nor
+ * an interface; amax over the whole tensor is the plainest reading of
+ * "dynamic tensorwise" scaling, and this call is this library's own.
+ *
  * amax_out[0] = max_i |x[i]| over n bf16 values, as fp32 (exact).
  *   x:        device, n bf16 values, 16-byte aligned.  n == 0 gives 0.
  *   amax_out: device, one fp32; overwritten (the call zeroes it first).
@@ -82,6 +90,15 @@ typedef enum { F8_E4M3 = 0, F8_E5M2 = 1 } f8_format;
 f8_status f8_amax(const void *x, int64_t n, float *amax_out, void *stream);
 
 /*
+ * Steps 2 and 3 of dynamic tensorwise scaling: the scale and the cast.
+ * Source: stanleyjacob.dev/oss/torchtitan, Part XI (reading list), item 9:
+ * torchtitan's Float8 uses the E4M3 encoding of "FP8 Formats for Deep
+ * Learning" (largest finite value 448, no infinities); the scale that maps
+ * amax onto 448 and the saturating round-to-nearest-even conversion follow
+ * from that format.  The pages print no interface; emitting both layouts
+ * in one pass is this library's design (the backward GEMMs take the
+ * transposed copy as a K-major operand).
+ *
  * Scale and cast one bf16 tensor to E4M3, emitting both layouts in one pass.
  *   x:          device bf16 [rows, cols], 16-byte aligned.
  *   amax:       device fp32 scalar (e.g. from f8_amax).
@@ -125,6 +142,48 @@ f8_status f8_quantize_fmt(const void *x, int64_t rows, int64_t cols, f8_format f
                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Dynamic tensorwise quantisation of several tensors at once, each with its
+ * own amax and scale: every tensor gets exactly what f8_quantize_fmt gives
+ * it (bit-identical), in two launches for all of them when every side is a
+ * multiple of 128 (one amax launch whose CTAs are split between the tensors
+ * in proportion to their sizes, then one TMA cast launch over all their
+ * 128 x 128 tiles), otherwise one f8_quantize_fmt per tensor, in order.
+ * Two launches instead of two per tensor matter for the small tensors of a
+ * step (the 8-33 MB weights of the Llama-3.1-8B attention projections),
+ * whose launches are dominated by ramp-up rather than bytes: e.g. all the
+ * weights of a model once per optimiser step, or the dY of linears that
+ * share an input.
+ *   tensors: host array of `count` (1 .. F8_MAX_MULTI_TENSORS) entries;
+ *            x, amax_out required, scale_out, q, q_t may be NULL; pointers
+ *            aligned as for f8_quantize.
+ *   fmt:     the format of every tensor of the call (F8_E4M3 or F8_E5M2).
+ *   workspace: f8_quantize_multi_workspace_bytes() bytes, 16-byte aligned,
+ *            contents need not be initialised.
+ * The scaling recipe is the one above (atlas summary Approach: Float8 as a
+ * per-linear transformation; one scale per tensor).  The pages print no
+ * interface for it.
+ */
+#define F8_MAX_MULTI_TENSORS 8
+typedef struct {
+    const void *x;          /* device bf16 [rows, cols] */
+    int64_t rows, cols;
+    float *amax_out;        /* device fp32 scalar receiving max |x| */
+    float *scale_out;       /* device fp32 scalar receiving the scale, or NULL */
+    uint8_t *q;             /* device codes [rows, cols] or NULL */
+    uint8_t *q_t;           /* device codes [cols, rows] or NULL */
+} f8_quant_tensor;
+size_t f8_quantize_multi_workspace_bytes(void);
+f8_status f8_quantize_multi(const f8_quant_tensor *tensors, int count, f8_format fmt,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Step 4 of the Float8 linear: the FP8 GEMM with the inverse-scale epilogue.
+ * Source: the discuss.pytorch.org torchtitan index, topic "[Distributed w/
+ * Torchtitan] Enabling Float8 All-Gather in FSDP2" (float8 speeds up large
+ * GEMMs), and the atlas summary's ablation table (Float8 on Llama 3.1 8B).
+ * Dividing the fp32 accumulator by the two scales undoes the scaling of
+ * the casts; the pages print no interface and no kernel.
+ *
  * C = bf16( A B^T / (scale_a * scale_b) ), fp32 accumulation on tcgen05.
  *   a:       device E4M3 [M, K] row-major (K contiguous), 16-byte aligned.
  *   b:       device E4M3 [N, K] row-major (K contiguous), 16-byte aligned.
@@ -157,20 +216,31 @@ typedef struct {
 } f8_gemm_problem;
 
 /*
- * `count` (1 or 2) independent GEMMs in one persistent launch.  Their
- * tiles share the CTA pairs under a static list schedule: the problem with
- * more K per tile is dealt round-robin, then the other problem's tiles go
- * in order to whichever pair frees up first.  One problem's last, partial
- * wave is thus filled with the other's tiles.  Each c is bit-identical to
- * f8_gemm_fmt on its problem (same tiles, same K order).  f8_linear_bwd
- * runs its dgrad and wgrad GEMMs this way: they are the two products of
- * the Float8 linear's backward pass, both reading q(dY).
+ * `count` (1 .. F8_MAX_GROUPED_GEMMS) independent GEMMs in as few
+ * persistent launches as pay.  A launch takes up to four problems whose K
+ * extents take at most two values; their tiles share the CTA pairs under a
+ * static list schedule: the problems with more K per tile are dealt
+ * round-robin, then the others' tiles go in order to whichever pair frees
+ * up first, so one problem's last, partial wave is filled with another's
+ * tiles.  A planner splits the problems into launches and shares a launch
+ * only where its predicted time beats one launch per problem by 4%.  Each
+ * c is bit-identical to f8_gemm_fmt on its problem (same tiles, same K
+ * order).  f8_linear_bwd runs its dgrad and wgrad GEMMs this way (the two
+ * products of the Float8 linear's backward pass, both reading q(dY)), and
+ * f8_linear_fwd_group / f8_linear_bwd_group the GEMMs of linears that
+ * share their input.
  *   problems: host array of `count` problems, each checked as by
- *   f8_gemm_fmt (F8_ERR_INVALID for count outside 1..2 or a NULL array).
- *   The c buffers must not overlap one another or any operand.
- * Problems that need different kernels (M < 256 for one, M >= 256 for the
- * other) or have a zero extent run as separate launches, in array order.
+ *   f8_gemm_fmt (F8_ERR_INVALID for count outside 1..F8_MAX_GROUPED_GEMMS
+ *   or a NULL array).  The c buffers must not overlap one another or any
+ *   operand.
+ * Problems that need different kernels (M < 256 for one, M >= 256 for
+ * another) or have a zero extent run as separate launches, in array order.
+ * The pages print no interface; the call exists because several GEMMs of
+ * one step are independent (the linear's own dgrad and wgrad; the q, k and
+ * v projections that share X in the Llama 3.1 block of the atlas summary's
+ * ablation table).
  */
+#define F8_MAX_GROUPED_GEMMS 8
 f8_status f8_gemm_grouped(const f8_gemm_problem *problems, int count, void *stream);
 
 /*
@@ -198,7 +268,14 @@ typedef struct {
 size_t f8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
- * Forward of a Float8 linear: Y [M,N] = X [M,K] W[N,K]^T.
+ * Forward of a Float8 linear.  Source: the atlas summary of the TorchTitan
+ * paper, Approach (Float8 applied to the model's linears as a composable
+ * transformation) and the ablation table's rows "add Float8 on top of
+ * torch.compile" (Llama 3.1 8B, 8 and 128 GPUs); wassimseifeddine.com,
+ * "Float8 Training".  Its steps are those of f8_amax, f8_cast_transpose and
+ * f8_gemm above on X and W; the pages print no interface.
+ *
+ * Y [M,N] = X [M,K] W[N,K]^T.
  *   x, w: device bf16 inputs; y: device bf16 output.
  *   saved: filled with q(X)^T, q(W)^T and the four scalars.
  *   workspace: device scratch of at least f8_linear_workspace_bytes(M,N,K)
@@ -210,6 +287,10 @@ f8_status f8_linear_fwd(const void *x, const void *w, int64_t M, int64_t N, int6
                         void *stream);
 
 /*
+ * Backward of a Float8 linear.  Source: as f8_linear_fwd (the atlas
+ * summary's Approach and ablation table: Float8 training of the linears,
+ * so their gradients too run as FP8 GEMMs); the pages print no interface.
+ *
  * Backward of the same linear: dX [M,K] = dY W, dW [N,K] = dY^T X, using the
  * saved q(X)^T, q(W)^T and scales from f8_linear_fwd (which must have been
  * enqueued earlier on the same stream, or otherwise completed).  dY is
@@ -231,16 +312,18 @@ f8_status f8_linear_bwd(const void *dy, const f8_linear_saved *saved, int64_t M,
  * forbids side allocations, or a service whose device-memory budget is fixed
  * at start-up.  Such a caller cannot supply f8_linear_fwd's workspace.
  *
- * What it does: exactly what f8_linear_fwd does, with the same kernels and
- * arguments, except that the workspace (the row-major E4M3 copies of X and
- * W) is a static device array of F8_NOALLOC_SCRATCH_BYTES compiled into the
- * library.  The caller still passes x, w, y and `saved`.  The call allocates
- * nothing and calls no allocating routine.
+ * What it does: exactly what f8_linear_fwd does (the same code, kernels and
+ * arguments), except that the workspace is a static device array of
+ * F8_NOALLOC_SCRATCH_BYTES compiled into the library.  The caller still
+ * passes x, w, y and `saved`.  The call allocates nothing and calls no
+ * allocating routine.
  *
  * Limits and rules:
- *  - M*K + N*K bytes (each rounded up to 256) must fit in
- *    F8_NOALLOC_SCRATCH_BYTES (64 MiB); larger problems return F8_ERR_SHAPE
- *    before anything is launched.  M, N, K: multiples of 16, > 0.
+ *  - f8_linear_fwd's workspace for (M, N, K) must fit in
+ *    F8_NOALLOC_SCRATCH_BYTES (64 MiB): the E4M3 copies of X and W, M*K +
+ *    N*K bytes each rounded up to 256, plus 32 KiB of partial maxima.
+ *    Larger problems return F8_ERR_SHAPE before anything is launched.
+ *    M, N, K: multiples of 16, > 0.
  *  - Every device that loads the library holds the array until the process
  *    exits.
  *  - All calls share the array.  Calls whose GPU work overlaps (different
@@ -252,6 +335,101 @@ f8_status f8_linear_bwd(const void *dy, const f8_linear_saved *saved, int64_t M,
 #define F8_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 f8_status f8_linear_fwd_noalloc(const void *x, const void *w, int64_t M, int64_t N, int64_t K,
                                 void *y, const f8_linear_saved *saved, void *stream);
+
+/*
+ * Linears that read one input X (in the Llama 3.1 block the q, k and v
+ * projections, and w1 and w3 of the FFN), each a Float8 linear of its own
+ * (atlas summary, Approach: Float8 is a per-linear transformation): X is
+ * quantised once with one scale, every weight W_i with its own scale, and
+ * every output is bit-identical to f8_linear_fwd / f8_linear_bwd_fmt on
+ * that member with the same X.  One member of the group:
+ *   N:     out-features of this linear (multiple of 16, > 0);
+ *   w:     forward: device bf16 W_i [N, K];  y: device bf16 Y_i [M, N];
+ *   dy:    backward: device bf16 dY_i [M, N];
+ *   dx:    backward: device bf16 dX_i [M, K] or NULL (this member's own
+ *          share; the caller sums the members' dX if the model does);
+ *   dw:    backward: device bf16 dW_i [N, K] or NULL;
+ *   saved: as for f8_linear_fwd.  x_t, amax_x and scale_x must be the same
+ *          buffers in every member (the group's one q(X)^T and X scalars,
+ *          written once); w_t, amax_w, scale_w are the member's own.
+ */
+#define F8_MAX_GROUP_LINEARS 4
+typedef struct {
+    int64_t N;
+    const void *w;
+    void *y;
+    const void *dy;
+    void *dx;
+    void *dw;
+    f8_linear_saved saved;
+} f8_group_linear;
+
+/*
+ * Device workspace (bytes) f8_linear_fwd_group and f8_linear_bwd_group need
+ * for M, K and the members' N (count of them); 256-byte aligned regions,
+ * contents need not be initialised.  0 for bad arguments.
+ */
+size_t f8_linear_group_workspace_bytes(int64_t M, int64_t K, const int64_t *N, int count);
+
+/*
+ * Forward of a group of `count` (1 .. F8_MAX_GROUP_LINEARS) linears sharing
+ * X [M, K]: Y_i = X W_i^T.  Launches: X and every W_i quantised together
+ * (f8_quantize_multi: two launches; per tensor where a side is not a
+ * multiple of 128), then the count GEMMs under f8_gemm_grouped's planner:
+ * with one K they form one class, and one launch runs all their tiles
+ * round-robin where that is predicted to pay (the skinny k and v
+ * projections, 128 tiles of 256 x 256 each at M = 8192, no longer run as
+ * launches of 1.7 waves).
+ *   members: host array; uses N, w, y, saved.  M, K multiples of 16, > 0.
+ */
+f8_status f8_linear_fwd_group(const void *x, int64_t M, int64_t K, const f8_group_linear *members,
+                              int count, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward of the same group: every dY_i quantised in format fmt_dy
+ * (f8_quantize_multi), then every member's dgrad dX_i = dY_i W_i and wgrad
+ * dW_i = dY_i^T X (up to 2 x count GEMMs) under f8_gemm_grouped's planner.
+ *   members: host array; uses N, dy, dx, dw, saved (from the forward,
+ *   enqueued earlier on the same stream or completed).
+ */
+f8_status f8_linear_bwd_group(const f8_group_linear *members, int count, int64_t M, int64_t K,
+                              f8_format fmt_dy, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/*
+ * The FP8 weight all-gather of FSDP2 (the discuss.pytorch.org torchtitan
+ * index, topic "[Distributed w/ Torchtitan] Enabling Float8 All-Gather in
+ * FSDP2": float8 saves network bandwidth with reduced message size).  Each
+ * rank holds a row shard of W; the ranks agree on one tensorwise scale
+ * (all-reduce MAX of the shards' amax), cast their shard with it and
+ * all-gather the E4M3 bytes, half the bytes of a bf16 gather.  The
+ * collectives themselves are the caller's (float8_mixed_precision_gb300.fsdp
+ * issues them with torch.distributed); these two calls are the device steps
+ * that the gathered weight then needs.  The pages print no interface.
+ *
+ * f8_transpose_u8: out[c, r] = in[r, c] for a [rows, cols] byte tensor
+ * (device pointers, no alignment rule, rows, cols >= 0; not in place).  It
+ * makes q(W)^T [K, N], the dgrad operand, from the gathered q(W) [N, K].
+ */
+f8_status f8_transpose_u8(const uint8_t *in, int64_t rows, int64_t cols, uint8_t *out,
+                          void *stream);
+
+/*
+ * Forward of a Float8 linear whose weight arrives already quantised (the
+ * gathered q(W) above): X is quantised as in f8_linear_fwd (amax launch,
+ * cast launch), then Y = bf16(q(X) q(W)^T / (s_x s_w)).
+ *   w_q:   device E4M3 [N, K], the row-major q(W).
+ *   saved: x_t, amax_x, scale_x are written; w_t, amax_w, scale_w are read
+ *          only and must already hold q(W)^T [K, N] and W's scalars (the
+ *          scale W was cast with), so f8_linear_bwd applies unchanged.
+ *   workspace: f8_linear_fwd_qw_workspace_bytes(M, K) bytes, 256-aligned.
+ * Outputs are bit-identical to f8_linear_fwd on the bf16 W whose
+ * quantisation q(W) is.
+ */
+size_t f8_linear_fwd_qw_workspace_bytes(int64_t M, int64_t K);
+f8_status f8_linear_fwd_qw(const void *x, const uint8_t *w_q, int64_t M, int64_t N, int64_t K,
+                           void *y, const f8_linear_saved *saved, void *workspace,
+                           size_t workspace_bytes, void *stream);
 
 /*
  * f8_linear_bwd with dY quantised to `fmt_dy` (E5M2: scale 57344/amax(dY);
@@ -267,11 +445,13 @@ f8_status f8_linear_bwd_fmt(const void *dy, f8_format fmt_dy, const f8_linear_sa
  * reads a and b, writes h and one partial maximum of |h| per CTA; launch two
  * is f8_quantize's cast of h.  Against forming h separately and then
  * running f8_quantize, the amax re-read of h (2 B/elem) is gone.
- * silu(a) = a * (1 / (1 + exp(-a))) in fp32, exp by Cody-Waite range
- * reduction and the degree-7 Taylor polynomial, the reciprocal correctly
- * rounded; each step one IEEE fp32 operation, then one RNE to bf16.  The
- * pages name the SwiGLU FFN of torchtitan's Llama 3.1 and credit Float8 on
- * top of torch.compile, which fuses such neighbouring elementwise work.
+ * h is the bf16 of silu(a) b with silu(a) = a / (1 + exp(-a)), evaluated
+ * in fp32 (exp by Cody-Waite range reduction and the degree-7 Taylor
+ * polynomial, the reciprocal correctly rounded): within one bf16 ulp of
+ * the exact value rounded once, and equal to it except where the exact
+ * value lies within a few fp32 ulp of a bf16 rounding boundary.  The pages
+ * name the SwiGLU FFN of torchtitan's Llama 3.1 and credit Float8 on top
+ * of torch.compile, which fuses such neighbouring elementwise work.
  *   a, b:     device bf16 [rows, cols], 16-byte aligned.
  *   h:        device bf16 [rows, cols] receiving h.
  *   amax_out, scale_out, q, q_t, workspace: as for f8_quantize.
@@ -348,10 +528,10 @@ f8_status f8_quantize_swiglu_bwd(const void *dh, const void *ab, int64_t M, int6
  * The backward of f8_linear_fwd_w13_swiglu for the gradient dh of h (in a
  * Llama FFN, the dX of the w2 linear):
  *   d(AB) = the gradient of h = silu(a) * b: db = bf16(dh * silu(a)),
- *           da = bf16(dh * b * silu'(a)) with silu'(a) = sigma fma(a, 1 - sigma,
- *           1), sigma and silu(a) as in the forward, each step one IEEE fp32
- *           operation; written in AB's column order, with its amax taken in
- *           the same pass (one partial per CTA);
+ *           da = bf16(dh * b * silu'(a)) with silu'(a) = sigma (1 + a (1 -
+ *           sigma)), in fp32 as in the forward and to the same bound (one
+ *           bf16 ulp of the exact value); written in AB's column order, with
+ *           its amax taken in the same pass (one partial per CTA);
  *   then the group's backward as f8_linear_bwd with dY = d(AB): cast of
  *           d(AB), dX = q(dAB) q(W13), dW13 = q(dAB)^T q(X).
  *   dh:    device bf16 [M, F].

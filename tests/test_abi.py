@@ -158,8 +158,9 @@ def test_gemm_grouped_rejects_bad_arguments_on_host(L):
     arr = (_GemmProblem * 3)(ok, ok, ok)
     f = L.f8_gemm_grouped
     assert f(None, 1, None) == 1                  # no array
-    assert f(arr, 0, None) == 1                   # count outside 1..2
-    assert f(arr, 3, None) == 1
+    assert f(arr, 0, None) == 1                   # count outside 1..8
+    big = (_GemmProblem * 9)(*([ok] * 9))
+    assert f(big, 9, None) == 1
 
     def with_field(name, value):
         p = _GemmProblem(FAKE, FAKE, 256, 256, 256, FAKE, FAKE + 4, FAKE, 0, 0)
@@ -183,8 +184,9 @@ def test_struct_layouts_match_the_header(tmp_path):
     cc = shutil.which("gcc") or shutil.which("cc")
     if cc is None:
         pytest.skip("no C compiler")
-    from float8_mixed_precision_gb300.binding import _GemmProblem, _Saved
-    structs = {"f8_linear_saved": _Saved, "f8_gemm_problem": _GemmProblem}
+    from float8_mixed_precision_gb300.binding import _GemmProblem, _GroupLinear, _QuantTensor, _Saved
+    structs = {"f8_linear_saved": _Saved, "f8_gemm_problem": _GemmProblem,
+               "f8_quant_tensor": _QuantTensor, "f8_group_linear": _GroupLinear}
     lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "f8.h"', "int main(void) {"]
     for cname, cls in structs.items():
         lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -206,3 +208,77 @@ def test_struct_layouts_match_the_header(tmp_path):
         for field, _ in cls._fields_:
             assert got[(cname, field)] == getattr(cls, field).offset, (cname, field)
     assert got[("f8_format", "size")] == ctypes.sizeof(ctypes.c_int)
+
+
+def test_quantize_multi_rejects_bad_arguments_on_host(L):
+    from float8_mixed_precision_gb300.binding import _QuantTensor
+    ok = _QuantTensor(FAKE, 256, 256, FAKE, FAKE + 4, FAKE, FAKE)
+    arr = (_QuantTensor * 9)(*([ok] * 9))
+    f = L.f8_quantize_multi
+    ws = L.f8_quantize_multi_workspace_bytes()
+    assert ws > 0
+    assert f(None, 1, 0, FAKE, ws, None) == 1          # no array
+    assert f(arr, 0, 0, FAKE, ws, None) == 1           # count outside 1..8
+    assert f(arr, 9, 0, FAKE, ws, None) == 1
+    assert f(arr, 2, 2, FAKE, ws, None) == 1           # no such format
+    assert f(arr, 2, 0, None, ws, None) == 1           # no workspace
+    assert f(arr, 2, 0, FAKE, ws - 1, None) == 1       # workspace too small
+    assert f(arr, 2, 0, FAKE_MIS, ws, None) == 2       # misaligned workspace
+
+    def with_field(name, value):
+        p = _QuantTensor(FAKE, 256, 256, FAKE, FAKE + 4, FAKE, FAKE)
+        setattr(p, name, value)
+        return (_QuantTensor * 2)(ok, p)
+
+    assert f(with_field("rows", -1), 2, 0, FAKE, ws, None) == 1
+    assert f(with_field("amax_out", None), 2, 0, FAKE, ws, None) == 1
+    assert f(with_field("x", None), 2, 0, FAKE, ws, None) == 1
+    assert f(with_field("q", FAKE_MIS), 2, 0, FAKE, ws, None) == 2
+
+
+def test_linear_group_rejects_bad_arguments_on_host(L):
+    from float8_mixed_precision_gb300.binding import _GroupLinear, _Saved
+    s0 = _Saved(FAKE, FAKE + 4096, FAKE, FAKE + 4, FAKE + 8, FAKE + 12)
+    s1 = _Saved(FAKE, FAKE + 8192, FAKE, FAKE + 4, FAKE + 16, FAKE + 20)
+    m0 = _GroupLinear(256, FAKE, FAKE, FAKE, FAKE, FAKE, s0)
+    m1 = _GroupLinear(512, FAKE, FAKE, FAKE, FAKE, FAKE, s1)
+    arr = (_GroupLinear * 5)(m0, m1, m0, m1, m0)
+    Ns = (ctypes.c_int64 * 2)(256, 512)
+    wsb = L.f8_linear_group_workspace_bytes(512, 256, Ns, 2)
+    assert wsb > 0
+    assert L.f8_linear_group_workspace_bytes(512, 256, Ns, 0) == 0
+    assert L.f8_linear_group_workspace_bytes(0, 256, Ns, 2) == 0
+    fwd, bwd = L.f8_linear_fwd_group, L.f8_linear_bwd_group
+    assert fwd(FAKE, 512, 256, None, 2, FAKE, wsb, None) == 1     # no array
+    assert fwd(FAKE, 512, 256, arr, 5, FAKE, wsb, None) == 1      # count outside 1..4
+    assert fwd(FAKE, 512, 256, arr, 2, FAKE, 4096, None) == 1     # workspace too small
+    assert bwd(arr, 2, 512, 256, 0, FAKE, wsb - 1, None) == 1     # (the backward needs wsb)
+    assert fwd(FAKE, 500, 256, arr, 2, FAKE, wsb, None) == 3      # M % 16
+    assert fwd(None, 512, 256, arr, 2, FAKE, wsb, None) == 1
+    assert fwd(FAKE_MIS, 512, 256, arr, 2, FAKE, wsb, None) == 2
+    assert bwd(arr, 2, 512, 256, 2, FAKE, wsb, None) == 1         # no such format
+    assert bwd(arr, 2, 512, 256, 0, FAKE_MIS, wsb, None) == 2     # workspace alignment
+    # the members must share q(X)^T and the X scalars
+    s_other = _Saved(FAKE + 65536, FAKE + 8192, FAKE, FAKE + 4, FAKE + 16, FAKE + 20)
+    bad = (_GroupLinear * 2)(m0, _GroupLinear(512, FAKE, FAKE, FAKE, FAKE, FAKE, s_other))
+    assert fwd(FAKE, 512, 256, bad, 2, FAKE, wsb, None) == 1
+    assert bwd(bad, 2, 512, 256, 0, FAKE, wsb, None) == 1
+    nody = (_GroupLinear * 2)(m0, _GroupLinear(512, FAKE, FAKE, None, FAKE, FAKE, s1))
+    assert bwd(nody, 2, 512, 256, 0, FAKE, wsb, None) == 1
+
+
+def test_transpose_and_fwd_qw_reject_bad_arguments_on_host(L):
+    from float8_mixed_precision_gb300.binding import _Saved
+    t = L.f8_transpose_u8
+    assert t(FAKE, -1, 4, FAKE, None) == 1
+    assert t(None, 4, 4, FAKE, None) == 1
+    assert t(FAKE, 0, 4, None, None) == 0          # nothing to do
+    s = _Saved(FAKE, FAKE, FAKE, FAKE + 4, FAKE + 8, FAKE + 12)
+    f = L.f8_linear_fwd_qw
+    wsb = L.f8_linear_fwd_qw_workspace_bytes(256, 512)
+    assert wsb >= 256 * 512 and L.f8_linear_fwd_qw_workspace_bytes(0, 512) == 0
+    assert f(FAKE, FAKE, 256, 128, 500, FAKE, ctypes.byref(s), FAKE, wsb, None) == 3   # K % 16
+    assert f(FAKE, None, 256, 128, 512, FAKE, ctypes.byref(s), FAKE, wsb, None) == 1
+    assert f(FAKE, FAKE, 256, 128, 512, FAKE, ctypes.byref(s), FAKE, wsb - 1, None) == 1
+    assert f(FAKE, FAKE_MIS, 256, 128, 512, FAKE, ctypes.byref(s), FAKE, wsb, None) == 2
+    assert f(FAKE, FAKE, 256, 128, 512, FAKE, None, FAKE, wsb, None) == 1

@@ -49,3 +49,31 @@ def test_cpu_baseline_reports_phases():
     assert "256 of 256 output rows" in c["sample"]
     empty = bench.cpu_baseline(1, 0)        # no GEMM rows: nothing to extrapolate from
     assert empty["extrapolated_step_seconds"] is None and empty["value"] == 0.0
+
+
+def test_reference_arm_config_matches_ours():
+    """Both arms print the same `config` (workload name, every linear with its
+    M, K, N, flops per step) for the same arguments, so the two lines can be
+    compared as one workload."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from float8_mixed_precision_gb300 import workloads as wl
+    r = _bench("--impl", "reference", "--config", "1", "--steps", "2", "--warmup", "3")
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][0])
+    args = bench.main.__globals__["argparse"].Namespace(
+        config=1, swiglu_input="given", fuse_shared_inputs=False, graph=1, groups=1)
+    assert d["config"] == bench.config_dict(wl, args, 1)
+    assert d["config"]["linears"] == ["tiny M=256 K=256 N=512"]
+    assert d["config"]["flops_per_step"] == 6 * 256 * 256 * 512
+
+
+def test_fp8_peak_follows_the_region_length():
+    """A rate measured over less than a second is held to the burst peak,
+    a longer one to the sustained (power-capped) peak; both x 2 for FP8."""
+    sys.path.insert(0, ROOT)
+    import bench
+    peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    assert bench.fp8_peak_for(0.05, peaks) == (3800.0, "burst")
+    assert bench.fp8_peak_for(0.999, peaks) == (3800.0, "burst")
+    assert bench.fp8_peak_for(2.0, peaks) == (3400.0, "sustained")

@@ -72,9 +72,20 @@ def test_every_wrapper_marshals(rec):
     binding.f8_quantize_swiglu_bwd(_bf(M, F), _bf(M, 2 * F))
     binding.f8_selftest_wait_timeout(1000)
     binding.f8_selftest_bounds()
+    binding.f8_quantize_multi([x, w, dy])
+    binding.f8_quantize_multi([x], fmt=binding.F8_E5M2, want_q=False)
+    binding.f8_gemm_grouped([(q, qb, torch.ones(1), torch.ones(1))] * 5)
+    ys, gsaved = binding.f8_linear_fwd_group(x, [w, _bf(2 * N, K)])
+    binding.f8_linear_bwd_group([dy, _bf(M, 2 * N)], gsaved, K)
+    binding.f8_linear_bwd_group([dy, _bf(M, 2 * N)], gsaved, K, want_dx=False)
+    assert gsaved[0].x_t is gsaved[1].x_t and gsaved[0].x_scalars is gsaved[1].x_scalars
+    binding.f8_transpose_u8(torch.zeros((N, K), dtype=torch.uint8))
+    binding.f8_linear_fwd_qw(x, torch.zeros((N, K), dtype=torch.uint8), saved)
     wrapped = {n for n in binding.EXPORTS if hasattr(binding, n)}
     called = set(rec.calls)
     assert wrapped - {"f8_status_string", "f8_last_device_status", "f8_set_wait_limit_ns",
                       "f8_kernel_launches",
-                      "f8_linear_workspace_bytes", "f8_quantize_workspace_bytes"} <= called, \
+                      "f8_linear_workspace_bytes", "f8_quantize_workspace_bytes",
+                      "f8_quantize_multi_workspace_bytes",
+                      "f8_linear_fwd_qw_workspace_bytes"} <= called, \
         sorted(wrapped - called)
