@@ -53,19 +53,40 @@ FP8_PER_BF16 = 2.0          # nominal dense FP8 : BF16 tensor throughput
 HBM_NOMINAL_GBS = 8000.0
 REF_BUDGET_S = 60.0   # timed seconds of the CPU reference arm
 
-# DRAM bytes (read + write) of the 12 GEMM launches of one attention fwd+bwd
-# step, from one ncu capture (profiles/gemm_traffic_attn8b.md), valid for the
-# GEMM sources whose hash is given; reported as null once they change.
-GEMM_TRAFFIC = {"workload": 2, "bytes_per_step": 761316864, "sources_sha256_16": "a205204bb5365e82"}
+# DRAM bytes (read + write) of all GEMM launches of one step of the default
+# workload (the Llama-3.1-8B block with its shared-input groups), from one
+# ncu capture of dram__bytes_read.sum + dram__bytes_write.sum; valid for the
+# GEMM sources whose hash is given, reported as null once they change.
+GEMM_TRAFFIC = {"workload": 5, "groups": 1, "bytes_per_step": None, "sources_sha256_16": None}
+# The same for the quantisation launches (amax and cast) of one step.
+QUANT_TRAFFIC = {"workload": 5, "groups": 1, "bytes_per_step": None, "sources_sha256_16": None}
 
 
-def gemm_sources_hash() -> str:
+def sources_hash(files) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("f8_gemm.cu", "f8_ptx.cuh", "f8_sched.h"):
+    for f in files:
         with open(os.path.join(ROOT, "float8_mixed_precision_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def gemm_sources_hash() -> str:
+    return sources_hash(("f8_gemm.cu", "f8_ptx.cuh", "f8_sched.h"))
+
+
+def quant_sources_hash() -> str:
+    return sources_hash(("f8_cast.cu", "f8_ptx.cuh"))
+
+
+def captured_traffic(rec: dict, args, current_hash: str):
+    """The captured DRAM bytes per step, if they were taken on this workload
+    and on the sources as they are now; else None."""
+    if (rec["bytes_per_step"] is None or args.config != rec["workload"]
+            or int(args.groups) != rec["groups"] or args.fuse_shared_inputs
+            or args.swiglu_input != "given" or current_hash != rec["sources_sha256_16"]):
+        return None
+    return rec["bytes_per_step"]
 
 
 # ------------------------------------------------------------------ helpers
@@ -714,6 +735,14 @@ def run_ours(args, world, rank, local):
                       "frac_of_fp8_nominal": rate / 1e12 / FP8_NOMINAL_TFLOPS})
         else:
             e.update({"gbs": rate / 1e9, "frac_of_hbm_measured": rate / 1e9 / peaks["hbm_gbs"]})
+            if kind == "quantize":
+                # DRAM bytes the quantisation launches move (ncu), against the
+                # algorithmic 4 B per element (2 read + 2 written)
+                qt = captured_traffic(QUANT_TRAFFIC, args, quant_sources_hash())
+                e.update({"algorithmic_bytes_per_step": d["work"] / nsteps_k,
+                          "dram_bytes_per_step": qt,
+                          "dram_over_algorithmic": (qt / (d["work"] / nsteps_k)) if qt else None,
+                          "dram_gbs": (qt / (d["ms"] / nsteps_k * 1e-3) / 1e9) if qt else None})
         kernels[kind] = e
     g = per["gemm"]
     achieved = g["work"] / (g["ms"] * 1e-3) / 1e12
@@ -729,9 +758,7 @@ def run_ours(args, world, rank, local):
                 "frac_of_burst": achieved / (peaks["bf16_tflops"] * FP8_PER_BF16),
                 "frac_of_sustained": achieved / (peaks["bf16_tflops_sustained"] * FP8_PER_BF16),
                 "frac_of_nominal_4500": achieved / FP8_NOMINAL_TFLOPS,
-                "traffic": (GEMM_TRAFFIC["bytes_per_step"]
-                            if args.config == GEMM_TRAFFIC["workload"]
-                            and gemm_sources_hash() == GEMM_TRAFFIC["sources_sha256_16"] else None),
+                "traffic": captured_traffic(GEMM_TRAFFIC, args, gemm_sources_hash()),
                 "traffic_unit": "bytes per step (all GEMM launches of the step, like achieved)",
                 # E4M3 operands read once + bf16 outputs written once, 3 GEMMs per linear
                 "algorithmic_bytes_per_step": sum(4 * (l.M * l.K + l.N * l.K + l.M * l.N)
