@@ -57,7 +57,8 @@ REF_BUDGET_S = 60.0   # timed seconds of the CPU reference arm
 # workload (the Llama-3.1-8B block with its shared-input groups), from one
 # ncu capture of dram__bytes_read.sum + dram__bytes_write.sum; valid for the
 # GEMM sources whose hash is given, reported as null once they change.
-GEMM_TRAFFIC = {"workload": 5, "groups": 1, "bytes_per_step": None, "sources_sha256_16": None}
+GEMM_TRAFFIC = {"workload": 5, "groups": 1, "bytes_per_step": 4815535872,
+                "sources_sha256_16": "b6d759a6a8fb6715"}
 # The same for the quantisation launches (amax and cast) of one step.
 QUANT_TRAFFIC = {"workload": 5, "groups": 1, "bytes_per_step": None, "sources_sha256_16": None}
 

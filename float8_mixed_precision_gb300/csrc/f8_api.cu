@@ -105,6 +105,46 @@ BwdWs bwd_ws(void *workspace, int64_t M, int64_t N)
     return w;
 }
 
+// Quantisation of n tensors in launch pairs: consecutive tensors go into
+// one multi-tensor pair while their bf16 total stays within `budget` bytes
+// (the amax pass's reads then still sit in L2 when the cast re-reads
+// them); a tensor beyond it, or one the TMA cast cannot take, gets a pair
+// of its own.  `parts` holds kMaxAmaxPartials partial maxima; the batches
+// reuse it one after the other (each amax launch waits for the cast before
+// it).
+cudaError_t quantize_batches(const QuantDesc *d, int n, int fmt, unsigned *parts, int64_t budget,
+                             const DeviceInfo &dev, cudaStream_t st)
+{
+    int i = 0;
+    while (i < n) {
+        int j = i;
+        int64_t bytes = 0;
+        while (j < n && quantize_multi_castable(&d[j], 1) &&
+               (j == i || bytes + 2 * d[j].rows * d[j].cols <= budget) && j - i < kMaxQuantTensors) {
+            bytes += 2 * d[j].rows * d[j].cols;
+            ++j;
+            if (bytes > budget)
+                break;
+        }
+        cudaError_t e;
+        if (j - i >= 2) {
+            e = launch_quantize_multi(&d[i], j - i, fmt, parts, dev, st);
+        } else {
+            j = i + 1;
+            int np = 0;
+            e = launch_amax_partials(d[i].x, d[i].rows * d[i].cols, parts, &np, dev, st);
+            if (e == cudaSuccess)
+                e = launch_cast_transpose(d[i].x, d[i].rows, d[i].cols, nullptr, parts, np,
+                                          d[i].amax_out, d[i].scale_out, d[i].q, d[i].q_t, fmt, dev,
+                                          st, true);
+        }
+        if (e != cudaSuccess)
+            return e;
+        i = j;
+    }
+    return cudaSuccess;
+}
+
 // The backward GEMMs of a linear from q(dY) (format fdy) and the saved
 // q(X)^T, q(W)^T; both in one launch when both are wanted:
 //   dX [M,K] = q(dY) [M,N] . (q(W)^T [K,N])^T
@@ -256,23 +296,13 @@ f8_status f8::linear_fwd_impl(const void *x, const void *w, int64_t M, int64_t N
     F8_TRY(get_device(&dev));
     const FwdWs fw = fwd_ws(workspace, M, N, K);
     // X and W together when they fit in L2 with room to spare (the cast
-    // re-reads what the amax launch just read): two launches instead of four
-    bool pair = quant_pair_enabled() && 2 * (M * K + N * K) <= kPairMaxBytes;
+    // re-reads what the amax launch just read): two launches instead of
+    // four; otherwise each cast follows its own amax
     const QuantDesc xw[2] = {{x, M, K, saved->amax_x, saved->scale_x, fw.x_q, saved->x_t},
                              {w, N, K, saved->amax_w, saved->scale_w, fw.w_q, saved->w_t}};
-    pair = pair && quantize_multi_castable(xw, 2);
-    if (pair) {
-        F8_TRY_CUDA(launch_quantize_multi(xw, 2, F8_E4M3, fw.parts_x, *dev, st));
-    } else {
-        int np = 0;
-        // each cast follows its own amax so that its re-read of the tensor hits L2
-        F8_TRY_CUDA(launch_amax_partials(x, M * K, fw.parts_x, &np, *dev, st));
-        F8_TRY_CUDA(launch_cast_transpose(x, M, K, nullptr, fw.parts_x, np, saved->amax_x,
-                                          saved->scale_x, fw.x_q, saved->x_t, 0, *dev, st, true));
-        F8_TRY_CUDA(launch_amax_partials(w, N * K, fw.parts_w, &np, *dev, st));
-        F8_TRY_CUDA(launch_cast_transpose(w, N, K, nullptr, fw.parts_w, np, saved->amax_w,
-                                          saved->scale_w, fw.w_q, saved->w_t, 0, *dev, st, true));
-    }
+    F8_TRY_CUDA(quantize_batches(xw, 2, F8_E4M3, fw.parts_x,
+                                 quant_pair_enabled() ? quant_batch_bytes(kPairMaxBytes) : 0, *dev,
+                                 st));
     return from_cuda(launch_gemm(fw.x_q, fw.w_q, M, N, K, saved->scale_x, saved->scale_w, y, *dev, st));
 }
 
@@ -457,13 +487,8 @@ f8_status f8_quantize_multi(const f8_quant_tensor *tensors, int count, f8_format
         const f8_quant_tensor &t = tensors[i];
         d[i] = QuantDesc{t.x, t.rows, t.cols, t.amax_out, t.scale_out, t.q, t.q_t};
     }
-    if (quantize_multi_castable(d, count))
-        return from_cuda(launch_quantize_multi(d, count, fmt, static_cast<unsigned *>(workspace),
-                                               *dev, st));
-    for (int i = 0; i < count; ++i)
-        F8_TRY(quantize_impl(d[i].x, d[i].rows, d[i].cols, fmt, d[i].amax_out, d[i].scale_out,
-                             d[i].q, d[i].q_t, workspace, workspace_bytes, stream));
-    return F8_OK;
+    return from_cuda(quantize_batches(d, count, fmt, static_cast<unsigned *>(workspace),
+                                      quant_batch_bytes(kPairMaxBytes), *dev, st));
 }
 
 size_t f8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K)
@@ -605,17 +630,8 @@ f8_status f8_linear_fwd_group(const void *x, int64_t M, int64_t K, const f8_grou
         const f8_linear_saved &si = members[i].saved;
         d[1 + i] = QuantDesc{members[i].w, N[i], K, si.amax_w, si.scale_w, w_q[i], si.w_t};
     }
-    if (quantize_multi_castable(d, 1 + count)) {
-        F8_TRY_CUDA(launch_quantize_multi(d, 1 + count, F8_E4M3, parts, *dev, st));
-    } else {
-        for (int i = 0; i <= count; ++i) {
-            int np = 0;
-            F8_TRY_CUDA(launch_amax_partials(d[i].x, d[i].rows * d[i].cols, parts, &np, *dev, st));
-            F8_TRY_CUDA(launch_cast_transpose(d[i].x, d[i].rows, d[i].cols, nullptr, parts, np,
-                                              d[i].amax_out, d[i].scale_out, d[i].q, d[i].q_t, 0,
-                                              *dev, st, true));
-        }
-    }
+    F8_TRY_CUDA(quantize_batches(d, 1 + count, F8_E4M3, parts, quant_batch_bytes(kPairMaxBytes),
+                                 *dev, st));
     GemmDesc g[F8_MAX_GROUP_LINEARS];
     for (int i = 0; i < count; ++i)
         g[i] = GemmDesc{x_q, w_q[i], M, N[i], K, s0.scale_x, members[i].saved.scale_w,
@@ -661,17 +677,8 @@ f8_status f8_linear_bwd_group(const f8_group_linear *members, int count, int64_t
     for (int i = 0; i < count; ++i)
         d[i] = QuantDesc{members[i].dy, M, N[i], amax[i], scale[i],
                          members[i].dx ? dy_q[i] : nullptr, members[i].dw ? dy_t[i] : nullptr};
-    if (quantize_multi_castable(d, count)) {
-        F8_TRY_CUDA(launch_quantize_multi(d, count, fmt_dy, parts, *dev, st));
-    } else {
-        for (int i = 0; i < count; ++i) {
-            int np = 0;
-            F8_TRY_CUDA(launch_amax_partials(d[i].x, M * N[i], parts, &np, *dev, st));
-            F8_TRY_CUDA(launch_cast_transpose(d[i].x, M, N[i], nullptr, parts, np, d[i].amax_out,
-                                              d[i].scale_out, d[i].q, d[i].q_t, fmt_dy, *dev, st,
-                                              true));
-        }
-    }
+    F8_TRY_CUDA(quantize_batches(d, count, fmt_dy, parts, quant_batch_bytes(kPairMaxBytes), *dev,
+                                 st));
     // dX_i [M,K] = q(dY_i) [M,N_i] . (q(W_i)^T [K,N_i])^T;  dW_i [N_i,K] = q(dY_i)^T . (q(X)^T [K,M])^T
     GemmDesc g[2 * F8_MAX_GROUP_LINEARS];
     int n = 0;

@@ -507,6 +507,7 @@ struct CastSet {
     int nseg;
     int early;   // 1: the inputs are complete before the dependency wait (the
                  // previous launch only read them: their amax pass)
+    int reverse; // 1: tiles last first
 };
 
 // Tiles are taken in reverse launch order (the last tile first): the amax
@@ -530,7 +531,8 @@ cast_transpose_tma_kernel(const __grid_constant__ CastSet<NS> set, unsigned *__r
     const int64_t nmine = ntiles > blockIdx.x ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     // the k-th tile of this CTA -> (tensor, tile row start, tile column start)
     auto locate = [&](int64_t k, int &sg, int64_t &r0, int64_t &c0) {
-        const int64_t tix = ntiles - 1 - (blockIdx.x + k * gridDim.x);
+        const int64_t fwd = blockIdx.x + k * gridDim.x;
+        const int64_t tix = set.reverse ? ntiles - 1 - fwd : fwd;
         sg = 0;
 #pragma unroll
         for (int i = 1; i < NS; ++i)
@@ -761,6 +763,7 @@ cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, con
         set.first_tile[1] = ntiles;
         set.nseg = 1;
         set.early = early ? 1 : 0;
+        set.reverse = cast_reverse_enabled() ? 1 : 0;
         return launch_pdl(fmt == 1 ? cast_transpose_tma_kernel<1, 1> : cast_transpose_tma_kernel<0, 1>,
                           dim3(static_cast<unsigned>(blocks)), dim3(kCastThreads), kTmaCastSmem,
                           stream, set, dev.status, wait_limit_ns());
@@ -871,6 +874,7 @@ cudaError_t launch_quantize_multi(const QuantDesc *t, int n, int fmt, unsigned *
     segs.nseg = n;
     set.nseg = n;
     set.early = 1;  // the amax launch just before only reads the inputs
+    set.reverse = cast_reverse_enabled() ? 1 : 0;
     cudaError_t e = launch_pdl(amax_multi_kernel, dim3(static_cast<unsigned>(segs.first_block[n])),
                                dim3(kAmaxThreads), 0, stream, segs, dev.status);
     if (e != cudaSuccess)

@@ -42,6 +42,24 @@ inline bool cast_tma_enabled()
     return e == nullptr || e[0] != '0';
 }
 
+// The TMA cast takes its tiles last first (so that its re-read starts
+// with what the amax pass left in L2) unless F8_CAST_REVERSE=0.
+inline bool cast_reverse_enabled()
+{
+    const char *e = std::getenv("F8_CAST_REVERSE");
+    return e == nullptr || e[0] != '0';
+}
+
+// Largest bf16 total (bytes) one multi-tensor quantisation launch pair
+// takes; larger lists are split into consecutive batches within it, and a
+// tensor larger than it is quantised alone.  F8_QUANT_BATCH_MB overrides
+// the default (for measurement).
+inline int64_t quant_batch_bytes(int64_t dflt)
+{
+    const char *e = std::getenv("F8_QUANT_BATCH_MB");
+    return e == nullptr ? dflt : static_cast<int64_t>(std::atoll(e)) << 20;
+}
+
 // X and W of a small linear are quantised together (one amax launch, one
 // cast launch) unless F8_QUANT_PAIR=0.
 inline bool quant_pair_enabled()
