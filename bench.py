@@ -326,6 +326,14 @@ class Linear8:
         """(linear, X, W, dY) of each linear, for the isolated kernel timings."""
         return [(self.lin, self.x, self.w, self.dy)]
 
+    def twin(self, f8, device):
+        """A second layer of the same shapes with buffers of its own (the
+        e2e leg alternates two, so host copies of one step overlap the
+        compute of the other)."""
+        ab = (self.a.clone(), self.b.clone()) if self.swiglu is not None else None
+        return Linear8(f8, self.lin, {"x": self.x.clone(), "w": self.w.clone(),
+                                      "dy": self.dy.clone()}, device, self.dy_fmt, self.swiglu, ab)
+
     def step(self, f8):
         if self.swiglu == "fused":
             f8.f8_linear_fwd_swiglu(self.a, self.b, self.w, self.y, self.saved, self.ws, h=self.h)
@@ -414,6 +422,10 @@ class GroupLinear8:
 
     def iso_items(self):
         return [(l, self.x, w, dy) for l, w, dy in zip(self.members, self.w, self.dy)]
+
+    def twin(self, f8, device):
+        return GroupLinear8(f8, self.members, self.x.clone(), [w.clone() for w in self.w],
+                            [d.clone() for d in self.dy], device, self.dy_fmt)
 
     def step(self, f8):
         f8.f8_linear_fwd_group(self.x, self.w, ys=self.y, saved=self.saved, ws=self.ws)
@@ -868,10 +880,15 @@ def kernel_bench(f8, layers, device, stream, iters=50):
 
 def run_e2e(f8, layers, args, device, stream, flops_step, world):
     """The whole step from pinned host buffers and back, through the public
-    API.  Three streams form a pipeline: the host-to-device copies of linear
-    i+1 and the device-to-host copies of linear i-1 run while linear i
-    computes; events keep each buffer's reuse ordered."""
+    API.  Three streams form a pipeline (host-to-device copies, compute,
+    device-to-host copies) over two sets of device buffers used by
+    alternate steps: the copies into one set overlap the compute and the
+    read-back of the other, and events order each buffer's reuse (a set's
+    inputs are overwritten only after its previous compute has read them,
+    its compute starts only after its previous outputs have been read
+    back)."""
     import torch
+    sets = [layers, [L.twin(f8, device) for L in layers]]
     host = []
     h2d = d2h = 0
     for L in layers:
@@ -882,30 +899,33 @@ def run_e2e(f8, layers, args, device, stream, flops_step, world):
         d2h += sum(t.numel() * t.element_size() for t in hout)
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     n = len(layers)
-    ev_in = [torch.cuda.Event() for _ in range(n)]
-    ev_comp = [torch.cuda.Event() for _ in range(n)]
-    ev_out = [torch.cuda.Event() for _ in range(n)]
-    first = [True] * n
+    ev_in = [[torch.cuda.Event() for _ in range(n)] for _ in sets]
+    ev_comp = [[torch.cuda.Event() for _ in range(n)] for _ in sets]
+    ev_out = [[torch.cuda.Event() for _ in range(n)] for _ in sets]
+    used = [[False] * n for _ in sets]
+    count = [0]
 
     def step():
-        for i, (L, (hin, hout)) in enumerate(zip(layers, host)):
+        k = count[0] % 2
+        count[0] += 1
+        for i, (L, (hin, hout)) in enumerate(zip(sets[k], host)):
             with torch.cuda.stream(s_in):
-                if not first[i]:
-                    s_in.wait_event(ev_comp[i])      # last step's compute has read the inputs
+                if used[k][i]:
+                    s_in.wait_event(ev_comp[k][i])   # this set's last compute has read its inputs
                 for d, h in zip(L.inputs(), hin):
                     d.copy_(h, non_blocking=True)
-                ev_in[i].record(s_in)
-            stream.wait_event(ev_in[i])
-            if not first[i]:
-                stream.wait_event(ev_out[i])         # last step's outputs have been read back
+                ev_in[k][i].record(s_in)
+            stream.wait_event(ev_in[k][i])
+            if used[k][i]:
+                stream.wait_event(ev_out[k][i])      # this set's last outputs have been read back
             L.step(f8)
-            ev_comp[i].record(stream)
+            ev_comp[k][i].record(stream)
             with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_comp[i])
+                s_out.wait_event(ev_comp[k][i])
                 for h, d in zip(hout, L.outputs()):
                     h.copy_(d, non_blocking=True)
-                ev_out[i].record(s_out)
-            first[i] = False
+                ev_out[k][i].record(s_out)
+            used[k][i] = True
 
     for _ in range(2):
         step()
@@ -922,32 +942,41 @@ def run_e2e(f8, layers, args, device, stream, flops_step, world):
     torch.cuda.synchronize()
     ms = max_over_ranks(t0.elapsed_time(t1), world, device)
     total = sum_over_ranks(flops_step * args.e2e_steps, world, device)
-    # the results really came back: spot-check one output against its device copy
-    ok = torch.equal(host[-1][1][-1][:4].to(device), layers[-1].outputs()[-1][:4])
+    # the results really came back: spot-check one output of the last step
+    last = sets[(count[0] - 1) % 2]
+    ok = torch.equal(host[-1][1][-1][:4].to(device), last[-1].outputs()[-1][:4])
+    del sets[1]
     link = host_link_gbs(device, s_in, s_out)
     moved = (h2d + d2h) * args.e2e_steps / (ms * 1e-3) / 1e9
     return {"value": total / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-            "ms_per_step": ms / args.e2e_steps, "pipelined": "3 streams (h2d, compute, d2h)",
+            "ms_per_step": ms / args.e2e_steps,
+            "pipelined": "3 streams (h2d, compute, d2h), two buffer sets on alternate steps",
             "readback_check": bool(ok), "host_bytes_gbs": moved,
             "host_link_gbs_measured": link, "frac_of_host_link": moved / link if link else None}
 
 
-def host_link_gbs(device, s_in, s_out, nbytes=256 << 20, reps=5):
+def host_link_gbs(device, s_in, s_out, nbytes=512 << 20, reps=6):
     """Pinned host<->device bandwidth of this machine with both directions busy
-    at once (as in the e2e step): bytes moved both ways / time."""
+    at once (as in the e2e step): bytes moved both ways / time, after one
+    untimed round that touches every page."""
     import torch
     hs = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
     hd = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
     ds = torch.empty(nbytes, dtype=torch.uint8, device=device)
     dd = torch.empty(nbytes, dtype=torch.uint8, device=device)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(reps):
+
+    def both():
         with torch.cuda.stream(s_in):
             ds.copy_(hs, non_blocking=True)
         with torch.cuda.stream(s_out):
             hd.copy_(dd, non_blocking=True)
+
+    both()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        both()
     torch.cuda.synchronize()
     sec = time.perf_counter() - t0
     return 2 * nbytes * reps / sec / 1e9

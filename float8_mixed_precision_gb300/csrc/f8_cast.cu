@@ -11,8 +11,8 @@
 // block result into the output with one atomicMax on the fp32 bit pattern,
 // or (inside a linear) writes one partial maximum per block, so that no
 // output has to be zeroed first; the cast kernel reduces the partials in its
-// prologue.  amax_pair_kernel does the same for two tensors in one launch,
-// its blocks split between them in proportion to their sizes.
+// prologue.  amax_multi_kernel does the same for up to eight tensors in one
+// launch, its blocks split between them in proportion to their sizes.
 //
 // cast_transpose_kernel: a CTA owns a 128 x 128 tile.  Phase 1 reads it with
 // 16-byte loads (each thread 16 consecutive bf16 of one row), scales in
@@ -23,8 +23,9 @@
 // loads, a byte transpose with PRMT, and four 16-byte stores of the
 // column-major copy (8 consecutive threads write 128 contiguous bytes of one
 // column).  cast_transpose_tma_kernel does the same with the bf16 tiles
-// brought in by TMA through a 3-stage ring, for one or two tensors whose
-// sides are multiples of 128; the register kernel takes the other shapes.
+// brought in by TMA through a 3-stage ring, for one tensor or up to eight
+// (each with its own scale) whose sides are multiples of 128; the register
+// kernel takes the other shapes.
 //
 // swiglu_amax_kernel / swiglu_bwd_amax_kernel: h = silu(a) b, and the
 // gradient d(AB) of the w1+w3 group, each produced in one pass that also

@@ -144,10 +144,12 @@ f8_status f8_quantize_fmt(const void *x, int64_t rows, int64_t cols, f8_format f
 /*
  * Dynamic tensorwise quantisation of several tensors at once, each with its
  * own amax and scale: every tensor gets exactly what f8_quantize_fmt gives
- * it (bit-identical), in two launches for all of them when every side is a
- * multiple of 128 (one amax launch whose CTAs are split between the tensors
- * in proportion to their sizes, then one TMA cast launch over all their
- * 128 x 128 tiles), otherwise one f8_quantize_fmt per tensor, in order.
+ * it (bit-identical).  Consecutive tensors whose sides are multiples of 128
+ * share a launch pair while their bf16 total stays within 112 MiB (one
+ * amax launch whose CTAs are split between the tensors in proportion to
+ * their sizes, then one TMA cast launch over all their 128 x 128 tiles; the
+ * cast's re-read then still finds the amax pass's reads in L2); a larger
+ * tensor, or one with other sides, gets f8_quantize_fmt's pair of its own.
  * Two launches instead of two per tensor matter for the small tensors of a
  * step (the 8-33 MB weights of the Llama-3.1-8B attention projections),
  * whose launches are dominated by ramp-up rather than bytes: e.g. all the
