@@ -53,14 +53,18 @@ FP8_PER_BF16 = 2.0          # nominal dense FP8 : BF16 tensor throughput
 HBM_NOMINAL_GBS = 8000.0
 REF_BUDGET_S = 60.0   # timed seconds of the CPU reference arm
 
-# DRAM bytes (read + write) of all GEMM launches of one step of the default
-# workload (the Llama-3.1-8B block with its shared-input groups), from one
-# ncu capture of dram__bytes_read.sum + dram__bytes_write.sum; valid for the
-# GEMM sources whose hash is given, reported as null once they change.
-GEMM_TRAFFIC = {"workload": 5, "groups": 1, "bytes_per_step": 4815535872,
+# DRAM bytes (read + write) of all GEMM launches, and of all quantisation
+# launches (amax and cast), of one step of the default workload (the
+# Llama-3.1-8B block with its shared-input groups), from one ncu capture of
+# dram__bytes_read.sum + dram__bytes_write.sum with --cache-control none
+# (1 pass, so each launch runs once and finds L2 as the step left it; a
+# launch's writes include earlier launches' lines that L2 evicts then, and
+# the two figures sum to the step's DRAM traffic); valid for the sources
+# whose hash is given, reported as null once they change.
+GEMM_TRAFFIC = {"workload": 5, "groups": 1, "bytes_per_step": 5383608576,
                 "sources_sha256_16": "b6d759a6a8fb6715"}
-# The same for the quantisation launches (amax and cast) of one step.
-QUANT_TRAFFIC = {"workload": 5, "groups": 1, "bytes_per_step": None, "sources_sha256_16": None}
+QUANT_TRAFFIC = {"workload": 5, "groups": 1, "bytes_per_step": 3926931456,
+                 "sources_sha256_16": "16b3f240e25bd695"}
 
 
 def sources_hash(files) -> str:
