@@ -43,10 +43,6 @@ f8_status from_cuda(cudaError_t e)
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// bf16 size above which a tensor's cast stores with the evict-first hint
-// (more than L2 holds: its re-read cannot find it all there anyway)
-constexpr int64_t kStreamOutBytes = 128ll << 20;
-
 // The GEMM kernels number the output tiles of a launch (128 x 256 at the
 // smallest) in 32-bit ints.
 bool tiles_fit(int64_t M, int64_t N) { return ((M + 127) / 128) * ((N + 255) / 256) <= INT32_MAX / 2; }
@@ -140,7 +136,7 @@ cudaError_t quantize_batches(const QuantDesc *d, int n, int fmt, unsigned *parts
             if (e == cudaSuccess)
                 e = launch_cast_transpose(d[i].x, d[i].rows, d[i].cols, nullptr, parts, np,
                                           d[i].amax_out, d[i].scale_out, d[i].q, d[i].q_t, fmt, dev,
-                                          st, true, 2 * d[i].rows * d[i].cols > kStreamOutBytes);
+                                          st, true);
         }
         if (e != cudaSuccess)
             return e;
@@ -378,8 +374,7 @@ static f8_status quantize_impl(const void *x, int64_t rows, int64_t cols, int fm
     int np = 0;
     F8_TRY_CUDA(launch_amax_partials(x, rows * cols, parts, &np, *dev, st));
     return from_cuda(launch_cast_transpose(x, rows, cols, nullptr, parts, np, amax_out, scale_out,
-                                           q, q_t, fmt, *dev, st, true,
-                                           2 * rows * cols > kStreamOutBytes));
+                                           q, q_t, fmt, *dev, st, true));
 }
 
 f8_status f8_quantize(const void *x, int64_t rows, int64_t cols, float *amax_out,
@@ -534,7 +529,7 @@ static f8_status linear_bwd_impl(const void *dy, int fdy, const f8_linear_saved 
     F8_TRY_CUDA(launch_amax_partials(dy, M * N, bw.parts_dy, &np, *dev, st));
     F8_TRY_CUDA(launch_cast_transpose(dy, M, N, nullptr, bw.parts_dy, np, bw.amax_dy, bw.scale_dy,
                                       dx ? bw.dy_q : nullptr, dw ? bw.dy_t : nullptr, fdy, *dev, st,
-                                      true, 2 * M * N > kStreamOutBytes));
+                                      true));
     return from_cuda(launch_bwd_gemms(bw, saved, M, N, K, fdy, dx, dw, *dev, st));
 }
 

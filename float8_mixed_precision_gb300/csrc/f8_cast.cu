@@ -374,7 +374,7 @@ swiglu_bwd_amax_kernel(const uint4 *__restrict__ dh, const uint4 *__restrict__ a
 // write 128 contiguous bytes of one column).
 __device__ __forceinline__ void transpose_out(const uint8_t *tile, uint8_t *__restrict__ qt,
                                               int64_t rows, int64_t cols, int64_t r0, int64_t c0,
-                                              int t, unsigned *status, bool stream = false)
+                                              int t, unsigned *status)
 {
     const int rs = t & 7;          // 16-row segment
     const int cg = t >> 3;         // 4-column group (0..31)
@@ -401,13 +401,9 @@ __device__ __forceinline__ void transpose_out(const uint8_t *tile, uint8_t *__re
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int64_t o = (c0 + cg * 4 + j) * rows + r0 + rs * 16;
-        if (in_range(o, 16, rows * cols, status)) {
-            const uint4 v = make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
-            if (stream)
-                __stcs(reinterpret_cast<uint4 *>(qt + o), v);
-            else
-                *reinterpret_cast<uint4 *>(qt + o) = v;
-        }
+        if (in_range(o, 16, rows * cols, status))
+            *reinterpret_cast<uint4 *>(qt + o) =
+                make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
     }
 }
 
@@ -513,9 +509,6 @@ struct CastSet {
     int early;   // 1: the inputs are complete before the dependency wait (the
                  // previous launch only read them: their amax pass)
     int reverse; // 1: tiles last first
-    int stream;  // 1: q and q^T stored with the evict-first hint (a tensor
-                 // larger than L2: its outputs then leave L2 before the
-                 // input lines the re-read still needs)
 };
 
 // Tiles are taken in reverse launch order (the last tile first): the amax
@@ -640,18 +633,14 @@ cast_transpose_tma_kernel(const __grid_constant__ CastSet<NS> set, unsigned *__r
             const uint4 v = *reinterpret_cast<const uint4 *>(src + row * (kTile * 2) + c8 * 16);
             const uint2 codes = cvt8<FMT>(v, s);
             const int64_t o = (r0 + row) * cols + c0 + c8 * 8;
-            if (q != nullptr && in_range(o, 8, rows * cols, status)) {
-                if (set.stream)
-                    __stcs(reinterpret_cast<uint2 *>(q + o), codes);
-                else
-                    *reinterpret_cast<uint2 *>(q + o) = codes;
-            }
+            if (q != nullptr && in_range(o, 8, rows * cols, status))
+                *reinterpret_cast<uint2 *>(q + o) = codes;
             const int pch = (c8 >> 1) ^ ((row >> 4) & 7);
             *reinterpret_cast<uint2 *>(tile + row * kTile + pch * 16 + (c8 & 1) * 8) = codes;
         }
         __syncthreads();
         if (qt != nullptr)
-            transpose_out(tile, qt, rows, cols, r0, c0, t, status, set.stream != 0);
+            transpose_out(tile, qt, rows, cols, r0, c0, t, status);
         __syncthreads();  // the input buffer and the parked tile are free again
     }
     if (t == 0) {
@@ -757,8 +746,7 @@ cudaError_t launch_amax_partials(const void *x, int64_t n, unsigned *partials, i
 cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, const float *amax,
                                   const unsigned *partials, int nparts, float *amax_out,
                                   float *scale_out, uint8_t *q, uint8_t *q_t, int fmt,
-                                  const DeviceInfo &dev, cudaStream_t stream, bool early,
-                                  bool stream_out)
+                                  const DeviceInfo &dev, cudaStream_t stream, bool early)
 {
     const int64_t ntiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
     CUtensorMap map;
@@ -777,7 +765,6 @@ cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, con
         set.nseg = 1;
         set.early = early ? 1 : 0;
         set.reverse = cast_reverse_enabled() ? 1 : 0;
-        set.stream = stream_out && cast_stream_enabled() ? 1 : 0;
         return launch_pdl(fmt == 1 ? cast_transpose_tma_kernel<1, 1> : cast_transpose_tma_kernel<0, 1>,
                           dim3(static_cast<unsigned>(blocks)), dim3(kCastThreads), kTmaCastSmem,
                           stream, set, dev.status, wait_limit_ns());
@@ -889,7 +876,6 @@ cudaError_t launch_quantize_multi(const QuantDesc *t, int n, int fmt, unsigned *
     set.nseg = n;
     set.early = 1;  // the amax launch just before only reads the inputs
     set.reverse = cast_reverse_enabled() ? 1 : 0;
-    set.stream = 0;  // a batch fits L2; its outputs may stay for the GEMMs
     cudaError_t e = launch_pdl(amax_multi_kernel, dim3(static_cast<unsigned>(segs.first_block[n])),
                                dim3(kAmaxThreads), 0, stream, segs, dev.status);
     if (e != cudaSuccess)

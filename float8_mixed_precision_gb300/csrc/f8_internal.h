@@ -50,14 +50,6 @@ inline bool cast_reverse_enabled()
     return e == nullptr || e[0] != '0';
 }
 
-// The cast of a tensor larger than L2 stores its codes with the evict-first
-// hint unless F8_CAST_STREAM=0.
-inline bool cast_stream_enabled()
-{
-    const char *e = std::getenv("F8_CAST_STREAM");
-    return e == nullptr || e[0] != '0';
-}
-
 // Largest bf16 total (bytes) one multi-tensor quantisation launch pair
 // takes; larger lists are split into consecutive batches within it, and a
 // tensor larger than it is quantised alone.  F8_QUANT_BATCH_MB overrides
@@ -169,14 +161,10 @@ cudaError_t launch_amax_partials(const void *x, int64_t n, unsigned *partials, i
 // amax pass), so x is complete when this kernel starts and its first tiles
 // may be loaded before the dependency wait.  Leave it false after a kernel
 // that writes x.
-// stream_out: store q and q^T with the evict-first hint (for a tensor larger
-// than L2, whose outputs would otherwise evict the input lines its re-read
-// still needs); ignored by the register cast.
 cudaError_t launch_cast_transpose(const void *x, int64_t rows, int64_t cols, const float *amax,
                                   const unsigned *partials, int nparts, float *amax_out,
                                   float *scale_out, uint8_t *q, uint8_t *q_t, int fmt,
-                                  const DeviceInfo &dev, cudaStream_t stream, bool early = false,
-                                  bool stream_out = false);
+                                  const DeviceInfo &dev, cudaStream_t stream, bool early = false);
 
 // Most tensors one multi-tensor quantisation launch pair takes.
 constexpr int kMaxQuantTensors = 8;
