@@ -272,6 +272,36 @@ class NvmlClockSampler:
                 "source": f"NVML, every {self.period * 1e3:g} ms"}
 
 
+def gpu_local_cpus(gpu_index: int):
+    """The CPUs NVML names as closest to the GPU (nvmlDeviceGetCpuAffinity, a
+    read-only query), or None.  The e2e leg runs on them so that its pinned
+    host buffers are allocated, and first touched, on the GPU's NUMA node."""
+    try:
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(gpu_index).uuid)
+            name = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            ok = lib.nvmlDeviceGetHandleByUUID(name.encode(), ctypes.byref(h)) == 0
+        except Exception:
+            ok = False
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(gpu_index, ctypes.byref(h)) != 0:
+            return None
+        words = 16
+        mask = (ctypes.c_ulong * words)()
+        if lib.nvmlDeviceGetCpuAffinity(h, words, mask) != 0:
+            return None
+        bits = ctypes.sizeof(ctypes.c_ulong) * 8
+        cpus = {w * bits + b for w in range(words) for b in range(bits) if (mask[w] >> b) & 1}
+        return cpus & os.sched_getaffinity(0) or None
+    except Exception:
+        return None
+
+
 def fp8_peak_for(seconds: float, peaks: dict) -> tuple[float, str]:
     """The FP8 dense peak a rate measured over a region of `seconds` is held
     to: the measured bf16 GEMM peak x 2 (the FP8 : BF16 dense ratio), burst
@@ -892,6 +922,12 @@ def run_e2e(f8, layers, args, device, stream, flops_step, world):
     its compute starts only after its previous outputs have been read
     back)."""
     import torch
+    # run on the GPU's NUMA-local CPUs while the pinned buffers are made and
+    # used (first touch places them on that node); restored at the end
+    old_aff = os.sched_getaffinity(0)
+    local = gpu_local_cpus(device.index if device.index is not None else 0)
+    if local:
+        os.sched_setaffinity(0, local)
     sets = [layers, [L.twin(f8, device) for L in layers]]
     host = []
     h2d = d2h = 0
@@ -952,12 +988,15 @@ def run_e2e(f8, layers, args, device, stream, flops_step, world):
     del sets[1]
     link = host_link_gbs(device, s_in, s_out)
     moved = (h2d + d2h) * args.e2e_steps / (ms * 1e-3) / 1e9
+    os.sched_setaffinity(0, old_aff)
     return {"value": total / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
             "ms_per_step": ms / args.e2e_steps,
             "pipelined": "3 streams (h2d, compute, d2h), two buffer sets on alternate steps",
             "readback_check": bool(ok), "host_bytes_gbs": moved,
-            "host_link_gbs_measured": link, "frac_of_host_link": moved / link if link else None}
+            "host_link_gbs_measured": link, "frac_of_host_link": moved / link if link else None,
+            "host_cpus": (f"{len(local)} GPU-local CPUs (NVML affinity)" if local
+                          else "no NVML affinity: unbound")}
 
 
 def host_link_gbs(device, s_in, s_out, nbytes=512 << 20, reps=6):
