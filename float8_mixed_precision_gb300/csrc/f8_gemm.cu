@@ -50,7 +50,9 @@
 #include <cuda_runtime.h>
 
 #include <cstdlib>
+#include <map>
 #include <mutex>
+#include <vector>
 
 #include "f8_internal.h"
 #include "f8_ptx.cuh"
@@ -787,6 +789,37 @@ int64_t variant_units(int v, const DeviceInfo &dev)
 
 SchedProblem sched_problem(const GemmDesc &g) { return SchedProblem{g.M, g.N, g.K}; }
 
+// sched_partition's plans, keyed by the problems' extents and the launch
+// geometry: a training step asks for the same few plans every step, and a
+// plan costs tens of microseconds of host time to search.
+std::mutex g_plan_mutex;
+std::map<std::vector<int64_t>, Partition> g_plan_cache;
+
+Partition cached_partition(const SchedProblem *sp, int n, int tile_m, int64_t units)
+{
+    std::vector<int64_t> key;
+    key.reserve(3 * n + 2);
+    for (int i = 0; i < n; ++i) {
+        key.push_back(sp[i].M);
+        key.push_back(sp[i].N);
+        key.push_back(sp[i].K);
+    }
+    key.push_back(tile_m);
+    key.push_back(units);
+    {
+        std::lock_guard<std::mutex> lock(g_plan_mutex);
+        auto it = g_plan_cache.find(key);
+        if (it != g_plan_cache.end())
+            return it->second;
+    }
+    const Partition part = sched_partition(sp, n, tile_m, 256, units);
+    std::lock_guard<std::mutex> lock(g_plan_mutex);
+    if (g_plan_cache.size() >= 1024)
+        g_plan_cache.clear();
+    g_plan_cache.emplace(std::move(key), part);
+    return part;
+}
+
 // One launch over probs[idx[0 .. n)], all of kernel variant v.
 cudaError_t launch_set(const GemmDesc *probs, const int *idx, int n, int v, const DeviceInfo &dev,
                        cudaStream_t stream)
@@ -853,7 +886,7 @@ cudaError_t launch_gemm_multi(const GemmDesc *g, int n, const DeviceInfo &dev, c
         for (int i = 0; i < n; ++i)
             part.idx[0][i] = i;
     } else {
-        part = sched_partition(sp, n, variant_tile_m(v0), 256, variant_units(v0, dev));
+        part = cached_partition(sp, n, variant_tile_m(v0), variant_units(v0, dev));
     }
     for (int j = 0; j < part.nlaunch; ++j) {
         const cudaError_t e = launch_set(g, part.idx[j], part.nprob[j], v0, dev, stream);
