@@ -795,7 +795,13 @@ def run_ours(args, world, rank, local):
                 e.update({"algorithmic_bytes_per_step": d["work"] / nsteps_k,
                           "dram_bytes_per_step": qt,
                           "dram_over_algorithmic": (qt / (d["work"] / nsteps_k)) if qt else None,
-                          "dram_gbs": (qt / (d["ms"] / nsteps_k * 1e-3) / 1e9) if qt else None})
+                          "dram_gbs": (qt / (d["ms"] / nsteps_k * 1e-3) / 1e9) if qt else None,
+                          # the same time against the bytes DRAM really moved, and the
+                          # best frac_of_hbm_measured those bytes allow (every byte at
+                          # the copy rate, no launch costs): the two-pass ceiling
+                          "dram_frac_of_hbm_measured": ((qt / (d["ms"] / nsteps_k * 1e-3) / 1e9)
+                                                        / peaks["hbm_gbs"]) if qt else None,
+                          "two_pass_ceiling_frac": ((d["work"] / nsteps_k) / qt) if qt else None})
         kernels[kind] = e
     g = per["gemm"]
     achieved = g["work"] / (g["ms"] * 1e-3) / 1e12
