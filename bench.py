@@ -474,23 +474,37 @@ class GroupLinear8:
 
     def step_timed(self, f8, ev):
         s = self.saved
-        M, K = self.M, self.K
         xs = s[0].x_scalars
         outs = [(self.xq, s[0].x_t, xs[1], xs[0])] + [
             (wq, si.w_t, si.scalars[3], si.scalars[2]) for wq, si in zip(self.wq, s)]
         ev("quantize", 4 * (self.x.numel() + sum(w.numel() for w in self.w)),
            lambda: f8.f8_quantize_multi([self.x] + self.w, outs=outs, ws=self.qws))
-        ev("gemm", sum(2 * M * N * K for N in self.Ns), lambda: f8.f8_gemm_grouped(
-            [(self.xq, wq, xs[1], si.scalars[3], y) for wq, si, y in zip(self.wq, s, self.y)]))
+        (_, fwd_flops, fwd), (_, bwd_flops, bwd) = self.gemm_calls(f8)
+        ev("gemm", fwd_flops, fwd)
         douts = [(q, t, d[1], d[0]) for q, t, d in zip(self.dyq, self.dyt, self.dys)]
         ev("quantize", 4 * sum(d.numel() for d in self.dy),
            lambda: f8.f8_quantize_multi(self.dy, fmt=self.dy_fmt, outs=douts, ws=self.qws))
-        probs = []
+        ev("gemm", bwd_flops, bwd)
+
+    def gemm_calls(self, f8):
+        """The group's forward GEMMs and its backward GEMMs, each as the
+        one f8_gemm_grouped call the group makes (the planner decides the
+        launches): [(label, flops, call), ...] on the decomposed path's
+        quantised operands."""
+        s = self.saved
+        M, K = self.M, self.K
+        xs = s[0].x_scalars
+        fwd = [(self.xq, wq, xs[1], si.scalars[3], y) for wq, si, y in zip(self.wq, s, self.y)]
+        bwd = []
         for i in range(len(self.Ns)):
-            probs.append((self.dyq[i], s[i].w_t, self.dys[i][1], s[i].scalars[3], self.dx[i],
-                          self.dy_fmt))
-            probs.append((self.dyt[i], s[i].x_t, self.dys[i][1], xs[1], self.dw[i], self.dy_fmt))
-        ev("gemm", sum(4 * M * N * K for N in self.Ns), lambda: f8.f8_gemm_grouped(probs))
+            bwd.append((self.dyq[i], s[i].w_t, self.dys[i][1], s[i].scalars[3], self.dx[i],
+                        self.dy_fmt))
+            bwd.append((self.dyt[i], s[i].x_t, self.dys[i][1], xs[1], self.dw[i], self.dy_fmt))
+        ns = "+".join(str(N) for N in self.Ns)
+        return [(f"{self.lin.name} fwd M={M} K={K} N={ns}", sum(2 * M * N * K for N in self.Ns),
+                 lambda: f8.f8_gemm_grouped(fwd)),
+                (f"{self.lin.name} dgrad+wgrad M={M} K={K} N={ns}",
+                 sum(4 * M * N * K for N in self.Ns), lambda: f8.f8_gemm_grouped(bwd))]
 
 
 class FfnIn8(Linear8):
@@ -920,6 +934,16 @@ def kernel_bench(f8, layers, device, stream, iters=50):
                             "frac_of_fp8_nominal": tf / FP8_NOMINAL_TFLOPS})
                 del c
             del ops
+        if isinstance(L, GroupLinear8):
+            # the members' GEMMs as the step launches them: the skinny wk, wv
+            # (or w1, w3) problems share launches with the others
+            for label, flops, fn in L.gemm_calls(f8):
+                ms = timed(fn)
+                tf = flops / ms / 1e9
+                out.append({"kernel": "gemm (the group's grouped call)", "shape": label,
+                            "us": ms * 1e3, "tflops": tf,
+                            "frac_of_fp8_measured_burst": tf / fp8_burst,
+                            "frac_of_fp8_nominal": tf / FP8_NOMINAL_TFLOPS})
     del flush, clean
     return out
 
