@@ -853,8 +853,8 @@ def run_ours(args, world, rank, local):
 
 
 def kernel_bench(f8, layers, device, stream, iters=50):
-    """Each kernel timed alone on the workload's tensors, L2 flushed before
-    every launch (a 1 GiB fill, then a 256 MB read so that the L2 holds
+    """Each kernel timed alone on the workload's tensors (10 warm-up
+    launches, then the median of `iters`), L2 flushed before every launch (a 1 GiB fill, then a 256 MB read so that the L2 holds
     clean lines and the timed kernel pays no write-back for the flush), CUDA
     events around the launch only.
     amax: 2 B/elem read; cast_transpose: 2 B/elem read + 2 x 1 B/elem
@@ -867,7 +867,7 @@ def kernel_bench(f8, layers, device, stream, iters=50):
 
     def timed(fn):
         ts = []
-        for _ in range(3):
+        for _ in range(10):  # warm-up launches
             fn()
         for _ in range(iters):
             flush.fill_(1)                # evicts everything from L2 ...
