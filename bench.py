@@ -853,9 +853,10 @@ def run_ours(args, world, rank, local):
 
 
 def kernel_bench(f8, layers, device, stream, iters=50):
-    """Each kernel timed alone on the workload's tensors (10 warm-up
-    launches, then the median of `iters`), L2 flushed before every launch (a 1 GiB fill, then a 256 MB read so that the L2 holds
-    clean lines and the timed kernel pays no write-back for the flush), CUDA
+    """Each kernel timed alone on the workload's tensors: 10 warm-up
+    launches, then the median of `iters`, with L2 flushed before every
+    launch (a 1 GiB fill, then a 256 MB read so that the L2 holds clean
+    lines and the timed kernel pays no write-back for the flush) and CUDA
     events around the launch only.
     amax: 2 B/elem read; cast_transpose: 2 B/elem read + 2 x 1 B/elem
     written; GEMM: 2 M N K flops.  f8_amax includes its 4-byte memset."""
