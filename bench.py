@@ -801,7 +801,8 @@ def run_ours(args, world, rank, local):
                       "fp8_peak_regime": regime,
                       "frac_of_fp8_nominal": rate / 1e12 / FP8_NOMINAL_TFLOPS})
         else:
-            e.update({"gbs": rate / 1e9, "frac_of_hbm_measured": rate / 1e9 / peaks["hbm_gbs"]})
+            e.update({"gbs": rate / 1e9, "frac_of_hbm_measured": rate / 1e9 / peaks["hbm_gbs"],
+                      "frac_of_hbm_nominal": rate / 1e9 / HBM_NOMINAL_GBS})
             if kind == "quantize":
                 # DRAM bytes the quantisation launches move (ncu), against the
                 # algorithmic 4 B per element (2 read + 2 written)
@@ -906,16 +907,19 @@ def kernel_bench(f8, layers, device, stream, iters=50):
                 ms = timed(lambda: f8.f8_amax(t, a1))
                 out.append({"kernel": "amax", "tensor": f"{lin.name}.{name} {list(t.shape)}",
                             "us": ms * 1e3, "gbs": 2 * t.numel() / ms / 1e6,
-                            "frac_of_hbm_measured": 2 * t.numel() / ms / 1e6 / peaks["hbm_gbs"]})
+                            "frac_of_hbm_measured": 2 * t.numel() / ms / 1e6 / peaks["hbm_gbs"],
+                            "frac_of_hbm_nominal": 2 * t.numel() / ms / 1e6 / HBM_NOMINAL_GBS})
                 ms = timed(lambda: f8.f8_cast_transpose(t, a1, sc, q, qt))
                 out.append({"kernel": "cast_transpose", "tensor": f"{lin.name}.{name} {list(t.shape)}",
                             "us": ms * 1e3, "gbs": 4 * t.numel() / ms / 1e6,
-                            "frac_of_hbm_measured": 4 * t.numel() / ms / 1e6 / peaks["hbm_gbs"]})
+                            "frac_of_hbm_measured": 4 * t.numel() / ms / 1e6 / peaks["hbm_gbs"],
+                            "frac_of_hbm_nominal": 4 * t.numel() / ms / 1e6 / HBM_NOMINAL_GBS})
                 ms = timed(lambda: f8.f8_quantize(t, a1, sc, q, qt, ws, fmt=fmt))
                 out.append({"kernel": "quantize (amax + cast_transpose launches)",
                             "tensor": f"{lin.name}.{name} {list(t.shape)}", "us": ms * 1e3,
                             "gbs": 4 * t.numel() / ms / 1e6,
                             "frac_of_hbm_measured": 4 * t.numel() / ms / 1e6 / peaks["hbm_gbs"],
+                            "frac_of_hbm_nominal": 4 * t.numel() / ms / 1e6 / HBM_NOMINAL_GBS,
                             "note": "4 B/elem counted (2 read + 2 written); the cast's re-read is not"})
             (xq, xt, sx), (wq, wt, sw), (dyq, dyt, sdy) = ops["x"], ops["w"], ops["dy"]
             for gname, (a, b, sa, sb, mm, nn, kk) in (
