@@ -1,6 +1,7 @@
 // C-ABI of libf8: argument checks on the host, per-device state, the
 // device status word, and the forward / backward composition of a Float8
 // linear out of the amax, cast_transpose and GEMM launches.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -167,11 +168,46 @@ cudaError_t launch_bwd_gemms(const BwdWs &bw, const f8_linear_saved *saved, int6
 
 } // namespace
 
+namespace {
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+CtxGetCurrentFn ctx_get_current_fn()
+{
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
+
+// A host thread that has made no context-bound CUDA call yet has no
+// current context, and the driver calls the library makes itself (the
+// tensor-map encoder) would fail in it.  Such a thread gets the current
+// device's primary context, as the runtime's own first launch would bind
+// it; a context the caller made current is left alone.
+void ensure_context(int dev)
+{
+    const CtxGetCurrentFn fn = ctx_get_current_fn();
+    CUcontext c = nullptr;
+    if (fn != nullptr && fn(&c) == CUDA_SUCCESS && c == nullptr)
+        cudaSetDevice(dev);
+}
+
+} // namespace
+
 const DeviceInfo *device_info()
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return nullptr;
+    ensure_context(dev);
     std::lock_guard<std::mutex> lock(g_dev_mutex);
     if (!g_dev_ready[dev]) {
         DeviceInfo info;

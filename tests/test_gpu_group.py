@@ -300,3 +300,79 @@ def test_llama8b_w13_group(f8):
     check_close(dws[0][torch.from_numpy(rows_n).to(DEV)],
                 oracle.gemm_rows(qdy["qt"], qx["qt"], qdy["scale"], qx["scale"], rows_n),
                 what="dW_w1 rows")
+
+
+def test_gemm_grouped_from_two_host_threads(f8):
+    """Two host threads call f8_gemm_grouped at the same time, each on its
+    own stream, alternating between two problem sets of their own, so the
+    planner's cache of launch plans is read and filled from both threads at
+    once.  The threads make no context-bound CUDA call of their own before
+    the library's first call, so the library binds the device's primary
+    context for them (its tensor-map encoder needs one).  Every output is
+    bit-identical to f8_gemm on its problem."""
+    import threading
+    sets = [
+        [[(512, 512, 1024, 0), (512, 256, 256, 0), (384, 128, 1024, 0)],
+         [(512, 256, 128, 0), (256, 512, 512, 0), (512, 128, 1024, 0), (256, 256, 128, 0)]],
+        [[(512, 384, 512, 0), (256, 256, 256, 1), (512, 640, 512, 0)],
+         [(768, 256, 256, 0), (512, 512, 768, 0), (256, 384, 256, 0)]],
+    ]
+    probs = [[_problems(s, 300 + 40 * t + 20 * j) for j, s in enumerate(ts)]
+             for t, ts in enumerate(sets)]
+    singles = [[[f8.f8_gemm(qa, qb, sa, sb, fmt_a=fa) for qa, qb, sa, sb, M, N, K, fa in p]
+                for p in tp] for tp in probs]
+    outs = [[[torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+              for _, _, _, _, M, N, _, _ in p] for p in tp] for tp in probs]
+    torch.cuda.synchronize()
+    errors = []
+
+    def work(t):
+        try:
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                for it in range(40):
+                    j = it % 2
+                    f8.f8_gemm_grouped([(qa, qb, sa, sb, o, fa) for (qa, qb, sa, sb, M, N, K, fa), o
+                                        in zip(probs[t][j], outs[t][j])])
+            stream.synchronize()
+        except Exception as e:  # reported on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(t,)) for t in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join(timeout=120)
+    assert not errors, errors
+    torch.cuda.synchronize()
+    assert f8.f8_last_device_status() == 0
+    for t in range(2):
+        for j in range(2):
+            for o, s in zip(outs[t][j], singles[t][j]):
+                assert _eq(o, s)
+
+
+def test_planner_cache_past_its_bound(f8):
+    """More distinct problem sets than the planner keeps plans for (1,100
+    against 1,024): the cache is emptied and refilled on the way, and the
+    outputs still equal single launches (checked on the first, the
+    1,030th and the last set)."""
+    K0, K1 = 256, 512
+    a0 = _bf((256, K0), 1.0, 501).to(DEV)
+    a1 = _bf((256, K1), 1.0, 502).to(DEV)
+    b0 = _bf((16 * 1100, K0), 0.05, 503).to(DEV)
+    b1 = _bf((64, K1), 0.05, 504).to(DEV)
+    qa0, _, sa0, _ = _quant(a0, 0)
+    qa1, _, sa1, _ = _quant(a1, 0)
+    qb0, _, sb0, _ = _quant(b0, 0)
+    qb1, _, sb1, _ = _quant(b1, 0)
+    checked = {0: None, 1029: None, 1099: None}
+    for i in range(1100):
+        N = 16 * (i + 1)
+        outs = f8.f8_gemm_grouped([(qa0, qb0[:N], sa0, sb0), (qa1, qb1, sa1, sb1)])
+        if i in checked:
+            checked[i] = (N, outs)
+    for i, (N, outs) in checked.items():
+        assert _eq(outs[0], f8.f8_gemm(qa0, qb0[:N], sa0, sb0)), i
+        assert _eq(outs[1], f8.f8_gemm(qa1, qb1, sa1, sb1)), i
+    assert f8.f8_last_device_status() == 0
