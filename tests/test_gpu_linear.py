@@ -325,3 +325,42 @@ def test_backward_groups_where_the_schedule_gains(f8, M, N, K, grouped):
     torch.cuda.synchronize()
     assert f8.f8_kernel_launches() - n0 == (3 if grouped else 4)
     assert f8.f8_last_device_status() == 0
+
+
+def _at_offset(t, offset_bytes):
+    """A copy of t whose storage starts `offset_bytes` (a multiple of 16)
+    past a 256-byte boundary: legal for the ABI (16-byte alignment), but not
+    the alignment torch's allocator gives."""
+    n = t.numel() * t.element_size()
+    raw = torch.empty(n + 256, dtype=torch.uint8, device=t.device)
+    view = raw[offset_bytes:offset_bytes + n].view(t.dtype).view(t.shape)
+    view.copy_(t)
+    return view
+
+
+@pytest.mark.parametrize("offset", [16, 48, 144])
+def test_linear_on_16_byte_aligned_buffers(f8, offset):
+    """Every tensor of a linear (X, W, dY, Y, dX, dW, the saved q^T copies
+    and scalars) at 16-byte but not 256-byte alignment: the TMA loads and
+    stores, the casts' vector stores and the epilogue take such addresses.
+    Outputs are bit-identical to the same linear on allocator-aligned
+    buffers."""
+    M, N, K = 512, 768, 1024
+    d = wl.custom_linear(M, K, N, seed=61, dy_std=0.1)
+    x, w, dy = d["x"].to(DEV), d["w"].to(DEV), d["dy"].to(DEV)
+    y0, s0 = f8.f8_linear_fwd(x, w)
+    dx0, dw0 = f8.f8_linear_bwd(dy, s0)
+    xo, wo, dyo = _at_offset(x, offset), _at_offset(w, offset), _at_offset(dy, offset)
+    assert xo.data_ptr() % 256 == offset % 256 and xo.data_ptr() % 16 == 0
+    yo = _at_offset(torch.zeros((M, N), dtype=torch.bfloat16, device=DEV), offset)
+    dxo = _at_offset(torch.zeros((M, K), dtype=torch.bfloat16, device=DEV), offset)
+    dwo = _at_offset(torch.zeros((N, K), dtype=torch.bfloat16, device=DEV), offset)
+    so = f8.LinearSaved(_at_offset(torch.zeros((K, M), dtype=torch.uint8, device=DEV), offset),
+                        _at_offset(torch.zeros((K, N), dtype=torch.uint8, device=DEV), offset),
+                        _at_offset(torch.zeros(4, dtype=torch.float32, device=DEV), offset))
+    f8.f8_linear_fwd(xo, wo, yo, so)
+    f8.f8_linear_bwd(dyo, so, dx=dxo, dw=dwo)
+    assert f8.f8_last_device_status() == 0
+    for got, want in ((yo, y0), (dxo, dx0), (dwo, dw0), (so.x_t, s0.x_t), (so.w_t, s0.w_t),
+                      (so.scalars, s0.scalars)):
+        assert torch.equal(got.contiguous().view(torch.uint8), want.contiguous().view(torch.uint8))
