@@ -186,6 +186,14 @@ def _stream(stream) -> int:
     return int(stream)
 
 
+def _need(what: str, dtype, *ts) -> None:
+    """TypeError unless every given tensor is 2-D of `dtype`: the C calls
+    read the bytes as that type and take the shape from the tensor."""
+    for t in ts:
+        if t is not None and (t.dtype != dtype or t.dim() != 2):
+            raise TypeError(f"{what} takes 2-D {str(dtype).replace('torch.', '')} tensors")
+
+
 def _ptr(t: torch.Tensor | None):
     if t is None:
         return None
@@ -298,6 +306,7 @@ def f8_gemm(a: torch.Tensor, b: torch.Tensor, scale_a: torch.Tensor, scale_b: to
             stream=None) -> torch.Tensor:
     """bf16(a b^T / (scale_a scale_b)) for FP8 codes a [M,K], b [N,K] (uint8);
     formats other than E4M3 go through f8_gemm_fmt."""
+    _need("f8_gemm", torch.uint8, a, b)
     M, K = a.shape
     N, K2 = b.shape
     if K != K2:
@@ -318,6 +327,8 @@ def f8_gemm_grouped(problems, stream=None) -> list:
     (f8_gemm_grouped).  Each problem is
     (a, b, scale_a, scale_b, out, fmt_a, fmt_b) as for f8_gemm (out, fmt_a
     and fmt_b may be None / omitted); returns the outputs."""
+    for p in problems:
+        _need("f8_gemm_grouped", torch.uint8, p[0], p[1])
     arr = (_GemmProblem * len(problems))()
     outs = []
     for i, p in enumerate(problems):
@@ -448,6 +459,7 @@ def f8_linear_fwd_group(x: torch.Tensor, ws_: list, ys: list | None = None, save
                         ws: torch.Tensor | None = None, stream=None):
     """Y_i = X W_i^T for linears sharing X (f8_linear_fwd_group): X quantised
     once, each W_i with its own scale; returns (ys, saved)."""
+    _need("f8_linear_fwd_group", torch.bfloat16, x, *ws_)
     M, K = x.shape
     Ns = [w.shape[0] for w in ws_]
     for w in ws_:
@@ -471,6 +483,7 @@ def f8_linear_bwd_group(dys: list, saved: list, K: int, dxs: list | None = None,
                         fmt: int = F8_E4M3, want_dx: bool = True, want_dw: bool = True, stream=None):
     """dX_i = dY_i W_i, dW_i = dY_i^T X for the group of f8_linear_fwd_group
     (f8_linear_bwd_group); returns (dxs, dws) (lists, or None if not wanted)."""
+    _need("f8_linear_bwd_group", torch.bfloat16, *dys)
     M = dys[0].shape[0]
     Ns = [dy.shape[1] for dy in dys]
     dev = dys[0].device
@@ -489,6 +502,7 @@ def f8_linear_bwd_group(dys: list, saved: list, K: int, dxs: list | None = None,
 def f8_linear_fwd(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | None = None,
                   saved: LinearSaved | None = None, ws: torch.Tensor | None = None, stream=None):
     """Y = X W^T through the Float8 path; returns (Y, saved)."""
+    _need("f8_linear_fwd", torch.bfloat16, x, w)
     M, K = x.shape
     N, K2 = w.shape
     if K != K2:
@@ -510,6 +524,7 @@ def f8_linear_fwd_noalloc(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | No
                           saved: LinearSaved | None = None, stream=None):
     """f8_linear_fwd without a workspace argument: the C entry point uses a
     static device array instead, for callers that cannot allocate device memory."""
+    _need("f8_linear_fwd_noalloc", torch.bfloat16, x, w)
     M, K = x.shape
     N, K2 = w.shape
     if K != K2:
@@ -550,6 +565,7 @@ def f8_linear_fwd_swiglu(a: torch.Tensor, b: torch.Tensor, w: torch.Tensor,
                          y: torch.Tensor | None = None, saved: LinearSaved | None = None,
                          ws: torch.Tensor | None = None, h: torch.Tensor | None = None, stream=None):
     """Y = h W^T with h = silu(a) * b produced with its amax; returns (Y, saved)."""
+    _need("f8_linear_fwd_swiglu", torch.bfloat16, a, b, w)
     M, K = a.shape
     N, K2 = w.shape
     if K != K2 or a.shape != b.shape:
@@ -594,6 +610,7 @@ def f8_linear_fwd_w13_swiglu(x: torch.Tensor, w13: torch.Tensor, ab: torch.Tenso
                              stream=None):
     """AB = X W13^T (Float8 linear), h = silu(a) * b and its E4M3 copies from
     the GEMM epilogue; returns (ab, h, saved, h_q, h_t, scale_h, amax_h)."""
+    _need("f8_linear_fwd_w13_swiglu", torch.bfloat16, x, w13)
     M, K = x.shape
     N, K2 = w13.shape
     if K != K2 or N % 256:
@@ -623,6 +640,7 @@ def f8_linear_bwd_w13_swiglu(dh: torch.Tensor, ab: torch.Tensor, saved: LinearSa
                              stream=None):
     """d(AB) from dh and the forward's AB (quantised in format dy_fmt), then
     dX, dW13 of the w1+w3 group; returns (dx, dw, dab)."""
+    _need("f8_linear_bwd_w13_swiglu", torch.bfloat16, dh, ab)
     M, F = dh.shape
     K = saved.x_t.shape[0]
     if ab.shape != (M, 2 * F):
@@ -646,6 +664,7 @@ def f8_quantize_swiglu_bwd(dh: torch.Tensor, ab: torch.Tensor, dab: torch.Tensor
                            fmt: int = F8_E4M3, stream=None):
     """d(AB) from dh and the forward's AB with its amax, then its cast to
     format fmt: returns (q, q_t, scale, amax, dab)."""
+    _need("f8_quantize_swiglu_bwd", torch.bfloat16, dh, ab)
     M, F = dh.shape
     if ab.shape != (M, 2 * F):
         raise ValueError("ab must be [M, 2F] for dh [M, F]")
@@ -670,6 +689,7 @@ def f8_gemm_w13_swiglu(x_q: torch.Tensor, w13_q: torch.Tensor, scale_x: torch.Te
                        stream=None):
     """AB = q(X) q(W13)^T / (s_x s_w13) and h = silu(a) * b with max |h|;
     returns (ab, h, amax_h)."""
+    _need("f8_gemm_w13_swiglu", torch.uint8, x_q, w13_q)
     M, K = x_q.shape
     N, K2 = w13_q.shape
     if K != K2 or N % 256:
@@ -690,6 +710,7 @@ def f8_linear_bwd(dy: torch.Tensor, saved: LinearSaved, K: int | None = None,
                   dy_fmt: int = F8_E4M3, stream=None):
     """(dX, dW) of the linear whose forward produced ``saved``; ``dy_fmt``
     E5M2 routes through f8_linear_bwd_fmt."""
+    _need("f8_linear_bwd", torch.bfloat16, dy)
     M, N = dy.shape
     K = saved.x_t.shape[0]
     dev = dy.device
@@ -730,6 +751,8 @@ def f8_linear_fwd_qw(x: torch.Tensor, w_q: torch.Tensor, saved: LinearSaved,
     """Y = X W^T for a weight that arrives quantised (w_q [N, K] uint8, with
     saved.w_t = q(W)^T and saved's amax_w / scale_w set by the caller);
     writes saved's X part; returns Y."""
+    _need("f8_linear_fwd_qw", torch.bfloat16, x)
+    _need("f8_linear_fwd_qw", torch.uint8, w_q)
     M, K = x.shape
     N, K2 = w_q.shape
     if K != K2:

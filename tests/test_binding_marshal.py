@@ -89,3 +89,40 @@ def test_every_wrapper_marshals(rec):
                       "f8_quantize_multi_workspace_bytes",
                       "f8_linear_fwd_qw_workspace_bytes"} <= called, \
         sorted(wrapped - called)
+
+
+def test_wrappers_reject_wrong_dtypes(rec):
+    """Every wrapper that hands a tensor's bytes to the C ABI refuses a
+    tensor of the wrong type or rank before any C call (the kernels would
+    read fp32 or fp8 bytes as bf16, or the reverse)."""
+    M, N, K, F = 32, 48, 64, 128
+    f32 = torch.zeros((M, K), dtype=torch.float32)
+    x, w, dy = _bf(M, K), _bf(N, K), _bf(M, N)
+    q, qb = torch.zeros((M, K), dtype=torch.uint8), torch.zeros((N, K), dtype=torch.uint8)
+    saved = binding.LinearSaved(torch.zeros((K, M), dtype=torch.uint8),
+                                torch.zeros((K, N), dtype=torch.uint8), torch.zeros(4))
+    one = torch.ones(1)
+    bad = [
+        lambda: binding.f8_linear_fwd(f32, w),
+        lambda: binding.f8_linear_fwd(x, w.float()),
+        lambda: binding.f8_linear_fwd(x.reshape(-1), w),
+        lambda: binding.f8_linear_fwd_noalloc(f32, w),
+        lambda: binding.f8_linear_bwd(dy.float(), saved),
+        lambda: binding.f8_gemm(x, qb, one, one),
+        lambda: binding.f8_gemm(q, w, one, one),
+        lambda: binding.f8_gemm_grouped([(q, qb.float(), one, one)]),
+        lambda: binding.f8_linear_fwd_group(f32, [w]),
+        lambda: binding.f8_linear_fwd_group(x, [w, w.float()]),
+        lambda: binding.f8_linear_bwd_group([dy.float()], [saved], K),
+        lambda: binding.f8_linear_fwd_qw(f32, qb, saved),
+        lambda: binding.f8_linear_fwd_qw(x, w, saved),
+        lambda: binding.f8_linear_fwd_swiglu(_bf(M, F), _bf(M, F).float(), _bf(N, F)),
+        lambda: binding.f8_linear_fwd_w13_swiglu(f32, _bf(2 * F, K)),
+        lambda: binding.f8_linear_bwd_w13_swiglu(_bf(M, F).float(), _bf(M, 2 * F), saved),
+        lambda: binding.f8_quantize_swiglu_bwd(_bf(M, F), _bf(M, 2 * F).float()),
+        lambda: binding.f8_gemm_w13_swiglu(x, torch.zeros((2 * F, K), dtype=torch.uint8), one, one),
+    ]
+    for i, call in enumerate(bad):
+        with pytest.raises(TypeError):
+            call()
+        assert rec.calls == [], (i, rec.calls)
