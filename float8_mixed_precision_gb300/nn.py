@@ -1,0 +1,124 @@
+"""PyTorch modules over libf8: a Float8 linear layer for training.
+
+The atlas.scime.ai summary of the TorchTitan paper (Approach) treats Float8
+as a per-linear transformation composed onto a model, and its ablation
+table measures it on Llama 3.1 8B.  This module is that transformation for
+modules whose linears have no bias (as in Llama):
+
+- Float8Linear: Y = X W^T with the forward and backward of a Float8 linear
+  (f8_linear_fwd, f8_linear_bwd): dynamic tensorwise E4M3 scaling of X, W
+  and dY, three FP8 GEMMs, bf16 outputs.  Autograd gets dX and dW from
+  libf8; nothing of the layer's arithmetic runs in torch.
+- to_float8_linears: swaps eligible nn.Linear modules of a model for
+  Float8Linear modules that share their weight Parameter.
+
+Inputs and weights must be bf16 CUDA tensors with every size a multiple of
+16 (the ABI's rule); anything else raises, there is no fallback path.
+"""
+from __future__ import annotations
+
+from typing import Callable
+
+import torch
+
+from . import binding
+
+
+class _Float8LinearFn(torch.autograd.Function):
+    """One Float8 linear: forward saves q(X)^T, q(W)^T and their scalars
+    (f8_linear_fwd); backward quantises dY and runs the dgrad and wgrad
+    GEMMs (f8_linear_bwd)."""
+
+    @staticmethod
+    def forward(ctx, x: torch.Tensor, weight: torch.Tensor) -> torch.Tensor:
+        lead = x.shape[:-1]
+        x2 = x.reshape(-1, x.shape[-1]).contiguous()
+        y, saved = binding.f8_linear_fwd(x2, weight.contiguous())
+        ctx.f8_saved = saved
+        ctx.x_shape = x.shape
+        ctx.needs = (ctx.needs_input_grad[0], ctx.needs_input_grad[1])
+        return y.reshape(*lead, weight.shape[0])
+
+    @staticmethod
+    def backward(ctx, dy: torch.Tensor):
+        want_dx, want_dw = ctx.needs
+        if not (want_dx or want_dw):
+            return None, None
+        dy2 = dy.reshape(-1, dy.shape[-1]).contiguous()
+        dx, dw = binding.f8_linear_bwd(dy2, ctx.f8_saved, want_dx=want_dx, want_dw=want_dw)
+        ctx.f8_saved = None
+        return (dx.reshape(ctx.x_shape) if want_dx else None), (dw if want_dw else None)
+
+
+def _check_sizes(in_features: int, out_features: int) -> None:
+    if in_features % 16 or out_features % 16:
+        raise ValueError("Float8Linear needs in_features and out_features that are multiples of 16")
+
+
+class Float8Linear(torch.nn.Module):
+    """A bias-free linear layer, y = x W^T, computed by the Float8 path.
+
+    `weight` is [out_features, in_features] bf16, as in nn.Linear.  The
+    input's last dimension is in_features; its other dimensions are
+    flattened into the GEMM's M, which must be a multiple of 16."""
+
+    def __init__(self, in_features: int, out_features: int, device=None,
+                 weight: torch.nn.Parameter | None = None):
+        super().__init__()
+        _check_sizes(in_features, out_features)
+        self.in_features = in_features
+        self.out_features = out_features
+        if weight is None:
+            weight = torch.nn.Parameter(torch.empty((out_features, in_features),
+                                                    dtype=torch.bfloat16, device=device))
+            torch.nn.init.normal_(weight, std=0.02)
+        if tuple(weight.shape) != (out_features, in_features) or weight.dtype != torch.bfloat16:
+            raise TypeError("Float8Linear's weight is a bf16 [out_features, in_features] tensor")
+        self.weight = weight
+
+    @classmethod
+    def from_linear(cls, linear: torch.nn.Linear) -> "Float8Linear":
+        """The Float8 counterpart of `linear`, sharing its weight Parameter."""
+        if linear.bias is not None:
+            raise ValueError("Float8Linear has no bias")
+        return cls(linear.in_features, linear.out_features, weight=linear.weight)
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        if x.dtype != torch.bfloat16:
+            raise TypeError("Float8Linear takes bf16 inputs")
+        if x.shape[-1] != self.in_features:
+            raise ValueError("the input's last dimension is not in_features")
+        if (x.numel() // self.in_features) % 16:
+            raise ValueError("Float8Linear needs a token count (the input's leading dimensions) "
+                             "that is a multiple of 16")
+        return _Float8LinearFn.apply(x, self.weight)
+
+    def extra_repr(self) -> str:
+        return f"in_features={self.in_features}, out_features={self.out_features}, float8=e4m3"
+
+
+def eligible(linear: torch.nn.Module) -> bool:
+    """An nn.Linear Float8Linear can stand in for: no bias, a bf16 weight,
+    both sizes multiples of 16."""
+    return (isinstance(linear, torch.nn.Linear) and linear.bias is None
+            and linear.weight.dtype == torch.bfloat16
+            and linear.in_features % 16 == 0 and linear.out_features % 16 == 0)
+
+
+def to_float8_linears(module: torch.nn.Module,
+                      keep: Callable[[str, torch.nn.Module], bool] | None = None) -> torch.nn.Module:
+    """Replaces, in place, every eligible nn.Linear below `module` for which
+    `keep(qualified_name, linear)` is true (all of them when `keep` is None)
+    with a Float8Linear sharing its weight Parameter; returns `module`."""
+    def visit(parent: torch.nn.Module, prefix: str) -> None:
+        for name, child in list(parent.named_children()):
+            qual = f"{prefix}.{name}" if prefix else name
+            if eligible(child) and (keep is None or keep(qual, child)):
+                setattr(parent, name, Float8Linear.from_linear(child))
+            else:
+                visit(child, qual)
+
+    if eligible(module) and (keep is None or keep("", module)):
+        raise ValueError("the module itself is a linear: use Float8Linear.from_linear")
+    visit(module, "")
+    return module

@@ -1,0 +1,106 @@
+"""float8_mixed_precision_gb300.nn on the GPU: Float8Linear under autograd
+gives exactly the outputs and gradients of the C-ABI calls it wraps, and a
+model converted by to_float8_linears trains through libf8.
+
+- One layer, input [2, 256, 512] -> 768: Y, dX and dW bit-identical to
+  f8_linear_fwd / f8_linear_bwd on the flattened tensors, and Y within the
+  GEMM bar of the oracle's linear.
+- A two-linear SwiGLU-free MLP (x -> w1 -> silu -> w2) after conversion:
+  the loss's gradients bit-identical to the same chain composed by hand
+  from the C-ABI calls and torch's silu backward, with libf8 launching the
+  backward's kernels (its launch counter grows during backward, which
+  autograd runs on its own device thread).
+- A layer whose input needs no gradient gets dW only (no dX GEMM).
+"""
+import pytest
+import torch
+
+import oracle
+from float8_mixed_precision_gb300 import workloads as wl
+from tolerance import check_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def f8():
+    import float8_mixed_precision_gb300 as m
+    from float8_mixed_precision_gb300 import build
+    build.build()
+    oracle.build()
+    m.lib()
+    return m
+
+
+def _eq(a, b):
+    return torch.equal(a.contiguous().view(torch.int16), b.contiguous().view(torch.int16))
+
+
+def test_layer_matches_the_abi_calls(f8):
+    from float8_mixed_precision_gb300 import nn as f8nn
+    B, T, K, N = 2, 256, 512, 768
+    d = wl.custom_linear(B * T, K, N, seed=81, dy_std=0.1)
+    x = d["x"].to(DEV).reshape(B, T, K).requires_grad_(True)
+    layer = f8nn.Float8Linear(K, N, weight=torch.nn.Parameter(d["w"].to(DEV)))
+    g = d["dy"].to(DEV).reshape(B, T, N)
+    y = layer(x)
+    y.backward(g)
+    assert f8.f8_last_device_status() == 0
+    y_ref, saved = f8.f8_linear_fwd(d["x"].to(DEV), d["w"].to(DEV))
+    dx_ref, dw_ref = f8.f8_linear_bwd(d["dy"].to(DEV), saved)
+    assert y.shape == (B, T, N) and x.grad.shape == (B, T, K)
+    assert _eq(y.reshape(-1, N), y_ref)
+    assert _eq(x.grad.reshape(-1, K), dx_ref)
+    assert _eq(layer.weight.grad, dw_ref)
+    fwd = oracle.linear_fwd(wl.bits(d["x"]), wl.bits(d["w"]))
+    check_close(y.reshape(-1, N), fwd["y"], what="Float8Linear Y")
+
+
+def test_converted_mlp_gradients(f8):
+    from float8_mixed_precision_gb300 import nn as f8nn
+    M, D, H = 512, 256, 768
+    torch.manual_seed(0)
+    model = torch.nn.Sequential(
+        torch.nn.Linear(D, H, bias=False, dtype=torch.bfloat16, device=DEV),
+        torch.nn.SiLU(),
+        torch.nn.Linear(H, D, bias=False, dtype=torch.bfloat16, device=DEV))
+    with torch.no_grad():
+        for lin in (model[0], model[2]):
+            lin.weight.normal_(0.0, 0.02)
+    w1, w2 = model[0].weight.detach().clone(), model[2].weight.detach().clone()
+    f8nn.to_float8_linears(model)
+    assert isinstance(model[0], f8nn.Float8Linear) and isinstance(model[2], f8nn.Float8Linear)
+    x = wl.normal((M, D), 1.0, 82).to(DEV).requires_grad_(True)
+    g = wl.normal((M, D), 0.05, 83).to(DEV)
+    torch.cuda.synchronize()
+    y = model(x)
+    n0 = f8.f8_kernel_launches()
+    (y * g).sum().backward()
+    torch.cuda.synchronize()
+    assert f8.f8_kernel_launches() > n0
+    assert f8.f8_last_device_status() == 0
+    # the same chain from the C-ABI calls
+    a1, s1 = f8.f8_linear_fwd(x.detach(), w1)
+    a1r = a1.clone().requires_grad_(True)
+    h = torch.nn.functional.silu(a1r)
+    y2, s2 = f8.f8_linear_fwd(h.detach(), w2)
+    assert _eq(y, y2)
+    dy2 = (g * torch.ones_like(y2)).to(torch.bfloat16)
+    dh, dw2 = f8.f8_linear_bwd(dy2, s2)
+    (da1,) = torch.autograd.grad(h, a1r, dh)
+    dx, dw1 = f8.f8_linear_bwd(da1, s1)
+    assert _eq(model[2].weight.grad, dw2)
+    assert _eq(model[0].weight.grad, dw1)
+    assert _eq(x.grad, dx)
+
+
+def test_frozen_input_gets_weight_gradient_only(f8):
+    from float8_mixed_precision_gb300 import nn as f8nn
+    M, K, N = 256, 256, 512
+    layer = f8nn.Float8Linear(K, N, device=DEV)
+    x = wl.normal((M, K), 1.0, 84).to(DEV)               # requires no gradient
+    y = layer(x)
+    y.backward(wl.normal((M, N), 0.1, 85).to(DEV))
+    assert f8.f8_last_device_status() == 0
+    assert layer.weight.grad is not None and x.grad is None

@@ -1,0 +1,67 @@
+"""float8_mixed_precision_gb300.nn without a GPU: which linears
+to_float8_linears swaps, that the swapped modules share the original weight
+Parameters, and that Float8Linear refuses what the ABI cannot take (wrong
+dtype, sizes that are not multiples of 16, host tensors) instead of
+computing anything in torch."""
+import pytest
+import torch
+
+from float8_mixed_precision_gb300 import nn as f8nn
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from float8_mixed_precision_gb300 import build
+    build.build()
+
+
+def _lin(i, o, bias=False, dtype=torch.bfloat16):
+    return torch.nn.Linear(i, o, bias=bias, dtype=dtype)
+
+
+def _model():
+    return torch.nn.ModuleDict({
+        "attn": torch.nn.ModuleDict({"wq": _lin(64, 64), "wk": _lin(64, 16), "wo": _lin(64, 64)}),
+        "ffn": torch.nn.Sequential(_lin(64, 128), torch.nn.SiLU(), _lin(128, 64)),
+        "head": _lin(64, 100),                 # 100 is not a multiple of 16
+        "proj": _lin(64, 64, bias=True),       # a bias
+        "fp32": _lin(64, 64, dtype=torch.float32),
+    })
+
+
+def test_swaps_eligible_linears_sharing_weights():
+    m = _model()
+    before = {n: mod.weight for n, mod in m.named_modules() if isinstance(mod, torch.nn.Linear)}
+    f8nn.to_float8_linears(m)
+    swapped = {n for n, mod in m.named_modules() if isinstance(mod, f8nn.Float8Linear)}
+    assert swapped == {"attn.wq", "attn.wk", "attn.wo", "ffn.0", "ffn.2"}
+    for n in swapped:
+        assert m.get_submodule(n).weight is before[n]
+    for n in ("head", "proj", "fp32"):
+        assert type(m.get_submodule(n)) is torch.nn.Linear
+    assert sum(1 for _ in m.parameters()) == sum(1 for _ in _model().parameters())
+
+
+def test_keep_filter():
+    m = _model()
+    f8nn.to_float8_linears(m, keep=lambda name, lin: name.startswith("ffn"))
+    assert isinstance(m["ffn"][0], f8nn.Float8Linear) and isinstance(m["ffn"][2], f8nn.Float8Linear)
+    assert type(m["attn"]["wq"]) is torch.nn.Linear
+
+
+def test_refusals():
+    with pytest.raises(ValueError):
+        f8nn.Float8Linear(64, 100)
+    with pytest.raises(ValueError):
+        f8nn.Float8Linear.from_linear(_lin(64, 64, bias=True))
+    with pytest.raises(ValueError):
+        f8nn.to_float8_linears(_lin(64, 64))
+    layer = f8nn.Float8Linear(64, 64)
+    with pytest.raises(TypeError):
+        layer(torch.zeros((16, 64), dtype=torch.float32))
+    with pytest.raises(ValueError):
+        layer(torch.zeros((15, 64), dtype=torch.bfloat16))       # 15 tokens
+    with pytest.raises(ValueError):
+        layer(torch.zeros((16, 48), dtype=torch.bfloat16))       # wrong in_features
+    with pytest.raises(ValueError, match="device tensors"):
+        layer(torch.zeros((2, 8, 64), dtype=torch.bfloat16))     # host tensors: no CPU path
