@@ -11,6 +11,8 @@ model converted by to_float8_linears trains through libf8.
   backward's kernels (its launch counter grows during backward, which
   autograd runs on its own device thread).
 - A layer whose input needs no gradient gets dW only (no dX GEMM).
+- A converted model's training step captured in a CUDA graph and replayed
+  gives the eager step's output and gradients.
 """
 import pytest
 import torch
@@ -104,3 +106,51 @@ def test_frozen_input_gets_weight_gradient_only(f8):
     y.backward(wl.normal((M, N), 0.1, 85).to(DEV))
     assert f8.f8_last_device_status() == 0
     assert layer.weight.grad is not None and x.grad is None
+
+
+def test_training_step_in_a_cuda_graph(f8):
+    """A converted model's forward and backward captured once in a CUDA
+    graph (torch.cuda.graph, static input and gradient buffers) and
+    replayed: the output and the weight gradients of a replay equal an eager
+    step's bit for bit."""
+    from float8_mixed_precision_gb300 import nn as f8nn
+    M, D, H = 256, 256, 512
+    model = torch.nn.Sequential(
+        torch.nn.Linear(D, H, bias=False, dtype=torch.bfloat16, device=DEV),
+        torch.nn.SiLU(),
+        torch.nn.Linear(H, D, bias=False, dtype=torch.bfloat16, device=DEV))
+    with torch.no_grad():
+        for lin in (model[0], model[2]):
+            lin.weight.normal_(0.0, 0.02)
+    f8nn.to_float8_linears(model)
+    x = wl.normal((M, D), 1.0, 86).to(DEV)
+    g = wl.normal((M, D), 0.05, 87).to(DEV)
+
+    def step():
+        for p in model.parameters():
+            p.grad = None
+        y = model(x)
+        y.backward(g)
+        return y
+
+    y_eager = step().detach().clone()
+    grads_eager = [p.grad.clone() for p in model.parameters()]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):                 # warm-up on the capture stream
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    for p in model.parameters():
+        p.grad = None
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        y_static = model(x)
+        y_static.backward(g)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert f8.f8_last_device_status() == 0
+    assert _eq(y_static, y_eager)
+    for p, ge in zip(model.parameters(), grads_eager):
+        assert _eq(p.grad, ge)
