@@ -9,6 +9,9 @@ modules whose linears have no bias (as in Llama):
   (f8_linear_fwd, f8_linear_bwd): dynamic tensorwise E4M3 scaling of X, W
   and dY, three FP8 GEMMs, bf16 outputs.  Autograd gets dX and dW from
   libf8; nothing of the layer's arithmetic runs in torch.
+- Float8LinearGroup: linears that read one input (q, k, v; w1, w3), each
+  its own Float8 linear, with X quantised once and shared GEMM launches
+  (f8_linear_fwd_group, f8_linear_bwd_group).
 - to_float8_linears: swaps eligible nn.Linear modules of a model for
   Float8Linear modules that share their weight Parameter.
 
@@ -48,6 +51,40 @@ class _Float8LinearFn(torch.autograd.Function):
         dx, dw = binding.f8_linear_bwd(dy2, ctx.f8_saved, want_dx=want_dx, want_dw=want_dw)
         ctx.f8_saved = None
         return (dx.reshape(ctx.x_shape) if want_dx else None), (dw if want_dw else None)
+
+
+class _Float8GroupFn(torch.autograd.Function):
+    """Linears that read one input: X quantised once, each W_i and dY_i with
+    its own scale (f8_linear_fwd_group, f8_linear_bwd_group); dX is the sum
+    of the members' dX_i, as autograd would form it for separate layers."""
+
+    @staticmethod
+    def forward(ctx, x: torch.Tensor, *weights: torch.Tensor):
+        lead = x.shape[:-1]
+        x2 = x.reshape(-1, x.shape[-1]).contiguous()
+        ys, saved = binding.f8_linear_fwd_group(x2, [w.contiguous() for w in weights])
+        ctx.f8_saved = saved
+        ctx.x_shape = x.shape
+        ctx.needs = tuple(ctx.needs_input_grad)
+        return tuple(y.reshape(*lead, y.shape[-1]) for y in ys)
+
+    @staticmethod
+    def backward(ctx, *dys: torch.Tensor):
+        want_dx, want_dw = ctx.needs[0], any(ctx.needs[1:])
+        if not (want_dx or want_dw):
+            return (None,) * len(ctx.needs)
+        dys2 = [dy.reshape(-1, dy.shape[-1]).contiguous() for dy in dys]
+        dxs, dws = binding.f8_linear_bwd_group(dys2, ctx.f8_saved, ctx.x_shape[-1],
+                                               want_dx=want_dx, want_dw=want_dw)
+        ctx.f8_saved = None
+        dx = None
+        if want_dx:
+            dx = dxs[0]
+            for d in dxs[1:]:
+                dx = dx + d
+            dx = dx.reshape(ctx.x_shape)
+        dws = dws if want_dw else [None] * (len(ctx.needs) - 1)
+        return (dx, *[dw if need else None for dw, need in zip(dws, ctx.needs[1:])])
 
 
 def _check_sizes(in_features: int, out_features: int) -> None:
@@ -92,6 +129,60 @@ class Float8Linear(torch.nn.Module):
             raise ValueError("Float8Linear needs a token count (the input's leading dimensions) "
                              "that is a multiple of 16")
         return _Float8LinearFn.apply(x, self.weight)
+
+    def extra_repr(self) -> str:
+        return f"in_features={self.in_features}, out_features={self.out_features}, float8=e4m3"
+
+
+class Float8LinearGroup(torch.nn.Module):
+    """Bias-free linears that read the same input, such as the q, k and v
+    projections of attention or w1 and w3 of a SwiGLU FFN: forward returns
+    one output per member.  Each member stays a Float8 linear with its own
+    weight and gradient scales; X is quantised once, and the members' GEMMs
+    share launches where the tile schedule gains.  Outputs and weight
+    gradients equal separate Float8Linear layers' bit for bit; dX is the sum
+    of the members' dX in member order.  At most four members."""
+
+    def __init__(self, in_features: int, out_features: list[int], device=None,
+                 weights: list[torch.nn.Parameter] | None = None):
+        super().__init__()
+        if not 1 <= len(out_features) <= binding.F8_MAX_GROUP_LINEARS:
+            raise ValueError(f"a group has 1 to {binding.F8_MAX_GROUP_LINEARS} members")
+        for n in out_features:
+            _check_sizes(in_features, n)
+        self.in_features = in_features
+        self.out_features = list(out_features)
+        if weights is None:
+            weights = []
+            for n in out_features:
+                w = torch.nn.Parameter(torch.empty((n, in_features), dtype=torch.bfloat16,
+                                                   device=device))
+                torch.nn.init.normal_(w, std=0.02)
+                weights.append(w)
+        for w, n in zip(weights, out_features):
+            if tuple(w.shape) != (n, in_features) or w.dtype != torch.bfloat16:
+                raise TypeError("each weight is a bf16 [out_features, in_features] tensor")
+        self.weights = torch.nn.ParameterList(weights)
+
+    @classmethod
+    def from_linears(cls, linears: list[torch.nn.Linear]) -> "Float8LinearGroup":
+        """The group of `linears` (same in_features, no bias), sharing their
+        weight Parameters."""
+        if any(l.bias is not None for l in linears):
+            raise ValueError("Float8LinearGroup has no bias")
+        if len({l.in_features for l in linears}) != 1:
+            raise ValueError("the members of a group read the same input")
+        return cls(linears[0].in_features, [l.out_features for l in linears],
+                   weights=[l.weight for l in linears])
+
+    def forward(self, x: torch.Tensor) -> tuple[torch.Tensor, ...]:
+        if x.dtype != torch.bfloat16:
+            raise TypeError("Float8LinearGroup takes bf16 inputs")
+        if x.shape[-1] != self.in_features:
+            raise ValueError("the input's last dimension is not in_features")
+        if (x.numel() // self.in_features) % 16:
+            raise ValueError("Float8LinearGroup needs a token count that is a multiple of 16")
+        return _Float8GroupFn.apply(x, *self.weights)
 
     def extra_repr(self) -> str:
         return f"in_features={self.in_features}, out_features={self.out_features}, float8=e4m3"

@@ -154,3 +154,29 @@ def test_training_step_in_a_cuda_graph(f8):
     assert _eq(y_static, y_eager)
     for p, ge in zip(model.parameters(), grads_eager):
         assert _eq(p.grad, ge)
+
+
+def test_group_matches_separate_layers(f8):
+    """Float8LinearGroup over q, k, v-like members (512 -> 512, 128, 128),
+    input [2, 128, 512]: each output and weight gradient bit-identical to
+    f8_linear_fwd / f8_linear_bwd of that member, dX the member-order sum of
+    the members' dX; a member whose output is unused gets a zero dY."""
+    from float8_mixed_precision_gb300 import nn as f8nn
+    B, T, K, Ns = 2, 128, 512, [512, 128, 128]
+    x0 = wl.normal((B * T, K), 1.0, 91).to(DEV)
+    ws = [wl.normal((n, K), 0.02, 92 + i).to(DEV) for i, n in enumerate(Ns)]
+    gs = [wl.normal((B * T, n), 0.1, 96 + i).to(DEV) for i, n in enumerate(Ns)]
+    group = f8nn.Float8LinearGroup(K, Ns, weights=[torch.nn.Parameter(w.clone()) for w in ws])
+    x = x0.reshape(B, T, K).clone().requires_grad_(True)
+    ys = group(x)
+    torch.autograd.backward([ys[0], ys[1]], [gs[0].reshape(B, T, -1), gs[1].reshape(B, T, -1)])
+    assert f8.f8_last_device_status() == 0
+    dx_sum = None
+    for i, (w, y) in enumerate(zip(ws, ys)):
+        y_ref, saved = f8.f8_linear_fwd(x0, w)
+        assert _eq(y.reshape(-1, Ns[i]), y_ref), i
+        dy = gs[i] if i < 2 else torch.zeros_like(gs[i])
+        dx_i, dw_i = f8.f8_linear_bwd(dy, saved)
+        assert _eq(group.weights[i].grad, dw_i), i
+        dx_sum = dx_i if dx_sum is None else dx_sum + dx_i
+    assert _eq(x.grad.reshape(-1, K), dx_sum)

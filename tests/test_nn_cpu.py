@@ -65,3 +65,20 @@ def test_refusals():
         layer(torch.zeros((16, 48), dtype=torch.bfloat16))       # wrong in_features
     with pytest.raises(ValueError, match="device tensors"):
         layer(torch.zeros((2, 8, 64), dtype=torch.bfloat16))     # host tensors: no CPU path
+
+
+def test_group_construction_and_refusals():
+    lins = [_lin(64, 64), _lin(64, 16), _lin(64, 16)]
+    g = f8nn.Float8LinearGroup.from_linears(lins)
+    assert g.out_features == [64, 16, 16]
+    assert all(w is l.weight for w, l in zip(g.weights, lins))
+    with pytest.raises(ValueError):
+        f8nn.Float8LinearGroup.from_linears([_lin(64, 64), _lin(32, 64)])
+    with pytest.raises(ValueError):
+        f8nn.Float8LinearGroup.from_linears([_lin(64, 64, bias=True)])
+    with pytest.raises(ValueError):
+        f8nn.Float8LinearGroup(64, [16] * 5)
+    with pytest.raises(TypeError):
+        g(torch.zeros((16, 64), dtype=torch.float32))
+    with pytest.raises(ValueError, match="device tensors"):
+        g(torch.zeros((16, 64), dtype=torch.bfloat16))
