@@ -12,6 +12,8 @@ modules whose linears have no bias (as in Llama):
 - Float8LinearGroup: linears that read one input (q, k, v; w1, w3), each
   its own Float8 linear, with X quantised once and shared GEMM launches
   (f8_linear_fwd_group, f8_linear_bwd_group).
+- Float8SwiGLU: the Llama FFN with the w1+w3 GEMM's epilogue forming h
+  and its amax, and the SwiGLU backward forming d(AB) with its amax.
 - to_float8_linears: swaps eligible nn.Linear modules of a model for
   Float8Linear modules that share their weight Parameter.
 
@@ -186,6 +188,99 @@ class Float8LinearGroup(torch.nn.Module):
 
     def extra_repr(self) -> str:
         return f"in_features={self.in_features}, out_features={self.out_features}, float8=e4m3"
+
+
+def interleave_w13(w1: torch.Tensor, w3: torch.Tensor) -> torch.Tensor:
+    """W13 [2F, D] from W1 and W3 [F, D]: blocks of 128 rows taken from W1
+    and W3 alternately, the layout whose 256-column output tiles hold 128
+    columns of a = X W1^T next to the matching 128 of b = X W3^T."""
+    if w1.shape != w3.shape or w1.shape[0] % 128:
+        raise ValueError("W1 and W3 are [F, D] with F a multiple of 128")
+    F, D = w1.shape
+    return torch.stack([w1.reshape(F // 128, 128, D), w3.reshape(F // 128, 128, D)],
+                       dim=1).reshape(2 * F, D)
+
+
+class _Float8SwiGLUFn(torch.autograd.Function):
+    """y = W2 h with h = silu(X W1^T) * (X W3^T), the Llama FFN:
+    forward f8_linear_fwd_w13_swiglu (the w1+w3 group as one Float8 linear
+    whose GEMM epilogue writes a, b, h and max|h|, then the cast of h), W2's
+    quantisation and the w2 GEMM on q(h); backward f8_linear_bwd (dh and dW2)
+    then f8_linear_bwd_w13_swiglu (d(AB) with its amax from dh, a and b,
+    then dX and dW13)."""
+
+    @staticmethod
+    def forward(ctx, x: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor) -> torch.Tensor:
+        lead, D = x.shape[:-1], x.shape[-1]
+        x2 = x.reshape(-1, D).contiguous()
+        M, F = x2.shape[0], w2.shape[1]
+        s2 = binding.LinearSaved.empty(M, D, F, x.device)   # w2: X part = h
+        ab, _, s13, h_q, _, _, _ = binding.f8_linear_fwd_w13_swiglu(
+            x2, w13.contiguous(), amax_h=s2.scalars[0:1], scale_h=s2.scalars[1:2], h_t=s2.x_t)
+        w2q, _, _, _ = binding.f8_quantize(w2.contiguous(), s2.scalars[2:3], s2.scalars[3:4],
+                                           q_t=s2.w_t)
+        y = binding.f8_gemm(h_q, w2q, s2.scalars[1:2], s2.scalars[3:4])
+        ctx.f8 = (ab, s13, s2)
+        ctx.x_shape = x.shape
+        return y.reshape(*lead, D)
+
+    @staticmethod
+    def backward(ctx, dy: torch.Tensor):
+        ab, s13, s2 = ctx.f8
+        ctx.f8 = None
+        dh, dw2 = binding.f8_linear_bwd(dy.reshape(-1, dy.shape[-1]).contiguous(), s2)
+        dx, dw13, _ = binding.f8_linear_bwd_w13_swiglu(dh, ab, s13)
+        return dx.reshape(ctx.x_shape), dw13, dw2
+
+
+class Float8SwiGLU(torch.nn.Module):
+    """The SwiGLU FFN of a Llama block, y = W2 (silu(W1 x) * (W3 x)), with
+    every GEMM a Float8 one and the SiLU, the product and the amax of h in
+    the epilogue of the w1+w3 GEMM (the amax-with-the-producer row).  The
+    w1+w3 group is one Float8 linear (one scale over W13); w2 is a Float8
+    linear of its own.  Its parameters are `w13` [2F, D], W1 and W3
+    interleaved by 128 rows (interleave_w13), and `w2` [D, F]; F a multiple
+    of 128, D of 16, and the token count of 16."""
+
+    def __init__(self, dim: int, hidden: int, device=None, w13: torch.nn.Parameter | None = None,
+                 w2: torch.nn.Parameter | None = None):
+        super().__init__()
+        if hidden % 128 or dim % 16:
+            raise ValueError("Float8SwiGLU needs hidden % 128 == 0 and dim % 16 == 0")
+        self.dim, self.hidden = dim, hidden
+        if w13 is None:
+            w13 = torch.nn.Parameter(torch.empty((2 * hidden, dim), dtype=torch.bfloat16,
+                                                 device=device))
+            torch.nn.init.normal_(w13, std=0.02)
+        if w2 is None:
+            w2 = torch.nn.Parameter(torch.empty((dim, hidden), dtype=torch.bfloat16, device=device))
+            torch.nn.init.normal_(w2, std=0.02)
+        if tuple(w13.shape) != (2 * hidden, dim) or tuple(w2.shape) != (dim, hidden) or \
+                w13.dtype != torch.bfloat16 or w2.dtype != torch.bfloat16:
+            raise TypeError("w13 is bf16 [2 hidden, dim] and w2 bf16 [dim, hidden]")
+        self.w13, self.w2 = w13, w2
+
+    @classmethod
+    def from_linears(cls, w1: torch.nn.Linear, w3: torch.nn.Linear,
+                     w2: torch.nn.Linear) -> "Float8SwiGLU":
+        """From a model's three FFN linears: w2's weight Parameter is shared,
+        W13 is a new Parameter holding W1 and W3 interleaved."""
+        if any(l.bias is not None for l in (w1, w3, w2)):
+            raise ValueError("Float8SwiGLU has no biases")
+        w13 = torch.nn.Parameter(interleave_w13(w1.weight.detach(), w3.weight.detach()))
+        return cls(w1.in_features, w1.out_features, w13=w13, w2=w2.weight)
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        if x.dtype != torch.bfloat16:
+            raise TypeError("Float8SwiGLU takes bf16 inputs")
+        if x.shape[-1] != self.dim:
+            raise ValueError("the input's last dimension is not dim")
+        if (x.numel() // self.dim) % 16:
+            raise ValueError("Float8SwiGLU needs a token count that is a multiple of 16")
+        return _Float8SwiGLUFn.apply(x, self.w13, self.w2)
+
+    def extra_repr(self) -> str:
+        return f"dim={self.dim}, hidden={self.hidden}, float8=e4m3"
 
 
 def eligible(linear: torch.nn.Module) -> bool:

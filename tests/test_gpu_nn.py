@@ -180,3 +180,42 @@ def test_group_matches_separate_layers(f8):
         assert _eq(group.weights[i].grad, dw_i), i
         dx_sum = dx_i if dx_sum is None else dx_sum + dx_i
     assert _eq(x.grad.reshape(-1, K), dx_sum)
+
+
+def test_swiglu_module(f8):
+    """Float8SwiGLU (dim 512, hidden 1024, 2 x 128 tokens): output and the
+    gradients of X, W13 and W2 bit-identical to the same chain of C-ABI
+    calls (w1+w3 linear with the SwiGLU epilogue, W2 quantised, GEMM on
+    q(h); f8_linear_bwd, then f8_linear_bwd_w13_swiglu); and the output near
+    an fp32 evaluation of the FFN on the bf16 inputs (FP8 error, relative
+    Frobenius below 0.12)."""
+    from float8_mixed_precision_gb300 import nn as f8nn
+    B, T, D, F = 2, 128, 512, 1024
+    x0 = wl.normal((B * T, D), 1.0, 101).to(DEV)
+    w1 = wl.normal((F, D), 0.02, 102).to(DEV)
+    w3 = wl.normal((F, D), 0.02, 103).to(DEV)
+    w2 = wl.normal((D, F), 0.02, 104).to(DEV)
+    g = wl.normal((B * T, D), 0.1, 105).to(DEV)
+    w13 = f8nn.interleave_w13(w1, w3)
+    ffn = f8nn.Float8SwiGLU(D, F, w13=torch.nn.Parameter(w13.clone()),
+                            w2=torch.nn.Parameter(w2.clone()))
+    x = x0.reshape(B, T, D).clone().requires_grad_(True)
+    y = ffn(x)
+    y.backward(g.reshape(B, T, D))
+    assert f8.f8_last_device_status() == 0
+    # the chain by hand
+    s2 = f8.LinearSaved.empty(B * T, D, F, DEV)
+    ab, _, s13, h_q, _, _, _ = f8.f8_linear_fwd_w13_swiglu(
+        x0, w13, amax_h=s2.scalars[0:1], scale_h=s2.scalars[1:2], h_t=s2.x_t)
+    w2q, _, _, _ = f8.f8_quantize(w2, s2.scalars[2:3], s2.scalars[3:4], q_t=s2.w_t)
+    y_ref = f8.f8_gemm(h_q, w2q, s2.scalars[1:2], s2.scalars[3:4])
+    dh, dw2 = f8.f8_linear_bwd(g, s2)
+    dx, dw13, _ = f8.f8_linear_bwd_w13_swiglu(dh, ab, s13)
+    assert _eq(y.reshape(-1, D), y_ref)
+    assert _eq(x.grad.reshape(-1, D), dx)
+    assert _eq(ffn.w13.grad, dw13)
+    assert _eq(ffn.w2.grad, dw2)
+    ref = (torch.nn.functional.silu(x0.float() @ w1.float().t()) * (x0.float() @ w3.float().t())) \
+        @ w2.float().t()
+    rel = (y.reshape(-1, D).float() - ref).norm() / ref.norm()
+    assert rel < 0.12, rel

@@ -82,3 +82,28 @@ def test_group_construction_and_refusals():
         g(torch.zeros((16, 64), dtype=torch.float32))
     with pytest.raises(ValueError, match="device tensors"):
         g(torch.zeros((16, 64), dtype=torch.bfloat16))
+
+
+def test_interleave_w13_layout():
+    F, D = 256, 32
+    w1 = torch.arange(F * D, dtype=torch.float32).reshape(F, D)
+    w3 = -w1
+    w13 = f8nn.interleave_w13(w1, w3)
+    assert w13.shape == (2 * F, D)
+    for j in range(F // 128):
+        assert torch.equal(w13[256 * j:256 * j + 128], w1[128 * j:128 * j + 128])
+        assert torch.equal(w13[256 * j + 128:256 * j + 256], w3[128 * j:128 * j + 128])
+    with pytest.raises(ValueError):
+        f8nn.interleave_w13(w1[:100], w3[:100])
+
+
+def test_swiglu_module_construction():
+    w1, w3, w2 = _lin(64, 256), _lin(64, 256), _lin(256, 64)
+    ffn = f8nn.Float8SwiGLU.from_linears(w1, w3, w2)
+    assert ffn.w2 is w2.weight and ffn.w13.shape == (512, 64)
+    with pytest.raises(ValueError):
+        f8nn.Float8SwiGLU(64, 200)
+    with pytest.raises(TypeError):
+        ffn(torch.zeros((16, 64), dtype=torch.float32))
+    with pytest.raises(ValueError, match="device tensors"):
+        ffn(torch.zeros((16, 64), dtype=torch.bfloat16))
