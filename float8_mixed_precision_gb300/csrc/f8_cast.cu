@@ -934,11 +934,53 @@ transpose_u8_kernel(const uint8_t *__restrict__ in, int64_t rows, int64_t cols,
         __syncthreads();
     }
 }
+
+// The same transpose for rows and cols multiples of 128 and 16-byte aligned
+// buffers: 128 x 128 tiles, each row read as 16-byte chunks into the
+// swizzled shared tile of the TMA cast, then written by the cast's PRMT
+// transpose (transpose_out) as 16-byte column segments.
+__global__ void __launch_bounds__(kCastThreads)
+transpose_u8_tile_kernel(const uint8_t *__restrict__ in, int64_t rows, int64_t cols,
+                         uint8_t *__restrict__ out, unsigned *__restrict__ status)
+{
+    __shared__ __align__(16) uint8_t tile[kTile * kTile];
+    griddep_wait();
+    griddep_launch_dependents();
+    const int t = threadIdx.x;
+    const int64_t tiles_c = cols / kTile;
+    const int64_t ntiles = (rows / kTile) * tiles_c;
+    const int64_t n = rows * cols;
+    for (int64_t tix = blockIdx.x; tix < ntiles; tix += gridDim.x) {
+        const int64_t r0 = (tix / tiles_c) * kTile, c0 = (tix % tiles_c) * kTile;
+#pragma unroll
+        for (int p = 0; p < kTile * kTile / 16 / kCastThreads; ++p) {
+            const int idx = p * kCastThreads + t;
+            const int row = idx >> 3, ch = idx & 7;   // 8 threads read one 128-byte row
+            const int64_t o = (r0 + row) * cols + c0 + ch * 16;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (in_range(o, 16, n, status))
+                v = *reinterpret_cast<const uint4 *>(in + o);
+            *reinterpret_cast<uint4 *>(tile + row * kTile + ((ch ^ ((row >> 4) & 7)) * 16)) = v;
+        }
+        __syncthreads();
+        transpose_out(tile, out, rows, cols, r0, c0, t, status);
+        __syncthreads();  // the tile is free again
+    }
+}
 } // namespace
 
 cudaError_t launch_transpose_u8(const uint8_t *in, int64_t rows, int64_t cols, uint8_t *out,
                                 const DeviceInfo &dev, cudaStream_t stream)
 {
+    if (rows % kTile == 0 && cols % kTile == 0 && reinterpret_cast<uintptr_t>(in) % 16 == 0 &&
+        reinterpret_cast<uintptr_t>(out) % 16 == 0) {
+        int64_t blocks = (rows / kTile) * (cols / kTile);
+        const int64_t cap = static_cast<int64_t>(dev.sm_count) * 4;
+        if (blocks > cap)
+            blocks = cap;
+        return launch_pdl(transpose_u8_tile_kernel, dim3(static_cast<unsigned>(blocks)),
+                          dim3(kCastThreads), 0, stream, in, rows, cols, out, dev.status);
+    }
     const int64_t ntiles = ((rows + kTrTile - 1) / kTrTile) * ((cols + kTrTile - 1) / kTrTile);
     int64_t blocks = ntiles;
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * 8;

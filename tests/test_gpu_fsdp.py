@@ -31,12 +31,25 @@ def f8():
     return m
 
 
-@pytest.mark.parametrize("rows,cols", [(1, 1), (7, 300), (64, 64), (130, 257), (1024, 4096)])
+# full 128 x 128 tiles take the 16-byte tiled kernel; ragged shapes and
+# buffers off 16-byte alignment the byte kernel
+@pytest.mark.parametrize("rows,cols", [(1, 1), (7, 300), (64, 64), (130, 257), (128, 200),
+                                       (256, 384), (1024, 4096), (1792, 4096)])
 def test_transpose_u8(f8, rows, cols):
     x = torch.randint(0, 256, (rows, cols), dtype=torch.uint8, device=DEV)
     t = f8.f8_transpose_u8(x)
     assert f8.f8_last_device_status() == 0
     assert torch.equal(t, x.t().contiguous())
+
+
+def test_transpose_u8_unaligned_buffers(f8):
+    rows, cols = 256, 384
+    raw = torch.randint(0, 256, (rows * cols + 8,), dtype=torch.uint8, device=DEV)
+    x = raw[8:].view(rows, cols)              # 8 bytes past a 16-byte boundary
+    out = torch.empty(rows * cols + 8, dtype=torch.uint8, device=DEV)[8:].view(cols, rows)
+    f8.f8_transpose_u8(x, out=out)
+    assert f8.f8_last_device_status() == 0
+    assert torch.equal(out, x.t().contiguous())
 
 
 @pytest.fixture(scope="module")
