@@ -35,11 +35,12 @@ class _Float8LinearFn(torch.autograd.Function):
     GEMMs (f8_linear_bwd)."""
 
     @staticmethod
-    def forward(ctx, x: torch.Tensor, weight: torch.Tensor) -> torch.Tensor:
+    def forward(ctx, x: torch.Tensor, weight: torch.Tensor, dy_fmt: int) -> torch.Tensor:
         lead = x.shape[:-1]
         x2 = x.reshape(-1, x.shape[-1]).contiguous()
         y, saved = binding.f8_linear_fwd(x2, weight.contiguous())
         ctx.f8_saved = saved
+        ctx.dy_fmt = dy_fmt
         ctx.x_shape = x.shape
         ctx.needs = (ctx.needs_input_grad[0], ctx.needs_input_grad[1])
         return y.reshape(*lead, weight.shape[0])
@@ -48,11 +49,12 @@ class _Float8LinearFn(torch.autograd.Function):
     def backward(ctx, dy: torch.Tensor):
         want_dx, want_dw = ctx.needs
         if not (want_dx or want_dw):
-            return None, None
+            return None, None, None
         dy2 = dy.reshape(-1, dy.shape[-1]).contiguous()
-        dx, dw = binding.f8_linear_bwd(dy2, ctx.f8_saved, want_dx=want_dx, want_dw=want_dw)
+        dx, dw = binding.f8_linear_bwd(dy2, ctx.f8_saved, want_dx=want_dx, want_dw=want_dw,
+                                       dy_fmt=ctx.dy_fmt)
         ctx.f8_saved = None
-        return (dx.reshape(ctx.x_shape) if want_dx else None), (dw if want_dw else None)
+        return (dx.reshape(ctx.x_shape) if want_dx else None), (dw if want_dw else None), None
 
 
 class _Float8GroupFn(torch.autograd.Function):
@@ -89,6 +91,15 @@ class _Float8GroupFn(torch.autograd.Function):
         return (dx, *[dw if need else None for dw, need in zip(dws, ctx.needs[1:])])
 
 
+def _grad_format(name: str) -> int:
+    """The FP8 format of dY: "e4m3" (scale 448/amax) or "e5m2" (scale
+    57344/amax, the wider-range gradient format of the FP8 formats paper)."""
+    formats = {"e4m3": binding.F8_E4M3, "e5m2": binding.F8_E5M2}
+    if name not in formats:
+        raise ValueError("grad_format is 'e4m3' or 'e5m2'")
+    return formats[name]
+
+
 def _check_sizes(in_features: int, out_features: int) -> None:
     if in_features % 16 or out_features % 16:
         raise ValueError("Float8Linear needs in_features and out_features that are multiples of 16")
@@ -102,11 +113,12 @@ class Float8Linear(torch.nn.Module):
     flattened into the GEMM's M, which must be a multiple of 16."""
 
     def __init__(self, in_features: int, out_features: int, device=None,
-                 weight: torch.nn.Parameter | None = None):
+                 weight: torch.nn.Parameter | None = None, grad_format: str = "e4m3"):
         super().__init__()
         _check_sizes(in_features, out_features)
         self.in_features = in_features
         self.out_features = out_features
+        self.grad_format = _grad_format(grad_format)
         if weight is None:
             weight = torch.nn.Parameter(torch.empty((out_features, in_features),
                                                     dtype=torch.bfloat16, device=device))
@@ -116,11 +128,12 @@ class Float8Linear(torch.nn.Module):
         self.weight = weight
 
     @classmethod
-    def from_linear(cls, linear: torch.nn.Linear) -> "Float8Linear":
+    def from_linear(cls, linear: torch.nn.Linear, grad_format: str = "e4m3") -> "Float8Linear":
         """The Float8 counterpart of `linear`, sharing its weight Parameter."""
         if linear.bias is not None:
             raise ValueError("Float8Linear has no bias")
-        return cls(linear.in_features, linear.out_features, weight=linear.weight)
+        return cls(linear.in_features, linear.out_features, weight=linear.weight,
+                   grad_format=grad_format)
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:
         if x.dtype != torch.bfloat16:
@@ -130,10 +143,12 @@ class Float8Linear(torch.nn.Module):
         if (x.numel() // self.in_features) % 16:
             raise ValueError("Float8Linear needs a token count (the input's leading dimensions) "
                              "that is a multiple of 16")
-        return _Float8LinearFn.apply(x, self.weight)
+        return _Float8LinearFn.apply(x, self.weight, self.grad_format)
 
     def extra_repr(self) -> str:
-        return f"in_features={self.in_features}, out_features={self.out_features}, float8=e4m3"
+        grads = "e5m2" if self.grad_format == binding.F8_E5M2 else "e4m3"
+        return (f"in_features={self.in_features}, out_features={self.out_features}, "
+                f"float8=e4m3, gradients={grads}")
 
 
 class Float8LinearGroup(torch.nn.Module):
@@ -292,15 +307,17 @@ def eligible(linear: torch.nn.Module) -> bool:
 
 
 def to_float8_linears(module: torch.nn.Module,
-                      keep: Callable[[str, torch.nn.Module], bool] | None = None) -> torch.nn.Module:
+                      keep: Callable[[str, torch.nn.Module], bool] | None = None,
+                      grad_format: str = "e4m3") -> torch.nn.Module:
     """Replaces, in place, every eligible nn.Linear below `module` for which
     `keep(qualified_name, linear)` is true (all of them when `keep` is None)
-    with a Float8Linear sharing its weight Parameter; returns `module`."""
+    with a Float8Linear sharing its weight Parameter (dY in `grad_format`);
+    returns `module`."""
     def visit(parent: torch.nn.Module, prefix: str) -> None:
         for name, child in list(parent.named_children()):
             qual = f"{prefix}.{name}" if prefix else name
             if eligible(child) and (keep is None or keep(qual, child)):
-                setattr(parent, name, Float8Linear.from_linear(child))
+                setattr(parent, name, Float8Linear.from_linear(child, grad_format))
             else:
                 visit(child, qual)
 

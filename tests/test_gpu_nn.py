@@ -219,3 +219,21 @@ def test_swiglu_module(f8):
         @ w2.float().t()
     rel = (y.reshape(-1, D).float() - ref).norm() / ref.norm()
     assert rel < 0.12, rel
+
+
+def test_layer_with_e5m2_gradients(f8):
+    """grad_format="e5m2": dY quantised to E5M2 (scale 57344/amax), dX and
+    dW bit-identical to f8_linear_bwd with dy_fmt E5M2."""
+    from float8_mixed_precision_gb300 import nn as f8nn
+    M, K, N = 256, 512, 384
+    d = wl.custom_linear(M, K, N, seed=111, dy_std=0.1)
+    x = d["x"].to(DEV).requires_grad_(True)
+    layer = f8nn.Float8Linear(K, N, weight=torch.nn.Parameter(d["w"].to(DEV)), grad_format="e5m2")
+    layer(x).backward(d["dy"].to(DEV))
+    assert f8.f8_last_device_status() == 0
+    _, saved = f8.f8_linear_fwd(d["x"].to(DEV), d["w"].to(DEV))
+    dx, dw = f8.f8_linear_bwd(d["dy"].to(DEV), saved, dy_fmt=f8.F8_E5M2)
+    assert _eq(x.grad, dx) and _eq(layer.weight.grad, dw)
+    _, saved4 = f8.f8_linear_fwd(d["x"].to(DEV), d["w"].to(DEV))
+    dx4, _ = f8.f8_linear_bwd(d["dy"].to(DEV), saved4)
+    assert not _eq(dx, dx4)          # the format really changed the gradient

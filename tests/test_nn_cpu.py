@@ -107,3 +107,13 @@ def test_swiglu_module_construction():
         ffn(torch.zeros((16, 64), dtype=torch.float32))
     with pytest.raises(ValueError, match="device tensors"):
         ffn(torch.zeros((16, 64), dtype=torch.bfloat16))
+
+
+def test_grad_format_option():
+    assert f8nn.Float8Linear(64, 64).grad_format == f8nn.binding.F8_E4M3
+    assert f8nn.Float8Linear(64, 64, grad_format="e5m2").grad_format == f8nn.binding.F8_E5M2
+    with pytest.raises(ValueError):
+        f8nn.Float8Linear(64, 64, grad_format="fp16")
+    m = _model()
+    f8nn.to_float8_linears(m, grad_format="e5m2")
+    assert m["attn"]["wq"].grad_format == f8nn.binding.F8_E5M2
