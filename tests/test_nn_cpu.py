@@ -117,3 +117,9 @@ def test_grad_format_option():
     m = _model()
     f8nn.to_float8_linears(m, grad_format="e5m2")
     assert m["attn"]["wq"].grad_format == f8nn.binding.F8_E5M2
+
+
+def test_example_module_imports():
+    import importlib
+    mod = importlib.import_module("float8_mixed_precision_gb300.example_block")
+    assert callable(mod.main)
