@@ -91,6 +91,33 @@ class _Float8GroupFn(torch.autograd.Function):
         return (dx, *[dw if need else None for dw, need in zip(dws, ctx.needs[1:])])
 
 
+class _Float8LinearQWFn(torch.autograd.Function):
+    """The linear on a weight quantised earlier (f8_linear_fwd_qw: only X is
+    quantised here), then f8_linear_bwd as usual."""
+
+    @staticmethod
+    def forward(ctx, x: torch.Tensor, weight: torch.Tensor, w_q: torch.Tensor, w_t: torch.Tensor,
+                w_scalars: torch.Tensor, dy_fmt: int) -> torch.Tensor:
+        lead, K = x.shape[:-1], x.shape[-1]
+        x2 = x.reshape(-1, K).contiguous()
+        M = x2.shape[0]
+        # W's amax and scale sit in w_scalars[2:4]; X's go to a buffer of
+        # this call's own
+        saved = binding.LinearSaved(torch.empty((K, M), dtype=torch.uint8, device=x.device), w_t,
+                                    w_scalars, torch.empty(2, dtype=torch.float32, device=x.device))
+        y = binding.f8_linear_fwd_qw(x2, w_q, saved)
+        ctx.f8_saved = saved
+        ctx.dy_fmt = dy_fmt
+        ctx.x_shape = x.shape
+        ctx.needs = (ctx.needs_input_grad[0], ctx.needs_input_grad[1])
+        return y.reshape(*lead, w_q.shape[0])
+
+    @staticmethod
+    def backward(ctx, dy: torch.Tensor):
+        dx, dw, _ = _Float8LinearFn.backward(ctx, dy)
+        return dx, dw, None, None, None, None
+
+
 def _grad_format(name: str) -> int:
     """The FP8 format of dY: "e4m3" (scale 448/amax) or "e5m2" (scale
     57344/amax, the wider-range gradient format of the FP8 formats paper)."""
@@ -113,12 +140,19 @@ class Float8Linear(torch.nn.Module):
     flattened into the GEMM's M, which must be a multiple of 16."""
 
     def __init__(self, in_features: int, out_features: int, device=None,
-                 weight: torch.nn.Parameter | None = None, grad_format: str = "e4m3"):
+                 weight: torch.nn.Parameter | None = None, grad_format: str = "e4m3",
+                 cache_weight: bool = False):
         super().__init__()
         _check_sizes(in_features, out_features)
         self.in_features = in_features
         self.out_features = out_features
         self.grad_format = _grad_format(grad_format)
+        # cache_weight: q(W), q(W)^T and W's scalars are kept and reused
+        # while the weight's storage and version are unchanged (e.g. across
+        # the micro-batches of one optimiser step); an in-place update of
+        # the weight bumps its version and the next forward quantises again
+        self.cache_weight = cache_weight
+        self._wcache = None
         if weight is None:
             weight = torch.nn.Parameter(torch.empty((out_features, in_features),
                                                     dtype=torch.bfloat16, device=device))
@@ -128,12 +162,25 @@ class Float8Linear(torch.nn.Module):
         self.weight = weight
 
     @classmethod
-    def from_linear(cls, linear: torch.nn.Linear, grad_format: str = "e4m3") -> "Float8Linear":
+    def from_linear(cls, linear: torch.nn.Linear, grad_format: str = "e4m3",
+                    cache_weight: bool = False) -> "Float8Linear":
         """The Float8 counterpart of `linear`, sharing its weight Parameter."""
         if linear.bias is not None:
             raise ValueError("Float8Linear has no bias")
         return cls(linear.in_features, linear.out_features, weight=linear.weight,
-                   grad_format=grad_format)
+                   grad_format=grad_format, cache_weight=cache_weight)
+
+    def quantized_weight(self):
+        """(q(W) [out, in], q(W)^T [in, out], scalars [4] with W's amax and
+        scale at [2:4]) for the weight as it is now: f8_quantize once per
+        weight version, then the cached tensors."""
+        w = self.weight
+        key = (w.data_ptr(), w._version)
+        if self._wcache is None or self._wcache[0] != key:
+            scalars = torch.zeros(4, dtype=torch.float32, device=w.device)
+            q, qt, _, _ = binding.f8_quantize(w.detach(), scalars[2:3], scalars[3:4])
+            self._wcache = (key, q, qt, scalars)
+        return self._wcache[1:]
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:
         if x.dtype != torch.bfloat16:
@@ -143,6 +190,9 @@ class Float8Linear(torch.nn.Module):
         if (x.numel() // self.in_features) % 16:
             raise ValueError("Float8Linear needs a token count (the input's leading dimensions) "
                              "that is a multiple of 16")
+        if self.cache_weight:
+            w_q, w_t, w_scalars = self.quantized_weight()
+            return _Float8LinearQWFn.apply(x, self.weight, w_q, w_t, w_scalars, self.grad_format)
         return _Float8LinearFn.apply(x, self.weight, self.grad_format)
 
     def extra_repr(self) -> str:
@@ -308,16 +358,16 @@ def eligible(linear: torch.nn.Module) -> bool:
 
 def to_float8_linears(module: torch.nn.Module,
                       keep: Callable[[str, torch.nn.Module], bool] | None = None,
-                      grad_format: str = "e4m3") -> torch.nn.Module:
+                      grad_format: str = "e4m3", cache_weights: bool = False) -> torch.nn.Module:
     """Replaces, in place, every eligible nn.Linear below `module` for which
     `keep(qualified_name, linear)` is true (all of them when `keep` is None)
-    with a Float8Linear sharing its weight Parameter (dY in `grad_format`);
-    returns `module`."""
+    with a Float8Linear sharing its weight Parameter (dY in `grad_format`;
+    `cache_weights` as Float8Linear's cache_weight); returns `module`."""
     def visit(parent: torch.nn.Module, prefix: str) -> None:
         for name, child in list(parent.named_children()):
             qual = f"{prefix}.{name}" if prefix else name
             if eligible(child) and (keep is None or keep(qual, child)):
-                setattr(parent, name, Float8Linear.from_linear(child, grad_format))
+                setattr(parent, name, Float8Linear.from_linear(child, grad_format, cache_weights))
             else:
                 visit(child, qual)
 

@@ -237,3 +237,39 @@ def test_layer_with_e5m2_gradients(f8):
     _, saved4 = f8.f8_linear_fwd(d["x"].to(DEV), d["w"].to(DEV))
     dx4, _ = f8.f8_linear_bwd(d["dy"].to(DEV), saved4)
     assert not _eq(dx, dx4)          # the format really changed the gradient
+
+
+def test_cached_weight_quantisation(f8):
+    """cache_weight=True: two micro-batches (gradient accumulation) reuse
+    one quantisation of W and give outputs, dX and the accumulated dW
+    bit-identical to the layer without the cache; an in-place update of the
+    weight (as an optimiser step makes) invalidates the cache, and the next
+    forward matches the uncached layer on the updated weight."""
+    from float8_mixed_precision_gb300 import nn as f8nn
+    M, K, N = 512, 1024, 768
+    w0 = wl.normal((N, K), 0.02, 121).to(DEV)
+    cached = f8nn.Float8Linear(K, N, weight=torch.nn.Parameter(w0.clone()), cache_weight=True)
+    plain = f8nn.Float8Linear(K, N, weight=torch.nn.Parameter(w0.clone()))
+    xs = [wl.normal((M, K), 1.0, 122 + i).to(DEV) for i in range(2)]
+    gs = [wl.normal((M, N), 0.1, 124 + i).to(DEV) for i in range(2)]
+    keys = []
+    for layer in (cached, plain):
+        for x, g in zip(xs, gs):
+            xr = x.clone().requires_grad_(True)
+            y = layer(xr)
+            y.backward(g)
+            layer.__dict__.setdefault("_outs", []).append((y.detach(), xr.grad))
+            if layer is cached:
+                keys.append(layer._wcache[0])
+    assert f8.f8_last_device_status() == 0
+    assert keys[0] == keys[1]                          # one quantisation for both micro-batches
+    for (yc, dxc), (yp, dxp) in zip(cached._outs, plain._outs):
+        assert _eq(yc, yp) and _eq(dxc, dxp)
+    assert _eq(cached.weight.grad, plain.weight.grad)
+    with torch.no_grad():                              # the optimiser's in-place update
+        for layer in (cached, plain):
+            layer.weight.add_(layer.weight.grad, alpha=-0.01)
+    y_c, y_p = cached(xs[0]), plain(xs[0])
+    assert cached._wcache[0] != keys[0]
+    assert f8.f8_last_device_status() == 0
+    assert _eq(y_c, y_p)
