@@ -784,6 +784,33 @@ def run_ours(args, world, rank, local):
         d["ms"] += a.elapsed_time(b)
         d["work"] += work
     tot_ms = sum(d["ms"] for d in per.values())
+
+    # ---- the step's GEMM launches alone, captured as a graph of their own
+    # (on the operands the replay above quantised): the replayed step's time
+    # minus theirs is what the quantisation adds to the replayed step, with
+    # programmatic launch overlapping neighbours as in the step itself
+    gemm_graph_ms = None
+    if args.graph:
+        torch.cuda.synchronize()
+        gg = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(gg, stream=cap):
+                for L in layers:
+                    L.step_timed(f8, lambda k, w, fn: fn() if k == "gemm" else None)
+        stream.wait_stream(cap)
+        for _ in range(2):
+            gg.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(nsteps_k):
+            gg.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        gemm_graph_ms = g0.elapsed_time(g1) / nsteps_k
+        del gg
     peaks = load_peaks()
     # the GPU has been busy from the start of the timed region to here: the
     # burst peak applies to a region under a second, the sustained one beyond
@@ -817,6 +844,31 @@ def run_ours(args, world, rank, local):
                           "dram_frac_of_hbm_measured": ((qt / (d["ms"] / nsteps_k * 1e-3) / 1e9)
                                                         / peaks["hbm_gbs"]) if qt else None,
                           "two_pass_ceiling_frac": ((d["work"] / nsteps_k) / qt) if qt else None})
+        if gemm_graph_ms is not None and kind == "gemm":
+            e.update({"graph_ms_per_step": gemm_graph_ms,
+                      "graph_tflops": d["work"] / nsteps_k / (gemm_graph_ms * 1e-3) / 1e12})
+        if gemm_graph_ms is not None and kind == "quantize":
+            # what the quantisation adds to the replayed step, bounded from
+            # below two ways: the step minus the event-timed GEMM calls, and
+            # the step minus the GEMM launches replayed alone as one graph.
+            # Both GEMM figures exceed the GEMMs' share of the replayed step
+            # (the calls pay their launch ramp without programmatic overlap;
+            # back to back, the GEMMs run hotter and slower), so both
+            # differences are lower bounds on the quantisation's time and
+            # their fractions upper bounds on its rate.  frac_of_hbm_measured
+            # above, from per-call events that include each call's launch,
+            # is a lower bound.
+            step_ms = ms_max / args.steps
+            alg = d["work"] / nsteps_k
+            g_ev = per["gemm"]["ms"] / nsteps_k
+
+            def frac(q_ms):
+                return alg / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"] if q_ms > 0 else None
+            e["in_step"] = {
+                "step_minus_gemm_calls": {"ms_per_step": step_ms - g_ev,
+                                          "frac_of_hbm_measured": frac(step_ms - g_ev)},
+                "step_minus_gemm_graph": {"ms_per_step": step_ms - gemm_graph_ms,
+                                          "frac_of_hbm_measured": frac(step_ms - gemm_graph_ms)}}
         kernels[kind] = e
     g = per["gemm"]
     achieved = g["work"] / (g["ms"] * 1e-3) / 1e12
