@@ -12,8 +12,9 @@ in TFLOP/s.
 Inputs are seeded synthetic bf16 tensors (float8_mixed_precision_gb300.workloads),
 resident in HBM before timing.  By default the step (every launch of every
 linear, made through f8_linear_fwd / f8_linear_bwd) is captured once as a
-CUDA graph and replayed each timed step (--graph 0: called each step).  A step's inputs (0.5 GB for the attention
-workload) exceed the 129 MB L2, so no L2 flush is inserted between steps.
+CUDA graph and replayed each timed step (--graph 0: called each step).  A
+step's inputs (0.5 GB for the attention workload, 3.2 GB for the block)
+exceed the 129 MB L2, so no L2 flush is inserted between steps.
 
 The JSON line carries, besides the contract keys:
   roofline      the GEMM kernel: GEMM flops of the step over the summed
@@ -23,7 +24,10 @@ The JSON line carries, besides the contract keys:
   kernels       the same breakdown for the quantisation of a tensor
                 (amax launch + cast_transpose launch, as the linear runs
                 them; algorithmic bytes 2 B/elem read + 2 x 1 B/elem
-                written, the cast's re-read of the tensor not counted);
+                written, the cast's re-read of the tensor not counted), its
+                DRAM bytes from an ncu capture, and bounds on what it adds
+                to the replayed step (in_step); the GEMMs' time replayed
+                alone as a graph (graph_ms_per_step);
   kernels_isolated  each kernel alone on the workload's tensors, L2 flushed;
   e2e           the same metric through the public API with pinned host
                 buffers: inputs copied in and Y, dX, dW copied out every step;
