@@ -13,7 +13,7 @@ Inputs are seeded synthetic bf16 tensors (float8_mixed_precision_gb300.workloads
 resident in HBM before timing.  By default the step (every launch of every
 linear, made through f8_linear_fwd / f8_linear_bwd) is captured once as a
 CUDA graph and replayed each timed step (--graph 0: called each step).  A
-step's inputs (0.5 GB for the attention workload, 3.2 GB for the block)
+step's inputs (0.5 GB for the attention workload, 1.6 GB for the block)
 exceed the 129 MB L2, so no L2 flush is inserted between steps.
 
 The JSON line carries, besides the contract keys:
