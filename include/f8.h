@@ -412,6 +412,8 @@ f8_status f8_linear_bwd_group(const f8_group_linear *members, int count, int64_t
  * f8_transpose_u8: out[c, r] = in[r, c] for a [rows, cols] byte tensor
  * (device pointers, no alignment rule, rows, cols >= 0; not in place).  It
  * makes q(W)^T [K, N], the dgrad operand, from the gathered q(W) [N, K].
+ * With rows and cols multiples of 128 and both pointers 16-byte aligned it
+ * moves 16-byte vectors through 128 x 128 tiles; otherwise it moves bytes.
  */
 f8_status f8_transpose_u8(const uint8_t *in, int64_t rows, int64_t cols, uint8_t *out,
                           void *stream);
