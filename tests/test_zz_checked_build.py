@@ -1,7 +1,8 @@
 """The checked build (device bounds checks compiled in, -DF8_BOUNDS_CHECK)
 runs the kernel, linear, E5M2, SwiGLU, W13, paired-quantisation, grouped
 (multi-tensor quantisation, grouped GEMMs, shared-input linears), FP8
-all-gather (byte transpose) and past-2^31-element parity tests in a child process.  Every manually indexed global access is tested
+all-gather (byte transpose), past-2^31-element and PyTorch-module parity
+tests in a child process.  Every manually indexed global access is tested
 against its buffer first, and every one of those tests asserts a clean
 device status, so a single index outside its buffer would fail the run as
 F8_ERR_BOUNDS.  The check mechanism itself is shown to fire by
@@ -56,7 +57,8 @@ def test_checked_build_selftest_fires(checked_lib):
 def test_parity_suites_under_checked_build(checked_lib):
     tests = ["tests/test_gpu_kernels.py", "tests/test_gpu_linear.py", "tests/test_gpu_e5m2.py",
              "tests/test_gpu_swiglu.py", "tests/test_gpu_w13.py", "tests/test_gpu_quant_pair.py",
-             "tests/test_gpu_group.py", "tests/test_gpu_fsdp.py", "tests/test_gpu_max_size.py"]
+             "tests/test_gpu_group.py", "tests/test_gpu_fsdp.py", "tests/test_gpu_max_size.py",
+             "tests/test_gpu_nn.py"]
     r = _child(checked_lib, ["-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
                              "-k", "not full_size and not every_output and not llama8b and not all_gather",
                              *tests],
